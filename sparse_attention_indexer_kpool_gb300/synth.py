@@ -1,0 +1,234 @@
+"""Seeded synthetic inputs for the DSA kpool selection + selected-row MLA path.
+
+This module only draws random numbers and lays them out in the library's tensor
+layout (ragged token axis with ``cu_seqlens``, pool-cache slices with
+``cu_pool_cap``).  It holds none of the method's arithmetic, so it may serve
+both the CUDA path and the CPU oracle.
+
+The workloads mirror the pages' geometry (32 index heads, head_dim 128, kpool 4,
+262 144-token contexts = 65 536 pools, 11 DSA layers) and the value
+distributions of the five named workloads:
+
+* ``tiny``      1 x 256 tokens, 3 tokens of left padding, fp32, 4 index heads of
+                dim 32, kpool 4 (63 pools), select_k 8, MLA 4 heads x latent 64;
+                integer keys/queries/gates in [-2, 2] drawn from a few template
+                pools so that exact score ties straddle the top-k cutoff.
+* ``single32k`` 1 x 32 768 tokens, bf16, 32 x 128 indexer, kpool 4, select_k 512,
+                MLA 64 heads x latent 512.
+* ``ragged64``  64 sequences, lengths U{4096..65536}, left padding U{0..7}.
+* ``long262k``  4 x 262 144 tokens (one DSA layer; a model step runs 11).
+* ``prefill``   4 096 query tokens appended to a 131 072-token context,
+                kpool 8, select_k 256, causal.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass
+class Geometry:
+    """Per-layer DSA geometry; every value is explicit (nothing defaulted)."""
+    D: int            # index head_dim
+    H: int            # index heads
+    kpool: int
+    select_k: int
+    out_width: int
+    Hm: int           # MLA heads
+    L: int            # MLA latent dim
+    dtype: str        # "bf16" | "f32"
+    ln_eps: float = 1e-5
+
+
+@dataclass
+class Batch:
+    """One layer's inputs in the library's layout (tensors on one device)."""
+    geo: Geometry
+    lengths: list          # T_b per sequence (padding included)
+    pads: list             # left padding per sequence
+    cu_seqlens: torch.Tensor   # [B+1] int32
+    cu_pool_cap: torch.Tensor  # [B+1] int32
+    P_ld: int
+    k: torch.Tensor        # [sum T, D]
+    gate: torch.Tensor     # [sum T, D]
+    valid: torch.Tensor    # [sum T] uint8
+    ape: torch.Tensor      # [kpool, D] fp32
+    ln_gamma: torch.Tensor  # [D]
+    ln_beta: torch.Tensor   # [D]
+    q: torch.Tensor        # [Q, H, D]
+    weights: torch.Tensor  # [Q, H] fp32
+    q_seq: torch.Tensor | None   # [Q] int32 or None (all queries on sequence 0)
+    q_pos: torch.Tensor | None   # [Q] int32 or None (every complete pool visible)
+    q_lat: torch.Tensor    # [Q, Hm, L]
+    kv: torch.Tensor       # [sum T, L]
+    scale: float
+    sm_scale: float
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def B(self):
+        return len(self.lengths)
+
+    @property
+    def Q(self):
+        return self.q.shape[0]
+
+
+def torch_dtype(name: str):
+    return {"bf16": torch.bfloat16, "f32": torch.float32}[name]
+
+
+def _gen(device, seed):
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def _normal(shape, std, g, device, dtype):
+    return (torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std).to(dtype)
+
+
+def _ints(shape, lo, hi, g, device, dtype):
+    return torch.randint(lo, hi + 1, shape, generator=g, device=device).to(dtype)
+
+
+def make_batch(geo: Geometry, lengths, pads, *, device="cpu", seed=0, queries="decode",
+               q_positions=None, q_sequence=0, dist="normal", pool_cap=None,
+               weights_std=None) -> Batch:
+    """Draw one layer's caches and queries.
+
+    queries="decode": one query per sequence at its last token.
+    queries="chunk":  len(q_positions) queries, all on sequence ``q_sequence``
+                      (the prefill-chunk form; q_seq is None, so the caller
+                      passes that sequence's cache slice).
+    dist="normal": k, gate, q, q_lat, kv ~ N(0,1); ape ~ N(0, 0.1);
+                   weights ~ N(0, 1/32) (std given by ``weights_std``);
+                   LayerNorm gamma = 1, beta ~ N(0, 0.1).
+    dist="ints":   k, gate, q, q_lat, kv integers in [-2, 2];
+                   weights ~ N(0,1)/2; same ape / gamma / beta.
+    """
+    dev = torch.device(device)
+    g = _gen(dev, seed)
+    act = torch_dtype(geo.dtype)
+    B = len(lengths)
+    lengths = [int(t) for t in lengths]
+    pads = [int(p) for p in pads]
+    assert len(pads) == B and all(0 <= p <= t for p, t in zip(pads, lengths))
+    total = sum(lengths)
+    cu = [0]
+    for t in lengths:
+        cu.append(cu[-1] + t)
+    caps = [t // geo.kpool for t in lengths] if pool_cap is None else list(pool_cap)
+    cu_cap = [0]
+    for c in caps:
+        cu_cap.append(cu_cap[-1] + c)
+    P_ld = max([1] + caps)
+    D, L = geo.D, geo.L
+    if dist == "ints":
+        k = _ints((total, D), -2, 2, g, dev, act)
+        gate = _ints((total, D), -2, 2, g, dev, act)
+    else:
+        k = _normal((total, D), 1.0, g, dev, act)
+        gate = _normal((total, D), 1.0, g, dev, act)
+    valid = torch.ones(total, dtype=torch.uint8, device=dev)
+    for b in range(B):
+        valid[cu[b]:cu[b] + pads[b]] = 0
+    ape = _normal((geo.kpool, D), 0.1, g, dev, torch.float32)
+    ln_gamma = torch.ones(D, dtype=act, device=dev)
+    ln_beta = _normal((D,), 0.1, g, dev, act)
+
+    if queries == "decode":
+        Q = B
+        q_seq = torch.arange(B, dtype=torch.int32, device=dev)
+        q_pos = torch.tensor([t - 1 for t in lengths], dtype=torch.int32, device=dev)
+    elif queries == "chunk":
+        Q = len(q_positions)
+        q_seq = None
+        q_pos = torch.tensor(list(q_positions), dtype=torch.int32, device=dev)
+    else:
+        raise ValueError(queries)
+    if dist == "ints":
+        q = _ints((Q, geo.H, D), -2, 2, g, dev, act)
+        weights = _normal((Q, geo.H), 0.5, g, dev, torch.float32)
+        q_lat = _ints((Q, geo.Hm, L), -2, 2, g, dev, act)
+        kv = _ints((total, L), -2, 2, g, dev, act)
+    else:
+        wstd = weights_std if weights_std is not None else math.sqrt(1.0 / 32.0)
+        q = _normal((Q, geo.H, D), 1.0, g, dev, act)
+        weights = _normal((Q, geo.H), wstd, g, dev, torch.float32)
+        q_lat = _normal((Q, geo.Hm, L), 1.0, g, dev, act)
+        kv = _normal((total, L), 1.0, g, dev, act)
+    return Batch(geo=geo, lengths=lengths, pads=pads,
+                 cu_seqlens=torch.tensor(cu, dtype=torch.int32, device=dev),
+                 cu_pool_cap=torch.tensor(cu_cap, dtype=torch.int32, device=dev),
+                 P_ld=P_ld, k=k, gate=gate, valid=valid, ape=ape, ln_gamma=ln_gamma,
+                 ln_beta=ln_beta, q=q, weights=weights, q_seq=q_seq, q_pos=q_pos,
+                 q_lat=q_lat, kv=kv, scale=1.0 / math.sqrt(D), sm_scale=1.0 / math.sqrt(L))
+
+
+# --------------------------------------------------------------------------
+# the five named workloads
+# --------------------------------------------------------------------------
+GEO_TINY = Geometry(D=32, H=4, kpool=4, select_k=8, out_width=32, Hm=4, L=64, dtype="f32")
+GEO_MAIN = Geometry(D=128, H=32, kpool=4, select_k=512, out_width=2048, Hm=64, L=512, dtype="bf16")
+GEO_PREFILL = Geometry(D=128, H=32, kpool=8, select_k=256, out_width=2048, Hm=64, L=512,
+                       dtype="bf16")
+
+
+def tiny(device="cpu", seed=0, n_templates=10, select_k=None, out_width=None) -> Batch:
+    """1 x 256 tokens, 3 padding tokens, fp32 integers with tie-making templates.
+
+    Each of the 63 full pools (tokens 3..254) copies its k and gate rows from one
+    of ``n_templates`` template pools, so equal templates give bit-identical
+    pool keys and scores: ties sit throughout the ranking, including the cutoff.
+    """
+    geo = Geometry(**{**GEO_TINY.__dict__})
+    if select_k is not None:
+        geo.select_k = select_k
+    if out_width is not None:
+        geo.out_width = out_width
+    elif select_k is not None:
+        geo.out_width = select_k * geo.kpool
+    bt = make_batch(geo, [256], [3], device=device, seed=seed, dist="ints")
+    g = _gen(torch.device(device), seed + 7919)
+    kp, t0, P = geo.kpool, 3, (256 - 3) // geo.kpool
+    tmpl = torch.randint(0, n_templates, (P,), generator=g, device=device).tolist()
+    src_k = bt.k[t0:t0 + n_templates * kp].clone()
+    src_g = bt.gate[t0:t0 + n_templates * kp].clone()
+    for p in range(P):
+        j = tmpl[p]
+        bt.k[t0 + p * kp:t0 + (p + 1) * kp] = src_k[j * kp:(j + 1) * kp]
+        bt.gate[t0 + p * kp:t0 + (p + 1) * kp] = src_g[j * kp:(j + 1) * kp]
+    bt.extra["templates"] = tmpl
+    bt.scale = 1.0 / math.sqrt(geo.D)
+    bt.sm_scale = 1.0 / 8.0
+    return bt
+
+
+def single32k(device="cpu", seed=1000) -> Batch:
+    return make_batch(GEO_MAIN, [32768], [0], device=device, seed=seed)
+
+
+def ragged_lengths(B=64, lo=4096, hi=65536, max_pad=7, seed=2000):
+    g = torch.Generator()
+    g.manual_seed(seed)
+    lengths = torch.randint(lo, hi + 1, (B,), generator=g).tolist()
+    pads = torch.randint(0, max_pad + 1, (B,), generator=g).tolist()
+    return lengths, pads
+
+
+def ragged64(device="cpu", seed=2000) -> Batch:
+    lengths, pads = ragged_lengths(seed=seed)
+    return make_batch(GEO_MAIN, lengths, pads, device=device, seed=seed + 1)
+
+
+def long262k(device="cpu", layer=0, seed=3000) -> Batch:
+    return make_batch(GEO_MAIN, [262144] * 4, [0] * 4, device=device, seed=seed + 100 * layer)
+
+
+def prefill(device="cpu", seed=4000, n_query=4096, ctx=131072) -> Batch:
+    T = ctx + n_query
+    return make_batch(GEO_PREFILL, [T], [0], device=device, seed=seed, queries="chunk",
+                      q_positions=list(range(ctx, T)))

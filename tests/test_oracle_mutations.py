@@ -1,0 +1,67 @@
+"""The oracle pins must reject plausible slips.
+
+Each case plants one mistake in a private copy of the oracle (on the CPU, never
+in the library) and checks that at least one pin in test_oracle_pins fails.
+"""
+import importlib.util
+import os
+import sys
+import tempfile
+
+import pytest
+
+import tests.test_oracle_pins as pins
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = open(os.path.join(HERE, "..", "oracle", "dsa_oracle.py")).read()
+
+MUTATIONS = {
+    "rmsnorm": ("mu = x.mean(axis=-1, keepdims=True)", "mu = 0.0 * x.mean(axis=-1, keepdims=True)"),
+    "unbiased_variance": ("var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)",
+                          "var = ((x - mu) ** 2).sum(axis=-1, keepdims=True) / (x.shape[-1] - 1)"),
+    "softmax_over_channels": ("m = logit.max(axis=0, keepdims=True)\n            e = np.exp(logit - m)\n"
+                              "            w = e / e.sum(axis=0, keepdims=True)",
+                              "m = logit.max(axis=1, keepdims=True)\n            e = np.exp(logit - m)\n"
+                              "            w = e / e.sum(axis=1, keepdims=True)"),
+    "ape_dropped": ("logit = gate[toks] + ape ", "logit = gate[toks] + 0 * ape "),
+    "pools_from_token_0": ("t0 = first_valid(valid[lo:hi])", "t0 = 0"),
+    "partial_pool_kept": ("P = (T - t0) // kpool", "P = -(-(T - t0) // kpool)"),
+    "any_valid_slot": ("pool_valid[g] = 1 if np.all(valid[toks] != 0) else 0",
+                       "pool_valid[g] = 1 if np.any(valid[toks] != 0) else 0"),
+    "relu_after_weight": ("s = (np.maximum(0.0, scale * dots) * w[i][None, :]).sum(axis=1)",
+                          "s = np.maximum(0.0, scale * dots * w[i][None, :]).sum(axis=1)"),
+    "scale_dropped": ("np.maximum(0.0, scale * dots)", "np.maximum(0.0, dots)"),
+    "causal_strict": ("cand &= last_tok <= int(q_pos[i])", "cand &= last_tok < int(q_pos[i])"),
+    "tie_order_reversed": ("order = np.lexsort((cand, -s))", "order = np.lexsort((-cand, -s))"),
+    "expand_without_base": ("out[i, j * kpool + s] = int(pool_start[base + p]) + s",
+                            "out[i, j * kpool + s] = int(pool_start[p]) + s"),
+    "mla_without_row_base": ("C = kv[lo + sel]", "C = kv[sel]"),
+    "mla_scale_dropped": ("z = sm_scale * (q_lat[i] @ C.T)", "z = (q_lat[i] @ C.T)"),
+    "bf16_truncates": ("r = np.rint(x / spacing) * spacing", "r = np.trunc(x / spacing) * spacing"),
+}
+
+
+def _load_mutant(src):
+    d = tempfile.mkdtemp()
+    path = os.path.join(d, "mutant_oracle.py")
+    open(path, "w").write(src)
+    spec = importlib.util.spec_from_file_location("mutant_oracle", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_reject_mutation(name, monkeypatch):
+    a, b = MUTATIONS[name]
+    assert SRC.count(a) == 1, name
+    mutant = _load_mutant(SRC.replace(a, b))
+    monkeypatch.setattr(pins, "oracle", mutant)
+    failed = []
+    for fn_name in sorted(dir(pins)):
+        if fn_name.startswith("test_"):
+            try:
+                getattr(pins, fn_name)()
+            except Exception:
+                failed.append(fn_name)
+    assert failed, f"no pin caught the planted mistake {name!r}"
