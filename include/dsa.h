@@ -1,0 +1,240 @@
+/*
+ * dsa.h - C ABI of libdsa: DeepSeek-Sparse-Attention kpool token selection and
+ * selected-row NoPE MLA decode for one GLM-5.3-Flash-style layer, on GB300
+ * (sm_103a).
+ *
+ * The five stage entry points follow the stage list of the DSA module page
+ * (module glm5next_dsa, "Shape of the pipeline"):
+ *
+ *   k, gate, valid, ape -> dsa_kpool_compress -> pool keys / starts / valid
+ *                       -> dsa_index_scores   -> [Q, P_ld] fp32 scores (-inf = not a candidate)
+ *                       -> dsa_topk_pools     -> [Q, select_k] pool ids
+ *                       -> dsa_expand_selection -> [Q, out_width] token ids (-1 = none)
+ *                       -> dsa_mla_selected_decode -> [Q, Hm, L] latent output + lse
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Ownership:  the caller allocates and owns every buffer, workspaces included
+ *             (sizes from the *_workspace_size queries).  The library never
+ *             allocates, frees or synchronizes; it keeps no state between calls.
+ * Pointers:   every tensor pointer is a DEVICE pointer of the current CUDA
+ *             device.  Tensors are dense, row-major, with the shapes given per
+ *             argument.  bf16/fp32 activation rows must start on 16-byte
+ *             boundaries (row sizes here are multiples of 16 bytes).
+ * Streams:    `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *             stream).  Every call is asynchronous on that stream and may be
+ *             captured into a CUDA graph.
+ * Geometry:   every size is an explicit argument; nothing is defaulted (module
+ *             glm5next_dsa, Structs, Glm5NextDsaConfig: geometry is read from
+ *             the checkpoint config, never defaulted).
+ * Validation: arguments are checked on the host before anything is launched.
+ *             On any error the call returns a non-zero DSA_ERR_* code, launches
+ *             nothing and writes no output.  Nothing is silently truncated: a
+ *             kpool above 8 is refused (module glm5next_dsa, Constants,
+ *             KERNEL_MAX_KPOOL).
+ * Device faults: faults only the device can see (a token id outside its
+ *             sequence, a pool count larger than its cache slice, ...) are
+ *             OR-ed as DSA_DEV_* bits into *status_dev when status_dev is not
+ *             NULL; the offending item is skipped, never trapped.  The caller
+ *             zeroes *status_dev and reads it back when convenient.
+ * Empty work: Q == 0 or B == 0 is a valid no-op returning DSA_OK.
+ *
+ * Layouts
+ * -------
+ * Token axis: the B sequences are concatenated; sequence b owns rows
+ *   [cu_seqlens[b], cu_seqlens[b+1]) of k, gate, valid and kv_latent.  Its
+ *   tokens are numbered 0..T_b-1 on its own axis, left padding included.
+ * Pool cache: sequence b owns entries [cu_pool_cap[b], cu_pool_cap[b+1]) of
+ *   pool_keys / pool_start / pool_valid (its capacity cap_b).  Pool ids and
+ *   pool_start values are local to the sequence.
+ * Queries: query q reads sequence q_seq[q] (q_seq == NULL: every query reads
+ *   sequence 0; pass cache pointers offset to the wanted sequence).
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ------------------------------------------------------ */
+#define DSA_OK 0
+#define DSA_ERR_INVALID_ARG 1  /* bad size, null pointer, kpool not in [1,8], out_width too small */
+#define DSA_ERR_MISALIGNED 2   /* a pointer is not aligned as documented                         */
+#define DSA_ERR_UNSUPPORTED 3  /* geometry / dtype combination this build has no kernel for      */
+#define DSA_ERR_WORKSPACE 4    /* workspace missing or smaller than the size query returns       */
+#define DSA_ERR_CUDA 5         /* a CUDA launch failed (cudaGetLastError after the launch)       */
+
+/* ---- activation dtypes ------------------------------------------------- */
+#define DSA_BF16 0
+#define DSA_F32 1
+
+/* ---- device status bits (OR-ed into *status_dev) ----------------------- */
+#define DSA_DEV_BAD_TOKEN 1        /* MLA: token id >= T_b; the row is skipped          */
+#define DSA_DEV_POOL_OVERFLOW 2    /* compress: more complete pools than cap_b           */
+#define DSA_DEV_POOL_UNCOVERED 4   /* compress: complete pools past pool_begin+max_pools */
+#define DSA_DEV_BAD_POOL_ID 8      /* expand: pool id >= cap_b; expands to -1            */
+#define DSA_DEV_BAD_QSEQ 16        /* q_seq[q] outside [0, B); the query gets no output  */
+#define DSA_DEV_POOL_RANGE 32      /* index: n_pools[b] > cap_b or > P_ld; clamped       */
+#define DSA_DEV_TIMEOUT 64         /* a bounded wait inside a kernel gave up             */
+
+#define DSA_KPOOL_MAX 8            /* module glm5next_dsa, Constants, KERNEL_MAX_KPOOL   */
+#define DSA_SELECT_K_MAX 4096
+
+/*
+ * dsa_kpool_compress - LayerNorm the indexer keys and pool them kpool at a time.
+ *
+ * Source: module glm5next_dsa, "Shape of the pipeline" (k, gate, valid, ape ->
+ * kpool_compress -> pool keys / indices / valid) and "Traps carried from Slice
+ * 8": k_norm is a LayerNorm with bias, not RMSNorm; the pool softmax runs over
+ * the slot axis per channel; pooling starts at the first valid token; a pool
+ * counts only if every slot is valid.  Constants, LAYERNORM_MODULE: the
+ * LayerNorm output is stored in the activation dtype before pooling.
+ *
+ * For sequence b: t0 = first token with valid != 0 (T_b if none),
+ * P_b = floor((T_b - t0) / kpool).  Pool p covers tokens t0 + p*kpool + s:
+ *   kn[s]      = LayerNorm(k[token]) * ln_gamma + ln_beta   (population variance,
+ *                ln_eps inside the square root), rounded to the activation dtype
+ *   logit[s,d] = gate[token, d] + ape[s, d]
+ *   key[p, d]  = sum_s softmax_s(logit[., d]) * kn[s][d], rounded to the dtype
+ *   pool_start[p] = t0 + p*kpool;  pool_valid[p] = all slots valid.
+ * Written pools: p in [pool_begin[b], min(pool_begin[b] + max_pools, cap_b)).
+ * Of those, p < P_b are computed and p >= P_b get the sentinel (key 0, start
+ * -1, valid 0).  Other entries are not touched (decode: pass the first pool
+ * that may have completed since the previous call).  n_pools[b] = min(P_b, cap_b).
+ *
+ *   k, gate     [sum T_b, D]  activation dtype
+ *   valid       [sum T_b]     uint8 (0 = padding / not a token)
+ *   ape         [kpool, D]    fp32, added to the gate logits per slot
+ *   ln_gamma, ln_beta [D]     activation dtype
+ *   cu_seqlens  [B+1] int32, cu_pool_cap [B+1] int32
+ *   pool_begin  [B] int32 or NULL (all zero)
+ *   max_pools   >= 0: launch extent in pools per sequence
+ *   pool_keys   [sum cap_b, D] activation dtype; pool_start [sum cap_b] int32;
+ *   pool_valid  [sum cap_b] uint8; n_pools [B] int32
+ * Supported: D in {32, 64, 128, 256}; kpool in [1, 8]; dtype DSA_BF16 or DSA_F32.
+ * Device faults: DSA_DEV_POOL_OVERFLOW, DSA_DEV_POOL_UNCOVERED.
+ */
+int dsa_kpool_compress(const void* k, const void* gate, const uint8_t* valid, const float* ape,
+                       const void* ln_gamma, const void* ln_beta, float ln_eps,
+                       const int32_t* cu_seqlens, const int32_t* cu_pool_cap,
+                       const int32_t* pool_begin, int B, int D, int kpool, int max_pools,
+                       int dtype, void* pool_keys, int32_t* pool_start, uint8_t* pool_valid,
+                       int32_t* n_pools, int32_t* status_dev, void* stream);
+
+/*
+ * dsa_index_scores - score every pool of the query's sequence.
+ *
+ * Source: module glm5next_dsa::tp, "Why the indexer is REPLICATED, not
+ * sharded": the score is a plain sum over heads of weights[h] * relu(scale *
+ * dot); module glm5next_dsa, "Shape of the pipeline": [Q, P] scores plus
+ * candidate validity.
+ *
+ *   scores[q, p] = sum_h weights[q, h] * max(0, scale * <q[q, h, :], pool_keys[p, :]>)
+ * for a candidate pool, -inf otherwise; -0 is written as +0; every one of the
+ * P_ld entries of a row is written.  Pool p of sequence b is a candidate when
+ * p < n_pools[b], pool_valid[p] != 0 and, if q_pos is not NULL,
+ * pool_start[p] + kpool - 1 <= q_pos[q] (the pool is complete at the query's
+ * position).  pool_start must be as dsa_kpool_compress wrote it.
+ *
+ *   q        [Q, H, D] activation dtype;  weights [Q, H] fp32;  scale > 0
+ *   pool_*   the cache written by dsa_kpool_compress (pool_start may be NULL
+ *            when q_pos is NULL); n_pools [B]; cu_pool_cap [B+1]
+ *   q_seq    [Q] int32 or NULL;  q_pos [Q] int32 or NULL (every complete pool)
+ *   scores   [Q, P_ld] fp32
+ * Supported: any H in [1, 64] and D in {32, 64, 128, 256} for both dtypes;
+ * H = 32, D = 128, bf16 runs on the tensor cores (q_seq == NULL with many
+ * queries: the dense prefill-chunk kernel).
+ * Device faults: DSA_DEV_BAD_QSEQ, DSA_DEV_POOL_RANGE.
+ */
+int dsa_index_scores(const void* q, const float* weights, float scale, const void* pool_keys,
+                     const int32_t* pool_start, const uint8_t* pool_valid,
+                     const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
+                     const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
+                     int dtype, float* scores, int32_t* status_dev, void* stream);
+
+/*
+ * dsa_topk_pools - deterministic top-k over each score row.
+ *
+ * Source: module glm5next_dsa::tp, "Why the indexer is REPLICATED": the tie
+ * order is pinned - higher score first, then the smaller pool index - because
+ * the order torch.topk gives equal values is undefined.  module glm5next_dsa,
+ * "Shape of the pipeline": [Q, select_k] pool ids.
+ *
+ * Candidates are the entries with score > -inf (NaN is not a candidate); -0
+ * and +0 are equal.  pool_ids[q, :] lists the first min(select_k, #candidates)
+ * candidates in (score descending, pool index ascending) order; the remaining
+ * entries are -1.  The result is unique and bit-reproducible.
+ *
+ *   scores   [Q, P_ld] fp32;  pool_ids [Q, select_k] int32
+ *   workspace: dsa_topk_pools_workspace_size(Q, P_ld, select_k) bytes, 16-byte aligned
+ * Supported: 1 <= select_k <= DSA_SELECT_K_MAX.
+ */
+int dsa_topk_pools(const float* scores, int Q, int P_ld, int select_k, int32_t* pool_ids,
+                   void* workspace, size_t ws_bytes, void* stream);
+size_t dsa_topk_pools_workspace_size(int Q, int P_ld, int select_k);
+
+/*
+ * dsa_expand_selection - pool ids to token ids.
+ *
+ * Source: module glm5next_dsa, "Shape of the pipeline" ([Q, out_width] token
+ * ids, -1 = invalid) and "Traps carried from Slice 8": the -1 destination is
+ * written in full (an unwritten tail once turned uninitialised memory into
+ * token indices).
+ *
+ *   token_ids[q, j*kpool + s] = pool_start[cap_base(b) + pool_ids[q, j]] + s
+ * for a selected pool; -1 when pool_ids[q, j] < 0 or its pool_start is -1;
+ * every column >= select_k*kpool is -1.  All Q*out_width entries are written.
+ *
+ *   pool_ids [Q, select_k]; pool_start, cu_pool_cap as for the cache; q_seq [Q] or NULL
+ *   token_ids [Q, out_width] int32, out_width >= select_k * kpool
+ * Device faults: DSA_DEV_BAD_POOL_ID (id >= cap_b -> -1), DSA_DEV_BAD_QSEQ.
+ */
+int dsa_expand_selection(const int32_t* pool_ids, const int32_t* pool_start,
+                         const int32_t* cu_pool_cap, const int32_t* q_seq, int Q, int B,
+                         int select_k, int kpool, int out_width, int32_t* token_ids,
+                         int32_t* status_dev, void* stream);
+
+/*
+ * dsa_mla_selected_decode - NoPE MLA decode restricted to the selected rows.
+ *
+ * Source: module glm5next_dsa, "Shape of the pipeline" (NoPE MLA restricted to
+ * the selected tokens), Modules, attend (the selected-index NoPE MLA decode
+ * launcher) and "Traps carried from Slice 8" (NoPE: no rotary slice anywhere).
+ *
+ * For query q (sequence b) and head h, over the selected rows
+ * c_j = kv_latent[cu_seqlens[b] + token_ids[q, j]] with token_ids[q, j] >= 0:
+ *   z_j = sm_scale * <q_lat[q, h, :], c_j>
+ *   out[q, h, :] = sum_j softmax(z)_j * c_j        (absorbed MLA: value = latent row)
+ *   lse[q, h]    = log(sum_j exp(z_j))            (natural log)
+ * An empty selection gives out = 0 and lse = -inf.
+ *
+ *   q_lat [Q, Hm, L] activation dtype; kv_latent [sum T_b, L] activation dtype
+ *   token_ids [Q, out_width] int32 (from dsa_expand_selection)
+ *   out [Q, Hm, L] activation dtype; lse [Q, Hm] fp32 (may be NULL)
+ *   workspace: dsa_mla_selected_decode_workspace_size(...) bytes, 16-byte aligned
+ * Supported: L multiple of 8 up to 1024 and Hm up to 128 in both dtypes; bf16
+ * with L = 512 and Hm a multiple of 16 runs on the tensor cores.
+ * Device faults: DSA_DEV_BAD_TOKEN (token id >= T_b: row skipped), DSA_DEV_BAD_QSEQ.
+ */
+int dsa_mla_selected_decode(const void* q_lat, const void* kv_latent, const int32_t* cu_seqlens,
+                            const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int Hm,
+                            int L, int out_width, float sm_scale, int dtype, void* out,
+                            float* lse, void* workspace, size_t ws_bytes, int32_t* status_dev,
+                            void* stream);
+size_t dsa_mla_selected_decode_workspace_size(int Q, int Hm, int L, int out_width, int dtype);
+
+/* Human-readable name of a DSA_* return code (static string). */
+const char* dsa_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int dsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

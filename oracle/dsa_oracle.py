@@ -271,7 +271,8 @@ def expand_selection(pool_ids, pool_start, cu_pool_cap, q_seq, kpool: int, out_w
     module glm5next_dsa, "Shape of the pipeline" ([Q, out_width] token ids, -1 =
     invalid) and "Traps carried from Slice 8" (the -1 destination is written in
     full: every column past select_k * kpool is -1).  A pool id outside its
-    sequence's cache slice yields -1 and a status bit.
+    sequence's cache slice yields -1 and a status bit; an id whose cache entry
+    is the sentinel (start -1) is not a pool and yields -1.
     """
     pool_ids = np.asarray(pool_ids, np.int64)
     Q, K = pool_ids.shape
@@ -293,8 +294,11 @@ def expand_selection(pool_ids, pool_start, cu_pool_cap, q_seq, kpool: int, out_w
             if p >= cap:
                 status |= ST_BAD_POOL_ID
                 continue
+            start = int(pool_start[base + p])
+            if start < 0:                                # sentinel entry: not a pool
+                continue
             for s in range(kpool):
-                out[i, j * kpool + s] = int(pool_start[base + p]) + s
+                out[i, j * kpool + s] = start + s
     return out, status
 
 

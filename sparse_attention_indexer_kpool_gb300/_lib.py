@@ -1,0 +1,62 @@
+"""ctypes loader for libdsa.so (the C ABI declared in include/dsa.h).
+
+The library is built in-tree by ``build.py``; if it is missing the first call
+raises: there is no CPU fallback anywhere in the product path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_LIB = None
+_LOCK = threading.Lock()
+
+c_void_p, c_int, c_float, c_size_t = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+# name -> (restype, argtypes); mirrors include/dsa.h
+SIGNATURES = {
+    "dsa_kpool_compress": (c_int, [c_void_p] * 6 + [c_float] + [c_void_p] * 3 + [c_int] * 5
+                           + [c_void_p] * 6),
+    "dsa_index_scores": (c_int, [c_void_p, c_void_p, c_float] + [c_void_p] * 7 + [c_int] * 7
+                         + [c_void_p] * 3),
+    "dsa_topk_pools": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_size_t,
+                               c_void_p]),
+    "dsa_topk_pools_workspace_size": (c_size_t, [c_int, c_int, c_int]),
+    "dsa_expand_selection": (c_int, [c_void_p] * 4 + [c_int] * 5 + [c_void_p] * 3),
+    "dsa_mla_selected_decode": (c_int, [c_void_p] * 5 + [c_int] * 5 + [c_float, c_int]
+                                + [c_void_p] * 3 + [c_size_t] + [c_void_p] * 2),
+    "dsa_mla_selected_decode_workspace_size": (c_size_t, [c_int] * 5),
+    "dsa_status_string": (ctypes.c_char_p, [c_int]),
+    "dsa_version": (c_int, []),
+}
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Load libdsa.so once; raise if it is not built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    with _LOCK:
+        if _LIB is not None:
+            return _LIB
+        path = lib_path()
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(
+                    f"libdsa.so is not built ({path}); run "
+                    "`python -m sparse_attention_indexer_kpool_gb300.build` (needs nvcc)")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB

@@ -1,0 +1,153 @@
+// C ABI of libdsa: host-side validation, then dispatch to the kernels.
+// Nothing is launched and no output is touched when validation fails.
+#include <math.h>
+
+#include "dsa_internal.cuh"
+
+namespace {
+
+inline bool aligned(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+inline bool dtype_ok(int dtype) { return dtype == DSA_BF16 || dtype == DSA_F32; }
+inline bool d_ok(int D) { return D == 32 || D == 64 || D == 128 || D == 256; }
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+int dsa_version(void) { return 10000; }
+
+const char* dsa_status_string(int status) {
+  switch (status) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG: bad size, null pointer or kpool";
+    case DSA_ERR_MISALIGNED: return "DSA_ERR_MISALIGNED: pointer alignment";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED: geometry or dtype";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE: workspace missing or too small";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA: kernel launch failed";
+    default: return "DSA_ERR_UNKNOWN";
+  }
+}
+
+int dsa_kpool_compress(const void* k, const void* gate, const uint8_t* valid, const float* ape,
+                       const void* ln_gamma, const void* ln_beta, float ln_eps,
+                       const int32_t* cu_seqlens, const int32_t* cu_pool_cap,
+                       const int32_t* pool_begin, int B, int D, int kpool, int max_pools,
+                       int dtype, void* pool_keys, int32_t* pool_start, uint8_t* pool_valid,
+                       int32_t* n_pools, int32_t* status_dev, void* stream) {
+  if (B < 0 || max_pools < 0) return DSA_ERR_INVALID_ARG;
+  if (kpool < 1 || kpool > DSA_KPOOL_MAX) return DSA_ERR_INVALID_ARG;  // refuse, never truncate
+  if (!dtype_ok(dtype) || !(ln_eps >= 0.f) || !isfinite(ln_eps)) return DSA_ERR_INVALID_ARG;
+  if (!d_ok(D)) return DSA_ERR_UNSUPPORTED;
+  if (B == 0) return DSA_OK;
+  if (!k || !gate || !valid || !ape || !ln_gamma || !ln_beta || !cu_seqlens || !cu_pool_cap ||
+      !pool_keys || !pool_start || !pool_valid || !n_pools)
+    return DSA_ERR_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(gate, 16) || !aligned(pool_keys, 16) || !aligned(ln_gamma, 16) ||
+      !aligned(ln_beta, 16) || !aligned(ape, 4) || !aligned(cu_seqlens, 4) ||
+      !aligned(cu_pool_cap, 4) || !aligned(pool_start, 4) || !aligned(n_pools, 4) ||
+      (pool_begin && !aligned(pool_begin, 4)) || (status_dev && !aligned(status_dev, 4)))
+    return DSA_ERR_MISALIGNED;
+  if (B > 65535) return DSA_ERR_UNSUPPORTED;
+  return dsa::launch_kpool_compress(k, gate, valid, ape, ln_gamma, ln_beta, ln_eps, cu_seqlens,
+                                    cu_pool_cap, pool_begin, B, D, kpool, max_pools, dtype,
+                                    pool_keys, pool_start, pool_valid, n_pools, status_dev,
+                                    as_stream(stream));
+}
+
+int dsa_index_scores(const void* q, const float* weights, float scale, const void* pool_keys,
+                     const int32_t* pool_start, const uint8_t* pool_valid,
+                     const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
+                     const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
+                     int dtype, float* scores, int32_t* status_dev, void* stream) {
+  if (Q < 0 || B < 0 || H < 1 || P_ld < 1) return DSA_ERR_INVALID_ARG;
+  if (kpool < 1 || kpool > DSA_KPOOL_MAX) return DSA_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype) || !(scale > 0.f) || !isfinite(scale)) return DSA_ERR_INVALID_ARG;
+  if (!d_ok(D) || H > 64) return DSA_ERR_UNSUPPORTED;
+  if (Q == 0) return DSA_OK;
+  if (B == 0) return DSA_ERR_INVALID_ARG;
+  if (!q || !weights || !pool_keys || !pool_valid || !n_pools || !cu_pool_cap || !scores)
+    return DSA_ERR_INVALID_ARG;
+  if (q_pos && !pool_start) return DSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(weights, 16) || !aligned(pool_keys, 16) || !aligned(scores, 4) ||
+      !aligned(n_pools, 4) || !aligned(cu_pool_cap, 4) || (q_seq && !aligned(q_seq, 4)) ||
+      (q_pos && !aligned(q_pos, 4)) || (pool_start && !aligned(pool_start, 4)) ||
+      (status_dev && !aligned(status_dev, 4)))
+    return DSA_ERR_MISALIGNED;
+  if (Q > 65535) return DSA_ERR_UNSUPPORTED;
+  return dsa::launch_index_scores(q, weights, scale, pool_keys, pool_start, pool_valid, n_pools,
+                                  cu_pool_cap, q_seq, q_pos, Q, B, H, D, kpool, P_ld, dtype,
+                                  scores, status_dev, as_stream(stream));
+}
+
+size_t dsa_topk_pools_workspace_size(int Q, int P_ld, int select_k) {
+  if (Q <= 0 || P_ld <= 0 || select_k <= 0) return 0;
+  return dsa::topk_workspace_size(Q, P_ld, select_k);
+}
+
+int dsa_topk_pools(const float* scores, int Q, int P_ld, int select_k, int32_t* pool_ids,
+                   void* workspace, size_t ws_bytes, void* stream) {
+  if (Q < 0 || P_ld < 1 || select_k < 1) return DSA_ERR_INVALID_ARG;
+  if (select_k > DSA_SELECT_K_MAX) return DSA_ERR_UNSUPPORTED;
+  if (Q == 0) return DSA_OK;
+  if (Q > 65535) return DSA_ERR_UNSUPPORTED;
+  if (!scores || !pool_ids) return DSA_ERR_INVALID_ARG;
+  if (!aligned(scores, 4) || !aligned(pool_ids, 4)) return DSA_ERR_MISALIGNED;
+  if (!workspace || ws_bytes < dsa::topk_workspace_size(Q, P_ld, select_k))
+    return DSA_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return DSA_ERR_MISALIGNED;
+  return dsa::launch_topk_pools(scores, Q, P_ld, select_k, pool_ids, workspace, ws_bytes,
+                                as_stream(stream));
+}
+
+int dsa_expand_selection(const int32_t* pool_ids, const int32_t* pool_start,
+                         const int32_t* cu_pool_cap, const int32_t* q_seq, int Q, int B,
+                         int select_k, int kpool, int out_width, int32_t* token_ids,
+                         int32_t* status_dev, void* stream) {
+  if (Q < 0 || B < 0 || select_k < 1 || out_width < 1) return DSA_ERR_INVALID_ARG;
+  if (kpool < 1 || kpool > DSA_KPOOL_MAX) return DSA_ERR_INVALID_ARG;
+  if ((long long)out_width < (long long)select_k * kpool) return DSA_ERR_INVALID_ARG;
+  if (Q == 0) return DSA_OK;
+  if (B == 0) return DSA_ERR_INVALID_ARG;
+  if (!pool_ids || !pool_start || !cu_pool_cap || !token_ids) return DSA_ERR_INVALID_ARG;
+  if (!aligned(pool_ids, 4) || !aligned(pool_start, 4) || !aligned(cu_pool_cap, 4) ||
+      !aligned(token_ids, 4) || (q_seq && !aligned(q_seq, 4)) ||
+      (status_dev && !aligned(status_dev, 4)))
+    return DSA_ERR_MISALIGNED;
+  if (Q > 65535) return DSA_ERR_UNSUPPORTED;
+  return dsa::launch_expand_selection(pool_ids, pool_start, cu_pool_cap, q_seq, Q, B, select_k,
+                                      kpool, out_width, token_ids, status_dev, as_stream(stream));
+}
+
+size_t dsa_mla_selected_decode_workspace_size(int Q, int Hm, int L, int out_width, int dtype) {
+  if (Q <= 0 || Hm <= 0 || L <= 0 || out_width <= 0 || !dtype_ok(dtype)) return 0;
+  return dsa::mla_workspace_size(Q, Hm, L, out_width, dtype);
+}
+
+int dsa_mla_selected_decode(const void* q_lat, const void* kv_latent, const int32_t* cu_seqlens,
+                            const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int Hm,
+                            int L, int out_width, float sm_scale, int dtype, void* out,
+                            float* lse, void* workspace, size_t ws_bytes, int32_t* status_dev,
+                            void* stream) {
+  if (Q < 0 || B < 0 || Hm < 1 || L < 1 || out_width < 1) return DSA_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype) || !isfinite(sm_scale)) return DSA_ERR_INVALID_ARG;
+  if (L % 8 != 0 || L > 1024 || Hm > 128) return DSA_ERR_UNSUPPORTED;
+  if (Q == 0) return DSA_OK;
+  if (B == 0) return DSA_ERR_INVALID_ARG;
+  if (!q_lat || !kv_latent || !cu_seqlens || !token_ids || !out) return DSA_ERR_INVALID_ARG;
+  if (!aligned(q_lat, 16) || !aligned(kv_latent, 16) || !aligned(out, 16) ||
+      !aligned(cu_seqlens, 4) || !aligned(token_ids, 4) || (lse && !aligned(lse, 4)) ||
+      (q_seq && !aligned(q_seq, 4)) || (status_dev && !aligned(status_dev, 4)))
+    return DSA_ERR_MISALIGNED;
+  const size_t need = dsa::mla_workspace_size(Q, Hm, L, out_width, dtype);
+  if (need > 0 && (!workspace || ws_bytes < need)) return DSA_ERR_WORKSPACE;
+  if (workspace && !aligned(workspace, 16)) return DSA_ERR_MISALIGNED;
+  if (Q > 65535) return DSA_ERR_UNSUPPORTED;
+  return dsa::launch_mla_selected_decode(q_lat, kv_latent, cu_seqlens, q_seq, token_ids, Q, B, Hm,
+                                         L, out_width, sm_scale, dtype, out, lse, workspace,
+                                         ws_bytes, status_dev, as_stream(stream));
+}
+
+}  // extern "C"

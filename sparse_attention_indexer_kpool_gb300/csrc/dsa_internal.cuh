@@ -1,0 +1,197 @@
+// Internal helpers shared by the libdsa kernels (sm_103a only).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dsa.h"
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
+#error "libdsa is built for sm_103a only"
+#endif
+
+namespace dsa {
+
+constexpr int kNumSMs = 152;         // GB300: 2 dies x 76 SMs (launch-shape heuristics only)
+constexpr int kKpoolMax = DSA_KPOOL_MAX;
+
+// ---------------------------------------------------------------- status
+__device__ __forceinline__ void flag(int32_t* status, int bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// ---------------------------------------------------------------- dtypes
+template <typename T> struct Act;
+template <> struct Act<float> {
+  static __device__ __forceinline__ float to_f(float x) { return x; }
+  static __device__ __forceinline__ float from_f(float x) { return x; }
+  static __device__ __forceinline__ float round(float x) { return x; }
+};
+template <> struct Act<__nv_bfloat16> {
+  static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+  static __device__ __forceinline__ float round(float x) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+  }
+};
+
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);  // .x = lo (low 16 bits)
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// ---------------------------------------------------------------- loads
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// ---------------------------------------------------------------- warp
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ---------------------------------------------------------------- mma.sync
+// D[16x8] += A[16x16] * B[16x8], bf16 inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                            uint32_t& r3, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                  uint32_t& r3, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// ---------------------------------------------------------------- cp.async (16 B)
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, bool pred) {
+  int n = pred ? 16 : 0;  // src-size 0 zero-fills the destination
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(g), "r"(n));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N));
+}
+
+// ---------------------------------------------------------------- mbarrier + bulk copy
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: gives up after `limit` polls and reports false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint32_t limit = (1u << 26)) {
+  for (uint32_t i = 0; i < limit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// 1-D bulk copy global -> shared (TMA engine), completion counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;");
+}
+
+// ---------------------------------------------------------------- score keys
+// Order-preserving map of an fp32 score to uint32 (bigger float -> bigger key);
+// -0 is mapped like +0 so the two compare equal.
+__device__ __forceinline__ uint32_t score_key(float s) {
+  uint32_t u = __float_as_uint(s);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ bool is_candidate(float s) { return s > -INFINITY; }
+
+}  // namespace dsa
+
+// ---------------------------------------------------------------- host launchers
+namespace dsa {
+int launch_kpool_compress(const void* k, const void* gate, const uint8_t* valid, const float* ape,
+                          const void* ln_gamma, const void* ln_beta, float ln_eps,
+                          const int32_t* cu_seqlens, const int32_t* cu_pool_cap,
+                          const int32_t* pool_begin, int B, int D, int kpool, int max_pools,
+                          int dtype, void* pool_keys, int32_t* pool_start, uint8_t* pool_valid,
+                          int32_t* n_pools, int32_t* status_dev, cudaStream_t stream);
+int launch_index_scores(const void* q, const float* weights, float scale, const void* pool_keys,
+                        const int32_t* pool_start, const uint8_t* pool_valid,
+                        const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
+                        const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
+                        int dtype, float* scores, int32_t* status_dev, cudaStream_t stream);
+size_t topk_workspace_size(int Q, int P_ld, int select_k);
+int launch_topk_pools(const float* scores, int Q, int P_ld, int select_k, int32_t* pool_ids,
+                      void* workspace, size_t ws_bytes, cudaStream_t stream);
+int launch_expand_selection(const int32_t* pool_ids, const int32_t* pool_start,
+                            const int32_t* cu_pool_cap, const int32_t* q_seq, int Q, int B,
+                            int select_k, int kpool, int out_width, int32_t* token_ids,
+                            int32_t* status_dev, cudaStream_t stream);
+size_t mla_workspace_size(int Q, int Hm, int L, int out_width, int dtype);
+int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
+                               const int32_t* q_seq, const int32_t* token_ids, int Q, int B,
+                               int Hm, int L, int out_width, float sm_scale, int dtype, void* out,
+                               float* lse, void* workspace, size_t ws_bytes, int32_t* status_dev,
+                               cudaStream_t stream);
+}  // namespace dsa
+
+#define DSA_LAUNCH_CHECK()                          \
+  do {                                              \
+    if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA; \
+  } while (0)

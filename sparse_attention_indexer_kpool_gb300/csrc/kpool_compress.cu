@@ -1,0 +1,284 @@
+// kpool_compress: fused indexer-key LayerNorm + per-channel slot-softmax pooling.
+//
+// Module glm5next_dsa, "Shape of the pipeline" (k, gate, valid, ape ->
+// kpool_compress -> pool keys / indices / valid) and "Traps carried from Slice 8"
+// (LayerNorm with bias, softmax over the slot axis per channel, pools start at
+// the first valid token, only full all-valid pools count).  Constants,
+// LAYERNORM_MODULE: the normalised key is stored in the activation dtype, so it
+// is rounded to that dtype in registers before it is pooled.
+//
+// One warp owns one pool.  Lane l owns channels [l*V, l*V + V) (V = D/32), so a
+// token row is read by the warp as one contiguous D-element segment.  The kpool
+// (<= 8) slots of the pool stay in registers: LayerNorm statistics are two warp
+// reductions per slot, the softmax runs over the slot axis in registers, and
+// the pooled key is written with one vector store per lane.  HBM-bound: a full
+// build streams 2 * D * sizeof(act) bytes per token and writes D * sizeof(act)
+// / kpool bytes per token.
+#include "dsa_internal.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kWarpsPerCta = 8;
+
+template <typename T, int V>
+struct Vec;  // V consecutive activation values
+template <>
+struct Vec<float, 1> {
+  static __device__ __forceinline__ void load(const float* p, float* o) { o[0] = __ldg(p); }
+  static __device__ __forceinline__ void store(float* p, const float* v) { *p = v[0]; }
+};
+template <>
+struct Vec<float, 2> {
+  static __device__ __forceinline__ void load(const float* p, float* o) {
+    float2 t = __ldg(reinterpret_cast<const float2*>(p));
+    o[0] = t.x; o[1] = t.y;
+  }
+  static __device__ __forceinline__ void store(float* p, const float* v) {
+    *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+  }
+};
+template <>
+struct Vec<float, 4> {
+  static __device__ __forceinline__ void load(const float* p, float* o) {
+    float4 t = __ldg(reinterpret_cast<const float4*>(p));
+    o[0] = t.x; o[1] = t.y; o[2] = t.z; o[3] = t.w;
+  }
+  static __device__ __forceinline__ void store(float* p, const float* v) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+};
+template <>
+struct Vec<float, 8> {
+  static __device__ __forceinline__ void load(const float* p, float* o) {
+    Vec<float, 4>::load(p, o);
+    Vec<float, 4>::load(p + 4, o + 4);
+  }
+  static __device__ __forceinline__ void store(float* p, const float* v) {
+    Vec<float, 4>::store(p, v);
+    Vec<float, 4>::store(p + 4, v + 4);
+  }
+};
+template <>
+struct Vec<__nv_bfloat16, 1> {
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float* o) {
+    o[0] = __bfloat162float(p[0]);
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float* v) {
+    p[0] = __float2bfloat16_rn(v[0]);
+  }
+};
+template <>
+struct Vec<__nv_bfloat16, 2> {
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float* o) {
+    uint32_t t = __ldg(reinterpret_cast<const unsigned int*>(p));
+    o[0] = bf16lo(t); o[1] = bf16hi(t);
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float* v) {
+    *reinterpret_cast<uint32_t*>(p) = pack_bf16(v[0], v[1]);
+  }
+};
+template <>
+struct Vec<__nv_bfloat16, 4> {
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float* o) {
+    uint2 t = __ldg(reinterpret_cast<const uint2*>(p));
+    o[0] = bf16lo(t.x); o[1] = bf16hi(t.x); o[2] = bf16lo(t.y); o[3] = bf16hi(t.y);
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float* v) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]));
+  }
+};
+template <>
+struct Vec<__nv_bfloat16, 8> {
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float* o) {
+    uint4 t = __ldg(reinterpret_cast<const uint4*>(p));
+    o[0] = bf16lo(t.x); o[1] = bf16hi(t.x); o[2] = bf16lo(t.y); o[3] = bf16hi(t.y);
+    o[4] = bf16lo(t.z); o[5] = bf16hi(t.z); o[6] = bf16lo(t.w); o[7] = bf16hi(t.w);
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float* v) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]),
+                                              pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+  }
+};
+
+// First valid token of sequence [lo, lo+T): block-wide scan from the front,
+// stopping at the first chunk that holds a valid byte.
+__device__ int first_valid_token(const uint8_t* valid, long long lo, int T, int* s_min) {
+  if (threadIdx.x == 0) *s_min = T;
+  __syncthreads();
+  for (int base = 0; base < T; base += blockDim.x) {
+    int t = base + threadIdx.x;
+    bool hit = (t < T) && valid[lo + t] != 0;
+    if (hit) atomicMin(s_min, t);
+    if (__syncthreads_or(hit)) break;
+  }
+  int r = *s_min;
+  __syncthreads();
+  return r;
+}
+
+template <typename T, int V>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+    kpool_compress_kernel(const T* __restrict__ k, const T* __restrict__ gate,
+                          const uint8_t* __restrict__ valid, const float* __restrict__ ape,
+                          const T* __restrict__ ln_gamma, const T* __restrict__ ln_beta,
+                          float ln_eps, const int32_t* __restrict__ cu_seqlens,
+                          const int32_t* __restrict__ cu_pool_cap,
+                          const int32_t* __restrict__ pool_begin, int kpool, int max_pools,
+                          T* __restrict__ pool_keys, int32_t* __restrict__ pool_start,
+                          uint8_t* __restrict__ pool_valid, int32_t* __restrict__ n_pools,
+                          int32_t* status) {
+  constexpr int D = 32 * V;
+  __shared__ int s_min;
+  pdl_wait();
+  const int b = blockIdx.y;
+  const long long lo = cu_seqlens[b];
+  const int Tb = cu_seqlens[b + 1] - cu_seqlens[b];
+  const long long cap_lo = cu_pool_cap[b];
+  const int cap = cu_pool_cap[b + 1] - cu_pool_cap[b];
+  const int begin = pool_begin ? pool_begin[b] : 0;
+  const long long end_ll = min((long long)begin + max_pools, (long long)cap);
+  const int end = (int)end_ll;
+
+  // Nothing of this sequence is in this CTA's pool range: skip the scan.
+  const int p_first = begin + blockIdx.x * kWarpsPerCta;
+  const bool cta_has_work = p_first < end || blockIdx.x == 0;
+  if (!cta_has_work) return;
+
+  const int t0 = first_valid_token(valid + 0, lo, Tb, &s_min);
+  const int P = (Tb - t0) / kpool;
+  const int P_eff = min(P, cap);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    n_pools[b] = P_eff;
+    if (P > cap) flag(status, DSA_DEV_POOL_OVERFLOW);
+    if (P_eff > end) flag(status, DSA_DEV_POOL_UNCOVERED);
+  }
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int p = p_first + warp;
+  if (p < 0 || p >= end) return;
+  T* out = pool_keys + (cap_lo + p) * D + lane * V;
+  if (p >= P_eff) {  // sentinel entry
+    float z[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) z[i] = 0.f;
+    Vec<T, V>::store(out, z);
+    if (lane == 0) {
+      pool_start[cap_lo + p] = -1;
+      pool_valid[cap_lo + p] = 0;
+    }
+    return;
+  }
+
+  float g[V], be[V];
+  Vec<T, V>::load(ln_gamma + lane * V, g);
+  Vec<T, V>::load(ln_beta + lane * V, be);
+
+  const long long s0 = lo + t0 + (long long)p * kpool;
+  float kn[kKpoolMax][V], lg[kKpoolMax][V];
+  bool all_valid = true;
+#pragma unroll
+  for (int s = 0; s < kKpoolMax; ++s) {
+    if (s < kpool) {
+      float x[V], gt[V];
+      Vec<T, V>::load(k + (s0 + s) * D + lane * V, x);
+      Vec<T, V>::load(gate + (s0 + s) * D + lane * V, gt);
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < V; ++i) sum += x[i];
+      const float mean = warp_sum(sum) * (1.0f / D);
+      float sq = 0.f;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const float dx = x[i] - mean;
+        sq += dx * dx;
+      }
+      const float var = warp_sum(sq) * (1.0f / D);
+      const float rstd = 1.0f / sqrtf(var + ln_eps);
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        kn[s][i] = Act<T>::round((x[i] - mean) * rstd * g[i] + be[i]);
+        lg[s][i] = gt[i] + __ldg(ape + s * D + lane * V + i);
+      }
+      all_valid &= valid[s0 + s] != 0;
+    }
+  }
+  float res[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    float m = lg[0][i];
+#pragma unroll
+    for (int s = 1; s < kKpoolMax; ++s)
+      if (s < kpool) m = fmaxf(m, lg[s][i]);
+    float den = 0.f, acc = 0.f;
+#pragma unroll
+    for (int s = 0; s < kKpoolMax; ++s) {
+      if (s < kpool) {
+        const float e = expf(lg[s][i] - m);
+        den += e;
+        acc += e * kn[s][i];
+      }
+    }
+    res[i] = acc / den;
+  }
+  Vec<T, V>::store(out, res);
+  if (lane == 0) {
+    pool_start[cap_lo + p] = t0 + p * kpool;
+    pool_valid[cap_lo + p] = all_valid ? 1 : 0;
+  }
+  pdl_launch_dependents();
+}
+
+template <typename T, int V>
+int launch_t(const void* k, const void* gate, const uint8_t* valid, const float* ape,
+             const void* g, const void* be, float eps, const int32_t* cu, const int32_t* cap,
+             const int32_t* begin, int B, int kpool, int max_pools, void* pk, int32_t* ps,
+             uint8_t* pv, int32_t* np, int32_t* st, cudaStream_t stream) {
+  const int gx = max(1, (max_pools + kWarpsPerCta - 1) / kWarpsPerCta);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(gx, B, 1);
+  cfg.blockDim = dim3(kWarpsPerCta * 32, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(
+      &cfg, kpool_compress_kernel<T, V>, (const T*)k, (const T*)gate, valid, ape, (const T*)g,
+      (const T*)be, eps, cu, cap, begin, kpool, max_pools, (T*)pk, ps, pv, np, st);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_kpool_compress(const void* k, const void* gate, const uint8_t* valid, const float* ape,
+                          const void* ln_gamma, const void* ln_beta, float ln_eps,
+                          const int32_t* cu_seqlens, const int32_t* cu_pool_cap,
+                          const int32_t* pool_begin, int B, int D, int kpool, int max_pools,
+                          int dtype, void* pool_keys, int32_t* pool_start, uint8_t* pool_valid,
+                          int32_t* n_pools, int32_t* status_dev, cudaStream_t stream) {
+#define DSA_COMPRESS_CASE(TT, VV)                                                            \
+  return launch_t<TT, VV>(k, gate, valid, ape, ln_gamma, ln_beta, ln_eps, cu_seqlens,        \
+                          cu_pool_cap, pool_begin, B, kpool, max_pools, pool_keys, pool_start, \
+                          pool_valid, n_pools, status_dev, stream)
+  if (dtype == DSA_BF16) {
+    switch (D) {
+      case 32: DSA_COMPRESS_CASE(__nv_bfloat16, 1);
+      case 64: DSA_COMPRESS_CASE(__nv_bfloat16, 2);
+      case 128: DSA_COMPRESS_CASE(__nv_bfloat16, 4);
+      case 256: DSA_COMPRESS_CASE(__nv_bfloat16, 8);
+    }
+  } else {
+    switch (D) {
+      case 32: DSA_COMPRESS_CASE(float, 1);
+      case 64: DSA_COMPRESS_CASE(float, 2);
+      case 128: DSA_COMPRESS_CASE(float, 4);
+      case 256: DSA_COMPRESS_CASE(float, 8);
+    }
+  }
+#undef DSA_COMPRESS_CASE
+  return DSA_ERR_UNSUPPORTED;
+}
+
+}  // namespace dsa

@@ -1,0 +1,449 @@
+// NoPE MLA decode restricted to the selected latent-KV rows.
+//
+// Module glm5next_dsa, "Shape of the pipeline" (NoPE MLA restricted to the
+// selected tokens), Modules, attend (selected-index NoPE MLA decode) and "Traps
+// carried from Slice 8" (NoPE: the rotary slice is empty, so a score is the
+// plain latent dot product).  The value of an absorbed-MLA latent row is the
+// row itself, so one gathered row feeds both the score and the output.
+//
+// Tensor-core kernel (bf16, L = 512, Hm % 16 == 0): one CTA = one query, one
+// group of 16 heads and one split of the selected rows.  Four warps each own a
+// 128-wide slice of the latent axis: for the scores they contract their slice
+// (partial 16 x 32 score tiles summed through shared memory), for the output
+// they own the matching 128 output columns (64 fp32 accumulators per thread).
+// Selected rows are gathered 32 at a time with 16-byte cp.async into a
+// double-buffered, XOR-swizzled shared tile (conflict-free ldmatrix), and the
+// softmax is the usual online (running max / running sum) form in base 2.
+// Splits are merged by a small combine kernel.
+#include <math.h>
+
+#include "dsa_internal.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kL = 512;
+constexpr int kHG = 16;            // heads per CTA
+constexpr int kNT = 32;            // rows per tile
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kChunks = kL / 8;    // 16-byte chunks per latent row
+constexpr int kPStride = 40;       // bf16 per sP row (32 + 8 pad)
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct MlaSmem {
+  __nv_bfloat16 q[kHG * kL];            // swizzled
+  __nv_bfloat16 kv[2][kNT * kL];        // swizzled, double buffered
+  float s_part[kWarps][kHG][kNT];
+  __nv_bfloat16 p[kHG * kPStride];
+  float m[kHG], l[kHG], alpha[kHG];
+  int row_ok[2][kNT];
+};
+
+__device__ __forceinline__ int swz(int row, int chunk) {  // element offset of a 16B chunk
+  return row * kL + ((chunk ^ (row & 7)) << 3);
+}
+
+__global__ void __launch_bounds__(kThreads)
+    mla_mma_kernel(const __nv_bfloat16* __restrict__ q_lat, const __nv_bfloat16* __restrict__ kv,
+                   const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ q_seq,
+                   const int32_t* __restrict__ token_ids, int B, int Hm, int W, int rows_per_split,
+                   float sm_scale, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                   float* __restrict__ part_o, float* __restrict__ part_ml,
+                   int32_t* status) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  MlaSmem& sm = *reinterpret_cast<MlaSmem*>(smem_raw);
+  pdl_wait();
+  const int qi = blockIdx.z, hg = blockIdx.y, split = blockIdx.x, n_split = gridDim.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int b = q_seq ? q_seq[qi] : 0;
+  const bool seq_ok = b >= 0 && b < B;
+  if (!seq_ok && split == 0 && hg == 0 && threadIdx.x == 0) flag(status, DSA_DEV_BAD_QSEQ);
+  const long long row_base = seq_ok ? cu_seqlens[b] : 0;
+  const int Tb = seq_ok ? cu_seqlens[b + 1] - cu_seqlens[b] : 0;
+  const int j_lo = min(W, split * rows_per_split);
+  const int j_hi = min(W, j_lo + rows_per_split);
+  const int n_tiles = (j_hi - j_lo + kNT - 1) / kNT;
+  const int32_t* toks = token_ids + (long long)qi * W;
+
+  // Stage the 16 x 512 query block (swizzled).
+  const __nv_bfloat16* qsrc = q_lat + ((long long)qi * Hm + hg * kHG) * kL;
+  for (int c = threadIdx.x; c < kHG * kChunks; c += kThreads) {
+    const int r = c / kChunks, ch = c % kChunks;
+    cp_async16(smem_u32(&sm.q[swz(r, ch)]), qsrc + (long long)r * kL + ch * 8, true);
+  }
+  auto load_tile = [&](int tile, int buf) {
+    const int j0 = j_lo + tile * kNT;
+    // row validity (one thread per row)
+    if (threadIdx.x < kNT) {
+      const int j = j0 + threadIdx.x;
+      int ok = 0;
+      if (j < j_hi && seq_ok) {
+        const int tok = toks[j];
+        if (tok >= Tb) flag(status, DSA_DEV_BAD_TOKEN);
+        ok = tok >= 0 && tok < Tb;
+      }
+      sm.row_ok[buf][threadIdx.x] = ok;
+    }
+    for (int c = threadIdx.x; c < kNT * kChunks; c += kThreads) {
+      const int r = c / kChunks, ch = c % kChunks;
+      const int j = j0 + r;
+      int tok = -1;
+      if (j < j_hi && seq_ok) tok = toks[j];
+      const bool ok = tok >= 0 && tok < Tb;
+      const __nv_bfloat16* src = kv + (row_base + (ok ? tok : 0)) * kL + ch * 8;
+      cp_async16(smem_u32(&sm.kv[buf][swz(r, ch)]), ok ? src : kv, ok);
+    }
+  };
+  if (threadIdx.x < kHG) {
+    sm.m[threadIdx.x] = -INFINITY;
+    sm.l[threadIdx.x] = 0.f;
+  }
+  if (n_tiles > 0) load_tile(0, 0);
+  cp_async_commit();
+
+  float o[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  uint32_t qf[8][4];
+  const float zscale = sm_scale * kLog2e;
+
+  for (int tile = 0; tile < n_tiles; ++tile) {
+    const int buf = tile & 1;
+    if (tile + 1 < n_tiles) load_tile(tile + 1, buf ^ 1);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    if (tile == 0) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int ch = warp * 16 + kk * 2 + (lane >> 4);
+        ldmatrix_x4(qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3],
+                    smem_u32(&sm.q[swz(lane & 15, ch)]));
+      }
+    }
+    // ---- partial scores over this warp's latent slice
+    float sacc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+    const __nv_bfloat16* kvb = sm.kv[buf];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+      for (int kk = 0; kk < 8; kk += 2) {
+        uint32_t b0, b1, b2, b3;
+        const int ch = warp * 16 + kk * 2 + (lane >> 3);
+        ldmatrix_x4(b0, b1, b2, b3, smem_u32(&kvb[swz(nt * 8 + (lane & 7), ch)]));
+        mma_bf16_16816(sacc[nt], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+        mma_bf16_16816(sacc[nt], qf[kk + 1][0], qf[kk + 1][1], qf[kk + 1][2], qf[kk + 1][3], b2,
+                       b3);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      sm.s_part[warp][g][nt * 8 + 2 * t] = sacc[nt][0];
+      sm.s_part[warp][g][nt * 8 + 2 * t + 1] = sacc[nt][1];
+      sm.s_part[warp][g + 8][nt * 8 + 2 * t] = sacc[nt][2];
+      sm.s_part[warp][g + 8][nt * 8 + 2 * t + 1] = sacc[nt][3];
+    }
+    __syncthreads();
+    // ---- online softmax: thread -> head h = tid/8, columns 4*(tid%8) .. +3
+    {
+      const int h = threadIdx.x >> 3, c0 = (threadIdx.x & 7) * 4;
+      float s[4];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = c0 + i;
+        float v = sm.s_part[0][h][c] + sm.s_part[1][h][c] + sm.s_part[2][h][c] +
+                  sm.s_part[3][h][c];
+        v = sm.row_ok[buf][c] ? v * zscale : -INFINITY;
+        s[i] = v;
+        mx = fmaxf(mx, v);
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      const float m_old = sm.m[h];
+      const float m_new = fmaxf(m_old, mx);
+      const bool none = m_new == -INFINITY;
+      const float alpha = none ? 1.f : exp2f(m_old - m_new);
+      float ps = 0.f;
+      float p[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        p[i] = none ? 0.f : exp2f(s[i] - m_new);
+        ps += p[i];
+      }
+      ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+      ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+      ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+      __nv_bfloat16* pr = &sm.p[h * kPStride + c0];
+      *reinterpret_cast<uint2*>(pr) = make_uint2(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]));
+      __syncwarp();
+      if ((threadIdx.x & 7) == 0) {
+        sm.m[h] = m_new;
+        sm.l[h] = sm.l[h] * alpha + ps;
+        sm.alpha[h] = alpha;
+      }
+    }
+    __syncthreads();
+    // ---- O = O * alpha + P V over this warp's 128 output columns
+    const float a_lo = sm.alpha[g], a_hi = sm.alpha[g + 8];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      o[nt][0] *= a_lo; o[nt][1] *= a_lo; o[nt][2] *= a_hi; o[nt][3] *= a_hi;
+    }
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4(a0, a1, a2, a3,
+                  smem_u32(&sm.p[(lane & 15) * kPStride + (kk * 2 + (lane >> 4)) * 8]));
+#pragma unroll
+      for (int nt = 0; nt < 16; nt += 2) {
+        uint32_t b0, b1, b2, b3;
+        const int r = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int ch = warp * 16 + nt + (lane >> 4);
+        ldmatrix_x4_trans(b0, b1, b2, b3, smem_u32(&kvb[swz(r, ch)]));
+        mma_bf16_16816(o[nt], a0, a1, a2, a3, b0, b1);
+        mma_bf16_16816(o[nt + 1], a0, a1, a2, a3, b2, b3);
+      }
+    }
+    __syncthreads();  // kv[buf], row_ok[buf], p and s_part are rewritten next tile
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // ---- epilogue
+  const float m_lo = sm.m[g], m_hi = sm.m[g + 8];
+  const float l_lo = sm.l[g], l_hi = sm.l[g + 8];
+  const int h_lo = hg * kHG + g, h_hi = h_lo + 8;
+  if (n_split == 1) {
+    const float inv_lo = l_lo > 0.f ? 1.f / l_lo : 0.f;
+    const float inv_hi = l_hi > 0.f ? 1.f / l_hi : 0.f;
+    __nv_bfloat16* o_lo = out + ((long long)qi * Hm + h_lo) * kL + warp * 128;
+    __nv_bfloat16* o_hi = out + ((long long)qi * Hm + h_hi) * kL + warp * 128;
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      *reinterpret_cast<uint32_t*>(o_lo + nt * 8 + 2 * t) =
+          pack_bf16(o[nt][0] * inv_lo, o[nt][1] * inv_lo);
+      *reinterpret_cast<uint32_t*>(o_hi + nt * 8 + 2 * t) =
+          pack_bf16(o[nt][2] * inv_hi, o[nt][3] * inv_hi);
+    }
+    if (lse && warp == 0 && t == 0) {
+      lse[(long long)qi * Hm + h_lo] = l_lo > 0.f ? (m_lo + log2f(l_lo)) / kLog2e : -INFINITY;
+      lse[(long long)qi * Hm + h_hi] = l_hi > 0.f ? (m_hi + log2f(l_hi)) / kLog2e : -INFINITY;
+    }
+  } else {
+    // partials: O unnormalised (fp32), m (base 2) and l
+    const long long slot_lo = ((long long)qi * Hm + h_lo) * n_split + split;
+    const long long slot_hi = ((long long)qi * Hm + h_hi) * n_split + split;
+    float* p_lo = part_o + slot_lo * kL + warp * 128;
+    float* p_hi = part_o + slot_hi * kL + warp * 128;
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      *reinterpret_cast<float2*>(p_lo + nt * 8 + 2 * t) = make_float2(o[nt][0], o[nt][1]);
+      *reinterpret_cast<float2*>(p_hi + nt * 8 + 2 * t) = make_float2(o[nt][2], o[nt][3]);
+    }
+    if (warp == 0 && t == 0) {
+      part_ml[slot_lo * 2] = m_lo;
+      part_ml[slot_lo * 2 + 1] = l_lo;
+      part_ml[slot_hi * 2] = m_hi;
+      part_ml[slot_hi * 2 + 1] = l_hi;
+    }
+  }
+  pdl_launch_dependents();
+}
+
+// Merge split partials: one CTA per (query, head), threads over the latent axis.
+template <typename T>
+__global__ void mla_combine_kernel(const float* __restrict__ part_o,
+                                   const float* __restrict__ part_ml, int Hm, int L, int n_split,
+                                   T* __restrict__ out, float* __restrict__ lse) {
+  pdl_wait();
+  const long long qh = (long long)blockIdx.y * Hm + blockIdx.x;
+  const float* ml = part_ml + qh * n_split * 2;
+  float m = -INFINITY;
+  for (int s = 0; s < n_split; ++s) m = fmaxf(m, ml[2 * s]);
+  float den = 0.f;
+  for (int s = 0; s < n_split; ++s)
+    if (ml[2 * s + 1] > 0.f) den += ml[2 * s + 1] * exp2f(ml[2 * s] - m);
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  for (int d = threadIdx.x; d < L; d += blockDim.x) {
+    float acc = 0.f;
+    for (int s = 0; s < n_split; ++s)
+      if (ml[2 * s + 1] > 0.f) acc += part_o[(qh * n_split + s) * L + d] * exp2f(ml[2 * s] - m);
+    out[qh * L + d] = Act<T>::from_f(acc * inv);
+  }
+  if (lse && threadIdx.x == 0) lse[qh] = den > 0.f ? (m + log2f(den)) / kLog2e : -INFINITY;
+}
+
+// Generic SIMT kernel: one CTA per (head, query); two passes over the rows.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    mla_simt_kernel(const T* __restrict__ q_lat, const T* __restrict__ kv,
+                    const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ q_seq,
+                    const int32_t* __restrict__ token_ids, int B, int Hm, int L, int W,
+                    float sm_scale, T* __restrict__ out, float* __restrict__ lse,
+                    int32_t* status) {
+  extern __shared__ float sh[];  // q [L] | z [W] | red [32]
+  float* sq = sh;
+  float* sz = sh + L;
+  float* red = sz + W;
+  pdl_wait();
+  const int h = blockIdx.x, qi = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int b = q_seq ? q_seq[qi] : 0;
+  const bool seq_ok = b >= 0 && b < B;
+  if (!seq_ok && h == 0 && threadIdx.x == 0) flag(status, DSA_DEV_BAD_QSEQ);
+  const long long row_base = seq_ok ? cu_seqlens[b] : 0;
+  const int Tb = seq_ok ? cu_seqlens[b + 1] - cu_seqlens[b] : 0;
+  for (int d = threadIdx.x; d < L; d += blockDim.x)
+    sq[d] = Act<T>::to_f(q_lat[((long long)qi * Hm + h) * L + d]);
+  __syncthreads();
+  const int32_t* toks = token_ids + (long long)qi * W;
+  for (int j = warp; j < W; j += nw) {
+    const int tok = seq_ok ? toks[j] : -1;
+    float z = -INFINITY;
+    if (tok >= Tb && lane == 0 && h == 0) flag(status, DSA_DEV_BAD_TOKEN);
+    if (tok >= 0 && tok < Tb) {
+      const T* row = kv + (row_base + tok) * L;
+      float acc = 0.f;
+      for (int d = lane; d < L; d += 32) acc = fmaf(Act<T>::to_f(row[d]), sq[d], acc);
+      z = warp_sum(acc) * sm_scale;
+    }
+    if (lane == 0) sz[j] = z;
+  }
+  __syncthreads();
+  float mx = -INFINITY;
+  for (int j = threadIdx.x; j < W; j += blockDim.x) mx = fmaxf(mx, sz[j]);
+  mx = warp_max(mx);
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = -INFINITY;
+    for (int w = 0; w < nw; ++w) m = fmaxf(m, red[w]);
+    red[0] = m;
+  }
+  __syncthreads();
+  const float m = red[0];
+  __syncthreads();
+  float den = 0.f;
+  for (int j = threadIdx.x; j < W; j += blockDim.x) {
+    const float e = (m == -INFINITY || sz[j] == -INFINITY) ? 0.f : expf(sz[j] - m);
+    sz[j] = e;
+    den += e;
+  }
+  den = warp_sum(den);
+  if (lane == 0) red[warp] = den;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < nw; ++w) s += red[w];
+    red[0] = s;
+  }
+  __syncthreads();
+  den = red[0];
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  for (int d = threadIdx.x; d < L; d += blockDim.x) {
+    float acc = 0.f;
+    for (int j = 0; j < W; ++j) {
+      const float e = sz[j];
+      if (e != 0.f) acc = fmaf(e, Act<T>::to_f(kv[(row_base + toks[j]) * L + d]), acc);
+    }
+    out[((long long)qi * Hm + h) * L + d] = Act<T>::from_f(acc * inv);
+  }
+  if (lse && threadIdx.x == 0) lse[(long long)qi * Hm + h] = den > 0.f ? m + logf(den) : -INFINITY;
+}
+
+bool fast_path(int Hm, int L, int dtype) { return dtype == DSA_BF16 && L == kL && Hm % kHG == 0; }
+
+void split_plan(int Q, int Hm, int W, int* n_split, int* rows_per_split) {
+  const int n_hg = Hm / kHG;
+  const int target = 2 * kNumSMs;
+  int s = (target + Q * n_hg - 1) / (Q * n_hg);
+  const int max_s = (W + kNT - 1) / kNT;
+  if (s > max_s) s = max_s;
+  if (s < 1) s = 1;
+  int rows = (W + s - 1) / s;
+  rows = (rows + kNT - 1) / kNT * kNT;
+  *rows_per_split = rows;
+  *n_split = (W + rows - 1) / rows;
+  if (*n_split < 1) *n_split = 1;
+}
+
+}  // namespace
+
+size_t mla_workspace_size(int Q, int Hm, int L, int out_width, int dtype) {
+  if (!fast_path(Hm, L, dtype)) return 0;
+  int n_split, rows;
+  split_plan(Q, Hm, out_width, &n_split, &rows);
+  if (n_split == 1) return 0;
+  const size_t slots = (size_t)Q * Hm * n_split;
+  return slots * L * 4 + slots * 2 * 4;
+}
+
+int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
+                               const int32_t* q_seq, const int32_t* token_ids, int Q, int B,
+                               int Hm, int L, int out_width, float sm_scale, int dtype, void* out,
+                               float* lse, void* workspace, size_t ws_bytes, int32_t* status_dev,
+                               cudaStream_t stream) {
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (fast_path(Hm, L, dtype)) {
+    int n_split, rows;
+    split_plan(Q, Hm, out_width, &n_split, &rows);
+    if (n_split > 1 && ws_bytes < mla_workspace_size(Q, Hm, L, out_width, dtype))
+      return DSA_ERR_WORKSPACE;
+    float* part_o = static_cast<float*>(workspace);
+    float* part_ml = part_o ? part_o + (size_t)Q * Hm * n_split * L : nullptr;
+    const size_t smem = sizeof(MlaSmem);
+    cudaFuncSetAttribute(mla_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cfg.gridDim = dim3(n_split, Hm / kHG, Q);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    if (cudaLaunchKernelEx(&cfg, mla_mma_kernel, (const __nv_bfloat16*)q_lat,
+                           (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, Hm,
+                           out_width, rows, sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml,
+                           status_dev) != cudaSuccess)
+      return DSA_ERR_CUDA;
+    if (n_split > 1) {
+      cfg.gridDim = dim3(Hm, Q, 1);
+      cfg.blockDim = dim3(128, 1, 1);
+      cfg.dynamicSmemBytes = 0;
+      if (cudaLaunchKernelEx(&cfg, mla_combine_kernel<__nv_bfloat16>, (const float*)part_o,
+                             (const float*)part_ml, Hm, L, n_split, (__nv_bfloat16*)out,
+                             lse) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
+  }
+  if (L % 8 != 0 || L > 1024 || Hm > 128 || out_width > 16384) return DSA_ERR_UNSUPPORTED;
+  const size_t smem = ((size_t)L + out_width + 32) * 4;
+  cfg.gridDim = dim3(Hm, Q, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaError_t e;
+  if (dtype == DSA_BF16) {
+    cudaFuncSetAttribute(mla_simt_kernel<__nv_bfloat16>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaLaunchKernelEx(&cfg, mla_simt_kernel<__nv_bfloat16>, (const __nv_bfloat16*)q_lat,
+                           (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, Hm, L,
+                           out_width, sm_scale, (__nv_bfloat16*)out, lse, status_dev);
+  } else {
+    cudaFuncSetAttribute(mla_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)smem);
+    e = cudaLaunchKernelEx(&cfg, mla_simt_kernel<float>, (const float*)q_lat, (const float*)kv,
+                           cu_seqlens, q_seq, token_ids, B, Hm, L, out_width, sm_scale,
+                           (float*)out, lse, status_dev);
+  }
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace dsa

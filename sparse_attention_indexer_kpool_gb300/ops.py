@@ -1,0 +1,132 @@
+"""Python binding of the libdsa C ABI: same names, torch tensors in.
+
+Argument marshalling only: each function checks device / dtype / contiguity,
+passes data pointers and the current CUDA stream to the C entry point of the
+same name, and raises ``DsaError`` on a non-zero return code.  Every step of
+the path runs in the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+DSA_BF16, DSA_F32 = 0, 1
+DEV_BAD_TOKEN, DEV_POOL_OVERFLOW, DEV_POOL_UNCOVERED = 1, 2, 4
+DEV_BAD_POOL_ID, DEV_BAD_QSEQ, DEV_POOL_RANGE, DEV_TIMEOUT = 8, 16, 32, 64
+
+
+class DsaError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        msg = _lib.load().dsa_status_string(code).decode()
+        super().__init__(f"{fn}: {msg} (code {code})")
+        self.code = code
+
+
+def _dtype_tag(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return DSA_BF16
+    if t.dtype == torch.float32:
+        return DSA_F32
+    raise TypeError(f"activation dtype must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(fn, code):
+    if code != 0:
+        raise DsaError(fn, code)
+
+
+def dsa_kpool_compress(k, gate, valid, ape, ln_gamma, ln_beta, ln_eps, cu_seqlens, cu_pool_cap,
+                       pool_begin, kpool, max_pools, pool_keys, pool_start, pool_valid, n_pools,
+                       status=None, stream=None):
+    act = k.dtype
+    B = cu_seqlens.numel() - 1
+    code = _lib.load().dsa_kpool_compress(
+        _ptr(k, act, "k"), _ptr(gate, act, "gate"), _ptr(valid, torch.uint8, "valid"),
+        _ptr(ape, torch.float32, "ape"), _ptr(ln_gamma, act, "ln_gamma"),
+        _ptr(ln_beta, act, "ln_beta"), float(ln_eps), _ptr(cu_seqlens, torch.int32, "cu_seqlens"),
+        _ptr(cu_pool_cap, torch.int32, "cu_pool_cap"), _ptr(pool_begin, torch.int32, "pool_begin"),
+        B, k.shape[-1], int(kpool), int(max_pools), _dtype_tag(k),
+        _ptr(pool_keys, act, "pool_keys"), _ptr(pool_start, torch.int32, "pool_start"),
+        _ptr(pool_valid, torch.uint8, "pool_valid"), _ptr(n_pools, torch.int32, "n_pools"),
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check("dsa_kpool_compress", code)
+
+
+def dsa_index_scores(q, weights, scale, pool_keys, pool_start, pool_valid, n_pools, cu_pool_cap,
+                     q_seq, q_pos, kpool, scores, status=None, stream=None):
+    Q, H, D = q.shape
+    act = q.dtype
+    code = _lib.load().dsa_index_scores(
+        _ptr(q, act, "q"), _ptr(weights, torch.float32, "weights"), float(scale),
+        _ptr(pool_keys, act, "pool_keys"), _ptr(pool_start, torch.int32, "pool_start"),
+        _ptr(pool_valid, torch.uint8, "pool_valid"), _ptr(n_pools, torch.int32, "n_pools"),
+        _ptr(cu_pool_cap, torch.int32, "cu_pool_cap"), _ptr(q_seq, torch.int32, "q_seq"),
+        _ptr(q_pos, torch.int32, "q_pos"), Q, cu_pool_cap.numel() - 1, H, D, int(kpool),
+        scores.shape[-1], _dtype_tag(q), _ptr(scores, torch.float32, "scores"),
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check("dsa_index_scores", code)
+
+
+def topk_workspace_bytes(Q, P_ld, select_k) -> int:
+    return int(_lib.load().dsa_topk_pools_workspace_size(Q, P_ld, select_k))
+
+
+def dsa_topk_pools(scores, select_k, pool_ids, workspace, stream=None):
+    Q, P_ld = scores.shape
+    code = _lib.load().dsa_topk_pools(
+        _ptr(scores, torch.float32, "scores"), Q, P_ld, int(select_k),
+        _ptr(pool_ids, torch.int32, "pool_ids"), _ptr(workspace, torch.uint8, "workspace"),
+        0 if workspace is None else workspace.numel(), _stream(stream))
+    _check("dsa_topk_pools", code)
+
+
+def dsa_expand_selection(pool_ids, pool_start, cu_pool_cap, q_seq, kpool, token_ids, status=None,
+                         stream=None):
+    Q, K = pool_ids.shape
+    code = _lib.load().dsa_expand_selection(
+        _ptr(pool_ids, torch.int32, "pool_ids"), _ptr(pool_start, torch.int32, "pool_start"),
+        _ptr(cu_pool_cap, torch.int32, "cu_pool_cap"), _ptr(q_seq, torch.int32, "q_seq"), Q,
+        cu_pool_cap.numel() - 1, K, int(kpool), token_ids.shape[-1],
+        _ptr(token_ids, torch.int32, "token_ids"), _ptr(status, torch.int32, "status"),
+        _stream(stream))
+    _check("dsa_expand_selection", code)
+
+
+def mla_workspace_bytes(Q, Hm, L, out_width, dtype_tag) -> int:
+    return int(_lib.load().dsa_mla_selected_decode_workspace_size(Q, Hm, L, out_width, dtype_tag))
+
+
+def dsa_mla_selected_decode(q_lat, kv_latent, cu_seqlens, q_seq, token_ids, sm_scale, out, lse,
+                            workspace=None, status=None, stream=None):
+    Q, Hm, L = q_lat.shape
+    act = q_lat.dtype
+    code = _lib.load().dsa_mla_selected_decode(
+        _ptr(q_lat, act, "q_lat"), _ptr(kv_latent, act, "kv_latent"),
+        _ptr(cu_seqlens, torch.int32, "cu_seqlens"), _ptr(q_seq, torch.int32, "q_seq"),
+        _ptr(token_ids, torch.int32, "token_ids"), Q, cu_seqlens.numel() - 1, Hm, L,
+        token_ids.shape[-1], float(sm_scale), _dtype_tag(q_lat), _ptr(out, act, "out"),
+        _ptr(lse, torch.float32, "lse"), _ptr(workspace, torch.uint8, "workspace"),
+        0 if workspace is None else workspace.numel(), _ptr(status, torch.int32, "status"),
+        _stream(stream))
+    _check("dsa_mla_selected_decode", code)

@@ -1,0 +1,138 @@
+"""The C ABI on a machine without a GPU: the library loads, exports every symbol
+include/dsa.h declares, and rejects bad arguments on the host before any CUDA
+call (so these calls are safe without a device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_attention_indexer_kpool_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(dsa_\w+)\s*\(", text, re.M)))
+
+
+def header_define(name):
+    m = re.search(rf"#define\s+{name}\s+(\d+)", open(HEADER).read())
+    return int(m.group(1))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(_lib.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = lib.dsa_status_string(code).decode()
+        assert s.startswith("DSA_")
+    assert lib.dsa_status_string(999).decode() == "DSA_ERR_UNKNOWN"
+    assert lib.dsa_version() >= 10000
+
+
+ERR = {n: header_define(n) for n in ("DSA_OK", "DSA_ERR_INVALID_ARG", "DSA_ERR_MISALIGNED",
+                                     "DSA_ERR_UNSUPPORTED", "DSA_ERR_WORKSPACE")}
+A = 0x10000          # a 16-byte-aligned fake address; never dereferenced by these calls
+
+
+def compress(lib, **kw):
+    a = dict(k=A, gate=A, valid=A, ape=A, g=A, b=A, eps=1e-5, cu=A, cap=A, begin=None, B=1, D=128,
+             kpool=4, max_pools=8, dtype=0, pk=A, ps=A, pv=A, np_=A, st=None, stream=None)
+    a.update(kw)
+    return lib.dsa_kpool_compress(a["k"], a["gate"], a["valid"], a["ape"], a["g"], a["b"],
+                                  a["eps"], a["cu"], a["cap"], a["begin"], a["B"], a["D"],
+                                  a["kpool"], a["max_pools"], a["dtype"], a["pk"], a["ps"], a["pv"],
+                                  a["np_"], a["st"], a["stream"])
+
+
+def test_compress_validation(lib):
+    assert compress(lib, kpool=9) == ERR["DSA_ERR_INVALID_ARG"]     # refuse, never truncate
+    assert compress(lib, kpool=0) == ERR["DSA_ERR_INVALID_ARG"]
+    assert compress(lib, dtype=7) == ERR["DSA_ERR_INVALID_ARG"]
+    assert compress(lib, eps=float("nan")) == ERR["DSA_ERR_INVALID_ARG"]
+    assert compress(lib, D=96) == ERR["DSA_ERR_UNSUPPORTED"]
+    assert compress(lib, k=None) == ERR["DSA_ERR_INVALID_ARG"]
+    assert compress(lib, k=A + 8) == ERR["DSA_ERR_MISALIGNED"]
+    assert compress(lib, B=0) == ERR["DSA_OK"]                        # empty batch: no-op
+    assert compress(lib, max_pools=-1) == ERR["DSA_ERR_INVALID_ARG"]
+
+
+def scores_call(lib, **kw):
+    a = dict(q=A, w=A, scale=0.088, pk=A, ps=A, pv=A, np_=A, cap=A, qs=A, qp=None, Q=4, B=4, H=32,
+             D=128, kpool=4, P_ld=64, dtype=0, out=A, st=None, stream=None)
+    a.update(kw)
+    return lib.dsa_index_scores(a["q"], a["w"], a["scale"], a["pk"], a["ps"], a["pv"], a["np_"],
+                                a["cap"], a["qs"], a["qp"], a["Q"], a["B"], a["H"], a["D"],
+                                a["kpool"], a["P_ld"], a["dtype"], a["out"], a["st"], a["stream"])
+
+
+def test_index_scores_validation(lib):
+    assert scores_call(lib, kpool=9) == ERR["DSA_ERR_INVALID_ARG"]
+    assert scores_call(lib, scale=0.0) == ERR["DSA_ERR_INVALID_ARG"]
+    assert scores_call(lib, scale=float("inf")) == ERR["DSA_ERR_INVALID_ARG"]
+    assert scores_call(lib, H=65) == ERR["DSA_ERR_UNSUPPORTED"]
+    assert scores_call(lib, D=100) == ERR["DSA_ERR_UNSUPPORTED"]
+    assert scores_call(lib, qp=A, ps=None) == ERR["DSA_ERR_INVALID_ARG"]   # causal needs starts
+    assert scores_call(lib, q=A + 4) == ERR["DSA_ERR_MISALIGNED"]
+    assert scores_call(lib, P_ld=0) == ERR["DSA_ERR_INVALID_ARG"]
+    assert scores_call(lib, Q=0) == ERR["DSA_OK"]
+
+
+def test_topk_validation(lib):
+    ws = lib.dsa_topk_pools_workspace_size(4, 1000, 16)
+    assert ws > 0
+    assert lib.dsa_topk_pools(A, 4, 1000, 0, A, A, ws, None) == ERR["DSA_ERR_INVALID_ARG"]
+    assert lib.dsa_topk_pools(A, 4, 1000, 4097, A, A, ws, None) == ERR["DSA_ERR_UNSUPPORTED"]
+    assert lib.dsa_topk_pools(A, 4, 1000, 16, A, A, ws - 1, None) == ERR["DSA_ERR_WORKSPACE"]
+    assert lib.dsa_topk_pools(A, 4, 1000, 16, A, None, ws, None) == ERR["DSA_ERR_WORKSPACE"]
+    assert lib.dsa_topk_pools(A, 4, 1000, 16, A, A + 8, ws, None) == ERR["DSA_ERR_MISALIGNED"]
+    assert lib.dsa_topk_pools(A, 0, 1000, 16, A, None, 0, None) == ERR["DSA_OK"]
+
+
+def test_expand_validation(lib):
+    f = lib.dsa_expand_selection
+    assert f(A, A, A, A, 2, 2, 8, 4, 31, A, None, None) == ERR["DSA_ERR_INVALID_ARG"]  # W < K*kp
+    assert f(A, A, A, A, 2, 2, 8, 9, 80, A, None, None) == ERR["DSA_ERR_INVALID_ARG"]
+    assert f(A, A, A, A, 2, 2, 8, 4, 32, None, None, None) == ERR["DSA_ERR_INVALID_ARG"]
+    assert f(A, A, A, A, 2, 2, 8, 4, 32, A + 2, None, None) == ERR["DSA_ERR_MISALIGNED"]
+    assert f(A, A, A, A, 0, 2, 8, 4, 32, A, None, None) == ERR["DSA_OK"]
+
+
+def test_mla_validation(lib):
+    f = lib.dsa_mla_selected_decode
+    ws = lib.dsa_mla_selected_decode_workspace_size(4, 64, 512, 2048, 0)
+    assert ws > 0
+    assert lib.dsa_mla_selected_decode_workspace_size(4, 64, 512, 2048, 1) == 0
+    assert f(A, A, A, A, A, 4, 4, 64, 500, 2048, 0.04, 0, A, A, A, ws, None, None) \
+        == ERR["DSA_ERR_UNSUPPORTED"]
+    assert f(A, A, A, A, A, 4, 4, 64, 512, 2048, 0.04, 0, A, A, A, ws - 1, None, None) \
+        == ERR["DSA_ERR_WORKSPACE"]
+    assert f(A, A, A, A, A, 4, 4, 64, 512, 2048, 0.04, 0, A + 8, A, A, ws, None, None) \
+        == ERR["DSA_ERR_MISALIGNED"]
+    assert f(A, A, A, A, A, 4, 4, 64, 512, 2048, float("nan"), 0, A, A, A, ws, None, None) \
+        == ERR["DSA_ERR_INVALID_ARG"]
+    assert f(A, A, A, A, A, 0, 4, 64, 512, 2048, 0.04, 0, A, A, A, ws, None, None) == ERR["DSA_OK"]
+
+
+def test_python_binding_fails_loudly_without_cuda_tensors(lib):
+    import torch
+    from sparse_attention_indexer_kpool_gb300 import ops
+    x = torch.zeros(4, 4)
+    with pytest.raises(ValueError):
+        ops._ptr(x, torch.float32, "x")                          # CPU tensor refused

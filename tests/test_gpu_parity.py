@@ -1,0 +1,219 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_attention_indexer_kpool_gb300 import ops, pipeline, synth
+from sparse_attention_indexer_kpool_gb300.synth import Geometry
+from tests import _parity as par
+from tests._util import npf, npi, oracle_inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def run_and_check(bt, expect_status=0, end_to_end=False):
+    buf = pipeline.LayerBuffers.alloc(bt)
+    pipeline.run_layer(bt, buf)
+    torch.cuda.synchronize()
+    o = oracle_inputs(bt)
+    st = par.check_compress(o, buf)
+    _, st2 = par.check_scores(o, buf)
+    par.check_topk(buf, bt.geo.select_k)
+    st3 = par.check_expand(o, buf)
+    st4 = par.check_mla(o, buf)
+    assert int(buf.status.item()) == (st | st2 | st3 | st4 | expect_status)
+    if end_to_end:
+        r = oracle.run_path(o)
+        assert np.array_equal(buf.pool_ids.cpu().numpy(), r["pool_ids"])
+        assert np.array_equal(buf.token_ids.cpu().numpy(), r["token_ids"])
+    return buf, o
+
+
+def test_tiny_fp32_all_stages():
+    bt = synth.tiny(device=DEV)
+    buf, o = run_and_check(bt, end_to_end=True)
+    s = buf.scores[0].cpu().double().numpy()
+    ids = buf.pool_ids[0].cpu().numpy()
+    kth = s[ids[-1]]
+    assert any(s[p] == kth for p in range(63) if p not in set(ids)), "tie must straddle cutoff"
+
+
+def test_tiny_sentinel_tail_and_wide_output():
+    bt = synth.tiny(device=DEV, select_k=64)          # 63 pools < 64: -1 tail
+    buf, _ = run_and_check(bt, end_to_end=True)
+    assert buf.pool_ids[0, 63].item() == -1 and (buf.token_ids[0, 252:] == -1).all()
+    bt = synth.tiny(device=DEV, select_k=8, out_width=40)   # columns 32..39 are -1
+    buf, _ = run_and_check(bt, end_to_end=True)
+    assert (buf.token_ids[0, 32:] == -1).all()
+
+
+def ragged_small(dtype="bf16", select_k=64, out_width=320, seed=11):
+    geo = Geometry(D=128, H=32, kpool=4, select_k=select_k, out_width=out_width, Hm=64, L=512,
+                   dtype=dtype)
+    # 0 tokens; kpool-1 valid tokens; 5*kpool+3 valid tokens; all padding; two long ones
+    lengths = [1203, 0, 3, 23, 50, 2500]
+    pads = [5, 0, 0, 0, 50, 1]
+    return synth.make_batch(geo, lengths, pads, device=DEV, seed=seed)
+
+
+def test_ragged_small_bf16_tensor_core_paths():
+    bt = ragged_small()
+    buf, _ = run_and_check(bt)
+    ids = buf.pool_ids.cpu().numpy()
+    assert (ids[1] == -1).all() and (ids[2] == -1).all() and (ids[4] == -1).all()
+    assert (ids[3, :5] >= 0).all() and (ids[3, 5:] == -1).all()    # 23 tokens -> 5 pools
+    tok = buf.token_ids.cpu().numpy()
+    assert (tok[:, 256:] == -1).all()
+    assert torch.all(buf.out[1] == 0) and torch.isinf(buf.lse[1]).all()
+
+
+def test_single32k_bf16():
+    bt = synth.single32k(device=DEV)
+    run_and_check(bt)
+
+
+def test_generic_kernels_bf16():
+    geo = Geometry(D=64, H=8, kpool=3, select_k=16, out_width=48, Hm=8, L=64, dtype="bf16")
+    bt = synth.make_batch(geo, [500, 97], [2, 0], device=DEV, seed=5)
+    run_and_check(bt)
+
+
+def test_generic_kernels_fp32_kpool8_and_1():
+    for kp in (8, 1):
+        geo = Geometry(D=32, H=4, kpool=kp, select_k=8, out_width=8 * kp + 3, Hm=4, L=64,
+                       dtype="f32")
+        bt = synth.make_batch(geo, [301, 64], [9, 1], device=DEV, seed=6 + kp)
+        run_and_check(bt)
+
+
+def test_incremental_compress_matches_full_build():
+    bt = ragged_small(seed=21)
+    buf = pipeline.LayerBuffers.alloc(bt)
+    pipeline.compress(bt, buf)
+    torch.cuda.synchronize()
+    # new data arrives for every sequence's last complete pool: rewrite those tokens
+    o = oracle_inputs(bt)
+    n = buf.n_pools.cpu().numpy()
+    begin = np.maximum(n - 1, 0).astype(np.int32)
+    for b in range(bt.B):
+        if n[b] == 0:
+            continue
+        lo = int(o["cu_seqlens"][b]) + int(buf.pool_start[int(o["cu_pool_cap"][b]) + n[b] - 1])
+        bt.k[lo:lo + 4] = torch.randn(4, 128, device=DEV).to(bt.k.dtype)
+        bt.gate[lo:lo + 4] = torch.randn(4, 128, device=DEV).to(bt.k.dtype)
+    cache = dict(pool_keys=npf(buf.pool_keys), pool_start=npi(buf.pool_start),
+                 pool_valid=buf.pool_valid.cpu().numpy())
+    pool_begin = torch.as_tensor(begin, device=DEV)
+    pipeline.compress(bt, buf, pool_begin=pool_begin, max_pools=1)
+    torch.cuda.synchronize()
+    o = oracle_inputs(bt)
+    par.check_compress(o, buf, pool_begin=begin, max_pools=1, cache=cache)
+    full = pipeline.LayerBuffers.alloc(bt)
+    pipeline.compress(bt, full)
+    torch.cuda.synchronize()
+    assert torch.equal(full.pool_keys, buf.pool_keys)
+    assert torch.equal(full.pool_start, buf.pool_start)
+
+
+def _topk_gpu(scores, k):
+    Q, P = scores.shape
+    ws = torch.empty(ops.topk_workspace_bytes(Q, P, k), dtype=torch.uint8, device=DEV)
+    ids = torch.full((Q, k), 0x7F7F7F7F, dtype=torch.int32, device=DEV)
+    ops.dsa_topk_pools(scores, k, ids, ws)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy().astype(np.int64)
+
+
+@pytest.mark.parametrize("P,k", [(1, 1), (17, 8), (1000, 8), (1000, 999), (1000, 1000),
+                                 (5000, 4096), (65536, 512), (70000, 2048)])
+def test_topk_tie_stress(P, k):
+    g = torch.Generator(device=DEV).manual_seed(P * 7 + k)
+    Q = 6
+    s = torch.randint(-4, 5, (Q, P), generator=g, device=DEV).float() * 0.25     # heavy ties
+    s[1] = torch.randn(P, generator=g, device=DEV)                                # distinct
+    s[2] = 0.0                                                                    # all equal
+    s[2, ::3] = -0.0
+    s[3, : P // 2] = -math.inf                                                    # half absent
+    s[4] = -math.inf                                                              # no candidate
+    s[5, ::5] = float("nan")
+    s[5, 1::7] = math.inf
+    got = _topk_gpu(s, k)
+    ref = oracle.topk_pools(s.cpu().double().numpy(), k)
+    assert np.array_equal(got, ref)
+
+
+def test_topk_tie_list_overflow_path():
+    # 20000 equal candidates in one histogram bin exceed the tie list: exact slow path
+    s = torch.full((3, 30000), 1.0, device=DEV)
+    s[0, 20000:] = 2.0 ** -30                       # lower bin
+    s[1, :100] = 5.0                                # 100 sure keys, the rest tied
+    s[2, 7::11] = 1.0 + 2.0 ** -20                  # same 12-bit bin, distinct low bits
+    for k in (1, 511, 4096):
+        assert np.array_equal(_topk_gpu(s, k), oracle.topk_pools(s.cpu().double().numpy(), k))
+
+
+def test_expand_overwrites_every_entry_and_flags_bad_ids():
+    cap = torch.tensor([0, 5, 9], dtype=torch.int32, device=DEV)
+    start = torch.tensor([0, 4, 8, 12, 16, 1, 9, 17, -1], dtype=torch.int32, device=DEV)
+    ids = torch.tensor([[4, 0, -1], [2, 3, 7], [0, -1, -1]], dtype=torch.int32, device=DEV)
+    q_seq = torch.tensor([0, 1, 1], dtype=torch.int32, device=DEV)
+    tok = torch.full((3, 14), 0x7F7F7F7F, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ops.dsa_expand_selection(ids, start, cap, q_seq, 4, tok, st)
+    torch.cuda.synchronize()
+    ref, rst = oracle.expand_selection(ids.cpu().numpy(), start.cpu().numpy(), [0, 5, 9],
+                                       [0, 1, 1], 4, 14)
+    assert np.array_equal(tok.cpu().numpy(), ref)
+    assert int(st.item()) == rst == ops.DEV_BAD_POOL_ID
+
+
+def test_mla_bad_tokens_and_empty_rows():
+    geo = synth.GEO_MAIN
+    bt = synth.make_batch(geo, [300, 700], [0, 0], device=DEV, seed=9)
+    W = 2048
+    g = torch.Generator(device=DEV).manual_seed(3)
+    tok = torch.randint(-1, 300, (2, W), generator=g, device=DEV, dtype=torch.int32)
+    tok[1, :] = -1                                 # empty selection
+    tok[0, 5] = 300                                # out of range for sequence 0 -> flagged
+    Q = 2
+    out = torch.empty(Q, 64, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(Q, 64, dtype=torch.float32, device=DEV)
+    nb = ops.mla_workspace_bytes(Q, 64, 512, W, ops.DSA_BF16)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ops.dsa_mla_selected_decode(bt.q_lat, bt.kv, bt.cu_seqlens, bt.q_seq, tok, bt.sm_scale, out,
+                                lse, ws, st)
+    torch.cuda.synchronize()
+    o = oracle_inputs(bt)
+    ref, ref_lse, rst = oracle.mla_selected_decode(o["q_lat"], o["kv"], o["cu_seqlens"],
+                                                   o["q_seq"], tok.cpu().numpy(), bt.sm_scale,
+                                                   "bf16")
+    assert np.abs(out.cpu().double().numpy() - ref).max() <= 1e-2
+    assert int(st.item()) == rst == ops.DEV_BAD_TOKEN
+    assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
+
+
+def test_bad_query_sequence_is_flagged_not_faulted():
+    bt = ragged_small(seed=31)
+    bt.q_seq[2] = 99
+    buf = pipeline.LayerBuffers.alloc(bt)
+    pipeline.run_layer(bt, buf)
+    torch.cuda.synchronize()
+    assert int(buf.status.item()) & ops.DEV_BAD_QSEQ
+    assert torch.all(torch.isneginf(buf.scores[2]))
+    assert torch.all(buf.token_ids[2] == -1) and torch.all(buf.out[2] == 0)
+
+
+def test_repeat_runs_are_bitwise_identical():
+    bt = synth.single32k(device=DEV, seed=77)
+    a = pipeline.LayerBuffers.alloc(bt)
+    b = pipeline.LayerBuffers.alloc(bt)
+    pipeline.run_layer(bt, a)
+    pipeline.run_layer(bt, b)
+    torch.cuda.synchronize()
+    for name in ("pool_keys", "scores", "pool_ids", "token_ids", "out", "lse"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name

@@ -33,8 +33,7 @@ MUTATIONS = {
     "scale_dropped": ("np.maximum(0.0, scale * dots)", "np.maximum(0.0, dots)"),
     "causal_strict": ("cand &= last_tok <= int(q_pos[i])", "cand &= last_tok < int(q_pos[i])"),
     "tie_order_reversed": ("order = np.lexsort((cand, -s))", "order = np.lexsort((-cand, -s))"),
-    "expand_without_base": ("out[i, j * kpool + s] = int(pool_start[base + p]) + s",
-                            "out[i, j * kpool + s] = int(pool_start[p]) + s"),
+    "expand_without_base": ("start = int(pool_start[base + p])", "start = int(pool_start[p])"),
     "mla_without_row_base": ("C = kv[lo + sel]", "C = kv[sel]"),
     "mla_scale_dropped": ("z = sm_scale * (q_lat[i] @ C.T)", "z = (q_lat[i] @ C.T)"),
     "bf16_truncates": ("r = np.rint(x / spacing) * spacing", "r = np.trunc(x / spacing) * spacing"),

@@ -364,6 +364,8 @@ def test_expand_sequence_bases_and_bad_ids():
                                       [0, 2, 5], [0, 1, 1], 2, 5)
     assert tok.tolist() == [[4, 5, -1, -1, -1], [14, 15, 10, 11, -1], [-1, -1, 12, 13, -1]]
     assert st == oracle.ST_BAD_POOL_ID
+    tok, st = oracle.expand_selection(np.array([[1, 0]]), np.array([5, -1]), [0, 2], None, 2, 4)
+    assert tok.tolist() == [[-1, -1, 5, 6]] and st == 0            # sentinel entry -> -1
     with pytest.raises(ValueError):
         oracle.expand_selection(np.zeros((1, 2), int), pool_start, [0, 5], None, 2, 3)
 
