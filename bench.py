@@ -1,0 +1,542 @@
+#!/usr/bin/env python
+"""Decode-step benchmark: DSA kpool selection + selected-row NoPE MLA at 262k context.
+
+Workload (default): 4 sequences x 262 144 tokens (65 536 pools each at kpool 4),
+32 index heads x head_dim 128, select_k 512 -> 2 048 token ids, MLA 64 heads x
+latent 512, bf16, 11 independent DSA layers per step (each with its own seeded
+caches and weights).  One step = every layer's decode pass for the 4 query
+tokens: incremental kpool_compress of the just-completed pool -> index_scores
+-> topk_pools -> expand_selection -> MLA over the selected rows.  The step is
+captured in a CUDA graph; caches live in HBM before the timed region starts and
+the 11 layers' 704 MB of pool keys cycle through the 129 MB L2, so every step
+reads its pool keys from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")   # the CPU oracle legs run on one core
+
+METRIC = "DSA decode queries/sec at 262k ctx; index+attend HBM GB/s vs peak (1 GB300)"
+UNIT = "queries/s"
+N_LAYERS = 11
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    # profiling helpers (non-default shapes are never reported as the metric)
+    ap.add_argument("--layers", type=int, default=N_LAYERS)
+    ap.add_argument("--seqlen", type=int, default=262144)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--breakdown", action="store_true",
+                    help="diagnostic: per-stage in-graph times (extra events between stages)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: no data-path collective)
+# ---------------------------------------------------------------------------
+class Dist:
+    def __init__(self, n_gpus):
+        import torch
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if torch.cuda.is_available():
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.uuid}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if self.proc is None:
+            return out
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if sm:
+            out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                   "reasons": sorted(reasons), "samples": len(sm)}
+        return out
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def algorithmic_bytes(B, P, D, H, Hm, L, K, kp, W):
+    """Bytes one decode query-layer must move at minimum (per stage)."""
+    idx = P * D * 2 + P * 1 + H * D * 2 + H * 4 + P * 4          # keys, valid, q, w, scores out
+    topk = P * 4 + K * 4                                           # scores in, pool ids out
+    expand = K * 4 + K * 4 + W * 4                                 # ids, pool starts, token ids
+    mla = W * 4 + W * L * 2 + Hm * L * 2 + Hm * L * 2 + Hm * 4    # ids, rows, q_lat, out, lse
+    comp = 2 * kp * D * 2 + kp + D * 2 + 4 + 1                     # last pool: k, gate, valid, out
+    return dict(index=idx, topk=topk, expand=expand, mla=mla, compress=comp,
+                total=idx + topk + expand + mla + comp)
+
+
+def run_ours(args, dist):
+    import torch
+
+    from sparse_attention_indexer_kpool_gb300 import build as libbuild
+    from sparse_attention_indexer_kpool_gb300 import ops, pipeline, synth
+
+    libbuild.build()
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    uuid = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else str(dist.local)
+    n_layers, T = args.layers, args.seqlen
+    full = (n_layers == N_LAYERS and T == 262144)
+    geo = synth.GEO_MAIN
+    B = 4
+    Q = B
+
+    # ---- per-step host I/O lives in two contiguous staging buffers
+    q_bytes = Q * geo.H * geo.D * 2
+    w_bytes = Q * geo.H * 4
+    ql_bytes = Q * geo.Hm * geo.L * 2
+    in_per_layer = q_bytes + w_bytes + ql_bytes
+    out_per_layer = Q * geo.Hm * geo.L * 2 + Q * geo.Hm * 4
+    stage_in = torch.empty(n_layers * in_per_layer, dtype=torch.uint8, device=dev)
+    stage_out = torch.empty(n_layers * out_per_layer, dtype=torch.uint8, device=dev)
+
+    layers = []
+    for l in range(n_layers):
+        bt = synth.make_batch(geo, [T] * B, [0] * B, device=dev, seed=3000 + 100 * l)
+        bt.q_pos = None                      # decode query at T-1: every complete pool is visible
+        o = l * in_per_layer
+        for name, nb, dt, shape in (("q", q_bytes, torch.bfloat16, (Q, geo.H, geo.D)),
+                                    ("weights", w_bytes, torch.float32, (Q, geo.H)),
+                                    ("q_lat", ql_bytes, torch.bfloat16, (Q, geo.Hm, geo.L))):
+            view = stage_in[o:o + nb].view(dt).view(shape)
+            view.copy_(getattr(bt, name))
+            setattr(bt, name, view)
+            o += nb
+        buf = pipeline.LayerBuffers.alloc(bt)
+        o = l * out_per_layer
+        ob = Q * geo.Hm * geo.L * 2
+        buf.out = stage_out[o:o + ob].view(torch.bfloat16).view(Q, geo.Hm, geo.L)
+        buf.lse = stage_out[o + ob:o + out_per_layer].view(torch.float32).view(Q, geo.Hm)
+        layers.append((bt, buf))
+    torch.cuda.synchronize()
+
+    # ---- full cache build (kpool_compress over every token), timed for information
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for bt, buf in layers:
+        pipeline.compress(bt, buf)
+    e1.record()
+    torch.cuda.synchronize()
+    build_ms = e0.elapsed_time(e1)
+    build_bytes = n_layers * (B * T * (2 * geo.D * 2 + 1) + B * (T // geo.kpool) * (geo.D * 2 + 5))
+    for bt, buf in layers:
+        assert int(buf.status.item()) == 0
+        buf.pool_begin = (buf.n_pools - 1).clamp(min=0).to(torch.int32)
+
+    def step(events=None):
+        """One decode step over every layer; events[layer] = (before, after) the
+        select call (index_scores + top-k + expand)."""
+        for li, (bt, buf) in enumerate(layers):
+            pipeline.compress(bt, buf, pool_begin=buf.pool_begin, max_pools=1)
+            if events is not None:
+                events[li][0].record()
+            pipeline.select(bt, buf)
+            if events is not None:
+                events[li][1].record()
+            pipeline.attend(bt, buf)
+
+    kernels_per_layer = 4   # compress, index scores (+histogram), select (+expand), MLA
+
+    # ---- warm-up (eager), then capture
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    S = max(d for d in range(1, min(K, 20) + 1) if K % d == 0)
+    R = K // S
+    try:
+        ev = [[[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+               for _ in range(n_layers)] for _ in range(S)]
+        ev_ok = True
+    except TypeError:
+        ev, ev_ok = None, False
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_ev, stream=side):
+            for s in range(S):
+                step(ev[s] if ev_ok else None)
+    g1 = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g1, stream=side):
+            step()
+    torch.cuda.synchronize()
+    g_ev.replay()
+    torch.cuda.synchronize()
+    for bt, buf in layers:
+        assert int(buf.status.item()) == 0, "device status set during warm-up"
+
+    # ---- timed region: K steps
+    sampler = ClockSampler(uuid)
+    dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(R):
+        g_ev.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks = sampler.stop()
+    ms = dist.max(t0.elapsed_time(t1))
+    idx_ms = None
+    if ev_ok:
+        durs = [ev[s][l][0].elapsed_time(ev[s][l][1]) for s in range(S) for l in range(n_layers)]
+        idx_ms = sum(durs) / len(durs)
+
+    # ---- end to end: pinned host inputs -> device, the step, results -> host
+    e2e = None
+    if not args.no_e2e:
+        h_in = torch.empty(stage_in.numel(), dtype=torch.uint8, pin_memory=True)
+        h_in.copy_(stage_in)
+        h_out = torch.empty(stage_out.numel(), dtype=torch.uint8, pin_memory=True)
+        stream = torch.cuda.current_stream()
+        for _ in range(3):
+            stage_in.copy_(h_in, non_blocking=True)
+            g1.replay()
+            h_out.copy_(stage_out, non_blocking=True)
+        torch.cuda.synchronize()
+        dist.barrier()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        wall0 = time.perf_counter()
+        a.record()
+        for _ in range(K):
+            stage_in.copy_(h_in, non_blocking=True)
+            g1.replay()
+            h_out.copy_(stage_out, non_blocking=True)
+        b_.record()
+        stream.synchronize()
+        wall = time.perf_counter() - wall0
+        e_ms = dist.max(max(a.elapsed_time(b_), wall * 1e3))
+        e2e = {"value": dist.world * Q * K / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(stage_in.numel()),
+               "d2h_bytes_per_step": int(stage_out.numel())}
+
+    breakdown = None
+    if args.breakdown:
+        names = ("compress", "select", "attend")
+        evb = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+               for _ in range(n_layers)]
+        gb = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(gb, stream=side):
+                for li, (bt, buf) in enumerate(layers):
+                    evb[li][0].record()
+                    pipeline.compress(bt, buf, pool_begin=buf.pool_begin, max_pools=1)
+                    evb[li][1].record()
+                    pipeline.select(bt, buf)
+                    evb[li][2].record()
+                    pipeline.attend(bt, buf)
+                    evb[li][3].record()
+        tot = {n: 0.0 for n in names}
+        reps = 20
+        for _ in range(reps):
+            gb.replay()
+            torch.cuda.synchronize()
+            for li in range(n_layers):
+                for i, n in enumerate(names):
+                    tot[n] += evb[li][i].elapsed_time(evb[li][i + 1])
+        breakdown = {n: round(v / (reps * n_layers) * 1e3, 2) for n, v in tot.items()}
+        breakdown["unit"] = "us per layer (in-graph, events between stages)"
+
+    # ---- numbers
+    ab = algorithmic_bytes(B, T // geo.kpool, geo.D, geo.H, geo.Hm, geo.L, geo.select_k,
+                           geo.kpool, geo.out_width)
+    per_step_bytes = ab["total"] * Q * n_layers
+    value = dist.world * Q * K / (ms / 1e3)
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        peaks = json.load(open(peaks_path))
+        hbm_peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+    else:
+        hbm_peak, peak_src = 6800.0, "fallback"
+    sel_bytes = (ab["index"] + ab["topk"] + ab["expand"]) * Q
+    roofline = None
+    if idx_ms:
+        achieved = sel_bytes / (idx_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm",
+                    "kernel": "dsa_select call: index_scores_mma_kernel + topk_select_kernel",
+                    "achieved": round(achieved, 1), "peak": hbm_peak, "peak_source": peak_src,
+                    "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                    "bytes_per_launch": sel_bytes, "launch_us": round(idx_ms * 1e3, 2)}
+    step_gbs = per_step_bytes / (ms / K * 1e-3) / 1e9
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": dist.world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) caches/queries, shapes of the pages' 262k workload)",
+        "config": {"workload": "long262k" if full else f"profile-{n_layers}x{T}",
+                   "sequences": B, "context": T, "pools_per_seq": T // geo.kpool,
+                   "layers": n_layers, "index_heads": geo.H, "head_dim": geo.D,
+                   "kpool": geo.kpool, "select_k": geo.select_k, "out_width": geo.out_width,
+                   "mla_heads": geo.Hm, "latent": geo.L,
+                   "l2": "inputs larger than L2: 11 layers x 64 MiB pool keys cycle through L2",
+                   "graph": "CUDA graph of %d steps replayed %d times" % (S, R)},
+        "gpu_launches": kernels_per_layer * n_layers * K,
+        "roofline": roofline,
+        "step_hbm_gbs": round(step_gbs, 1), "step_frac_of_peak": round(step_gbs / hbm_peak, 4),
+        "algorithmic_bytes_per_query_layer": ab,
+        "compress_build": {"ms": round(build_ms, 3),
+                           "gbs": round(build_bytes / (build_ms * 1e-3) / 1e9, 1)},
+        "clocks": clocks, "e2e": e2e,
+    }
+    if breakdown:
+        out["breakdown"] = breakdown
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(layers[0], args.cpu_seconds)
+    if dist.rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs
+# ---------------------------------------------------------------------------
+def oracle_query_layer(host, b):
+    """One decode query-layer through the oracle, stage after stage."""
+    import numpy as np
+
+    import oracle
+    kp = host["kpool"]
+    # incremental compress of the last complete pool of sequence b
+    pk, ps, pv, n, _ = oracle.kpool_compress(
+        host["k"][b], host["gate"][b], host["valid"][b], host["ape"], host["ln_gamma"],
+        host["ln_beta"], host["ln_eps"], [0, host["T"]], [0, host["cap"]], kp, "bf16",
+        pool_begin=[host["cap"] - 1], max_pools=1, pool_keys=host["pool_keys"][b],
+        pool_start=host["pool_start"][b], pool_valid=host["pool_valid"][b])
+    scores, _ = oracle.index_scores(host["q"][b:b + 1], host["w"][b:b + 1], host["scale"], pk, ps,
+                                    pv, n, [0, host["cap"]], None, None, kp, host["cap"])
+    ids = oracle.topk_pools(scores, host["select_k"])
+    tok, _ = oracle.expand_selection(ids, ps, [0, host["cap"]], None, kp, host["out_width"])
+    out, lse, _ = oracle.mla_selected_decode(host["q_lat"][b:b + 1], host["kv"][b], [0, host["T"]],
+                                             None, tok, host["sm_scale"], "bf16")
+    return out
+
+
+class _Rows:
+    """Row access to a host bf16 tensor that yields exact float64 rows."""
+
+    def __init__(self, t):
+        self.t = t
+        self.shape = tuple(t.shape)
+
+    def __getitem__(self, idx):
+        import numpy as np
+        import torch
+        if isinstance(idx, slice):
+            return self.t[idx].to(torch.float64).numpy()
+        return self.t[torch.as_tensor(np.asarray(idx))].to(torch.float64).numpy()
+
+
+def host_layer(layer):
+    """Host copies of one layer for the oracle (bf16 kept; rows widen on access)."""
+    import torch
+    bt, buf = layer
+    T, B = bt.lengths[0], bt.B
+    cap = T // bt.geo.kpool
+    f = lambda t: t.detach().to("cpu", torch.float64).numpy()
+    cpu = lambda t: t.detach().to("cpu")
+    return {
+        "T": T, "cap": cap, "kpool": bt.geo.kpool, "select_k": bt.geo.select_k,
+        "out_width": bt.geo.out_width, "scale": bt.scale, "sm_scale": bt.sm_scale,
+        "ln_eps": bt.geo.ln_eps, "ape": f(bt.ape), "ln_gamma": f(bt.ln_gamma),
+        "ln_beta": f(bt.ln_beta),
+        "k": [_Rows(cpu(bt.k[b * T:(b + 1) * T])) for b in range(B)],
+        "gate": [_Rows(cpu(bt.gate[b * T:(b + 1) * T])) for b in range(B)],
+        "valid": [bt.valid[b * T:(b + 1) * T].cpu().numpy() for b in range(B)],
+        "kv": [_Rows(cpu(bt.kv[b * T:(b + 1) * T])) for b in range(B)],
+        "pool_keys": [f(buf.pool_keys[b * cap:(b + 1) * cap]) for b in range(B)],
+        "pool_start": [buf.pool_start[b * cap:(b + 1) * cap].cpu().numpy() for b in range(B)],
+        "pool_valid": [buf.pool_valid[b * cap:(b + 1) * cap].cpu().numpy() for b in range(B)],
+        "q": f(bt.q), "w": f(bt.weights), "q_lat": f(bt.q_lat),
+    }
+
+
+def cpu_baseline(layer, seconds):
+    host = host_layer(layer)
+    B = len(host["k"])
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_query_layer(host, n % B)
+        n += 1
+        if time.perf_counter() - t0 >= seconds or n >= 4 * N_LAYERS:
+            break
+    dt = time.perf_counter() - t0
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", "1"))
+    return {"value": round(n / dt / N_LAYERS, 4), "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": f"{n} decode query-layers of the 262k workload (layer 0, sequences "
+                      f"round-robin) through the numpy float64 oracle in {dt:.1f} s; "
+                      f"queries/s = query-layers/s / {N_LAYERS} layers"}
+
+
+def run_reference(args, dist):
+    """The CPU oracle as the reference arm: bounded samples of the same workload."""
+    if dist.rank != 0:
+        return
+    import torch
+
+    from sparse_attention_indexer_kpool_gb300 import synth
+    # caches are synthesised on the GPU when one is present (fast), else on the CPU
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    geo = synth.GEO_MAIN
+    bt = synth.make_batch(geo, [args.seqlen] * 4, [0] * 4, device=dev, seed=3000)
+    import numpy as np
+
+    import oracle
+    # the oracle builds its own pool cache for the sample (setup, not timed)
+    T = args.seqlen
+    cap = T // geo.kpool
+
+    class _Buf:
+        pass
+    buf = _Buf()
+    f = lambda t: t.detach().to("cpu", torch.float64).numpy()
+    pk, ps, pv = [], [], []
+    for b in range(4):
+        o = oracle.kpool_compress(f(bt.k[b * T:(b + 1) * T]), f(bt.gate[b * T:(b + 1) * T]),
+                                  bt.valid[b * T:(b + 1) * T].cpu().numpy(), f(bt.ape),
+                                  f(bt.ln_gamma), f(bt.ln_beta), geo.ln_eps, [0, T], [0, cap],
+                                  geo.kpool, "bf16")
+        pk.append(o[0]); ps.append(o[1]); pv.append(o[2])
+    buf.pool_keys = torch.tensor(np.concatenate(pk), dtype=torch.float64)
+    buf.pool_start = torch.tensor(np.concatenate(ps), dtype=torch.int32)
+    buf.pool_valid = torch.tensor(np.concatenate(pv), dtype=torch.uint8)
+    host = host_layer((bt, buf))
+    for _ in range(args.warmup):
+        oracle_query_layer(host, 0)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        for b in range(4):
+            oracle_query_layer(host, b)
+    dt = time.perf_counter() - t0
+    value = 4 * args.steps / dt / N_LAYERS
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", "1"))
+    sample = (f"each step = one DSA layer's decode for the 4 queries (4 query-layers) through "
+              f"the numpy float64 oracle; queries/s = query-layers/s / {N_LAYERS}")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "long262k", "sequences": 4, "context": args.seqlen,
+                   "layers": N_LAYERS},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
+def main():
+    args = parse()
+    dist = Dist(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist)
+        else:
+            run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -170,7 +170,8 @@ int dsa_index_scores(const void* q, const float* weights, float scale, const voi
  * entries are -1.  The result is unique and bit-reproducible.
  *
  *   scores   [Q, P_ld] fp32;  pool_ids [Q, select_k] int32
- *   workspace: dsa_topk_pools_workspace_size(Q, P_ld, select_k) bytes, 16-byte aligned
+ *   workspace: dsa_topk_pools_workspace_size(Q, P_ld, select_k) bytes (currently 0:
+ *   the histogram and candidate lists live in shared memory); may be NULL when 0
  * Supported: 1 <= select_k <= DSA_SELECT_K_MAX.
  */
 int dsa_topk_pools(const float* scores, int Q, int P_ld, int select_k, int32_t* pool_ids,
@@ -226,6 +227,29 @@ int dsa_mla_selected_decode(const void* q_lat, const void* kv_latent, const int3
                             float* lse, void* workspace, size_t ws_bytes, int32_t* status_dev,
                             void* stream);
 size_t dsa_mla_selected_decode_workspace_size(int Q, int Hm, int L, int out_width, int dtype);
+
+/*
+ * dsa_select - index_scores -> topk_pools -> expand_selection in one call.
+ *
+ * Source: module glm5next_dsa, Modules, select (the production launcher of the
+ * indexer pipeline) and "Shape of the pipeline".  Writes exactly what the three
+ * stage calls above write, in the same buffers (scores [Q, P_ld], pool_ids
+ * [Q, select_k], token_ids [Q, out_width]), with the same arguments and device
+ * faults, but fuses the top-k histogram into the scoring kernel and the
+ * expansion into the top-k kernel.
+ *
+ *   workspace: dsa_select_workspace_size(Q, P_ld, select_k) bytes, 16-byte
+ *   aligned, ZERO-FILLED BEFORE ITS FIRST USE; every call leaves it zeroed, so a
+ *   workspace is zeroed once at allocation and then reused.  Two calls in
+ *   flight at the same time must not share a workspace.
+ */
+int dsa_select(const void* q, const float* weights, float scale, const void* pool_keys,
+               const int32_t* pool_start, const uint8_t* pool_valid, const int32_t* n_pools,
+               const int32_t* cu_pool_cap, const int32_t* q_seq, const int32_t* q_pos, int Q,
+               int B, int H, int D, int kpool, int P_ld, int select_k, int out_width, int dtype,
+               float* scores, int32_t* pool_ids, int32_t* token_ids, void* workspace,
+               size_t ws_bytes, int32_t* status_dev, void* stream);
+size_t dsa_select_workspace_size(int Q, int P_ld, int select_k);
 
 /* Human-readable name of a DSA_* return code (static string). */
 const char* dsa_status_string(int status);

@@ -141,8 +141,6 @@ def kpool_compress(k, gate, valid, ape, gamma, beta, eps, cu_seqlens, cu_pool_ca
     """
     if not (1 <= kpool <= KPOOL_MAX):
         raise ValueError("kpool must be in [1, 8]")  # Constants, KERNEL_MAX_KPOOL
-    k = np.asarray(k, np.float64)
-    gate = np.asarray(gate, np.float64)
     valid = np.asarray(valid)
     ape = np.asarray(ape, np.float64).reshape(kpool, -1)
     B = len(cu_seqlens) - 1
@@ -174,23 +172,27 @@ def kpool_compress(k, gate, valid, ape, gamma, beta, eps, cu_seqlens, cu_pool_ca
         if P_eff > end:
             status |= ST_POOL_UNCOVERED
         n_pools[b] = P_eff
-        for p in range(begin, end):
-            g = cap_lo + p
-            if p >= P_eff:
-                pool_keys[g] = 0.0
-                pool_start[g] = -1
-                pool_valid[g] = 0
-                continue
-            s0 = lo + t0 + p * kpool
-            toks = slice(s0, s0 + kpool)
-            kn = round_store(layernorm(k[toks], gamma, beta, eps), dtype)   # [kpool, D]
-            logit = gate[toks] + ape                                        # [kpool, D]
-            m = logit.max(axis=0, keepdims=True)
-            e = np.exp(logit - m)
-            w = e / e.sum(axis=0, keepdims=True)                            # softmax over slots
-            pool_keys[g] = round_store((w * kn).sum(axis=0), dtype)
-            pool_start[g] = t0 + p * kpool
-            pool_valid[g] = 1 if np.all(valid[toks] != 0) else 0
+        # sentinel entries: pools of the range that are not complete pools
+        first = max(begin, 0)                    # negative pool ids do not exist
+        tail = np.arange(max(first, P_eff), end)
+        pool_keys[cap_lo + tail] = 0.0
+        pool_start[cap_lo + tail] = -1
+        pool_valid[cap_lo + tail] = 0
+        # complete pools of the range, all at once: axis 0 = pool, 1 = slot, 2 = channel
+        pools = np.arange(first, min(end, P_eff))
+        if pools.size == 0:
+            continue
+        tok = lo + t0 + pools[:, None] * kpool + np.arange(kpool)[None, :]   # [n, kpool]
+        kk = np.asarray(k[tok.reshape(-1)], np.float64)
+        kn = round_store(layernorm(kk, gamma, beta, eps), dtype).reshape(len(pools), kpool, -1)
+        logit = np.asarray(gate[tok.reshape(-1)], np.float64).reshape(len(pools), kpool, -1)
+        logit = logit + ape[None, :, :]
+        m = logit.max(axis=1, keepdims=True)
+        e = np.exp(logit - m)
+        w = e / e.sum(axis=1, keepdims=True)                                 # softmax over slots
+        pool_keys[cap_lo + pools] = round_store((w * kn).sum(axis=1), dtype)
+        pool_start[cap_lo + pools] = t0 + pools * kpool
+        pool_valid[cap_lo + pools] = np.all(valid[tok] != 0, axis=1).astype(np.uint8)
     return pool_keys, pool_start, pool_valid, n_pools, status
 
 
@@ -319,7 +321,6 @@ def mla_selected_decode(q_lat, kv, cu_seqlens, q_seq, token_ids, sm_scale: float
     outside [0, T_b) is skipped and flagged.
     """
     q_lat = np.asarray(q_lat, np.float64)
-    kv = np.asarray(kv, np.float64)
     token_ids = np.asarray(token_ids, np.int64)
     Q, Hm, L = q_lat.shape
     out = np.zeros((Q, Hm, L), np.float64)
@@ -339,7 +340,7 @@ def mla_selected_decode(q_lat, kv, cu_seqlens, q_seq, token_ids, sm_scale: float
             sel = sel[sel < T]
         if sel.size == 0:
             continue
-        C = kv[lo + sel]                                  # [n, L]
+        C = np.asarray(kv[lo + sel], np.float64)          # [n, L]
         z = sm_scale * (q_lat[i] @ C.T)                   # [Hm, n]
         m = z.max(axis=1, keepdims=True)
         e = np.exp(z - m)

@@ -29,6 +29,9 @@ SIGNATURES = {
     "dsa_mla_selected_decode": (c_int, [c_void_p] * 5 + [c_int] * 5 + [c_float, c_int]
                                 + [c_void_p] * 3 + [c_size_t] + [c_void_p] * 2),
     "dsa_mla_selected_decode_workspace_size": (c_size_t, [c_int] * 5),
+    "dsa_select": (c_int, [c_void_p, c_void_p, c_float] + [c_void_p] * 7 + [c_int] * 9
+                   + [c_void_p] * 4 + [c_size_t] + [c_void_p] * 2),
+    "dsa_select_workspace_size": (c_size_t, [c_int, c_int, c_int]),
     "dsa_status_string": (ctypes.c_char_p, [c_int]),
     "dsa_version": (c_int, []),
 }

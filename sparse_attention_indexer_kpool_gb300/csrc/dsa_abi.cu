@@ -79,12 +79,12 @@ int dsa_index_scores(const void* q, const float* weights, float scale, const voi
   if (Q > 65535) return DSA_ERR_UNSUPPORTED;
   return dsa::launch_index_scores(q, weights, scale, pool_keys, pool_start, pool_valid, n_pools,
                                   cu_pool_cap, q_seq, q_pos, Q, B, H, D, kpool, P_ld, dtype,
-                                  scores, status_dev, as_stream(stream));
+                                  scores, nullptr, status_dev, as_stream(stream));
 }
 
 size_t dsa_topk_pools_workspace_size(int Q, int P_ld, int select_k) {
   if (Q <= 0 || P_ld <= 0 || select_k <= 0) return 0;
-  return dsa::topk_workspace_size(Q, P_ld, select_k);
+  return dsa::topk_workspace_size(Q, P_ld, select_k);  // 0: the histogram lives on chip
 }
 
 int dsa_topk_pools(const float* scores, int Q, int P_ld, int select_k, int32_t* pool_ids,
@@ -95,9 +95,8 @@ int dsa_topk_pools(const float* scores, int Q, int P_ld, int select_k, int32_t* 
   if (Q > 65535) return DSA_ERR_UNSUPPORTED;
   if (!scores || !pool_ids) return DSA_ERR_INVALID_ARG;
   if (!aligned(scores, 4) || !aligned(pool_ids, 4)) return DSA_ERR_MISALIGNED;
-  if (!workspace || ws_bytes < dsa::topk_workspace_size(Q, P_ld, select_k))
-    return DSA_ERR_WORKSPACE;
-  if (!aligned(workspace, 16)) return DSA_ERR_MISALIGNED;
+  if (ws_bytes < dsa::topk_workspace_size(Q, P_ld, select_k)) return DSA_ERR_WORKSPACE;
+  if (workspace && !aligned(workspace, 16)) return DSA_ERR_MISALIGNED;
   return dsa::launch_topk_pools(scores, Q, P_ld, select_k, pool_ids, workspace, ws_bytes,
                                 as_stream(stream));
 }
@@ -119,6 +118,58 @@ int dsa_expand_selection(const int32_t* pool_ids, const int32_t* pool_start,
   if (Q > 65535) return DSA_ERR_UNSUPPORTED;
   return dsa::launch_expand_selection(pool_ids, pool_start, cu_pool_cap, q_seq, Q, B, select_k,
                                       kpool, out_width, token_ids, status_dev, as_stream(stream));
+}
+
+size_t dsa_select_workspace_size(int Q, int P_ld, int select_k) {
+  if (Q <= 0 || P_ld <= 0 || select_k <= 0) return 0;
+  return dsa::select_workspace_size(Q, P_ld, select_k);
+}
+
+int dsa_select(const void* q, const float* weights, float scale, const void* pool_keys,
+               const int32_t* pool_start, const uint8_t* pool_valid, const int32_t* n_pools,
+               const int32_t* cu_pool_cap, const int32_t* q_seq, const int32_t* q_pos, int Q,
+               int B, int H, int D, int kpool, int P_ld, int select_k, int out_width, int dtype,
+               float* scores, int32_t* pool_ids, int32_t* token_ids, void* workspace,
+               size_t ws_bytes, int32_t* status_dev, void* stream) {
+  if (Q < 0 || B < 0 || H < 1 || P_ld < 1 || select_k < 1 || out_width < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (kpool < 1 || kpool > DSA_KPOOL_MAX) return DSA_ERR_INVALID_ARG;
+  if ((long long)out_width < (long long)select_k * kpool) return DSA_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype) || !(scale > 0.f) || !isfinite(scale)) return DSA_ERR_INVALID_ARG;
+  if (!d_ok(D) || H > 64 || select_k > DSA_SELECT_K_MAX) return DSA_ERR_UNSUPPORTED;
+  if (Q == 0) return DSA_OK;
+  if (B == 0) return DSA_ERR_INVALID_ARG;
+  if (!q || !weights || !pool_keys || !pool_start || !pool_valid || !n_pools || !cu_pool_cap ||
+      !scores || !pool_ids || !token_ids)
+    return DSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(weights, 16) || !aligned(pool_keys, 16) || !aligned(scores, 4) ||
+      !aligned(n_pools, 4) || !aligned(cu_pool_cap, 4) || !aligned(pool_start, 4) ||
+      !aligned(pool_ids, 4) || !aligned(token_ids, 4) || (q_seq && !aligned(q_seq, 4)) ||
+      (q_pos && !aligned(q_pos, 4)) || (status_dev && !aligned(status_dev, 4)))
+    return DSA_ERR_MISALIGNED;
+  if (!workspace || ws_bytes < dsa::select_workspace_size(Q, P_ld, select_k))
+    return DSA_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return DSA_ERR_MISALIGNED;
+  if (Q > 65535) return DSA_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  if (dsa::index_uses_tensor_cores(H, D, dtype)) {
+    int r = dsa::launch_index_scores(q, weights, scale, pool_keys, pool_start, pool_valid,
+                                     n_pools, cu_pool_cap, q_seq, q_pos, Q, B, H, D, kpool, P_ld,
+                                     dtype, scores, dsa::topk_workspace_hist(workspace),
+                                     status_dev, st);
+    if (r != DSA_OK) return r;
+    return dsa::launch_select_after_index(scores, Q, P_ld, select_k, pool_ids, workspace,
+                                          pool_start, cu_pool_cap, q_seq, B, kpool, out_width,
+                                          token_ids, status_dev, st);
+  }
+  int r = dsa::launch_index_scores(q, weights, scale, pool_keys, pool_start, pool_valid, n_pools,
+                                   cu_pool_cap, q_seq, q_pos, Q, B, H, D, kpool, P_ld, dtype,
+                                   scores, nullptr, status_dev, st);
+  if (r != DSA_OK) return r;
+  r = dsa::launch_topk_pools(scores, Q, P_ld, select_k, pool_ids, workspace, ws_bytes, st);
+  if (r != DSA_OK) return r;
+  return dsa::launch_expand_selection(pool_ids, pool_start, cu_pool_cap, q_seq, Q, B, select_k,
+                                      kpool, out_width, token_ids, status_dev, st);
 }
 
 size_t dsa_mla_selected_decode_workspace_size(int Q, int Hm, int L, int out_width, int dtype) {

@@ -175,8 +175,17 @@ int launch_index_scores(const void* q, const float* weights, float scale, const 
                         const int32_t* pool_start, const uint8_t* pool_valid,
                         const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
                         const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
-                        int dtype, float* scores, int32_t* status_dev, cudaStream_t stream);
+                        int dtype, float* scores, uint32_t* score_hist, int32_t* status_dev,
+                        cudaStream_t stream);
 size_t topk_workspace_size(int Q, int P_ld, int select_k);
+size_t select_workspace_size(int Q, int P_ld, int select_k);
+uint32_t* topk_workspace_hist(void* workspace);
+int launch_select_after_index(const float* scores, int Q, int P_ld, int select_k,
+                              int32_t* pool_ids, void* workspace, const int32_t* pool_start,
+                              const int32_t* cu_pool_cap, const int32_t* q_seq, int B, int kpool,
+                              int out_width, int32_t* token_ids, int32_t* status_dev,
+                              cudaStream_t stream);
+bool index_uses_tensor_cores(int H, int D, int dtype);
 int launch_topk_pools(const float* scores, int Q, int P_ld, int select_k, int32_t* pool_ids,
                       void* workspace, size_t ws_bytes, cudaStream_t stream);
 int launch_expand_selection(const int32_t* pool_ids, const int32_t* pool_start,

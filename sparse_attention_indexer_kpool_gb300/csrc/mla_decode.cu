@@ -12,9 +12,13 @@
 // (partial 16 x 32 score tiles summed through shared memory), for the output
 // they own the matching 128 output columns (64 fp32 accumulators per thread).
 // Selected rows are gathered 32 at a time with 16-byte cp.async into a
-// double-buffered, XOR-swizzled shared tile (conflict-free ldmatrix), and the
-// softmax is the usual online (running max / running sum) form in base 2.
-// Splits are merged by a small combine kernel.
+// 4-stage, XOR-swizzled shared ring (conflict-free ldmatrix), and the softmax
+// is the usual online (running max / running sum) form in base 2.  The splits
+// of one (query, head group) form a thread-block cluster: after the row loop
+// each CTA parks its partial output in its own shared memory and every CTA of
+// the cluster merges one latent slice from all members through distributed
+// shared memory, so no partials go to global memory and no second kernel runs.
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "dsa_internal.cuh"
@@ -22,41 +26,58 @@
 namespace dsa {
 namespace {
 
+namespace cg = cooperative_groups;
+
 constexpr int kL = 512;
 constexpr int kHG = 16;            // heads per CTA
 constexpr int kNT = 32;            // rows per tile
+constexpr int kRing = 4;           // gather stages
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kChunks = kL / 8;    // 16-byte chunks per latent row
 constexpr int kPStride = 40;       // bf16 per sP row (32 + 8 pad)
+constexpr int kMaxSplit = 8;       // portable cluster size
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct MlaSmem {
-  __nv_bfloat16 q[kHG * kL];            // swizzled
-  __nv_bfloat16 kv[2][kNT * kL];        // swizzled, double buffered
+  union {
+    __nv_bfloat16 kv[kRing][kNT * kL];   // swizzled gather ring
+    float part[kHG][kL];                 // this CTA's partial output (after the loop)
+  };
+  __nv_bfloat16 q[kHG * kL];             // swizzled
   float s_part[kWarps][kHG][kNT];
   __nv_bfloat16 p[kHG * kPStride];
   float m[kHG], l[kHG], alpha[kHG];
-  int row_ok[2][kNT];
+  // followed by int s_tok[rows_per_split]: this split's token ids (-1 = skip)
 };
 
 __device__ __forceinline__ int swz(int row, int chunk) {  // element offset of a 16B chunk
   return row * kL + ((chunk ^ (row & 7)) << 3);
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
     mla_mma_kernel(const __nv_bfloat16* __restrict__ q_lat, const __nv_bfloat16* __restrict__ kv,
                    const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ q_seq,
                    const int32_t* __restrict__ token_ids, int B, int Hm, int W, int rows_per_split,
                    float sm_scale, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
-                   float* __restrict__ part_o, float* __restrict__ part_ml,
                    int32_t* status) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   MlaSmem& sm = *reinterpret_cast<MlaSmem*>(smem_raw);
-  pdl_wait();
   const int qi = blockIdx.z, hg = blockIdx.y, split = blockIdx.x, n_split = gridDim.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
+
+  // q_lat does not depend on the previous kernel: stage it before the grid wait
+  const __nv_bfloat16* qsrc = q_lat + ((long long)qi * Hm + hg * kHG) * kL;
+  for (int c = threadIdx.x; c < kHG * kChunks; c += kThreads) {
+    const int r = c / kChunks, ch = c % kChunks;
+    cp_async16(smem_u32(&sm.q[swz(r, ch)]), qsrc + (long long)r * kL + ch * 8, true);
+  }
+  if (threadIdx.x < kHG) {
+    sm.m[threadIdx.x] = -INFINITY;
+    sm.l[threadIdx.x] = 0.f;
+  }
+  pdl_wait();  // token ids come from the selection kernel
   const int b = q_seq ? q_seq[qi] : 0;
   const bool seq_ok = b >= 0 && b < B;
   if (!seq_ok && split == 0 && hg == 0 && threadIdx.x == 0) flag(status, DSA_DEV_BAD_QSEQ);
@@ -66,42 +87,39 @@ __global__ void __launch_bounds__(kThreads)
   const int j_hi = min(W, j_lo + rows_per_split);
   const int n_tiles = (j_hi - j_lo + kNT - 1) / kNT;
   const int32_t* toks = token_ids + (long long)qi * W;
-
-  // Stage the 16 x 512 query block (swizzled).
-  const __nv_bfloat16* qsrc = q_lat + ((long long)qi * Hm + hg * kHG) * kL;
-  for (int c = threadIdx.x; c < kHG * kChunks; c += kThreads) {
-    const int r = c / kChunks, ch = c % kChunks;
-    cp_async16(smem_u32(&sm.q[swz(r, ch)]), qsrc + (long long)r * kL + ch * 8, true);
-  }
-  auto load_tile = [&](int tile, int buf) {
-    const int j0 = j_lo + tile * kNT;
-    // row validity (one thread per row)
-    if (threadIdx.x < kNT) {
-      const int j = j0 + threadIdx.x;
-      int ok = 0;
-      if (j < j_hi && seq_ok) {
-        const int tok = toks[j];
-        if (tok >= Tb) flag(status, DSA_DEV_BAD_TOKEN);
-        ok = tok >= 0 && tok < Tb;
+  int* s_tok = reinterpret_cast<int*>(smem_raw + sizeof(MlaSmem));
+  // one coalesced pass: token ids of this split, validated (-1 = not a row)
+  for (int j = j_lo + threadIdx.x; j < j_lo + n_tiles * kNT; j += kThreads) {
+    int tok = -1;
+    if (j < j_hi && seq_ok) {
+      tok = toks[j];
+      if (tok >= Tb) {
+        if (hg == 0) flag(status, DSA_DEV_BAD_TOKEN);
+        tok = -1;
       }
-      sm.row_ok[buf][threadIdx.x] = ok;
+      if (tok < 0) tok = -1;
     }
+    s_tok[j - j_lo] = tok;
+  }
+  __syncthreads();
+
+  auto load_tile = [&](int tile) {
+    const int buf = tile % kRing;
+    const int* tt = s_tok + tile * kNT;
     for (int c = threadIdx.x; c < kNT * kChunks; c += kThreads) {
       const int r = c / kChunks, ch = c % kChunks;
-      const int j = j0 + r;
-      int tok = -1;
-      if (j < j_hi && seq_ok) tok = toks[j];
-      const bool ok = tok >= 0 && tok < Tb;
+      const int tok = tt[r];
+      const bool ok = tok >= 0;
       const __nv_bfloat16* src = kv + (row_base + (ok ? tok : 0)) * kL + ch * 8;
       cp_async16(smem_u32(&sm.kv[buf][swz(r, ch)]), ok ? src : kv, ok);
     }
   };
-  if (threadIdx.x < kHG) {
-    sm.m[threadIdx.x] = -INFINITY;
-    sm.l[threadIdx.x] = 0.f;
+  // prologue: the query block plus the first kRing-1 tiles in flight
+#pragma unroll
+  for (int i = 0; i < kRing - 1; ++i) {
+    if (i < n_tiles) load_tile(i);
+    cp_async_commit();
   }
-  if (n_tiles > 0) load_tile(0, 0);
-  cp_async_commit();
 
   float o[16][4];
 #pragma unroll
@@ -110,10 +128,10 @@ __global__ void __launch_bounds__(kThreads)
   const float zscale = sm_scale * kLog2e;
 
   for (int tile = 0; tile < n_tiles; ++tile) {
-    const int buf = tile & 1;
-    if (tile + 1 < n_tiles) load_tile(tile + 1, buf ^ 1);
+    const int buf = tile % kRing;
+    if (tile + kRing - 1 < n_tiles) load_tile(tile + kRing - 1);
     cp_async_commit();
-    cp_async_wait<1>();
+    cp_async_wait<kRing - 1>();
     __syncthreads();
     if (tile == 0) {
 #pragma unroll
@@ -151,15 +169,15 @@ __global__ void __launch_bounds__(kThreads)
     // ---- online softmax: thread -> head h = tid/8, columns 4*(tid%8) .. +3
     {
       const int h = threadIdx.x >> 3, c0 = (threadIdx.x & 7) * 4;
-      float s[4];
+      float sv[4];
       float mx = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int c = c0 + i;
         float v = sm.s_part[0][h][c] + sm.s_part[1][h][c] + sm.s_part[2][h][c] +
                   sm.s_part[3][h][c];
-        v = sm.row_ok[buf][c] ? v * zscale : -INFINITY;
-        s[i] = v;
+        v = s_tok[tile * kNT + c] >= 0 ? v * zscale : -INFINITY;
+        sv[i] = v;
         mx = fmaxf(mx, v);
       }
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -170,17 +188,17 @@ __global__ void __launch_bounds__(kThreads)
       const bool none = m_new == -INFINITY;
       const float alpha = none ? 1.f : exp2f(m_old - m_new);
       float ps = 0.f;
-      float p[4];
+      float pv[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        p[i] = none ? 0.f : exp2f(s[i] - m_new);
-        ps += p[i];
+        pv[i] = none ? 0.f : exp2f(sv[i] - m_new);
+        ps += pv[i];
       }
       ps += __shfl_xor_sync(0xffffffffu, ps, 1);
       ps += __shfl_xor_sync(0xffffffffu, ps, 2);
       ps += __shfl_xor_sync(0xffffffffu, ps, 4);
       __nv_bfloat16* pr = &sm.p[h * kPStride + c0];
-      *reinterpret_cast<uint2*>(pr) = make_uint2(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]));
+      *reinterpret_cast<uint2*>(pr) = make_uint2(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]));
       __syncwarp();
       if ((threadIdx.x & 7) == 0) {
         sm.m[h] = m_new;
@@ -210,16 +228,16 @@ __global__ void __launch_bounds__(kThreads)
         mma_bf16_16816(o[nt + 1], a0, a1, a2, a3, b2, b3);
       }
     }
-    __syncthreads();  // kv[buf], row_ok[buf], p and s_part are rewritten next tile
+    __syncthreads();  // this ring slot, p and s_part are rewritten next tile
   }
   cp_async_wait<0>();
   __syncthreads();
+  pdl_launch_dependents();
 
-  // ---- epilogue
-  const float m_lo = sm.m[g], m_hi = sm.m[g + 8];
-  const float l_lo = sm.l[g], l_hi = sm.l[g + 8];
   const int h_lo = hg * kHG + g, h_hi = h_lo + 8;
   if (n_split == 1) {
+    const float m_lo = sm.m[g], m_hi = sm.m[g + 8];
+    const float l_lo = sm.l[g], l_hi = sm.l[g + 8];
     const float inv_lo = l_lo > 0.f ? 1.f / l_lo : 0.f;
     const float inv_hi = l_hi > 0.f ? 1.f / l_hi : 0.f;
     __nv_bfloat16* o_lo = out + ((long long)qi * Hm + h_lo) * kL + warp * 128;
@@ -235,48 +253,41 @@ __global__ void __launch_bounds__(kThreads)
       lse[(long long)qi * Hm + h_lo] = l_lo > 0.f ? (m_lo + log2f(l_lo)) / kLog2e : -INFINITY;
       lse[(long long)qi * Hm + h_hi] = l_hi > 0.f ? (m_hi + log2f(l_hi)) / kLog2e : -INFINITY;
     }
-  } else {
-    // partials: O unnormalised (fp32), m (base 2) and l
-    const long long slot_lo = ((long long)qi * Hm + h_lo) * n_split + split;
-    const long long slot_hi = ((long long)qi * Hm + h_hi) * n_split + split;
-    float* p_lo = part_o + slot_lo * kL + warp * 128;
-    float* p_hi = part_o + slot_hi * kL + warp * 128;
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      *reinterpret_cast<float2*>(p_lo + nt * 8 + 2 * t) = make_float2(o[nt][0], o[nt][1]);
-      *reinterpret_cast<float2*>(p_hi + nt * 8 + 2 * t) = make_float2(o[nt][2], o[nt][3]);
-    }
-    if (warp == 0 && t == 0) {
-      part_ml[slot_lo * 2] = m_lo;
-      part_ml[slot_lo * 2 + 1] = l_lo;
-      part_ml[slot_hi * 2] = m_hi;
-      part_ml[slot_hi * 2 + 1] = l_hi;
-    }
+    return;
   }
-  pdl_launch_dependents();
-}
 
-// Merge split partials: one CTA per (query, head), threads over the latent axis.
-template <typename T>
-__global__ void mla_combine_kernel(const float* __restrict__ part_o,
-                                   const float* __restrict__ part_ml, int Hm, int L, int n_split,
-                                   T* __restrict__ out, float* __restrict__ lse) {
-  pdl_wait();
-  const long long qh = (long long)blockIdx.y * Hm + blockIdx.x;
-  const float* ml = part_ml + qh * n_split * 2;
-  float m = -INFINITY;
-  for (int s = 0; s < n_split; ++s) m = fmaxf(m, ml[2 * s]);
-  float den = 0.f;
-  for (int s = 0; s < n_split; ++s)
-    if (ml[2 * s + 1] > 0.f) den += ml[2 * s + 1] * exp2f(ml[2 * s] - m);
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  for (int d = threadIdx.x; d < L; d += blockDim.x) {
-    float acc = 0.f;
-    for (int s = 0; s < n_split; ++s)
-      if (ml[2 * s + 1] > 0.f) acc += part_o[(qh * n_split + s) * L + d] * exp2f(ml[2 * s] - m);
-    out[qh * L + d] = Act<T>::from_f(acc * inv);
+  // ---- split merge inside the cluster (distributed shared memory)
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt) {
+    *reinterpret_cast<float2*>(&sm.part[g][warp * 128 + nt * 8 + 2 * t]) =
+        make_float2(o[nt][0], o[nt][1]);
+    *reinterpret_cast<float2*>(&sm.part[g + 8][warp * 128 + nt * 8 + 2 * t]) =
+        make_float2(o[nt][2], o[nt][3]);
   }
-  if (lse && threadIdx.x == 0) lse[qh] = den > 0.f ? (m + log2f(den)) / kLog2e : -INFINITY;
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();  // every member's partial, m and l are visible cluster-wide
+  const int rank = (int)cluster.block_rank();
+  const int c_lo = rank * kL / n_split;     // latent slice [c_lo, c_hi) merged by this CTA
+  const int cols = (rank + 1) * kL / n_split - c_lo;
+  for (int e = threadIdx.x; e < kHG * cols; e += kThreads) {
+    const int h = e / cols, c = c_lo + e % cols;
+    float M = -INFINITY;
+    for (int r = 0; r < n_split; ++r) M = fmaxf(M, cluster.map_shared_rank(sm.m, r)[h]);
+    float den = 0.f, acc = 0.f;
+    for (int r = 0; r < n_split; ++r) {
+      const float lr = cluster.map_shared_rank(sm.l, r)[h];
+      if (lr > 0.f) {
+        const float wgt = exp2f(cluster.map_shared_rank(sm.m, r)[h] - M);
+        den += lr * wgt;
+        acc += cluster.map_shared_rank(&sm.part[0][0], r)[h * kL + c] * wgt;
+      }
+    }
+    out[((long long)qi * Hm + hg * kHG + h) * kL + c] =
+        __float2bfloat16_rn(den > 0.f ? acc / den : 0.f);
+    if (lse && rank == 0 && e % cols == 0)
+      lse[(long long)qi * Hm + hg * kHG + h] = den > 0.f ? (M + log2f(den)) / kLog2e : -INFINITY;
+  }
+  cluster.sync();  // keep this CTA's shared memory alive until every member has read it
 }
 
 // Generic SIMT kernel: one CTA per (head, query); two passes over the rows.
@@ -359,29 +370,27 @@ __global__ void __launch_bounds__(256)
 
 bool fast_path(int Hm, int L, int dtype) { return dtype == DSA_BF16 && L == kL && Hm % kHG == 0; }
 
+// Split count: enough (query, head group, split) CTAs to cover the SMs once,
+// at most one portable cluster (8) per (query, head group).
 void split_plan(int Q, int Hm, int W, int* n_split, int* rows_per_split) {
   const int n_hg = Hm / kHG;
-  const int target = 2 * kNumSMs;
-  int s = (target + Q * n_hg - 1) / (Q * n_hg);
+  int s = (kNumSMs + Q * n_hg - 1) / (Q * n_hg);
   const int max_s = (W + kNT - 1) / kNT;
   if (s > max_s) s = max_s;
+  if (s > kMaxSplit) s = kMaxSplit;
   if (s < 1) s = 1;
   int rows = (W + s - 1) / s;
   rows = (rows + kNT - 1) / kNT * kNT;
   *rows_per_split = rows;
-  *n_split = (W + rows - 1) / rows;
-  if (*n_split < 1) *n_split = 1;
+  // the cluster size equals the split count; every split gets rows < W
+  *n_split = s;
 }
 
 }  // namespace
 
 size_t mla_workspace_size(int Q, int Hm, int L, int out_width, int dtype) {
-  if (!fast_path(Hm, L, dtype)) return 0;
-  int n_split, rows;
-  split_plan(Q, Hm, out_width, &n_split, &rows);
-  if (n_split == 1) return 0;
-  const size_t slots = (size_t)Q * Hm * n_split;
-  return slots * L * 4 + slots * 2 * 4;
+  (void)Q; (void)Hm; (void)L; (void)out_width; (void)dtype;
+  return 0;  // split partials are merged in distributed shared memory
 }
 
 int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
@@ -389,39 +398,33 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
                                int Hm, int L, int out_width, float sm_scale, int dtype, void* out,
                                float* lse, void* workspace, size_t ws_bytes, int32_t* status_dev,
                                cudaStream_t stream) {
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr.val.programmaticStreamSerializationAllowed = 1;
+  (void)workspace; (void)ws_bytes;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.stream = stream;
-  cfg.attrs = &attr;
+  cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (fast_path(Hm, L, dtype)) {
     int n_split, rows;
     split_plan(Q, Hm, out_width, &n_split, &rows);
-    if (n_split > 1 && ws_bytes < mla_workspace_size(Q, Hm, L, out_width, dtype))
-      return DSA_ERR_WORKSPACE;
-    float* part_o = static_cast<float*>(workspace);
-    float* part_ml = part_o ? part_o + (size_t)Q * Hm * n_split * L : nullptr;
-    const size_t smem = sizeof(MlaSmem);
+    const size_t smem = sizeof(MlaSmem) + (size_t)(rows + kNT) * 4;
+    if (smem > 227 * 1024) return DSA_ERR_UNSUPPORTED;
     cudaFuncSetAttribute(mla_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = n_split;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
     cfg.gridDim = dim3(n_split, Hm / kHG, Q);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     if (cudaLaunchKernelEx(&cfg, mla_mma_kernel, (const __nv_bfloat16*)q_lat,
                            (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, Hm,
-                           out_width, rows, sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml,
+                           out_width, rows, sm_scale, (__nv_bfloat16*)out, lse,
                            status_dev) != cudaSuccess)
       return DSA_ERR_CUDA;
-    if (n_split > 1) {
-      cfg.gridDim = dim3(Hm, Q, 1);
-      cfg.blockDim = dim3(128, 1, 1);
-      cfg.dynamicSmemBytes = 0;
-      if (cudaLaunchKernelEx(&cfg, mla_combine_kernel<__nv_bfloat16>, (const float*)part_o,
-                             (const float*)part_ml, Hm, L, n_split, (__nv_bfloat16*)out,
-                             lse) != cudaSuccess)
-        return DSA_ERR_CUDA;
-    }
     return DSA_OK;
   }
   if (L % 8 != 0 || L > 1024 || Hm > 128 || out_width > 16384) return DSA_ERR_UNSUPPORTED;

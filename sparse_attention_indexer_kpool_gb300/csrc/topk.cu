@@ -10,15 +10,16 @@
 // ~pool), so "score descending, pool ascending" is plain key-descending order
 // and the selected set and its order are unique.
 //
-// Top-k is a radix select spread over C CTAs per query row:
-//   1. histogram of the top 12 key bits over the row (C CTAs, one global
-//      histogram per query);
-//   2. each CTA finds the threshold bin (the bin where the count from the top
-//      reaches select_k), appends keys above it to a "sure" list and keys in it
-//      to a "tie" list; the last CTA to finish the row (atomic ticket, no
-//      waiting) picks the exact remaining keys from the tie list by rank or by
-//      a radix select on the remaining 52 key bits, sorts the select_k keys and
-//      writes the row.
+// One CTA per query row, everything on chip:
+//   1. a 4096-bin histogram of the top 12 key bits (built by the scoring kernel
+//      on the fused path, else by a first pass over the row here);
+//   2. the threshold bin, where the count from the top reaches select_k;
+//   3. one pass over the row: keys above the bin go to a "sure" list, keys in
+//      it to a "tie" list (shared memory);
+//   4. exact finish: both lists sorted by a register bitonic network (the sure
+//      keys all precede the tie keys), or, for big lists, a radix select of the
+//      missing keys and a shared-memory sort;
+//   5. pool ids written, and optionally expanded to token ids in place.
 #include "dsa_internal.cuh"
 
 namespace dsa {
@@ -26,35 +27,21 @@ namespace {
 
 constexpr int kBins = 4096;           // top 12 bits of the 32-bit score key
 constexpr int kBinShift = 20;
-constexpr int kTieCap = 4096;         // tie-list capacity per query (overflow: slow exact path)
-constexpr int kThreads = 512;
-constexpr int kSmallSort = 1024;      // rank sort up to this many keys, bitonic above
+constexpr int kTieCap = 4096;         // on-chip tie-list capacity (overflow: exact slow path)
+constexpr int kThreads = 1024;
+constexpr int kFast = 512;            // register bitonic width (keys per half block)
+constexpr int kSmallSort = 1024;      // general path: rank sort up to this many keys
 
-struct TopkWs {
-  uint32_t* hist;     // [Q][kBins]
-  uint32_t* ctr;      // [Q][4]: n_sure, n_tie, done, spare
-  uint64_t* sure;     // [Q][K]
-  uint64_t* tie;      // [Q][kTieCap]
+struct ExpandArgs {   // optional fused expand_selection (token_ids == nullptr: off)
+  const int32_t* pool_start;
+  const int32_t* cu_pool_cap;
+  const int32_t* q_seq;
+  int B, kpool, W;
+  int32_t* token_ids;
+  int32_t* status;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
-__host__ __device__ inline size_t ws_header_bytes(int Q) {
-  return align256((size_t)Q * kBins * 4) + align256((size_t)Q * 16);
-}
-
-__host__ __device__ inline TopkWs carve(void* ws, int Q, int K) {
-  char* p = static_cast<char*>(ws);
-  TopkWs w;
-  w.hist = reinterpret_cast<uint32_t*>(p);
-  p += align256((size_t)Q * kBins * 4);
-  w.ctr = reinterpret_cast<uint32_t*>(p);
-  p += align256((size_t)Q * 16);
-  w.sure = reinterpret_cast<uint64_t*>(p);
-  p += align256((size_t)Q * K * 8);
-  w.tie = reinterpret_cast<uint64_t*>(p);
-  return w;
-}
 
 __device__ __forceinline__ uint64_t full_key(float s, int p) {
   return ((uint64_t)score_key(s) << 32) | (uint64_t)(0xffffffffu - (uint32_t)p);
@@ -63,67 +50,52 @@ __device__ __forceinline__ int key_pool(uint64_t key) {
   return (int)(0xffffffffu - (uint32_t)(key & 0xffffffffu));
 }
 
-__global__ void __launch_bounds__(kThreads)
-    topk_hist_kernel(const float* __restrict__ scores, int P_ld, int chunks, TopkWs ws) {
-  __shared__ uint32_t h[kBins];
-  pdl_wait();
-  for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = 0;
-  __syncthreads();
-  const int q = blockIdx.y;
-  const long long lo = (long long)P_ld * blockIdx.x / chunks;
-  const long long hi = (long long)P_ld * (blockIdx.x + 1) / chunks;
-  const float* row = scores + (long long)q * P_ld;
-  for (long long i = lo + threadIdx.x; i < hi; i += kThreads) {
-    const float s = row[i];
-    if (is_candidate(s)) atomicAdd(&h[score_key(s) >> kBinShift], 1u);
-  }
-  __syncthreads();
-  uint32_t* gh = ws.hist + (size_t)q * kBins;
-  for (int i = threadIdx.x; i < kBins; i += kThreads)
-    if (h[i]) atomicAdd(&gh[i], h[i]);
-}
-
-// Block-wide: threshold bin for select_k over hist (smem).  Sets *thr (-1 when
-// every candidate fits) and *above (count strictly above the bin).
-__device__ void find_threshold(const uint32_t* h, int K, int* s_thr, uint32_t* s_above,
-                               uint32_t* s_scan) {
-  constexpr int kPer = kBins / kThreads;  // 8 bins per thread
-  const int tid = threadIdx.x;
+// Block-wide (kThreads): threshold bin for K over hist h (smem).  *thr = -1
+// when every candidate fits.
+__device__ void find_threshold(const uint32_t* h, int K, int* s_thr, uint32_t* s_wtot) {
+  constexpr int kPer = kBins / kThreads;  // 4 bins per thread
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t local = 0;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) local += h[tid * kPer + i];
-  s_scan[tid] = local;
-  __syncthreads();
-  // suffix sums over threads (Hillis-Steele on kThreads entries)
-  for (int o = 1; o < kThreads; o <<= 1) {
-    uint32_t v = s_scan[tid] + ((tid + o < kThreads) ? s_scan[tid + o] : 0u);
-    __syncthreads();
-    s_scan[tid] = v;
-    __syncthreads();
+  uint32_t x = local;  // inclusive suffix sum inside the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_down_sync(0xffffffffu, x, o);
+    if (lane + o < 32) x += y;
   }
-  const uint32_t total = s_scan[0];
-  if (tid == 0) { *s_thr = -1; *s_above = total; }
+  if (lane == 0) s_wtot[warp] = x;
+  if (tid == 0) *s_thr = -1;
   __syncthreads();
-  if (total > (uint32_t)K) {
-    const uint32_t incl = s_scan[tid];                     // bins >= tid*kPer
-    const uint32_t excl = incl - local;                    // bins > tid*kPer+kPer-1
-    if (excl < (uint32_t)K && incl >= (uint32_t)K) {
-      uint32_t run = excl;
-      for (int i = kPer - 1; i >= 0; --i) {
-        const uint32_t c = h[tid * kPer + i];
-        if (run + c >= (uint32_t)K) {
-          *s_thr = tid * kPer + i;
-          *s_above = run;
-          break;
-        }
-        run += c;
+  if (warp == 0) {  // exclusive suffix over warps
+    const uint32_t v = s_wtot[lane];
+    uint32_t z = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_down_sync(0xffffffffu, z, o);
+      if (lane + o < 32) z += y;
+    }
+    s_wtot[32 + lane] = z - v;
+  }
+  __syncthreads();
+  const uint32_t incl = x + s_wtot[32 + warp];   // candidates in bins >= tid*kPer
+  const uint32_t excl = incl - local;            // candidates in bins > tid*kPer + kPer-1
+  const uint32_t total = s_wtot[32] + s_wtot[0];
+  if (total > (uint32_t)K && excl < (uint32_t)K && incl >= (uint32_t)K) {
+    uint32_t run = excl;
+    for (int i = kPer - 1; i >= 0; --i) {
+      const uint32_t c = h[tid * kPer + i];
+      if (run + c >= (uint32_t)K) {
+        *s_thr = tid * kPer + i;
+        break;
       }
+      run += c;
     }
   }
   __syncthreads();
 }
 
-// Warp-aggregated append of `key` (when `take`) into list[ctr++], capped.
+// Warp-aggregated append of `key` (when `take`) into an on-chip list, capped.
 __device__ __forceinline__ void append(bool take, uint64_t key, uint32_t* ctr, uint64_t* list,
                                        uint32_t cap) {
   const unsigned mask = __ballot_sync(0xffffffffu, take);
@@ -173,7 +145,7 @@ __device__ uint64_t radix_kth(int n, uint32_t R, Get get, uint32_t* sh, uint64_t
   return prefix;
 }
 
-// Sort n (<= cap) keys in smem descending; keys[n..cap) are scratch.
+// Sort n keys in smem descending (general path); tmp has room for n keys.
 __device__ void sort_desc(uint64_t* keys, int n, uint64_t* tmp) {
   if (n <= kSmallSort) {
     for (int i = threadIdx.x; i < n; i += kThreads) {
@@ -206,86 +178,148 @@ __device__ void sort_desc(uint64_t* keys, int n, uint64_t* tmp) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads)
-    topk_select_kernel(const float* __restrict__ scores, int P_ld, int K, int chunks, TopkWs ws,
-                       int32_t* __restrict__ pool_ids) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  uint32_t* h = reinterpret_cast<uint32_t*>(smem);                 // kBins
-  uint32_t* s_scan = h + kBins;                                    // kThreads
-  // final-phase buffers reuse the same dynamic smem after the filter pass
+// Two independent 512-key descending bitonic sorts, one per half of the block,
+// one key per thread: xor-shuffles for partner distances < 32, shared memory
+// (xch, 1024 keys) above.
+__device__ uint64_t bitonic512_desc(uint64_t key, uint64_t* xch) {
+  const int pos = threadIdx.x & (kFast - 1);
+#pragma unroll 1
+  for (int k = 2; k <= kFast; k <<= 1) {
+#pragma unroll 1
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      uint64_t other;
+      if (j >= 32) {
+        xch[threadIdx.x] = key;
+        __syncthreads();
+        other = xch[threadIdx.x ^ j];
+        __syncthreads();
+      } else {
+        const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)key, j);
+        const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(key >> 32), j);
+        other = ((uint64_t)hi << 32) | lo;
+      }
+      const bool lower = (pos & j) == 0;
+      const bool desc_block = (pos & k) == 0;
+      const bool keep_max = lower == desc_block;
+      key = keep_max ? (key > other ? key : other) : (key < other ? key : other);
+    }
+  }
+  return key;
+}
+
+// Shared-memory layout of the select kernel (dynamic):
+//   h[kBins] u32 | s_ids[K] i32 | sure[K] u64 | tie[kTieCap] u64 | scratch[2*max(K,kTieCap,1024)] u64
+struct SelLayout {
+  size_t ids, sure, tie, scratch, total;
+  __host__ __device__ SelLayout(int K) {
+    const size_t kmax = (size_t)(K > kTieCap ? K : kTieCap);
+    ids = align256((size_t)kBins * 4);
+    sure = ids + align256((size_t)K * 4);
+    tie = sure + align256((size_t)K * 8);
+    scratch = tie + align256((size_t)kTieCap * 8);
+    total = scratch + 2 * kmax * 8;
+  }
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    topk_select_kernel(const float* __restrict__ scores, int P_ld, int K,
+                       uint32_t* __restrict__ hist_in, int32_t* __restrict__ pool_ids,
+                       ExpandArgs ex) {
+  extern __shared__ __align__(256) unsigned char smem[];
+  const SelLayout lay(K);
+  uint32_t* h = reinterpret_cast<uint32_t*>(smem);
+  int32_t* s_ids = reinterpret_cast<int32_t*>(smem + lay.ids);
+  uint64_t* sure = reinterpret_cast<uint64_t*>(smem + lay.sure);
+  uint64_t* tie = reinterpret_cast<uint64_t*>(smem + lay.tie);
+  uint64_t* scratch = reinterpret_cast<uint64_t*>(smem + lay.scratch);
   __shared__ int s_thr;
-  __shared__ uint32_t s_above, s_last, s_r, s_nsel;
+  __shared__ uint32_t s_nsure, s_ntie, s_r, s_nsel;
+  __shared__ uint32_t s_wtot[64];
   __shared__ uint64_t s_res;
-  pdl_wait();
-  const int q = blockIdx.y;
-  const uint32_t* gh = ws.hist + (size_t)q * kBins;
-  for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = __ldcg(gh + i);
-  __syncthreads();
-  find_threshold(h, K, &s_thr, &s_above, s_scan);
-  const int thr = s_thr;
-  uint32_t* ctr = ws.ctr + (size_t)q * 4;
-  uint64_t* sure = ws.sure + (size_t)q * K;
-  uint64_t* tie = ws.tie + (size_t)q * kTieCap;
+  const int q = blockIdx.x;
   const float* row = scores + (long long)q * P_ld;
-  const long long lo = (long long)P_ld * blockIdx.x / chunks;
-  const long long hi = (long long)P_ld * (blockIdx.x + 1) / chunks;
-  for (long long base = lo; base < hi; base += kThreads) {
-    const long long i = base + threadIdx.x;
+  if (threadIdx.x == 0) { s_nsure = 0; s_ntie = 0; }
+  pdl_wait();
+
+  // ---- 1. histogram of the top 12 key bits
+  uint32_t* gh = hist_in ? hist_in + (size_t)q * kBins : nullptr;
+  if (gh) {
+    for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = __ldcg(gh + i);
+  } else {
+    for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < P_ld; i += kThreads) {
+      const float sc = row[i];
+      if (is_candidate(sc)) atomicAdd(&h[score_key(sc) >> kBinShift], 1u);
+    }
+  }
+  __syncthreads();
+  // ---- 2. threshold bin
+  find_threshold(h, K, &s_thr, s_wtot);
+  const int thr = s_thr;
+  // ---- 3. one pass: sure and tie lists
+  for (int base = 0; base < P_ld; base += kThreads) {
+    const int i = base + threadIdx.x;
     bool in_sure = false, in_tie = false;
     uint64_t key = 0;
-    if (i < hi) {
-      const float s = row[i];
-      if (is_candidate(s)) {
-        key = full_key(s, (int)i);
+    if (i < P_ld) {
+      const float sc = row[i];
+      if (is_candidate(sc)) {
+        key = full_key(sc, i);
         const int bin = (int)(key >> (32 + kBinShift));
         in_sure = bin > thr;
         in_tie = bin == thr;
       }
     }
-    append(in_sure, key, &ctr[0], sure, (uint32_t)K);
-    append(in_tie, key, &ctr[1], tie, (uint32_t)kTieCap);
+    append(in_sure, key, &s_nsure, sure, (uint32_t)K);
+    append(in_tie, key, &s_ntie, tie, (uint32_t)kTieCap);
   }
-  __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(&ctr[2], 1u) == (uint32_t)(chunks - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  // ---- final phase: this CTA owns the row now.
-  uint64_t* sel = reinterpret_cast<uint64_t*>(smem);              // up to 2*max(K, kTieCap) keys
-  uint64_t* tmp = sel + (K > kTieCap ? K : kTieCap);
-  const uint32_t n_sure = __ldcg(&ctr[0]);
-  const uint32_t n_tie = __ldcg(&ctr[1]);
+  const uint32_t n_sure = s_nsure, n_tie = s_ntie;
   uint32_t n_sel;
-  if (thr < 0) {
-    n_sel = n_sure;  // every candidate is in the sure list (<= K of them)
-    for (uint32_t i = threadIdx.x; i < n_sel; i += kThreads) sel[i] = __ldcg(sure + i);
+  // ---- 4. exact finish
+  const bool fast = K <= kFast && n_sure <= (uint32_t)kFast &&
+                    (thr < 0 || n_tie <= (uint32_t)kFast);
+  if (fast) {
+    // threads [0,512) sort the sure keys, [512,1024) the tie keys, concurrently
+    uint64_t* xch = scratch;                 // 1024 keys
+    uint64_t* srt = scratch + kThreads;      // 1024 keys
+    const int pos = threadIdx.x & (kFast - 1);
+    const bool tie_half = threadIdx.x >= kFast;
+    uint64_t key = 0;
+    if (!tie_half && pos < (int)n_sure) key = sure[pos];
+    if (tie_half && thr >= 0 && pos < (int)n_tie) key = tie[pos];
+    key = bitonic512_desc(key, xch);
+    srt[threadIdx.x] = key;
+    __syncthreads();
+    n_sel = thr < 0 ? n_sure : (uint32_t)K;
+    for (int j = threadIdx.x; j < K; j += kThreads) {
+      uint64_t k2 = 0;
+      if ((uint32_t)j < n_sure) k2 = srt[j];
+      else if ((uint32_t)j < n_sel) k2 = srt[kFast + (j - (int)n_sure)];
+      s_ids[j] = (uint32_t)j < n_sel ? key_pool(k2) : -1;
+    }
     __syncthreads();
   } else {
-    const uint32_t R = (uint32_t)K - n_sure;                      // keys still needed, >= 1
-    n_sel = (uint32_t)K;
-    for (uint32_t i = threadIdx.x; i < n_sure; i += kThreads) sel[i] = __ldcg(sure + i);
-    if (threadIdx.x == 0) s_nsel = n_sure;
-    __syncthreads();
-    if (n_tie <= (uint32_t)kSmallSort) {
-      for (uint32_t i = threadIdx.x; i < n_tie; i += kThreads) tmp[i] = __ldcg(tie + i);
-      __syncthreads();
-      for (uint32_t i = threadIdx.x; i < n_tie; i += kThreads) {
-        const uint64_t k = tmp[i];
-        uint32_t rank = 0;
-        for (uint32_t j = 0; j < n_tie; ++j) rank += tmp[j] > k;
-        if (rank < R) sel[n_sure + rank] = k;
-      }
+    const int kmax = K > kTieCap ? K : kTieCap;
+    uint64_t* sel = scratch;
+    uint64_t* tmp = scratch + kmax;
+    if (thr < 0) {
+      n_sel = n_sure;  // every candidate is in the sure list (<= K of them)
+      for (uint32_t i = threadIdx.x; i < n_sel; i += kThreads) sel[i] = sure[i];
       __syncthreads();
     } else {
-      uint64_t T;
+      const uint32_t R = (uint32_t)K - n_sure;                    // keys still needed, >= 1
+      n_sel = (uint32_t)K;
+      for (uint32_t i = threadIdx.x; i < n_sure; i += kThreads) sel[i] = sure[i];
+      if (threadIdx.x == 0) s_nsel = n_sure;
+      __syncthreads();
       uint32_t* sh = reinterpret_cast<uint32_t*>(tmp);
       if (n_tie <= (uint32_t)kTieCap) {
-        auto get = [&](int i, uint64_t& k) { k = __ldcg(tie + i); return true; };
-        T = radix_kth((int)n_tie, R, get, sh, &s_res, &s_r);
+        auto get = [&](int i, uint64_t& k) { k = tie[i]; return true; };
+        const uint64_t T = radix_kth((int)n_tie, R, get, sh, &s_res, &s_r);
         for (uint32_t i = threadIdx.x; i < n_tie; i += kThreads) {
-          const uint64_t k = __ldcg(tie + i);
+          const uint64_t k = tie[i];
           if (k >= T) {
             const uint32_t slot = atomicAdd(&s_nsel, 1u);
             if (slot < (uint32_t)K) sel[slot] = k;
@@ -293,12 +327,12 @@ __global__ void __launch_bounds__(kThreads)
         }
       } else {  // tie list overflowed: exact select straight from the row
         auto get = [&](int i, uint64_t& k) {
-          const float s = row[i];
-          if (!is_candidate(s)) return false;
-          k = full_key(s, i);
+          const float sc = row[i];
+          if (!is_candidate(sc)) return false;
+          k = full_key(sc, i);
           return (int)(k >> (32 + kBinShift)) == thr;
         };
-        T = radix_kth(P_ld, R, get, sh, &s_res, &s_r);
+        const uint64_t T = radix_kth(P_ld, R, get, sh, &s_res, &s_r);
         for (int i = threadIdx.x; i < P_ld; i += kThreads) {
           uint64_t k;
           if (get(i, k) && k >= T) {
@@ -309,11 +343,37 @@ __global__ void __launch_bounds__(kThreads)
       }
       __syncthreads();
     }
+    sort_desc(sel, (int)n_sel, tmp);
+    for (int j = threadIdx.x; j < K; j += kThreads) s_ids[j] = j < (int)n_sel ? key_pool(sel[j]) : -1;
+    __syncthreads();
   }
-  sort_desc(sel, (int)n_sel, tmp);
+  // ---- 5. outputs
   int32_t* out = pool_ids + (long long)q * K;
-  for (int j = threadIdx.x; j < K; j += kThreads)
-    out[j] = j < (int)n_sel ? key_pool(sel[j]) : -1;
+  for (int j = threadIdx.x; j < K; j += kThreads) out[j] = s_ids[j];
+  if (ex.token_ids) {  // fused expand_selection
+    const int b = ex.q_seq ? ex.q_seq[q] : 0;
+    const bool seq_ok = b >= 0 && b < ex.B;
+    if (!seq_ok && threadIdx.x == 0) flag(ex.status, DSA_DEV_BAD_QSEQ);
+    const long long base = seq_ok ? ex.cu_pool_cap[b] : 0;
+    const int cap = seq_ok ? ex.cu_pool_cap[b + 1] - ex.cu_pool_cap[b] : 0;
+    int32_t* tok = ex.token_ids + (long long)q * ex.W;
+    for (int c = threadIdx.x; c < ex.W; c += kThreads) {
+      int v = -1;
+      if (seq_ok && c < K * ex.kpool) {
+        const int j = c / ex.kpool, s = c - j * ex.kpool;
+        const int p = s_ids[j];
+        if (p >= cap) {
+          if (s == 0) flag(ex.status, DSA_DEV_BAD_POOL_ID);
+        } else if (p >= 0) {
+          const int st = ex.pool_start[base + p];
+          if (st >= 0) v = st + s;
+        }
+      }
+      tok[c] = v;
+    }
+  }
+  if (gh)  // leave the histogram the scoring kernel filled zeroed for the next call
+    for (int i = threadIdx.x; i < kBins; i += kThreads) gh[i] = 0;
   pdl_launch_dependents();
 }
 
@@ -346,52 +406,56 @@ __global__ void expand_kernel(const int32_t* __restrict__ pool_ids,
   pdl_launch_dependents();
 }
 
-int chunks_for(int Q, int P_ld) {
-  const int target = 2 * kNumSMs;
-  int c = (target + Q - 1) / Q;
-  const int max_c = (P_ld + 1023) / 1024;
-  if (c > max_c) c = max_c;
-  return c < 1 ? 1 : c;
-}
-
-}  // namespace
-
-size_t topk_workspace_size(int Q, int P_ld, int select_k) {
-  (void)P_ld;
-  return ws_header_bytes(Q) + align256((size_t)Q * select_k * 8) +
-         align256((size_t)Q * kTieCap * 8);
-}
-
-int launch_topk_pools(const float* scores, int Q, int P_ld, int select_k, int32_t* pool_ids,
-                      void* workspace, size_t ws_bytes, cudaStream_t stream) {
-  (void)ws_bytes;
-  TopkWs ws = carve(workspace, Q, select_k);
-  if (cudaMemsetAsync(workspace, 0, ws_header_bytes(Q), stream) != cudaSuccess)
-    return DSA_ERR_CUDA;
-  const int chunks = chunks_for(Q, P_ld);
+int launch_select(const float* scores, int Q, int P_ld, int select_k, int32_t* pool_ids,
+                  uint32_t* hist, const ExpandArgs& ex, cudaStream_t stream) {
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr.val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(chunks, Q, 1);
+  cfg.gridDim = dim3(Q, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.stream = stream;
   cfg.attrs = &attr;
-  cfg.numAttrs = 0;  // follows a memset, not a kernel: plain stream order
-  if (cudaLaunchKernelEx(&cfg, topk_hist_kernel, scores, P_ld, chunks, ws) != cudaSuccess)
-    return DSA_ERR_CUDA;
   cfg.numAttrs = 1;
-  const int kmax = select_k > kTieCap ? select_k : kTieCap;
-  size_t smem = (size_t)kBins * 4 + kThreads * 4;
-  const size_t final_smem = 2 * (size_t)kmax * 8;
-  if (final_smem > smem) smem = final_smem;
+  const size_t smem = SelLayout(select_k).total;
+  if (smem > 227 * 1024) return DSA_ERR_UNSUPPORTED;
   cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
   cfg.dynamicSmemBytes = smem;
-  if (cudaLaunchKernelEx(&cfg, topk_select_kernel, scores, P_ld, select_k, chunks, ws,
-                         pool_ids) != cudaSuccess)
-    return DSA_ERR_CUDA;
-  return DSA_OK;
+  return cudaLaunchKernelEx(&cfg, topk_select_kernel, scores, P_ld, select_k, hist, pool_ids,
+                            ex) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace
+
+// Standalone top-k needs no workspace: the histogram lives on chip.  The fused
+// select path keeps a [Q][4096] histogram in its workspace.
+size_t topk_workspace_size(int Q, int P_ld, int select_k) {
+  (void)Q; (void)P_ld; (void)select_k;
+  return 0;
+}
+size_t select_workspace_size(int Q, int P_ld, int select_k) {
+  (void)P_ld; (void)select_k;
+  return align256((size_t)Q * kBins * 4);
+}
+
+uint32_t* topk_workspace_hist(void* workspace) { return static_cast<uint32_t*>(workspace); }
+
+int launch_topk_pools(const float* scores, int Q, int P_ld, int select_k, int32_t* pool_ids,
+                      void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  (void)workspace; (void)ws_bytes;
+  ExpandArgs ex = {};
+  return launch_select(scores, Q, P_ld, select_k, pool_ids, nullptr, ex, stream);
+}
+
+int launch_select_after_index(const float* scores, int Q, int P_ld, int select_k,
+                              int32_t* pool_ids, void* workspace, const int32_t* pool_start,
+                              const int32_t* cu_pool_cap, const int32_t* q_seq, int B, int kpool,
+                              int out_width, int32_t* token_ids, int32_t* status_dev,
+                              cudaStream_t stream) {
+  ExpandArgs ex = {pool_start, cu_pool_cap, q_seq, B, kpool, out_width, token_ids, status_dev};
+  return launch_select(scores, Q, P_ld, select_k, pool_ids,
+                       static_cast<uint32_t*>(workspace), ex, stream);
 }
 
 int launch_expand_selection(const int32_t* pool_ids, const int32_t* pool_start,

@@ -27,6 +27,7 @@ class LayerBuffers:
     out: torch.Tensor
     lse: torch.Tensor
     ws_topk: torch.Tensor
+    ws_select: torch.Tensor
     ws_mla: torch.Tensor | None
     status: torch.Tensor
 
@@ -37,6 +38,7 @@ class LayerBuffers:
         total_cap = int(bt.cu_pool_cap[-1].item())
         Q = bt.Q
         ws_t = ops.topk_workspace_bytes(Q, bt.P_ld, g.select_k)
+        ws_s = ops.select_workspace_bytes(Q, bt.P_ld, g.select_k)
         tag = ops.DSA_BF16 if g.dtype == "bf16" else ops.DSA_F32
         ws_m = ops.mla_workspace_bytes(Q, g.Hm, g.L, g.out_width, tag)
         return LayerBuffers(
@@ -50,6 +52,7 @@ class LayerBuffers:
             out=torch.empty(Q, g.Hm, g.L, dtype=bt.q_lat.dtype, device=dev),
             lse=torch.empty(Q, g.Hm, dtype=torch.float32, device=dev),
             ws_topk=torch.empty(max(ws_t, 16), dtype=torch.uint8, device=dev),
+            ws_select=torch.zeros(max(ws_s, 16), dtype=torch.uint8, device=dev),
             ws_mla=torch.empty(ws_m, dtype=torch.uint8, device=dev) if ws_m else None,
             status=torch.zeros(1, dtype=torch.int32, device=dev))
 
@@ -63,8 +66,8 @@ def compress(bt: Batch, buf: LayerBuffers, pool_begin=None, max_pools=None, stre
                            stream)
 
 
-def select(bt: Batch, buf: LayerBuffers, stream=None):
-    """index_scores -> topk_pools -> expand_selection."""
+def select_stages(bt: Batch, buf: LayerBuffers, stream=None):
+    """index_scores -> topk_pools -> expand_selection as three separate calls."""
     g = bt.geo
     ops.dsa_index_scores(bt.q, bt.weights, bt.scale, buf.pool_keys, buf.pool_start,
                          buf.pool_valid, buf.n_pools, bt.cu_pool_cap, bt.q_seq, bt.q_pos,
@@ -74,12 +77,20 @@ def select(bt: Batch, buf: LayerBuffers, stream=None):
                              buf.token_ids, buf.status, stream)
 
 
+def select(bt: Batch, buf: LayerBuffers, stream=None):
+    """The fused select call (same outputs as select_stages)."""
+    ops.dsa_select(bt.q, bt.weights, bt.scale, buf.pool_keys, buf.pool_start, buf.pool_valid,
+                   buf.n_pools, bt.cu_pool_cap, bt.q_seq, bt.q_pos, bt.geo.kpool, buf.scores,
+                   buf.pool_ids, buf.token_ids, buf.ws_select, buf.status, stream)
+
+
 def attend(bt: Batch, buf: LayerBuffers, stream=None):
     ops.dsa_mla_selected_decode(bt.q_lat, bt.kv, bt.cu_seqlens, bt.q_seq, buf.token_ids,
                                 bt.sm_scale, buf.out, buf.lse, buf.ws_mla, buf.status, stream)
 
 
-def run_layer(bt: Batch, buf: LayerBuffers, pool_begin=None, max_pools=None, stream=None):
+def run_layer(bt: Batch, buf: LayerBuffers, pool_begin=None, max_pools=None, stream=None,
+              fused=True):
     compress(bt, buf, pool_begin, max_pools, stream)
-    select(bt, buf, stream)
+    (select if fused else select_stages)(bt, buf, stream)
     attend(bt, buf, stream)

@@ -95,13 +95,13 @@ def test_index_scores_validation(lib):
 
 
 def test_topk_validation(lib):
-    ws = lib.dsa_topk_pools_workspace_size(4, 1000, 16)
-    assert ws > 0
-    assert lib.dsa_topk_pools(A, 4, 1000, 0, A, A, ws, None) == ERR["DSA_ERR_INVALID_ARG"]
-    assert lib.dsa_topk_pools(A, 4, 1000, 4097, A, A, ws, None) == ERR["DSA_ERR_UNSUPPORTED"]
-    assert lib.dsa_topk_pools(A, 4, 1000, 16, A, A, ws - 1, None) == ERR["DSA_ERR_WORKSPACE"]
-    assert lib.dsa_topk_pools(A, 4, 1000, 16, A, None, ws, None) == ERR["DSA_ERR_WORKSPACE"]
-    assert lib.dsa_topk_pools(A, 4, 1000, 16, A, A + 8, ws, None) == ERR["DSA_ERR_MISALIGNED"]
+    # the histogram and candidate lists live on chip: no workspace is needed
+    assert lib.dsa_topk_pools_workspace_size(4, 1000, 16) == 0
+    assert lib.dsa_topk_pools(A, 4, 1000, 0, A, None, 0, None) == ERR["DSA_ERR_INVALID_ARG"]
+    assert lib.dsa_topk_pools(A, 4, 0, 16, A, None, 0, None) == ERR["DSA_ERR_INVALID_ARG"]
+    assert lib.dsa_topk_pools(A, 4, 1000, 4097, A, None, 0, None) == ERR["DSA_ERR_UNSUPPORTED"]
+    assert lib.dsa_topk_pools(A + 2, 4, 1000, 16, A, None, 0, None) == ERR["DSA_ERR_MISALIGNED"]
+    assert lib.dsa_topk_pools(None, 4, 1000, 16, A, None, 0, None) == ERR["DSA_ERR_INVALID_ARG"]
     assert lib.dsa_topk_pools(A, 0, 1000, 16, A, None, 0, None) == ERR["DSA_OK"]
 
 
@@ -116,18 +116,33 @@ def test_expand_validation(lib):
 
 def test_mla_validation(lib):
     f = lib.dsa_mla_selected_decode
-    ws = lib.dsa_mla_selected_decode_workspace_size(4, 64, 512, 2048, 0)
-    assert ws > 0
+    # splits are merged on chip: the tensor-core path needs no workspace
+    assert lib.dsa_mla_selected_decode_workspace_size(4, 64, 512, 2048, 0) == 0
     assert lib.dsa_mla_selected_decode_workspace_size(4, 64, 512, 2048, 1) == 0
-    assert f(A, A, A, A, A, 4, 4, 64, 500, 2048, 0.04, 0, A, A, A, ws, None, None) \
+    assert f(A, A, A, A, A, 4, 4, 64, 500, 2048, 0.04, 0, A, A, None, 0, None, None) \
         == ERR["DSA_ERR_UNSUPPORTED"]
-    assert f(A, A, A, A, A, 4, 4, 64, 512, 2048, 0.04, 0, A, A, A, ws - 1, None, None) \
-        == ERR["DSA_ERR_WORKSPACE"]
-    assert f(A, A, A, A, A, 4, 4, 64, 512, 2048, 0.04, 0, A + 8, A, A, ws, None, None) \
+    assert f(A, A, A, A, A, 4, 4, 64, 512, 2048, 0.04, 0, A + 8, A, None, 0, None, None) \
         == ERR["DSA_ERR_MISALIGNED"]
-    assert f(A, A, A, A, A, 4, 4, 64, 512, 2048, float("nan"), 0, A, A, A, ws, None, None) \
+    assert f(A, A, A, A, A, 4, 4, 64, 512, 2048, float("nan"), 0, A, A, None, 0, None, None) \
         == ERR["DSA_ERR_INVALID_ARG"]
-    assert f(A, A, A, A, A, 0, 4, 64, 512, 2048, 0.04, 0, A, A, A, ws, None, None) == ERR["DSA_OK"]
+    assert f(A, A, A, A, A, 0, 4, 64, 512, 2048, 0.04, 0, A, A, None, 0, None, None) == ERR["DSA_OK"]
+
+
+def test_select_validation(lib):
+    f = lib.dsa_select
+    ws = lib.dsa_select_workspace_size(4, 1000, 16)
+    assert ws > 0
+    args = lambda **kw: [kw.get("q", A), A, kw.get("scale", 0.1), A, A, A, A, A, A, None,
+                         kw.get("Q", 4), 4, 32, 128, kw.get("kpool", 4), 1000,
+                         kw.get("k", 16), kw.get("W", 64), 0, A, A, A, kw.get("ws", A),
+                         kw.get("wsb", ws), None, None]
+    assert f(*args(kpool=9)) == ERR["DSA_ERR_INVALID_ARG"]
+    assert f(*args(W=63)) == ERR["DSA_ERR_INVALID_ARG"]                 # out_width < K*kpool
+    assert f(*args(k=5000, W=20000)) == ERR["DSA_ERR_UNSUPPORTED"]
+    assert f(*args(wsb=ws - 1)) == ERR["DSA_ERR_WORKSPACE"]
+    assert f(*args(ws=None)) == ERR["DSA_ERR_WORKSPACE"]
+    assert f(*args(q=A + 2)) == ERR["DSA_ERR_MISALIGNED"]
+    assert f(*args(Q=0)) == ERR["DSA_OK"]
 
 
 def test_python_binding_fails_loudly_without_cuda_tensors(lib):

@@ -217,3 +217,17 @@ def test_repeat_runs_are_bitwise_identical():
     torch.cuda.synchronize()
     for name in ("pool_keys", "scores", "pool_ids", "token_ids", "out", "lse"):
         assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+def test_fused_select_matches_stage_calls_and_leaves_workspace_zeroed():
+    for bt in (ragged_small(seed=41), synth.tiny(device=DEV), synth.single32k(device=DEV, seed=5)):
+        a = pipeline.LayerBuffers.alloc(bt)
+        b = pipeline.LayerBuffers.alloc(bt)
+        pipeline.run_layer(bt, a, fused=True)
+        pipeline.run_layer(bt, b, fused=False)
+        pipeline.select(bt, a)                      # second call reuses the workspace
+        torch.cuda.synchronize()
+        for name in ("scores", "pool_ids", "token_ids", "out", "lse"):
+            assert torch.equal(getattr(a, name), getattr(b, name)), name
+        hdr = a.ws_select[: 4096 * 4 * bt.Q]
+        assert int(hdr.count_nonzero().item()) == 0, "histogram not left zeroed"

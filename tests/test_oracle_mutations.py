@@ -19,22 +19,26 @@ MUTATIONS = {
     "rmsnorm": ("mu = x.mean(axis=-1, keepdims=True)", "mu = 0.0 * x.mean(axis=-1, keepdims=True)"),
     "unbiased_variance": ("var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)",
                           "var = ((x - mu) ** 2).sum(axis=-1, keepdims=True) / (x.shape[-1] - 1)"),
-    "softmax_over_channels": ("m = logit.max(axis=0, keepdims=True)\n            e = np.exp(logit - m)\n"
-                              "            w = e / e.sum(axis=0, keepdims=True)",
-                              "m = logit.max(axis=1, keepdims=True)\n            e = np.exp(logit - m)\n"
-                              "            w = e / e.sum(axis=1, keepdims=True)"),
-    "ape_dropped": ("logit = gate[toks] + ape ", "logit = gate[toks] + 0 * ape "),
+    "softmax_over_channels": ("m = logit.max(axis=1, keepdims=True)\n        e = np.exp(logit - m)\n"
+                              "        w = e / e.sum(axis=1, keepdims=True)",
+                              "m = logit.max(axis=2, keepdims=True)\n        e = np.exp(logit - m)\n"
+                              "        w = e / e.sum(axis=2, keepdims=True)"),
+    "softmax_over_pools": ("m = logit.max(axis=1, keepdims=True)\n        e = np.exp(logit - m)\n"
+                           "        w = e / e.sum(axis=1, keepdims=True)",
+                           "m = logit.max(axis=0, keepdims=True)\n        e = np.exp(logit - m)\n"
+                           "        w = e / e.sum(axis=0, keepdims=True)"),
+    "ape_dropped": ("logit = logit + ape[None, :, :]", "logit = logit + 0 * ape[None, :, :]"),
     "pools_from_token_0": ("t0 = first_valid(valid[lo:hi])", "t0 = 0"),
     "partial_pool_kept": ("P = (T - t0) // kpool", "P = -(-(T - t0) // kpool)"),
-    "any_valid_slot": ("pool_valid[g] = 1 if np.all(valid[toks] != 0) else 0",
-                       "pool_valid[g] = 1 if np.any(valid[toks] != 0) else 0"),
+    "any_valid_slot": ("np.all(valid[tok] != 0, axis=1)", "np.any(valid[tok] != 0, axis=1)"),
     "relu_after_weight": ("s = (np.maximum(0.0, scale * dots) * w[i][None, :]).sum(axis=1)",
                           "s = np.maximum(0.0, scale * dots * w[i][None, :]).sum(axis=1)"),
     "scale_dropped": ("np.maximum(0.0, scale * dots)", "np.maximum(0.0, dots)"),
     "causal_strict": ("cand &= last_tok <= int(q_pos[i])", "cand &= last_tok < int(q_pos[i])"),
     "tie_order_reversed": ("order = np.lexsort((cand, -s))", "order = np.lexsort((-cand, -s))"),
     "expand_without_base": ("start = int(pool_start[base + p])", "start = int(pool_start[p])"),
-    "mla_without_row_base": ("C = kv[lo + sel]", "C = kv[sel]"),
+    "mla_without_row_base": ("C = np.asarray(kv[lo + sel], np.float64)",
+                             "C = np.asarray(kv[sel], np.float64)"),
     "mla_scale_dropped": ("z = sm_scale * (q_lat[i] @ C.T)", "z = (q_lat[i] @ C.T)"),
     "bf16_truncates": ("r = np.rint(x / spacing) * spacing", "r = np.trunc(x / spacing) * spacing"),
 }
