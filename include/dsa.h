@@ -251,6 +251,28 @@ int dsa_select(const void* q, const float* weights, float scale, const void* poo
                size_t ws_bytes, int32_t* status_dev, void* stream);
 size_t dsa_select_workspace_size(int Q, int P_ld, int select_k);
 
+/*
+ * dsa_select_noalloc - dsa_select for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart: this is a deployment variant of dsa_select.
+ * Callers recording into a CUDA stream capture, plugins whose host framework
+ * owns every device allocation, or serving loops that forbid allocation after
+ * start-up cannot provide dsa_select's workspace.  This call takes the same
+ * arguments minus the workspace and writes the same outputs; its scratch (a
+ * 4096-bin histogram per query) lives in a static 1 MiB device array that every
+ * GPU loading the library keeps until the process exits.
+ *   Q must be <= 64 (else DSA_ERR_UNSUPPORTED).  All calls on a device share the
+ *   array: each call clears the part it uses first, and calls that overlap on
+ *   the GPU race on it.  The first call on a device looks up the array's device
+ *   address; make it before any stream capture.  It allocates nothing.
+ */
+int dsa_select_noalloc(const void* q, const float* weights, float scale, const void* pool_keys,
+                       const int32_t* pool_start, const uint8_t* pool_valid,
+                       const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
+                       const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
+                       int select_k, int out_width, int dtype, float* scores, int32_t* pool_ids,
+                       int32_t* token_ids, int32_t* status_dev, void* stream);
+
 /* Human-readable name of a DSA_* return code (static string). */
 const char* dsa_status_string(int status);
 

@@ -32,6 +32,8 @@ SIGNATURES = {
     "dsa_select": (c_int, [c_void_p, c_void_p, c_float] + [c_void_p] * 7 + [c_int] * 9
                    + [c_void_p] * 4 + [c_size_t] + [c_void_p] * 2),
     "dsa_select_workspace_size": (c_size_t, [c_int, c_int, c_int]),
+    "dsa_select_noalloc": (c_int, [c_void_p, c_void_p, c_float] + [c_void_p] * 7 + [c_int] * 9
+                           + [c_void_p] * 5),
     "dsa_status_string": (ctypes.c_char_p, [c_int]),
     "dsa_version": (c_int, []),
 }

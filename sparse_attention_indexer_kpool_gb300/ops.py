@@ -154,3 +154,24 @@ def dsa_select(q, weights, scale, pool_keys, pool_start, pool_valid, n_pools, cu
         0 if workspace is None else workspace.numel(), _ptr(status, torch.int32, "status"),
         _stream(stream))
     _check("dsa_select", code)
+
+
+def dsa_select_noalloc(q, weights, scale, pool_keys, pool_start, pool_valid, n_pools, cu_pool_cap,
+                       q_seq, q_pos, kpool, scores, pool_ids, token_ids, status=None, stream=None):
+    """dsa_select without a workspace, for callers that cannot allocate device
+    memory (stream capture, host frameworks owning all allocations, hot loops
+    that forbid allocation): its scratch is a static device array shared by all
+    calls on the device, so calls must not overlap on the GPU; Q <= 64."""
+    Q, H, D = q.shape
+    act = q.dtype
+    code = _lib.load().dsa_select_noalloc(
+        _ptr(q, act, "q"), _ptr(weights, torch.float32, "weights"), float(scale),
+        _ptr(pool_keys, act, "pool_keys"), _ptr(pool_start, torch.int32, "pool_start"),
+        _ptr(pool_valid, torch.uint8, "pool_valid"), _ptr(n_pools, torch.int32, "n_pools"),
+        _ptr(cu_pool_cap, torch.int32, "cu_pool_cap"), _ptr(q_seq, torch.int32, "q_seq"),
+        _ptr(q_pos, torch.int32, "q_pos"), Q, cu_pool_cap.numel() - 1, H, D, int(kpool),
+        scores.shape[-1], pool_ids.shape[-1], token_ids.shape[-1], _dtype_tag(q),
+        _ptr(scores, torch.float32, "scores"), _ptr(pool_ids, torch.int32, "pool_ids"),
+        _ptr(token_ids, torch.int32, "token_ids"), _ptr(status, torch.int32, "status"),
+        _stream(stream))
+    _check("dsa_select_noalloc", code)
