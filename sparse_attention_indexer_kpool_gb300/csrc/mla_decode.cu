@@ -7,18 +7,17 @@
 // row itself, so one gathered row feeds both the score and the output.
 //
 // Tensor-core kernel (bf16, L = 512, Hm % 16 == 0): one CTA = one query, one
-// group of 16 heads and one split of the selected rows.  Four warps each own a
-// 128-wide slice of the latent axis: for the scores they contract their slice
-// (partial 16 x 32 score tiles summed through shared memory), for the output
-// they own the matching 128 output columns (64 fp32 accumulators per thread).
-// Selected rows are gathered 32 at a time with 16-byte cp.async into a
-// 4-stage, XOR-swizzled shared ring (conflict-free ldmatrix), and the softmax
-// is the usual online (running max / running sum) form in base 2.  The splits
-// of one (query, head group) form a thread-block cluster: after the row loop
-// each CTA parks its partial output in its own shared memory and every CTA of
-// the cluster merges one latent slice from all members through distributed
-// shared memory, so no partials go to global memory and no second kernel runs.
-#include <cooperative_groups.h>
+// group of 16 heads and one split of the selected rows; splits are sized so the
+// CTAs cover the SMs once.  Eight warps: warp w owns latent quarter w % 4 and
+// row half w / 4 of each 64-row tile.  Scores: each warp contracts its latent
+// quarter for its 32 rows (partial 16 x 32 tiles summed through shared
+// memory).  Output: each warp accumulates its latent quarter over its 32 rows
+// (64 fp32 accumulators per thread); the two row halves are added at the end.
+// Selected rows are gathered 64 at a time with 16-byte cp.async into a
+// double-buffered, XOR-swizzled shared ring (conflict-free ldmatrix), and the
+// softmax is the usual online (running max / running sum) form in base 2.
+// With more than one split, each CTA writes its unnormalised partial and its
+// (max, sum) to the workspace and a small merge kernel combines them.
 #include <math.h>
 
 #include "dsa_internal.cuh"
@@ -26,29 +25,27 @@
 namespace dsa {
 namespace {
 
-namespace cg = cooperative_groups;
-
 constexpr int kL = 512;
 constexpr int kHG = 16;            // heads per CTA
-constexpr int kNT = 32;            // rows per tile
-constexpr int kRing = 4;           // gather stages
-constexpr int kWarps = 4;
+constexpr int kNT = 64;            // rows per tile
+constexpr int kRing = 2;           // gather stages
+constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kChunks = kL / 8;    // 16-byte chunks per latent row
-constexpr int kPStride = 40;       // bf16 per sP row (32 + 8 pad)
-constexpr int kMaxSplit = 8;       // portable cluster size
+constexpr int kPStride = kNT + 8;  // bf16 per sP row (padded)
+constexpr int kMaxRows = 8192;     // rows per split held in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct MlaSmem {
   union {
     __nv_bfloat16 kv[kRing][kNT * kL];   // swizzled gather ring
-    float part[kHG][kL];                 // this CTA's partial output (after the loop)
+    float ohalf[4][kHG][128];            // row-half-1 partial outputs (after the loop)
   };
   __nv_bfloat16 q[kHG * kL];             // swizzled
-  float s_part[kWarps][kHG][kNT];
+  float s_part[4][kHG][kNT];
   __nv_bfloat16 p[kHG * kPStride];
   float m[kHG], l[kHG], alpha[kHG];
-  // followed by int s_tok[rows_per_split]: this split's token ids (-1 = skip)
+  // followed by int s_tok[rows_per_split rounded up to a tile]
 };
 
 __device__ __forceinline__ int swz(int row, int chunk) {  // element offset of a 16B chunk
@@ -60,11 +57,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ q_seq,
                    const int32_t* __restrict__ token_ids, int B, int Hm, int W, int rows_per_split,
                    float sm_scale, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
-                   int32_t* status) {
+                   float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* status) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   MlaSmem& sm = *reinterpret_cast<MlaSmem*>(smem_raw);
+  int* s_tok = reinterpret_cast<int*>(smem_raw + sizeof(MlaSmem));
   const int qi = blockIdx.z, hg = blockIdx.y, split = blockIdx.x, n_split = gridDim.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3, half = warp >> 2;
   const int g = lane >> 2, t = lane & 3;
 
   // q_lat does not depend on the previous kernel: stage it before the grid wait
@@ -87,8 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int j_hi = min(W, j_lo + rows_per_split);
   const int n_tiles = (j_hi - j_lo + kNT - 1) / kNT;
   const int32_t* toks = token_ids + (long long)qi * W;
-  int* s_tok = reinterpret_cast<int*>(smem_raw + sizeof(MlaSmem));
-  // one coalesced pass: token ids of this split, validated (-1 = not a row)
+  // one coalesced pass: this split's token ids, validated (-1 = not a row)
   for (int j = j_lo + threadIdx.x; j < j_lo + n_tiles * kNT; j += kThreads) {
     int tok = -1;
     if (j < j_hi && seq_ok) {
@@ -114,12 +112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       cp_async16(smem_u32(&sm.kv[buf][swz(r, ch)]), ok ? src : kv, ok);
     }
   };
-  // prologue: the query block plus the first kRing-1 tiles in flight
-#pragma unroll
-  for (int i = 0; i < kRing - 1; ++i) {
-    if (i < n_tiles) load_tile(i);
-    cp_async_commit();
-  }
+  if (n_tiles > 0) load_tile(0);
+  cp_async_commit();
 
   float o[16][4];
 #pragma unroll
@@ -129,30 +123,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   for (int tile = 0; tile < n_tiles; ++tile) {
     const int buf = tile % kRing;
-    if (tile + kRing - 1 < n_tiles) load_tile(tile + kRing - 1);
+    if (tile + 1 < n_tiles) load_tile(tile + 1);
     cp_async_commit();
-    cp_async_wait<kRing - 1>();
+    cp_async_wait<1>();
     __syncthreads();
     if (tile == 0) {
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        const int ch = warp * 16 + kk * 2 + (lane >> 4);
+        const int ch = quarter * 16 + kk * 2 + (lane >> 4);
         ldmatrix_x4(qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3],
                     smem_u32(&sm.q[swz(lane & 15, ch)]));
       }
     }
-    // ---- partial scores over this warp's latent slice
+    // ---- partial scores: this warp's latent quarter x its 32 rows
+    const __nv_bfloat16* kvb = sm.kv[buf];
     float sacc[4][4];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-    const __nv_bfloat16* kvb = sm.kv[buf];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
+    for (int kk = 0; kk < 8; kk += 2) {
 #pragma unroll
-      for (int kk = 0; kk < 8; kk += 2) {
+      for (int nt = 0; nt < 4; ++nt) {
         uint32_t b0, b1, b2, b3;
-        const int ch = warp * 16 + kk * 2 + (lane >> 3);
-        ldmatrix_x4(b0, b1, b2, b3, smem_u32(&kvb[swz(nt * 8 + (lane & 7), ch)]));
+        const int ch = quarter * 16 + kk * 2 + (lane >> 3);
+        ldmatrix_x4(b0, b1, b2, b3, smem_u32(&kvb[swz(half * 32 + nt * 8 + (lane & 7), ch)]));
         mma_bf16_16816(sacc[nt], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
         mma_bf16_16816(sacc[nt], qf[kk + 1][0], qf[kk + 1][1], qf[kk + 1][2], qf[kk + 1][3], b2,
                        b3);
@@ -160,29 +154,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
-      sm.s_part[warp][g][nt * 8 + 2 * t] = sacc[nt][0];
-      sm.s_part[warp][g][nt * 8 + 2 * t + 1] = sacc[nt][1];
-      sm.s_part[warp][g + 8][nt * 8 + 2 * t] = sacc[nt][2];
-      sm.s_part[warp][g + 8][nt * 8 + 2 * t + 1] = sacc[nt][3];
+      const int c = half * 32 + nt * 8 + 2 * t;
+      *reinterpret_cast<float2*>(&sm.s_part[quarter][g][c]) = make_float2(sacc[nt][0], sacc[nt][1]);
+      *reinterpret_cast<float2*>(&sm.s_part[quarter][g + 8][c]) =
+          make_float2(sacc[nt][2], sacc[nt][3]);
     }
     __syncthreads();
-    // ---- online softmax: thread -> head h = tid/8, columns 4*(tid%8) .. +3
+    // ---- online softmax: thread -> head h = tid/16, columns 4*(tid%16) .. +3
     {
-      const int h = threadIdx.x >> 3, c0 = (threadIdx.x & 7) * 4;
+      const int h = threadIdx.x >> 4, c0 = (threadIdx.x & 15) * 4;
       float sv[4];
       float mx = -INFINITY;
+      const float4 p0 = *reinterpret_cast<const float4*>(&sm.s_part[0][h][c0]);
+      const float4 p1 = *reinterpret_cast<const float4*>(&sm.s_part[1][h][c0]);
+      const float4 p2 = *reinterpret_cast<const float4*>(&sm.s_part[2][h][c0]);
+      const float4 p3 = *reinterpret_cast<const float4*>(&sm.s_part[3][h][c0]);
+      const float ssum[4] = {p0.x + p1.x + p2.x + p3.x, p0.y + p1.y + p2.y + p3.y,
+                             p0.z + p1.z + p2.z + p3.z, p0.w + p1.w + p2.w + p3.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int c = c0 + i;
-        float v = sm.s_part[0][h][c] + sm.s_part[1][h][c] + sm.s_part[2][h][c] +
-                  sm.s_part[3][h][c];
-        v = s_tok[tile * kNT + c] >= 0 ? v * zscale : -INFINITY;
+        const float v = s_tok[tile * kNT + c0 + i] >= 0 ? ssum[i] * zscale : -INFINITY;
         sv[i] = v;
         mx = fmaxf(mx, v);
       }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+#pragma unroll
+      for (int o2 = 1; o2 < 16; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
       const float m_old = sm.m[h];
       const float m_new = fmaxf(m_old, mx);
       const bool none = m_new == -INFINITY;
@@ -194,20 +190,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         pv[i] = none ? 0.f : exp2f(sv[i] - m_new);
         ps += pv[i];
       }
-      ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-      ps += __shfl_xor_sync(0xffffffffu, ps, 2);
-      ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-      __nv_bfloat16* pr = &sm.p[h * kPStride + c0];
-      *reinterpret_cast<uint2*>(pr) = make_uint2(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]));
+#pragma unroll
+      for (int o2 = 1; o2 < 16; o2 <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o2);
+      *reinterpret_cast<uint2*>(&sm.p[h * kPStride + c0]) =
+          make_uint2(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]));
       __syncwarp();
-      if ((threadIdx.x & 7) == 0) {
+      if ((threadIdx.x & 15) == 0) {
         sm.m[h] = m_new;
         sm.l[h] = sm.l[h] * alpha + ps;
         sm.alpha[h] = alpha;
       }
     }
     __syncthreads();
-    // ---- O = O * alpha + P V over this warp's 128 output columns
+    // ---- O = O * alpha + P V: latent quarter, this warp's 32 rows
     const float a_lo = sm.alpha[g], a_hi = sm.alpha[g + 8];
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt) {
@@ -215,14 +210,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
+      const int rbase = half * 32 + kk * 16;
       uint32_t a0, a1, a2, a3;
       ldmatrix_x4(a0, a1, a2, a3,
-                  smem_u32(&sm.p[(lane & 15) * kPStride + (kk * 2 + (lane >> 4)) * 8]));
+                  smem_u32(&sm.p[(lane & 15) * kPStride + rbase + (lane >> 4) * 8]));
 #pragma unroll
       for (int nt = 0; nt < 16; nt += 2) {
         uint32_t b0, b1, b2, b3;
-        const int r = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int ch = warp * 16 + nt + (lane >> 4);
+        const int r = rbase + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int ch = quarter * 16 + nt + (lane >> 4);
         ldmatrix_x4_trans(b0, b1, b2, b3, smem_u32(&kvb[swz(r, ch)]));
         mma_bf16_16816(o[nt], a0, a1, a2, a3, b0, b1);
         mma_bf16_16816(o[nt + 1], a0, a1, a2, a3, b2, b3);
@@ -232,16 +228,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   cp_async_wait<0>();
   __syncthreads();
+  // ---- add the two row halves
+  if (half == 1) {
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      *reinterpret_cast<float2*>(&sm.ohalf[quarter][g][nt * 8 + 2 * t]) =
+          make_float2(o[nt][0], o[nt][1]);
+      *reinterpret_cast<float2*>(&sm.ohalf[quarter][g + 8][nt * 8 + 2 * t]) =
+          make_float2(o[nt][2], o[nt][3]);
+    }
+  }
+  __syncthreads();
   pdl_launch_dependents();
-
+  if (half == 1) return;
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt) {
+    const float2 x = *reinterpret_cast<const float2*>(&sm.ohalf[quarter][g][nt * 8 + 2 * t]);
+    const float2 y = *reinterpret_cast<const float2*>(&sm.ohalf[quarter][g + 8][nt * 8 + 2 * t]);
+    o[nt][0] += x.x; o[nt][1] += x.y; o[nt][2] += y.x; o[nt][3] += y.y;
+  }
   const int h_lo = hg * kHG + g, h_hi = h_lo + 8;
+  const float m_lo = sm.m[g], m_hi = sm.m[g + 8];
+  const float l_lo = sm.l[g], l_hi = sm.l[g + 8];
   if (n_split == 1) {
-    const float m_lo = sm.m[g], m_hi = sm.m[g + 8];
-    const float l_lo = sm.l[g], l_hi = sm.l[g + 8];
     const float inv_lo = l_lo > 0.f ? 1.f / l_lo : 0.f;
     const float inv_hi = l_hi > 0.f ? 1.f / l_hi : 0.f;
-    __nv_bfloat16* o_lo = out + ((long long)qi * Hm + h_lo) * kL + warp * 128;
-    __nv_bfloat16* o_hi = out + ((long long)qi * Hm + h_hi) * kL + warp * 128;
+    __nv_bfloat16* o_lo = out + ((long long)qi * Hm + h_lo) * kL + quarter * 128;
+    __nv_bfloat16* o_hi = out + ((long long)qi * Hm + h_hi) * kL + quarter * 128;
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt) {
       *reinterpret_cast<uint32_t*>(o_lo + nt * 8 + 2 * t) =
@@ -249,45 +262,69 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<uint32_t*>(o_hi + nt * 8 + 2 * t) =
           pack_bf16(o[nt][2] * inv_hi, o[nt][3] * inv_hi);
     }
-    if (lse && warp == 0 && t == 0) {
+    if (lse && quarter == 0 && t == 0) {
       lse[(long long)qi * Hm + h_lo] = l_lo > 0.f ? (m_lo + log2f(l_lo)) / kLog2e : -INFINITY;
       lse[(long long)qi * Hm + h_hi] = l_hi > 0.f ? (m_hi + log2f(l_hi)) / kLog2e : -INFINITY;
     }
     return;
   }
-
-  // ---- split merge inside the cluster (distributed shared memory)
+  // partial: unnormalised O, running max (base 2) and sum
+  const long long slot_lo = ((long long)qi * Hm + h_lo) * n_split + split;
+  const long long slot_hi = ((long long)qi * Hm + h_hi) * n_split + split;
+  float* p_lo = part_o + slot_lo * kL + quarter * 128;
+  float* p_hi = part_o + slot_hi * kL + quarter * 128;
 #pragma unroll
   for (int nt = 0; nt < 16; ++nt) {
-    *reinterpret_cast<float2*>(&sm.part[g][warp * 128 + nt * 8 + 2 * t]) =
-        make_float2(o[nt][0], o[nt][1]);
-    *reinterpret_cast<float2*>(&sm.part[g + 8][warp * 128 + nt * 8 + 2 * t]) =
-        make_float2(o[nt][2], o[nt][3]);
+    *reinterpret_cast<float2*>(p_lo + nt * 8 + 2 * t) = make_float2(o[nt][0], o[nt][1]);
+    *reinterpret_cast<float2*>(p_hi + nt * 8 + 2 * t) = make_float2(o[nt][2], o[nt][3]);
   }
-  cg::cluster_group cluster = cg::this_cluster();
-  cluster.sync();  // every member's partial, m and l are visible cluster-wide
-  const int rank = (int)cluster.block_rank();
-  const int c_lo = rank * kL / n_split;     // latent slice [c_lo, c_hi) merged by this CTA
-  const int cols = (rank + 1) * kL / n_split - c_lo;
-  for (int e = threadIdx.x; e < kHG * cols; e += kThreads) {
-    const int h = e / cols, c = c_lo + e % cols;
-    float M = -INFINITY;
-    for (int r = 0; r < n_split; ++r) M = fmaxf(M, cluster.map_shared_rank(sm.m, r)[h]);
-    float den = 0.f, acc = 0.f;
-    for (int r = 0; r < n_split; ++r) {
-      const float lr = cluster.map_shared_rank(sm.l, r)[h];
-      if (lr > 0.f) {
-        const float wgt = exp2f(cluster.map_shared_rank(sm.m, r)[h] - M);
-        den += lr * wgt;
-        acc += cluster.map_shared_rank(&sm.part[0][0], r)[h * kL + c] * wgt;
-      }
+  if (quarter == 0 && t == 0) {
+    part_ml[slot_lo * 2] = m_lo;
+    part_ml[slot_lo * 2 + 1] = l_lo;
+    part_ml[slot_hi * 2] = m_hi;
+    part_ml[slot_hi * 2 + 1] = l_hi;
+  }
+}
+
+// Merge split partials: one CTA per (query, head); 128 threads x 4 latent columns.
+__global__ void __launch_bounds__(128)
+    mla_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int Hm,
+                     int n_split, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+  __shared__ float s_w[64];
+  __shared__ float s_den, s_m;
+  pdl_wait();
+  const long long qh = (long long)blockIdx.y * Hm + blockIdx.x;
+  const float* ml = part_ml + qh * n_split * 2;
+  if (threadIdx.x < 32) {
+    float mx = -INFINITY;
+    for (int sp = threadIdx.x; sp < n_split; sp += 32) mx = fmaxf(mx, ml[2 * sp]);
+    mx = warp_max(mx);
+    float den = 0.f;
+    for (int sp = threadIdx.x; sp < n_split; sp += 32) {
+      const float l = ml[2 * sp + 1];
+      const float w = l > 0.f ? exp2f(ml[2 * sp] - mx) : 0.f;
+      s_w[sp] = w;
+      den += l * w;
     }
-    out[((long long)qi * Hm + hg * kHG + h) * kL + c] =
-        __float2bfloat16_rn(den > 0.f ? acc / den : 0.f);
-    if (lse && rank == 0 && e % cols == 0)
-      lse[(long long)qi * Hm + hg * kHG + h] = den > 0.f ? (M + log2f(den)) / kLog2e : -INFINITY;
+    den = warp_sum(den);
+    if (threadIdx.x == 0) { s_den = den; s_m = mx; }
   }
-  cluster.sync();  // keep this CTA's shared memory alive until every member has read it
+  __syncthreads();
+  const float den = s_den;
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  const int d = threadIdx.x * 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int sp = 0; sp < n_split; ++sp) {
+    const float w = s_w[sp];
+    if (w != 0.f) {
+      const float4 v = *reinterpret_cast<const float4*>(part_o + (qh * n_split + sp) * kL + d);
+      acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+    }
+  }
+  *reinterpret_cast<uint2*>(out + qh * kL + d) =
+      make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+  if (lse && threadIdx.x == 0) lse[qh] = den > 0.f ? (s_m + log2f(den)) / kLog2e : -INFINITY;
+  pdl_launch_dependents();
 }
 
 // Generic SIMT kernel: one CTA per (head, query); two passes over the rows.
@@ -370,27 +407,29 @@ __global__ void __launch_bounds__(256)
 
 bool fast_path(int Hm, int L, int dtype) { return dtype == DSA_BF16 && L == kL && Hm % kHG == 0; }
 
-// Split count: enough (query, head group, split) CTAs to cover the SMs once,
-// at most one portable cluster (8) per (query, head group).
+// Split count: (query, head group, split) CTAs covering the SMs once at most;
+// at most 64 splits (the merge keeps one weight per split on chip).
 void split_plan(int Q, int Hm, int W, int* n_split, int* rows_per_split) {
   const int n_hg = Hm / kHG;
-  int s = (kNumSMs + Q * n_hg - 1) / (Q * n_hg);
+  int s = kNumSMs / (Q * n_hg);
   const int max_s = (W + kNT - 1) / kNT;
   if (s > max_s) s = max_s;
-  if (s > kMaxSplit) s = kMaxSplit;
+  if (s > 64) s = 64;
   if (s < 1) s = 1;
   int rows = (W + s - 1) / s;
-  rows = (rows + kNT - 1) / kNT * kNT;
   *rows_per_split = rows;
-  // the cluster size equals the split count; every split gets rows < W
-  *n_split = s;
+  *n_split = (W + rows - 1) / rows;
 }
 
 }  // namespace
 
 size_t mla_workspace_size(int Q, int Hm, int L, int out_width, int dtype) {
-  (void)Q; (void)Hm; (void)L; (void)out_width; (void)dtype;
-  return 0;  // split partials are merged in distributed shared memory
+  if (!fast_path(Hm, L, dtype)) return 0;
+  int n_split, rows;
+  split_plan(Q, Hm, out_width, &n_split, &rows);
+  if (n_split == 1) return 0;
+  const size_t slots = (size_t)Q * Hm * n_split;
+  return slots * L * 4 + slots * 2 * 4;
 }
 
 int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
@@ -398,33 +437,40 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
                                int Hm, int L, int out_width, float sm_scale, int dtype, void* out,
                                float* lse, void* workspace, size_t ws_bytes, int32_t* status_dev,
                                cudaStream_t stream) {
-  (void)workspace; (void)ws_bytes;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.stream = stream;
-  cfg.attrs = attr;
+  cfg.attrs = &attr;
   cfg.numAttrs = 1;
   if (fast_path(Hm, L, dtype)) {
     int n_split, rows;
     split_plan(Q, Hm, out_width, &n_split, &rows);
-    const size_t smem = sizeof(MlaSmem) + (size_t)(rows + kNT) * 4;
-    if (smem > 227 * 1024) return DSA_ERR_UNSUPPORTED;
+    if (rows > kMaxRows) return DSA_ERR_UNSUPPORTED;
+    if (n_split > 1 && ws_bytes < mla_workspace_size(Q, Hm, L, out_width, dtype))
+      return DSA_ERR_WORKSPACE;
+    float* part_o = static_cast<float*>(workspace);
+    float* part_ml = part_o ? part_o + (size_t)Q * Hm * n_split * L : nullptr;
+    const size_t smem = sizeof(MlaSmem) + (size_t)((rows + kNT - 1) / kNT * kNT) * 4;
     cudaFuncSetAttribute(mla_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = n_split;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.numAttrs = 2;
     cfg.gridDim = dim3(n_split, Hm / kHG, Q);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     if (cudaLaunchKernelEx(&cfg, mla_mma_kernel, (const __nv_bfloat16*)q_lat,
                            (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, Hm,
-                           out_width, rows, sm_scale, (__nv_bfloat16*)out, lse,
+                           out_width, rows, sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml,
                            status_dev) != cudaSuccess)
       return DSA_ERR_CUDA;
+    if (n_split > 1) {
+      cfg.gridDim = dim3(Hm, Q, 1);
+      cfg.blockDim = dim3(128, 1, 1);
+      cfg.dynamicSmemBytes = 0;
+      if (cudaLaunchKernelEx(&cfg, mla_merge_kernel, (const float*)part_o,
+                             (const float*)part_ml, Hm, n_split, (__nv_bfloat16*)out,
+                             lse) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    }
     return DSA_OK;
   }
   if (L % 8 != 0 || L > 1024 || Hm > 128 || out_width > 16384) return DSA_ERR_UNSUPPORTED;

@@ -10,16 +10,20 @@
 // ~pool), so "score descending, pool ascending" is plain key-descending order
 // and the selected set and its order are unique.
 //
-// One CTA per query row, everything on chip:
+// A thread-block cluster of C CTAs per query row (C <= 8), everything on chip:
 //   1. a 4096-bin histogram of the top 12 key bits (built by the scoring kernel
-//      on the fused path, else by a first pass over the row here);
+//      on the fused path; else each CTA counts its slice and every CTA sums the
+//      C slice histograms through distributed shared memory);
 //   2. the threshold bin, where the count from the top reaches select_k;
-//   3. one pass over the row: keys above the bin go to a "sure" list, keys in
-//      it to a "tie" list (shared memory);
-//   4. exact finish: both lists sorted by a register bitonic network (the sure
-//      keys all precede the tie keys), or, for big lists, a radix select of the
+//   3. each CTA scans its slice of the row (8 loads in flight per thread): keys
+//      above the bin go to its "sure" list, keys in it to its "tie" list;
+//   4. rank 0 gathers the lists over distributed shared memory and finishes
+//      exactly: both lists sorted by a register bitonic network (the sure keys
+//      all precede the tie keys), or, for big lists, a radix select of the
 //      missing keys and a shared-memory sort;
 //   5. pool ids written, and optionally expanded to token ids in place.
+#include <cooperative_groups.h>
+
 #include "dsa_internal.cuh"
 
 namespace dsa {
@@ -208,18 +212,23 @@ __device__ uint64_t bitonic512_desc(uint64_t key, uint64_t* xch) {
 }
 
 // Shared-memory layout of the select kernel (dynamic):
-//   h[kBins] u32 | s_ids[K] i32 | sure[K] u64 | tie[kTieCap] u64 | scratch[2*max(K,kTieCap,1024)] u64
+//   h[kBins] | hsum[kBins] | ids[K] | sure[K] | tie[kTieCap] | scratch[2*max(K,kTieCap,1024)]
 struct SelLayout {
-  size_t ids, sure, tie, scratch, total;
+  size_t hsum, ids, sure, tie, scratch, total;
   __host__ __device__ SelLayout(int K) {
     const size_t kmax = (size_t)(K > kTieCap ? K : kTieCap);
-    ids = align256((size_t)kBins * 4);
+    hsum = align256((size_t)kBins * 4);
+    ids = hsum + align256((size_t)kBins * 4);
     sure = ids + align256((size_t)K * 4);
     tie = sure + align256((size_t)K * 8);
     scratch = tie + align256((size_t)kTieCap * 8);
     total = scratch + 2 * kmax * 8;
   }
 };
+
+constexpr int kBatch = 8;  // row elements in flight per thread
+
+namespace cg = cooperative_groups;
 
 __global__ void __launch_bounds__(kThreads, 1)
     topk_select_kernel(const float* __restrict__ scores, int P_ld, int K,
@@ -228,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(256) unsigned char smem[];
   const SelLayout lay(K);
   uint32_t* h = reinterpret_cast<uint32_t*>(smem);
+  uint32_t* hsum = reinterpret_cast<uint32_t*>(smem + lay.hsum);
   int32_t* s_ids = reinterpret_cast<int32_t*>(smem + lay.ids);
   uint64_t* sure = reinterpret_cast<uint64_t*>(smem + lay.sure);
   uint64_t* tie = reinterpret_cast<uint64_t*>(smem + lay.tie);
@@ -236,46 +246,95 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t s_nsure, s_ntie, s_r, s_nsel;
   __shared__ uint32_t s_wtot[64];
   __shared__ uint64_t s_res;
-  const int q = blockIdx.x;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int C = (int)cluster.num_blocks();
+  const int q = blockIdx.y;
   const float* row = scores + (long long)q * P_ld;
+  const int lo = (int)((long long)P_ld * rank / C);
+  const int hi = (int)((long long)P_ld * (rank + 1) / C);
   if (threadIdx.x == 0) { s_nsure = 0; s_ntie = 0; }
   pdl_wait();
 
   // ---- 1. histogram of the top 12 key bits
   uint32_t* gh = hist_in ? hist_in + (size_t)q * kBins : nullptr;
+  uint32_t* hh = h;
   if (gh) {
     for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = __ldcg(gh + i);
+    __syncthreads();
   } else {
     for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < P_ld; i += kThreads) {
-      const float sc = row[i];
-      if (is_candidate(sc)) atomicAdd(&h[score_key(sc) >> kBinShift], 1u);
+    for (int base = lo; base < hi; base += kThreads * kBatch) {
+      float v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = base + u * kThreads + threadIdx.x;
+        v[u] = i < hi ? row[i] : -INFINITY;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (is_candidate(v[u])) atomicAdd(&h[score_key(v[u]) >> kBinShift], 1u);
     }
+    if (C > 1) {
+      cluster.sync();  // every slice histogram is complete
+      for (int i = threadIdx.x; i < kBins; i += kThreads) {
+        uint32_t t = 0;
+        for (int r = 0; r < C; ++r) t += cluster.map_shared_rank(h, r)[i];
+        hsum[i] = t;
+      }
+      hh = hsum;
+    }
+    __syncthreads();
   }
-  __syncthreads();
   // ---- 2. threshold bin
-  find_threshold(h, K, &s_thr, s_wtot);
+  find_threshold(hh, K, &s_thr, s_wtot);
   const int thr = s_thr;
-  // ---- 3. one pass: sure and tie lists
-  for (int base = 0; base < P_ld; base += kThreads) {
-    const int i = base + threadIdx.x;
-    bool in_sure = false, in_tie = false;
-    uint64_t key = 0;
-    if (i < P_ld) {
-      const float sc = row[i];
-      if (is_candidate(sc)) {
-        key = full_key(sc, i);
+  // ---- 3. this CTA's slice: sure and tie lists
+  for (int base = lo; base < hi; base += kThreads * kBatch) {
+    float v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * kThreads + threadIdx.x;
+      v[u] = i < hi ? row[i] : -INFINITY;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * kThreads + threadIdx.x;
+      bool in_sure = false, in_tie = false;
+      uint64_t key = 0;
+      if (is_candidate(v[u])) {
+        key = full_key(v[u], i);
         const int bin = (int)(key >> (32 + kBinShift));
         in_sure = bin > thr;
         in_tie = bin == thr;
       }
+      append(in_sure, key, &s_nsure, sure, (uint32_t)K);
+      append(in_tie, key, &s_ntie, tie, (uint32_t)kTieCap);
     }
-    append(in_sure, key, &s_nsure, sure, (uint32_t)K);
-    append(in_tie, key, &s_ntie, tie, (uint32_t)kTieCap);
   }
+  cluster.sync();  // every slice's lists and counts are final
+  uint32_t n_sure, n_tie;
+  if (rank == 0) {
+    // gather the other slices' lists after this CTA's own
+    n_sure = s_nsure;
+    n_tie = s_ntie;
+    for (int r = 1; r < C; ++r) {
+      const uint32_t ns = *cluster.map_shared_rank(&s_nsure, r);
+      const uint32_t nt = *cluster.map_shared_rank(&s_ntie, r);
+      const uint64_t* rs = cluster.map_shared_rank(sure, r);
+      const uint64_t* rt = cluster.map_shared_rank(tie, r);
+      for (uint32_t i = threadIdx.x; i < ns; i += kThreads)
+        if (n_sure + i < (uint32_t)K) sure[n_sure + i] = rs[i];
+      for (uint32_t i = threadIdx.x; i < nt && i < (uint32_t)kTieCap; i += kThreads)
+        if (n_tie + i < (uint32_t)kTieCap) tie[n_tie + i] = rt[i];
+      n_sure += ns;
+      n_tie += nt;   // may exceed the capacity: then the exact slow path runs
+    }
+  }
+  cluster.sync();  // the other CTAs may leave once their lists are copied
+  if (rank != 0) return;
   __syncthreads();
-  const uint32_t n_sure = s_nsure, n_tie = s_ntie;
   uint32_t n_sel;
   // ---- 4. exact finish
   const bool fast = K <= kFast && n_sure <= (uint32_t)kFast &&
@@ -325,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (slot < (uint32_t)K) sel[slot] = k;
           }
         }
-      } else {  // tie list overflowed: exact select straight from the row
+      } else {  // the tie lists overflowed: exact select straight from the row
         auto get = [&](int i, uint64_t& k) {
           const float sc = row[i];
           if (!is_candidate(sc)) return false;
@@ -408,15 +467,23 @@ __global__ void expand_kernel(const int32_t* __restrict__ pool_ids,
 
 int launch_select(const float* scores, int Q, int P_ld, int select_k, int32_t* pool_ids,
                   uint32_t* hist, const ExpandArgs& ex, cudaStream_t stream) {
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr.val.programmaticStreamSerializationAllowed = 1;
+  // cluster size: enough CTAs to spread a few rows over the SMs, a slice of at
+  // least 4096 scores per CTA, at most 8 (portable clusters)
+  int C = 1;
+  while (C < 8 && Q * C * 2 <= kNumSMs && (long long)P_ld >= (long long)C * 2 * 4096) C *= 2;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = C;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(Q, 1, 1);
+  cfg.gridDim = dim3(C, Q, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.stream = stream;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   const size_t smem = SelLayout(select_k).total;
   if (smem > 227 * 1024) return DSA_ERR_UNSUPPORTED;
   cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -116,16 +116,19 @@ def test_expand_validation(lib):
 
 def test_mla_validation(lib):
     f = lib.dsa_mla_selected_decode
-    # splits are merged on chip: the tensor-core path needs no workspace
-    assert lib.dsa_mla_selected_decode_workspace_size(4, 64, 512, 2048, 0) == 0
+    ws = lib.dsa_mla_selected_decode_workspace_size(4, 64, 512, 2048, 0)   # split partials
+    assert ws > 0
     assert lib.dsa_mla_selected_decode_workspace_size(4, 64, 512, 2048, 1) == 0
-    assert f(A, A, A, A, A, 4, 4, 64, 500, 2048, 0.04, 0, A, A, None, 0, None, None) \
+    assert lib.dsa_mla_selected_decode_workspace_size(4096, 64, 512, 2048, 0) == 0   # no split
+    assert f(A, A, A, A, A, 4, 4, 64, 500, 2048, 0.04, 0, A, A, A, ws, None, None) \
         == ERR["DSA_ERR_UNSUPPORTED"]
-    assert f(A, A, A, A, A, 4, 4, 64, 512, 2048, 0.04, 0, A + 8, A, None, 0, None, None) \
+    assert f(A, A, A, A, A, 4, 4, 64, 512, 2048, 0.04, 0, A, A, A, ws - 1, None, None) \
+        == ERR["DSA_ERR_WORKSPACE"]
+    assert f(A, A, A, A, A, 4, 4, 64, 512, 2048, 0.04, 0, A + 8, A, A, ws, None, None) \
         == ERR["DSA_ERR_MISALIGNED"]
-    assert f(A, A, A, A, A, 4, 4, 64, 512, 2048, float("nan"), 0, A, A, None, 0, None, None) \
+    assert f(A, A, A, A, A, 4, 4, 64, 512, 2048, float("nan"), 0, A, A, A, ws, None, None) \
         == ERR["DSA_ERR_INVALID_ARG"]
-    assert f(A, A, A, A, A, 0, 4, 64, 512, 2048, 0.04, 0, A, A, None, 0, None, None) == ERR["DSA_OK"]
+    assert f(A, A, A, A, A, 0, 4, 64, 512, 2048, 0.04, 0, A, A, A, ws, None, None) == ERR["DSA_OK"]
 
 
 def test_select_validation(lib):
