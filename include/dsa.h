@@ -80,6 +80,8 @@ extern "C" {
 #define DSA_DEV_BAD_QSEQ 16        /* q_seq[q] outside [0, B); the query gets no output  */
 #define DSA_DEV_POOL_RANGE 32      /* index: n_pools[b] > cap_b or > P_ld; clamped       */
 #define DSA_DEV_TIMEOUT 64         /* a bounded wait inside a kernel gave up             */
+#define DSA_DEV_HIST_MISMATCH 128  /* dsa_select: workspace histogram did not match the
+                                      scores (workspace not zero-filled); exact fallback ran */
 
 #define DSA_KPOOL_MAX 8            /* module glm5next_dsa, Constants, KERNEL_MAX_KPOOL   */
 #define DSA_SELECT_K_MAX 4096

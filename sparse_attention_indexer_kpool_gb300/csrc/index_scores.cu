@@ -162,9 +162,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   if (hist)
     for (int i = threadIdx.x; i < kHistBins; i += kIdxThreads) sm.hist[i] = 0;
   pdl_wait();  // the pool cache may come from the kernel just before
+  pdl_launch_dependents();  // the selection kernel may start its prologue
   tile_prefix(s_prefix, Q, q_seq, q_pos, n_pools, cu_pool_cap, pool_start, B, kpool, P_ld,
               status);
-  pdl_launch_dependents();
   const int NT = s_prefix[Q];
   const long long t_lo = (long long)NT * blockIdx.x / gridDim.x;
   const long long t_hi = (long long)NT * (blockIdx.x + 1) / gridDim.x;

@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   constexpr int D = 32 * V;
   __shared__ int s_min;
   pdl_wait();
+  pdl_launch_dependents();  // the next kernel may start its prologue
   const int b = blockIdx.y;
   const long long lo = cu_seqlens[b];
   const int Tb = cu_seqlens[b + 1] - cu_seqlens[b];
@@ -226,7 +227,6 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
     pool_start[cap_lo + p] = t0 + p * kpool;
     pool_valid[cap_lo + p] = all_valid ? 1 : 0;
   }
-  pdl_launch_dependents();
 }
 
 template <typename T, int V>

@@ -66,38 +66,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int quarter = warp & 3, half = warp >> 2;
   const int g = lane >> 2, t = lane & 3;
 
-  // q_lat does not depend on the previous kernel: stage it before the grid wait
+  if (threadIdx.x < kHG) {
+    sm.m[threadIdx.x] = -INFINITY;
+    sm.l[threadIdx.x] = 0.f;
+  }
+  // every input may come from the kernel just before: wait for it first
+  pdl_wait();
+  pdl_launch_dependents();  // the merge kernel may start its prologue
   const __nv_bfloat16* qsrc = q_lat + ((long long)qi * Hm + hg * kHG) * kL;
   for (int c = threadIdx.x; c < kHG * kChunks; c += kThreads) {
     const int r = c / kChunks, ch = c % kChunks;
     cp_async16(smem_u32(&sm.q[swz(r, ch)]), qsrc + (long long)r * kL + ch * 8, true);
   }
-  if (threadIdx.x < kHG) {
-    sm.m[threadIdx.x] = -INFINITY;
-    sm.l[threadIdx.x] = 0.f;
+  const int j_lo = min(W, split * rows_per_split);
+  const int j_hi = min(W, j_lo + rows_per_split);
+  const int n_tiles = (j_hi - j_lo + kNT - 1) / kNT;
+  const int32_t* toks = token_ids + (long long)qi * W;
+  // token ids first: their loads do not wait for the sequence lookup
+  constexpr int kTokPer = 8;  // covers rows_per_split <= kThreads * kTokPer in one pass
+  int tk[kTokPer];
+#pragma unroll
+  for (int u = 0; u < kTokPer; ++u) {
+    const int j = j_lo + u * kThreads + threadIdx.x;
+    tk[u] = j < j_hi ? toks[j] : -1;
   }
-  pdl_wait();  // token ids come from the selection kernel
   const int b = q_seq ? q_seq[qi] : 0;
   const bool seq_ok = b >= 0 && b < B;
   if (!seq_ok && split == 0 && hg == 0 && threadIdx.x == 0) flag(status, DSA_DEV_BAD_QSEQ);
   const long long row_base = seq_ok ? cu_seqlens[b] : 0;
   const int Tb = seq_ok ? cu_seqlens[b + 1] - cu_seqlens[b] : 0;
-  const int j_lo = min(W, split * rows_per_split);
-  const int j_hi = min(W, j_lo + rows_per_split);
-  const int n_tiles = (j_hi - j_lo + kNT - 1) / kNT;
-  const int32_t* toks = token_ids + (long long)qi * W;
-  // one coalesced pass: this split's token ids, validated (-1 = not a row)
-  for (int j = j_lo + threadIdx.x; j < j_lo + n_tiles * kNT; j += kThreads) {
-    int tok = -1;
-    if (j < j_hi && seq_ok) {
-      tok = toks[j];
+  // validated token ids of this split (-1 = not a row), padded to whole tiles
+  for (int j0 = 0; j0 < n_tiles * kNT; j0 += kThreads * kTokPer) {
+#pragma unroll
+    for (int u = 0; u < kTokPer; ++u) {
+      const int jj = j0 + u * kThreads + threadIdx.x;
+      if (jj >= n_tiles * kNT) continue;
+      int tok = (j0 == 0) ? tk[u] : (j_lo + jj < j_hi ? toks[j_lo + jj] : -1);
+      if (!seq_ok) tok = -1;
       if (tok >= Tb) {
         if (hg == 0) flag(status, DSA_DEV_BAD_TOKEN);
         tok = -1;
       }
       if (tok < 0) tok = -1;
+      s_tok[jj] = tok;
     }
-    s_tok[j - j_lo] = tok;
   }
   __syncthreads();
 
@@ -239,7 +251,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  pdl_launch_dependents();
   if (half == 1) return;
 #pragma unroll
   for (int nt = 0; nt < 16; ++nt) {

@@ -17,10 +17,13 @@
 //   2. the threshold bin, where the count from the top reaches select_k;
 //   3. each CTA scans its slice of the row (8 loads in flight per thread): keys
 //      above the bin go to its "sure" list, keys in it to its "tie" list;
-//   4. rank 0 gathers the lists over distributed shared memory and finishes
-//      exactly: both lists sorted by a register bitonic network (the sure keys
-//      all precede the tie keys), or, for big lists, a radix select of the
-//      missing keys and a shared-memory sort;
+//   4. every CTA all-gathers the cluster's lists over distributed shared
+//      memory and places its own keys exactly: a sure key's output slot is the
+//      number of larger sure keys; a tie key is selected when fewer than
+//      select_k - #sure tie keys are larger, and sits after all sure keys (keys
+//      are distinct, so these counts are the sorted positions; no sort runs);
+//      if the tie lists overflow their on-chip capacity, rank 0 falls back to
+//      an exact radix select over the row and a shared-memory sort;
 //   5. pool ids written, and optionally expanded to token ids in place.
 #include <cooperative_groups.h>
 
@@ -211,24 +214,44 @@ __device__ uint64_t bitonic512_desc(uint64_t key, uint64_t* xch) {
   return key;
 }
 
-// Shared-memory layout of the select kernel (dynamic):
-//   h[kBins] | hsum[kBins] | ids[K] | sure[K] | tie[kTieCap] | scratch[2*max(K,kTieCap,1024)]
+// Shared-memory layout of the select kernel (dynamic).  Region A holds the
+// per-slice state and is reused as sort scratch on the slow path; region B the
+// gathered lists and the output ids.
+//   A: h[kBins] | hsum[kBins] | own_sure[K] | own_tie[kTieCap]     (>= 2*max(K,kTieCap) keys)
+//   B: all_sure[K] | all_tie[kTieCap] | ids[K]
 struct SelLayout {
-  size_t hsum, ids, sure, tie, scratch, total;
+  size_t hsum, own_sure, own_tie, a_end, all_sure, all_tie, ids, total;
   __host__ __device__ SelLayout(int K) {
     const size_t kmax = (size_t)(K > kTieCap ? K : kTieCap);
     hsum = align256((size_t)kBins * 4);
-    ids = hsum + align256((size_t)kBins * 4);
-    sure = ids + align256((size_t)K * 4);
-    tie = sure + align256((size_t)K * 8);
-    scratch = tie + align256((size_t)kTieCap * 8);
-    total = scratch + 2 * kmax * 8;
+    own_sure = hsum + align256((size_t)kBins * 4);
+    own_tie = own_sure + align256((size_t)K * 8);
+    a_end = own_tie + align256((size_t)kTieCap * 8);
+    if (a_end < 2 * kmax * 8) a_end = align256(2 * kmax * 8);
+    all_sure = a_end;
+    all_tie = all_sure + align256((size_t)K * 8);
+    ids = all_tie + align256((size_t)kTieCap * 8);
+    total = ids + align256((size_t)K * 4);
   }
 };
 
 constexpr int kBatch = 8;  // row elements in flight per thread
 
 namespace cg = cooperative_groups;
+
+// Number of keys in list[0..n) larger than x, computed by `parts` cooperating
+// lanes (a power of two <= 32, aligned in the warp); every lane gets the total.
+__device__ __forceinline__ uint32_t count_larger(const uint64_t* list, uint32_t n, uint64_t x,
+                                                 int part, int parts) {
+  uint32_t c = 0;
+  uint32_t j = part;
+  for (; j + 3 * parts < n; j += 4 * parts)
+    c += (list[j] > x) + (list[j + parts] > x) + (list[j + 2 * parts] > x) +
+         (list[j + 3 * parts] > x);
+  for (; j < n; j += parts) c += list[j] > x;
+  for (int o = parts >> 1; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  return c;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     topk_select_kernel(const float* __restrict__ scores, int P_ld, int K,
@@ -238,13 +261,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const SelLayout lay(K);
   uint32_t* h = reinterpret_cast<uint32_t*>(smem);
   uint32_t* hsum = reinterpret_cast<uint32_t*>(smem + lay.hsum);
+  uint64_t* own_sure = reinterpret_cast<uint64_t*>(smem + lay.own_sure);
+  uint64_t* own_tie = reinterpret_cast<uint64_t*>(smem + lay.own_tie);
+  uint64_t* all_sure = reinterpret_cast<uint64_t*>(smem + lay.all_sure);
+  uint64_t* all_tie = reinterpret_cast<uint64_t*>(smem + lay.all_tie);
   int32_t* s_ids = reinterpret_cast<int32_t*>(smem + lay.ids);
-  uint64_t* sure = reinterpret_cast<uint64_t*>(smem + lay.sure);
-  uint64_t* tie = reinterpret_cast<uint64_t*>(smem + lay.tie);
-  uint64_t* scratch = reinterpret_cast<uint64_t*>(smem + lay.scratch);
   __shared__ int s_thr;
   __shared__ uint32_t s_nsure, s_ntie, s_r, s_nsel;
   __shared__ uint32_t s_wtot[64];
+  __shared__ uint32_t s_cnt[2][9];   // per-rank sure / tie counts, exclusive prefix in [.][r]
   __shared__ uint64_t s_res;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -255,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hi = (int)((long long)P_ld * (rank + 1) / C);
   if (threadIdx.x == 0) { s_nsure = 0; s_ntie = 0; }
   pdl_wait();
+  pdl_launch_dependents();  // the next kernel may start its own prologue
 
   // ---- 1. histogram of the top 12 key bits
   uint32_t* gh = hist_in ? hist_in + (size_t)q * kBins : nullptr;
@@ -309,131 +335,162 @@ __global__ void __launch_bounds__(kThreads, 1)
         in_sure = bin > thr;
         in_tie = bin == thr;
       }
-      append(in_sure, key, &s_nsure, sure, (uint32_t)K);
-      append(in_tie, key, &s_ntie, tie, (uint32_t)kTieCap);
+      append(in_sure, key, &s_nsure, own_sure, (uint32_t)K);
+      append(in_tie, key, &s_ntie, own_tie, (uint32_t)kTieCap);
     }
   }
   cluster.sync();  // every slice's lists and counts are final
-  uint32_t n_sure, n_tie;
-  if (rank == 0) {
-    // gather the other slices' lists after this CTA's own
-    n_sure = s_nsure;
-    n_tie = s_ntie;
-    for (int r = 1; r < C; ++r) {
-      const uint32_t ns = *cluster.map_shared_rank(&s_nsure, r);
-      const uint32_t nt = *cluster.map_shared_rank(&s_ntie, r);
-      const uint64_t* rs = cluster.map_shared_rank(sure, r);
-      const uint64_t* rt = cluster.map_shared_rank(tie, r);
-      for (uint32_t i = threadIdx.x; i < ns; i += kThreads)
-        if (n_sure + i < (uint32_t)K) sure[n_sure + i] = rs[i];
-      for (uint32_t i = threadIdx.x; i < nt && i < (uint32_t)kTieCap; i += kThreads)
-        if (n_tie + i < (uint32_t)kTieCap) tie[n_tie + i] = rt[i];
-      n_sure += ns;
-      n_tie += nt;   // may exceed the capacity: then the exact slow path runs
-    }
+  // ---- 4. all-gather the cluster's lists
+  if (threadIdx.x < 2 * C) {
+    const int r = threadIdx.x % C, which = threadIdx.x / C;
+    s_cnt[which][r + 1] = *cluster.map_shared_rank(which ? &s_ntie : &s_nsure, r);
   }
-  cluster.sync();  // the other CTAs may leave once their lists are copied
-  if (rank != 0) return;
   __syncthreads();
-  uint32_t n_sel;
-  // ---- 4. exact finish
-  const bool fast = K <= kFast && n_sure <= (uint32_t)kFast &&
-                    (thr < 0 || n_tie <= (uint32_t)kFast);
-  if (fast) {
-    // threads [0,512) sort the sure keys, [512,1024) the tie keys, concurrently
-    uint64_t* xch = scratch;                 // 1024 keys
-    uint64_t* srt = scratch + kThreads;      // 1024 keys
-    const int pos = threadIdx.x & (kFast - 1);
-    const bool tie_half = threadIdx.x >= kFast;
-    uint64_t key = 0;
-    if (!tie_half && pos < (int)n_sure) key = sure[pos];
-    if (tie_half && thr >= 0 && pos < (int)n_tie) key = tie[pos];
-    key = bitonic512_desc(key, xch);
-    srt[threadIdx.x] = key;
-    __syncthreads();
-    n_sel = thr < 0 ? n_sure : (uint32_t)K;
-    for (int j = threadIdx.x; j < K; j += kThreads) {
-      uint64_t k2 = 0;
-      if ((uint32_t)j < n_sure) k2 = srt[j];
-      else if ((uint32_t)j < n_sel) k2 = srt[kFast + (j - (int)n_sure)];
-      s_ids[j] = (uint32_t)j < n_sel ? key_pool(k2) : -1;
-    }
-    __syncthreads();
-  } else {
-    const int kmax = K > kTieCap ? K : kTieCap;
-    uint64_t* sel = scratch;
-    uint64_t* tmp = scratch + kmax;
-    if (thr < 0) {
-      n_sel = n_sure;  // every candidate is in the sure list (<= K of them)
-      for (uint32_t i = threadIdx.x; i < n_sel; i += kThreads) sel[i] = sure[i];
-      __syncthreads();
-    } else {
-      const uint32_t R = (uint32_t)K - n_sure;                    // keys still needed, >= 1
-      n_sel = (uint32_t)K;
-      for (uint32_t i = threadIdx.x; i < n_sure; i += kThreads) sel[i] = sure[i];
-      if (threadIdx.x == 0) s_nsel = n_sure;
-      __syncthreads();
-      uint32_t* sh = reinterpret_cast<uint32_t*>(tmp);
-      if (n_tie <= (uint32_t)kTieCap) {
-        auto get = [&](int i, uint64_t& k) { k = tie[i]; return true; };
-        const uint64_t T = radix_kth((int)n_tie, R, get, sh, &s_res, &s_r);
-        for (uint32_t i = threadIdx.x; i < n_tie; i += kThreads) {
-          const uint64_t k = tie[i];
-          if (k >= T) {
-            const uint32_t slot = atomicAdd(&s_nsel, 1u);
-            if (slot < (uint32_t)K) sel[slot] = k;
-          }
-        }
-      } else {  // the tie lists overflowed: exact select straight from the row
-        auto get = [&](int i, uint64_t& k) {
-          const float sc = row[i];
-          if (!is_candidate(sc)) return false;
-          k = full_key(sc, i);
-          return (int)(k >> (32 + kBinShift)) == thr;
-        };
-        const uint64_t T = radix_kth(P_ld, R, get, sh, &s_res, &s_r);
-        for (int i = threadIdx.x; i < P_ld; i += kThreads) {
-          uint64_t k;
-          if (get(i, k) && k >= T) {
-            const uint32_t slot = atomicAdd(&s_nsel, 1u);
-            if (slot < (uint32_t)K) sel[slot] = k;
-          }
+  if (threadIdx.x < 2) {
+    s_cnt[threadIdx.x][0] = 0;
+    for (int r = 0; r < C; ++r) s_cnt[threadIdx.x][r + 1] += s_cnt[threadIdx.x][r];
+  }
+  __syncthreads();
+  const uint32_t n_sure = s_cnt[0][C], n_tie = s_cnt[1][C];
+  const bool ties_fit = n_tie <= (uint32_t)kTieCap;
+  {
+    // one flat pass over (rank, element): every remote load is issued before any
+    // local store, so the copy costs a single distributed-shared-memory round trip
+    const uint32_t n_s = n_sure < (uint32_t)K ? n_sure : (uint32_t)K;
+    const uint32_t n_all = n_s + (ties_fit ? n_tie : 0u);
+    constexpr int kPer = 4;
+    for (uint32_t base = 0; base < n_all; base += kThreads * kPer) {
+      uint64_t v[kPer];
+      uint32_t dst[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const uint32_t f = base + u * kThreads + threadIdx.x;
+        dst[u] = 0xffffffffu;
+        v[u] = 0;
+        if (f < n_all) {
+          const bool is_tie = f >= n_s;
+          const uint32_t g = is_tie ? f - n_s : f;
+          int r = 0;
+          while (r + 1 < C && s_cnt[is_tie][r + 1] <= g) ++r;
+          const uint64_t* src = cluster.map_shared_rank(is_tie ? own_tie : own_sure, r);
+          v[u] = src[g - s_cnt[is_tie][r]];
+          dst[u] = f;
         }
       }
-      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        if (dst[u] == 0xffffffffu) continue;
+        if (dst[u] < n_s) all_sure[dst[u]] = v[u];
+        else all_tie[dst[u] - n_s] = v[u];
+      }
     }
-    sort_desc(sel, (int)n_sel, tmp);
-    for (int j = threadIdx.x; j < K; j += kThreads) s_ids[j] = j < (int)n_sel ? key_pool(sel[j]) : -1;
-    __syncthreads();
   }
-  // ---- 5. outputs
+  cluster.sync();  // every CTA has its copy: the others' shared memory may go away
+  const int32_t* pstart = ex.pool_start;
+  const int b = ex.token_ids ? (ex.q_seq ? ex.q_seq[q] : 0) : 0;
+  const bool seq_ok = !ex.token_ids || (b >= 0 && b < ex.B);
+  const long long cap_base = (ex.token_ids && seq_ok) ? ex.cu_pool_cap[b] : 0;
+  const int cap = (ex.token_ids && seq_ok) ? ex.cu_pool_cap[b + 1] - ex.cu_pool_cap[b] : 0;
   int32_t* out = pool_ids + (long long)q * K;
-  for (int j = threadIdx.x; j < K; j += kThreads) out[j] = s_ids[j];
-  if (ex.token_ids) {  // fused expand_selection
-    const int b = ex.q_seq ? ex.q_seq[q] : 0;
-    const bool seq_ok = b >= 0 && b < ex.B;
-    if (!seq_ok && threadIdx.x == 0) flag(ex.status, DSA_DEV_BAD_QSEQ);
-    const long long base = seq_ok ? ex.cu_pool_cap[b] : 0;
-    const int cap = seq_ok ? ex.cu_pool_cap[b + 1] - ex.cu_pool_cap[b] : 0;
-    int32_t* tok = ex.token_ids + (long long)q * ex.W;
-    for (int c = threadIdx.x; c < ex.W; c += kThreads) {
-      int v = -1;
-      if (seq_ok && c < K * ex.kpool) {
-        const int j = c / ex.kpool, s = c - j * ex.kpool;
-        const int p = s_ids[j];
-        if (p >= cap) {
-          if (s == 0) flag(ex.status, DSA_DEV_BAD_POOL_ID);
-        } else if (p >= 0) {
-          const int st = ex.pool_start[base + p];
-          if (st >= 0) v = st + s;
+  int32_t* tok = ex.token_ids ? ex.token_ids + (long long)q * ex.W : nullptr;
+  // writes one selected key's pool id and token ids at output slot `pos`
+  auto emit = [&](uint32_t pos, uint64_t key) {
+    const int p = key_pool(key);
+    out[pos] = p;
+    if (tok) {
+      int st = -1;
+      if (!seq_ok) {
+      } else if (p >= cap) {
+        flag(ex.status, DSA_DEV_BAD_POOL_ID);
+      } else {
+        st = pstart[cap_base + p];
+      }
+      for (int s = 0; s < ex.kpool; ++s) tok[pos * ex.kpool + s] = (st >= 0) ? st + s : -1;
+    }
+  };
+  // The lists are exactly the selection only if they agree with the histogram
+  // (a workspace that was not zero-filled breaks that); otherwise rank 0 runs an
+  // exact select that never looks at the histogram.
+  const bool consistent = thr < 0 ? n_sure <= (uint32_t)K
+                                  : (n_sure < (uint32_t)K && n_sure + n_tie >= (uint32_t)K);
+  if (consistent && ties_fit) {
+    const uint32_t n_sel = thr < 0 ? n_sure : (uint32_t)K;
+    if (rank == 0) {  // the -1 tail of both outputs
+      for (int j = n_sel + threadIdx.x; j < K; j += kThreads) out[j] = -1;
+      if (tok)
+        for (int c = n_sel * ex.kpool + threadIdx.x; c < ex.W; c += kThreads) tok[c] = -1;
+      if (tok && !seq_ok && threadIdx.x == 0) flag(ex.status, DSA_DEV_BAD_QSEQ);
+    }
+    // ---- 5. place this CTA's own keys by counting larger keys
+    const uint32_t my_s0 = s_cnt[0][rank], my_ns = s_cnt[0][rank + 1] - my_s0;
+    const uint32_t my_t0 = s_cnt[1][rank], my_nt = thr < 0 ? 0 : s_cnt[1][rank + 1] - my_t0;
+    const uint32_t n_own = my_ns + my_nt;
+    const uint32_t R = thr < 0 ? 0 : (uint32_t)K - n_sure;
+    int parts = 1;
+    while (parts < 32 && (uint32_t)parts * 2 * n_own <= (uint32_t)kThreads) parts *= 2;
+    for (uint32_t base = 0; base < n_own * parts; base += kThreads) {
+      const uint32_t w = base + threadIdx.x;
+      const uint32_t i = w / parts;
+      const int part = (int)(w % parts);
+      const bool act = i < n_own;
+      const bool is_tie = i >= my_ns;
+      uint64_t x = 0;
+      if (act) x = is_tie ? all_tie[my_t0 + (i - my_ns)] : all_sure[my_s0 + i];
+      // lanes of one key share a warp (parts divides 32); inactive lanes count
+      // nothing; one call site, so every lane runs the same shuffles
+      const uint64_t* lst = is_tie ? all_tie : all_sure;
+      const uint32_t nl = act ? (is_tie ? n_tie : n_sure) : 0u;
+      const uint32_t c = count_larger(lst, nl, x, part, parts);
+      if (act && part == 0) {
+        if (!is_tie) emit(c, x);
+        else if (c < R) emit(n_sure + c, x);
+      }
+    }
+  } else if (rank == 0) {
+    // ---- 5'. exact select straight from the row (tie lists overflowed, or the
+    // histogram did not describe these scores)
+    if (!consistent && threadIdx.x == 0) flag(ex.status, DSA_DEV_HIST_MISMATCH);
+    if (tok && !seq_ok && threadIdx.x == 0) flag(ex.status, DSA_DEV_BAD_QSEQ);
+    uint64_t* sel = reinterpret_cast<uint64_t*>(smem);               // region A as scratch
+    const int kmax = K > kTieCap ? K : kTieCap;
+    uint64_t* tmp = sel + kmax;
+    uint32_t* sh = reinterpret_cast<uint32_t*>(tmp);
+    if (threadIdx.x == 0) s_nsel = 0;
+    __syncthreads();
+    uint32_t cnt = 0;
+    for (int i = threadIdx.x; i < P_ld; i += kThreads) cnt += is_candidate(row[i]);
+    atomicAdd(&s_nsel, cnt);
+    __syncthreads();
+    const uint32_t n_cand = s_nsel;
+    const uint32_t n_sel = n_cand < (uint32_t)K ? n_cand : (uint32_t)K;
+    __syncthreads();
+    if (threadIdx.x == 0) s_nsel = 0;
+    __syncthreads();
+    if (n_sel > 0) {
+      auto get = [&](int i, uint64_t& k) {
+        const float sc = row[i];
+        if (!is_candidate(sc)) return false;
+        k = full_key(sc, i);
+        return true;
+      };
+      const uint64_t T = radix_kth(P_ld, n_sel, get, sh, &s_res, &s_r);
+      for (int i = threadIdx.x; i < P_ld; i += kThreads) {
+        uint64_t k;
+        if (get(i, k) && k >= T) {
+          const uint32_t slot = atomicAdd(&s_nsel, 1u);
+          if (slot < (uint32_t)K) sel[slot] = k;
         }
       }
-      tok[c] = v;
+      __syncthreads();
+      sort_desc(sel, (int)n_sel, tmp);
     }
+    for (int j = threadIdx.x; j < (int)n_sel; j += kThreads) emit(j, sel[j]);
+    for (int j = n_sel + threadIdx.x; j < K; j += kThreads) out[j] = -1;
+    if (tok)
+      for (int c = n_sel * ex.kpool + threadIdx.x; c < ex.W; c += kThreads) tok[c] = -1;
   }
-  if (gh)  // leave the histogram the scoring kernel filled zeroed for the next call
+  if (gh && rank == 0)  // leave the histogram the scoring kernel filled zeroed for the next call
     for (int i = threadIdx.x; i < kBins; i += kThreads) gh[i] = 0;
-  pdl_launch_dependents();
 }
 
 __global__ void expand_kernel(const int32_t* __restrict__ pool_ids,

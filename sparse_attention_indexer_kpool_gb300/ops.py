@@ -14,6 +14,7 @@ from . import _lib
 DSA_BF16, DSA_F32 = 0, 1
 DEV_BAD_TOKEN, DEV_POOL_OVERFLOW, DEV_POOL_UNCOVERED = 1, 2, 4
 DEV_BAD_POOL_ID, DEV_BAD_QSEQ, DEV_POOL_RANGE, DEV_TIMEOUT = 8, 16, 32, 64
+DEV_HIST_MISMATCH = 128
 
 
 class DsaError(RuntimeError):

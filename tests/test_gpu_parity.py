@@ -231,3 +231,29 @@ def test_fused_select_matches_stage_calls_and_leaves_workspace_zeroed():
             assert torch.equal(getattr(a, name), getattr(b, name)), name
         hdr = a.ws_select[: 4096 * 4 * bt.Q]
         assert int(hdr.count_nonzero().item()) == 0, "histogram not left zeroed"
+
+
+def test_select_with_dirty_workspace_falls_back_exactly():
+    """A dsa_select workspace that was not zero-filled gives a histogram that does
+    not describe the scores; the selection must still be exact (fallback path),
+    flagged, and the workspace left zeroed for the next call."""
+    for fill in (0xFF, 0x01):
+        bt = synth.single32k(device=DEV, seed=91)
+        a = pipeline.LayerBuffers.alloc(bt)
+        b = pipeline.LayerBuffers.alloc(bt)
+        pipeline.compress(bt, a)
+        pipeline.compress(bt, b)
+        a.ws_select.fill_(fill)
+        pipeline.select(bt, a)
+        pipeline.select_stages(bt, b)
+        torch.cuda.synchronize()
+        assert int(a.status.item()) & ops.DEV_HIST_MISMATCH
+        for name in ("scores", "pool_ids", "token_ids"):
+            assert torch.equal(getattr(a, name), getattr(b, name)), name
+        hdr = a.ws_select[: 4096 * 4 * bt.Q]
+        assert int(hdr.count_nonzero().item()) == 0
+        a.status.zero_()
+        pipeline.select(bt, a)                       # clean again: fast path, no flag
+        torch.cuda.synchronize()
+        assert int(a.status.item()) == 0
+        assert torch.equal(a.pool_ids, b.pool_ids)
