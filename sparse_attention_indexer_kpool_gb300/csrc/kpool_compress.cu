@@ -178,30 +178,36 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   const long long s0 = lo + t0 + (long long)p * kpool;
   float kn[kKpoolMax][V], lg[kKpoolMax][V];
   bool all_valid = true;
+  // every slot's rows are requested before any reduction runs, so the loads of
+  // the pool overlap instead of waiting one slot at a time
 #pragma unroll
   for (int s = 0; s < kKpoolMax; ++s) {
     if (s < kpool) {
-      float x[V], gt[V];
-      Vec<T, V>::load(k + (s0 + s) * D + lane * V, x);
-      Vec<T, V>::load(gate + (s0 + s) * D + lane * V, gt);
+      Vec<T, V>::load(k + (s0 + s) * D + lane * V, kn[s]);
+      Vec<T, V>::load(gate + (s0 + s) * D + lane * V, lg[s]);
+      all_valid &= valid[s0 + s] != 0;
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < kKpoolMax; ++s) {
+    if (s < kpool) {
       float sum = 0.f;
 #pragma unroll
-      for (int i = 0; i < V; ++i) sum += x[i];
+      for (int i = 0; i < V; ++i) sum += kn[s][i];
       const float mean = warp_sum(sum) * (1.0f / D);
       float sq = 0.f;
 #pragma unroll
       for (int i = 0; i < V; ++i) {
-        const float dx = x[i] - mean;
+        const float dx = kn[s][i] - mean;
         sq += dx * dx;
       }
       const float var = warp_sum(sq) * (1.0f / D);
       const float rstd = 1.0f / sqrtf(var + ln_eps);
 #pragma unroll
       for (int i = 0; i < V; ++i) {
-        kn[s][i] = Act<T>::round((x[i] - mean) * rstd * g[i] + be[i]);
-        lg[s][i] = gt[i] + __ldg(ape + s * D + lane * V + i);
+        kn[s][i] = Act<T>::round((kn[s][i] - mean) * rstd * g[i] + be[i]);
+        lg[s][i] = lg[s][i] + __ldg(ape + s * D + lane * V + i);
       }
-      all_valid &= valid[s0 + s] != 0;
     }
   }
   float res[V];

@@ -298,44 +298,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merge split partials: one CTA per (query, head); 128 threads x 4 latent columns.
+// Every split's partial row is requested up front, together with the (max, sum)
+// pairs, so the merge waits for memory once.
+constexpr int kMergeMax = 16;   // splits held in registers; more splits loop
 __global__ void __launch_bounds__(128)
     mla_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int Hm,
                      int n_split, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
-  __shared__ float s_w[64];
-  __shared__ float s_den, s_m;
   pdl_wait();
   const long long qh = (long long)blockIdx.y * Hm + blockIdx.x;
   const float* ml = part_ml + qh * n_split * 2;
-  if (threadIdx.x < 32) {
-    float mx = -INFINITY;
-    for (int sp = threadIdx.x; sp < n_split; sp += 32) mx = fmaxf(mx, ml[2 * sp]);
-    mx = warp_max(mx);
-    float den = 0.f;
-    for (int sp = threadIdx.x; sp < n_split; sp += 32) {
-      const float l = ml[2 * sp + 1];
-      const float w = l > 0.f ? exp2f(ml[2 * sp] - mx) : 0.f;
-      s_w[sp] = w;
-      den += l * w;
-    }
-    den = warp_sum(den);
-    if (threadIdx.x == 0) { s_den = den; s_m = mx; }
-  }
-  __syncthreads();
-  const float den = s_den;
-  const float inv = den > 0.f ? 1.f / den : 0.f;
   const int d = threadIdx.x * 4;
+  float mx = -INFINITY;
+  for (int sp = 0; sp < n_split; ++sp) mx = fmaxf(mx, __ldg(ml + 2 * sp));
+  float den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int sp = 0; sp < n_split; ++sp) {
-    const float w = s_w[sp];
-    if (w != 0.f) {
-      const float4 v = *reinterpret_cast<const float4*>(part_o + (qh * n_split + sp) * kL + d);
-      acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+  for (int s0 = 0; s0 < n_split; s0 += kMergeMax) {
+    float4 v[kMergeMax];
+    float mm[kMergeMax], ll[kMergeMax];
+#pragma unroll
+    for (int u = 0; u < kMergeMax; ++u) {
+      const int sp = s0 + u;
+      if (sp < n_split) {
+        v[u] = __ldg(reinterpret_cast<const float4*>(part_o + (qh * n_split + sp) * kL + d));
+        mm[u] = __ldg(ml + 2 * sp);
+        ll[u] = __ldg(ml + 2 * sp + 1);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kMergeMax; ++u) {
+      if (s0 + u < n_split && ll[u] > 0.f) {
+        const float w = exp2f(mm[u] - mx);
+        den += ll[u] * w;
+        acc.x += w * v[u].x; acc.y += w * v[u].y; acc.z += w * v[u].z; acc.w += w * v[u].w;
+      }
     }
   }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
   *reinterpret_cast<uint2*>(out + qh * kL + d) =
       make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
-  if (lse && threadIdx.x == 0) lse[qh] = den > 0.f ? (s_m + log2f(den)) / kLog2e : -INFINITY;
-  pdl_launch_dependents();
+  if (lse && threadIdx.x == 0) lse[qh] = den > 0.f ? (mx + log2f(den)) / kLog2e : -INFINITY;
 }
 
 // Generic SIMT kernel: one CTA per (head, query); two passes over the rows.
