@@ -372,7 +372,7 @@ def run_ours(args, dist):
     if idx_ms:
         achieved = sel_bytes / (idx_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm",
-                    "kernel": "dsa_select call: index_scores_mma_kernel + topk_select_kernel",
+                    "kernel": "dsa_select call: index_scores_umma_kernel + topk_select_kernel",
                     "achieved": round(achieved, 1), "peak": hbm_peak, "peak_source": peak_src,
                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
                     "bytes_per_launch": sel_bytes, "launch_us": round(idx_ms * 1e3, 2)}

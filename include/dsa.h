@@ -143,17 +143,20 @@ int dsa_kpool_compress(const void* k, const void* gate, const uint8_t* valid, co
  * position).  pool_start must be as dsa_kpool_compress wrote it.
  *
  *   q        [Q, H, D] activation dtype;  weights [Q, H] fp32;  scale > 0
- *   pool_*   the cache written by dsa_kpool_compress (pool_start may be NULL
- *            when q_pos is NULL); n_pools [B]; cu_pool_cap [B+1]
+ *   pool_keys the cache written by dsa_kpool_compress, pool_rows rows of D
+ *            (pool_rows >= cu_pool_cap[B]; no row at or past it is read)
+ *   pool_*   the rest of that cache (pool_start may be NULL when q_pos is
+ *            NULL); n_pools [B]; cu_pool_cap [B+1]
  *   q_seq    [Q] int32 or NULL;  q_pos [Q] int32 or NULL (every complete pool)
  *   scores   [Q, P_ld] fp32
  * Supported: any H in [1, 64] and D in {32, 64, 128, 256} for both dtypes;
- * H = 32, D = 128, bf16 runs on the tensor cores (q_seq == NULL with many
- * queries: the dense prefill-chunk kernel).
+ * H = 32, D = 128, bf16 runs on the tcgen05 tensor cores (with q_seq == NULL
+ * and Q >= 64, eight queries share each key tile: the dense prefill-chunk
+ * form).  pool_keys and q must be 16-byte aligned.
  * Device faults: DSA_DEV_BAD_QSEQ, DSA_DEV_POOL_RANGE.
  */
 int dsa_index_scores(const void* q, const float* weights, float scale, const void* pool_keys,
-                     const int32_t* pool_start, const uint8_t* pool_valid,
+                     int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
                      const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
                      const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
                      int dtype, float* scores, int32_t* status_dev, void* stream);
@@ -237,8 +240,9 @@ size_t dsa_mla_selected_decode_workspace_size(int Q, int Hm, int L, int out_widt
  * indexer pipeline) and "Shape of the pipeline".  Writes exactly what the three
  * stage calls above write, in the same buffers (scores [Q, P_ld], pool_ids
  * [Q, select_k], token_ids [Q, out_width]), with the same arguments and device
- * faults, but fuses the top-k histogram into the scoring kernel and the
- * expansion into the top-k kernel.
+ * faults, but fuses the expansion into the top-k kernel and, for the decode
+ * geometry (bf16, H = 32, D = 128, one query per key tile), the top-k
+ * histogram into the scoring kernel.
  *
  *   workspace: dsa_select_workspace_size(Q, P_ld, select_k) bytes, 16-byte
  *   aligned, ZERO-FILLED BEFORE ITS FIRST USE; every call leaves it zeroed, so a
@@ -246,9 +250,10 @@ size_t dsa_mla_selected_decode_workspace_size(int Q, int Hm, int L, int out_widt
  *   flight at the same time must not share a workspace.
  */
 int dsa_select(const void* q, const float* weights, float scale, const void* pool_keys,
-               const int32_t* pool_start, const uint8_t* pool_valid, const int32_t* n_pools,
-               const int32_t* cu_pool_cap, const int32_t* q_seq, const int32_t* q_pos, int Q,
-               int B, int H, int D, int kpool, int P_ld, int select_k, int out_width, int dtype,
+               int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
+               const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
+               const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
+               int select_k, int out_width, int dtype,
                float* scores, int32_t* pool_ids, int32_t* token_ids, void* workspace,
                size_t ws_bytes, int32_t* status_dev, void* stream);
 size_t dsa_select_workspace_size(int Q, int P_ld, int select_k);
@@ -269,7 +274,7 @@ size_t dsa_select_workspace_size(int Q, int P_ld, int select_k);
  *   address; make it before any stream capture.  It allocates nothing.
  */
 int dsa_select_noalloc(const void* q, const float* weights, float scale, const void* pool_keys,
-                       const int32_t* pool_start, const uint8_t* pool_valid,
+                       int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
                        const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
                        const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
                        int select_k, int out_width, int dtype, float* scores, int32_t* pool_ids,

@@ -20,8 +20,8 @@ c_void_p, c_int, c_float, c_size_t = ctypes.c_void_p, ctypes.c_int, ctypes.c_flo
 SIGNATURES = {
     "dsa_kpool_compress": (c_int, [c_void_p] * 6 + [c_float] + [c_void_p] * 3 + [c_int] * 5
                            + [c_void_p] * 6),
-    "dsa_index_scores": (c_int, [c_void_p, c_void_p, c_float] + [c_void_p] * 7 + [c_int] * 7
-                         + [c_void_p] * 3),
+    "dsa_index_scores": (c_int, [c_void_p, c_void_p, c_float, c_void_p, c_int] + [c_void_p] * 6
+                         + [c_int] * 7 + [c_void_p] * 3),
     "dsa_topk_pools": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_size_t,
                                c_void_p]),
     "dsa_topk_pools_workspace_size": (c_size_t, [c_int, c_int, c_int]),
@@ -29,11 +29,11 @@ SIGNATURES = {
     "dsa_mla_selected_decode": (c_int, [c_void_p] * 5 + [c_int] * 5 + [c_float, c_int]
                                 + [c_void_p] * 3 + [c_size_t] + [c_void_p] * 2),
     "dsa_mla_selected_decode_workspace_size": (c_size_t, [c_int] * 5),
-    "dsa_select": (c_int, [c_void_p, c_void_p, c_float] + [c_void_p] * 7 + [c_int] * 9
-                   + [c_void_p] * 4 + [c_size_t] + [c_void_p] * 2),
+    "dsa_select": (c_int, [c_void_p, c_void_p, c_float, c_void_p, c_int] + [c_void_p] * 6
+                   + [c_int] * 9 + [c_void_p] * 4 + [c_size_t] + [c_void_p] * 2),
     "dsa_select_workspace_size": (c_size_t, [c_int, c_int, c_int]),
-    "dsa_select_noalloc": (c_int, [c_void_p, c_void_p, c_float] + [c_void_p] * 7 + [c_int] * 9
-                           + [c_void_p] * 5),
+    "dsa_select_noalloc": (c_int, [c_void_p, c_void_p, c_float, c_void_p, c_int]
+                           + [c_void_p] * 6 + [c_int] * 9 + [c_void_p] * 5),
     "dsa_status_string": (ctypes.c_char_p, [c_int]),
     "dsa_version": (c_int, []),
 }

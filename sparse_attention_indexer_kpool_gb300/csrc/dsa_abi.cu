@@ -58,11 +58,11 @@ int dsa_kpool_compress(const void* k, const void* gate, const uint8_t* valid, co
 }
 
 int dsa_index_scores(const void* q, const float* weights, float scale, const void* pool_keys,
-                     const int32_t* pool_start, const uint8_t* pool_valid,
+                     int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
                      const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
                      const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
                      int dtype, float* scores, int32_t* status_dev, void* stream) {
-  if (Q < 0 || B < 0 || H < 1 || P_ld < 1) return DSA_ERR_INVALID_ARG;
+  if (Q < 0 || B < 0 || H < 1 || P_ld < 1 || pool_rows < 1) return DSA_ERR_INVALID_ARG;
   if (kpool < 1 || kpool > DSA_KPOOL_MAX) return DSA_ERR_INVALID_ARG;
   if (!dtype_ok(dtype) || !(scale > 0.f) || !isfinite(scale)) return DSA_ERR_INVALID_ARG;
   if (!d_ok(D) || H > 64) return DSA_ERR_UNSUPPORTED;
@@ -77,9 +77,9 @@ int dsa_index_scores(const void* q, const float* weights, float scale, const voi
       (status_dev && !aligned(status_dev, 4)))
     return DSA_ERR_MISALIGNED;
   if (Q > 65535) return DSA_ERR_UNSUPPORTED;
-  return dsa::launch_index_scores(q, weights, scale, pool_keys, pool_start, pool_valid, n_pools,
-                                  cu_pool_cap, q_seq, q_pos, Q, B, H, D, kpool, P_ld, dtype,
-                                  scores, nullptr, status_dev, as_stream(stream));
+  return dsa::launch_index_scores(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid,
+                                  n_pools, cu_pool_cap, q_seq, q_pos, Q, B, H, D, kpool, P_ld,
+                                  dtype, scores, nullptr, status_dev, as_stream(stream));
 }
 
 size_t dsa_topk_pools_workspace_size(int Q, int P_ld, int select_k) {
@@ -126,12 +126,13 @@ size_t dsa_select_workspace_size(int Q, int P_ld, int select_k) {
 }
 
 int dsa_select(const void* q, const float* weights, float scale, const void* pool_keys,
-               const int32_t* pool_start, const uint8_t* pool_valid, const int32_t* n_pools,
+               int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
+               const int32_t* n_pools,
                const int32_t* cu_pool_cap, const int32_t* q_seq, const int32_t* q_pos, int Q,
                int B, int H, int D, int kpool, int P_ld, int select_k, int out_width, int dtype,
                float* scores, int32_t* pool_ids, int32_t* token_ids, void* workspace,
                size_t ws_bytes, int32_t* status_dev, void* stream) {
-  if (Q < 0 || B < 0 || H < 1 || P_ld < 1 || select_k < 1 || out_width < 1)
+  if (Q < 0 || B < 0 || H < 1 || P_ld < 1 || select_k < 1 || out_width < 1 || pool_rows < 1)
     return DSA_ERR_INVALID_ARG;
   if (kpool < 1 || kpool > DSA_KPOOL_MAX) return DSA_ERR_INVALID_ARG;
   if ((long long)out_width < (long long)select_k * kpool) return DSA_ERR_INVALID_ARG;
@@ -152,24 +153,19 @@ int dsa_select(const void* q, const float* weights, float scale, const void* poo
   if (!aligned(workspace, 16)) return DSA_ERR_MISALIGNED;
   if (Q > 65535) return DSA_ERR_UNSUPPORTED;
   cudaStream_t st = as_stream(stream);
-  if (dsa::index_uses_tensor_cores(H, D, dtype)) {
-    int r = dsa::launch_index_scores(q, weights, scale, pool_keys, pool_start, pool_valid,
-                                     n_pools, cu_pool_cap, q_seq, q_pos, Q, B, H, D, kpool, P_ld,
-                                     dtype, scores, dsa::topk_workspace_hist(workspace),
-                                     status_dev, st);
-    if (r != DSA_OK) return r;
-    return dsa::launch_select_after_index(scores, Q, P_ld, select_k, pool_ids, workspace,
-                                          pool_start, cu_pool_cap, q_seq, B, kpool, out_width,
-                                          token_ids, status_dev, st);
-  }
-  int r = dsa::launch_index_scores(q, weights, scale, pool_keys, pool_start, pool_valid, n_pools,
-                                   cu_pool_cap, q_seq, q_pos, Q, B, H, D, kpool, P_ld, dtype,
-                                   scores, nullptr, status_dev, st);
+  // Decode geometry: the scoring kernel also counts each query's score
+  // histogram into the workspace and the selection starts from it.  Otherwise
+  // the selection kernel builds the histogram itself.
+  const bool hist = dsa::index_fills_histogram(Q, q_seq, H, D, dtype);
+  int r = dsa::launch_index_scores(q, weights, scale, pool_keys, pool_rows, pool_start,
+                                   pool_valid, n_pools, cu_pool_cap, q_seq, q_pos, Q, B, H, D,
+                                   kpool, P_ld, dtype, scores,
+                                   hist ? dsa::topk_workspace_hist(workspace) : nullptr,
+                                   status_dev, st);
   if (r != DSA_OK) return r;
-  r = dsa::launch_topk_pools(scores, Q, P_ld, select_k, pool_ids, workspace, ws_bytes, st);
-  if (r != DSA_OK) return r;
-  return dsa::launch_expand_selection(pool_ids, pool_start, cu_pool_cap, q_seq, Q, B, select_k,
-                                      kpool, out_width, token_ids, status_dev, st);
+  return dsa::launch_select_after_index(scores, Q, P_ld, select_k, pool_ids,
+                                        hist ? workspace : nullptr, pool_start, cu_pool_cap,
+                                        q_seq, B, kpool, out_width, token_ids, status_dev, st);
 }
 
 size_t dsa_mla_selected_decode_workspace_size(int Q, int Hm, int L, int out_width, int dtype) {

@@ -172,11 +172,22 @@ int launch_kpool_compress(const void* k, const void* gate, const uint8_t* valid,
                           int dtype, void* pool_keys, int32_t* pool_start, uint8_t* pool_valid,
                           int32_t* n_pools, int32_t* status_dev, cudaStream_t stream);
 int launch_index_scores(const void* q, const float* weights, float scale, const void* pool_keys,
-                        const int32_t* pool_start, const uint8_t* pool_valid,
+                        int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
                         const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
                         const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
                         int dtype, float* scores, uint32_t* score_hist, int32_t* status_dev,
                         cudaStream_t stream);
+// tcgen05 index kernel: queries per key tile (1 or 8), 0 when Q does not fit it
+int umma_index_group(int Q, const int32_t* q_seq);
+int launch_index_scores_umma(const void* q, const float* weights, float scale,
+                             const void* pool_keys, int pool_rows, const int32_t* pool_start,
+                             const uint8_t* pool_valid, const int32_t* n_pools,
+                             const int32_t* cu_pool_cap, const int32_t* q_seq,
+                             const int32_t* q_pos, int Q, int B, int kpool, int P_ld,
+                             float* scores, uint32_t* hist, int32_t* status_dev,
+                             cudaStream_t stream);
+// true when launch_index_scores also counts the per-query score histogram
+bool index_fills_histogram(int Q, const int32_t* q_seq, int H, int D, int dtype);
 size_t topk_workspace_size(int Q, int P_ld, int select_k);
 size_t select_workspace_size(int Q, int P_ld, int select_k);
 uint32_t* topk_workspace_hist(void* workspace);

@@ -1,0 +1,588 @@
+// index_scores on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// score[q, p] = sum_h w[q, h] * max(0, scale * <q[q, h, :], key[p, :]>)   (module
+// glm5next_dsa::tp, "Why the indexer is REPLICATED": a plain sum over heads of
+// weights[h] * relu(scale * dot); module glm5next_dsa, "Shape of the pipeline":
+// [Q, P] scores, -inf where a pool is not a candidate).  Geometry: bf16 keys and
+// queries, 32 heads, head_dim 128.
+//
+// Swap-AB contraction: A = 128 pool keys (M = 128 -> TMEM lanes), B = G queries
+// x 32 heads (N = 32 G -> TMEM columns), K = 128 channels in 8 steps of 16.
+// G = 1 serves decode (one query per sequence, any q_seq); G = 8 serves a chunk
+// of queries on one sequence (q_seq absent), the dense [Q*32, 128] x [128, P]
+// prefill contraction, where one key tile feeds eight queries.
+//
+// One persistent CTA per SM owns a balanced contiguous range of the flattened
+// (query group, 128-pool tile) space.  Warp roles:
+//   warp 0     TMA producer: per query group, the query block (B, two 64-channel
+//              boxes, 128-byte swizzle) and its head weights; then the group's
+//              key tiles (A, two boxes of 128 rows x 64 channels) into a ring;
+//   warp 1     MMA issuer: one thread issues 8 tcgen05.mma per tile into one of
+//              two TMEM accumulators, then commits to the ring slot's "empty"
+//              barrier and the accumulator's "full" barrier;
+//   warps 2-9  epilogue: tcgen05.ld of the accumulator rows (a warp reads the 32
+//              TMEM lanes of its quarter), relu / weight / head sum in registers,
+//              -0 -> +0, candidate mask, coalesced score stores and (decode) a
+//              4096-bin histogram of the score keys' top 12 bits for the top-k
+//              that follows.  For G = 1 the two halves of the epilogue take
+//              alternate tiles (one accumulator each); for G = 8 each half takes
+//              four of the eight queries of every tile.
+// Every mbarrier wait is bounded.  On a timeout the kernel flags DSA_DEV_TIMEOUT,
+// stops issuing work, waits (bounded) for its own copies and MMAs in flight and
+// frees its TMEM before it returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "dsa_internal.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kD = 128, kH = 32;
+constexpr int kBM = 128;                       // pools per tile (MMA M)
+constexpr int kABytes = kBM * kD * 2;          // 32 KB key tile
+constexpr int kHalfA = kBM * 64 * 2;           // one 64-channel box of it
+constexpr int kEpiWarps = 8;
+constexpr int kThreadsU = (2 + kEpiWarps) * 32;
+constexpr int kHistBins = 4096;
+constexpr int kSmemMax = 227 * 1024;
+
+template <int G>
+struct Cfg {
+  static constexpr int N = 32 * G;                         // MMA N: queries x heads
+  static constexpr int kStages = G == 1 ? 4 : 3;           // key tile ring
+  static constexpr int kBSlots = G == 1 ? 2 : 1;           // query blocks in flight
+  static constexpr int kBBytes = N * kD * 2;
+  static constexpr int kTmemCols = 2 * N < 32 ? 32 : 2 * N;  // two accumulators
+  static constexpr int kTileWarps = G == 1 ? 4 : 8;        // epilogue warps per tile
+  static_assert((2 * N & (2 * N - 1)) == 0, "TMEM allocation must be a power of two");
+};
+
+struct Ctl {
+  uint64_t full[4], empty[4];      // key tile ring
+  uint64_t bfull[2], bempty[2];    // query block slots
+  uint64_t tfull[2], tempty[2];    // TMEM accumulators
+  uint64_t done;                   // all MMAs of the CTA retired
+  uint32_t tmem_base;
+  int abort;
+  int scan_warp[kThreadsU / 32];   // tile prefix scan: per-warp totals and carry
+  int scan_carry;
+};
+
+// Shared-memory layout (offsets from a 1 KB-aligned base): the swizzled tiles
+// first, each on a 1 KB boundary as the 128-byte swizzle atoms require.
+template <int G>
+struct Layout {
+  static constexpr size_t a = 0;
+  static constexpr size_t b = (size_t)Cfg<G>::kStages * kABytes;
+  static constexpr size_t ctl = b + (size_t)Cfg<G>::kBSlots * Cfg<G>::kBBytes;
+  static constexpr size_t w = ctl + ((sizeof(Ctl) + 15) & ~size_t(15));
+  static constexpr size_t hist = w + (size_t)Cfg<G>::kBSlots * G * kH * 4;
+  static constexpr size_t prefix = hist + (G == 1 ? (size_t)kHistBins * 4 : 0);
+  static size_t bytes(int n_groups) { return 1024 + prefix + (size_t)(n_groups + 1) * 4; }
+};
+
+struct QMeta {
+  long long base;  // first cache row of the query's sequence
+  int n_cand;      // pools [0, n_cand) may be candidates
+  int pos;         // query position (causal rule) or INT_MAX
+  int valid;       // the query exists and its sequence id is in range
+};
+
+// Candidate range of query qi (as the other index kernels define it).
+__device__ __forceinline__ QMeta qmeta(int qi, int Q, const int32_t* q_seq, const int32_t* q_pos,
+                                       const int32_t* n_pools, const int32_t* cu_pool_cap,
+                                       const int32_t* pool_start, int B, int kpool, int P_ld,
+                                       int32_t* status, bool report) {
+  QMeta m{0, 0, 0x7fffffff, 0};
+  if (qi >= Q) return m;
+  const int b = q_seq ? q_seq[qi] : 0;
+  if (b < 0 || b >= B) {
+    if (report) flag(status, DSA_DEV_BAD_QSEQ);
+    return m;
+  }
+  m.valid = 1;
+  m.base = cu_pool_cap[b];
+  const int cap = cu_pool_cap[b + 1] - cu_pool_cap[b];
+  const int np = n_pools[b];
+  int P = min(np, min(cap, P_ld));
+  if (np > P && report) flag(status, DSA_DEV_POOL_RANGE);
+  P = max(P, 0);
+  if (q_pos != nullptr && P > 0) {
+    // pool p is complete at pos when t0 + p*kpool + kpool - 1 <= pos
+    m.pos = q_pos[qi];
+    const long long t0 = pool_start[m.base];
+    const long long nv = (m.pos - t0 + 1) >= 0 ? (m.pos - t0 + 1) / kpool : 0;
+    P = (int)min((long long)P, nv);
+  }
+  m.n_cand = P;
+  return m;
+}
+
+// ---- tcgen05 / TMA wrappers ------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// Shared-memory matrix descriptor: K-major operand with the 128-byte swizzle
+// (rows of 128 bytes, 8-row atoms 1024 bytes apart), sm_100 descriptor version.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(kBM >> 4) << 24);
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 32 consecutive fp32 columns of the warp's 32 TMEM lanes (one lane per thread).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+}
+// Bounded wait that also gives up at once after another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              int32_t* status) {
+  if (*abort) return false;
+  if (mbar_wait_bounded(bar, parity)) return true;
+  flag(status, DSA_DEV_TIMEOUT);
+  *abort = 1;
+  return false;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreadsU, 1)
+    index_scores_umma_kernel(const __grid_constant__ CUtensorMap tmap_keys,
+                             const __grid_constant__ CUtensorMap tmap_q,
+                             const float* __restrict__ wts, float scale,
+                             const int32_t* __restrict__ pool_start,
+                             const uint8_t* __restrict__ pool_valid,
+                             const int32_t* __restrict__ n_pools,
+                             const int32_t* __restrict__ cu_pool_cap,
+                             const int32_t* __restrict__ q_seq, const int32_t* __restrict__ q_pos,
+                             int Q, int B, int kpool, int P_ld, float* __restrict__ scores,
+                             uint32_t* __restrict__ hist, int32_t* status) {
+  using C = Cfg<G>;
+  using LY = Layout<G>;
+  constexpr int N = C::N;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char* sbase = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  Ctl& ctl = *reinterpret_cast<Ctl*>(sbase + LY::ctl);
+  float* s_w = reinterpret_cast<float*>(sbase + LY::w);
+  uint32_t* s_hist = reinterpret_cast<uint32_t*>(sbase + LY::hist);
+  int* s_prefix = reinterpret_cast<int*>(sbase + LY::prefix);
+  volatile int* abort = &ctl.abort;
+  const bool use_hist = G == 1 && hist != nullptr;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_groups = (Q + G - 1) / G;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&ctl.full[s], 1);
+      mbar_init(&ctl.empty[s], 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&ctl.bfull[j], 1);
+      mbar_init(&ctl.bempty[j], 1 + kEpiWarps);  // the MMA commit + every epilogue warp
+      mbar_init(&ctl.tfull[j], 1);
+      mbar_init(&ctl.tempty[j], C::kTileWarps);
+    }
+    mbar_init(&ctl.done, 1);
+    fence_mbar_init();
+    ctl.abort = 0;
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_keys))
+                 : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_q))
+                 : "memory");
+  }
+  if (warp == 1) {  // two accumulators of N fp32 columns
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ctl.tmem_base)),
+                 "n"(C::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  if (use_hist)
+    for (int i = threadIdx.x; i < kHistBins; i += kThreadsU) s_hist[i] = 0;
+  pdl_wait();  // the pool cache may come from the kernel just before
+  pdl_launch_dependents();
+
+  // ---- tiles per query group (its widest candidate range) and their prefix sum
+  {
+    int* s_warp = ctl.scan_warp;
+    int& s_carry = ctl.scan_carry;
+    if (threadIdx.x == 0) {
+      s_prefix[0] = 0;
+      s_carry = 0;
+    }
+    __syncthreads();
+    for (int c0 = 0; c0 < n_groups; c0 += kThreadsU) {
+      const int gi = c0 + threadIdx.x;
+      int n = 0;
+      if (gi < n_groups) {
+        int mx = 0;
+        for (int u = 0; u < G; ++u) {
+          const QMeta m = qmeta(gi * G + u, Q, q_seq, q_pos, n_pools, cu_pool_cap, pool_start, B,
+                                kpool, P_ld, status, blockIdx.x == 0);
+          mx = max(mx, m.n_cand);
+        }
+        n = (mx + kBM - 1) / kBM;
+      }
+      int x = n;  // inclusive warp scan
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) s_warp[warp] = x;
+      __syncthreads();
+      int off = s_carry;
+      for (int w = 0; w < warp; ++w) off += s_warp[w];
+      if (gi < n_groups) s_prefix[gi + 1] = off + x;
+      __syncthreads();
+      if (threadIdx.x == kThreadsU - 1) s_carry = off + x;
+      __syncthreads();
+    }
+  }
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  const long long NT = s_prefix[n_groups];
+  const long long t_lo = NT * blockIdx.x / gridDim.x;
+  const long long t_hi = NT * (blockIdx.x + 1) / gridDim.x;
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      uint32_t a_par = 0, a_used = 0;  // per ring slot: parity of its next fill, ever filled
+      uint32_t b_par = 0, b_used = 0;  // the same for the query block slots
+      int stage = 0, gi = 0, seg = 0;
+      for (long long t = t_lo; t < t_hi && !*abort; ++seg) {
+        while (s_prefix[gi + 1] <= t) ++gi;
+        const long long seg_hi = min(t_hi, (long long)s_prefix[gi + 1]);
+        const int slot = seg % C::kBSlots;
+        if (((b_used >> slot) & 1) &&
+            !wait_or_abort(&ctl.bempty[slot], ((b_par >> slot) & 1) ^ 1, abort, status))
+          break;
+        const QMeta m0 = qmeta(gi * G, Q, q_seq, q_pos, n_pools, cu_pool_cap, pool_start, B,
+                               kpool, P_ld, status, false);
+        const int nq = min(G, Q - gi * G);
+        unsigned char* bt = sbase + LY::b + (size_t)slot * C::kBBytes;
+        mbar_arrive_expect_tx(&ctl.bfull[slot], C::kBBytes + nq * kH * 4);
+        tma_load_2d(bt, &tmap_q, 0, gi * N, &ctl.bfull[slot]);
+        tma_load_2d(bt + N * 128, &tmap_q, 64, gi * N, &ctl.bfull[slot]);
+        bulk_g2s(s_w + slot * G * kH, wts + (long long)gi * G * kH, nq * kH * 4,
+                 &ctl.bfull[slot]);
+        b_par ^= 1u << slot;
+        b_used |= 1u << slot;
+        for (; t < seg_hi; ++t) {
+          if (((a_used >> stage) & 1) &&
+              !wait_or_abort(&ctl.empty[stage], ((a_par >> stage) & 1) ^ 1, abort, status))
+            break;
+          const int row = (int)(m0.base + (t - s_prefix[gi]) * kBM);
+          unsigned char* at = sbase + LY::a + (size_t)stage * kABytes;
+          mbar_arrive_expect_tx(&ctl.full[stage], kABytes);
+          tma_load_2d(at, &tmap_keys, 0, row, &ctl.full[stage]);
+          tma_load_2d(at + kHalfA, &tmap_keys, 64, row, &ctl.full[stage]);
+          a_par ^= 1u << stage;
+          a_used |= 1u << stage;
+          stage = stage + 1 == C::kStages ? 0 : stage + 1;
+        }
+        if (t < seg_hi) break;  // aborted inside the segment
+      }
+      // Never leave a copy in flight: wait for the last fill of every slot.
+      for (int s = 0; s < C::kStages; ++s)
+        if ((a_used >> s) & 1) mbar_wait_bounded(&ctl.full[s], ((a_par >> s) & 1) ^ 1);
+      for (int s = 0; s < C::kBSlots; ++s)
+        if ((b_used >> s) & 1) mbar_wait_bounded(&ctl.bfull[s], ((b_par >> s) & 1) ^ 1);
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(N);
+      uint32_t a_par = 0;  // per ring slot: parity of its next "full" phase
+      int stage = 0, gi = 0, seg = 0;
+      long long tc = 0;    // tiles issued by this CTA
+      for (long long t = t_lo; t < t_hi && !*abort; ++seg) {
+        while (s_prefix[gi + 1] <= t) ++gi;
+        const long long seg_hi = min(t_hi, (long long)s_prefix[gi + 1]);
+        const int slot = seg % C::kBSlots;
+        if (!wait_or_abort(&ctl.bfull[slot], (seg / C::kBSlots) & 1, abort, status)) break;
+        const uint32_t b_lo = smem_u32(sbase + LY::b + (size_t)slot * C::kBBytes);
+        const uint32_t b_hi = b_lo + N * 128;
+        for (; t < seg_hi; ++t, ++tc) {
+          const int acc = (int)(tc & 1);
+          if (!wait_or_abort(&ctl.full[stage], (a_par >> stage) & 1, abort, status)) break;
+          a_par ^= 1u << stage;
+          if (tc >= 2 &&  // the epilogue has drained this accumulator's previous tile
+              !wait_or_abort(&ctl.tempty[acc], (uint32_t)((tc >> 1) - 1) & 1, abort, status))
+            break;
+          tc_fence_after();
+          const uint32_t a_lo = smem_u32(sbase + LY::a + (size_t)stage * kABytes);
+          const uint32_t a_hi = a_lo + kHalfA;
+          const uint32_t d = tmem + (uint32_t)(acc * N);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (uint32_t)(kk & 3) * 32;  // 16 channels = 32 bytes
+            umma_bf16(d, sw128_desc((kk < 4 ? a_lo : a_hi) + off),
+                      sw128_desc((kk < 4 ? b_lo : b_hi) + off), idesc, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&ctl.empty[stage]);  // the key tile may be refilled
+          umma_commit(&ctl.tfull[acc]);    // the accumulator is ready
+          stage = stage + 1 == C::kStages ? 0 : stage + 1;
+        }
+        if (t < seg_hi) break;
+        umma_commit(&ctl.bempty[slot]);  // no more MMAs read this query block
+      }
+      umma_commit(&ctl.done);  // retire every MMA before TMEM is freed
+      mbar_wait_bounded(&ctl.done, 0);
+    }
+  } else {
+    // ================= epilogue =================
+    constexpr int GH = G == 1 ? 1 : G / 2;  // queries per warp of each tile
+    const int ew = warp - 2;                // 0..7
+    const int quarter = warp & 3;           // the TMEM lanes this warp may read
+    const int half = ew >> 2;
+    const int r = quarter * 32 + lane;      // pool row within the tile
+    const int qw0 = G == 1 ? 0 : half * GH; // this warp's first query of the group
+    int gi = 0, seg = 0;
+    long long tc = 0;
+    for (long long t = t_lo; t < t_hi; ++seg) {
+      while (s_prefix[gi + 1] <= t) ++gi;
+      const long long seg_hi = min(t_hi, (long long)s_prefix[gi + 1]);
+      const int slot = seg % C::kBSlots;
+      QMeta mq[GH];
+      int ncmax = 0;
+#pragma unroll
+      for (int u = 0; u < GH; ++u) {
+        mq[u] = qmeta(gi * G + qw0 + u, Q, q_seq, q_pos, n_pools, cu_pool_cap, pool_start, B,
+                      kpool, P_ld, status, false);
+        ncmax = max(ncmax, mq[u].n_cand);
+      }
+      const long long base = mq[0].base;  // every query of a group reads one sequence
+      const bool b_ok = wait_or_abort(&ctl.bfull[slot], (seg / C::kBSlots) & 1, abort, status);
+      const float* wq = s_w + slot * G * kH;
+      for (; t < seg_hi; ++t, ++tc) {
+        const int acc = (int)(tc & 1);
+        if (G == 1 && acc != half) continue;  // the other half's tile
+        const int p = (int)(t - s_prefix[gi]) * kBM + r;
+        // candidate metadata first: its latency hides behind the accumulator wait
+        uint8_t pv = 0;
+        int ps = 0;
+        if (p < ncmax) {
+          pv = pool_valid[base + p];
+          if (q_pos != nullptr) ps = pool_start[base + p];
+        }
+        if (!b_ok || !wait_or_abort(&ctl.tfull[acc], (uint32_t)(tc >> 1) & 1, abort, status))
+          continue;  // keep walking so that every warp meets the same barriers
+        tc_fence_after();
+        const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N);
+#pragma unroll
+        for (int u = 0; u < GH; ++u) {
+          float v[32];
+          tmem_ld32(tb + (uint32_t)((qw0 + u) * kH), v);
+          const float4* w4 = reinterpret_cast<const float4*>(wq + (qw0 + u) * kH);
+          float sc = 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 w = w4[i];
+            sc = fmaf(w.x, fmaxf(scale * v[4 * i + 0], 0.f), sc);
+            sc = fmaf(w.y, fmaxf(scale * v[4 * i + 1], 0.f), sc);
+            sc = fmaf(w.z, fmaxf(scale * v[4 * i + 2], 0.f), sc);
+            sc = fmaf(w.w, fmaxf(scale * v[4 * i + 3], 0.f), sc);
+          }
+          if (sc == 0.f) sc = 0.f;  // -0 -> +0
+          const QMeta& m = mq[u];
+          if (m.valid && p < P_ld) {
+            bool cand = p < m.n_cand && pv != 0;
+            if (cand && q_pos != nullptr) cand = ps + kpool - 1 <= m.pos;
+            scores[(long long)(gi * G + qw0 + u) * P_ld + p] = cand ? sc : -INFINITY;
+            if (use_hist && cand) atomicAdd(&s_hist[score_key(sc) >> 20], 1u);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive1(&ctl.tempty[acc]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(&ctl.bempty[slot]);  // done with this query block's weights
+      if (use_hist) {  // flush this query's histogram
+        epi_bar();
+        uint32_t* gh = hist + (size_t)gi * kHistBins;
+        for (int i = ew * 32 + lane; i < kHistBins; i += kEpiWarps * 32) {
+          const uint32_t v = s_hist[i];
+          if (v) {
+            atomicAdd(&gh[i], v);
+            s_hist[i] = 0;
+          }
+        }
+        epi_bar();
+      }
+    }
+  }
+
+  // Fill the rest of each row (pools past every tile of its group) with -inf.
+  if (n_groups >= (int)gridDim.x) {
+    for (int gi = blockIdx.x; gi < n_groups; gi += gridDim.x) {
+      const long long start = (long long)(s_prefix[gi + 1] - s_prefix[gi]) * kBM;
+      for (int u = 0; u < G && gi * G + u < Q; ++u) {
+        float* row = scores + (long long)(gi * G + u) * P_ld;
+        for (long long i = start + threadIdx.x; i < P_ld; i += kThreadsU) row[i] = -INFINITY;
+      }
+    }
+  } else {
+    const long long gtid = (long long)blockIdx.x * kThreadsU + threadIdx.x;
+    const long long gstride = (long long)gridDim.x * kThreadsU;
+    for (int gi = 0; gi < n_groups; ++gi) {
+      const long long start = (long long)(s_prefix[gi + 1] - s_prefix[gi]) * kBM;
+      for (int u = 0; u < G && gi * G + u < Q; ++u) {
+        float* row = scores + (long long)(gi * G + u) * P_ld;
+        for (long long i = start + gtid; i < P_ld; i += gstride) row[i] = -INFINITY;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "n"(C::kTmemCols)
+                 : "memory");
+  }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// [rows, 128] bf16 row-major matrix, boxes of 64 channels x box_rows rows,
+// 128-byte swizzle; rows at or beyond `rows` read as zeros.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int G>
+int launch_g(const void* q, const float* weights, float scale, const void* pool_keys,
+             int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
+             const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
+             const int32_t* q_pos, int Q, int B, int kpool, int P_ld, float* scores,
+             uint32_t* hist, int32_t* status, cudaStream_t stream) {
+  const size_t smem = Layout<G>::bytes((Q + G - 1) / G);
+  if (smem > (size_t)kSmemMax) return DSA_ERR_UNSUPPORTED;
+  CUtensorMap mk, mq;
+  if (!make_map(&mk, pool_keys, (uint64_t)pool_rows, kBM)) return DSA_ERR_CUDA;
+  if (!make_map(&mq, q, (uint64_t)Q * kH, 32 * G)) return DSA_ERR_CUDA;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(index_scores_umma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         kSmemMax);
+  });
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kNumSMs, 1, 1);
+  cfg.blockDim = dim3(kThreadsU, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, index_scores_umma_kernel<G>, mk, mq, weights,
+                                           scale, pool_start, pool_valid, n_pools, cu_pool_cap,
+                                           q_seq, q_pos, Q, B, kpool, P_ld, scores, hist, status);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace
+
+int umma_index_group(int Q, const int32_t* q_seq) {
+  // eight queries share every key tile when they all read one sequence
+  const int G = (q_seq == nullptr && Q >= 64) ? 8 : 1;
+  const size_t smem = G == 8 ? Layout<8>::bytes((Q + 7) / 8) : Layout<1>::bytes(Q);
+  return smem <= (size_t)kSmemMax ? G : 0;
+}
+
+int launch_index_scores_umma(const void* q, const float* weights, float scale,
+                             const void* pool_keys, int pool_rows, const int32_t* pool_start,
+                             const uint8_t* pool_valid, const int32_t* n_pools,
+                             const int32_t* cu_pool_cap, const int32_t* q_seq,
+                             const int32_t* q_pos, int Q, int B, int kpool, int P_ld,
+                             float* scores, uint32_t* hist, int32_t* status_dev,
+                             cudaStream_t stream) {
+  const int G = umma_index_group(Q, q_seq);
+  if (G == 8)
+    return launch_g<8>(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid, n_pools,
+                       cu_pool_cap, q_seq, q_pos, Q, B, kpool, P_ld, scores, nullptr,
+                       status_dev, stream);
+  if (G == 1)
+    return launch_g<1>(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid, n_pools,
+                       cu_pool_cap, q_seq, q_pos, Q, B, kpool, P_ld, scores, hist, status_dev,
+                       stream);
+  return DSA_ERR_UNSUPPORTED;
+}
+
+}  // namespace dsa

@@ -59,14 +59,15 @@ inline bool aligned(const void* p, size_t a) {
 }  // namespace
 
 extern "C" int dsa_select_noalloc(const void* q, const float* weights, float scale,
-                                  const void* pool_keys, const int32_t* pool_start,
+                                  const void* pool_keys, int pool_rows,
+                                  const int32_t* pool_start,
                                   const uint8_t* pool_valid, const int32_t* n_pools,
                                   const int32_t* cu_pool_cap, const int32_t* q_seq,
                                   const int32_t* q_pos, int Q, int B, int H, int D, int kpool,
                                   int P_ld, int select_k, int out_width, int dtype, float* scores,
                                   int32_t* pool_ids, int32_t* token_ids, int32_t* status_dev,
                                   void* stream) {
-  if (Q < 0 || B < 0 || H < 1 || P_ld < 1 || select_k < 1 || out_width < 1)
+  if (Q < 0 || B < 0 || H < 1 || P_ld < 1 || select_k < 1 || out_width < 1 || pool_rows < 1)
     return DSA_ERR_INVALID_ARG;
   if (kpool < 1 || kpool > DSA_KPOOL_MAX) return DSA_ERR_INVALID_ARG;
   if ((long long)out_width < (long long)select_k * kpool) return DSA_ERR_INVALID_ARG;
@@ -85,29 +86,23 @@ extern "C" int dsa_select_noalloc(const void* q, const float* weights, float sca
       !aligned(pool_ids, 4) || !aligned(token_ids, 4) || (q_seq && !aligned(q_seq, 4)) ||
       (q_pos && !aligned(q_pos, 4)) || (status_dev && !aligned(status_dev, 4)))
     return DSA_ERR_MISALIGNED;
-  uint32_t* hist = nullptr;
-  int r = scratch_for_current_device(&hist);
-  if (r != DSA_OK) return r;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (dsa::index_uses_tensor_cores(H, D, dtype)) {
+  uint32_t* hist = nullptr;
+  int r;
+  if (dsa::index_fills_histogram(Q, q_seq, H, D, dtype)) {
+    r = scratch_for_current_device(&hist);
+    if (r != DSA_OK) return r;
     // the histogram must start at zero: clear this call's share of the array
     if (cudaMemsetAsync(hist, 0, (size_t)Q * kHistBins * sizeof(uint32_t), st) != cudaSuccess)
       return DSA_ERR_CUDA;
-    r = dsa::launch_index_scores(q, weights, scale, pool_keys, pool_start, pool_valid, n_pools,
-                                 cu_pool_cap, q_seq, q_pos, Q, B, H, D, kpool, P_ld, dtype,
-                                 scores, hist, status_dev, st);
-    if (r != DSA_OK) return r;
-    return dsa::launch_select_after_index(scores, Q, P_ld, select_k, pool_ids, hist, pool_start,
-                                          cu_pool_cap, q_seq, B, kpool, out_width, token_ids,
-                                          status_dev, st);
   }
-  // other geometries keep their histogram on chip: no scratch is touched
-  r = dsa::launch_index_scores(q, weights, scale, pool_keys, pool_start, pool_valid, n_pools,
-                               cu_pool_cap, q_seq, q_pos, Q, B, H, D, kpool, P_ld, dtype, scores,
-                               nullptr, status_dev, st);
+  // without the scoring kernel's histogram the selection kernel builds its
+  // own on chip: no scratch is touched
+  r = dsa::launch_index_scores(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid,
+                               n_pools, cu_pool_cap, q_seq, q_pos, Q, B, H, D, kpool, P_ld, dtype,
+                               scores, hist, status_dev, st);
   if (r != DSA_OK) return r;
-  r = dsa::launch_topk_pools(scores, Q, P_ld, select_k, pool_ids, nullptr, 0, st);
-  if (r != DSA_OK) return r;
-  return dsa::launch_expand_selection(pool_ids, pool_start, cu_pool_cap, q_seq, Q, B, select_k,
-                                      kpool, out_width, token_ids, status_dev, st);
+  return dsa::launch_select_after_index(scores, Q, P_ld, select_k, pool_ids, hist, pool_start,
+                                        cu_pool_cap, q_seq, B, kpool, out_width, token_ids,
+                                        status_dev, st);
 }

@@ -52,6 +52,12 @@ def _stream(stream):
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _pool_rows(pool_keys) -> int:
+    if pool_keys.dim() != 2:
+        raise ValueError("pool_keys must be [pool_rows, D]")
+    return pool_keys.shape[0]
+
+
 def _check(fn, code):
     if code != 0:
         raise DsaError(fn, code)
@@ -80,7 +86,8 @@ def dsa_index_scores(q, weights, scale, pool_keys, pool_start, pool_valid, n_poo
     act = q.dtype
     code = _lib.load().dsa_index_scores(
         _ptr(q, act, "q"), _ptr(weights, torch.float32, "weights"), float(scale),
-        _ptr(pool_keys, act, "pool_keys"), _ptr(pool_start, torch.int32, "pool_start"),
+        _ptr(pool_keys, act, "pool_keys"), _pool_rows(pool_keys),
+        _ptr(pool_start, torch.int32, "pool_start"),
         _ptr(pool_valid, torch.uint8, "pool_valid"), _ptr(n_pools, torch.int32, "n_pools"),
         _ptr(cu_pool_cap, torch.int32, "cu_pool_cap"), _ptr(q_seq, torch.int32, "q_seq"),
         _ptr(q_pos, torch.int32, "q_pos"), Q, cu_pool_cap.numel() - 1, H, D, int(kpool),
@@ -145,7 +152,8 @@ def dsa_select(q, weights, scale, pool_keys, pool_start, pool_valid, n_pools, cu
     act = q.dtype
     code = _lib.load().dsa_select(
         _ptr(q, act, "q"), _ptr(weights, torch.float32, "weights"), float(scale),
-        _ptr(pool_keys, act, "pool_keys"), _ptr(pool_start, torch.int32, "pool_start"),
+        _ptr(pool_keys, act, "pool_keys"), _pool_rows(pool_keys),
+        _ptr(pool_start, torch.int32, "pool_start"),
         _ptr(pool_valid, torch.uint8, "pool_valid"), _ptr(n_pools, torch.int32, "n_pools"),
         _ptr(cu_pool_cap, torch.int32, "cu_pool_cap"), _ptr(q_seq, torch.int32, "q_seq"),
         _ptr(q_pos, torch.int32, "q_pos"), Q, cu_pool_cap.numel() - 1, H, D, int(kpool),
@@ -167,7 +175,8 @@ def dsa_select_noalloc(q, weights, scale, pool_keys, pool_start, pool_valid, n_p
     act = q.dtype
     code = _lib.load().dsa_select_noalloc(
         _ptr(q, act, "q"), _ptr(weights, torch.float32, "weights"), float(scale),
-        _ptr(pool_keys, act, "pool_keys"), _ptr(pool_start, torch.int32, "pool_start"),
+        _ptr(pool_keys, act, "pool_keys"), _pool_rows(pool_keys),
+        _ptr(pool_start, torch.int32, "pool_start"),
         _ptr(pool_valid, torch.uint8, "pool_valid"), _ptr(n_pools, torch.int32, "n_pools"),
         _ptr(cu_pool_cap, torch.int32, "cu_pool_cap"), _ptr(q_seq, torch.int32, "q_seq"),
         _ptr(q_pos, torch.int32, "q_pos"), Q, cu_pool_cap.numel() - 1, H, D, int(kpool),

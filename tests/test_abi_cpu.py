@@ -74,10 +74,11 @@ def test_compress_validation(lib):
 
 
 def scores_call(lib, **kw):
-    a = dict(q=A, w=A, scale=0.088, pk=A, ps=A, pv=A, np_=A, cap=A, qs=A, qp=None, Q=4, B=4, H=32,
-             D=128, kpool=4, P_ld=64, dtype=0, out=A, st=None, stream=None)
+    a = dict(q=A, w=A, scale=0.088, pk=A, rows=256, ps=A, pv=A, np_=A, cap=A, qs=A, qp=None, Q=4,
+             B=4, H=32, D=128, kpool=4, P_ld=64, dtype=0, out=A, st=None, stream=None)
     a.update(kw)
-    return lib.dsa_index_scores(a["q"], a["w"], a["scale"], a["pk"], a["ps"], a["pv"], a["np_"],
+    return lib.dsa_index_scores(a["q"], a["w"], a["scale"], a["pk"], a["rows"], a["ps"], a["pv"],
+                                a["np_"],
                                 a["cap"], a["qs"], a["qp"], a["Q"], a["B"], a["H"], a["D"],
                                 a["kpool"], a["P_ld"], a["dtype"], a["out"], a["st"], a["stream"])
 
@@ -91,6 +92,7 @@ def test_index_scores_validation(lib):
     assert scores_call(lib, qp=A, ps=None) == ERR["DSA_ERR_INVALID_ARG"]   # causal needs starts
     assert scores_call(lib, q=A + 4) == ERR["DSA_ERR_MISALIGNED"]
     assert scores_call(lib, P_ld=0) == ERR["DSA_ERR_INVALID_ARG"]
+    assert scores_call(lib, rows=0) == ERR["DSA_ERR_INVALID_ARG"]      # empty pool cache
     assert scores_call(lib, Q=0) == ERR["DSA_OK"]
 
 
@@ -135,7 +137,8 @@ def test_select_validation(lib):
     f = lib.dsa_select
     ws = lib.dsa_select_workspace_size(4, 1000, 16)
     assert ws > 0
-    args = lambda **kw: [kw.get("q", A), A, kw.get("scale", 0.1), A, A, A, A, A, A, None,
+    args = lambda **kw: [kw.get("q", A), A, kw.get("scale", 0.1), A, kw.get("rows", 256),
+                         A, A, A, A, A, None,
                          kw.get("Q", 4), 4, 32, 128, kw.get("kpool", 4), 1000,
                          kw.get("k", 16), kw.get("W", 64), 0, A, A, A, kw.get("ws", A),
                          kw.get("wsb", ws), None, None]
@@ -145,6 +148,7 @@ def test_select_validation(lib):
     assert f(*args(wsb=ws - 1)) == ERR["DSA_ERR_WORKSPACE"]
     assert f(*args(ws=None)) == ERR["DSA_ERR_WORKSPACE"]
     assert f(*args(q=A + 2)) == ERR["DSA_ERR_MISALIGNED"]
+    assert f(*args(rows=0)) == ERR["DSA_ERR_INVALID_ARG"]
     assert f(*args(Q=0)) == ERR["DSA_OK"]
 
 
