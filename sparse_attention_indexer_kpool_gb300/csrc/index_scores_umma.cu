@@ -48,6 +48,7 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreadsU = (2 + kEpiWarps) * 32;
 constexpr int kHistBins = 4096;
 constexpr int kSmemMax = 227 * 1024;
+constexpr int kBaseCache = 4096;               // groups whose cache base is kept on chip
 
 template <int G>
 struct Cfg {
@@ -80,8 +81,11 @@ struct Layout {
   static constexpr size_t ctl = b + (size_t)Cfg<G>::kBSlots * Cfg<G>::kBBytes;
   static constexpr size_t w = ctl + ((sizeof(Ctl) + 15) & ~size_t(15));
   static constexpr size_t hist = w + (size_t)Cfg<G>::kBSlots * G * kH * 4;
-  static constexpr size_t prefix = hist + (G == 1 ? (size_t)kHistBins * 4 : 0);
-  static size_t bytes(int n_groups) { return 1024 + prefix + (size_t)(n_groups + 1) * 4; }
+  static constexpr size_t base = hist + (G == 1 ? (size_t)kHistBins * 4 : 0);
+  __host__ __device__ static size_t prefix(int n_groups) {
+    return base + (size_t)(n_groups < kBaseCache ? n_groups : kBaseCache) * 4;
+  }
+  static size_t bytes(int n_groups) { return 1024 + prefix(n_groups) + (size_t)(n_groups + 1) * 4; }
 };
 
 struct QMeta {
@@ -214,12 +218,13 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   Ctl& ctl = *reinterpret_cast<Ctl*>(sbase + LY::ctl);
   float* s_w = reinterpret_cast<float*>(sbase + LY::w);
   uint32_t* s_hist = reinterpret_cast<uint32_t*>(sbase + LY::hist);
-  int* s_prefix = reinterpret_cast<int*>(sbase + LY::prefix);
+  const int n_groups = (Q + G - 1) / G;
+  int* s_base = reinterpret_cast<int*>(sbase + LY::base);  // first cache row of group gi
+  int* s_prefix = reinterpret_cast<int*>(sbase + LY::prefix(n_groups));
   volatile int* abort = &ctl.abort;
   const bool use_hist = G == 1 && hist != nullptr;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_groups = (Q + G - 1) / G;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -271,6 +276,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           const QMeta m = qmeta(gi * G + u, Q, q_seq, q_pos, n_pools, cu_pool_cap, pool_start, B,
                                 kpool, P_ld, status, blockIdx.x == 0);
           mx = max(mx, m.n_cand);
+          if (u == 0 && gi < kBaseCache) s_base[gi] = (int)m.base;
         }
         n = (mx + kBM - 1) / kBM;
       }
@@ -309,8 +315,10 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         if (((b_used >> slot) & 1) &&
             !wait_or_abort(&ctl.bempty[slot], ((b_par >> slot) & 1) ^ 1, abort, status))
           break;
-        const QMeta m0 = qmeta(gi * G, Q, q_seq, q_pos, n_pools, cu_pool_cap, pool_start, B,
-                               kpool, P_ld, status, false);
+        const long long base0 =
+            gi < kBaseCache ? (long long)s_base[gi]
+                            : qmeta(gi * G, Q, q_seq, q_pos, n_pools, cu_pool_cap, pool_start, B,
+                                    kpool, P_ld, status, false).base;
         const int nq = min(G, Q - gi * G);
         unsigned char* bt = sbase + LY::b + (size_t)slot * C::kBBytes;
         mbar_arrive_expect_tx(&ctl.bfull[slot], C::kBBytes + nq * kH * 4);
@@ -324,7 +332,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           if (((a_used >> stage) & 1) &&
               !wait_or_abort(&ctl.empty[stage], ((a_par >> stage) & 1) ^ 1, abort, status))
             break;
-          const int row = (int)(m0.base + (t - s_prefix[gi]) * kBM);
+          const int row = (int)(base0 + (t - s_prefix[gi]) * kBM);
           unsigned char* at = sbase + LY::a + (size_t)stage * kABytes;
           mbar_arrive_expect_tx(&ctl.full[stage], kABytes);
           tma_load_2d(at, &tmap_keys, 0, row, &ctl.full[stage]);
