@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--breakdown", action="store_true",
                     help="diagnostic: per-stage in-graph times (extra events between stages)")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the prefill-chunk scoring measurement")
     return ap.parse_args()
 
 
@@ -180,6 +182,55 @@ def profiled_traffic(kernel):
     if hashlib.sha256(open(src, "rb").read()).hexdigest() != fields.get("source_sha256"):
         return None
     return int(fields["traffic_bytes_per_launch"])
+
+
+def prefill_index(peaks_path, reps=10):
+    """The prefill-chunk scoring pass: 4096 queries appended to a 131 072-token
+    context (kpool 8, 16 896 pools, causal), one dsa_index_scores launch, L2
+    flushed before every timed launch.  Reported against the bf16 tensor peak
+    over the causal flops 2*H*D*sum_q(visible pools of q)."""
+    import torch
+
+    from sparse_attention_indexer_kpool_gb300 import ops, pipeline, synth
+    bt = synth.prefill(device="cuda")
+    buf = pipeline.LayerBuffers.alloc(bt)
+    pipeline.compress(bt, buf)
+    torch.cuda.synchronize()
+    assert int(buf.status.item()) == 0
+    g = bt.geo
+    P = int(buf.n_pools[0].item())
+    pos = bt.q_pos.to(torch.int64)
+    visible = torch.clamp((pos + 1) // g.kpool, max=P)        # no padding: t0 = 0
+    flops = 2.0 * g.H * g.D * float(visible.sum().item())
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def launch():
+        ops.dsa_index_scores(bt.q, bt.weights, bt.scale, buf.pool_keys, buf.pool_start,
+                             buf.pool_valid, buf.n_pools, bt.cu_pool_cap, bt.q_seq, bt.q_pos,
+                             g.kpool, buf.scores, buf.status)
+    for _ in range(3):
+        launch()
+    times = []
+    for _ in range(reps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        launch()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    assert int(buf.status.item()) == 0
+    us = statistics.median(times) * 1e3
+    peak = json.load(open(peaks_path))["bf16_tflops"] if os.path.exists(peaks_path) else 1900.0
+    tf = flops / (us * 1e-6) / 1e12
+    return {"workload": "prefill: 4096 chunk queries after 131072 ctx, kpool 8, %d pools, "
+                        "causal" % P,
+            "kernel": "index_scores_umma_kernel (8 queries per key tile)",
+            "us": round(us, 2), "flops": flops, "tflops": round(tf, 1), "bound": "tensor",
+            "peak_tflops": peak, "peak_source": "measured bf16 burst" if
+            os.path.exists(peaks_path) else "fallback", "frac": round(tf / peak, 4),
+            "score_bytes": int(buf.scores.numel() * 4),
+            "timing": "median of %d launches, L2 flushed before each" % reps}
 
 
 def run_ours(args, dist):
@@ -450,6 +501,8 @@ def run_ours(args, dist):
     }
     if breakdown:
         out["breakdown"] = breakdown
+    if not args.no_prefill:
+        out["prefill_index"] = prefill_index(peaks_path)
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(layers[0], args.cpu_seconds)
     if dist.rank == 0:

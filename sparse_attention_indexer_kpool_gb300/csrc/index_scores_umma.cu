@@ -21,7 +21,8 @@
 //              two TMEM accumulators, then commits to the ring slot's "empty"
 //              barrier and the accumulator's "full" barrier;
 //   warps 2-9  epilogue: tcgen05.ld of the accumulator rows (a warp reads the 32
-//              TMEM lanes of its quarter), relu / weight / head sum in registers,
+//              TMEM lanes of its quarter), relu / weight / head sum in registers
+//              (scale folded into the weights once per query group),
 //              -0 -> +0, candidate mask, coalesced score stores and (decode) a
 //              4096-bin histogram of the score keys' top 12 bits for the top-k
 //              that follows.  For G = 1 the two halves of the epilogue take
@@ -414,7 +415,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       }
       const long long base = mq[0].base;  // every query of a group reads one sequence
       const bool b_ok = wait_or_abort(&ctl.bfull[slot], (seg / C::kBSlots) & 1, abort, status);
-      const float* wq = s_w + slot * G * kH;
+      float* wq = s_w + slot * G * kH;
+      // fold scale into the weights once per group: w * max(0, scale * dot) equals
+      // (w * scale) * max(0, dot) for scale > 0 (up to rounding)
+      if (b_ok && ew * 32 + lane < G * kH) wq[ew * 32 + lane] *= scale;
+      epi_bar();
       for (; t < seg_hi; ++t, ++tc) {
         const int acc = (int)(tc & 1);
         if (G == 1 && acc != half) continue;  // the other half's tile
@@ -439,10 +444,10 @@ __global__ void __launch_bounds__(kThreadsU, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float4 w = w4[i];
-            sc = fmaf(w.x, fmaxf(scale * v[4 * i + 0], 0.f), sc);
-            sc = fmaf(w.y, fmaxf(scale * v[4 * i + 1], 0.f), sc);
-            sc = fmaf(w.z, fmaxf(scale * v[4 * i + 2], 0.f), sc);
-            sc = fmaf(w.w, fmaxf(scale * v[4 * i + 3], 0.f), sc);
+            sc = fmaf(w.x, fmaxf(v[4 * i + 0], 0.f), sc);
+            sc = fmaf(w.y, fmaxf(v[4 * i + 1], 0.f), sc);
+            sc = fmaf(w.z, fmaxf(v[4 * i + 2], 0.f), sc);
+            sc = fmaf(w.w, fmaxf(v[4 * i + 3], 0.f), sc);
           }
           if (sc == 0.f) sc = 0.f;  // -0 -> +0
           const QMeta& m = mq[u];
