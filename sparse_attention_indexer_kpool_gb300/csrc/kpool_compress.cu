@@ -146,6 +146,28 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   const bool cta_has_work = p_first < end || blockIdx.x == 0;
   if (!cta_has_work) return;
 
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int p = p_first + warp;
+  // An incremental call (begin > 0) extends a cache whose first pool starts at
+  // the sequence's first valid token.  Warm this warp's token rows in L2 from
+  // that start while the scan below confirms it, so the two cold misses overlap
+  // instead of following each other.  Only in-range addresses are touched.
+  if (begin > 0 && p >= 0 && p < end) {
+    const int t0g = pool_start[cap_lo];
+    const long long s0 = lo + t0g + (long long)p * kpool;
+    if (t0g >= 0 && s0 + kpool <= lo + Tb) {
+      constexpr int kLines = (D * (int)sizeof(T) + 127) / 128;   // 128-byte lines per row
+      for (int i = lane; i < 2 * kKpoolMax * kLines; i += 32) {
+        const int arr = i / (kKpoolMax * kLines), r = i % (kKpoolMax * kLines);
+        const int s = r / kLines, l = r % kLines;
+        if (s < kpool) {
+          const T* row = (arr ? gate : k) + (s0 + s) * D;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(row) + l * 128));
+        }
+      }
+      if (lane == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(valid + s0));
+    }
+  }
   const int t0 = first_valid_token(valid + 0, lo, Tb, &s_min);
   const int P = (Tb - t0) / kpool;
   const int P_eff = min(P, cap);
@@ -155,8 +177,6 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
     if (P_eff > end) flag(status, DSA_DEV_POOL_UNCOVERED);
   }
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int p = p_first + warp;
   if (p < 0 || p >= end) return;
   T* out = pool_keys + (cap_lo + p) * D + lane * V;
   if (p >= P_eff) {  // sentinel entry

@@ -282,6 +282,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
   pdl_launch_dependents();  // the next kernel may start its own prologue
 
+  // The first batch of this CTA's slice and the expansion's sequence lookup are
+  // requested together with the histogram, so their latencies overlap.
+  float v_first[kBatch];
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) {
+    const int i = lo + u * kThreads + threadIdx.x;
+    v_first[u] = i < hi ? row[i] : -INFINITY;
+  }
+  const int b = ex.token_ids ? (ex.q_seq ? ex.q_seq[q] : 0) : 0;
+  const bool seq_ok = !ex.token_ids || (b >= 0 && b < ex.B);
+  const long long cap_base = (ex.token_ids && seq_ok) ? ex.cu_pool_cap[b] : 0;
+  const int cap = (ex.token_ids && seq_ok) ? ex.cu_pool_cap[b + 1] - ex.cu_pool_cap[b] : 0;
+  // slice element i of the pass starting at `base` (the first batch is in registers)
+  auto slice = [&](int base, int u) -> float {
+    const int i = base + u * kThreads + threadIdx.x;
+    return base == lo ? v_first[u] : (i < hi ? row[i] : -INFINITY);
+  };
+
   // ---- 1. histogram of the top 12 key bits
   uint32_t* gh = hist_in ? hist_in + (size_t)q * kBins : nullptr;
   uint32_t* hh = h;
@@ -294,10 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int base = lo; base < hi; base += kThreads * kBatch) {
       float v[kBatch];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int i = base + u * kThreads + threadIdx.x;
-        v[u] = i < hi ? row[i] : -INFINITY;
-      }
+      for (int u = 0; u < kBatch; ++u) v[u] = slice(base, u);
 #pragma unroll
       for (int u = 0; u < kBatch; ++u)
         if (is_candidate(v[u])) atomicAdd(&h[score_key(v[u]) >> kBinShift], 1u);
@@ -320,10 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int base = lo; base < hi; base += kThreads * kBatch) {
     float v[kBatch];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = base + u * kThreads + threadIdx.x;
-      v[u] = i < hi ? row[i] : -INFINITY;
-    }
+    for (int u = 0; u < kBatch; ++u) v[u] = slice(base, u);
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int i = base + u * kThreads + threadIdx.x;
@@ -387,10 +399,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   cluster.sync();  // every CTA has its copy: the others' shared memory may go away
   const int32_t* pstart = ex.pool_start;
-  const int b = ex.token_ids ? (ex.q_seq ? ex.q_seq[q] : 0) : 0;
-  const bool seq_ok = !ex.token_ids || (b >= 0 && b < ex.B);
-  const long long cap_base = (ex.token_ids && seq_ok) ? ex.cu_pool_cap[b] : 0;
-  const int cap = (ex.token_ids && seq_ok) ? ex.cu_pool_cap[b + 1] - ex.cu_pool_cap[b] : 0;
   int32_t* out = pool_ids + (long long)q * K;
   int32_t* tok = ex.token_ids ? ex.token_ids + (long long)q * ex.W : nullptr;
   // writes one selected key's pool id and token ids at output slot `pos`
