@@ -204,6 +204,13 @@ int launch_expand_selection(const int32_t* pool_ids, const int32_t* pool_start,
                             int select_k, int kpool, int out_width, int32_t* token_ids,
                             int32_t* status_dev, cudaStream_t stream);
 size_t mla_workspace_size(int Q, int Hm, int L, int out_width, int dtype);
+// tcgen05 attention (bf16, 64 heads, latent 512): one CTA per 128 selected rows
+bool mla_umma_ok(int Q, int Hm, int L, int out_width, int dtype);
+int mla_umma_splits(int out_width);
+int launch_mla_umma(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
+                    const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int out_width,
+                    float sm_scale, void* out, float* lse, float* part_o, float* part_ml,
+                    int32_t* status_dev, cudaStream_t stream);
 int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
                                const int32_t* q_seq, const int32_t* token_ids, int Q, int B,
                                int Hm, int L, int out_width, float sm_scale, int dtype, void* out,

@@ -37,6 +37,7 @@
 #include <mutex>
 
 #include "dsa_internal.cuh"
+#include "umma.cuh"
 
 namespace dsa {
 namespace {
@@ -126,66 +127,6 @@ __device__ __forceinline__ QMeta qmeta(int qi, int Q, const int32_t* q_seq, cons
   return m;
 }
 
-// ---- tcgen05 / TMA wrappers ------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-// Shared-memory matrix descriptor: K-major operand with the 128-byte swizzle
-// (rows of 128 bytes, 8-row atoms 1024 bytes apart), sm_100 descriptor version.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) |
-         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, M = 128, N = n.
-__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
-         ((uint32_t)(kBM >> 4) << 24);
-}
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// 32 consecutive fp32 columns of the warp's 32 TMEM lanes (one lane per thread).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 __device__ __forceinline__ void epi_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
 }
@@ -306,6 +247,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   if (warp == 0) {
     // ================= TMA producer =================
     if (lane == 0) {
+      // keys are read once per call: do not let them push the step's other data out of L2
+      const uint64_t keys_policy = l2_policy_evict_first();
       uint32_t a_par = 0, a_used = 0;  // per ring slot: parity of its next fill, ever filled
       uint32_t b_par = 0, b_used = 0;  // the same for the query block slots
       int stage = 0, gi = 0, seg = 0;
@@ -336,8 +279,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           const int row = (int)(base0 + (t - s_prefix[gi]) * kBM);
           unsigned char* at = sbase + LY::a + (size_t)stage * kABytes;
           mbar_arrive_expect_tx(&ctl.full[stage], kABytes);
-          tma_load_2d(at, &tmap_keys, 0, row, &ctl.full[stage]);
-          tma_load_2d(at + kHalfA, &tmap_keys, 64, row, &ctl.full[stage]);
+          tma_load_2d_hint(at, &tmap_keys, 0, row, &ctl.full[stage], keys_policy);
+          tma_load_2d_hint(at + kHalfA, &tmap_keys, 64, row, &ctl.full[stage], keys_policy);
           a_par ^= 1u << stage;
           a_used |= 1u << stage;
           stage = stage + 1 == C::kStages ? 0 : stage + 1;
@@ -353,7 +296,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   } else if (warp == 1) {
     // ================= MMA issuer =================
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(N);
+      constexpr uint32_t idesc = umma_idesc_bf16(kBM, N, false);
       uint32_t a_par = 0;  // per ring slot: parity of its next "full" phase
       int stage = 0, gi = 0, seg = 0;
       long long tc = 0;    // tiles issued by this CTA

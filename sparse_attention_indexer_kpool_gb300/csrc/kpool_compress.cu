@@ -196,15 +196,17 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   Vec<T, V>::load(ln_beta + lane * V, be);
 
   const long long s0 = lo + t0 + (long long)p * kpool;
-  float kn[kKpoolMax][V], lg[kKpoolMax][V];
+  float kn[kKpoolMax][V], lg[kKpoolMax][V], ap[kKpoolMax][V];
   bool all_valid = true;
-  // every slot's rows are requested before any reduction runs, so the loads of
-  // the pool overlap instead of waiting one slot at a time
+  // every slot's rows and slot biases are requested before any reduction runs,
+  // so the loads of the pool overlap instead of waiting one slot at a time
 #pragma unroll
   for (int s = 0; s < kKpoolMax; ++s) {
     if (s < kpool) {
       Vec<T, V>::load(k + (s0 + s) * D + lane * V, kn[s]);
       Vec<T, V>::load(gate + (s0 + s) * D + lane * V, lg[s]);
+#pragma unroll
+      for (int i = 0; i < V; ++i) ap[s][i] = __ldg(ape + s * D + lane * V + i);  // 4-byte aligned
       all_valid &= valid[s0 + s] != 0;
     }
   }
@@ -226,7 +228,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
 #pragma unroll
       for (int i = 0; i < V; ++i) {
         kn[s][i] = Act<T>::round((kn[s][i] - mean) * rstd * g[i] + be[i]);
-        lg[s][i] = lg[s][i] + __ldg(ape + s * D + lane * V + i);
+        lg[s][i] = lg[s][i] + ap[s][i];
       }
     }
   }

@@ -436,9 +436,13 @@ void split_plan(int Q, int Hm, int W, int* n_split, int* rows_per_split) {
 }  // namespace
 
 size_t mla_workspace_size(int Q, int Hm, int L, int out_width, int dtype) {
-  if (!fast_path(Hm, L, dtype)) return 0;
-  int n_split, rows;
-  split_plan(Q, Hm, out_width, &n_split, &rows);
+  int n_split = 1;
+  if (mla_umma_ok(Q, Hm, L, out_width, dtype)) {
+    n_split = mla_umma_splits(out_width);
+  } else if (fast_path(Hm, L, dtype)) {
+    int rows;
+    split_plan(Q, Hm, out_width, &n_split, &rows);
+  }
   if (n_split == 1) return 0;
   const size_t slots = (size_t)Q * Hm * n_split;
   return slots * L * 4 + slots * 2 * 4;
@@ -456,6 +460,22 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
   cfg.stream = stream;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
+  if (mla_umma_ok(Q, Hm, L, out_width, dtype)) {
+    const int n_split = mla_umma_splits(out_width);
+    if (n_split > 1 && ws_bytes < mla_workspace_size(Q, Hm, L, out_width, dtype))
+      return DSA_ERR_WORKSPACE;
+    float* part_o = n_split > 1 ? static_cast<float*>(workspace) : nullptr;
+    float* part_ml = part_o ? part_o + (size_t)Q * Hm * n_split * L : nullptr;
+    const int r = launch_mla_umma(q_lat, kv, cu_seqlens, q_seq, token_ids, Q, B, out_width,
+                                  sm_scale, out, lse, part_o, part_ml, status_dev, stream);
+    if (r != DSA_OK || n_split == 1) return r;
+    cfg.gridDim = dim3(Hm, Q, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, mla_merge_kernel, (const float*)part_o,
+                              (const float*)part_ml, Hm, n_split, (__nv_bfloat16*)out,
+                              lse) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  }
   if (fast_path(Hm, L, dtype)) {
     int n_split, rows;
     split_plan(Q, Hm, out_width, &n_split, &rows);

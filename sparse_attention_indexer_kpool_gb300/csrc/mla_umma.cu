@@ -1,0 +1,316 @@
+// NoPE MLA decode over the selected latent rows on the tcgen05 tensor cores.
+//
+// Module glm5next_dsa, "Shape of the pipeline" (NoPE MLA restricted to the
+// selected tokens), Modules, attend, and "Traps carried from Slice 8" (NoPE: the
+// score is the plain latent dot product).  In absorbed MLA the value of a latent
+// row is the row itself, so one gathered tile feeds both products.
+//
+// Geometry: bf16, 64 heads, latent 512.  One CTA = one query, one split of 128
+// selected rows and one half of the heads (32):
+//   1. the query's q_lat half (32 x 512) and the split's 128 latent rows are
+//      gathered with 16-byte cp.async into 128-byte-swizzled tiles (eight
+//      64-column blocks each);
+//   2. S^T = C q^T on the tensor cores: M = 128 rows, N = 32 heads, K = 512, one
+//      thread issues 32 MMAs into TMEM;
+//   3. softmax per head over the 128 rows: each thread reads its row's scores
+//      of 16 heads, a butterfly over the warp reduces the 16 columns across the
+//      warp's 32 rows, four warps combine through shared memory; the
+//      probabilities are written to shared memory as P^T (32 heads x 128 rows,
+//      bf16, swizzled) and the per-head max (base 2) and sum are kept;
+//   4. O^T = C^T P^T: M = 128 latent columns (four chunks), N = 32 heads, K = 128
+//      rows.  A is the same gathered tile read MN-major, so the rows are never
+//      transposed;
+//   5. O^T is staged in shared memory (the row tile is no longer needed) and the
+//      unnormalised partial rows leave with coalesced 16-byte stores, with the
+//      per-head max and sum (or, with a single split, the normalised output and
+//      lse go straight to the outputs); the merge kernel combines the splits.
+// Waits on the MMA completions are bounded (DSA_DEV_TIMEOUT on expiry).
+#include <math.h>
+
+#include <mutex>
+
+#include "dsa_internal.cuh"
+#include "umma.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kL = 512, kHm = 64, kHh = 32, kRows = 128;
+constexpr int kThreadsM = 256;
+constexpr int kKvBlock = kRows * 128;   // 128 rows x 64 latent columns, 16 KB
+constexpr int kQBlock = kHh * 128;      // 32 heads x 64 latent columns, 4 KB
+constexpr int kPtBlock = kHh * 128;     // 32 heads x 64 rows, 4 KB
+constexpr int kTmemCols = 256;          // S^T (32 columns) + O^T (4 x 32 columns)
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct MCtl {
+  uint64_t s_ready, o_ready;
+  uint32_t tmem_base;
+  int pad;
+  int tok[kRows];
+  float red[2][4][16];  // [head quarter pair][row quarter][head]: per-warp partials
+  float m_fin[kHh], l_fin[kHh];
+};
+constexpr size_t kOffKv = 0;
+constexpr size_t kOffQ = kOffKv + 8 * (size_t)kKvBlock;
+constexpr size_t kOffPt = kOffQ + 8 * (size_t)kQBlock;
+constexpr size_t kOffCtl = kOffPt + 2 * (size_t)kPtBlock;
+constexpr size_t kSmemBytes = 1024 + kOffCtl + sizeof(MCtl);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert((size_t)kHh * kL * 4 <= 8 * (size_t)kKvBlock, "O staging fits the row tile");
+
+// 16 values per lane (one row, 16 heads) reduced over the warp's 32 rows; lanes
+// l and l + 16 end with the reduction of head l.  A plain exchange across the
+// two half-warps, then halving steps that keep half of the values and swap the
+// other half with the partner lane: 31 shuffles in all.
+template <bool kMax>
+__device__ __forceinline__ float transpose_reduce16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float o = __shfl_xor_sync(0xffffffffu, v[i], 16);
+    v[i] = kMax ? fmaxf(v[i], o) : v[i] + o;
+  }
+#pragma unroll
+  for (int s = 8; s >= 1; s >>= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      const float send = upper ? v[i] : v[i + s];
+      const float keep = upper ? v[i + s] : v[i];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, s);
+      v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  return v[0];
+}
+
+__global__ void __launch_bounds__(kThreadsM, 1)
+    mla_umma_kernel(const __nv_bfloat16* __restrict__ q_lat, const __nv_bfloat16* __restrict__ kv,
+                    const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ q_seq,
+                    const int32_t* __restrict__ token_ids, int B, int W, float sm_scale,
+                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                    float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char* sb = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  MCtl& c = *reinterpret_cast<MCtl*>(sb + kOffCtl);
+  const int split = blockIdx.x, n_split = gridDim.x, hf = blockIdx.y, qi = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qw = warp & 3;   // TMEM lanes 32 qw .. 32 qw + 31
+  const int hq = warp >> 2;  // softmax: heads 16 hq .. 16 hq + 15; epilogue: chunk pair
+
+  if (threadIdx.x == 0) {
+    mbar_init(&c.s_ready, 1);
+    mbar_init(&c.o_ready, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc<kTmemCols>(&c.tmem_base);
+    tc_fence_before();
+  }
+  // every input may come from the kernel just before: wait for it first
+  pdl_wait();
+  pdl_launch_dependents();
+
+  // ---- 1. gathers: the query block first (no dependency), then the rows
+  const long long qh0 = (long long)qi * kHm + hf * kHh;   // first (query, head) row
+  const __nv_bfloat16* qsrc = q_lat + qh0 * kL;
+  for (int i = threadIdx.x; i < kHh * 64; i += kThreadsM) {
+    const int h = i >> 6, ch = i & 63;
+    cp_async16(smem_u32(sb + kOffQ + (ch >> 3) * kQBlock + h * 128 + (((ch & 7) ^ (h & 7)) << 4)),
+               qsrc + (long long)h * kL + ch * 8, true);
+  }
+  cp_async_commit();
+  const int b = q_seq ? q_seq[qi] : 0;
+  const bool seq_ok = b >= 0 && b < B;
+  if (!seq_ok && split == 0 && hf == 0 && threadIdx.x == 0) flag(status, DSA_DEV_BAD_QSEQ);
+  const long long row_base = seq_ok ? cu_seqlens[b] : 0;
+  const int Tb = seq_ok ? cu_seqlens[b + 1] - cu_seqlens[b] : 0;
+  if (threadIdx.x < kRows) {
+    const int j = split * kRows + threadIdx.x;
+    int tok = (j < W && seq_ok) ? token_ids[(long long)qi * W + j] : -1;
+    if (tok >= Tb) {
+      if (hf == 0) flag(status, DSA_DEV_BAD_TOKEN);
+      tok = -1;
+    }
+    c.tok[threadIdx.x] = tok < 0 ? -1 : tok;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kRows * 64; i += kThreadsM) {
+    const int r = i >> 6, ch = i & 63;
+    const int tok = c.tok[r];
+    const bool ok = tok >= 0;
+    cp_async16(smem_u32(sb + kOffKv + (ch >> 3) * kKvBlock + r * 128 + (((ch & 7) ^ (r & 7)) << 4)),
+               ok ? kv + (row_base + tok) * kL + ch * 8 : kv, ok);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = c.tmem_base;
+  const uint32_t kvb = smem_u32(sb + kOffKv), qb = smem_u32(sb + kOffQ);
+  const uint32_t ptb = smem_u32(sb + kOffPt);
+
+  // ---- 2. S^T = C q^T  (M = 128 rows, N = 32 heads, K = 512)
+  if (threadIdx.x == 0) {
+    constexpr uint32_t idesc = umma_idesc_bf16(kRows, kHh, false);
+#pragma unroll
+    for (int kk = 0; kk < 32; ++kk) {
+      const uint32_t blk = kk >> 2, off = (kk & 3) * 32;
+      umma_bf16(tmem, sw128_desc(kvb + blk * kKvBlock + off), sw128_desc(qb + blk * kQBlock + off),
+                idesc, kk > 0 ? 1u : 0u);
+    }
+    umma_commit(&c.s_ready);
+  }
+  bool ok = mbar_wait_bounded(&c.s_ready, 0);
+  if (!ok && lane == 0) flag(status, DSA_DEV_TIMEOUT);
+  tc_fence_after();
+
+  // ---- 3. softmax over the rows, per head (thread = row r, heads 16 hq .. 16 hq + 15)
+  const int r = qw * 32 + lane;
+  float z[16];
+  tmem_ld16(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(hq * 16), z);
+  const bool row_ok = c.tok[r] >= 0 && ok;
+  const float zs = sm_scale * kLog2e;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) z[i] = row_ok ? z[i] * zs : -INFINITY;
+  {
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) t[i] = z[i];
+    const float m = transpose_reduce16<true>(t, lane);
+    if (lane < 16) c.red[hq][qw][lane] = m;
+  }
+  __syncthreads();
+  if (threadIdx.x < kHh) {
+    const int h2 = threadIdx.x >> 4, l2 = threadIdx.x & 15;
+    c.m_fin[threadIdx.x] =
+        fmaxf(fmaxf(c.red[h2][0][l2], c.red[h2][1][l2]), fmaxf(c.red[h2][2][l2], c.red[h2][3][l2]));
+  }
+  __syncthreads();
+  float p[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int h = hq * 16 + i;
+    const float m = c.m_fin[h];
+    p[i] = (m == -INFINITY || z[i] == -INFINITY) ? 0.f : exp2f(z[i] - m);
+    *reinterpret_cast<__nv_bfloat16*>(sb + kOffPt + (r >> 6) * kPtBlock + h * 128 +
+                                      ((((r & 63) >> 3) ^ (h & 7)) << 4) + (r & 7) * 2) =
+        __float2bfloat16_rn(p[i]);
+  }
+  {
+    const float l = transpose_reduce16<false>(p, lane);
+    if (lane < 16) c.red[hq][qw][lane] = l;
+  }
+  fence_proxy_async_smem();  // P^T is read by the tensor cores next
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < kHh) {
+    const int h2 = threadIdx.x >> 4, l2 = threadIdx.x & 15;
+    c.l_fin[threadIdx.x] =
+        (c.red[h2][0][l2] + c.red[h2][1][l2]) + (c.red[h2][2][l2] + c.red[h2][3][l2]);
+  }
+
+  // ---- 4. O^T = C^T P^T  (M = 128 latent columns x 4 chunks, N = 32 heads, K = 128 rows)
+  if (threadIdx.x == 0) {
+    tc_fence_after();
+    constexpr uint32_t idesc = umma_idesc_bf16(128, kHh, true);
+#pragma unroll
+    for (int mc = 0; mc < 4; ++mc) {
+#pragma unroll
+      for (int kr = 0; kr < 8; ++kr) {
+        const uint64_t a = umma_desc_sw128(kvb + 2 * mc * kKvBlock + kr * 2048, kKvBlock, 1024);
+        const uint64_t bd = sw128_desc(ptb + (kr >> 2) * kPtBlock + (kr & 3) * 32);
+        umma_bf16(tmem + kHh + mc * kHh, a, bd, idesc, kr > 0 ? 1u : 0u);
+      }
+    }
+    umma_commit(&c.o_ready);
+  }
+  __syncthreads();  // l_fin is complete
+  ok = mbar_wait_bounded(&c.o_ready, 0) && ok;
+  if (!ok && lane == 0) flag(status, DSA_DEV_TIMEOUT);
+  tc_fence_after();
+
+  // ---- 5. epilogue: O^T -> shared [head][latent] fp32 (the row tile is free now),
+  // then whole partial rows with 16-byte stores
+  float* stage = reinterpret_cast<float*>(sb + kOffKv);
+#pragma unroll 1
+  for (int cc = 0; cc < 2; ++cc) {
+    const int mc = hq + 2 * cc;
+    const int col = mc * 128 + qw * 32 + lane;
+    float o[32];
+    tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHh + mc * kHh), o);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) stage[i * kL + col] = ok ? o[i] : 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  for (int f = threadIdx.x; f < kHh * kL / 4; f += kThreadsM) {
+    const int h = f / (kL / 4), c4 = f % (kL / 4);
+    const float4 v = *reinterpret_cast<const float4*>(stage + h * kL + c4 * 4);
+    if (n_split == 1) {
+      const float l = c.l_fin[h];
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      *reinterpret_cast<uint2*>(out + (qh0 + h) * kL + c4 * 4) =
+          make_uint2(pack_bf16(v.x * inv, v.y * inv), pack_bf16(v.z * inv, v.w * inv));
+    } else {
+      *reinterpret_cast<float4*>(part_o + ((qh0 + h) * n_split + split) * kL + c4 * 4) = v;
+    }
+  }
+  if (threadIdx.x < kHh) {
+    const int h = threadIdx.x;
+    const float m = c.m_fin[h], l = ok ? c.l_fin[h] : 0.f;
+    if (n_split == 1) {
+      if (lse) lse[qh0 + h] = l > 0.f ? (m + log2f(l)) / kLog2e : -INFINITY;
+    } else {
+      part_ml[((qh0 + h) * n_split + split) * 2] = m;
+      part_ml[((qh0 + h) * n_split + split) * 2 + 1] = l;
+    }
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc<kTmemCols>(tmem);
+  }
+}
+
+}  // namespace
+
+int mla_umma_splits(int out_width) { return (out_width + kRows - 1) / kRows; }
+// Few queries (decode): one CTA per 128 selected rows and 32 heads, at most
+// four waves of CTAs; many queries keep the 16-head-group kernel, whose splits
+// adapt to Q.
+bool mla_umma_ok(int Q, int Hm, int L, int out_width, int dtype) {
+  return dtype == DSA_BF16 && Hm == kHm && L == kL &&
+         (long long)Q * mla_umma_splits(out_width) * (kHm / kHh) <= 4LL * kNumSMs;
+}
+
+int launch_mla_umma(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
+                    const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int out_width,
+                    float sm_scale, void* out, float* lse, float* part_o, float* part_ml,
+                    int32_t* status_dev, cudaStream_t stream) {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(mla_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)kSmemBytes);
+  });
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(mla_umma_splits(out_width), kHm / kHh, Q);
+  cfg.blockDim = dim3(kThreadsM, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_umma_kernel, (const __nv_bfloat16*)q_lat,
+                            (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, out_width,
+                            sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml,
+                            status_dev) == cudaSuccess
+             ? DSA_OK
+             : DSA_ERR_CUDA;
+}
+
+}  // namespace dsa

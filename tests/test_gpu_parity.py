@@ -298,3 +298,15 @@ def test_prefill_chunk_fused_matches_stage_calls():
     for name in ("scores", "pool_ids", "token_ids", "out", "lse"):
         assert torch.equal(getattr(a, name), getattr(b, name)), name
     assert int(a.ws_select.count_nonzero().item()) == 0
+
+
+@pytest.mark.parametrize("Hm,K,W,lengths", [
+    (64, 16, 64, [700, 2100]),         # one split of <= 128 rows: output written directly
+    (64, 48, 200, [3000, 41, 900]),    # ragged last split (200 = 128 + 72 rows)
+    (32, 64, 256, [2500, 1300]),       # 16-head groups on mma.sync (not 64 heads)
+    (128, 32, 128, [1800]),            # 16-head groups, 8 groups
+])
+def test_mla_tensor_core_variants(Hm, K, W, lengths):
+    geo = Geometry(D=128, H=32, kpool=4, select_k=K, out_width=W, Hm=Hm, L=512, dtype="bf16")
+    bt = synth.make_batch(geo, lengths, [1] * len(lengths), device=DEV, seed=500 + Hm + W)
+    run_and_check(bt)
