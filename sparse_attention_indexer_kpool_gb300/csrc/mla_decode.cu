@@ -298,9 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merge split partials: one CTA per (query, head); 128 threads x 4 latent columns.
-// Every split's partial row is requested up front, together with the (max, sum)
-// pairs, so the merge waits for memory once.
-constexpr int kMergeMax = 16;   // splits held in registers; more splits loop
+// Every split's partial row and (max, sum) pair of a batch is requested before
+// any of them is used, and the batch maximum rescales the running sums, so up to
+// kMergeMax splits cost a single round trip to memory.
+constexpr int kMergeMax = 16;   // splits held in registers per batch
 __global__ void __launch_bounds__(128)
     mla_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int Hm,
                      int n_split, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
@@ -308,9 +309,7 @@ __global__ void __launch_bounds__(128)
   const long long qh = (long long)blockIdx.y * Hm + blockIdx.x;
   const float* ml = part_ml + qh * n_split * 2;
   const int d = threadIdx.x * 4;
-  float mx = -INFINITY;
-  for (int sp = 0; sp < n_split; ++sp) mx = fmaxf(mx, __ldg(ml + 2 * sp));
-  float den = 0.f;
+  float mx = -INFINITY, den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s0 = 0; s0 < n_split; s0 += kMergeMax) {
     float4 v[kMergeMax];
@@ -318,15 +317,26 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int u = 0; u < kMergeMax; ++u) {
       const int sp = s0 + u;
+      ll[u] = 0.f;
+      mm[u] = -INFINITY;
       if (sp < n_split) {
         v[u] = __ldg(reinterpret_cast<const float4*>(part_o + (qh * n_split + sp) * kL + d));
         mm[u] = __ldg(ml + 2 * sp);
         ll[u] = __ldg(ml + 2 * sp + 1);
       }
     }
+    float bm = mx;
+#pragma unroll
+    for (int u = 0; u < kMergeMax; ++u)
+      if (ll[u] > 0.f) bm = fmaxf(bm, mm[u]);
+    if (bm == -INFINITY) continue;  // nothing selected so far
+    const float r = mx == -INFINITY ? 0.f : exp2f(mx - bm);
+    den *= r;
+    acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
+    mx = bm;
 #pragma unroll
     for (int u = 0; u < kMergeMax; ++u) {
-      if (s0 + u < n_split && ll[u] > 0.f) {
+      if (ll[u] > 0.f) {
         const float w = exp2f(mm[u] - mx);
         den += ll[u] * w;
         acc.x += w * v[u].x; acc.y += w * v[u].y; acc.z += w * v[u].z; acc.w += w * v[u].w;

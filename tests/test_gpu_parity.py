@@ -310,3 +310,14 @@ def test_mla_tensor_core_variants(Hm, K, W, lengths):
     geo = Geometry(D=128, H=32, kpool=4, select_k=K, out_width=W, Hm=Hm, L=512, dtype="bf16")
     bt = synth.make_batch(geo, lengths, [1] * len(lengths), device=DEV, seed=500 + Hm + W)
     run_and_check(bt)
+
+
+def test_mla_tensor_core_many_queries_merge_kernel():
+    """12 queries x 16 splits x 2 head halves: the split partials of many queries
+    go through the merge kernel."""
+    geo = Geometry(D=128, H=32, kpool=4, select_k=512, out_width=2048, Hm=64, L=512,
+                   dtype="bf16")
+    rng = np.random.default_rng(12)
+    lengths = [int(x) for x in rng.integers(2100, 4200, 12)]
+    bt = synth.make_batch(geo, lengths, [0] * 12, device=DEV, seed=612)
+    run_and_check(bt)
