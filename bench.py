@@ -5,11 +5,11 @@ Workload (default): 4 sequences x 262 144 tokens (65 536 pools each at kpool 4),
 32 index heads x head_dim 128, select_k 512 -> 2 048 token ids, MLA 64 heads x
 latent 512, bf16, 11 independent DSA layers per step (each with its own seeded
 caches and weights).  One step = every layer's decode pass for the 4 query
-tokens: incremental kpool_compress of the just-completed pool -> index_scores
--> topk_pools -> expand_selection -> MLA over the selected rows.  The step is
-captured in a CUDA graph; caches live in HBM before the timed region starts and
-the 11 layers' 704 MB of pool keys cycle through the 129 MB L2, so every step
-reads its pool keys from HBM.
+tokens, one dsa_decode_layer call per layer: incremental kpool_compress of the
+just-completed pool -> index_scores -> topk_pools -> expand_selection -> MLA
+over the selected rows.  The step is captured in a CUDA graph; caches live in
+HBM before the timed region starts and the 11 layers' 704 MB of pool keys
+cycle through the 129 MB L2, so every step reads its pool keys from HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -294,15 +294,18 @@ def run_ours(args, dist):
         buf.pool_begin = (buf.n_pools - 1).clamp(min=0).to(torch.int32)
 
     def step(events=None):
-        """One decode step over every layer; events[layer] = (before, after) the
-        select call (index_scores + top-k + expand)."""
+        """One decode step over every layer: one dsa_decode_layer call per layer
+        (compress of the just-completed pool -> select -> attend).  With events,
+        the three stage calls run separately and events[layer] = (before, after)
+        the select call (index_scores + top-k + expand)."""
         for li, (bt, buf) in enumerate(layers):
+            if events is None:
+                pipeline.decode_layer(bt, buf, pool_begin=buf.pool_begin, max_pools=1)
+                continue
             pipeline.compress(bt, buf, pool_begin=buf.pool_begin, max_pools=1)
-            if events is not None:
-                events[li][0].record()
+            events[li][0].record()
             pipeline.select(bt, buf)
-            if events is not None:
-                events[li][1].record()
+            events[li][1].record()
             pipeline.attend(bt, buf)
 
     kernels_per_layer = 5   # compress, index scores (+histogram), select (+expand), MLA, MLA merge
@@ -473,7 +476,8 @@ def run_ours(args, dist):
     sel_bytes = (ab["index"] + ab["topk"] + ab["expand"]) * Q
     select_call = None
     if idx_ms:
-        select_call = {"kernels": "index_scores_umma_kernel + topk_select_kernel",
+        select_call = {"kernels": "index_scores_umma_kernel + topk_select_kernel "
+                                  "(three-call form of the step, events around dsa_select)",
                        "us": round(idx_ms * 1e3, 2), "bytes": sel_bytes,
                        "gbs": round(sel_bytes / (idx_ms * 1e-3) / 1e9, 1)}
     step_gbs = per_step_bytes / (ms / K * 1e-3) / 1e9

@@ -280,6 +280,73 @@ int dsa_select_noalloc(const void* q, const float* weights, float scale, const v
                        int select_k, int out_width, int dtype, float* scores, int32_t* pool_ids,
                        int32_t* token_ids, int32_t* status_dev, void* stream);
 
+/*
+ * dsa_decode_layer - one layer of the decode path in one call:
+ *   dsa_kpool_compress (the pools [pool_begin[b], pool_begin[b] + max_pools))
+ *   -> dsa_select -> dsa_mla_selected_decode.
+ *
+ * Source: module glm5next_dsa, "Shape of the pipeline" (the five stages in
+ * order).  The pages have no fused call; this one writes exactly what the three
+ * calls above write, with their arguments (gathered in the struct below), their
+ * validation (all three stages are checked before anything is launched) and
+ * their device faults.  Being one call, its later kernels may start on data
+ * that its earlier kernels do not write: the scoring kernel streams the key
+ * tiles below pool_begin[b] while the compress still runs (decode geometry,
+ * q_pos == NULL), and the attention kernel loads its query block before the
+ * token ids exist.  As with every call, inputs are ordered by the stream: work
+ * enqueued before the call has finished writing them when it starts.
+ *   ws_select: dsa_select_workspace_size(Q, P_ld, select_k) bytes, zero-filled
+ *              before first use, left zeroed (as for dsa_select).
+ *   ws_mla:    dsa_mla_selected_decode_workspace_size(Q, Hm, L, out_width, dtype).
+ *   pool_begin may be NULL (every pool from 0; no early streaming).
+ */
+typedef struct dsa_decode_layer_args {
+  /* kpool_compress inputs */
+  const void* k;
+  const void* gate;
+  const uint8_t* valid;
+  const float* ape;
+  const void* ln_gamma;
+  const void* ln_beta;
+  float ln_eps;
+  const int32_t* cu_seqlens;
+  const int32_t* pool_begin;
+  int max_pools;
+  /* pool cache (written by the compress, read by the selection) */
+  void* pool_keys;
+  int pool_rows;
+  int32_t* pool_start;
+  uint8_t* pool_valid;
+  int32_t* n_pools;
+  const int32_t* cu_pool_cap;
+  /* queries */
+  const void* q;
+  const float* weights;
+  float scale;
+  const int32_t* q_seq;
+  const int32_t* q_pos;
+  const void* q_lat;
+  const void* kv_latent;
+  float sm_scale;
+  /* geometry */
+  int Q, B, H, D, kpool, P_ld, select_k, out_width, Hm, L, dtype;
+  /* outputs and workspaces */
+  float* scores;
+  int32_t* pool_ids;
+  int32_t* token_ids;
+  void* out;
+  float* lse;
+  void* ws_select;
+  size_t ws_select_bytes;
+  void* ws_mla;
+  size_t ws_mla_bytes;
+  int32_t* status_dev;
+} dsa_decode_layer_args;
+int dsa_decode_layer(const dsa_decode_layer_args* args, void* stream);
+/* Workspace sizes for the geometry in *args; returns their sum. */
+size_t dsa_decode_layer_workspace_size(const dsa_decode_layer_args* args, size_t* ws_select,
+                                       size_t* ws_mla);
+
 /* Human-readable name of a DSA_* return code (static string). */
 const char* dsa_status_string(int status);
 

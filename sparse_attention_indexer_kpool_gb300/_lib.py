@@ -16,6 +16,22 @@ _LOCK = threading.Lock()
 
 c_void_p, c_int, c_float, c_size_t = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 
+
+class DecodeLayerArgs(ctypes.Structure):
+    """dsa_decode_layer_args (include/dsa.h), field for field."""
+    _fields_ = [(n, c_void_p) for n in ("k", "gate", "valid", "ape", "ln_gamma", "ln_beta")] + [
+        ("ln_eps", c_float), ("cu_seqlens", c_void_p), ("pool_begin", c_void_p),
+        ("max_pools", c_int), ("pool_keys", c_void_p), ("pool_rows", c_int),
+        ("pool_start", c_void_p), ("pool_valid", c_void_p), ("n_pools", c_void_p),
+        ("cu_pool_cap", c_void_p), ("q", c_void_p), ("weights", c_void_p), ("scale", c_float),
+        ("q_seq", c_void_p), ("q_pos", c_void_p), ("q_lat", c_void_p), ("kv_latent", c_void_p),
+        ("sm_scale", c_float)] + [(n, c_int) for n in (
+            "Q", "B", "H", "D", "kpool", "P_ld", "select_k", "out_width", "Hm", "L", "dtype")] + [
+        (n, c_void_p) for n in ("scores", "pool_ids", "token_ids", "out", "lse", "ws_select")] + [
+        ("ws_select_bytes", c_size_t), ("ws_mla", c_void_p), ("ws_mla_bytes", c_size_t),
+        ("status_dev", c_void_p)]
+
+
 # name -> (restype, argtypes); mirrors include/dsa.h
 SIGNATURES = {
     "dsa_kpool_compress": (c_int, [c_void_p] * 6 + [c_float] + [c_void_p] * 3 + [c_int] * 5
@@ -34,6 +50,10 @@ SIGNATURES = {
     "dsa_select_workspace_size": (c_size_t, [c_int, c_int, c_int]),
     "dsa_select_noalloc": (c_int, [c_void_p, c_void_p, c_float, c_void_p, c_int]
                            + [c_void_p] * 6 + [c_int] * 9 + [c_void_p] * 5),
+    "dsa_decode_layer": (c_int, [ctypes.POINTER(DecodeLayerArgs), c_void_p]),
+    "dsa_decode_layer_workspace_size": (c_size_t, [ctypes.POINTER(DecodeLayerArgs),
+                                                   ctypes.POINTER(c_size_t),
+                                                   ctypes.POINTER(c_size_t)]),
     "dsa_status_string": (ctypes.c_char_p, [c_int]),
     "dsa_version": (c_int, []),
 }

@@ -13,6 +13,104 @@ inline bool dtype_ok(int dtype) { return dtype == DSA_BF16 || dtype == DSA_F32; 
 inline bool d_ok(int D) { return D == 32 || D == 64 || D == 128 || D == 256; }
 inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
+constexpr int kNoWork = -1;  // valid call with nothing to do
+
+int check_compress(const void* k, const void* gate, const uint8_t* valid, const float* ape,
+                   const void* ln_gamma, const void* ln_beta, float ln_eps,
+                   const int32_t* cu_seqlens, const int32_t* cu_pool_cap,
+                   const int32_t* pool_begin, int B, int D, int kpool, int max_pools, int dtype,
+                   void* pool_keys, int32_t* pool_start, uint8_t* pool_valid, int32_t* n_pools,
+                   int32_t* status_dev) {
+  if (B < 0 || max_pools < 0) return DSA_ERR_INVALID_ARG;
+  if (kpool < 1 || kpool > DSA_KPOOL_MAX) return DSA_ERR_INVALID_ARG;  // refuse, never truncate
+  if (!dtype_ok(dtype) || !(ln_eps >= 0.f) || !isfinite(ln_eps)) return DSA_ERR_INVALID_ARG;
+  if (!d_ok(D)) return DSA_ERR_UNSUPPORTED;
+  if (B == 0) return kNoWork;
+  if (!k || !gate || !valid || !ape || !ln_gamma || !ln_beta || !cu_seqlens || !cu_pool_cap ||
+      !pool_keys || !pool_start || !pool_valid || !n_pools)
+    return DSA_ERR_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(gate, 16) || !aligned(pool_keys, 16) || !aligned(ln_gamma, 16) ||
+      !aligned(ln_beta, 16) || !aligned(ape, 4) || !aligned(cu_seqlens, 4) ||
+      !aligned(cu_pool_cap, 4) || !aligned(pool_start, 4) || !aligned(n_pools, 4) ||
+      (pool_begin && !aligned(pool_begin, 4)) || (status_dev && !aligned(status_dev, 4)))
+    return DSA_ERR_MISALIGNED;
+  if (B > 65535) return DSA_ERR_UNSUPPORTED;
+    return DSA_OK;
+}
+
+int check_select(const void* q, const float* weights, float scale, const void* pool_keys,
+                 int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
+                 const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
+                 const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
+                 int select_k, int out_width, int dtype, float* scores, int32_t* pool_ids,
+                 int32_t* token_ids, void* workspace, size_t ws_bytes, int32_t* status_dev) {
+  if (Q < 0 || B < 0 || H < 1 || P_ld < 1 || select_k < 1 || out_width < 1 || pool_rows < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (kpool < 1 || kpool > DSA_KPOOL_MAX) return DSA_ERR_INVALID_ARG;
+  if ((long long)out_width < (long long)select_k * kpool) return DSA_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype) || !(scale > 0.f) || !isfinite(scale)) return DSA_ERR_INVALID_ARG;
+  if (!d_ok(D) || H > 64 || select_k > DSA_SELECT_K_MAX) return DSA_ERR_UNSUPPORTED;
+  if (Q == 0) return kNoWork;
+  if (B == 0) return DSA_ERR_INVALID_ARG;
+  if (!q || !weights || !pool_keys || !pool_start || !pool_valid || !n_pools || !cu_pool_cap ||
+      !scores || !pool_ids || !token_ids)
+    return DSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(weights, 16) || !aligned(pool_keys, 16) || !aligned(scores, 4) ||
+      !aligned(n_pools, 4) || !aligned(cu_pool_cap, 4) || !aligned(pool_start, 4) ||
+      !aligned(pool_ids, 4) || !aligned(token_ids, 4) || (q_seq && !aligned(q_seq, 4)) ||
+      (q_pos && !aligned(q_pos, 4)) || (status_dev && !aligned(status_dev, 4)))
+    return DSA_ERR_MISALIGNED;
+  if (!workspace || ws_bytes < dsa::select_workspace_size(Q, P_ld, select_k))
+    return DSA_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return DSA_ERR_MISALIGNED;
+  if (Q > 65535) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
+// index_scores -> top-k (+ expansion); safe_begin: see dsa::launch_index_scores
+int run_select(const void* q, const float* weights, float scale, const void* pool_keys,
+               int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
+               const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
+               const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
+               int select_k, int out_width, int dtype, float* scores, int32_t* pool_ids,
+               int32_t* token_ids, void* workspace, int32_t* status_dev, cudaStream_t st,
+               const int32_t* safe_begin) {
+  // Decode geometry: the scoring kernel also counts each query's score
+  // histogram into the workspace and the selection starts from it.  Otherwise
+  // the selection kernel builds the histogram itself.
+  const bool hist = dsa::index_fills_histogram(Q, q_seq, H, D, dtype);
+  int r = dsa::launch_index_scores(q, weights, scale, pool_keys, pool_rows, pool_start,
+                                   pool_valid, n_pools, cu_pool_cap, q_seq, q_pos, Q, B, H, D,
+                                   kpool, P_ld, dtype, scores,
+                                   hist ? dsa::topk_workspace_hist(workspace) : nullptr,
+                                   status_dev, st, safe_begin);
+  if (r != DSA_OK) return r;
+  return dsa::launch_select_after_index(scores, Q, P_ld, select_k, pool_ids,
+                                        hist ? workspace : nullptr, pool_start, cu_pool_cap,
+                                        q_seq, B, kpool, out_width, token_ids, status_dev, st);
+}
+
+int check_mla(const void* q_lat, const void* kv_latent, const int32_t* cu_seqlens,
+              const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int Hm, int L,
+              int out_width, float sm_scale, int dtype, void* out, float* lse, void* workspace,
+              size_t ws_bytes, int32_t* status_dev) {
+  if (Q < 0 || B < 0 || Hm < 1 || L < 1 || out_width < 1) return DSA_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype) || !isfinite(sm_scale)) return DSA_ERR_INVALID_ARG;
+  if (L % 8 != 0 || L > 1024 || Hm > 128) return DSA_ERR_UNSUPPORTED;
+  if (Q == 0) return kNoWork;
+  if (B == 0) return DSA_ERR_INVALID_ARG;
+  if (!q_lat || !kv_latent || !cu_seqlens || !token_ids || !out) return DSA_ERR_INVALID_ARG;
+  if (!aligned(q_lat, 16) || !aligned(kv_latent, 16) || !aligned(out, 16) ||
+      !aligned(cu_seqlens, 4) || !aligned(token_ids, 4) || (lse && !aligned(lse, 4)) ||
+      (q_seq && !aligned(q_seq, 4)) || (status_dev && !aligned(status_dev, 4)))
+    return DSA_ERR_MISALIGNED;
+  const size_t need = dsa::mla_workspace_size(Q, Hm, L, out_width, dtype);
+  if (need > 0 && (!workspace || ws_bytes < need)) return DSA_ERR_WORKSPACE;
+  if (workspace && !aligned(workspace, 16)) return DSA_ERR_MISALIGNED;
+  if (Q > 65535) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -37,20 +135,10 @@ int dsa_kpool_compress(const void* k, const void* gate, const uint8_t* valid, co
                        const int32_t* pool_begin, int B, int D, int kpool, int max_pools,
                        int dtype, void* pool_keys, int32_t* pool_start, uint8_t* pool_valid,
                        int32_t* n_pools, int32_t* status_dev, void* stream) {
-  if (B < 0 || max_pools < 0) return DSA_ERR_INVALID_ARG;
-  if (kpool < 1 || kpool > DSA_KPOOL_MAX) return DSA_ERR_INVALID_ARG;  // refuse, never truncate
-  if (!dtype_ok(dtype) || !(ln_eps >= 0.f) || !isfinite(ln_eps)) return DSA_ERR_INVALID_ARG;
-  if (!d_ok(D)) return DSA_ERR_UNSUPPORTED;
-  if (B == 0) return DSA_OK;
-  if (!k || !gate || !valid || !ape || !ln_gamma || !ln_beta || !cu_seqlens || !cu_pool_cap ||
-      !pool_keys || !pool_start || !pool_valid || !n_pools)
-    return DSA_ERR_INVALID_ARG;
-  if (!aligned(k, 16) || !aligned(gate, 16) || !aligned(pool_keys, 16) || !aligned(ln_gamma, 16) ||
-      !aligned(ln_beta, 16) || !aligned(ape, 4) || !aligned(cu_seqlens, 4) ||
-      !aligned(cu_pool_cap, 4) || !aligned(pool_start, 4) || !aligned(n_pools, 4) ||
-      (pool_begin && !aligned(pool_begin, 4)) || (status_dev && !aligned(status_dev, 4)))
-    return DSA_ERR_MISALIGNED;
-  if (B > 65535) return DSA_ERR_UNSUPPORTED;
+  const int r = check_compress(k, gate, valid, ape, ln_gamma, ln_beta, ln_eps, cu_seqlens,
+                               cu_pool_cap, pool_begin, B, D, kpool, max_pools, dtype, pool_keys,
+                               pool_start, pool_valid, n_pools, status_dev);
+  if (r != DSA_OK) return r == kNoWork ? DSA_OK : r;
   return dsa::launch_kpool_compress(k, gate, valid, ape, ln_gamma, ln_beta, ln_eps, cu_seqlens,
                                     cu_pool_cap, pool_begin, B, D, kpool, max_pools, dtype,
                                     pool_keys, pool_start, pool_valid, n_pools, status_dev,
@@ -132,40 +220,15 @@ int dsa_select(const void* q, const float* weights, float scale, const void* poo
                int B, int H, int D, int kpool, int P_ld, int select_k, int out_width, int dtype,
                float* scores, int32_t* pool_ids, int32_t* token_ids, void* workspace,
                size_t ws_bytes, int32_t* status_dev, void* stream) {
-  if (Q < 0 || B < 0 || H < 1 || P_ld < 1 || select_k < 1 || out_width < 1 || pool_rows < 1)
-    return DSA_ERR_INVALID_ARG;
-  if (kpool < 1 || kpool > DSA_KPOOL_MAX) return DSA_ERR_INVALID_ARG;
-  if ((long long)out_width < (long long)select_k * kpool) return DSA_ERR_INVALID_ARG;
-  if (!dtype_ok(dtype) || !(scale > 0.f) || !isfinite(scale)) return DSA_ERR_INVALID_ARG;
-  if (!d_ok(D) || H > 64 || select_k > DSA_SELECT_K_MAX) return DSA_ERR_UNSUPPORTED;
-  if (Q == 0) return DSA_OK;
-  if (B == 0) return DSA_ERR_INVALID_ARG;
-  if (!q || !weights || !pool_keys || !pool_start || !pool_valid || !n_pools || !cu_pool_cap ||
-      !scores || !pool_ids || !token_ids)
-    return DSA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(weights, 16) || !aligned(pool_keys, 16) || !aligned(scores, 4) ||
-      !aligned(n_pools, 4) || !aligned(cu_pool_cap, 4) || !aligned(pool_start, 4) ||
-      !aligned(pool_ids, 4) || !aligned(token_ids, 4) || (q_seq && !aligned(q_seq, 4)) ||
-      (q_pos && !aligned(q_pos, 4)) || (status_dev && !aligned(status_dev, 4)))
-    return DSA_ERR_MISALIGNED;
-  if (!workspace || ws_bytes < dsa::select_workspace_size(Q, P_ld, select_k))
-    return DSA_ERR_WORKSPACE;
-  if (!aligned(workspace, 16)) return DSA_ERR_MISALIGNED;
-  if (Q > 65535) return DSA_ERR_UNSUPPORTED;
-  cudaStream_t st = as_stream(stream);
-  // Decode geometry: the scoring kernel also counts each query's score
-  // histogram into the workspace and the selection starts from it.  Otherwise
-  // the selection kernel builds the histogram itself.
-  const bool hist = dsa::index_fills_histogram(Q, q_seq, H, D, dtype);
-  int r = dsa::launch_index_scores(q, weights, scale, pool_keys, pool_rows, pool_start,
-                                   pool_valid, n_pools, cu_pool_cap, q_seq, q_pos, Q, B, H, D,
-                                   kpool, P_ld, dtype, scores,
-                                   hist ? dsa::topk_workspace_hist(workspace) : nullptr,
-                                   status_dev, st);
-  if (r != DSA_OK) return r;
-  return dsa::launch_select_after_index(scores, Q, P_ld, select_k, pool_ids,
-                                        hist ? workspace : nullptr, pool_start, cu_pool_cap,
-                                        q_seq, B, kpool, out_width, token_ids, status_dev, st);
+  const int r = check_select(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid,
+                             n_pools, cu_pool_cap, q_seq, q_pos, Q, B, H, D, kpool, P_ld,
+                             select_k, out_width, dtype, scores, pool_ids, token_ids, workspace,
+                             ws_bytes, status_dev);
+  if (r != DSA_OK) return r == kNoWork ? DSA_OK : r;
+  return run_select(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid, n_pools,
+                    cu_pool_cap, q_seq, q_pos, Q, B, H, D, kpool, P_ld, select_k, out_width,
+                    dtype, scores, pool_ids, token_ids, workspace, status_dev, as_stream(stream),
+                    nullptr);
 }
 
 size_t dsa_mla_selected_decode_workspace_size(int Q, int Hm, int L, int out_width, int dtype) {
@@ -178,23 +241,70 @@ int dsa_mla_selected_decode(const void* q_lat, const void* kv_latent, const int3
                             int L, int out_width, float sm_scale, int dtype, void* out,
                             float* lse, void* workspace, size_t ws_bytes, int32_t* status_dev,
                             void* stream) {
-  if (Q < 0 || B < 0 || Hm < 1 || L < 1 || out_width < 1) return DSA_ERR_INVALID_ARG;
-  if (!dtype_ok(dtype) || !isfinite(sm_scale)) return DSA_ERR_INVALID_ARG;
-  if (L % 8 != 0 || L > 1024 || Hm > 128) return DSA_ERR_UNSUPPORTED;
-  if (Q == 0) return DSA_OK;
-  if (B == 0) return DSA_ERR_INVALID_ARG;
-  if (!q_lat || !kv_latent || !cu_seqlens || !token_ids || !out) return DSA_ERR_INVALID_ARG;
-  if (!aligned(q_lat, 16) || !aligned(kv_latent, 16) || !aligned(out, 16) ||
-      !aligned(cu_seqlens, 4) || !aligned(token_ids, 4) || (lse && !aligned(lse, 4)) ||
-      (q_seq && !aligned(q_seq, 4)) || (status_dev && !aligned(status_dev, 4)))
-    return DSA_ERR_MISALIGNED;
-  const size_t need = dsa::mla_workspace_size(Q, Hm, L, out_width, dtype);
-  if (need > 0 && (!workspace || ws_bytes < need)) return DSA_ERR_WORKSPACE;
-  if (workspace && !aligned(workspace, 16)) return DSA_ERR_MISALIGNED;
-  if (Q > 65535) return DSA_ERR_UNSUPPORTED;
+  const int r = check_mla(q_lat, kv_latent, cu_seqlens, q_seq, token_ids, Q, B, Hm, L, out_width,
+                          sm_scale, dtype, out, lse, workspace, ws_bytes, status_dev);
+  if (r != DSA_OK) return r == kNoWork ? DSA_OK : r;
   return dsa::launch_mla_selected_decode(q_lat, kv_latent, cu_seqlens, q_seq, token_ids, Q, B, Hm,
                                          L, out_width, sm_scale, dtype, out, lse, workspace,
                                          ws_bytes, status_dev, as_stream(stream));
+}
+
+size_t dsa_decode_layer_workspace_size(const dsa_decode_layer_args* a, size_t* ws_select,
+                                       size_t* ws_mla) {
+  if (!a) return 0;
+  const size_t s = (a->Q > 0 && a->P_ld > 0 && a->select_k > 0)
+                       ? dsa::select_workspace_size(a->Q, a->P_ld, a->select_k)
+                       : 0;
+  const size_t m = (a->Q > 0 && a->Hm > 0 && a->L > 0 && a->out_width > 0 && dtype_ok(a->dtype))
+                       ? dsa::mla_workspace_size(a->Q, a->Hm, a->L, a->out_width, a->dtype)
+                       : 0;
+  if (ws_select) *ws_select = s;
+  if (ws_mla) *ws_mla = m;
+  return s + m;
+}
+
+int dsa_decode_layer(const dsa_decode_layer_args* a, void* stream) {
+  if (!a) return DSA_ERR_INVALID_ARG;
+  // every stage is checked before anything is launched
+  const int rc = check_compress(a->k, a->gate, a->valid, a->ape, a->ln_gamma, a->ln_beta,
+                                a->ln_eps, a->cu_seqlens, a->cu_pool_cap, a->pool_begin, a->B,
+                                a->D, a->kpool, a->max_pools, a->dtype, a->pool_keys,
+                                a->pool_start, a->pool_valid, a->n_pools, a->status_dev);
+  if (rc != DSA_OK && rc != kNoWork) return rc;
+  const int rs = check_select(a->q, a->weights, a->scale, a->pool_keys, a->pool_rows,
+                              a->pool_start, a->pool_valid, a->n_pools, a->cu_pool_cap, a->q_seq,
+                              a->q_pos, a->Q, a->B, a->H, a->D, a->kpool, a->P_ld, a->select_k,
+                              a->out_width, a->dtype, a->scores, a->pool_ids, a->token_ids,
+                              a->ws_select, a->ws_select_bytes, a->status_dev);
+  if (rs != DSA_OK && rs != kNoWork) return rs;
+  const int rm = check_mla(a->q_lat, a->kv_latent, a->cu_seqlens, a->q_seq, a->token_ids, a->Q,
+                           a->B, a->Hm, a->L, a->out_width, a->sm_scale, a->dtype, a->out, a->lse,
+                           a->ws_mla, a->ws_mla_bytes, a->status_dev);
+  if (rm != DSA_OK && rm != kNoWork) return rm;
+  cudaStream_t st = as_stream(stream);
+  int r;
+  if (rc == DSA_OK) {
+    r = dsa::launch_kpool_compress(a->k, a->gate, a->valid, a->ape, a->ln_gamma, a->ln_beta,
+                                   a->ln_eps, a->cu_seqlens, a->cu_pool_cap, a->pool_begin, a->B,
+                                   a->D, a->kpool, a->max_pools, a->dtype, a->pool_keys,
+                                   a->pool_start, a->pool_valid, a->n_pools, a->status_dev, st);
+    if (r != DSA_OK) return r;
+  }
+  if (rs == kNoWork) return DSA_OK;  // no queries: nothing to select or attend
+  // Inside this call the scoring kernel may stream the key tiles below
+  // pool_begin[b] before the compress ends (it does not write them); with no
+  // pool_begin the compress rewrites every pool.
+  r = run_select(a->q, a->weights, a->scale, a->pool_keys, a->pool_rows, a->pool_start,
+                 a->pool_valid, a->n_pools, a->cu_pool_cap, a->q_seq, a->q_pos, a->Q, a->B, a->H,
+                 a->D, a->kpool, a->P_ld, a->select_k, a->out_width, a->dtype, a->scores,
+                 a->pool_ids, a->token_ids, a->ws_select, a->status_dev, st,
+                 rc == DSA_OK ? a->pool_begin : nullptr);
+  if (r != DSA_OK) return r;
+  // the attention's inputs other than the token ids predate this call
+  return dsa::launch_mla_selected_decode(a->q_lat, a->kv_latent, a->cu_seqlens, a->q_seq,
+                                         a->token_ids, a->Q, a->B, a->Hm, a->L, a->out_width,
+                                         a->sm_scale, a->dtype, a->out, a->lse, a->ws_mla,
+                                         a->ws_mla_bytes, a->status_dev, st, true);
 }
 
 }  // extern "C"

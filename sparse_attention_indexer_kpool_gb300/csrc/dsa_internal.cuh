@@ -176,7 +176,7 @@ int launch_index_scores(const void* q, const float* weights, float scale, const 
                         const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
                         const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
                         int dtype, float* scores, uint32_t* score_hist, int32_t* status_dev,
-                        cudaStream_t stream);
+                        cudaStream_t stream, const int32_t* safe_begin = nullptr);
 // tcgen05 index kernel: queries per key tile (1 or 8), 0 when Q does not fit it
 int umma_index_group(int Q, const int32_t* q_seq);
 int launch_index_scores_umma(const void* q, const float* weights, float scale,
@@ -184,8 +184,10 @@ int launch_index_scores_umma(const void* q, const float* weights, float scale,
                              const uint8_t* pool_valid, const int32_t* n_pools,
                              const int32_t* cu_pool_cap, const int32_t* q_seq,
                              const int32_t* q_pos, int Q, int B, int kpool, int P_ld,
-                             float* scores, uint32_t* hist, int32_t* status_dev,
-                             cudaStream_t stream);
+                             float* scores, uint32_t* hist, const int32_t* safe_begin,
+                             int32_t* status_dev, cudaStream_t stream);
+// whether the decode kernel can start streaming before the compress of its call ends
+bool umma_index_early_ok(int Q, const int32_t* q_seq, const int32_t* q_pos);
 // true when launch_index_scores also counts the per-query score histogram
 bool index_fills_histogram(int Q, const int32_t* q_seq, int H, int D, int dtype);
 size_t topk_workspace_size(int Q, int P_ld, int select_k);
@@ -210,12 +212,14 @@ int mla_umma_splits(int out_width);
 int launch_mla_umma(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
                     const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int out_width,
                     float sm_scale, void* out, float* lse, float* part_o, float* part_ml,
-                    int32_t* status_dev, cudaStream_t stream);
+                    bool early, int32_t* status_dev, cudaStream_t stream);
+// early: the caller guarantees that only the token ids come from kernels still in
+// flight (the attention of a fused decode call), so the rest is read before the wait
 int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
                                const int32_t* q_seq, const int32_t* token_ids, int Q, int B,
                                int Hm, int L, int out_width, float sm_scale, int dtype, void* out,
                                float* lse, void* workspace, size_t ws_bytes, int32_t* status_dev,
-                               cudaStream_t stream);
+                               cudaStream_t stream, bool early = false);
 }  // namespace dsa
 
 #define DSA_LAUNCH_CHECK()                          \

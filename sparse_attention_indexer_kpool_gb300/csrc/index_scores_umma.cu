@@ -84,10 +84,16 @@ struct Layout {
   static constexpr size_t w = ctl + ((sizeof(Ctl) + 15) & ~size_t(15));
   static constexpr size_t hist = w + (size_t)Cfg<G>::kBSlots * G * kH * 4;
   static constexpr size_t base = hist + (G == 1 ? (size_t)kHistBins * 4 : 0);
-  __host__ __device__ static size_t prefix(int n_groups) {
-    return base + (size_t)(n_groups < kBaseCache ? n_groups : kBaseCache) * 4;
+  // cache bases, then (early start) the safe tile counts, then the tile prefix
+  __host__ __device__ static size_t cached(int n_groups) {
+    return (size_t)(n_groups < kBaseCache ? n_groups : kBaseCache);
   }
-  static size_t bytes(int n_groups) { return 1024 + prefix(n_groups) + (size_t)(n_groups + 1) * 4; }
+  __host__ __device__ static size_t prefix(int n_groups, bool early) {
+    return base + cached(n_groups) * 4 * (early ? 2 : 1);
+  }
+  static size_t bytes(int n_groups, bool early) {
+    return 1024 + prefix(n_groups, early) + (size_t)(n_groups + 1) * 4;
+  }
 };
 
 struct QMeta {
@@ -151,7 +157,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                              const int32_t* __restrict__ cu_pool_cap,
                              const int32_t* __restrict__ q_seq, const int32_t* __restrict__ q_pos,
                              int Q, int B, int kpool, int P_ld, float* __restrict__ scores,
-                             uint32_t* __restrict__ hist, int32_t* status) {
+                             uint32_t* __restrict__ hist, const int32_t* __restrict__ safe_begin,
+                             int32_t* status) {
   using C = Cfg<G>;
   using LY = Layout<G>;
   constexpr int N = C::N;
@@ -161,8 +168,14 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   float* s_w = reinterpret_cast<float*>(sbase + LY::w);
   uint32_t* s_hist = reinterpret_cast<uint32_t*>(sbase + LY::hist);
   const int n_groups = (Q + G - 1) / G;
+  // Early start (decode, inside one call after the compress of pools
+  // [safe_begin[b], ...)): the tile plan comes from the call's inputs only, and
+  // the key tiles below safe_begin[b], which that compress does not write, are
+  // streamed before the compress has finished.
+  const bool early = G == 1 && safe_begin != nullptr;
   int* s_base = reinterpret_cast<int*>(sbase + LY::base);  // first cache row of group gi
-  int* s_prefix = reinterpret_cast<int*>(sbase + LY::prefix(n_groups));
+  int* s_safe = s_base + LY::cached(n_groups);             // early: tiles readable at once
+  int* s_prefix = reinterpret_cast<int*>(sbase + LY::prefix(n_groups, early));
   volatile int* abort = &ctl.abort;
   const bool use_hist = G == 1 && hist != nullptr;
 
@@ -197,8 +210,10 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   }
   if (use_hist)
     for (int i = threadIdx.x; i < kHistBins; i += kThreadsU) s_hist[i] = 0;
-  pdl_wait();  // the pool cache may come from the kernel just before
-  pdl_launch_dependents();
+  if (!early) {
+    pdl_wait();  // the pool cache may come from the kernel just before
+    pdl_launch_dependents();
+  }
 
   // ---- tiles per query group (its widest candidate range) and their prefix sum
   {
@@ -212,7 +227,23 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     for (int c0 = 0; c0 < n_groups; c0 += kThreadsU) {
       const int gi = c0 + threadIdx.x;
       int n = 0;
-      if (gi < n_groups) {
+      if (gi < n_groups && early) {
+        // every pool of the sequence's slice that a score row can hold
+        const int b = q_seq ? q_seq[gi] : 0;
+        int nt = 0, safe = 0;
+        long long base = 0;
+        if (b >= 0 && b < B) {
+          base = cu_pool_cap[b];
+          const int cap = cu_pool_cap[b + 1] - cu_pool_cap[b];
+          nt = (max(0, min(cap, P_ld)) + kBM - 1) / kBM;
+          safe = min(nt, max(0, safe_begin[b]) / kBM);
+        } else if (blockIdx.x == 0) {
+          flag(status, DSA_DEV_BAD_QSEQ);
+        }
+        s_base[gi] = (int)base;
+        s_safe[gi] = safe;
+        n = nt;
+      } else if (gi < n_groups) {
         int mx = 0;
         for (int u = 0; u < G; ++u) {
           const QMeta m = qmeta(gi * G + u, Q, q_seq, q_pos, n_pools, cu_pool_cap, pool_start, B,
@@ -252,6 +283,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       uint32_t a_par = 0, a_used = 0;  // per ring slot: parity of its next fill, ever filled
       uint32_t b_par = 0, b_used = 0;  // the same for the query block slots
       int stage = 0, gi = 0, seg = 0;
+      bool waited = !early;            // the compress before this kernel is complete
       for (long long t = t_lo; t < t_hi && !*abort; ++seg) {
         while (s_prefix[gi + 1] <= t) ++gi;
         const long long seg_hi = min(t_hi, (long long)s_prefix[gi + 1]);
@@ -276,6 +308,10 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           if (((a_used >> stage) & 1) &&
               !wait_or_abort(&ctl.empty[stage], ((a_par >> stage) & 1) ^ 1, abort, status))
             break;
+          if (!waited && t - s_prefix[gi] >= s_safe[gi]) {
+            pdl_wait();  // this tile may hold a pool the compress rewrites
+            waited = true;
+          }
           const int row = (int)(base0 + (t - s_prefix[gi]) * kBM);
           unsigned char* at = sbase + LY::a + (size_t)stage * kABytes;
           mbar_arrive_expect_tx(&ctl.full[stage], kABytes);
@@ -342,6 +378,14 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     const int half = ew >> 2;
     const int r = quarter * 32 + lane;      // pool row within the tile
     const int qw0 = G == 1 ? 0 : half * GH; // this warp's first query of the group
+    if (early) {
+      pdl_wait();  // n_pools, pool_valid and pool_start of this step
+      pdl_launch_dependents();
+      if (blockIdx.x == 0)  // the range checks the tile plan skipped
+        for (int qi = ew * 32 + lane; qi < Q; qi += kEpiWarps * 32)
+          qmeta(qi, Q, q_seq, q_pos, n_pools, cu_pool_cap, pool_start, B, kpool, P_ld, status,
+                true);
+    }
     int gi = 0, seg = 0;
     long long tc = 0;
     for (long long t = t_lo; t < t_hi; ++seg) {
@@ -486,8 +530,8 @@ int launch_g(const void* q, const float* weights, float scale, const void* pool_
              int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
              const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
              const int32_t* q_pos, int Q, int B, int kpool, int P_ld, float* scores,
-             uint32_t* hist, int32_t* status, cudaStream_t stream) {
-  const size_t smem = Layout<G>::bytes((Q + G - 1) / G);
+             uint32_t* hist, const int32_t* safe_begin, int32_t* status, cudaStream_t stream) {
+  const size_t smem = Layout<G>::bytes((Q + G - 1) / G, safe_begin != nullptr);
   if (smem > (size_t)kSmemMax) return DSA_ERR_UNSUPPORTED;
   CUtensorMap mk, mq;
   if (!make_map(&mk, pool_keys, (uint64_t)pool_rows, kBM)) return DSA_ERR_CUDA;
@@ -509,7 +553,8 @@ int launch_g(const void* q, const float* weights, float scale, const void* pool_
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, index_scores_umma_kernel<G>, mk, mq, weights,
                                            scale, pool_start, pool_valid, n_pools, cu_pool_cap,
-                                           q_seq, q_pos, Q, B, kpool, P_ld, scores, hist, status);
+                                           q_seq, q_pos, Q, B, kpool, P_ld, scores, hist,
+                                           safe_begin, status);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -518,8 +563,13 @@ int launch_g(const void* q, const float* weights, float scale, const void* pool_
 int umma_index_group(int Q, const int32_t* q_seq) {
   // eight queries share every key tile when they all read one sequence
   const int G = (q_seq == nullptr && Q >= 64) ? 8 : 1;
-  const size_t smem = G == 8 ? Layout<8>::bytes((Q + 7) / 8) : Layout<1>::bytes(Q);
+  const size_t smem = G == 8 ? Layout<8>::bytes((Q + 7) / 8, false) : Layout<1>::bytes(Q, false);
   return smem <= (size_t)kSmemMax ? G : 0;
+}
+
+bool umma_index_early_ok(int Q, const int32_t* q_seq, const int32_t* q_pos) {
+  return umma_index_group(Q, q_seq) == 1 && q_pos == nullptr && Q <= kBaseCache &&
+         Layout<1>::bytes(Q, true) <= (size_t)kSmemMax;
 }
 
 int launch_index_scores_umma(const void* q, const float* weights, float scale,
@@ -527,16 +577,17 @@ int launch_index_scores_umma(const void* q, const float* weights, float scale,
                              const uint8_t* pool_valid, const int32_t* n_pools,
                              const int32_t* cu_pool_cap, const int32_t* q_seq,
                              const int32_t* q_pos, int Q, int B, int kpool, int P_ld,
-                             float* scores, uint32_t* hist, int32_t* status_dev,
-                             cudaStream_t stream) {
+                             float* scores, uint32_t* hist, const int32_t* safe_begin,
+                             int32_t* status_dev, cudaStream_t stream) {
   const int G = umma_index_group(Q, q_seq);
   if (G == 8)
     return launch_g<8>(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid, n_pools,
-                       cu_pool_cap, q_seq, q_pos, Q, B, kpool, P_ld, scores, nullptr,
+                       cu_pool_cap, q_seq, q_pos, Q, B, kpool, P_ld, scores, nullptr, nullptr,
                        status_dev, stream);
   if (G == 1)
     return launch_g<1>(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid, n_pools,
-                       cu_pool_cap, q_seq, q_pos, Q, B, kpool, P_ld, scores, hist, status_dev,
+                       cu_pool_cap, q_seq, q_pos, Q, B, kpool, P_ld, scores, hist,
+                       umma_index_early_ok(Q, q_seq, q_pos) ? safe_begin : nullptr, status_dev,
                        stream);
   return DSA_ERR_UNSUPPORTED;
 }

@@ -462,7 +462,7 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
                                const int32_t* q_seq, const int32_t* token_ids, int Q, int B,
                                int Hm, int L, int out_width, float sm_scale, int dtype, void* out,
                                float* lse, void* workspace, size_t ws_bytes, int32_t* status_dev,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, bool early) {
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr.val.programmaticStreamSerializationAllowed = 1;
@@ -477,7 +477,8 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
     float* part_o = n_split > 1 ? static_cast<float*>(workspace) : nullptr;
     float* part_ml = part_o ? part_o + (size_t)Q * Hm * n_split * L : nullptr;
     const int r = launch_mla_umma(q_lat, kv, cu_seqlens, q_seq, token_ids, Q, B, out_width,
-                                  sm_scale, out, lse, part_o, part_ml, status_dev, stream);
+                                  sm_scale, out, lse, part_o, part_ml, early, status_dev,
+                                  stream);
     if (r != DSA_OK || n_split == 1) return r;
     cfg.gridDim = dim3(Hm, Q, 1);
     cfg.blockDim = dim3(128, 1, 1);

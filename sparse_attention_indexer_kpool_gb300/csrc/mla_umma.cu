@@ -89,7 +89,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                     const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ q_seq,
                     const int32_t* __restrict__ token_ids, int B, int W, float sm_scale,
                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
-                    float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* status) {
+                    float* __restrict__ part_o, float* __restrict__ part_ml, int early,
+                    int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char* sb = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   MCtl& c = *reinterpret_cast<MCtl*>(sb + kOffCtl);
@@ -107,9 +108,13 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     tmem_alloc<kTmemCols>(&c.tmem_base);
     tc_fence_before();
   }
-  // every input may come from the kernel just before: wait for it first
-  pdl_wait();
-  pdl_launch_dependents();
+  // Standalone, every input may come from the kernel just before: wait for it
+  // first.  Inside a call whose earlier kernels write only the token ids
+  // (early), the query block and the sequence lookup go ahead of the wait.
+  if (!early) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
 
   // ---- 1. gathers: the query block first (no dependency), then the rows
   const long long qh0 = (long long)qi * kHm + hf * kHh;   // first (query, head) row
@@ -125,6 +130,10 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   if (!seq_ok && split == 0 && hf == 0 && threadIdx.x == 0) flag(status, DSA_DEV_BAD_QSEQ);
   const long long row_base = seq_ok ? cu_seqlens[b] : 0;
   const int Tb = seq_ok ? cu_seqlens[b + 1] - cu_seqlens[b] : 0;
+  if (early) {
+    pdl_wait();  // the token ids of this call
+    pdl_launch_dependents();
+  }
   if (threadIdx.x < kRows) {
     const int j = split * kRows + threadIdx.x;
     int tok = (j < W && seq_ok) ? token_ids[(long long)qi * W + j] : -1;
@@ -289,7 +298,7 @@ bool mla_umma_ok(int Q, int Hm, int L, int out_width, int dtype) {
 int launch_mla_umma(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
                     const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int out_width,
                     float sm_scale, void* out, float* lse, float* part_o, float* part_ml,
-                    int32_t* status_dev, cudaStream_t stream) {
+                    bool early, int32_t* status_dev, cudaStream_t stream) {
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(mla_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -307,7 +316,7 @@ int launch_mla_umma(const void* q_lat, const void* kv, const int32_t* cu_seqlens
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, mla_umma_kernel, (const __nv_bfloat16*)q_lat,
                             (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, out_width,
-                            sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml,
+                            sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml, early ? 1 : 0,
                             status_dev) == cudaSuccess
              ? DSA_OK
              : DSA_ERR_CUDA;

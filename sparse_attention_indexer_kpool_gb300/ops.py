@@ -7,6 +7,8 @@ the path runs in the library's CUDA kernels.
 """
 from __future__ import annotations
 
+import ctypes
+
 import torch
 
 from . import _lib
@@ -185,3 +187,40 @@ def dsa_select_noalloc(q, weights, scale, pool_keys, pool_start, pool_valid, n_p
         _ptr(token_ids, torch.int32, "token_ids"), _ptr(status, torch.int32, "status"),
         _stream(stream))
     _check("dsa_select_noalloc", code)
+
+
+def dsa_decode_layer(k, gate, valid, ape, ln_gamma, ln_beta, ln_eps, cu_seqlens, pool_begin,
+                     max_pools, pool_keys, pool_start, pool_valid, n_pools, cu_pool_cap, q,
+                     weights, scale, q_seq, q_pos, q_lat, kv_latent, sm_scale, kpool, scores,
+                     pool_ids, token_ids, out, lse, ws_select, ws_mla=None, status=None,
+                     stream=None):
+    """dsa_kpool_compress -> dsa_select -> dsa_mla_selected_decode in one call
+    (same outputs); ``ws_select`` must be zero-filled before its first use."""
+    act = k.dtype
+    Q, H, D = q.shape
+    _, Hm, L = q_lat.shape
+    a = _lib.DecodeLayerArgs(
+        k=_ptr(k, act, "k"), gate=_ptr(gate, act, "gate"), valid=_ptr(valid, torch.uint8, "valid"),
+        ape=_ptr(ape, torch.float32, "ape"), ln_gamma=_ptr(ln_gamma, act, "ln_gamma"),
+        ln_beta=_ptr(ln_beta, act, "ln_beta"), ln_eps=float(ln_eps),
+        cu_seqlens=_ptr(cu_seqlens, torch.int32, "cu_seqlens"),
+        pool_begin=_ptr(pool_begin, torch.int32, "pool_begin"), max_pools=int(max_pools),
+        pool_keys=_ptr(pool_keys, act, "pool_keys"), pool_rows=_pool_rows(pool_keys),
+        pool_start=_ptr(pool_start, torch.int32, "pool_start"),
+        pool_valid=_ptr(pool_valid, torch.uint8, "pool_valid"),
+        n_pools=_ptr(n_pools, torch.int32, "n_pools"),
+        cu_pool_cap=_ptr(cu_pool_cap, torch.int32, "cu_pool_cap"), q=_ptr(q, act, "q"),
+        weights=_ptr(weights, torch.float32, "weights"), scale=float(scale),
+        q_seq=_ptr(q_seq, torch.int32, "q_seq"), q_pos=_ptr(q_pos, torch.int32, "q_pos"),
+        q_lat=_ptr(q_lat, act, "q_lat"), kv_latent=_ptr(kv_latent, act, "kv_latent"),
+        sm_scale=float(sm_scale), Q=Q, B=cu_pool_cap.numel() - 1, H=H, D=D, kpool=int(kpool),
+        P_ld=scores.shape[-1], select_k=pool_ids.shape[-1], out_width=token_ids.shape[-1], Hm=Hm,
+        L=L, dtype=_dtype_tag(q), scores=_ptr(scores, torch.float32, "scores"),
+        pool_ids=_ptr(pool_ids, torch.int32, "pool_ids"),
+        token_ids=_ptr(token_ids, torch.int32, "token_ids"), out=_ptr(out, act, "out"),
+        lse=_ptr(lse, torch.float32, "lse"), ws_select=_ptr(ws_select, torch.uint8, "ws_select"),
+        ws_select_bytes=0 if ws_select is None else ws_select.numel(),
+        ws_mla=_ptr(ws_mla, torch.uint8, "ws_mla"),
+        ws_mla_bytes=0 if ws_mla is None else ws_mla.numel(),
+        status_dev=_ptr(status, torch.int32, "status"))
+    _check("dsa_decode_layer", _lib.load().dsa_decode_layer(ctypes.byref(a), _stream(stream)))

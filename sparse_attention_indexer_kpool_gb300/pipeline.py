@@ -89,6 +89,19 @@ def attend(bt: Batch, buf: LayerBuffers, stream=None):
                                 bt.sm_scale, buf.out, buf.lse, buf.ws_mla, buf.status, stream)
 
 
+def decode_layer(bt: Batch, buf: LayerBuffers, pool_begin=None, max_pools=None, stream=None):
+    """compress -> select -> attend as the single fused call (same outputs as
+    run_layer)."""
+    if max_pools is None:
+        max_pools = bt.P_ld
+    ops.dsa_decode_layer(bt.k, bt.gate, bt.valid, bt.ape, bt.ln_gamma, bt.ln_beta, bt.geo.ln_eps,
+                         bt.cu_seqlens, pool_begin, max_pools, buf.pool_keys, buf.pool_start,
+                         buf.pool_valid, buf.n_pools, bt.cu_pool_cap, bt.q, bt.weights, bt.scale,
+                         bt.q_seq, bt.q_pos, bt.q_lat, bt.kv, bt.sm_scale, bt.geo.kpool,
+                         buf.scores, buf.pool_ids, buf.token_ids, buf.out, buf.lse,
+                         buf.ws_select, buf.ws_mla, buf.status, stream)
+
+
 def run_layer(bt: Batch, buf: LayerBuffers, pool_begin=None, max_pools=None, stream=None,
               fused=True):
     compress(bt, buf, pool_begin, max_pools, stream)

@@ -158,3 +158,35 @@ def test_python_binding_fails_loudly_without_cuda_tensors(lib):
     x = torch.zeros(4, 4)
     with pytest.raises(ValueError):
         ops._ptr(x, torch.float32, "x")                          # CPU tensor refused
+
+
+def test_decode_layer_validation(lib):
+    """All three stages are checked on the host before anything is launched."""
+    def args(**kw):
+        a = _lib.DecodeLayerArgs(k=A, gate=A, valid=A, ape=A, ln_gamma=A, ln_beta=A, ln_eps=1e-5,
+                                 cu_seqlens=A, pool_begin=A, max_pools=1, pool_keys=A,
+                                 pool_rows=256, pool_start=A, pool_valid=A, n_pools=A,
+                                 cu_pool_cap=A, q=A, weights=A, scale=0.088, q_seq=A, q_pos=None,
+                                 q_lat=A, kv_latent=A, sm_scale=0.044, Q=4, B=4, H=32, D=128,
+                                 kpool=4, P_ld=64, select_k=16, out_width=64, Hm=64, L=512,
+                                 dtype=0, scores=A, pool_ids=A, token_ids=A, out=A, lse=A,
+                                 ws_select=A, ws_select_bytes=1 << 20, ws_mla=A,
+                                 ws_mla_bytes=1 << 24, status_dev=None)
+        for n, v in kw.items():
+            setattr(a, n, v)
+        return ctypes.byref(a)
+    f = lib.dsa_decode_layer
+    assert f(None, None) == ERR["DSA_ERR_INVALID_ARG"]
+    assert f(args(kpool=9), None) == ERR["DSA_ERR_INVALID_ARG"]            # compress and select
+    assert f(args(k=None), None) == ERR["DSA_ERR_INVALID_ARG"]             # compress input
+    assert f(args(q=A + 8), None) == ERR["DSA_ERR_MISALIGNED"]             # select input
+    assert f(args(ws_select_bytes=1), None) == ERR["DSA_ERR_WORKSPACE"]
+    assert f(args(out_width=63), None) == ERR["DSA_ERR_INVALID_ARG"]       # W < K * kpool
+    assert f(args(kv_latent=None), None) == ERR["DSA_ERR_INVALID_ARG"]     # attention input
+    assert f(args(L=500), None) == ERR["DSA_ERR_UNSUPPORTED"]              # attention geometry
+    s_sel, s_mla = ctypes.c_size_t(), ctypes.c_size_t()
+    tot = lib.dsa_decode_layer_workspace_size(args(Q=4, P_ld=1000, out_width=2048, select_k=512),
+                                              ctypes.byref(s_sel), ctypes.byref(s_mla))
+    assert s_sel.value == lib.dsa_select_workspace_size(4, 1000, 512)
+    assert s_mla.value == lib.dsa_mla_selected_decode_workspace_size(4, 64, 512, 2048, 0)
+    assert tot == s_sel.value + s_mla.value

@@ -321,3 +321,49 @@ def test_mla_tensor_core_many_queries_merge_kernel():
     lengths = [int(x) for x in rng.integers(2100, 4200, 12)]
     bt = synth.make_batch(geo, lengths, [0] * 12, device=DEV, seed=612)
     run_and_check(bt)
+
+
+def _assert_same_outputs(a, b):
+    for name in ("pool_keys", "pool_start", "pool_valid", "n_pools", "scores", "pool_ids",
+                 "token_ids", "out", "lse", "status"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+def test_decode_layer_matches_the_three_calls():
+    """The fused call writes what compress -> select -> attend write, for a full
+    build and for an incremental step (the scoring kernel then starts streaming
+    the key tiles below pool_begin before the compress has finished)."""
+    for bt in (ragged_small(seed=51), synth.single32k(device=DEV, seed=52), synth.tiny(device=DEV)):
+        a = pipeline.LayerBuffers.alloc(bt)
+        b = pipeline.LayerBuffers.alloc(bt)
+        pipeline.decode_layer(bt, a)
+        pipeline.run_layer(bt, b)
+        torch.cuda.synchronize()
+        _assert_same_outputs(a, b)
+        begin = (a.n_pools - 1).clamp(min=0).to(torch.int32)
+        # new content for each sequence's last complete pool, then one decode step
+        for s in range(bt.B):
+            lo = int(bt.cu_seqlens[s]) + bt.pads[s] + max(int(a.n_pools[s]) - 1, 0) * bt.geo.kpool
+            bt.k[lo:lo + bt.geo.kpool] *= -1
+        for buf in (a, b):
+            buf.out.zero_()
+            buf.scores.fill_(7.0)
+        pipeline.decode_layer(bt, a, pool_begin=begin, max_pools=1)
+        pipeline.run_layer(bt, b, pool_begin=begin, max_pools=1)
+        torch.cuda.synchronize()
+        _assert_same_outputs(a, b)
+        assert int(a.status.item()) == 0
+
+
+def test_decode_layer_parity_against_the_oracle():
+    bt = ragged_small(seed=53)
+    buf = pipeline.LayerBuffers.alloc(bt)
+    pipeline.decode_layer(bt, buf)
+    torch.cuda.synchronize()
+    o = oracle_inputs(bt)
+    st = par.check_compress(o, buf)
+    _, st2 = par.check_scores(o, buf)
+    par.check_topk(buf, bt.geo.select_k)
+    st3 = par.check_expand(o, buf)
+    st4 = par.check_mla(o, buf)
+    assert int(buf.status.item()) == (st | st2 | st3 | st4)
