@@ -278,8 +278,9 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   if (warp == 0) {
     // ================= TMA producer =================
     if (lane == 0) {
-      // keys are read once per call: do not let them push the step's other data out of L2
-      const uint64_t keys_policy = l2_policy_evict_first();
+      // decode reads every key once: keep the call's other data in L2 instead; in a
+      // chunk every query group rereads every key tile, so there the keys stay
+      const uint64_t keys_policy = G == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
       uint32_t a_par = 0, a_used = 0;  // per ring slot: parity of its next fill, ever filled
       uint32_t b_par = 0, b_used = 0;  // the same for the query block slots
       int stage = 0, gi = 0, seg = 0;
