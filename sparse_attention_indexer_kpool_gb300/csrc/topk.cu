@@ -402,20 +402,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* out = pool_ids + (long long)q * K;
   int32_t* tok = ex.token_ids ? ex.token_ids + (long long)q * ex.W : nullptr;
   // writes one selected key's pool id and token ids at output slot `pos`
-  auto emit = [&](uint32_t pos, uint64_t key) {
+  // start of a selected pool's tokens (-1 when it cannot be expanded)
+  auto pool_first_token = [&](uint64_t key) -> int {
+    const int p = key_pool(key);
+    return (tok && seq_ok && p < cap) ? pstart[cap_base + p] : -1;
+  };
+  // writes one selected key's pool id and token ids at output slot `pos`
+  auto emit_with = [&](uint32_t pos, uint64_t key, int st) {
     const int p = key_pool(key);
     out[pos] = p;
     if (tok) {
-      int st = -1;
-      if (!seq_ok) {
-      } else if (p >= cap) {
-        flag(ex.status, DSA_DEV_BAD_POOL_ID);
-      } else {
-        st = pstart[cap_base + p];
-      }
+      if (seq_ok && p >= cap) flag(ex.status, DSA_DEV_BAD_POOL_ID);
       for (int s = 0; s < ex.kpool; ++s) tok[pos * ex.kpool + s] = (st >= 0) ? st + s : -1;
     }
   };
+  auto emit = [&](uint32_t pos, uint64_t key) { emit_with(pos, key, pool_first_token(key)); };
   // The lists are exactly the selection only if they agree with the histogram
   // (a workspace that was not zero-filled breaks that); otherwise rank 0 runs an
   // exact select that never looks at the histogram.
@@ -448,10 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // nothing; one call site, so every lane runs the same shuffles
       const uint64_t* lst = is_tie ? all_tie : all_sure;
       const uint32_t nl = act ? (is_tie ? n_tie : n_sure) : 0u;
+      // the pool's first token is fetched before the count, so the two overlap
+      const int st = (act && part == 0) ? pool_first_token(x) : -1;
       const uint32_t c = count_larger(lst, nl, x, part, parts);
       if (act && part == 0) {
-        if (!is_tie) emit(c, x);
-        else if (c < R) emit(n_sure + c, x);
+        if (!is_tie) emit_with(c, x, st);
+        else if (c < R) emit_with(n_sure + c, x, st);
       }
     }
   } else if (rank == 0) {
@@ -568,7 +571,12 @@ size_t topk_workspace_size(int Q, int P_ld, int select_k) {
 }
 size_t select_workspace_size(int Q, int P_ld, int select_k) {
   (void)P_ld; (void)select_k;
-  return align256((size_t)Q * kBins * 4);
+  return align256((size_t)Q * kBins * 4) + 256;  // histograms, then the tile counter
+}
+
+int* select_workspace_counter(void* workspace, int Q) {
+  return reinterpret_cast<int*>(static_cast<unsigned char*>(workspace) +
+                                align256((size_t)Q * kBins * 4));
 }
 
 uint32_t* topk_workspace_hist(void* workspace) { return static_cast<uint32_t*>(workspace); }
