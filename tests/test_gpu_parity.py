@@ -367,3 +367,53 @@ def test_decode_layer_parity_against_the_oracle():
     st3 = par.check_expand(o, buf)
     st4 = par.check_mla(o, buf)
     assert int(buf.status.item()) == (st | st2 | st3 | st4)
+
+
+def test_decode_layer_dirty_workspace_falls_back_exactly():
+    """In the fused call the attention CTAs select from the scoring kernel's
+    histograms; a selection workspace that was not zero-filled must still give
+    the exact selection (flagged), and the call leaves the histograms zeroed."""
+    for fill in (0xFF, 0x01):
+        bt = ragged_small(seed=61)
+        a = pipeline.LayerBuffers.alloc(bt)
+        b = pipeline.LayerBuffers.alloc(bt)
+        a.ws_select.fill_(fill)
+        pipeline.decode_layer(bt, a)
+        pipeline.run_layer(bt, b, fused=False)
+        torch.cuda.synchronize()
+        assert int(a.status.item()) & ops.DEV_HIST_MISMATCH
+        for name in ("scores", "pool_ids", "token_ids", "out", "lse"):
+            assert torch.equal(getattr(a, name), getattr(b, name)), name
+        assert int(a.ws_select[: 4096 * 4 * bt.Q].count_nonzero().item()) == 0
+        a.status.zero_()
+        pipeline.decode_layer(bt, a)                 # clean again: no flag
+        torch.cuda.synchronize()
+        assert int(a.status.item()) == 0
+        _assert_same_outputs(a, b)
+
+
+def test_decode_layer_equal_scores():
+    """Queries whose index weights are zero score every visible pool 0.0: the
+    order among equal scores is pool ascending, in the bin-and-count path (ties
+    on chip) and in the exact paths (more ties than fit on chip; more float4
+    groups with a tie than the attention kernel stages)."""
+    big = Geometry(D=128, H=32, kpool=4, select_k=512, out_width=2048, Hm=64, L=512, dtype="bf16")
+    for bt in (ragged_small(seed=62), synth.single32k(device=DEV, seed=63),
+               synth.make_batch(big, [70000, 3000], [0, 1], device=DEV, seed=64)):
+        bt.weights[0] = 0.0
+        a = pipeline.LayerBuffers.alloc(bt)
+        b = pipeline.LayerBuffers.alloc(bt)
+        pipeline.decode_layer(bt, a)
+        pipeline.run_layer(bt, b, fused=False)
+        torch.cuda.synchronize()
+        _assert_same_outputs(a, b)
+        s0 = a.scores[0]
+        n0 = int(torch.isfinite(s0).sum().item())
+        assert n0 == 0 or bool((s0[torch.isfinite(s0)] == 0).all())
+        k = min(bt.geo.select_k, n0)
+        ids = a.pool_ids[0].cpu().numpy()
+        fin = torch.nonzero(torch.isfinite(s0)).flatten().cpu().numpy()
+        assert np.array_equal(ids[:k], fin[:k]) and (ids[k:] == -1).all()
+        o = oracle_inputs(bt)
+        par.check_topk(a, bt.geo.select_k)
+        par.check_mla(o, a)
