@@ -40,6 +40,10 @@ rule counts a pool when its last token is at or before the query position; the
 attention output stays in latent space with an explicit softmax scale; an empty
 selection gives out = 0, lse = -inf.
 
+The paged-cache attention (the pages' paged decode and its fp8 variant) reads
+its rows through a block table and decodes E4M3 codes with one fp32 scale per
+row: readings of a layout the pages do not give.
+
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 (hand-worked values, closed forms, invariants, brute force on tiny inputs,
 textbook routines).  No function is left unpinned.
@@ -57,6 +61,7 @@ ST_BAD_TOKEN = 1 << 0         # a selected token id outside its sequence
 ST_BAD_POOL_ID = 1 << 3       # a pool id outside its cache slice
 ST_BAD_QSEQ = 1 << 4          # a query's sequence index outside [0, B)
 ST_POOL_RANGE = 1 << 5        # n_pools beyond the cache slice or the score row
+ST_BAD_PAGE = 1 << 8          # paged cache: a token's block outside the table or its page
 
 
 # --------------------------------------------------------------------------
@@ -341,12 +346,99 @@ def mla_selected_decode(q_lat, kv, cu_seqlens, q_seq, token_ids, sm_scale: float
         if sel.size == 0:
             continue
         C = np.asarray(kv[lo + sel], np.float64)          # [n, L]
-        z = sm_scale * (q_lat[i] @ C.T)                   # [Hm, n]
-        m = z.max(axis=1, keepdims=True)
-        e = np.exp(z - m)
-        den = e.sum(axis=1, keepdims=True)
-        out[i] = (e @ C) / den
-        lse[i] = (m + np.log(den))[:, 0]
+        out[i], lse[i] = attend_rows(q_lat[i], C, sm_scale)
+    return round_store(out, dtype), lse, status
+
+
+def attend_rows(q_i, C, sm_scale: float):
+    """Softmax attention of the heads q_i [Hm, L] over the latent rows C [n, L]
+    (n >= 1): z = sm_scale * q_i C^T, out = softmax(z) C, lse = log sum exp z."""
+    z = sm_scale * (q_i @ C.T)                        # [Hm, n]
+    m = z.max(axis=1, keepdims=True)
+    e = np.exp(z - m)
+    den = e.sum(axis=1, keepdims=True)
+    return (e @ C) / den, (m + np.log(den))[:, 0]
+
+
+# --------------------------------------------------------------------------
+# a6 on a paged latent cache (bf16 or fp8 E4M3 rows)
+# --------------------------------------------------------------------------
+def fp8_e4m3_decode(codes) -> np.ndarray:
+    """Values of 8-bit floating-point codes in the E4M3 encoding.
+
+    The attention's fp8 twin (module glm5next_dsa, Constants, KERNEL_KV_LORA_DIM:
+    the mla_paged_decode kernel and its _fp8 variant) stores latent rows in 8
+    bits; the pages do not spell out the encoding, read here as the E4M3 format
+    of the OCP 8-bit floating-point specification: bit 7 is the sign, bits 6..3
+    the exponent with bias 7, bits 2..0 the mantissa.  Exponent 0 encodes the
+    subnormals (m / 8) * 2^-6; exponents 1..15 encode (1 + m / 8) * 2^(e - 7);
+    exponent 15 with mantissa 7 is NaN, and there is no infinity.
+    """
+    c = np.asarray(codes, np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.ldexp(1.0, e - 7))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def mla_paged_decode(q_lat, pages, row_scale, kv_dtype: str, block_table, seq_lens,
+                     page_size: int, q_seq, token_ids, sm_scale: float, dtype: str):
+    """The selected-row attention (a6) reading its latent rows from a paged cache.
+
+    module glm5next_dsa, Modules, attend (the selected-index NoPE MLA paged
+    decode) and Constants, KERNEL_KV_LORA_DIM (its mla_paged_decode kernel and
+    the _fp8 variant).  The pages give no layout; the reading used here:
+
+    * the cache is ``pages`` [n_pages * page_size, L]: page g holds the rows
+      g * page_size .. g * page_size + page_size - 1;
+    * ``block_table`` [B, max_pages]: token t of sequence b lives in page
+      block_table[b, t // page_size], row t % page_size of it;
+    * ``kv_dtype`` "bf16": ``pages`` holds the row values; "fp8_e4m3": ``pages``
+      holds E4M3 codes and a row's value is decode(code) * row_scale[row]
+      (one fp32 scale per physical row).
+
+    A token id at or past seq_lens[b] is skipped and flagged ST_BAD_TOKEN; a
+    token whose block is past the table, or whose page is outside
+    [0, n_pages), is skipped and flagged ST_BAD_PAGE.  The attention over the
+    rows kept is that of ``mla_selected_decode``.
+    """
+    q_lat = np.asarray(q_lat, np.float64)
+    token_ids = np.asarray(token_ids, np.int64)
+    block_table = np.asarray(block_table, np.int64)
+    Q, Hm, L = q_lat.shape
+    B, max_pages = block_table.shape
+    n_pages = pages.shape[0] // page_size
+    out = np.zeros((Q, Hm, L), np.float64)
+    lse = np.full((Q, Hm), -np.inf, np.float64)
+    status = 0
+    for i in range(Q):
+        b = 0 if q_seq is None else int(q_seq[i])
+        if not (0 <= b < B):
+            status |= ST_BAD_QSEQ
+            continue
+        toks = token_ids[i]
+        sel = toks[toks >= 0]
+        if np.any(sel >= int(seq_lens[b])):
+            status |= ST_BAD_TOKEN
+            sel = sel[sel < int(seq_lens[b])]
+        blk = sel // page_size
+        inside = blk < max_pages
+        page = np.where(inside, block_table[b, np.minimum(blk, max_pages - 1)], -1)
+        ok = (page >= 0) & (page < n_pages)
+        if not np.all(ok):
+            status |= ST_BAD_PAGE
+        rows = page[ok] * page_size + sel[ok] % page_size
+        if rows.size == 0:
+            continue
+        if kv_dtype == "fp8_e4m3":
+            C = fp8_e4m3_decode(pages[rows]) * np.asarray(row_scale, np.float64)[rows][:, None]
+        elif kv_dtype == "bf16":
+            C = np.asarray(pages[rows], np.float64)
+        else:
+            raise ValueError(f"unknown kv dtype {kv_dtype!r}")
+        out[i], lse[i] = attend_rows(q_lat[i], C, sm_scale)
     return round_store(out, dtype), lse, status
 
 

@@ -39,8 +39,15 @@ MUTATIONS = {
     "expand_without_base": ("start = int(pool_start[base + p])", "start = int(pool_start[p])"),
     "mla_without_row_base": ("C = np.asarray(kv[lo + sel], np.float64)",
                              "C = np.asarray(kv[sel], np.float64)"),
-    "mla_scale_dropped": ("z = sm_scale * (q_lat[i] @ C.T)", "z = (q_lat[i] @ C.T)"),
+    "mla_scale_dropped": ("z = sm_scale * (q_i @ C.T)", "z = (q_i @ C.T)"),
     "bf16_truncates": ("r = np.rint(x / spacing) * spacing", "r = np.trunc(x / spacing) * spacing"),
+    "paged_row_without_page_size": ("rows = page[ok] * page_size + sel[ok] % page_size",
+                                    "rows = page[ok] + sel[ok] % page_size"),
+    "paged_block_by_modulo": ("blk = sel // page_size", "blk = sel % page_size"),
+    "fp8_bias_8": ("np.ldexp(1.0, e - 7)", "np.ldexp(1.0, e - 8)"),
+    "fp8_subnormals_as_normals": ("np.where(e == 0, (m / 8.0) * 2.0 ** -6,",
+                                  "np.where(e == 0, (1.0 + m / 8.0) * 2.0 ** -7,"),
+    "fp8_row_scale_dropped": ("* np.asarray(row_scale, np.float64)[rows][:, None]", "* 1.0"),
 }
 
 

@@ -436,3 +436,125 @@ def test_mla_bf16_output_rounding():
     kv = np.array([[1.0 + 2 ** -9, 3.0]])
     out, _, _ = _mla(np.ones((1, 1, 2)), kv, [[0]], 1.0, dtype="bf16")
     assert out[0, 0, 0] == 1.0 and out[0, 0, 1] == 3.0
+
+
+# ---------------------------------------------------------------- a6 on a paged cache, fp8 rows
+E4M3_HAND = {0x00: 0.0, 0x38: 1.0, 0xB8: -1.0, 0x3C: 1.5, 0x40: 2.0, 0x7E: 448.0, 0xFE: -448.0,
+             0x08: 2.0 ** -6, 0x0F: 1.875 * 2.0 ** -6, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9}
+
+
+def test_fp8_e4m3_hand_values():
+    # 1.0 = exponent 7 (the bias), mantissa 0; 448 = the largest finite value;
+    # 2^-6 = the smallest normal, 2^-9 = the smallest subnormal
+    codes = np.array(sorted(E4M3_HAND), np.uint8)
+    got = oracle.fp8_e4m3_decode(codes)
+    assert np.array_equal(got, np.array([E4M3_HAND[c] for c in sorted(E4M3_HAND)]))
+    neg0 = oracle.fp8_e4m3_decode(np.array([0x80], np.uint8))[0]
+    assert neg0 == 0.0 and math.copysign(1.0, neg0) < 0
+    nan = np.isnan(oracle.fp8_e4m3_decode(np.arange(256, dtype=np.uint8)))
+    assert np.flatnonzero(nan).tolist() == [0x7F, 0xFF]           # no infinities, two NaNs
+
+
+def test_fp8_e4m3_matches_torch_on_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.fp8_e4m3_decode(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin])
+    assert np.array_equal(np.signbit(got[fin]), np.signbit(ref[fin]))
+
+
+def _paged_layout(rng, lengths, page_size, n_extra=3, fill=None):
+    """Scatter a contiguous cache (rows of sequence b at cu[b] + t) into shuffled
+    pages of page_size rows; unused rows and pages hold other values."""
+    B = len(lengths)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    blocks = [-(-T // page_size) for T in lengths]
+    n_pages = sum(blocks) + n_extra
+    perm = rng.permutation(n_pages)
+    table = np.full((B, max(blocks) + 1), -1, np.int64)
+    rows = np.zeros(n_pages * page_size, np.int64) - 1      # physical row -> contiguous row
+    k = 0
+    for b, T in enumerate(lengths):
+        for blk in range(blocks[b]):
+            g = int(perm[k])
+            k += 1
+            table[b, blk] = g
+            for s in range(page_size):
+                if blk * page_size + s < T:
+                    rows[g * page_size + s] = cu[b] + blk * page_size + s
+    return cu, table, rows
+
+
+def _paged_query(rng, lengths, Q=4, W=12):
+    q_seq = rng.integers(0, len(lengths), Q)
+    tok = np.full((Q, W), -1, np.int64)
+    for i in range(Q):
+        T = lengths[q_seq[i]]
+        n = rng.integers(1, min(W, T) + 1)
+        tok[i, :n] = rng.choice(T, n, replace=False)
+    return q_seq, tok
+
+
+def test_mla_paged_is_the_contiguous_attention_under_any_paging():
+    rng = np.random.default_rng(40)
+    lengths, L, Hm = [13, 5, 30], 8, 3
+    kv = rng.normal(size=(sum(lengths), L))
+    q = rng.normal(size=(4, Hm, L))
+    q_seq, tok = _paged_query(rng, lengths)
+    ref = _mla(q, kv, tok, 0.3, cu=np.concatenate([[0], np.cumsum(lengths)]), q_seq=q_seq)
+    for page_size in (1, 4, 7, 64):
+        cu, table, rows = _paged_layout(rng, lengths, page_size)
+        pages = rng.normal(size=(len(rows), L))
+        pages[rows >= 0] = kv[rows[rows >= 0]]
+        got = oracle.mla_paged_decode(q, pages, None, "bf16", table, lengths, page_size, q_seq,
+                                      tok, 0.3, "f32")
+        assert got[2] == ref[2] == 0
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1]), page_size
+
+
+def test_mla_paged_fp8_rows_are_code_times_row_scale():
+    rng = np.random.default_rng(41)
+    lengths, L, Hm, page_size = [20, 9], 16, 2, 4
+    cu, table, rows = _paged_layout(rng, lengths, page_size)
+    codes = rng.integers(0, 256, size=(len(rows), L)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38                       # no NaN codes
+    scale = rng.uniform(0.01, 3.0, size=len(rows))
+    dec = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    kv = np.zeros((sum(lengths), L))
+    kv[rows[rows >= 0]] = dec[rows >= 0] * scale[rows >= 0][:, None]
+    q = rng.normal(size=(3, Hm, L))
+    q_seq, tok = _paged_query(rng, lengths, Q=3)
+    ref = _mla(q, kv, tok, 0.25, cu=cu, q_seq=q_seq)
+    got = oracle.mla_paged_decode(q, codes, scale, "fp8_e4m3", table, lengths, page_size, q_seq,
+                                  tok, 0.25, "f32")
+    assert np.allclose(got[0], ref[0], rtol=1e-12, atol=1e-12)
+    assert np.allclose(got[1], ref[1], rtol=1e-12, atol=1e-12)
+
+
+def test_mla_paged_bad_page_and_bad_token_skip_the_row():
+    rng = np.random.default_rng(42)
+    lengths, L, page_size = [10, 6], 4, 4
+    cu, table, rows = _paged_layout(rng, lengths, page_size)
+    pages = rng.normal(size=(len(rows), L))
+    q = rng.normal(size=(1, 2, L))
+    tok = np.array([[0, 5, 9, -1]])
+    want = oracle.mla_paged_decode(q, pages, None, "bf16", table, lengths, page_size, [0],
+                                   np.array([[0, 5, -1, -1]]), 1.0, "f32")
+    bad = table.copy()
+    bad[0, 2] = -1                                          # block of token 9: no page
+    got = oracle.mla_paged_decode(q, pages, None, "bf16", bad, lengths, page_size, [0], tok, 1.0,
+                                  "f32")
+    assert got[2] == oracle.ST_BAD_PAGE and np.array_equal(got[0], want[0])
+    bad[0, 2] = len(rows) // page_size                      # page past the cache
+    got = oracle.mla_paged_decode(q, pages, None, "bf16", bad, lengths, page_size, [0], tok, 1.0,
+                                  "f32")
+    assert got[2] == oracle.ST_BAD_PAGE and np.array_equal(got[0], want[0])
+    narrow = table[:, :2]                                   # table too short for token 9
+    got = oracle.mla_paged_decode(q, pages, None, "bf16", narrow, lengths, page_size, [0], tok,
+                                  1.0, "f32")
+    assert got[2] == oracle.ST_BAD_PAGE and np.array_equal(got[0], want[0])
+    got = oracle.mla_paged_decode(q, pages, None, "bf16", table, lengths, page_size, [0],
+                                  np.array([[0, 5, 10, -1]]), 1.0, "f32")   # 10 >= seq_lens[0]
+    assert got[2] == oracle.ST_BAD_TOKEN and np.array_equal(got[0], want[0])
