@@ -71,6 +71,7 @@ extern "C" {
 /* ---- activation dtypes ------------------------------------------------- */
 #define DSA_BF16 0
 #define DSA_F32 1
+#define DSA_FP8_E4M3 2  /* paged latent rows only: 8-bit E4M3 codes, one fp32 scale per row */
 
 /* ---- device status bits (OR-ed into *status_dev) ----------------------- */
 #define DSA_DEV_BAD_TOKEN 1        /* MLA: token id >= T_b; the row is skipped          */
@@ -80,6 +81,8 @@ extern "C" {
 #define DSA_DEV_BAD_QSEQ 16        /* q_seq[q] outside [0, B); the query gets no output  */
 #define DSA_DEV_POOL_RANGE 32      /* index: n_pools[b] > cap_b or > P_ld; clamped       */
 #define DSA_DEV_TIMEOUT 64         /* a bounded wait inside a kernel gave up             */
+#define DSA_DEV_BAD_PAGE 256      /* paged MLA: block past the table or page outside
+                                      [0, n_pages); the row is skipped              */
 #define DSA_DEV_HIST_MISMATCH 128  /* dsa_select: workspace histogram did not match the
                                       scores (workspace not zero-filled); exact fallback ran */
 
@@ -232,6 +235,44 @@ int dsa_mla_selected_decode(const void* q_lat, const void* kv_latent, const int3
                             float* lse, void* workspace, size_t ws_bytes, int32_t* status_dev,
                             void* stream);
 size_t dsa_mla_selected_decode_workspace_size(int Q, int Hm, int L, int out_width, int dtype);
+
+/*
+ * dsa_mla_paged_decode - the selected-row attention above, reading the latent
+ * rows from a paged cache, in bf16 or as 8-bit E4M3 codes.
+ *
+ * Source: module glm5next_dsa, Modules, attend (the launcher of the
+ * selected-index NoPE MLA *paged* decode) and Constants, KERNEL_KV_LORA_DIM
+ * (its kernel mla_paged_decode and the _fp8 twin).  The pages give no layout;
+ * this one is the plain reading:
+ *
+ *   pages [n_pages * page_size, L]: page g holds rows g*page_size ..
+ *     g*page_size + page_size - 1; 16-byte aligned; kv_dtype DSA_BF16, DSA_F32
+ *     or DSA_FP8_E4M3 (E4M3 of the OCP 8-bit floating-point format);
+ *   row_scale [n_pages * page_size] fp32 (DSA_FP8_E4M3 only, else NULL): the
+ *     value of a row is decode(code) * row_scale[row];
+ *   block_table [B, max_pages] int32: token t of sequence b is row
+ *     t % page_size of page block_table[b * max_pages + t / page_size];
+ *   seq_lens [B] int32: token ids at or past seq_lens[b] are flagged.
+ * Every other argument, output and fault is that of dsa_mla_selected_decode.
+ * A token whose block is past the table or whose page is outside [0, n_pages)
+ * is skipped and flagged DSA_DEV_BAD_PAGE.  The library reads the cache and
+ * the table; it owns none of them.
+ * Supported: dtype bf16 with kv_dtype bf16 or E4M3, 64 heads and L = 512 on the
+ * tensor cores; any geometry of dsa_mla_selected_decode on the generic kernel.
+ */
+typedef struct dsa_paged_kv {
+  const void* pages;
+  const float* row_scale;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int n_pages, page_size, max_pages, kv_dtype;
+} dsa_paged_kv;
+int dsa_mla_paged_decode(const void* q_lat, const dsa_paged_kv* kv, const int32_t* q_seq,
+                         const int32_t* token_ids, int Q, int B, int Hm, int L, int out_width,
+                         float sm_scale, int dtype, void* out, float* lse, void* workspace,
+                         size_t ws_bytes, int32_t* status_dev, void* stream);
+size_t dsa_mla_paged_decode_workspace_size(int Q, int Hm, int L, int out_width, int dtype,
+                                           int kv_dtype);
 
 /*
  * dsa_select - index_scores -> topk_pools -> expand_selection in one call.

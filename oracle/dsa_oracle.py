@@ -395,7 +395,7 @@ def mla_paged_decode(q_lat, pages, row_scale, kv_dtype: str, block_table, seq_le
       g * page_size .. g * page_size + page_size - 1;
     * ``block_table`` [B, max_pages]: token t of sequence b lives in page
       block_table[b, t // page_size], row t % page_size of it;
-    * ``kv_dtype`` "bf16": ``pages`` holds the row values; "fp8_e4m3": ``pages``
+    * ``kv_dtype`` "bf16" or "f32": ``pages`` holds the row values; "fp8_e4m3": ``pages``
       holds E4M3 codes and a row's value is decode(code) * row_scale[row]
       (one fp32 scale per physical row).
 
@@ -434,7 +434,7 @@ def mla_paged_decode(q_lat, pages, row_scale, kv_dtype: str, block_table, seq_le
             continue
         if kv_dtype == "fp8_e4m3":
             C = fp8_e4m3_decode(pages[rows]) * np.asarray(row_scale, np.float64)[rows][:, None]
-        elif kv_dtype == "bf16":
+        elif kv_dtype in ("bf16", "f32"):
             C = np.asarray(pages[rows], np.float64)
         else:
             raise ValueError(f"unknown kv dtype {kv_dtype!r}")

@@ -32,6 +32,12 @@ class DecodeLayerArgs(ctypes.Structure):
         ("status_dev", c_void_p)]
 
 
+class PagedKv(ctypes.Structure):
+    """dsa_paged_kv (include/dsa.h), field for field."""
+    _fields_ = [(n, c_void_p) for n in ("pages", "row_scale", "block_table", "seq_lens")] + [
+        (n, c_int) for n in ("n_pages", "page_size", "max_pages", "kv_dtype")]
+
+
 # name -> (restype, argtypes); mirrors include/dsa.h
 SIGNATURES = {
     "dsa_kpool_compress": (c_int, [c_void_p] * 6 + [c_float] + [c_void_p] * 3 + [c_int] * 5
@@ -45,6 +51,10 @@ SIGNATURES = {
     "dsa_mla_selected_decode": (c_int, [c_void_p] * 5 + [c_int] * 5 + [c_float, c_int]
                                 + [c_void_p] * 3 + [c_size_t] + [c_void_p] * 2),
     "dsa_mla_selected_decode_workspace_size": (c_size_t, [c_int] * 5),
+    "dsa_mla_paged_decode": (c_int, [c_void_p, ctypes.POINTER(PagedKv), c_void_p, c_void_p]
+                             + [c_int] * 5 + [c_float, c_int] + [c_void_p] * 3 + [c_size_t]
+                             + [c_void_p] * 2),
+    "dsa_mla_paged_decode_workspace_size": (c_size_t, [c_int] * 6),
     "dsa_select": (c_int, [c_void_p, c_void_p, c_float, c_void_p, c_int] + [c_void_p] * 6
                    + [c_int] * 9 + [c_void_p] * 4 + [c_size_t] + [c_void_p] * 2),
     "dsa_select_workspace_size": (c_size_t, [c_int, c_int, c_int]),

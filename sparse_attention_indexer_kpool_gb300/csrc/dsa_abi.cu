@@ -111,6 +111,34 @@ int check_mla(const void* q_lat, const void* kv_latent, const int32_t* cu_seqlen
   return DSA_OK;
 }
 
+int check_mla_paged(const void* q_lat, const dsa_paged_kv* kv, const int32_t* q_seq,
+                    const int32_t* token_ids, int Q, int B, int Hm, int L, int out_width,
+                    float sm_scale, int dtype, void* out, float* lse, void* workspace,
+                    size_t ws_bytes, int32_t* status_dev) {
+  if (!kv || Q < 0 || B < 0 || Hm < 1 || L < 1 || out_width < 1) return DSA_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype) || !isfinite(sm_scale)) return DSA_ERR_INVALID_ARG;
+  const int kd = kv->kv_dtype;
+  if (kd != DSA_BF16 && kd != DSA_F32 && kd != DSA_FP8_E4M3) return DSA_ERR_INVALID_ARG;
+  if (kv->n_pages < 1 || kv->page_size < 1 || kv->max_pages < 1) return DSA_ERR_INVALID_ARG;
+  if ((kd == DSA_FP8_E4M3) != (kv->row_scale != nullptr)) return DSA_ERR_INVALID_ARG;
+  if (L % 8 != 0 || L > 1024 || Hm > 128) return DSA_ERR_UNSUPPORTED;
+  if ((long long)kv->n_pages * kv->page_size > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+  if (Q == 0) return kNoWork;
+  if (B == 0) return DSA_ERR_INVALID_ARG;
+  if (!q_lat || !kv->pages || !kv->block_table || !kv->seq_lens || !token_ids || !out)
+    return DSA_ERR_INVALID_ARG;
+  if (!aligned(q_lat, 16) || !aligned(kv->pages, 16) || !aligned(out, 16) ||
+      !aligned(kv->block_table, 4) || !aligned(kv->seq_lens, 4) || !aligned(token_ids, 4) ||
+      (kv->row_scale && !aligned(kv->row_scale, 4)) || (lse && !aligned(lse, 4)) ||
+      (q_seq && !aligned(q_seq, 4)) || (status_dev && !aligned(status_dev, 4)))
+    return DSA_ERR_MISALIGNED;
+  const size_t need = dsa::mla_paged_workspace_size(Q, Hm, L, out_width, dtype, kd);
+  if (need > 0 && (!workspace || ws_bytes < need)) return DSA_ERR_WORKSPACE;
+  if (workspace && !aligned(workspace, 16)) return DSA_ERR_MISALIGNED;
+  if (Q > 65535) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -247,6 +275,26 @@ int dsa_mla_selected_decode(const void* q_lat, const void* kv_latent, const int3
   return dsa::launch_mla_selected_decode(q_lat, kv_latent, cu_seqlens, q_seq, token_ids, Q, B, Hm,
                                          L, out_width, sm_scale, dtype, out, lse, workspace,
                                          ws_bytes, status_dev, as_stream(stream));
+}
+
+size_t dsa_mla_paged_decode_workspace_size(int Q, int Hm, int L, int out_width, int dtype,
+                                           int kv_dtype) {
+  if (Q <= 0 || Hm <= 0 || L <= 0 || out_width <= 0 || !dtype_ok(dtype)) return 0;
+  return dsa::mla_paged_workspace_size(Q, Hm, L, out_width, dtype, kv_dtype);
+}
+
+int dsa_mla_paged_decode(const void* q_lat, const dsa_paged_kv* kv, const int32_t* q_seq,
+                         const int32_t* token_ids, int Q, int B, int Hm, int L, int out_width,
+                         float sm_scale, int dtype, void* out, float* lse, void* workspace,
+                         size_t ws_bytes, int32_t* status_dev, void* stream) {
+  const int r = check_mla_paged(q_lat, kv, q_seq, token_ids, Q, B, Hm, L, out_width, sm_scale,
+                                dtype, out, lse, workspace, ws_bytes, status_dev);
+  if (r != DSA_OK) return r == kNoWork ? DSA_OK : r;
+  const dsa::PagedKv pk{kv->pages,    kv->row_scale, kv->block_table, kv->seq_lens,
+                        kv->n_pages,  kv->page_size, kv->max_pages,   kv->kv_dtype};
+  return dsa::launch_mla_paged_decode(q_lat, pk, q_seq, token_ids, Q, B, Hm, L, out_width,
+                                      sm_scale, dtype, out, lse, workspace, ws_bytes, status_dev,
+                                      as_stream(stream));
 }
 
 size_t dsa_decode_layer_workspace_size(const dsa_decode_layer_args* a, size_t* ws_select,

@@ -206,13 +206,30 @@ int launch_expand_selection(const int32_t* pool_ids, const int32_t* pool_start,
                             int select_k, int kpool, int out_width, int32_t* token_ids,
                             int32_t* status_dev, cudaStream_t stream);
 size_t mla_workspace_size(int Q, int Hm, int L, int out_width, int dtype);
+// A paged latent cache (dsa_paged_kv after validation).
+struct PagedKv {
+  const void* pages;
+  const float* row_scale;      // E4M3 only
+  const int32_t* block_table;  // [B, max_pages]
+  const int32_t* seq_lens;     // [B]
+  int n_pages, page_size, max_pages, kv_dtype;
+};
 // tcgen05 attention (bf16, 64 heads, latent 512): one CTA per 128 selected rows
 bool mla_umma_ok(int Q, int Hm, int L, int out_width, int dtype);
 int mla_umma_splits(int out_width);
+// paged: NULL for the contiguous cache (kv + cu_seqlens)
 int launch_mla_umma(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
                     const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int out_width,
                     float sm_scale, void* out, float* lse, float* part_o, float* part_ml,
-                    bool early, int32_t* status_dev, cudaStream_t stream);
+                    bool early, int32_t* status_dev, cudaStream_t stream,
+                    const PagedKv* paged = nullptr);
+// the paged attention: the tcgen05 kernel when mla_umma_ok and the rows are
+// bf16 or E4M3, else the generic kernel
+size_t mla_paged_workspace_size(int Q, int Hm, int L, int out_width, int dtype, int kv_dtype);
+int launch_mla_paged_decode(const void* q_lat, const PagedKv& kv, const int32_t* q_seq,
+                            const int32_t* token_ids, int Q, int B, int Hm, int L, int out_width,
+                            float sm_scale, int dtype, void* out, float* lse, void* workspace,
+                            size_t ws_bytes, int32_t* status_dev, cudaStream_t stream);
 // early: the caller guarantees that only the token ids come from kernels still in
 // flight (the attention of a fused decode call), so the rest is read before the wait
 int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t* cu_seqlens,

@@ -18,6 +18,8 @@
 // softmax is the usual online (running max / running sum) form in base 2.
 // With more than one split, each CTA writes its unnormalised partial and its
 // (max, sum) to the workspace and a small merge kernel combines them.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include "dsa_internal.cuh"
@@ -427,6 +429,108 @@ __global__ void __launch_bounds__(256)
   if (lse && threadIdx.x == 0) lse[(long long)qi * Hm + h] = den > 0.f ? m + logf(den) : -INFINITY;
 }
 
+// Generic kernel on a paged cache: the kernel above with each token's row found
+// through the block table and read as bf16, fp32 or E4M3 code * row scale.
+__device__ __forceinline__ float paged_value(const PagedKv& pk, long long prow, int d, int L) {
+  const long long o = prow * L + d;
+  if (pk.kv_dtype == DSA_BF16)
+    return __bfloat162float(static_cast<const __nv_bfloat16*>(pk.pages)[o]);
+  if (pk.kv_dtype == DSA_F32) return static_cast<const float*>(pk.pages)[o];
+  const __half_raw h =
+      __nv_cvt_fp8_to_halfraw(static_cast<const __nv_fp8_storage_t*>(pk.pages)[o], __NV_E4M3);
+  return __half2float(*reinterpret_cast<const __half*>(&h)) * pk.row_scale[prow];
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+    mla_simt_paged_kernel(const T* __restrict__ q_lat, PagedKv pk,
+                          const int32_t* __restrict__ q_seq, const int32_t* __restrict__ token_ids,
+                          int B, int Hm, int L, int W, float sm_scale, T* __restrict__ out,
+                          float* __restrict__ lse, int32_t* status) {
+  extern __shared__ float sh[];  // q [L] | z [W] | row [W] (int) | red [32]
+  float* sq = sh;
+  float* sz = sh + L;
+  int* srow = reinterpret_cast<int*>(sz + W);
+  float* red = reinterpret_cast<float*>(srow + W);
+  pdl_wait();
+  const int h = blockIdx.x, qi = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int b = q_seq ? q_seq[qi] : 0;
+  const bool seq_ok = b >= 0 && b < B;
+  if (!seq_ok && h == 0 && threadIdx.x == 0) flag(status, DSA_DEV_BAD_QSEQ);
+  const int Tb = seq_ok ? pk.seq_lens[b] : 0;
+  for (int d = threadIdx.x; d < L; d += blockDim.x)
+    sq[d] = Act<T>::to_f(q_lat[((long long)qi * Hm + h) * L + d]);
+  const int32_t* toks = token_ids + (long long)qi * W;
+  for (int j = threadIdx.x; j < W; j += blockDim.x) {
+    const int tok = seq_ok ? toks[j] : -1;
+    int prow = -1;
+    if (tok >= Tb) {
+      if (h == 0) flag(status, DSA_DEV_BAD_TOKEN);
+    } else if (tok >= 0) {
+      const int blk = tok / pk.page_size;
+      const int page = blk < pk.max_pages ? pk.block_table[(long long)b * pk.max_pages + blk] : -1;
+      if (page < 0 || page >= pk.n_pages) {
+        if (h == 0) flag(status, DSA_DEV_BAD_PAGE);
+      } else {
+        prow = page * pk.page_size + tok % pk.page_size;
+      }
+    }
+    srow[j] = prow;
+  }
+  __syncthreads();
+  for (int j = warp; j < W; j += nw) {
+    const int prow = srow[j];
+    float z = -INFINITY;
+    if (prow >= 0) {
+      float acc = 0.f;
+      for (int d = lane; d < L; d += 32) acc = fmaf(paged_value(pk, prow, d, L), sq[d], acc);
+      z = warp_sum(acc) * sm_scale;
+    }
+    if (lane == 0) sz[j] = z;
+  }
+  __syncthreads();
+  float mx = -INFINITY;
+  for (int j = threadIdx.x; j < W; j += blockDim.x) mx = fmaxf(mx, sz[j]);
+  mx = warp_max(mx);
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = -INFINITY;
+    for (int w = 0; w < nw; ++w) m = fmaxf(m, red[w]);
+    red[0] = m;
+  }
+  __syncthreads();
+  const float m = red[0];
+  __syncthreads();
+  float den = 0.f;
+  for (int j = threadIdx.x; j < W; j += blockDim.x) {
+    const float e = (m == -INFINITY || sz[j] == -INFINITY) ? 0.f : expf(sz[j] - m);
+    sz[j] = e;
+    den += e;
+  }
+  den = warp_sum(den);
+  if (lane == 0) red[warp] = den;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < nw; ++w) s += red[w];
+    red[0] = s;
+  }
+  __syncthreads();
+  den = red[0];
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  for (int d = threadIdx.x; d < L; d += blockDim.x) {
+    float acc = 0.f;
+    for (int j = 0; j < W; ++j) {
+      const float e = sz[j];
+      if (e != 0.f) acc = fmaf(e, paged_value(pk, srow[j], d, L), acc);
+    }
+    out[((long long)qi * Hm + h) * L + d] = Act<T>::from_f(acc * inv);
+  }
+  if (lse && threadIdx.x == 0) lse[(long long)qi * Hm + h] = den > 0.f ? m + logf(den) : -INFINITY;
+}
+
 bool fast_path(int Hm, int L, int dtype) { return dtype == DSA_BF16 && L == kL && Hm % kHG == 0; }
 
 // Split count: (query, head group, split) CTAs covering the SMs once at most;
@@ -534,6 +638,71 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
     e = cudaLaunchKernelEx(&cfg, mla_simt_kernel<float>, (const float*)q_lat, (const float*)kv,
                            cu_seqlens, q_seq, token_ids, B, Hm, L, out_width, sm_scale,
                            (float*)out, lse, status_dev);
+  }
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+namespace {
+bool paged_umma(int Q, int Hm, int L, int out_width, int dtype, int kv_dtype) {
+  return mla_umma_ok(Q, Hm, L, out_width, dtype) &&
+         (kv_dtype == DSA_BF16 || kv_dtype == DSA_FP8_E4M3);
+}
+}  // namespace
+
+size_t mla_paged_workspace_size(int Q, int Hm, int L, int out_width, int dtype, int kv_dtype) {
+  if (!paged_umma(Q, Hm, L, out_width, dtype, kv_dtype)) return 0;
+  const int n_split = mla_umma_splits(out_width);
+  if (n_split == 1) return 0;
+  const size_t slots = (size_t)Q * Hm * n_split;
+  return slots * L * 4 + slots * 2 * 4;
+}
+
+int launch_mla_paged_decode(const void* q_lat, const PagedKv& kv, const int32_t* q_seq,
+                            const int32_t* token_ids, int Q, int B, int Hm, int L, int out_width,
+                            float sm_scale, int dtype, void* out, float* lse, void* workspace,
+                            size_t ws_bytes, int32_t* status_dev, cudaStream_t stream) {
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (paged_umma(Q, Hm, L, out_width, dtype, kv.kv_dtype)) {
+    const int n_split = mla_umma_splits(out_width);
+    if (ws_bytes < mla_paged_workspace_size(Q, Hm, L, out_width, dtype, kv.kv_dtype))
+      return DSA_ERR_WORKSPACE;
+    float* part_o = n_split > 1 ? static_cast<float*>(workspace) : nullptr;
+    float* part_ml = part_o ? part_o + (size_t)Q * Hm * n_split * L : nullptr;
+    const int r = launch_mla_umma(q_lat, nullptr, nullptr, q_seq, token_ids, Q, B, out_width,
+                                  sm_scale, out, lse, part_o, part_ml, false, status_dev, stream,
+                                  &kv);
+    if (r != DSA_OK || n_split == 1) return r;
+    cfg.gridDim = dim3(Hm, Q, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, mla_merge_kernel, (const float*)part_o,
+                              (const float*)part_ml, Hm, n_split, (__nv_bfloat16*)out,
+                              lse) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  }
+  if (L % 8 != 0 || L > 1024 || Hm > 128 || out_width > 16384) return DSA_ERR_UNSUPPORTED;
+  const size_t smem = ((size_t)L + 2 * (size_t)out_width + 32) * 4;
+  cfg.gridDim = dim3(Hm, Q, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaError_t e;
+  if (dtype == DSA_BF16) {
+    cudaFuncSetAttribute(mla_simt_paged_kernel<__nv_bfloat16>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaLaunchKernelEx(&cfg, mla_simt_paged_kernel<__nv_bfloat16>,
+                           (const __nv_bfloat16*)q_lat, kv, q_seq, token_ids, B, Hm, L, out_width,
+                           sm_scale, (__nv_bfloat16*)out, lse, status_dev);
+  } else {
+    cudaFuncSetAttribute(mla_simt_paged_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)smem);
+    e = cudaLaunchKernelEx(&cfg, mla_simt_paged_kernel<float>, (const float*)q_lat, kv, q_seq,
+                           token_ids, B, Hm, L, out_width, sm_scale, (float*)out, lse,
+                           status_dev);
   }
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

@@ -25,6 +25,16 @@
 //      per-head max and sum (or, with a single split, the normalised output and
 //      lse go straight to the outputs); the merge kernel combines the splits.
 // Waits on the MMA completions are bounded (DSA_DEV_TIMEOUT on expiry).
+//
+// The same kernel reads a paged cache (Modules, attend: the paged decode; a
+// block table maps a token to its page) in bf16 or as E4M3 codes with one fp32
+// scale per row (Constants, KERNEL_KV_LORA_DIM: the _fp8 twin).  E4M3 codes
+// convert exactly to bf16 while they are gathered, so the tensor cores see the
+// codes; the row's scale multiplies its logit and its probability in the P^T
+// tile, and the softmax sum stays that of the unscaled probabilities:
+//   z = s * <q, code row>,  O = sum_r p_r * s_r * code_r / sum_r p_r.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include <mutex>
@@ -43,11 +53,18 @@ constexpr int kPtBlock = kHh * 128;     // 32 heads x 64 rows, 4 KB
 constexpr int kTmemCols = 256;          // S^T (32 columns) + O^T (4 x 32 columns)
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Row sources of the kernel.
+constexpr int kKvContig = 0;   // bf16 rows at cu_seqlens[b] + tok
+constexpr int kKvPaged = 1;    // bf16 rows through the block table
+constexpr int kKvPagedE4M3 = 2;  // E4M3 rows through the block table, one fp32 scale per row
+
 struct MCtl {
   uint64_t s_ready, o_ready;
   uint32_t tmem_base;
   int pad;
   int tok[kRows];
+  int prow[kRows];   // the row of the cache (-1: none)
+  float rs[kRows];   // E4M3: the row's scale
   float red[2][4][16];  // [head quarter pair][row quarter][head]: per-warp partials
   float m_fin[kHh], l_fin[kHh];
 };
@@ -58,6 +75,15 @@ constexpr size_t kOffCtl = kOffPt + 2 * (size_t)kPtBlock;
 constexpr size_t kSmemBytes = 1024 + kOffCtl + sizeof(MCtl);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert((size_t)kHh * kL * 4 <= 8 * (size_t)kKvBlock, "O staging fits the row tile");
+
+// Two E4M3 codes (low byte first) -> two bf16 (low half first), exactly: every
+// E4M3 value is a half and a bfloat16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  const __nv_bfloat162 v = __floats2bfloat162_rn(f.x, f.y);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
 
 // 16 values per lane (one row, 16 heads) reduced over the warp's 32 rows; lanes
 // l and l + 16 end with the reduction of head l.  A plain exchange across the
@@ -84,13 +110,14 @@ __device__ __forceinline__ float transpose_reduce16(float (&v)[16], int lane) {
   return v[0];
 }
 
+template <int kKv>
 __global__ void __launch_bounds__(kThreadsM, 1)
     mla_umma_kernel(const __nv_bfloat16* __restrict__ q_lat, const __nv_bfloat16* __restrict__ kv,
                     const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ q_seq,
                     const int32_t* __restrict__ token_ids, int B, int W, float sm_scale,
                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                     float* __restrict__ part_o, float* __restrict__ part_ml, int early,
-                    int32_t* status) {
+                    PagedKv pk, int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char* sb = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   MCtl& c = *reinterpret_cast<MCtl*>(sb + kOffCtl);
@@ -128,8 +155,14 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   const int b = q_seq ? q_seq[qi] : 0;
   const bool seq_ok = b >= 0 && b < B;
   if (!seq_ok && split == 0 && hf == 0 && threadIdx.x == 0) flag(status, DSA_DEV_BAD_QSEQ);
-  const long long row_base = seq_ok ? cu_seqlens[b] : 0;
-  const int Tb = seq_ok ? cu_seqlens[b + 1] - cu_seqlens[b] : 0;
+  long long row_base = 0;
+  int Tb = 0;
+  if (kKv == kKvContig) {
+    row_base = seq_ok ? cu_seqlens[b] : 0;
+    Tb = seq_ok ? cu_seqlens[b + 1] - cu_seqlens[b] : 0;
+  } else {
+    Tb = seq_ok ? pk.seq_lens[b] : 0;
+  }
   if (early) {
     pdl_wait();  // the token ids of this call
     pdl_launch_dependents();
@@ -141,15 +174,67 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       if (hf == 0) flag(status, DSA_DEV_BAD_TOKEN);
       tok = -1;
     }
-    c.tok[threadIdx.x] = tok < 0 ? -1 : tok;
+    tok = tok < 0 ? -1 : tok;
+    long long prow = tok >= 0 ? row_base + tok : -1;
+    if (kKv != kKvContig && tok >= 0) {
+      const int blk = tok / pk.page_size;
+      const int page = blk < pk.max_pages ? pk.block_table[(long long)b * pk.max_pages + blk] : -1;
+      if (page < 0 || page >= pk.n_pages) {
+        if (hf == 0) flag(status, DSA_DEV_BAD_PAGE);
+        tok = -1;
+        prow = -1;
+      } else {
+        prow = (long long)page * pk.page_size + tok % pk.page_size;
+      }
+    }
+    c.tok[threadIdx.x] = tok;
+    c.prow[threadIdx.x] = (int)prow;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < kRows * 64; i += kThreadsM) {
-    const int r = i >> 6, ch = i & 63;
-    const int tok = c.tok[r];
-    const bool ok = tok >= 0;
-    cp_async16(smem_u32(sb + kOffKv + (ch >> 3) * kKvBlock + r * 128 + (((ch & 7) ^ (r & 7)) << 4)),
-               ok ? kv + (row_base + tok) * kL + ch * 8 : kv, ok);
+  if (kKv != kKvPagedE4M3) {
+    const __nv_bfloat16* src =
+        kKv == kKvContig ? kv : static_cast<const __nv_bfloat16*>(pk.pages);
+    for (int i = threadIdx.x; i < kRows * 64; i += kThreadsM) {
+      const int r = i >> 6, ch = i & 63;
+      const int prow = c.prow[r];
+      const bool ok = prow >= 0;
+      cp_async16(
+          smem_u32(sb + kOffKv + (ch >> 3) * kKvBlock + r * 128 + (((ch & 7) ^ (r & 7)) << 4)),
+          ok ? src + (long long)prow * kL + ch * 8 : src, ok);
+    }
+  } else {
+    // 16 codes per 16-byte load, every load of the tile in flight at once; each
+    // load becomes two 16-byte bf16 chunks of the swizzled tile
+    const uint4* src = static_cast<const uint4*>(pk.pages);
+    constexpr int kPer = kRows * (kL / 16) / kThreadsM;  // 16 loads per thread
+    uint4 raw[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = u * kThreadsM + threadIdx.x;
+      const int prow = c.prow[i >> 5];
+      raw[u] = prow >= 0 ? __ldg(src + (long long)prow * (kL / 16) + (i & 31))
+                         : make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (threadIdx.x < kRows) {
+      const int prow = c.prow[threadIdx.x];
+      c.rs[threadIdx.x] = prow >= 0 ? pk.row_scale[prow] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = u * kThreadsM + threadIdx.x;
+      const int r = i >> 5, c16 = i & 31;
+      const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int ch = 2 * c16 + half;
+        const uint4 v = make_uint4(e4m3x2_to_bf16x2(w[2 * half] & 0xffffu),
+                                   e4m3x2_to_bf16x2(w[2 * half] >> 16),
+                                   e4m3x2_to_bf16x2(w[2 * half + 1] & 0xffffu),
+                                   e4m3x2_to_bf16x2(w[2 * half + 1] >> 16));
+        *reinterpret_cast<uint4*>(sb + kOffKv + (ch >> 3) * kKvBlock + r * 128 +
+                                  (((ch & 7) ^ (r & 7)) << 4)) = v;
+      }
+    }
   }
   cp_async_commit();
   cp_async_wait<0>();
@@ -181,7 +266,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   float z[16];
   tmem_ld16(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(hq * 16), z);
   const bool row_ok = c.tok[r] >= 0 && ok;
-  const float zs = sm_scale * kLog2e;
+  const float rs = kKv == kKvPagedE4M3 ? c.rs[r] : 1.f;  // the row's E4M3 scale
+  const float zs = kKv == kKvPagedE4M3 ? sm_scale * kLog2e * rs : sm_scale * kLog2e;
 #pragma unroll
   for (int i = 0; i < 16; ++i) z[i] = row_ok ? z[i] * zs : -INFINITY;
   {
@@ -206,7 +292,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     p[i] = (m == -INFINITY || z[i] == -INFINITY) ? 0.f : exp2f(z[i] - m);
     *reinterpret_cast<__nv_bfloat16*>(sb + kOffPt + (r >> 6) * kPtBlock + h * 128 +
                                       ((((r & 63) >> 3) ^ (h & 7)) << 4) + (r & 7) * 2) =
-        __float2bfloat16_rn(p[i]);
+        __float2bfloat16_rn(kKv == kKvPagedE4M3 ? p[i] * rs : p[i]);
   }
   {
     const float l = transpose_reduce16<false>(p, lane);
@@ -295,13 +381,15 @@ bool mla_umma_ok(int Q, int Hm, int L, int out_width, int dtype) {
          (long long)Q * mla_umma_splits(out_width) * (kHm / kHh) <= 4LL * kNumSMs;
 }
 
-int launch_mla_umma(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
-                    const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int out_width,
-                    float sm_scale, void* out, float* lse, float* part_o, float* part_ml,
-                    bool early, int32_t* status_dev, cudaStream_t stream) {
+namespace {
+template <int kKv>
+int launch_kind(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
+                const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int out_width,
+                float sm_scale, void* out, float* lse, float* part_o, float* part_ml, bool early,
+                const PagedKv& pk, int32_t* status_dev, cudaStream_t stream) {
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute(mla_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(mla_umma_kernel<kKv>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)kSmemBytes);
   });
   cudaLaunchAttribute attr;
@@ -314,12 +402,30 @@ int launch_mla_umma(const void* q_lat, const void* kv, const int32_t* cu_seqlens
   cfg.stream = stream;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_umma_kernel, (const __nv_bfloat16*)q_lat,
+  return cudaLaunchKernelEx(&cfg, mla_umma_kernel<kKv>, (const __nv_bfloat16*)q_lat,
                             (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, out_width,
                             sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml, early ? 1 : 0,
-                            status_dev) == cudaSuccess
+                            pk, status_dev) == cudaSuccess
              ? DSA_OK
              : DSA_ERR_CUDA;
+}
+}  // namespace
+
+int launch_mla_umma(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
+                    const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int out_width,
+                    float sm_scale, void* out, float* lse, float* part_o, float* part_ml,
+                    bool early, int32_t* status_dev, cudaStream_t stream, const PagedKv* paged) {
+  if (!paged)
+    return launch_kind<kKvContig>(q_lat, kv, cu_seqlens, q_seq, token_ids, Q, B, out_width,
+                                  sm_scale, out, lse, part_o, part_ml, early, PagedKv{},
+                                  status_dev, stream);
+  if (paged->kv_dtype == DSA_FP8_E4M3)
+    return launch_kind<kKvPagedE4M3>(q_lat, nullptr, nullptr, q_seq, token_ids, Q, B, out_width,
+                                     sm_scale, out, lse, part_o, part_ml, early, *paged,
+                                     status_dev, stream);
+  return launch_kind<kKvPaged>(q_lat, nullptr, nullptr, q_seq, token_ids, Q, B, out_width,
+                               sm_scale, out, lse, part_o, part_ml, early, *paged, status_dev,
+                               stream);
 }
 
 }  // namespace dsa

@@ -13,10 +13,10 @@ import torch
 
 from . import _lib
 
-DSA_BF16, DSA_F32 = 0, 1
+DSA_BF16, DSA_F32, DSA_FP8_E4M3 = 0, 1, 2
 DEV_BAD_TOKEN, DEV_POOL_OVERFLOW, DEV_POOL_UNCOVERED = 1, 2, 4
 DEV_BAD_POOL_ID, DEV_BAD_QSEQ, DEV_POOL_RANGE, DEV_TIMEOUT = 8, 16, 32, 64
-DEV_HIST_MISMATCH = 128
+DEV_HIST_MISMATCH, DEV_BAD_PAGE = 128, 256
 
 
 class DsaError(RuntimeError):
@@ -140,6 +140,46 @@ def dsa_mla_selected_decode(q_lat, kv_latent, cu_seqlens, q_seq, token_ids, sm_s
         0 if workspace is None else workspace.numel(), _ptr(status, torch.int32, "status"),
         _stream(stream))
     _check("dsa_mla_selected_decode", code)
+
+
+def _kv_tag(pages: torch.Tensor) -> int:
+    if pages.dtype == torch.bfloat16:
+        return DSA_BF16
+    if pages.dtype == torch.float32:
+        return DSA_F32
+    if pages.dtype in (torch.float8_e4m3fn, torch.uint8):
+        return DSA_FP8_E4M3
+    raise TypeError(f"pages must be bfloat16, float32 or float8_e4m3fn, got {pages.dtype}")
+
+
+def mla_paged_workspace_bytes(q_lat, pages, out_width) -> int:
+    Q, Hm, L = q_lat.shape
+    return int(_lib.load().dsa_mla_paged_decode_workspace_size(
+        Q, Hm, L, int(out_width), _dtype_tag(q_lat), _kv_tag(pages)))
+
+
+def dsa_mla_paged_decode(q_lat, pages, row_scale, block_table, seq_lens, page_size, q_seq,
+                         token_ids, sm_scale, out, lse, workspace=None, status=None, stream=None):
+    """``pages`` [n_pages * page_size, L] (bf16, fp32, or float8_e4m3fn / uint8 codes with
+    ``row_scale`` [n_pages * page_size] fp32); ``block_table`` [B, max_pages] int32."""
+    Q, Hm, L = q_lat.shape
+    if pages.dim() != 2 or pages.shape[1] != L or pages.shape[0] % int(page_size) != 0:
+        raise ValueError("pages must be [n_pages * page_size, L]")
+    if block_table.dim() != 2 or seq_lens.numel() != block_table.shape[0]:
+        raise ValueError("block_table must be [B, max_pages] and seq_lens [B]")
+    act = q_lat.dtype
+    kv = _lib.PagedKv(_ptr(pages, pages.dtype, "pages"), _ptr(row_scale, torch.float32, "row_scale"),
+                      _ptr(block_table, torch.int32, "block_table"),
+                      _ptr(seq_lens, torch.int32, "seq_lens"), pages.shape[0] // int(page_size),
+                      int(page_size), block_table.shape[1], _kv_tag(pages))
+    code = _lib.load().dsa_mla_paged_decode(
+        _ptr(q_lat, act, "q_lat"), ctypes.byref(kv), _ptr(q_seq, torch.int32, "q_seq"),
+        _ptr(token_ids, torch.int32, "token_ids"), Q, block_table.shape[0], Hm, L,
+        token_ids.shape[-1], float(sm_scale), _dtype_tag(q_lat), _ptr(out, act, "out"),
+        _ptr(lse, torch.float32, "lse"), _ptr(workspace, torch.uint8, "workspace"),
+        0 if workspace is None else workspace.numel(), _ptr(status, torch.int32, "status"),
+        _stream(stream))
+    _check("dsa_mla_paged_decode", code)
 
 
 def select_workspace_bytes(Q, P_ld, select_k) -> int:

@@ -232,3 +232,60 @@ def prefill(device="cpu", seed=4000, n_query=4096, ctx=131072) -> Batch:
     T = ctx + n_query
     return make_batch(GEO_PREFILL, [T], [0], device=device, seed=seed, queries="chunk",
                       q_positions=list(range(ctx, T)))
+
+
+@dataclass
+class PagedCache:
+    """A latent cache laid out in pages (the paged attention's input)."""
+    pages: torch.Tensor          # [n_pages * page_size, L] bf16 / fp32, or float8_e4m3fn codes
+    row_scale: torch.Tensor | None   # [n_pages * page_size] fp32 (E4M3 only)
+    block_table: torch.Tensor    # [B, max_pages] int32
+    seq_lens: torch.Tensor       # [B] int32
+    page_size: int
+
+
+def paged_cache(kv, cu_seqlens, page_size: int, *, e4m3=False, seed=0, n_spare=3,
+                extra_blocks=1) -> PagedCache:
+    """Lay the contiguous cache ``kv`` [sum T_b, L] (sequence b at rows
+    cu_seqlens[b] ..) out in shuffled pages of ``page_size`` rows.
+
+    Block i of sequence b (tokens i*page_size ..) goes to a page drawn from a
+    seeded permutation; ``n_spare`` pages and the rows past each sequence's
+    last token hold other values, and the table has ``extra_blocks`` unused
+    (-1) columns.  e4m3: each row is stored as E4M3 codes of row / s with
+    s = max|row| / 448 (1 for an all-zero row), s kept per row.
+    """
+    dev = kv.device
+    cu = [int(x) for x in cu_seqlens.tolist()]
+    B, L = len(cu) - 1, kv.shape[1]
+    lengths = [cu[b + 1] - cu[b] for b in range(B)]
+    blocks = [-(-T // page_size) for T in lengths]
+    n_pages = sum(blocks) + n_spare
+    g = _gen(dev, seed)
+    perm = torch.randperm(n_pages, generator=g, device=dev)
+    table = torch.full((B, max(blocks) + extra_blocks), -1, dtype=torch.int32, device=dev)
+    src, dst = [], []
+    k = 0
+    for b in range(B):
+        if blocks[b]:
+            table[b, :blocks[b]] = perm[k:k + blocks[b]].to(torch.int32)
+        k += blocks[b]
+        t = torch.arange(lengths[b], device=dev)
+        src.append(cu[b] + t)
+        dst.append(table[b, t // page_size].long() * page_size + t % page_size)
+    src, dst = torch.cat(src), torch.cat(dst)
+    n_rows = n_pages * page_size
+    filler = _normal((n_rows, L), 1.0, g, dev, torch.float32)
+    seq_lens = torch.tensor(lengths, dtype=torch.int32, device=dev)
+    if not e4m3:
+        pages = filler.to(kv.dtype)
+        pages[dst] = kv[src]
+        return PagedCache(pages, None, table, seq_lens, page_size)
+    rows = kv[src].float()
+    s = rows.abs().amax(dim=1) / 448.0
+    s = torch.where(s > 0, s, torch.ones_like(s))
+    scale = torch.rand(n_rows, generator=g, device=dev) + 0.5
+    codes = (filler * 100.0).clamp(-448, 448).to(torch.float8_e4m3fn)
+    codes[dst] = (rows / s[:, None]).to(torch.float8_e4m3fn)
+    scale[dst] = s
+    return PagedCache(codes, scale.float(), table, seq_lens, page_size)

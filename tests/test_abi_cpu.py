@@ -133,6 +133,46 @@ def test_mla_validation(lib):
     assert f(A, A, A, A, A, 0, 4, 64, 512, 2048, 0.04, 0, A, A, A, ws, None, None) == ERR["DSA_OK"]
 
 
+def test_mla_paged_validation(lib):
+    f = lib.dsa_mla_paged_decode
+    fp8 = header_define("DSA_FP8_E4M3")
+    assert header_define("DSA_DEV_BAD_PAGE") == 256
+    ws = lib.dsa_mla_paged_decode_workspace_size(4, 64, 512, 2048, 0, fp8)   # tensor cores, split
+    assert ws > 0 and ws == lib.dsa_mla_paged_decode_workspace_size(4, 64, 512, 2048, 0, 0)
+    assert lib.dsa_mla_paged_decode_workspace_size(4, 64, 512, 2048, 0, 1) == 0   # generic kernel
+    assert lib.dsa_mla_paged_decode_workspace_size(4, 32, 512, 2048, 0, fp8) == 0
+
+    def kv(**kw):
+        a = dict(pages=A, row_scale=A, block_table=A, seq_lens=A, n_pages=100, page_size=64,
+                 max_pages=8, kv_dtype=fp8)
+        a.update(kw)
+        return ctypes.byref(_lib.PagedKv(a["pages"], a["row_scale"], a["block_table"],
+                                         a["seq_lens"], a["n_pages"], a["page_size"],
+                                         a["max_pages"], a["kv_dtype"]))
+
+    def call(k, Q=4, L=512, sm=0.04, out=A, ws_bytes=ws, q_seq=A):
+        return f(A, k, q_seq, A, Q, 4, 64, L, 2048, sm, 0, out, A, A, ws_bytes, None, None)
+
+    assert call(kv(), ws_bytes=ws - 1) == ERR["DSA_ERR_WORKSPACE"]
+    assert call(kv(row_scale=None)) == ERR["DSA_ERR_INVALID_ARG"]          # E4M3 needs scales
+    assert call(kv(kv_dtype=0)) == ERR["DSA_ERR_INVALID_ARG"]              # bf16 takes none
+    assert call(kv(kv_dtype=7)) == ERR["DSA_ERR_INVALID_ARG"]
+    assert call(kv(page_size=0)) == ERR["DSA_ERR_INVALID_ARG"]
+    assert call(kv(n_pages=0)) == ERR["DSA_ERR_INVALID_ARG"]
+    assert call(kv(max_pages=0)) == ERR["DSA_ERR_INVALID_ARG"]
+    assert call(kv(block_table=None)) == ERR["DSA_ERR_INVALID_ARG"]
+    assert call(kv(seq_lens=None)) == ERR["DSA_ERR_INVALID_ARG"]
+    assert call(kv(n_pages=1 << 20, page_size=1 << 12)) == ERR["DSA_ERR_UNSUPPORTED"]
+    assert call(kv(pages=A + 8)) == ERR["DSA_ERR_MISALIGNED"]
+    assert call(kv(block_table=A + 2)) == ERR["DSA_ERR_MISALIGNED"]
+    assert call(kv(), out=A + 8) == ERR["DSA_ERR_MISALIGNED"]
+    assert call(kv(), L=500) == ERR["DSA_ERR_UNSUPPORTED"]
+    assert call(kv(), sm=float("inf")) == ERR["DSA_ERR_INVALID_ARG"]
+    assert f(A, None, A, A, 4, 4, 64, 512, 2048, 0.04, 0, A, A, A, ws, None, None) \
+        == ERR["DSA_ERR_INVALID_ARG"]
+    assert call(kv(), Q=0) == ERR["DSA_OK"]                                   # nothing to do
+
+
 def test_select_validation(lib):
     f = lib.dsa_select
     ws = lib.dsa_select_workspace_size(4, 1000, 16)

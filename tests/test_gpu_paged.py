@@ -1,0 +1,133 @@
+"""The selected-row attention on a paged latent cache (module glm5next_dsa,
+Modules, attend: the paged decode, and Constants, KERNEL_KV_LORA_DIM: its fp8
+twin).  bf16 / fp32 pages give exactly the contiguous attention (the same
+kernel reads the same rows); E4M3 pages match the oracle; blocks past the table
+and pages outside the cache are flagged and skipped."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_attention_indexer_kpool_gb300 import ops, pipeline, synth
+from sparse_attention_indexer_kpool_gb300.synth import Geometry
+from tests._parity import mla_tol
+from tests._util import npf, npi
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def ragged_small(seed):
+    geo = Geometry(D=128, H=32, kpool=4, select_k=64, out_width=320, Hm=64, L=512, dtype="bf16")
+    return synth.make_batch(geo, [1203, 0, 3, 23, 50, 2500], [5, 0, 0, 0, 50, 1], device=DEV,
+                            seed=seed)
+
+
+def run_paged(bt, token_ids, pc):
+    Q, Hm, L = bt.q_lat.shape
+    out = torch.full((Q, Hm, L), 7.0, dtype=bt.q_lat.dtype, device=DEV)
+    lse = torch.full((Q, Hm), 7.0, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    n = ops.mla_paged_workspace_bytes(bt.q_lat, pc.pages, token_ids.shape[1])
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=DEV)
+    ops.dsa_mla_paged_decode(bt.q_lat, pc.pages, pc.row_scale, pc.block_table, pc.seq_lens,
+                             pc.page_size, bt.q_seq, token_ids, bt.sm_scale, out, lse, ws, st)
+    torch.cuda.synchronize()
+    return out, lse, int(st.item())
+
+
+def oracle_paged(bt, token_ids, pc, block_table=None, seq_lens=None):
+    e4 = pc.row_scale is not None
+    pages = pc.pages.view(torch.uint8).cpu().numpy() if e4 else npf(pc.pages)
+    kd = "fp8_e4m3" if e4 else ("bf16" if pc.pages.dtype == torch.bfloat16 else "f32")
+    return oracle.mla_paged_decode(
+        npf(bt.q_lat), pages, npf(pc.row_scale) if e4 else None, kd,
+        npi(pc.block_table if block_table is None else block_table),
+        npi(pc.seq_lens if seq_lens is None else seq_lens), pc.page_size, npi(bt.q_seq),
+        npi(token_ids), bt.sm_scale, bt.geo.dtype)
+
+
+def assert_close(out, lse, ref, dtype):
+    ref_out, ref_lse, _ = ref
+    got = out.cpu().double().numpy()
+    err = np.abs(got - ref_out)
+    assert np.all(err <= mla_tol(ref_out, dtype)), f"attention out error {err.max():.3g}"
+    lse = lse.cpu().double().numpy()
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(lse), fin)
+    assert np.all(np.abs(lse[fin] - ref_lse[fin]) <= 1e-3 * np.maximum(1.0, np.abs(ref_lse[fin])))
+
+
+def contiguous(bt):
+    buf = pipeline.LayerBuffers.alloc(bt)
+    pipeline.run_layer(bt, buf)
+    torch.cuda.synchronize()
+    return buf
+
+
+@pytest.mark.parametrize("which", ["ragged_small", "single32k", "tiny"])
+def test_paged_rows_give_exactly_the_contiguous_attention(which):
+    bt = {"ragged_small": lambda: ragged_small(71), "single32k": lambda: synth.single32k(DEV, 72),
+          "tiny": lambda: synth.tiny(DEV)}[which]()
+    buf = contiguous(bt)
+    for i, page_size in enumerate((64, 16, 1)):
+        pc = synth.paged_cache(bt.kv, bt.cu_seqlens, page_size, seed=80 + i)
+        out, lse, st = run_paged(bt, buf.token_ids, pc)
+        assert st == 0
+        assert torch.equal(out, buf.out), page_size
+        assert torch.equal(lse, buf.lse), page_size
+
+
+@pytest.mark.parametrize("which", ["ragged_small", "single32k", "tiny"])
+def test_paged_e4m3_rows_match_the_oracle(which):
+    bt = {"ragged_small": lambda: ragged_small(73), "single32k": lambda: synth.single32k(DEV, 74),
+          "tiny": lambda: synth.tiny(DEV)}[which]()
+    buf = contiguous(bt)
+    for page_size in (64, 5):
+        pc = synth.paged_cache(bt.kv, bt.cu_seqlens, page_size, e4m3=True, seed=90)
+        out, lse, st = run_paged(bt, buf.token_ids, pc)
+        ref = oracle_paged(bt, buf.token_ids, pc)
+        assert st == ref[2]
+        assert_close(out, lse, ref, bt.geo.dtype)
+
+
+@pytest.mark.parametrize("e4m3", [False, True])
+def test_paged_bad_pages_and_tokens_are_flagged_and_skipped(e4m3):
+    bt = ragged_small(75)
+    buf = contiguous(bt)
+    pc = synth.paged_cache(bt.kv, bt.cu_seqlens, 16, e4m3=e4m3, seed=91)
+    n_pages = pc.pages.shape[0] // pc.page_size
+    tok = buf.token_ids.clone()
+    # query 0 (sequence 0): a block with no page, a page past the cache
+    b0 = int(bt.q_seq[0]) if bt.q_seq is not None else 0
+    t0, t1 = int(tok[0, 0]), int(tok[0, 4])
+    table = pc.block_table.clone()
+    table[b0, t0 // 16] = -1
+    table[b0, t1 // 16] = n_pages + 5
+    bad = synth.PagedCache(pc.pages, pc.row_scale, table, pc.seq_lens, pc.page_size)
+    out, lse, st = run_paged(bt, tok, bad)
+    ref = oracle_paged(bt, tok, bad)
+    assert st == ref[2] and st & ops.DEV_BAD_PAGE
+    assert_close(out, lse, ref, bt.geo.dtype)
+    # a table too narrow for the longest sequence, and a sequence shorter than its ids
+    narrow = pc.block_table[:, :40].contiguous()
+    lens = pc.seq_lens.clone()
+    lens[int(bt.q_seq[-1])] = 100
+    short = synth.PagedCache(pc.pages, pc.row_scale, narrow, lens, pc.page_size)
+    out, lse, st = run_paged(bt, tok, short)
+    ref = oracle_paged(bt, tok, short)
+    assert st == ref[2] and st & ops.DEV_BAD_PAGE and st & ops.DEV_BAD_TOKEN
+    assert_close(out, lse, ref, bt.geo.dtype)
+
+
+def test_paged_e4m3_long262k_layer():
+    """The 262k decode layer (4 x 262144 tokens, 2048 selected rows per query) on
+    an E4M3 cache in pages of 64 rows, every query against the oracle."""
+    bt = synth.long262k(DEV, layer=0)
+    buf = contiguous(bt)
+    pc = synth.paged_cache(bt.kv, bt.cu_seqlens, 64, e4m3=True, seed=92)
+    del bt.k, bt.gate
+    out, lse, st = run_paged(bt, buf.token_ids, pc)
+    assert st == 0
+    ref = oracle_paged(bt, buf.token_ids, pc)
+    assert_close(out, lse, ref, bt.geo.dtype)
