@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--breakdown", action="store_true",
                     help="diagnostic: per-stage in-graph times (extra events between stages)")
+    ap.add_argument("--no-paged", action="store_true",
+                    help="skip the paged / E4M3 attention leg")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the prefill-chunk scoring measurement")
     return ap.parse_args()
@@ -231,6 +233,72 @@ def prefill_index(peaks_path, reps=10):
             os.path.exists(peaks_path) else "fallback", "frac": round(tf / peak, 4),
             "score_bytes": int(buf.scores.numel() * 4),
             "timing": "median of %d launches, L2 flushed before each" % reps}
+
+
+def paged_attention(reps=20, page_size=64):
+    """The selected-row attention of the 64-sequence ragged decode batch (64
+    queries, T_b ~ U{4096..65536}, 2048 selected rows each: 128 MiB of bf16
+    rows, well past the L2) on the contiguous bf16 cache and on paged caches
+    (pages of 64 rows) in bf16 and E4M3: one call each (attention and merge
+    kernels), L2 flushed before every timed call.  The token ids are the
+    batch's own selection."""
+    import torch
+
+    from sparse_attention_indexer_kpool_gb300 import ops, pipeline, synth
+    bt = synth.ragged64(device="cuda")
+    buf = pipeline.LayerBuffers.alloc(bt)
+    pipeline.run_layer(bt, buf)
+    torch.cuda.synchronize()
+    assert int(buf.status.item()) == 0
+    del bt.k, bt.gate
+    Q, Hm, L = bt.q_lat.shape
+    W = buf.token_ids.shape[1]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(buf.out)
+    lse = torch.empty_like(buf.lse)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pcs = {"paged_bf16": synth.paged_cache(bt.kv, bt.cu_seqlens, page_size, seed=5),
+           "paged_e4m3": synth.paged_cache(bt.kv, bt.cu_seqlens, page_size, e4m3=True, seed=6)}
+    ws = torch.empty(max(ops.mla_paged_workspace_bytes(bt.q_lat, bt.kv, W), 16),
+                     dtype=torch.uint8, device="cuda")
+    calls = {"contiguous_bf16": lambda: ops.dsa_mla_selected_decode(
+        bt.q_lat, bt.kv, bt.cu_seqlens, bt.q_seq, buf.token_ids, bt.sm_scale, out, lse,
+        buf.ws_mla, st)}
+    for name, pc in pcs.items():
+        calls[name] = (lambda pc=pc: ops.dsa_mla_paged_decode(
+            bt.q_lat, pc.pages, pc.row_scale, pc.block_table, pc.seq_lens, pc.page_size,
+            bt.q_seq, buf.token_ids, bt.sm_scale, out, lse, ws, st))
+    fixed = W * 4 + 2 * Hm * L * 2 + Hm * 4          # ids, q, out, lse per query
+    per_query = {"contiguous_bf16": W * L * 2 + fixed,
+                 "paged_bf16": W * L * 2 + W * 4 + fixed,
+                 "paged_e4m3": W * L + W * 4 + W * 4 + fixed}
+    res = {}
+    for name, f in calls.items():
+        for _ in range(3):
+            f()
+        times = []
+        for _ in range(reps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            f()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        us = statistics.median(times) * 1e3
+        nbytes = per_query[name] * Q
+        res[name] = {"us": round(us, 2), "bytes": nbytes,
+                     "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
+    assert int(st.item()) == 0, "device status set by the attention"
+    return {"workload": "64-sequence ragged decode batch: %d queries x %d selected rows, %d heads, "
+                        "latent %d, pages of %d rows" % (Q, W, Hm, L, page_size),
+            "kernels": {"contiguous_bf16": "mla_mma_kernel (mma.sync, 16-head groups) + merge",
+                        "paged_bf16": "mla_umma_kernel (tcgen05, paged rows) + merge",
+                        "paged_e4m3": "mla_umma_kernel (tcgen05, E4M3 rows) + merge"},
+            "calls": res,
+            "bytes": "per call: rows (bf16 2 B, E4M3 1 B per value; E4M3 adds a 4 B row "
+                     "scale), 4 B token id and (paged) 4 B table entry per row, q, out, lse",
+            "timing": "median of %d calls, L2 flushed before each" % reps}
 
 
 def run_ours(args, dist):
@@ -507,6 +575,8 @@ def run_ours(args, dist):
         out["breakdown"] = breakdown
     if not args.no_prefill:
         out["prefill_index"] = prefill_index(peaks_path)
+    if not args.no_paged:
+        out["paged_attention"] = paged_attention()
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(layers[0], args.cpu_seconds)
     if dist.rank == 0:

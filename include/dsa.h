@@ -258,7 +258,8 @@ size_t dsa_mla_selected_decode_workspace_size(int Q, int Hm, int L, int out_widt
  * is skipped and flagged DSA_DEV_BAD_PAGE.  The library reads the cache and
  * the table; it owns none of them.
  * Supported: dtype bf16 with kv_dtype bf16 or E4M3, 64 heads and L = 512 on the
- * tensor cores; any geometry of dsa_mla_selected_decode on the generic kernel.
+ * tensor cores (any number of queries); any geometry of dsa_mla_selected_decode
+ * on the generic kernel.
  */
 typedef struct dsa_paged_kv {
   const void* pages;

@@ -216,6 +216,7 @@ struct PagedKv {
 };
 // tcgen05 attention (bf16, 64 heads, latent 512): one CTA per 128 selected rows
 bool mla_umma_ok(int Q, int Hm, int L, int out_width, int dtype);
+bool mla_umma_shape_ok(int Hm, int L, int dtype);  // the geometry alone, any number of queries
 int mla_umma_splits(int out_width);
 // paged: NULL for the contiguous cache (kv + cu_seqlens)
 int launch_mla_umma(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
@@ -223,8 +224,8 @@ int launch_mla_umma(const void* q_lat, const void* kv, const int32_t* cu_seqlens
                     float sm_scale, void* out, float* lse, float* part_o, float* part_ml,
                     bool early, int32_t* status_dev, cudaStream_t stream,
                     const PagedKv* paged = nullptr);
-// the paged attention: the tcgen05 kernel when mla_umma_ok and the rows are
-// bf16 or E4M3, else the generic kernel
+// the paged attention: the tcgen05 kernel for its geometry (any number of
+// queries) and bf16 or E4M3 rows, else the generic kernel
 size_t mla_paged_workspace_size(int Q, int Hm, int L, int out_width, int dtype, int kv_dtype);
 int launch_mla_paged_decode(const void* q_lat, const PagedKv& kv, const int32_t* q_seq,
                             const int32_t* token_ids, int Q, int B, int Hm, int L, int out_width,

@@ -377,8 +377,11 @@ int mla_umma_splits(int out_width) { return (out_width + kRows - 1) / kRows; }
 // four waves of CTAs; many queries keep the 16-head-group kernel, whose splits
 // adapt to Q.
 bool mla_umma_ok(int Q, int Hm, int L, int out_width, int dtype) {
-  return dtype == DSA_BF16 && Hm == kHm && L == kL &&
+  return mla_umma_shape_ok(Hm, L, dtype) &&
          (long long)Q * mla_umma_splits(out_width) * (kHm / kHh) <= 4LL * kNumSMs;
+}
+bool mla_umma_shape_ok(int Hm, int L, int dtype) {
+  return dtype == DSA_BF16 && Hm == kHm && L == kL;
 }
 
 namespace {

@@ -275,17 +275,18 @@ def paged_cache(kv, cu_seqlens, page_size: int, *, e4m3=False, seed=0, n_spare=3
         dst.append(table[b, t // page_size].long() * page_size + t % page_size)
     src, dst = torch.cat(src), torch.cat(dst)
     n_rows = n_pages * page_size
-    filler = _normal((n_rows, L), 1.0, g, dev, torch.float32)
     seq_lens = torch.tensor(lengths, dtype=torch.int32, device=dev)
     if not e4m3:
-        pages = filler.to(kv.dtype)
+        pages = torch.randn((n_rows, L), generator=g, device=dev, dtype=kv.dtype)
         pages[dst] = kv[src]
         return PagedCache(pages, None, table, seq_lens, page_size)
-    rows = kv[src].float()
-    s = rows.abs().amax(dim=1) / 448.0
-    s = torch.where(s > 0, s, torch.ones_like(s))
+    codes = (torch.randn((n_rows, L), generator=g, device=dev, dtype=torch.bfloat16) * 100.0
+             ).clamp(-448, 448).to(torch.float8_e4m3fn)
     scale = torch.rand(n_rows, generator=g, device=dev) + 0.5
-    codes = (filler * 100.0).clamp(-448, 448).to(torch.float8_e4m3fn)
-    codes[dst] = (rows / s[:, None]).to(torch.float8_e4m3fn)
-    scale[dst] = s
+    for c0 in range(0, src.numel(), 1 << 20):           # bounded float32 temporaries
+        rows = kv[src[c0:c0 + (1 << 20)]].float()
+        s = rows.abs().amax(dim=1) / 448.0
+        s = torch.where(s > 0, s, torch.ones_like(s))
+        codes[dst[c0:c0 + (1 << 20)]] = (rows / s[:, None]).to(torch.float8_e4m3fn)
+        scale[dst[c0:c0 + (1 << 20)]] = s
     return PagedCache(codes, scale.float(), table, seq_lens, page_size)

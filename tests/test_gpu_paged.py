@@ -120,6 +120,27 @@ def test_paged_bad_pages_and_tokens_are_flagged_and_skipped(e4m3):
     assert_close(out, lse, ref, bt.geo.dtype)
 
 
+@pytest.mark.parametrize("e4m3", [False, True])
+def test_paged_many_queries_on_the_tensor_cores(e4m3):
+    """64 decode queries x 2048 rows: more than four waves of attention CTAs
+    (the contiguous call takes its other tensor-core kernel there; the paged one
+    keeps the tcgen05 kernel), sampled queries against the oracle."""
+    geo = Geometry(D=128, H=32, kpool=4, select_k=512, out_width=2048, Hm=64, L=512,
+                   dtype="bf16")
+    rng = np.random.default_rng(5)
+    lengths = [int(x) for x in rng.integers(2100, 4000, 64)]
+    bt = synth.make_batch(geo, lengths, [0] * 64, device=DEV, seed=93)
+    buf = contiguous(bt)
+    pc = synth.paged_cache(bt.kv, bt.cu_seqlens, 64, e4m3=e4m3, seed=94)
+    out, lse, st = run_paged(bt, buf.token_ids, pc)
+    assert st == 0
+    rows = [0, 17, 40, 63]
+    idx = torch.as_tensor(rows, device=DEV)
+    sub = synth.Batch(**{**bt.__dict__, "q_lat": bt.q_lat[idx], "q_seq": bt.q_seq[idx]})
+    ref = oracle_paged(sub, buf.token_ids[idx], pc)
+    assert_close(out[idx], lse[idx], ref, "bf16")
+
+
 def test_paged_e4m3_long262k_layer():
     """The 262k decode layer (4 x 262144 tokens, 2048 selected rows per query) on
     an E4M3 cache in pages of 64 rows, every query against the oracle."""
