@@ -224,6 +224,13 @@ int launch_mla_umma(const void* q_lat, const void* kv, const int32_t* cu_seqlens
                     float sm_scale, void* out, float* lse, float* part_o, float* part_ml,
                     bool early, int32_t* status_dev, cudaStream_t stream,
                     const PagedKv* paged = nullptr);
+// streaming tcgen05 attention (same geometry, many queries): one CTA per query
+// and range of 128-row tiles, all 64 heads, online softmax; splits of the tiles
+int mla_stream_splits(int Q, int out_width);
+int launch_mla_stream(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
+                      const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int out_width,
+                      float sm_scale, void* out, float* lse, float* part_o, float* part_ml,
+                      int32_t* status_dev, cudaStream_t stream, const PagedKv* paged = nullptr);
 // the paged attention: the tcgen05 kernel for its geometry (any number of
 // queries) and bf16 or E4M3 rows, else the generic kernel
 size_t mla_paged_workspace_size(int Q, int Hm, int L, int out_width, int dtype, int kv_dtype);

@@ -553,6 +553,8 @@ size_t mla_workspace_size(int Q, int Hm, int L, int out_width, int dtype) {
   int n_split = 1;
   if (mla_umma_ok(Q, Hm, L, out_width, dtype)) {
     n_split = mla_umma_splits(out_width);
+  } else if (mla_umma_shape_ok(Hm, L, dtype)) {
+    n_split = mla_stream_splits(Q, out_width);
   } else if (fast_path(Hm, L, dtype)) {
     int rows;
     split_plan(Q, Hm, out_width, &n_split, &rows);
@@ -583,6 +585,22 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
     const int r = launch_mla_umma(q_lat, kv, cu_seqlens, q_seq, token_ids, Q, B, out_width,
                                   sm_scale, out, lse, part_o, part_ml, early, status_dev,
                                   stream);
+    if (r != DSA_OK || n_split == 1) return r;
+    cfg.gridDim = dim3(Hm, Q, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, mla_merge_kernel, (const float*)part_o,
+                              (const float*)part_ml, Hm, n_split, (__nv_bfloat16*)out,
+                              lse) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  }
+  if (mla_umma_shape_ok(Hm, L, dtype)) {  // many queries: the streaming tcgen05 kernel
+    const int n_split = mla_stream_splits(Q, out_width);
+    if (n_split > 1 && ws_bytes < mla_workspace_size(Q, Hm, L, out_width, dtype))
+      return DSA_ERR_WORKSPACE;
+    float* part_o = n_split > 1 ? static_cast<float*>(workspace) : nullptr;
+    float* part_ml = part_o ? part_o + (size_t)Q * Hm * n_split * L : nullptr;
+    const int r = launch_mla_stream(q_lat, kv, cu_seqlens, q_seq, token_ids, Q, B, out_width,
+                                    sm_scale, out, lse, part_o, part_ml, status_dev, stream);
     if (r != DSA_OK || n_split == 1) return r;
     cfg.gridDim = dim3(Hm, Q, 1);
     cfg.blockDim = dim3(128, 1, 1);
@@ -643,8 +661,8 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
 }
 
 namespace {
-// The paged calls have no other tensor-core kernel, so the tcgen05 one takes
-// every query count (more than four waves of CTAs included).
+// The paged calls run the tcgen05 kernels at every query count: the one-tile
+// kernel for few queries, the streaming one beyond four waves of its CTAs.
 bool paged_umma(int Q, int Hm, int L, int out_width, int dtype, int kv_dtype) {
   (void)Q;
   (void)out_width;
@@ -654,7 +672,8 @@ bool paged_umma(int Q, int Hm, int L, int out_width, int dtype, int kv_dtype) {
 
 size_t mla_paged_workspace_size(int Q, int Hm, int L, int out_width, int dtype, int kv_dtype) {
   if (!paged_umma(Q, Hm, L, out_width, dtype, kv_dtype)) return 0;
-  const int n_split = mla_umma_splits(out_width);
+  const int n_split = mla_umma_ok(Q, Hm, L, out_width, dtype) ? mla_umma_splits(out_width)
+                                                              : mla_stream_splits(Q, out_width);
   if (n_split == 1) return 0;
   const size_t slots = (size_t)Q * Hm * n_split;
   return slots * L * 4 + slots * 2 * 4;
@@ -672,14 +691,19 @@ int launch_mla_paged_decode(const void* q_lat, const PagedKv& kv, const int32_t*
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   if (paged_umma(Q, Hm, L, out_width, dtype, kv.kv_dtype)) {
-    const int n_split = mla_umma_splits(out_width);
+    // few queries: one CTA per 128 rows and 32 heads; many: the streaming kernel
+    const bool few = mla_umma_ok(Q, Hm, L, out_width, dtype);
+    const int n_split = few ? mla_umma_splits(out_width) : mla_stream_splits(Q, out_width);
     if (ws_bytes < mla_paged_workspace_size(Q, Hm, L, out_width, dtype, kv.kv_dtype))
       return DSA_ERR_WORKSPACE;
     float* part_o = n_split > 1 ? static_cast<float*>(workspace) : nullptr;
     float* part_ml = part_o ? part_o + (size_t)Q * Hm * n_split * L : nullptr;
-    const int r = launch_mla_umma(q_lat, nullptr, nullptr, q_seq, token_ids, Q, B, out_width,
-                                  sm_scale, out, lse, part_o, part_ml, false, status_dev, stream,
-                                  &kv);
+    const int r = few ? launch_mla_umma(q_lat, nullptr, nullptr, q_seq, token_ids, Q, B,
+                                        out_width, sm_scale, out, lse, part_o, part_ml, false,
+                                        status_dev, stream, &kv)
+                      : launch_mla_stream(q_lat, nullptr, nullptr, q_seq, token_ids, Q, B,
+                                          out_width, sm_scale, out, lse, part_o, part_ml,
+                                          status_dev, stream, &kv);
     if (r != DSA_OK || n_split == 1) return r;
     cfg.gridDim = dim3(Hm, Q, 1);
     cfg.blockDim = dim3(128, 1, 1);

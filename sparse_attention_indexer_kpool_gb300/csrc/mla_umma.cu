@@ -370,6 +370,373 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   }
 }
 
+// ---- streaming form: many queries ------------------------------------------
+// One CTA = one query, all 64 heads, and a range of 128-row tiles taken in
+// turn; the output accumulator O^T stays in TMEM across the tiles and the
+// softmax is the online one (running max and sum per head).  Each tile:
+// gather the rows (the next tile's rows are prefetched into L2 meanwhile),
+// S^T = C q^T (M 128 rows, N 64 heads), softmax against the running max,
+// O^T += C^T P^T (M 128 latent x 4 chunks, N 64 heads).  The running max is
+// raised only when a tile's max exceeds it by more than 8 (base 2): then O^T
+// and the sum are rescaled first; otherwise probabilities up to 2^8 are kept,
+// which is exact up to rounding since O and the sum share the reference.
+constexpr int kHs = 64;                  // heads per CTA
+constexpr int kQBlockS = kHs * 128;      // 64 heads x 64 latent columns, 8 KB
+constexpr int kPtBlockS = kHs * 128;     // 64 heads x 64 rows, 8 KB
+constexpr int kTmemColsS = 512;          // S^T (64) + O^T (4 x 64)
+constexpr float kRescaleAt = 8.f;        // base-2 growth of the max that forces a rescale
+
+struct SCtl {
+  uint64_t s_ready, o_ready;
+  uint32_t tmem_base;
+  int rescale;
+  int tok[kRows];
+  int prow[kRows];
+  float rs[kRows];
+  float red[4][kHs];  // [row quarter][head]: per-warp partials
+  float m_run[kHs], l_run[kHs], alpha[kHs], tsum[kHs];
+};
+constexpr size_t kOffKvS = 0;
+constexpr size_t kOffQS = kOffKvS + 8 * (size_t)kKvBlock;
+constexpr size_t kOffPtS = kOffQS + 8 * (size_t)kQBlockS;
+constexpr size_t kOffCtlS = kOffPtS + 2 * (size_t)kPtBlockS;
+constexpr size_t kSmemBytesS = 1024 + kOffCtlS + sizeof(SCtl);
+static_assert(kSmemBytesS <= 227 * 1024, "shared memory budget");
+static_assert((size_t)kHs * kL * 4 <= 8 * (size_t)kKvBlock, "O staging fits the row tile");
+
+// 32 values per lane (one row, 32 heads) reduced over the warp's 32 rows; lane l
+// ends with the reduction of head l (31 shuffles).
+template <bool kMax>
+__device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      const float send = upper ? v[i] : v[i + s];
+      const float keep = upper ? v[i + s] : v[i];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, s);
+      v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  return v[0];
+}
+
+template <int kKv>
+__global__ void __launch_bounds__(kThreadsM, 1)
+    mla_stream_kernel(const __nv_bfloat16* __restrict__ q_lat,
+                      const __nv_bfloat16* __restrict__ kv, const int32_t* __restrict__ cu_seqlens,
+                      const int32_t* __restrict__ q_seq, const int32_t* __restrict__ token_ids,
+                      int B, int W, int tiles_per_split, float sm_scale,
+                      __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                      float* __restrict__ part_o, float* __restrict__ part_ml, PagedKv pk,
+                      int32_t* status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char* sb = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  SCtl& c = *reinterpret_cast<SCtl*>(sb + kOffCtlS);
+  const int split = blockIdx.x, n_split = gridDim.x, qi = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qw = warp & 3;   // TMEM lanes 32 qw .. 32 qw + 31
+  const int hg = warp >> 2;  // heads 32 hg .. 32 hg + 31
+  const int n_tiles = (W + kRows - 1) / kRows;
+  const int t_lo = split * tiles_per_split;
+  const int t_hi = min(n_tiles, t_lo + tiles_per_split);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&c.s_ready, 1);
+    mbar_init(&c.o_ready, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc<kTmemColsS>(&c.tmem_base);
+    tc_fence_before();
+  }
+  if (threadIdx.x < kHs) {
+    c.m_run[threadIdx.x] = -INFINITY;
+    c.l_run[threadIdx.x] = 0.f;
+  }
+  pdl_wait();  // every input may come from the kernel just before
+  pdl_launch_dependents();
+
+  const long long qh0 = (long long)qi * kHm;  // the query's first (query, head) row
+  {
+    const __nv_bfloat16* qsrc = q_lat + qh0 * kL;
+    for (int i = threadIdx.x; i < kHs * 64; i += kThreadsM) {
+      const int h = i >> 6, ch = i & 63;
+      cp_async16(
+          smem_u32(sb + kOffQS + (ch >> 3) * kQBlockS + h * 128 + (((ch & 7) ^ (h & 7)) << 4)),
+          qsrc + (long long)h * kL + ch * 8, true);
+    }
+    cp_async_commit();
+  }
+  const int b = q_seq ? q_seq[qi] : 0;
+  const bool seq_ok = b >= 0 && b < B;
+  if (!seq_ok && split == 0 && threadIdx.x == 0) flag(status, DSA_DEV_BAD_QSEQ);
+  long long row_base = 0;
+  int Tb = 0;
+  if (kKv == kKvContig) {
+    row_base = seq_ok ? cu_seqlens[b] : 0;
+    Tb = seq_ok ? cu_seqlens[b + 1] - cu_seqlens[b] : 0;
+  } else {
+    Tb = seq_ok ? pk.seq_lens[b] : 0;
+  }
+  tc_fence_after();
+  const uint32_t tmem = c.tmem_base;
+  const uint32_t kvb = smem_u32(sb + kOffKvS), qb = smem_u32(sb + kOffQS);
+  const uint32_t ptb = smem_u32(sb + kOffPtS);
+  const int32_t* toks = token_ids + (long long)qi * W;
+  const size_t row_bytes = kKv == kKvPagedE4M3 ? (size_t)kL : (size_t)kL * 2;
+  const unsigned char* rows_base = static_cast<const unsigned char*>(
+      kKv == kKvContig ? static_cast<const void*>(kv) : pk.pages);
+  bool ok = true;
+  int r = qw * 32 + lane;  // this thread's row of the tile in the softmax
+
+  // the cache row of tile row `rr` (-1: none); flags bad ids and pages
+  auto row_of = [&](int t, int rr, int* tok_out) -> int {
+    const int j = t * kRows + rr;
+    int tok = (j < W && seq_ok) ? toks[j] : -1;
+    if (tok >= Tb) {
+      flag(status, DSA_DEV_BAD_TOKEN);
+      tok = -1;
+    }
+    tok = tok < 0 ? -1 : tok;
+    long long prow = tok >= 0 ? row_base + tok : -1;
+    if (kKv != kKvContig && tok >= 0) {
+      const int blk = tok / pk.page_size;
+      const int page = blk < pk.max_pages ? pk.block_table[(long long)b * pk.max_pages + blk] : -1;
+      if (page < 0 || page >= pk.n_pages) {
+        flag(status, DSA_DEV_BAD_PAGE);
+        tok = -1;
+        prow = -1;
+      } else {
+        prow = (long long)page * pk.page_size + tok % pk.page_size;
+      }
+    }
+    *tok_out = tok;
+    return (int)prow;
+  };
+
+  for (int t = t_lo; t < t_hi && ok; ++t) {
+    const uint32_t ph = (uint32_t)((t - t_lo) & 1);
+    // ---- 1. this tile's rows; the next tile's rows go to L2 meanwhile
+    if (threadIdx.x < kRows) {
+      int tok;
+      const int prow = row_of(t, threadIdx.x, &tok);
+      c.tok[threadIdx.x] = tok;
+      c.prow[threadIdx.x] = prow;
+    } else if (t + 1 < t_hi) {
+      const int rr = threadIdx.x - kRows;
+      const int j = (t + 1) * kRows + rr;
+      const int tok = (j < W && seq_ok) ? toks[j] : -1;
+      if (tok >= 0 && tok < Tb) {
+        long long prow = row_base + tok;
+        if (kKv != kKvContig) {
+          const int blk = tok / pk.page_size;
+          const int page =
+              blk < pk.max_pages ? pk.block_table[(long long)b * pk.max_pages + blk] : -1;
+          prow = (page >= 0 && page < pk.n_pages) ? (long long)page * pk.page_size +
+                                                        tok % pk.page_size
+                                                  : -1;
+        }
+        if (prow >= 0) {
+          const unsigned char* p = rows_base + (size_t)prow * row_bytes;
+          for (size_t o = 0; o < row_bytes; o += 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p + o));
+        }
+      }
+    }
+    __syncthreads();
+    if (kKv != kKvPagedE4M3) {
+      const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(rows_base);
+      for (int i = threadIdx.x; i < kRows * 64; i += kThreadsM) {
+        const int rr = i >> 6, ch = i & 63;
+        const int prow = c.prow[rr];
+        const bool okr = prow >= 0;
+        cp_async16(smem_u32(sb + kOffKvS + (ch >> 3) * kKvBlock + rr * 128 +
+                            (((ch & 7) ^ (rr & 7)) << 4)),
+                   okr ? src + (long long)prow * kL + ch * 8 : src, okr);
+      }
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(rows_base);
+      constexpr int kPer = kRows * (kL / 16) / kThreadsM;
+      uint4 raw[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int i = u * kThreadsM + threadIdx.x;
+        const int prow = c.prow[i >> 5];
+        raw[u] = prow >= 0 ? __ldg(src + (long long)prow * (kL / 16) + (i & 31))
+                           : make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (threadIdx.x < kRows) {
+        const int prow = c.prow[threadIdx.x];
+        c.rs[threadIdx.x] = prow >= 0 ? pk.row_scale[prow] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int i = u * kThreadsM + threadIdx.x;
+        const int rr = i >> 5, c16 = i & 31;
+        const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+        for (int hf2 = 0; hf2 < 2; ++hf2) {
+          const int ch = 2 * c16 + hf2;
+          const uint4 v = make_uint4(e4m3x2_to_bf16x2(w[2 * hf2] & 0xffffu),
+                                     e4m3x2_to_bf16x2(w[2 * hf2] >> 16),
+                                     e4m3x2_to_bf16x2(w[2 * hf2 + 1] & 0xffffu),
+                                     e4m3x2_to_bf16x2(w[2 * hf2 + 1] >> 16));
+          *reinterpret_cast<uint4*>(sb + kOffKvS + (ch >> 3) * kKvBlock + rr * 128 +
+                                    (((ch & 7) ^ (rr & 7)) << 4)) = v;
+        }
+      }
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- 2. S^T = C q^T  (M = 128 rows, N = 64 heads, K = 512)
+    if (threadIdx.x == 0) {
+      constexpr uint32_t idesc = umma_idesc_bf16(kRows, kHs, false);
+#pragma unroll
+      for (int kk = 0; kk < 32; ++kk) {
+        const uint32_t blk = kk >> 2, off = (kk & 3) * 32;
+        umma_bf16(tmem, sw128_desc(kvb + blk * kKvBlock + off),
+                  sw128_desc(qb + blk * kQBlockS + off), idesc, kk > 0 ? 1u : 0u);
+      }
+      umma_commit(&c.s_ready);
+    }
+    ok = mbar_wait_bounded(&c.s_ready, ph);
+    if (!ok && lane == 0) flag(status, DSA_DEV_TIMEOUT);
+    tc_fence_after();
+
+    // ---- 3. softmax against the running max (thread = row r, heads 32 hg ..)
+    float z[32];
+    tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(hg * 32), z);
+    const bool row_ok = c.tok[r] >= 0 && ok;
+    const float rsr = kKv == kKvPagedE4M3 ? c.rs[r] : 1.f;
+    const float zs = kKv == kKvPagedE4M3 ? sm_scale * kLog2e * rsr : sm_scale * kLog2e;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = row_ok ? z[i] * zs : -INFINITY;
+    {
+      float tt[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) tt[i] = z[i];
+      c.red[qw][hg * 32 + lane] = transpose_reduce32<true>(tt, lane);
+    }
+    if (threadIdx.x == 0) c.rescale = 0;
+    __syncthreads();
+    if (threadIdx.x < kHs) {
+      const int h = threadIdx.x;
+      const float tmax = fmaxf(fmaxf(c.red[0][h], c.red[1][h]), fmaxf(c.red[2][h], c.red[3][h]));
+      const float m_old = c.m_run[h];
+      float m_new = m_old, alpha = 1.f;
+      if (m_old == -INFINITY) {
+        m_new = tmax;  // first rows of this head: nothing accumulated yet
+      } else if (tmax > m_old + kRescaleAt) {
+        m_new = tmax;
+        alpha = exp2f(m_old - m_new);
+        c.rescale = 1;
+      }
+      c.m_run[h] = m_new;
+      c.alpha[h] = alpha;
+    }
+    __syncthreads();
+    float p[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int h = hg * 32 + i;
+      const float m = c.m_run[h];
+      p[i] = (m == -INFINITY || z[i] == -INFINITY) ? 0.f : exp2f(z[i] - m);
+      *reinterpret_cast<__nv_bfloat16*>(sb + kOffPtS + (r >> 6) * kPtBlockS + h * 128 +
+                                        ((((r & 63) >> 3) ^ (h & 7)) << 4) + (r & 7) * 2) =
+          __float2bfloat16_rn(kKv == kKvPagedE4M3 ? p[i] * rsr : p[i]);
+    }
+    c.red[qw][hg * 32 + lane] = transpose_reduce32<false>(p, lane);
+    // a raised reference: rescale what O^T holds so far (never on the first tile)
+    if (c.rescale && t > t_lo) {
+#pragma unroll 1
+      for (int mc = 0; mc < 4; ++mc) {
+        float o[32];
+        const uint32_t ta = tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHs + mc * kHs + hg * 32);
+        tmem_ld32(ta, o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] *= c.alpha[hg * 32 + i];
+        tmem_st32(ta, o);
+      }
+    }
+    fence_proxy_async_smem();  // P^T is read by the tensor cores next
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < kHs) {
+      const int h = threadIdx.x;
+      const float s = (c.red[0][h] + c.red[1][h]) + (c.red[2][h] + c.red[3][h]);
+      c.l_run[h] = c.l_run[h] * c.alpha[h] + s;
+    }
+
+    // ---- 4. O^T += C^T P^T  (M = 128 latent x 4 chunks, N = 64 heads, K = 128 rows)
+    if (threadIdx.x == 0) {
+      tc_fence_after();
+      constexpr uint32_t idesc = umma_idesc_bf16(128, kHs, true);
+#pragma unroll
+      for (int mc = 0; mc < 4; ++mc) {
+#pragma unroll
+        for (int kr = 0; kr < 8; ++kr) {
+          const uint64_t a = umma_desc_sw128(kvb + 2 * mc * kKvBlock + kr * 2048, kKvBlock, 1024);
+          const uint64_t bd = sw128_desc(ptb + (kr >> 2) * kPtBlockS + (kr & 3) * 32);
+          umma_bf16(tmem + kHs + mc * kHs, a, bd, idesc, (t > t_lo || kr > 0) ? 1u : 0u);
+        }
+      }
+      umma_commit(&c.o_ready);
+    }
+    ok = mbar_wait_bounded(&c.o_ready, ph) && ok;  // the tiles are free again after this
+    if (!ok && lane == 0) flag(status, DSA_DEV_TIMEOUT);
+    tc_fence_after();
+    __syncthreads();
+  }
+
+  // ---- 5. epilogue: O^T -> shared [head][latent] fp32, then whole rows out
+  float* stage = reinterpret_cast<float*>(sb + kOffKvS);
+  const bool any = t_hi > t_lo;
+#pragma unroll 1
+  for (int mc = 0; mc < 4; ++mc) {
+    float o[32];
+    tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHs + mc * kHs + hg * 32), o);
+    const int col = mc * 128 + qw * 32 + lane;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) stage[(hg * 32 + i) * kL + col] = (ok && any) ? o[i] : 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  for (int f = threadIdx.x; f < kHs * kL / 4; f += kThreadsM) {
+    const int h = f / (kL / 4), c4 = f % (kL / 4);
+    const float4 v = *reinterpret_cast<const float4*>(stage + h * kL + c4 * 4);
+    if (n_split == 1) {
+      const float l = c.l_run[h];
+      const float inv = (ok && l > 0.f) ? 1.f / l : 0.f;
+      *reinterpret_cast<uint2*>(out + (qh0 + h) * kL + c4 * 4) =
+          make_uint2(pack_bf16(v.x * inv, v.y * inv), pack_bf16(v.z * inv, v.w * inv));
+    } else {
+      *reinterpret_cast<float4*>(part_o + ((qh0 + h) * n_split + split) * kL + c4 * 4) = v;
+    }
+  }
+  if (threadIdx.x < kHs) {
+    const int h = threadIdx.x;
+    const float m = c.m_run[h], l = (ok && any) ? c.l_run[h] : 0.f;
+    if (n_split == 1) {
+      if (lse) lse[qh0 + h] = l > 0.f ? (m + log2f(l)) / kLog2e : -INFINITY;
+    } else {
+      part_ml[((qh0 + h) * n_split + split) * 2] = m;
+      part_ml[((qh0 + h) * n_split + split) * 2 + 1] = l;
+    }
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc<kTmemColsS>(tmem);
+  }
+}
+
 }  // namespace
 
 int mla_umma_splits(int out_width) { return (out_width + kRows - 1) / kRows; }
@@ -413,6 +780,65 @@ int launch_kind(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
              : DSA_ERR_CUDA;
 }
 }  // namespace
+
+int mla_stream_splits(int Q, int out_width) {
+  const int n_tiles = (out_width + kRows - 1) / kRows;
+  int s = Q >= kNumSMs ? 1 : kNumSMs / Q;  // CTAs within one wave
+  s = s < 1 ? 1 : (s > n_tiles ? n_tiles : s);
+  const int per = (n_tiles + s - 1) / s;
+  return (n_tiles + per - 1) / per;
+}
+
+namespace {
+template <int kKv>
+int launch_stream_kind(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
+                       const int32_t* q_seq, const int32_t* token_ids, int Q, int B,
+                       int out_width, float sm_scale, void* out, float* lse, float* part_o,
+                       float* part_ml, const PagedKv& pk, int32_t* status_dev,
+                       cudaStream_t stream) {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(mla_stream_kernel<kKv>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)kSmemBytesS);
+  });
+  const int n_tiles = (out_width + kRows - 1) / kRows;
+  const int n_split = mla_stream_splits(Q, out_width);
+  const int per = (n_tiles + n_split - 1) / n_split;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_split, 1, Q);
+  cfg.blockDim = dim3(kThreadsM, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytesS;
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_stream_kernel<kKv>, (const __nv_bfloat16*)q_lat,
+                            (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, out_width,
+                            per, sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml, pk,
+                            status_dev) == cudaSuccess
+             ? DSA_OK
+             : DSA_ERR_CUDA;
+}
+}  // namespace
+
+int launch_mla_stream(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
+                      const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int out_width,
+                      float sm_scale, void* out, float* lse, float* part_o, float* part_ml,
+                      int32_t* status_dev, cudaStream_t stream, const PagedKv* paged) {
+  if (!paged)
+    return launch_stream_kind<kKvContig>(q_lat, kv, cu_seqlens, q_seq, token_ids, Q, B,
+                                         out_width, sm_scale, out, lse, part_o, part_ml,
+                                         PagedKv{}, status_dev, stream);
+  if (paged->kv_dtype == DSA_FP8_E4M3)
+    return launch_stream_kind<kKvPagedE4M3>(q_lat, nullptr, nullptr, q_seq, token_ids, Q, B,
+                                            out_width, sm_scale, out, lse, part_o, part_ml,
+                                            *paged, status_dev, stream);
+  return launch_stream_kind<kKvPaged>(q_lat, nullptr, nullptr, q_seq, token_ids, Q, B,
+                                      out_width, sm_scale, out, lse, part_o, part_ml, *paged,
+                                      status_dev, stream);
+}
 
 int launch_mla_umma(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
                     const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int out_width,

@@ -417,3 +417,32 @@ def test_decode_layer_equal_scores():
         o = oracle_inputs(bt)
         par.check_topk(a, bt.geo.select_k)
         par.check_mla(o, a)
+
+
+@pytest.mark.parametrize("tile", [0, 11])
+def test_streaming_attention_large_logit_in_a_late_or_first_tile(tile):
+    """40 decode queries x 2048 rows run the streaming attention (more than four
+    waves of one-tile CTAs).  A selected row aligned with head 0's query, placed
+    in tile `tile` of some queries, raises that head's max by far more than the
+    lazy-rescale margin (2^8): in a late tile the accumulator is rescaled, in the
+    first tile later tiles stay below the reference."""
+    geo = Geometry(D=128, H=32, kpool=4, select_k=512, out_width=2048, Hm=64, L=512,
+                   dtype="bf16")
+    rng = np.random.default_rng(77)
+    lengths = [int(x) for x in rng.integers(2100, 3500, 40)]
+    bt = synth.make_batch(geo, lengths, [0] * 40, device=DEV, seed=78)
+    buf = pipeline.LayerBuffers.alloc(bt)
+    pipeline.run_layer(bt, buf)
+    torch.cuda.synchronize()
+    for q in (0, 7, 39):
+        tok = int(buf.token_ids[q, tile * 128 + 5])
+        b = int(bt.q_seq[q])
+        row = int(bt.cu_seqlens[b]) + tok
+        bt.kv[row] = bt.q_lat[q, 0].to(bt.kv.dtype)
+    buf.out.zero_()
+    pipeline.attend(bt, buf)
+    torch.cuda.synchronize()
+    o = oracle_inputs(bt)
+    st = par.check_mla(o, buf)
+    assert st == 0 and int(buf.status.item()) == 0
+    assert float(buf.lse[0, 0]) > float(buf.lse[0, 1]) + 8.0
