@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--breakdown", action="store_true",
                     help="diagnostic: per-stage in-graph times (extra events between stages)")
+    ap.add_argument("--leg", choices=["prefill_index", "prefill_attention", "paged_attention"],
+                    help="run only this side measurement and print its JSON object (for "
+                         "profiling one kernel without the decode step)")
     ap.add_argument("--no-paged", action="store_true",
                     help="skip the paged / E4M3 attention leg")
     ap.add_argument("--no-prefill", action="store_true",
@@ -233,6 +236,48 @@ def prefill_index(peaks_path, reps=10):
             os.path.exists(peaks_path) else "fallback", "frac": round(tf / peak, 4),
             "score_bytes": int(buf.scores.numel() * 4),
             "timing": "median of %d launches, L2 flushed before each" % reps}
+
+
+def prefill_attention(peaks_path, reps=5):
+    """The selected-row attention of the prefill chunk: 4096 queries after a
+    131 072-token context, 2048 selected rows each (kpool 8, 256 pools), 64
+    heads, latent 512, on the streaming tensor-core kernel; the token ids are
+    the chunk's own selection.  L2 flushed before every timed call; reported
+    against the bf16 tensor peak over 2 * 2 * Hm * L flops per selected row."""
+    import torch
+
+    from sparse_attention_indexer_kpool_gb300 import ops, pipeline, synth
+    bt = synth.prefill(device="cuda")
+    buf = pipeline.LayerBuffers.alloc(bt)
+    pipeline.compress(bt, buf)
+    pipeline.select(bt, buf)
+    torch.cuda.synchronize()
+    assert int(buf.status.item()) == 0
+    Q, Hm, L = bt.q_lat.shape
+    rows = int((buf.token_ids >= 0).sum().item())
+    flops = 4.0 * Hm * L * rows
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        pipeline.attend(bt, buf)
+    times = []
+    for _ in range(reps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        pipeline.attend(bt, buf)
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    assert int(buf.status.item()) == 0
+    us = statistics.median(times) * 1e3
+    peak = json.load(open(peaks_path))["bf16_tflops"] if os.path.exists(peaks_path) else 1900.0
+    tf = flops / (us * 1e-6) / 1e12
+    return {"workload": "prefill chunk attention: %d queries x %d selected rows (%d valid), %d "
+                        "heads, latent %d" % (Q, buf.token_ids.shape[1], rows, Hm, L),
+            "kernel": "mla_stream_kernel (tcgen05, 64 heads per CTA, 128-row tiles)",
+            "us": round(us, 1), "flops": flops, "tflops": round(tf, 1), "bound": "tensor",
+            "peak_tflops": peak, "frac": round(tf / peak, 4),
+            "timing": "median of %d calls, L2 flushed before each" % reps}
 
 
 def paged_attention(reps=20, page_size=64):
@@ -575,6 +620,7 @@ def run_ours(args, dist):
         out["breakdown"] = breakdown
     if not args.no_prefill:
         out["prefill_index"] = prefill_index(peaks_path)
+        out["prefill_attention"] = prefill_attention(peaks_path)
     if not args.no_paged:
         out["paged_attention"] = paged_attention()
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -739,7 +785,15 @@ def main():
     args = parse()
     dist = Dist(args.gpus)
     try:
-        if args.impl == "reference":
+        if args.leg:
+            from sparse_attention_indexer_kpool_gb300 import build as libbuild
+            libbuild.build()
+            peaks = os.path.join(ROOT, "MEASURED_PEAKS.json")
+            legs = {"prefill_index": lambda: prefill_index(peaks),
+                    "prefill_attention": lambda: prefill_attention(peaks),
+                    "paged_attention": paged_attention}
+            print(json.dumps({args.leg: legs[args.leg]()}), flush=True)
+        elif args.impl == "reference":
             run_reference(args, dist)
         else:
             run_ours(args, dist)
