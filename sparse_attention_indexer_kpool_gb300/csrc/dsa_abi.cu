@@ -74,7 +74,7 @@ int run_select(const void* q, const float* weights, float scale, const void* poo
                const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
                int select_k, int out_width, int dtype, float* scores, int32_t* pool_ids,
                int32_t* token_ids, void* workspace, int32_t* status_dev, cudaStream_t st,
-               const int32_t* safe_begin) {
+               const int32_t* safe_begin, int busy_ctas = 0) {
   // Decode geometry: the scoring kernel also counts each query's score
   // histogram into the workspace and the selection starts from it.  Otherwise
   // the selection kernel builds the histogram itself.
@@ -83,7 +83,7 @@ int run_select(const void* q, const float* weights, float scale, const void* poo
                                    pool_valid, n_pools, cu_pool_cap, q_seq, q_pos, Q, B, H, D,
                                    kpool, P_ld, dtype, scores,
                                    hist ? dsa::topk_workspace_hist(workspace) : nullptr,
-                                   status_dev, st, safe_begin);
+                                   status_dev, st, safe_begin, busy_ctas);
   if (r != DSA_OK) return r;
   return dsa::launch_select_after_index(scores, Q, P_ld, select_k, pool_ids,
                                         hist ? workspace : nullptr, pool_start, cu_pool_cap,
@@ -346,7 +346,8 @@ int dsa_decode_layer(const dsa_decode_layer_args* a, void* stream) {
                  a->pool_valid, a->n_pools, a->cu_pool_cap, a->q_seq, a->q_pos, a->Q, a->B, a->H,
                  a->D, a->kpool, a->P_ld, a->select_k, a->out_width, a->dtype, a->scores,
                  a->pool_ids, a->token_ids, a->ws_select, a->status_dev, st,
-                 rc == DSA_OK ? a->pool_begin : nullptr);
+                 rc == DSA_OK ? a->pool_begin : nullptr,
+                 rc == DSA_OK ? dsa::kpool_compress_ctas(a->B, a->max_pools) : 0);
   if (r != DSA_OK) return r;
   // the attention's inputs other than the token ids predate this call
   return dsa::launch_mla_selected_decode(a->q_lat, a->kv_latent, a->cu_seqlens, a->q_seq,

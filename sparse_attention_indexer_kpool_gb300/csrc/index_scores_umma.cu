@@ -531,7 +531,8 @@ int launch_g(const void* q, const float* weights, float scale, const void* pool_
              int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
              const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
              const int32_t* q_pos, int Q, int B, int kpool, int P_ld, float* scores,
-             uint32_t* hist, const int32_t* safe_begin, int32_t* status, cudaStream_t stream) {
+             uint32_t* hist, const int32_t* safe_begin, int32_t* status, cudaStream_t stream,
+             int busy_ctas) {
   const size_t smem = Layout<G>::bytes((Q + G - 1) / G, safe_begin != nullptr);
   if (smem > (size_t)kSmemMax) return DSA_ERR_UNSUPPORTED;
   CUtensorMap mk, mq;
@@ -546,7 +547,11 @@ int launch_g(const void* q, const float* weights, float scale, const void* pool_
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr.val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kNumSMs, 1, 1);
+  // A scoring CTA cannot share an SM with a CTA of the compress kernel still
+  // running beside an early start (measured: those CTAs begin ~2 us late and
+  // finish last), so a few busy SMs are left out of the grid.
+  const int grid = (busy_ctas > 0 && busy_ctas <= kNumSMs / 8) ? kNumSMs - busy_ctas : kNumSMs;
+  cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kThreadsU, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -579,17 +584,18 @@ int launch_index_scores_umma(const void* q, const float* weights, float scale,
                              const int32_t* cu_pool_cap, const int32_t* q_seq,
                              const int32_t* q_pos, int Q, int B, int kpool, int P_ld,
                              float* scores, uint32_t* hist, const int32_t* safe_begin,
-                             int32_t* status_dev, cudaStream_t stream) {
+                             int32_t* status_dev, cudaStream_t stream, int busy_ctas) {
   const int G = umma_index_group(Q, q_seq);
   if (G == 8)
     return launch_g<8>(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid, n_pools,
                        cu_pool_cap, q_seq, q_pos, Q, B, kpool, P_ld, scores, nullptr, nullptr,
-                       status_dev, stream);
-  if (G == 1)
+                       status_dev, stream, 0);
+  if (G == 1) {
+    const bool early = safe_begin != nullptr && umma_index_early_ok(Q, q_seq, q_pos);
     return launch_g<1>(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid, n_pools,
                        cu_pool_cap, q_seq, q_pos, Q, B, kpool, P_ld, scores, hist,
-                       umma_index_early_ok(Q, q_seq, q_pos) ? safe_begin : nullptr, status_dev,
-                       stream);
+                       early ? safe_begin : nullptr, status_dev, stream, early ? busy_ctas : 0);
+  }
   return DSA_ERR_UNSUPPORTED;
 }
 

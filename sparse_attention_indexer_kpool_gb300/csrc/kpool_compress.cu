@@ -280,6 +280,10 @@ int launch_t(const void* k, const void* gate, const uint8_t* valid, const float*
 
 }  // namespace
 
+int kpool_compress_ctas(int B, int max_pools) {
+  return max(1, (max_pools + kWarpsPerCta - 1) / kWarpsPerCta) * B;
+}
+
 int launch_kpool_compress(const void* k, const void* gate, const uint8_t* valid, const float* ape,
                           const void* ln_gamma, const void* ln_beta, float ln_eps,
                           const int32_t* cu_seqlens, const int32_t* cu_pool_cap,
