@@ -10,7 +10,7 @@
 // ~pool), so "score descending, pool ascending" is plain key-descending order
 // and the selected set and its order are unique.
 //
-// A thread-block cluster of C CTAs per query row (C <= 8), everything on chip:
+// A thread-block cluster of C CTAs per query row (C <= 16), everything on chip:
 //   1. a 4096-bin histogram of the top 12 key bits (built by the scoring kernel
 //      on the fused path; else each CTA counts its slice and every CTA sums the
 //      C slice histograms through distributed shared memory);
@@ -26,6 +26,9 @@
 //      an exact radix select over the row and a shared-memory sort;
 //   5. pool ids written, and optionally expanded to token ids in place.
 #include <cooperative_groups.h>
+
+#include <map>
+#include <mutex>
 
 #include "dsa_internal.cuh"
 
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_thr;
   __shared__ uint32_t s_nsure, s_ntie, s_r, s_nsel;
   __shared__ uint32_t s_wtot[64];
-  __shared__ uint32_t s_cnt[2][9];   // per-rank sure / tie counts, exclusive prefix in [.][r]
+  __shared__ uint32_t s_cnt[2][17];  // per-rank sure / tie counts, exclusive prefix in [.][r]
   __shared__ uint64_t s_res;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -533,12 +536,48 @@ __global__ void expand_kernel(const int32_t* __restrict__ pool_ids,
   pdl_launch_dependents();
 }
 
+// How many clusters of 16 top-k CTAs can be resident at once (per shared
+// memory size; asked once).
+int clusters16_resident(size_t smem) {
+  static std::mutex mu;
+  static std::map<size_t, int> known;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto it = known.find(smem);
+  if (it != known.end()) return it->second;
+  int n = 0;
+  if (cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                           1) == cudaSuccess &&
+      cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) == cudaSuccess) {
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeClusterDimension;
+    a.val.clusterDim.x = 16;
+    a.val.clusterDim.y = 1;
+    a.val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = &a;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, topk_select_kernel, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();  // a refused query leaves no error behind
+  known[smem] = n;
+  return n;
+}
+
 int launch_select(const float* scores, int Q, int P_ld, int select_k, int32_t* pool_ids,
                   uint32_t* hist, const ExpandArgs& ex, cudaStream_t stream) {
   // cluster size: enough CTAs to spread a few rows over the SMs, a slice of at
-  // least 4096 scores per CTA, at most 8 (portable clusters)
+  // least 4096 scores per CTA, at most 16 (16 is a non-portable size, taken
+  // only when all Q clusters of 16 can be resident at once; measured on the
+  // 4-query 262k step: 8 -> 16 CTAs per row, 0.459 -> 0.451 ms)
+  const size_t smem = SelLayout(select_k).total;
+  if (smem > 227 * 1024) return DSA_ERR_UNSUPPORTED;
   int C = 1;
-  while (C < 8 && Q * C * 2 <= kNumSMs && (long long)P_ld >= (long long)C * 2 * 4096) C *= 2;
+  while (C < 16 && Q * C * 2 <= kNumSMs && (long long)P_ld >= (long long)C * 2 * 4096) C *= 2;
+  if (C == 16 && clusters16_resident(smem) < Q) C = 8;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -552,8 +591,6 @@ int launch_select(const float* scores, int Q, int P_ld, int select_k, int32_t* p
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const size_t smem = SelLayout(select_k).total;
-  if (smem > 227 * 1024) return DSA_ERR_UNSUPPORTED;
   cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
   cfg.dynamicSmemBytes = smem;
