@@ -381,7 +381,6 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 // and the sum are rescaled first; otherwise probabilities up to 2^8 are kept,
 // which is exact up to rounding since O and the sum share the reference.
 constexpr int kHs = 64;                  // heads per CTA
-constexpr int kThreadsS = 512;           // 16 warps: 4 row quarters x 4 groups of 16 heads
 constexpr int kQBlockS = kHs * 128;      // 64 heads x 64 latent columns, 8 KB
 constexpr int kPtBlockS = kHs * 128;     // 64 heads x 64 rows, 8 KB
 constexpr int kTmemColsS = 512;          // S^T (64) + O^T (4 x 64)
@@ -405,8 +404,26 @@ constexpr size_t kSmemBytesS = 1024 + kOffCtlS + sizeof(SCtl);
 static_assert(kSmemBytesS <= 227 * 1024, "shared memory budget");
 static_assert((size_t)kHs * kL * 4 <= 8 * (size_t)kKvBlock, "O staging fits the row tile");
 
+// 32 values per lane (one row, 32 heads) reduced over the warp's 32 rows; lane l
+// ends with the reduction of head l (31 shuffles).
+template <bool kMax>
+__device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      const float send = upper ? v[i] : v[i + s];
+      const float keep = upper ? v[i + s] : v[i];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, s);
+      v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  return v[0];
+}
+
 template <int kKv>
-__global__ void __launch_bounds__(kThreadsS, 1)
+__global__ void __launch_bounds__(kThreadsM, 1)
     mla_stream_kernel(const __nv_bfloat16* __restrict__ q_lat,
                       const __nv_bfloat16* __restrict__ kv, const int32_t* __restrict__ cu_seqlens,
                       const int32_t* __restrict__ q_seq, const int32_t* __restrict__ token_ids,
@@ -420,7 +437,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   const int split = blockIdx.x, n_split = gridDim.x, qi = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qw = warp & 3;   // TMEM lanes 32 qw .. 32 qw + 31
-  const int hg = warp >> 2;  // heads 16 hg .. 16 hg + 15
+  const int hg = warp >> 2;  // heads 32 hg .. 32 hg + 31
   const int n_tiles = (W + kRows - 1) / kRows;
   const int t_lo = split * tiles_per_split;
   const int t_hi = min(n_tiles, t_lo + tiles_per_split);
@@ -444,7 +461,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   const long long qh0 = (long long)qi * kHm;  // the query's first (query, head) row
   {
     const __nv_bfloat16* qsrc = q_lat + qh0 * kL;
-    for (int i = threadIdx.x; i < kHs * 64; i += kThreadsS) {
+    for (int i = threadIdx.x; i < kHs * 64; i += kThreadsM) {
       const int h = i >> 6, ch = i & 63;
       cp_async16(
           smem_u32(sb + kOffQS + (ch >> 3) * kQBlockS + h * 128 + (((ch & 7) ^ (h & 7)) << 4)),
@@ -507,7 +524,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       const int prow = row_of(t, threadIdx.x, &tok);
       c.tok[threadIdx.x] = tok;
       c.prow[threadIdx.x] = prow;
-    } else if (threadIdx.x < 2 * kRows && t + 1 < t_hi) {
+    } else if (t + 1 < t_hi) {
       const int rr = threadIdx.x - kRows;
       const int j = (t + 1) * kRows + rr;
       const int tok = (j < W && seq_ok) ? toks[j] : -1;
@@ -531,7 +548,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     __syncthreads();
     if (kKv != kKvPagedE4M3) {
       const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(rows_base);
-      for (int i = threadIdx.x; i < kRows * 64; i += kThreadsS) {
+      for (int i = threadIdx.x; i < kRows * 64; i += kThreadsM) {
         const int rr = i >> 6, ch = i & 63;
         const int prow = c.prow[rr];
         const bool okr = prow >= 0;
@@ -541,11 +558,11 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       }
     } else {
       const uint4* src = reinterpret_cast<const uint4*>(rows_base);
-      constexpr int kPer = kRows * (kL / 16) / kThreadsS;
+      constexpr int kPer = kRows * (kL / 16) / kThreadsM;
       uint4 raw[kPer];
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
-        const int i = u * kThreadsS + threadIdx.x;
+        const int i = u * kThreadsM + threadIdx.x;
         const int prow = c.prow[i >> 5];
         raw[u] = prow >= 0 ? __ldg(src + (long long)prow * (kL / 16) + (i & 31))
                            : make_uint4(0u, 0u, 0u, 0u);
@@ -556,7 +573,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       }
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
-        const int i = u * kThreadsS + threadIdx.x;
+        const int i = u * kThreadsM + threadIdx.x;
         const int rr = i >> 5, c16 = i & 31;
         const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
 #pragma unroll
@@ -593,20 +610,19 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     if (!ok && lane == 0) flag(status, DSA_DEV_TIMEOUT);
     tc_fence_after();
 
-    // ---- 3. softmax against the running max (thread = row r, heads 16 hg ..)
-    float z[16];
-    tmem_ld16(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(hg * 16), z);
+    // ---- 3. softmax against the running max (thread = row r, heads 32 hg ..)
+    float z[32];
+    tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(hg * 32), z);
     const bool row_ok = c.tok[r] >= 0 && ok;
     const float rsr = kKv == kKvPagedE4M3 ? c.rs[r] : 1.f;
     const float zs = kKv == kKvPagedE4M3 ? sm_scale * kLog2e * rsr : sm_scale * kLog2e;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) z[i] = row_ok ? z[i] * zs : -INFINITY;
+    for (int i = 0; i < 32; ++i) z[i] = row_ok ? z[i] * zs : -INFINITY;
     {
-      float tt[16];
+      float tt[32];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) tt[i] = z[i];
-      const float m = transpose_reduce16<true>(tt, lane);
-      if (lane < 16) c.red[qw][hg * 16 + lane] = m;
+      for (int i = 0; i < 32; ++i) tt[i] = z[i];
+      c.red[qw][hg * 32 + lane] = transpose_reduce32<true>(tt, lane);
     }
     if (threadIdx.x == 0) c.rescale = 0;
     __syncthreads();
@@ -626,30 +642,27 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       c.alpha[h] = alpha;
     }
     __syncthreads();
-    float p[16];
+    float p[32];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int h = hg * 16 + i;
+    for (int i = 0; i < 32; ++i) {
+      const int h = hg * 32 + i;
       const float m = c.m_run[h];
       p[i] = (m == -INFINITY || z[i] == -INFINITY) ? 0.f : exp2f(z[i] - m);
       *reinterpret_cast<__nv_bfloat16*>(sb + kOffPtS + (r >> 6) * kPtBlockS + h * 128 +
                                         ((((r & 63) >> 3) ^ (h & 7)) << 4) + (r & 7) * 2) =
           __float2bfloat16_rn(kKv == kKvPagedE4M3 ? p[i] * rsr : p[i]);
     }
-    {
-      const float l = transpose_reduce16<false>(p, lane);
-      if (lane < 16) c.red[qw][hg * 16 + lane] = l;
-    }
+    c.red[qw][hg * 32 + lane] = transpose_reduce32<false>(p, lane);
     // a raised reference: rescale what O^T holds so far (never on the first tile)
     if (c.rescale && t > t_lo) {
 #pragma unroll 1
       for (int mc = 0; mc < 4; ++mc) {
-        float o[16];
-        const uint32_t ta = tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHs + mc * kHs + hg * 16);
-        tmem_ld16(ta, o);
+        float o[32];
+        const uint32_t ta = tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHs + mc * kHs + hg * 32);
+        tmem_ld32(ta, o);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] *= c.alpha[hg * 16 + i];
-        tmem_st16(ta, o);
+        for (int i = 0; i < 32; ++i) o[i] *= c.alpha[hg * 32 + i];
+        tmem_st32(ta, o);
       }
     }
     fence_proxy_async_smem();  // P^T is read by the tensor cores next
@@ -687,15 +700,15 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   const bool any = t_hi > t_lo;
 #pragma unroll 1
   for (int mc = 0; mc < 4; ++mc) {
-    float o[16];
-    tmem_ld16(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHs + mc * kHs + hg * 16), o);
+    float o[32];
+    tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHs + mc * kHs + hg * 32), o);
     const int col = mc * 128 + qw * 32 + lane;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) stage[(hg * 16 + i) * kL + col] = (ok && any) ? o[i] : 0.f;
+    for (int i = 0; i < 32; ++i) stage[(hg * 32 + i) * kL + col] = (ok && any) ? o[i] : 0.f;
   }
   tc_fence_before();
   __syncthreads();
-  for (int f = threadIdx.x; f < kHs * kL / 4; f += kThreadsS) {
+  for (int f = threadIdx.x; f < kHs * kL / 4; f += kThreadsM) {
     const int h = f / (kL / 4), c4 = f % (kL / 4);
     const float4 v = *reinterpret_cast<const float4*>(stage + h * kL + c4 * 4);
     if (n_split == 1) {
@@ -796,7 +809,7 @@ int launch_stream_kind(const void* q_lat, const void* kv, const int32_t* cu_seql
   attr.val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_split, 1, Q);
-  cfg.blockDim = dim3(kThreadsS, 1, 1);
+  cfg.blockDim = dim3(kThreadsM, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytesS;
   cfg.stream = stream;
   cfg.attrs = &attr;
