@@ -327,31 +327,44 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   if (!ok && lane == 0) flag(status, DSA_DEV_TIMEOUT);
   tc_fence_after();
 
-  // ---- 5. epilogue: O^T -> shared [head][latent] fp32 (the row tile is free now),
-  // then whole partial rows with 16-byte stores
-  float* stage = reinterpret_cast<float*>(sb + kOffKv);
+  // ---- 5. epilogue.  Split partials: straight from TMEM (a warp's 32 lanes are
+  // 32 consecutive latent columns of one head, so each store is a 128-byte row
+  // piece).  A single split: staged through shared memory [head][latent] (the
+  // row tile is free now) and normalised into bf16 with 8-byte stores.
+  if (n_split > 1) {
 #pragma unroll 1
-  for (int cc = 0; cc < 2; ++cc) {
-    const int mc = hq + 2 * cc;
-    const int col = mc * 128 + qw * 32 + lane;
-    float o[32];
-    tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHh + mc * kHh), o);
+    for (int cc = 0; cc < 2; ++cc) {
+      const int mc = hq + 2 * cc;
+      const int col = mc * 128 + qw * 32 + lane;
+      float o[32];
+      tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHh + mc * kHh), o);
+      float* dst = part_o + (qh0 * n_split + split) * kL + col;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) stage[i * kL + col] = ok ? o[i] : 0.f;
+      for (int i = 0; i < 32; ++i) dst[(long long)i * n_split * kL] = ok ? o[i] : 0.f;
+    }
+    tc_fence_before();
   }
-  tc_fence_before();
+  float* stage = reinterpret_cast<float*>(sb + kOffKv);
+  if (n_split == 1) {
+#pragma unroll 1
+    for (int cc = 0; cc < 2; ++cc) {
+      const int mc = hq + 2 * cc;
+      const int col = mc * 128 + qw * 32 + lane;
+      float o[32];
+      tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHh + mc * kHh), o);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) stage[i * kL + col] = ok ? o[i] : 0.f;
+    }
+    tc_fence_before();
+  }
   __syncthreads();
-  for (int f = threadIdx.x; f < kHh * kL / 4; f += kThreadsM) {
+  for (int f = threadIdx.x; n_split == 1 && f < kHh * kL / 4; f += kThreadsM) {
     const int h = f / (kL / 4), c4 = f % (kL / 4);
     const float4 v = *reinterpret_cast<const float4*>(stage + h * kL + c4 * 4);
-    if (n_split == 1) {
-      const float l = c.l_fin[h];
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      *reinterpret_cast<uint2*>(out + (qh0 + h) * kL + c4 * 4) =
-          make_uint2(pack_bf16(v.x * inv, v.y * inv), pack_bf16(v.z * inv, v.w * inv));
-    } else {
-      *reinterpret_cast<float4*>(part_o + ((qh0 + h) * n_split + split) * kL + c4 * 4) = v;
-    }
+    const float l = c.l_fin[h];
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    *reinterpret_cast<uint2*>(out + (qh0 + h) * kL + c4 * 4) =
+        make_uint2(pack_bf16(v.x * inv, v.y * inv), pack_bf16(v.z * inv, v.w * inv));
   }
   if (threadIdx.x < kHh) {
     const int h = threadIdx.x;
