@@ -105,22 +105,6 @@ __device__ void find_threshold(const uint32_t* h, int K, int* s_thr, uint32_t* s
   __syncthreads();
 }
 
-// Warp-aggregated append of `key` (when `take`) into an on-chip list, capped.
-__device__ __forceinline__ void append(bool take, uint64_t key, uint32_t* ctr, uint64_t* list,
-                                       uint32_t cap) {
-  const unsigned mask = __ballot_sync(0xffffffffu, take);
-  if (!mask) return;
-  const int lane = threadIdx.x & 31;
-  const int leader = __ffs(mask) - 1;
-  uint32_t base = 0;
-  if (lane == leader) base = atomicAdd(ctr, (uint32_t)__popc(mask));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  if (take) {
-    const uint32_t slot = base + __popc(mask & ((1u << lane) - 1u));
-    if (slot < cap) list[slot] = key;
-  }
-}
-
 // Exact R-th largest key (1-based) among keys given by get(i) (i < n, present
 // flag), by 8-bit radix passes from the top.  Block-wide; smem hist[256].
 template <typename Get>
@@ -335,23 +319,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   find_threshold(hh, K, &s_thr, s_wtot);
   const int thr = s_thr;
   // ---- 3. this CTA's slice: sure and tie lists
+  // A thread marks its batch's keys above and in the threshold bin; a scan
+  // over the warp's counts and one shared atomic per warp and list reserve the
+  // slots, so no atomic result is waited for per element.
   for (int base = lo; base < hi; base += kThreads * kBatch) {
     float v[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) v[u] = slice(base, u);
+    uint32_t sure_bits = 0, tie_bits = 0;  // bit u: element u goes to that list
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
-      const int i = base + u * kThreads + threadIdx.x;
-      bool in_sure = false, in_tie = false;
-      uint64_t key = 0;
       if (is_candidate(v[u])) {
-        key = full_key(v[u], i);
-        const int bin = (int)(key >> (32 + kBinShift));
-        in_sure = bin > thr;
-        in_tie = bin == thr;
+        const int bin = (int)(score_key(v[u]) >> kBinShift);
+        sure_bits |= (uint32_t)(bin > thr) << u;
+        tie_bits |= (uint32_t)(bin == thr) << u;
       }
-      append(in_sure, key, &s_nsure, own_sure, (uint32_t)K);
-      append(in_tie, key, &s_ntie, own_tie, (uint32_t)kTieCap);
+    }
+    const int lane = threadIdx.x & 31;
+    const uint32_t cs = __popc(sure_bits), ct = __popc(tie_bits);
+    uint32_t incl_s = cs, incl_t = ct;  // inclusive prefix inside the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t ys = __shfl_up_sync(0xffffffffu, incl_s, o);
+      const uint32_t yt = __shfl_up_sync(0xffffffffu, incl_t, o);
+      if (lane >= o) {
+        incl_s += ys;
+        incl_t += yt;
+      }
+    }
+    const uint32_t warp_s = __shfl_sync(0xffffffffu, incl_s, 31);
+    const uint32_t warp_t = __shfl_sync(0xffffffffu, incl_t, 31);
+    uint32_t base_s = 0, base_t = 0;
+    if (lane == 31) {
+      if (warp_s) base_s = atomicAdd(&s_nsure, warp_s);
+      if (warp_t) base_t = atomicAdd(&s_ntie, warp_t);
+    }
+    uint32_t slot_s = __shfl_sync(0xffffffffu, base_s, 31) + incl_s - cs;
+    uint32_t slot_t = __shfl_sync(0xffffffffu, base_t, 31) + incl_t - ct;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (((sure_bits | tie_bits) >> u) & 1u) {
+        const uint64_t key = full_key(v[u], base + u * kThreads + threadIdx.x);
+        if ((sure_bits >> u) & 1u) {
+          if (slot_s < (uint32_t)K) own_sure[slot_s] = key;
+          ++slot_s;
+        } else {
+          if (slot_t < (uint32_t)kTieCap) own_tie[slot_t] = key;
+          ++slot_t;
+        }
+      }
     }
   }
   cluster.sync();  // every slice's lists and counts are final
