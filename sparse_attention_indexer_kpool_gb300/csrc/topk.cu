@@ -269,8 +269,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
   pdl_launch_dependents();  // the next kernel may start its own prologue
 
-  // The first batch of this CTA's slice and the expansion's sequence lookup are
-  // requested together with the histogram, so their latencies overlap.
+  // The histogram (when the scoring kernel counted it), the first batch of this
+  // CTA's slice and the expansion's sequence index are requested together, so
+  // their latencies overlap; the sequence's cache slice, a load that depends on
+  // that index and that only the placement needs, comes after the slice scan.
+  uint32_t* gh = hist_in ? hist_in + (size_t)q * kBins : nullptr;
+  constexpr int kHistPer = kBins / kThreads;  // 4 bins per thread
+  uint32_t hv[kHistPer];
+  if (gh) {
+#pragma unroll
+    for (int u = 0; u < kHistPer; ++u) hv[u] = __ldcg(gh + u * kThreads + threadIdx.x);
+  }
   float v_first[kBatch];
 #pragma unroll
   for (int u = 0; u < kBatch; ++u) {
@@ -279,8 +288,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int b = ex.token_ids ? (ex.q_seq ? ex.q_seq[q] : 0) : 0;
   const bool seq_ok = !ex.token_ids || (b >= 0 && b < ex.B);
-  const long long cap_base = (ex.token_ids && seq_ok) ? ex.cu_pool_cap[b] : 0;
-  const int cap = (ex.token_ids && seq_ok) ? ex.cu_pool_cap[b + 1] - ex.cu_pool_cap[b] : 0;
   // slice element i of the pass starting at `base` (the first batch is in registers)
   auto slice = [&](int base, int u) -> float {
     const int i = base + u * kThreads + threadIdx.x;
@@ -288,10 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // ---- 1. histogram of the top 12 key bits
-  uint32_t* gh = hist_in ? hist_in + (size_t)q * kBins : nullptr;
   uint32_t* hh = h;
   if (gh) {
-    for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = __ldcg(gh + i);
+#pragma unroll
+    for (int u = 0; u < kHistPer; ++u) h[u * kThreads + threadIdx.x] = hv[u];
     __syncthreads();
   } else {
     for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = 0;
@@ -370,6 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  const long long cap_base = (ex.token_ids && seq_ok) ? ex.cu_pool_cap[b] : 0;
+  const int cap = (ex.token_ids && seq_ok) ? ex.cu_pool_cap[b + 1] - ex.cu_pool_cap[b] : 0;
   cluster.sync();  // every slice's lists and counts are final
   // ---- 4. all-gather the cluster's lists
   if (threadIdx.x < 2 * C) {
