@@ -67,14 +67,14 @@ int check_select(const void* q, const float* weights, float scale, const void* p
   return DSA_OK;
 }
 
-// index_scores -> top-k (+ expansion); safe_begin: see dsa::launch_index_scores
+// index_scores -> top-k (+ expansion); early: see dsa::EarlyStart
 int run_select(const void* q, const float* weights, float scale, const void* pool_keys,
                int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
                const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
                const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
                int select_k, int out_width, int dtype, float* scores, int32_t* pool_ids,
                int32_t* token_ids, void* workspace, int32_t* status_dev, cudaStream_t st,
-               const int32_t* safe_begin, int busy_ctas = 0) {
+               dsa::EarlyStart early = {}, int busy_ctas = 0) {
   // Decode geometry: the scoring kernel also counts each query's score
   // histogram into the workspace and the selection starts from it.  Otherwise
   // the selection kernel builds the histogram itself.
@@ -83,7 +83,7 @@ int run_select(const void* q, const float* weights, float scale, const void* poo
                                    pool_valid, n_pools, cu_pool_cap, q_seq, q_pos, Q, B, H, D,
                                    kpool, P_ld, dtype, scores,
                                    hist ? dsa::topk_workspace_hist(workspace) : nullptr,
-                                   status_dev, st, safe_begin, busy_ctas);
+                                   status_dev, st, early, busy_ctas);
   if (r != DSA_OK) return r;
   return dsa::launch_select_after_index(scores, Q, P_ld, select_k, pool_ids,
                                         hist ? workspace : nullptr, pool_start, cu_pool_cap,
@@ -255,8 +255,7 @@ int dsa_select(const void* q, const float* weights, float scale, const void* poo
   if (r != DSA_OK) return r == kNoWork ? DSA_OK : r;
   return run_select(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid, n_pools,
                     cu_pool_cap, q_seq, q_pos, Q, B, H, D, kpool, P_ld, select_k, out_width,
-                    dtype, scores, pool_ids, token_ids, workspace, status_dev, as_stream(stream),
-                    nullptr);
+                    dtype, scores, pool_ids, token_ids, workspace, status_dev, as_stream(stream));
 }
 
 size_t dsa_mla_selected_decode_workspace_size(int Q, int Hm, int L, int out_width, int dtype) {
@@ -346,7 +345,8 @@ int dsa_decode_layer(const dsa_decode_layer_args* a, void* stream) {
                  a->pool_valid, a->n_pools, a->cu_pool_cap, a->q_seq, a->q_pos, a->Q, a->B, a->H,
                  a->D, a->kpool, a->P_ld, a->select_k, a->out_width, a->dtype, a->scores,
                  a->pool_ids, a->token_ids, a->ws_select, a->status_dev, st,
-                 rc == DSA_OK ? a->pool_begin : nullptr,
+                 rc == DSA_OK ? dsa::EarlyStart{a->pool_begin, a->valid, a->cu_seqlens}
+                              : dsa::EarlyStart{},
                  rc == DSA_OK ? dsa::kpool_compress_ctas(a->B, a->max_pools) : 0);
   if (r != DSA_OK) return r;
   // the attention's inputs other than the token ids predate this call

@@ -168,6 +168,14 @@ namespace dsa {
 // CTAs of one launch of the compress kernel (they stay resident while a
 // scoring kernel of the same call starts early)
 int kpool_compress_ctas(int B, int max_pools);
+// The compress of the same call, for a scoring kernel that starts before that
+// compress has ended: it rewrites pools [pool_begin[b], ...) of sequence b, and
+// the pool count it writes follows from the first valid token of the sequence.
+struct EarlyStart {
+  const int32_t* pool_begin = nullptr;  // nullptr: no early start
+  const uint8_t* valid = nullptr;
+  const int32_t* cu_seqlens = nullptr;
+};
 int launch_kpool_compress(const void* k, const void* gate, const uint8_t* valid, const float* ape,
                           const void* ln_gamma, const void* ln_beta, float ln_eps,
                           const int32_t* cu_seqlens, const int32_t* cu_pool_cap,
@@ -179,8 +187,7 @@ int launch_index_scores(const void* q, const float* weights, float scale, const 
                         const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
                         const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
                         int dtype, float* scores, uint32_t* score_hist, int32_t* status_dev,
-                        cudaStream_t stream, const int32_t* safe_begin = nullptr,
-                        int busy_ctas = 0);
+                        cudaStream_t stream, EarlyStart early = {}, int busy_ctas = 0);
 // tcgen05 index kernel: queries per key tile (1 or 8), 0 when Q does not fit it
 int umma_index_group(int Q, const int32_t* q_seq);
 int launch_index_scores_umma(const void* q, const float* weights, float scale,
@@ -188,7 +195,7 @@ int launch_index_scores_umma(const void* q, const float* weights, float scale,
                              const uint8_t* pool_valid, const int32_t* n_pools,
                              const int32_t* cu_pool_cap, const int32_t* q_seq,
                              const int32_t* q_pos, int Q, int B, int kpool, int P_ld,
-                             float* scores, uint32_t* hist, const int32_t* safe_begin,
+                             float* scores, uint32_t* hist, EarlyStart early,
                              int32_t* status_dev, cudaStream_t stream, int busy_ctas = 0);
 // whether the decode kernel can start streaming before the compress of its call ends
 bool umma_index_early_ok(int Q, const int32_t* q_seq, const int32_t* q_pos);

@@ -84,12 +84,13 @@ struct Layout {
   static constexpr size_t w = ctl + ((sizeof(Ctl) + 15) & ~size_t(15));
   static constexpr size_t hist = w + (size_t)Cfg<G>::kBSlots * G * kH * 4;
   static constexpr size_t base = hist + (G == 1 ? (size_t)kHistBins * 4 : 0);
-  // cache bases, then (early start) the safe tile counts, then the tile prefix
+  // cache bases, then (early start) the safe tile counts and the pool counts
+  // found from the compress's inputs, then the tile prefix
   __host__ __device__ static size_t cached(int n_groups) {
     return (size_t)(n_groups < kBaseCache ? n_groups : kBaseCache);
   }
   __host__ __device__ static size_t prefix(int n_groups, bool early) {
-    return base + cached(n_groups) * 4 * (early ? 2 : 1);
+    return base + cached(n_groups) * 4 * (early ? 3 : 1);
   }
   static size_t bytes(int n_groups, bool early) {
     return 1024 + prefix(n_groups, early) + (size_t)(n_groups + 1) * 4;
@@ -104,10 +105,12 @@ struct QMeta {
 };
 
 // Candidate range of query qi (as the other index kernels define it).
+// np_known >= 0 stands in for n_pools[b] (the same value, found before the
+// kernel that writes n_pools has ended).
 __device__ __forceinline__ QMeta qmeta(int qi, int Q, const int32_t* q_seq, const int32_t* q_pos,
                                        const int32_t* n_pools, const int32_t* cu_pool_cap,
                                        const int32_t* pool_start, int B, int kpool, int P_ld,
-                                       int32_t* status, bool report) {
+                                       int32_t* status, bool report, int np_known = -1) {
   QMeta m{0, 0, 0x7fffffff, 0};
   if (qi >= Q) return m;
   const int b = q_seq ? q_seq[qi] : 0;
@@ -118,7 +121,7 @@ __device__ __forceinline__ QMeta qmeta(int qi, int Q, const int32_t* q_seq, cons
   m.valid = 1;
   m.base = cu_pool_cap[b];
   const int cap = cu_pool_cap[b + 1] - cu_pool_cap[b];
-  const int np = n_pools[b];
+  const int np = np_known >= 0 ? np_known : n_pools[b];
   int P = min(np, min(cap, P_ld));
   if (np > P && report) flag(status, DSA_DEV_POOL_RANGE);
   P = max(P, 0);
@@ -131,6 +134,32 @@ __device__ __forceinline__ QMeta qmeta(int qi, int Q, const int32_t* q_seq, cons
   }
   m.n_cand = P;
   return m;
+}
+
+// The pool count that the compress of the same call writes for sequence b:
+// min((T - t0) / kpool, cap), t0 its first valid token (T when it has none).
+// Found when t0 lies among the first kScanTokens tokens or the sequence is no
+// longer than that, else -1.  Called by a whole warp; every lane gets the value.
+constexpr int kScanTokens = 256;
+__device__ __forceinline__ int early_pool_count(const EarlyStart& es, int b, int cap, int kpool,
+                                                int lane) {
+  const long long lo = es.cu_seqlens[b];
+  const int T = es.cu_seqlens[b + 1] - es.cu_seqlens[b];
+  const int lim = min(T, kScanTokens);
+  uint32_t nz[kScanTokens / 32];
+#pragma unroll
+  for (int j = 0; j < kScanTokens / 32; ++j) {  // every load first, then the votes
+    const int t = j * 32 + lane;
+    nz[j] = t < lim ? es.valid[lo + t] : 0u;
+  }
+  int t0 = -1;
+#pragma unroll
+  for (int j = 0; j < kScanTokens / 32; ++j) {
+    const uint32_t m = __ballot_sync(0xffffffffu, nz[j] != 0u);
+    if (t0 < 0 && m != 0u) t0 = j * 32 + __ffs((int)m) - 1;
+  }
+  if (t0 < 0 && T <= kScanTokens) t0 = T;
+  return t0 < 0 ? -1 : min((T - t0) / kpool, cap);
 }
 
 __device__ __forceinline__ void epi_bar() {
@@ -157,7 +186,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                              const int32_t* __restrict__ cu_pool_cap,
                              const int32_t* __restrict__ q_seq, const int32_t* __restrict__ q_pos,
                              int Q, int B, int kpool, int P_ld, float* __restrict__ scores,
-                             uint32_t* __restrict__ hist, const int32_t* __restrict__ safe_begin,
+                             uint32_t* __restrict__ hist, const EarlyStart es,
                              int32_t* status) {
   using C = Cfg<G>;
   using LY = Layout<G>;
@@ -169,12 +198,14 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   uint32_t* s_hist = reinterpret_cast<uint32_t*>(sbase + LY::hist);
   const int n_groups = (Q + G - 1) / G;
   // Early start (decode, inside one call after the compress of pools
-  // [safe_begin[b], ...)): the tile plan comes from the call's inputs only, and
-  // the key tiles below safe_begin[b], which that compress does not write, are
-  // streamed before the compress has finished.
-  const bool early = G == 1 && safe_begin != nullptr;
+  // [es.pool_begin[b], ...)): the tile plan comes from the call's inputs only;
+  // the key tiles below pool_begin[b], which that compress does not write, are
+  // streamed and scored before the compress has finished, with the pool count
+  // found from the compress's own inputs.
+  const bool early = G == 1 && es.pool_begin != nullptr;
   int* s_base = reinterpret_cast<int*>(sbase + LY::base);  // first cache row of group gi
   int* s_safe = s_base + LY::cached(n_groups);             // early: tiles readable at once
+  int* s_np = s_safe + LY::cached(n_groups);               // early: pool count, or -1
   int* s_prefix = reinterpret_cast<int*>(sbase + LY::prefix(n_groups, early));
   volatile int* abort = &ctl.abort;
   const bool use_hist = G == 1 && hist != nullptr;
@@ -236,7 +267,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           base = cu_pool_cap[b];
           const int cap = cu_pool_cap[b + 1] - cu_pool_cap[b];
           nt = (max(0, min(cap, P_ld)) + kBM - 1) / kBM;
-          safe = min(nt, max(0, safe_begin[b]) / kBM);
+          safe = min(nt, max(0, es.pool_begin[b]) / kBM);
         } else if (blockIdx.x == 0) {
           flag(status, DSA_DEV_BAD_QSEQ);
         }
@@ -379,13 +410,29 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     const int half = ew >> 2;
     const int r = quarter * 32 + lane;      // pool row within the tile
     const int qw0 = G == 1 ? 0 : half * GH; // this warp's first query of the group
+    bool waited = !early;  // the compress of this call has ended
     if (early) {
-      pdl_wait();  // n_pools, pool_valid and pool_start of this step
+      // A kernel after the first of its call may let its dependents launch
+      // before its own wait: it was itself launched by the trigger of a kernel
+      // that had waited, so nothing enqueued before the call is still running.
       pdl_launch_dependents();
-      if (blockIdx.x == 0)  // the range checks the tile plan skipped
-        for (int qi = ew * 32 + lane; qi < Q; qi += kEpiWarps * 32)
-          qmeta(qi, Q, q_seq, q_pos, n_pools, cu_pool_cap, pool_start, B, kpool, P_ld, status,
-                true);
+      // the pool count of every sequence this CTA scores: with it, the tiles
+      // below pool_begin need nothing that the compress writes
+      if (t_lo < t_hi) {
+        int g_lo = 0;
+        while (s_prefix[g_lo + 1] <= t_lo) ++g_lo;
+        int g_hi = g_lo;
+        while (g_hi + 1 < n_groups && s_prefix[g_hi + 1] < t_hi) ++g_hi;
+        for (int g = g_lo + ew; g <= g_hi; g += kEpiWarps) {
+          const int b = q_seq ? q_seq[g] : 0;
+          const int np = (b >= 0 && b < B) ? early_pool_count(es, b,
+                                                              cu_pool_cap[b + 1] - cu_pool_cap[b],
+                                                              kpool, lane)
+                                           : -1;
+          if (lane == 0) s_np[g] = np;
+        }
+      }
+      epi_bar();
     }
     int gi = 0, seg = 0;
     long long tc = 0;
@@ -393,12 +440,20 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       while (s_prefix[gi + 1] <= t) ++gi;
       const long long seg_hi = min(t_hi, (long long)s_prefix[gi + 1]);
       const int slot = seg % C::kBSlots;
+      int np_known = -1;
+      if (early) {
+        np_known = s_np[gi];
+        if (np_known < 0 && !waited) {  // not found from the inputs: read what the compress wrote
+          pdl_wait();
+          waited = true;
+        }
+      }
       QMeta mq[GH];
       int ncmax = 0;
 #pragma unroll
       for (int u = 0; u < GH; ++u) {
         mq[u] = qmeta(gi * G + qw0 + u, Q, q_seq, q_pos, n_pools, cu_pool_cap, pool_start, B,
-                      kpool, P_ld, status, false);
+                      kpool, P_ld, status, false, np_known);
         ncmax = max(ncmax, mq[u].n_cand);
       }
       const long long base = mq[0].base;  // every query of a group reads one sequence
@@ -411,6 +466,10 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       for (; t < seg_hi; ++t, ++tc) {
         const int acc = (int)(tc & 1);
         if (G == 1 && acc != half) continue;  // the other half's tile
+        if (!waited && t - s_prefix[gi] >= s_safe[gi]) {  // a tile the compress may rewrite
+          pdl_wait();
+          waited = true;
+        }
         const int p = (int)(t - s_prefix[gi]) * kBM + r;
         // candidate metadata first: its latency hides behind the accumulator wait
         uint8_t pv = 0;
@@ -464,6 +523,15 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         }
         epi_bar();
       }
+    }
+    if (early) {
+      // every CTA ends after the compress, so that the end of this kernel
+      // implies the end of the compress for whatever waits on it
+      if (!waited) pdl_wait();
+      if (blockIdx.x == 0)  // the range checks the tile plan skipped
+        for (int qi = ew * 32 + lane; qi < Q; qi += kEpiWarps * 32)
+          qmeta(qi, Q, q_seq, q_pos, n_pools, cu_pool_cap, pool_start, B, kpool, P_ld, status,
+                true);
     }
   }
 
@@ -531,9 +599,9 @@ int launch_g(const void* q, const float* weights, float scale, const void* pool_
              int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
              const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
              const int32_t* q_pos, int Q, int B, int kpool, int P_ld, float* scores,
-             uint32_t* hist, const int32_t* safe_begin, int32_t* status, cudaStream_t stream,
+             uint32_t* hist, const EarlyStart& es, int32_t* status, cudaStream_t stream,
              int busy_ctas) {
-  const size_t smem = Layout<G>::bytes((Q + G - 1) / G, safe_begin != nullptr);
+  const size_t smem = Layout<G>::bytes((Q + G - 1) / G, es.pool_begin != nullptr);
   if (smem > (size_t)kSmemMax) return DSA_ERR_UNSUPPORTED;
   CUtensorMap mk, mq;
   if (!make_map(&mk, pool_keys, (uint64_t)pool_rows, kBM)) return DSA_ERR_CUDA;
@@ -560,7 +628,7 @@ int launch_g(const void* q, const float* weights, float scale, const void* pool_
   const cudaError_t e = cudaLaunchKernelEx(&cfg, index_scores_umma_kernel<G>, mk, mq, weights,
                                            scale, pool_start, pool_valid, n_pools, cu_pool_cap,
                                            q_seq, q_pos, Q, B, kpool, P_ld, scores, hist,
-                                           safe_begin, status);
+                                           es, status);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -583,18 +651,19 @@ int launch_index_scores_umma(const void* q, const float* weights, float scale,
                              const uint8_t* pool_valid, const int32_t* n_pools,
                              const int32_t* cu_pool_cap, const int32_t* q_seq,
                              const int32_t* q_pos, int Q, int B, int kpool, int P_ld,
-                             float* scores, uint32_t* hist, const int32_t* safe_begin,
+                             float* scores, uint32_t* hist, EarlyStart es,
                              int32_t* status_dev, cudaStream_t stream, int busy_ctas) {
   const int G = umma_index_group(Q, q_seq);
   if (G == 8)
     return launch_g<8>(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid, n_pools,
-                       cu_pool_cap, q_seq, q_pos, Q, B, kpool, P_ld, scores, nullptr, nullptr,
-                       status_dev, stream, 0);
+                       cu_pool_cap, q_seq, q_pos, Q, B, kpool, P_ld, scores, nullptr,
+                       EarlyStart{}, status_dev, stream, 0);
   if (G == 1) {
-    const bool early = safe_begin != nullptr && umma_index_early_ok(Q, q_seq, q_pos);
+    const bool early = es.pool_begin != nullptr && es.valid != nullptr &&
+                       es.cu_seqlens != nullptr && umma_index_early_ok(Q, q_seq, q_pos);
     return launch_g<1>(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid, n_pools,
                        cu_pool_cap, q_seq, q_pos, Q, B, kpool, P_ld, scores, hist,
-                       early ? safe_begin : nullptr, status_dev, stream, early ? busy_ctas : 0);
+                       early ? es : EarlyStart{}, status_dev, stream, early ? busy_ctas : 0);
   }
   return DSA_ERR_UNSUPPORTED;
 }

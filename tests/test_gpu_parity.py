@@ -355,6 +355,43 @@ def test_decode_layer_matches_the_three_calls():
         assert int(a.status.item()) == 0
 
 
+@pytest.mark.parametrize("step", ["last_pool", "past_last_pool", "half"])
+def test_decode_layer_incremental_pool_count_from_the_valid_mask(step):
+    """Incremental steps on sequences that start with 0, 37, 255, 256 or 1000
+    padding tokens, a short fully valid one and an all-padding one.  Inside the
+    fused call the scoring kernel scores the key tiles below pool_begin before
+    the compress has ended, with each pool count found from the valid mask when
+    the first valid token is among the sequence's first 256 tokens (else it
+    reads the count the compress wrote); the fused call must write exactly what
+    the three separate calls write."""
+    big = Geometry(D=128, H=32, kpool=4, select_k=512, out_width=2048, Hm=64, L=512, dtype="bf16")
+    lengths = [3000, 3000, 2900, 3100, 4000, 250, 200]
+    pads = [0, 37, 255, 256, 1000, 0, 200]
+    bt = synth.make_batch(big, lengths, pads, device=DEV, seed=71)
+    a = pipeline.LayerBuffers.alloc(bt)
+    b = pipeline.LayerBuffers.alloc(bt)
+    pipeline.decode_layer(bt, a)
+    pipeline.run_layer(bt, b)
+    torch.cuda.synchronize()
+    _assert_same_outputs(a, b)
+    n = a.n_pools.clone()
+    begin = {"last_pool": (n - 1).clamp(min=0), "past_last_pool": n,
+             "half": n // 2}[step].to(torch.int32)
+    for s in range(bt.B):
+        lo = int(bt.cu_seqlens[s]) + bt.pads[s] + max(int(n[s]) - 1, 0) * bt.geo.kpool
+        bt.k[lo:lo + bt.geo.kpool] *= -1
+    for buf in (a, b):
+        buf.out.zero_()
+        buf.scores.fill_(7.0)
+        buf.status.zero_()
+    max_pools = bt.P_ld if step == "half" else 1
+    pipeline.decode_layer(bt, a, pool_begin=begin, max_pools=max_pools)
+    pipeline.run_layer(bt, b, pool_begin=begin, max_pools=max_pools)
+    torch.cuda.synchronize()
+    _assert_same_outputs(a, b)
+    assert torch.equal(a.n_pools, n)
+
+
 def test_decode_layer_parity_against_the_oracle():
     bt = ragged_small(seed=53)
     buf = pipeline.LayerBuffers.alloc(bt)
