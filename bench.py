@@ -421,8 +421,6 @@ def run_ours(args, dist):
             events[li][1].record()
             pipeline.attend(bt, buf)
 
-    kernels_per_layer = 5   # compress, index scores (+histogram), select (+expand), MLA, MLA merge
-
     # ---- warm-up (eager), then capture
     for _ in range(max(3, args.warmup)):
         step()
@@ -435,10 +433,13 @@ def run_ours(args, dist):
     side.wait_stream(torch.cuda.current_stream())
     # g_plain: the production step, kernels chained by programmatic dependent launch
     g_plain = torch.cuda.CUDAGraph()
+    n0 = ops.dsa_kernel_launches()
     with torch.cuda.stream(side):
         with torch.cuda.graph(g_plain, stream=side):
             for s in range(S):
                 step()
+    # the library's own count of the kernels recorded for S steps
+    launches_per_step = (ops.dsa_kernel_launches() - n0) // S
     # g_ev: the same steps with timing events around every select call (the
     # event nodes break the launch chain there, so this graph runs a little slower)
     try:
@@ -607,7 +608,7 @@ def run_ours(args, dist):
                    "l2": "inputs larger than L2: %d layers x %d MiB pool keys cycle through "
                          "the 129 MB L2" % (n_layers, B * (T // geo.kpool) * geo.D * 2 >> 20),
                    "graph": "CUDA graph of %d steps replayed %d times" % (S, R)},
-        "gpu_launches": kernels_per_layer * n_layers * K,
+        "gpu_launches": launches_per_step * K,
         "roofline": roofline, "select_call_in_step": select_call,
         "step_hbm_gbs": round(step_gbs, 1), "step_frac_of_peak": round(step_gbs / hbm_peak, 4),
         "ms_per_step_with_event_nodes": None if ev_step_ms is None else round(ev_step_ms, 5),

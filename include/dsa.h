@@ -395,6 +395,12 @@ const char* dsa_status_string(int status);
 /* Library version: major * 10000 + minor * 100 + patch. */
 int dsa_version(void);
 
+/* Number of kernels the library has launched, or recorded into a stream
+   capture, since it was loaded (every thread and device).  Replays of a
+   captured graph launch its kernels without passing through the library and
+   are not counted: count the capture, then multiply by the replays. */
+uint64_t dsa_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

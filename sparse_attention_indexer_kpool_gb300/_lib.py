@@ -66,6 +66,7 @@ SIGNATURES = {
                                                    ctypes.POINTER(c_size_t)]),
     "dsa_status_string": (ctypes.c_char_p, [c_int]),
     "dsa_version": (c_int, []),
+    "dsa_kernel_launches": (ctypes.c_uint64, []),
 }
 
 

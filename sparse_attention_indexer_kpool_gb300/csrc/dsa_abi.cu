@@ -141,9 +141,18 @@ int check_mla_paged(const void* q_lat, const dsa_paged_kv* kv, const int32_t* q_
 
 }  // namespace
 
+namespace dsa {
+std::atomic<unsigned long long>& launch_counter() {
+  static std::atomic<unsigned long long> n{0};
+  return n;
+}
+}  // namespace dsa
+
 extern "C" {
 
 int dsa_version(void) { return 10000; }
+
+uint64_t dsa_kernel_launches(void) { return dsa::launch_counter().load(); }
 
 const char* dsa_status_string(int status) {
   switch (status) {

@@ -5,6 +5,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <utility>
+
 #include "../../include/dsa.h"
 
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
@@ -15,6 +18,18 @@ namespace dsa {
 
 constexpr int kNumSMs = 152;         // GB300: 2 dies x 76 SMs (launch-shape heuristics only)
 constexpr int kKpoolMax = DSA_KPOOL_MAX;
+
+// ---------------------------------------------------------------- launches
+// Every kernel of the library is launched through launch_kernel, which counts
+// the launches that succeed (dsa_kernel_launches reports the count).
+std::atomic<unsigned long long>& launch_counter();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(const cudaLaunchConfig_t* cfg, void (*kernel)(KArgs...),
+                          Args&&... args) {
+  const cudaError_t e = cudaLaunchKernelEx(cfg, kernel, std::forward<Args>(args)...);
+  if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
 
 // ---------------------------------------------------------------- status
 __device__ __forceinline__ void flag(int32_t* status, int bit) {

@@ -625,7 +625,7 @@ int launch_g(const void* q, const float* weights, float scale, const void* pool_
   cfg.stream = stream;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, index_scores_umma_kernel<G>, mk, mq, weights,
+  const cudaError_t e = launch_kernel(&cfg, index_scores_umma_kernel<G>, mk, mq, weights,
                                            scale, pool_start, pool_valid, n_pools, cu_pool_cap,
                                            q_seq, q_pos, Q, B, kpool, P_ld, scores, hist,
                                            es, status);

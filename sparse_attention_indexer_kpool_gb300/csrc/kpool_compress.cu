@@ -272,7 +272,7 @@ int launch_t(const void* k, const void* gate, const uint8_t* valid, const float*
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(
+  cudaError_t e = launch_kernel(
       &cfg, kpool_compress_kernel<T, V>, (const T*)k, (const T*)gate, valid, ape, (const T*)g,
       (const T*)be, eps, cu, cap, begin, kpool, max_pools, (T*)pk, ps, pv, np, st);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;

@@ -589,7 +589,7 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
     cfg.gridDim = dim3(Hm, Q, 1);
     cfg.blockDim = dim3(128, 1, 1);
     cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, mla_merge_kernel, (const float*)part_o,
+    return launch_kernel(&cfg, mla_merge_kernel, (const float*)part_o,
                               (const float*)part_ml, Hm, n_split, (__nv_bfloat16*)out,
                               lse) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
   }
@@ -605,7 +605,7 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
     cfg.gridDim = dim3(Hm, Q, 1);
     cfg.blockDim = dim3(128, 1, 1);
     cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, mla_merge_kernel, (const float*)part_o,
+    return launch_kernel(&cfg, mla_merge_kernel, (const float*)part_o,
                               (const float*)part_ml, Hm, n_split, (__nv_bfloat16*)out,
                               lse) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
   }
@@ -622,7 +622,7 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
     cfg.gridDim = dim3(n_split, Hm / kHG, Q);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
-    if (cudaLaunchKernelEx(&cfg, mla_mma_kernel, (const __nv_bfloat16*)q_lat,
+    if (launch_kernel(&cfg, mla_mma_kernel, (const __nv_bfloat16*)q_lat,
                            (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, Hm,
                            out_width, rows, sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml,
                            status_dev) != cudaSuccess)
@@ -631,7 +631,7 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
       cfg.gridDim = dim3(Hm, Q, 1);
       cfg.blockDim = dim3(128, 1, 1);
       cfg.dynamicSmemBytes = 0;
-      if (cudaLaunchKernelEx(&cfg, mla_merge_kernel, (const float*)part_o,
+      if (launch_kernel(&cfg, mla_merge_kernel, (const float*)part_o,
                              (const float*)part_ml, Hm, n_split, (__nv_bfloat16*)out,
                              lse) != cudaSuccess)
         return DSA_ERR_CUDA;
@@ -647,13 +647,13 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
   if (dtype == DSA_BF16) {
     cudaFuncSetAttribute(mla_simt_kernel<__nv_bfloat16>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    e = cudaLaunchKernelEx(&cfg, mla_simt_kernel<__nv_bfloat16>, (const __nv_bfloat16*)q_lat,
+    e = launch_kernel(&cfg, mla_simt_kernel<__nv_bfloat16>, (const __nv_bfloat16*)q_lat,
                            (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, Hm, L,
                            out_width, sm_scale, (__nv_bfloat16*)out, lse, status_dev);
   } else {
     cudaFuncSetAttribute(mla_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
-    e = cudaLaunchKernelEx(&cfg, mla_simt_kernel<float>, (const float*)q_lat, (const float*)kv,
+    e = launch_kernel(&cfg, mla_simt_kernel<float>, (const float*)q_lat, (const float*)kv,
                            cu_seqlens, q_seq, token_ids, B, Hm, L, out_width, sm_scale,
                            (float*)out, lse, status_dev);
   }
@@ -708,7 +708,7 @@ int launch_mla_paged_decode(const void* q_lat, const PagedKv& kv, const int32_t*
     cfg.gridDim = dim3(Hm, Q, 1);
     cfg.blockDim = dim3(128, 1, 1);
     cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, mla_merge_kernel, (const float*)part_o,
+    return launch_kernel(&cfg, mla_merge_kernel, (const float*)part_o,
                               (const float*)part_ml, Hm, n_split, (__nv_bfloat16*)out,
                               lse) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
   }
@@ -721,13 +721,13 @@ int launch_mla_paged_decode(const void* q_lat, const PagedKv& kv, const int32_t*
   if (dtype == DSA_BF16) {
     cudaFuncSetAttribute(mla_simt_paged_kernel<__nv_bfloat16>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    e = cudaLaunchKernelEx(&cfg, mla_simt_paged_kernel<__nv_bfloat16>,
+    e = launch_kernel(&cfg, mla_simt_paged_kernel<__nv_bfloat16>,
                            (const __nv_bfloat16*)q_lat, kv, q_seq, token_ids, B, Hm, L, out_width,
                            sm_scale, (__nv_bfloat16*)out, lse, status_dev);
   } else {
     cudaFuncSetAttribute(mla_simt_paged_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
-    e = cudaLaunchKernelEx(&cfg, mla_simt_paged_kernel<float>, (const float*)q_lat, kv, q_seq,
+    e = launch_kernel(&cfg, mla_simt_paged_kernel<float>, (const float*)q_lat, kv, q_seq,
                            token_ids, B, Hm, L, out_width, sm_scale, (float*)out, lse,
                            status_dev);
   }

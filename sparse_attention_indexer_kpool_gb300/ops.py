@@ -264,3 +264,8 @@ def dsa_decode_layer(k, gate, valid, ape, ln_gamma, ln_beta, ln_eps, cu_seqlens,
         ws_mla_bytes=0 if ws_mla is None else ws_mla.numel(),
         status_dev=_ptr(status, torch.int32, "status"))
     _check("dsa_decode_layer", _lib.load().dsa_decode_layer(ctypes.byref(a), _stream(stream)))
+
+
+def dsa_kernel_launches() -> int:
+    """Kernels the library has launched (or recorded into a stream capture) so far."""
+    return int(_lib.load().dsa_kernel_launches())

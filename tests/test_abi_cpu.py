@@ -22,7 +22,8 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(dsa_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|uint64_t|const char\*)\s+(dsa_\w+)\s*\(",
+                                 text, re.M)))
 
 
 def header_define(name):
@@ -105,6 +106,13 @@ def test_topk_validation(lib):
     assert lib.dsa_topk_pools(A + 2, 4, 1000, 16, A, None, 0, None) == ERR["DSA_ERR_MISALIGNED"]
     assert lib.dsa_topk_pools(None, 4, 1000, 16, A, None, 0, None) == ERR["DSA_ERR_INVALID_ARG"]
     assert lib.dsa_topk_pools(A, 0, 1000, 16, A, None, 0, None) == ERR["DSA_OK"]
+
+
+def test_rejected_and_empty_calls_launch_nothing(lib):
+    n = lib.dsa_kernel_launches()
+    assert lib.dsa_topk_pools(A, 4, 1000, 0, A, None, 0, None) == ERR["DSA_ERR_INVALID_ARG"]
+    assert lib.dsa_topk_pools(A, 0, 1000, 16, A, None, 0, None) == ERR["DSA_OK"]  # no queries
+    assert lib.dsa_kernel_launches() == n
 
 
 def test_expand_validation(lib):

@@ -392,6 +392,24 @@ def test_decode_layer_incremental_pool_count_from_the_valid_mask(step):
     assert torch.equal(a.n_pools, n)
 
 
+def test_decode_layer_launches_what_the_three_calls_launch():
+    """The library's launch count: the fused call launches as many kernels as
+    compress -> select -> attend, and an incremental step launches them again."""
+    bt = ragged_small(seed=54)
+    a = pipeline.LayerBuffers.alloc(bt)
+    b = pipeline.LayerBuffers.alloc(bt)
+    n0 = ops.dsa_kernel_launches()
+    pipeline.decode_layer(bt, a)
+    n1 = ops.dsa_kernel_launches()
+    pipeline.run_layer(bt, b)
+    n2 = ops.dsa_kernel_launches()
+    torch.cuda.synchronize()
+    assert n1 - n0 == n2 - n1 >= 4
+    begin = (a.n_pools - 1).clamp(min=0).to(torch.int32)
+    pipeline.decode_layer(bt, a, pool_begin=begin, max_pools=1)
+    assert ops.dsa_kernel_launches() - n2 == n1 - n0
+
+
 def test_decode_layer_parity_against_the_oracle():
     bt = ragged_small(seed=53)
     buf = pipeline.LayerBuffers.alloc(bt)
