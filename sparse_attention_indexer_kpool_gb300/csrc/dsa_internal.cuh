@@ -118,6 +118,19 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N));
 }
+// The same with a count known only after unrolling (0..7; more waits for all).
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+  switch (n) {
+    case 7: cp_async_wait<7>(); break;
+    case 6: cp_async_wait<6>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 1: cp_async_wait<1>(); break;
+    default: cp_async_wait<0>(); break;
+  }
+}
 
 // ---------------------------------------------------------------- mbarrier + bulk copy
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -9,9 +9,9 @@
 // selected rows and one half of the heads (32):
 //   1. the query's q_lat half (32 x 512) and the split's 128 latent rows are
 //      gathered with 16-byte cp.async into 128-byte-swizzled tiles (eight
-//      64-column blocks each);
+//      64-column blocks each; bf16 rows in one cp.async group per block);
 //   2. S^T = C q^T on the tensor cores: M = 128 rows, N = 32 heads, K = 512, one
-//      thread issues 32 MMAs into TMEM;
+//      thread issues 32 MMAs into TMEM, four per block as each block lands;
 //   3. softmax per head over the 128 rows: each thread reads its row's scores
 //      of 16 heads, a butterfly over the warp reduces the 16 columns across the
 //      warp's 32 rows, four warps combine through shared memory; the
@@ -191,16 +191,44 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     c.prow[threadIdx.x] = (int)prow;
   }
   __syncthreads();
+  const uint32_t kvb = smem_u32(sb + kOffKv), qb = smem_u32(sb + kOffQ);
+  const uint32_t ptb = smem_u32(sb + kOffPt);
+  constexpr uint32_t idesc_s = umma_idesc_bf16(kRows, kHh, false);
+
+  // ---- 2. S^T = C q^T  (M = 128 rows, N = 32 heads, K = 512)
   if (kKv != kKvPagedE4M3) {
+    // One cp.async group per 64-column block of the rows (after the query
+    // block's group).  The four MMAs of a block go out as soon as it has
+    // landed, while the later blocks are still in flight.
     const __nv_bfloat16* src =
         kKv == kKvContig ? kv : static_cast<const __nv_bfloat16*>(pk.pages);
-    for (int i = threadIdx.x; i < kRows * 64; i += kThreadsM) {
-      const int r = i >> 6, ch = i & 63;
-      const int prow = c.prow[r];
-      const bool ok = prow >= 0;
-      cp_async16(
-          smem_u32(sb + kOffKv + (ch >> 3) * kKvBlock + r * 128 + (((ch & 7) ^ (r & 7)) << 4)),
-          ok ? src + (long long)prow * kL + ch * 8 : src, ok);
+#pragma unroll
+    for (int blk = 0; blk < 8; ++blk) {
+#pragma unroll
+      for (int u = 0; u < kRows * 8 / kThreadsM; ++u) {
+        const int i = u * kThreadsM + threadIdx.x;
+        const int r = i >> 3, c8 = i & 7;  // eight consecutive threads: one 128-byte row piece
+        const int prow = c.prow[r];
+        const bool ok = prow >= 0;
+        cp_async16(smem_u32(sb + kOffKv + blk * kKvBlock + r * 128 + ((c8 ^ (r & 7)) << 4)),
+                   ok ? src + (long long)prow * kL + blk * 64 + c8 * 8 : src, ok);
+      }
+      cp_async_commit();
+    }
+#pragma unroll
+    for (int blk = 0; blk < 8; ++blk) {
+      cp_async_wait_pending(7 - blk);  // the query block and row blocks 0..blk
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        tc_fence_after();
+        const uint32_t tm = c.tmem_base;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_bf16(tm, sw128_desc(kvb + blk * kKvBlock + k * 32),
+                    sw128_desc(qb + blk * kQBlock + k * 32), idesc_s, (blk | k) ? 1u : 0u);
+      }
     }
   } else {
     // 16 codes per 16-byte load, every load of the tile in flight at once; each
@@ -235,28 +263,25 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                                   (((ch & 7) ^ (r & 7)) << 4)) = v;
       }
     }
+    cp_async_commit();
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      tc_fence_after();
+      const uint32_t tm = c.tmem_base;
+#pragma unroll
+      for (int kk = 0; kk < 32; ++kk) {
+        const uint32_t blk = kk >> 2, off = (kk & 3) * 32;
+        umma_bf16(tm, sw128_desc(kvb + blk * kKvBlock + off),
+                  sw128_desc(qb + blk * kQBlock + off), idesc_s, kk > 0 ? 1u : 0u);
+      }
+    }
   }
-  cp_async_commit();
-  cp_async_wait<0>();
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
+  if (threadIdx.x == 0) umma_commit(&c.s_ready);
   tc_fence_after();
   const uint32_t tmem = c.tmem_base;
-  const uint32_t kvb = smem_u32(sb + kOffKv), qb = smem_u32(sb + kOffQ);
-  const uint32_t ptb = smem_u32(sb + kOffPt);
-
-  // ---- 2. S^T = C q^T  (M = 128 rows, N = 32 heads, K = 512)
-  if (threadIdx.x == 0) {
-    constexpr uint32_t idesc = umma_idesc_bf16(kRows, kHh, false);
-#pragma unroll
-    for (int kk = 0; kk < 32; ++kk) {
-      const uint32_t blk = kk >> 2, off = (kk & 3) * 32;
-      umma_bf16(tmem, sw128_desc(kvb + blk * kKvBlock + off), sw128_desc(qb + blk * kQBlock + off),
-                idesc, kk > 0 ? 1u : 0u);
-    }
-    umma_commit(&c.s_ready);
-  }
   bool ok = mbar_wait_bounded(&c.s_ready, 0);
   if (!ok && lane == 0) flag(status, DSA_DEV_TIMEOUT);
   tc_fence_after();
