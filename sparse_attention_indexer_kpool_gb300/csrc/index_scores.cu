@@ -131,15 +131,15 @@ int launch_index_scores(const void* q, const float* weights, float scale, const 
     cudaFuncSetAttribute(index_scores_simt_kernel<__nv_bfloat16>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, 80 * 1024);
     e = launch_kernel(&cfg, index_scores_simt_kernel<__nv_bfloat16>,
-                           (const __nv_bfloat16*)q, weights, scale,
-                           (const __nv_bfloat16*)pool_keys, pool_start, pool_valid, n_pools,
-                           cu_pool_cap, q_seq, q_pos, B, H, D, kpool, P_ld, scores, status_dev);
+                      (const __nv_bfloat16*)q, weights, scale,
+                      (const __nv_bfloat16*)pool_keys, pool_start, pool_valid, n_pools,
+                      cu_pool_cap, q_seq, q_pos, B, H, D, kpool, P_ld, scores, status_dev);
   } else {
     cudaFuncSetAttribute(index_scores_simt_kernel<float>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, 80 * 1024);
     e = launch_kernel(&cfg, index_scores_simt_kernel<float>, (const float*)q, weights, scale,
-                           (const float*)pool_keys, pool_start, pool_valid, n_pools, cu_pool_cap,
-                           q_seq, q_pos, B, H, D, kpool, P_ld, scores, status_dev);
+                      (const float*)pool_keys, pool_start, pool_valid, n_pools, cu_pool_cap,
+                      q_seq, q_pos, B, H, D, kpool, P_ld, scores, status_dev);
   }
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

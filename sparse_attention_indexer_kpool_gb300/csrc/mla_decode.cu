@@ -590,8 +590,8 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
     cfg.blockDim = dim3(128, 1, 1);
     cfg.dynamicSmemBytes = 0;
     return launch_kernel(&cfg, mla_merge_kernel, (const float*)part_o,
-                              (const float*)part_ml, Hm, n_split, (__nv_bfloat16*)out,
-                              lse) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+                         (const float*)part_ml, Hm, n_split, (__nv_bfloat16*)out,
+                         lse) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
   }
   if (mla_umma_shape_ok(Hm, L, dtype)) {  // many queries: the streaming tcgen05 kernel
     const int n_split = mla_stream_splits(Q, out_width);
@@ -606,8 +606,8 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
     cfg.blockDim = dim3(128, 1, 1);
     cfg.dynamicSmemBytes = 0;
     return launch_kernel(&cfg, mla_merge_kernel, (const float*)part_o,
-                              (const float*)part_ml, Hm, n_split, (__nv_bfloat16*)out,
-                              lse) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+                         (const float*)part_ml, Hm, n_split, (__nv_bfloat16*)out,
+                         lse) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
   }
   if (fast_path(Hm, L, dtype)) {
     int n_split, rows;
@@ -623,17 +623,17 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     if (launch_kernel(&cfg, mla_mma_kernel, (const __nv_bfloat16*)q_lat,
-                           (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, Hm,
-                           out_width, rows, sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml,
-                           status_dev) != cudaSuccess)
+                      (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, Hm,
+                      out_width, rows, sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml,
+                      status_dev) != cudaSuccess)
       return DSA_ERR_CUDA;
     if (n_split > 1) {
       cfg.gridDim = dim3(Hm, Q, 1);
       cfg.blockDim = dim3(128, 1, 1);
       cfg.dynamicSmemBytes = 0;
       if (launch_kernel(&cfg, mla_merge_kernel, (const float*)part_o,
-                             (const float*)part_ml, Hm, n_split, (__nv_bfloat16*)out,
-                             lse) != cudaSuccess)
+                        (const float*)part_ml, Hm, n_split, (__nv_bfloat16*)out,
+                        lse) != cudaSuccess)
         return DSA_ERR_CUDA;
     }
     return DSA_OK;
@@ -648,14 +648,14 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
     cudaFuncSetAttribute(mla_simt_kernel<__nv_bfloat16>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     e = launch_kernel(&cfg, mla_simt_kernel<__nv_bfloat16>, (const __nv_bfloat16*)q_lat,
-                           (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, Hm, L,
-                           out_width, sm_scale, (__nv_bfloat16*)out, lse, status_dev);
+                      (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, Hm, L,
+                      out_width, sm_scale, (__nv_bfloat16*)out, lse, status_dev);
   } else {
     cudaFuncSetAttribute(mla_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
     e = launch_kernel(&cfg, mla_simt_kernel<float>, (const float*)q_lat, (const float*)kv,
-                           cu_seqlens, q_seq, token_ids, B, Hm, L, out_width, sm_scale,
-                           (float*)out, lse, status_dev);
+                      cu_seqlens, q_seq, token_ids, B, Hm, L, out_width, sm_scale,
+                      (float*)out, lse, status_dev);
   }
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
@@ -709,8 +709,8 @@ int launch_mla_paged_decode(const void* q_lat, const PagedKv& kv, const int32_t*
     cfg.blockDim = dim3(128, 1, 1);
     cfg.dynamicSmemBytes = 0;
     return launch_kernel(&cfg, mla_merge_kernel, (const float*)part_o,
-                              (const float*)part_ml, Hm, n_split, (__nv_bfloat16*)out,
-                              lse) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+                         (const float*)part_ml, Hm, n_split, (__nv_bfloat16*)out,
+                         lse) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
   }
   if (L % 8 != 0 || L > 1024 || Hm > 128 || out_width > 16384) return DSA_ERR_UNSUPPORTED;
   const size_t smem = ((size_t)L + 2 * (size_t)out_width + 32) * 4;
@@ -722,14 +722,14 @@ int launch_mla_paged_decode(const void* q_lat, const PagedKv& kv, const int32_t*
     cudaFuncSetAttribute(mla_simt_paged_kernel<__nv_bfloat16>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     e = launch_kernel(&cfg, mla_simt_paged_kernel<__nv_bfloat16>,
-                           (const __nv_bfloat16*)q_lat, kv, q_seq, token_ids, B, Hm, L, out_width,
-                           sm_scale, (__nv_bfloat16*)out, lse, status_dev);
+                      (const __nv_bfloat16*)q_lat, kv, q_seq, token_ids, B, Hm, L, out_width,
+                      sm_scale, (__nv_bfloat16*)out, lse, status_dev);
   } else {
     cudaFuncSetAttribute(mla_simt_paged_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
     e = launch_kernel(&cfg, mla_simt_paged_kernel<float>, (const float*)q_lat, kv, q_seq,
-                           token_ids, B, Hm, L, out_width, sm_scale, (float*)out, lse,
-                           status_dev);
+                      token_ids, B, Hm, L, out_width, sm_scale, (float*)out, lse,
+                      status_dev);
   }
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

@@ -811,9 +811,9 @@ int launch_kind(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   return launch_kernel(&cfg, mla_umma_kernel<kKv>, (const __nv_bfloat16*)q_lat,
-                            (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, out_width,
-                            sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml, early ? 1 : 0,
-                            pk, status_dev) == cudaSuccess
+                       (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, out_width,
+                       sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml, early ? 1 : 0,
+                       pk, status_dev) == cudaSuccess
              ? DSA_OK
              : DSA_ERR_CUDA;
 }
@@ -853,9 +853,9 @@ int launch_stream_kind(const void* q_lat, const void* kv, const int32_t* cu_seql
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   return launch_kernel(&cfg, mla_stream_kernel<kKv>, (const __nv_bfloat16*)q_lat,
-                            (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, out_width,
-                            per, sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml, pk,
-                            status_dev) == cudaSuccess
+                       (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, out_width,
+                       per, sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml, pk,
+                       status_dev) == cudaSuccess
              ? DSA_OK
              : DSA_ERR_CUDA;
 }

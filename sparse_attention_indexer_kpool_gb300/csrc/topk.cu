@@ -620,7 +620,7 @@ int launch_select(const float* scores, int Q, int P_ld, int select_k, int32_t* p
                        (int)smem);
   cfg.dynamicSmemBytes = smem;
   return launch_kernel(&cfg, topk_select_kernel, scores, P_ld, select_k, hist, pool_ids,
-                            ex) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+                       ex) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 }  // namespace
@@ -674,7 +674,7 @@ int launch_expand_selection(const int32_t* pool_ids, const int32_t* pool_start,
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   cudaError_t e = launch_kernel(&cfg, expand_kernel, pool_ids, pool_start, cu_pool_cap, q_seq,
-                                     B, select_k, kpool, out_width, token_ids, status_dev);
+                                B, select_k, kpool, out_width, token_ids, status_dev);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
