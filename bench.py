@@ -337,9 +337,9 @@ def paged_attention(reps=20, page_size=64):
     assert int(st.item()) == 0, "device status set by the attention"
     return {"workload": "64-sequence ragged decode batch: %d queries x %d selected rows, %d heads, "
                         "latent %d, pages of %d rows" % (Q, W, Hm, L, page_size),
-            "kernels": {"contiguous_bf16": "mla_mma_kernel (mma.sync, 16-head groups) + merge",
-                        "paged_bf16": "mla_umma_kernel (tcgen05, paged rows) + merge",
-                        "paged_e4m3": "mla_umma_kernel (tcgen05, E4M3 rows) + merge"},
+            "kernels": {"contiguous_bf16": "mla_stream_kernel (tcgen05, bf16 rows) + merge",
+                        "paged_bf16": "mla_stream_kernel (tcgen05, paged rows) + merge",
+                        "paged_e4m3": "mla_stream_kernel (tcgen05, E4M3 rows) + merge"},
             "calls": res,
             "bytes": "per call: rows (bf16 2 B, E4M3 1 B per value; E4M3 adds a 4 B row "
                      "scale), 4 B token id and (paged) 4 B table entry per row, q, out, lse",
