@@ -1,6 +1,6 @@
 """The replica plumbing of bench.py on CPU: two gloo ranks, barrier and the
 max over ranks that the timed region uses; the reference arm runs on rank 0
-only."""
+only and prints one contract line."""
 import os
 import socket
 
@@ -54,3 +54,27 @@ def test_single_process_needs_no_process_group():
     assert d.pg is None and d.max(3.5) == 3.5
     d.barrier()
     d.close()
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one JSON
+    line with the headline metric, its own cpu_baseline and a zero-copy e2e."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    base = json.load(open(os.path.join(root, "BASELINE.json")))
+    assert d["impl"] == "reference" and d["metric"] == base["metric"]
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["n_gpus"] == 1
+    assert d["steps"] == 1 and d["warmup"] == 3 and d["config"]["workload"] == "long262k"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert cb["unit"] == d["unit"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
