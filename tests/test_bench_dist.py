@@ -69,8 +69,8 @@ def test_reference_arm_prints_one_contract_line():
     lines = [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
     assert len(lines) == 1
     d = json.loads(lines[0])
-    base = json.load(open(os.path.join(root, "BASELINE.json")))
-    assert d["impl"] == "reference" and d["metric"] == base["metric"]
+    import bench
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
     assert d["value"] > 0 and d["higher_is_better"] is True and d["n_gpus"] == 1
     assert d["steps"] == 1 and d["warmup"] == 3 and d["config"]["workload"] == "long262k"
     cb = d["cpu_baseline"]
