@@ -64,7 +64,7 @@ extern "C" {
 #define DSA_OK 0
 #define DSA_ERR_INVALID_ARG 1  /* bad size, null pointer, kpool not in [1,8], out_width too small */
 #define DSA_ERR_MISALIGNED 2   /* a pointer is not aligned as documented                         */
-#define DSA_ERR_UNSUPPORTED 3  /* geometry / dtype combination this build has no kernel for      */
+#define DSA_ERR_UNSUPPORTED 3  /* geometry / dtype combination the library has no kernel for     */
 #define DSA_ERR_WORKSPACE 4    /* workspace missing or smaller than the size query returns       */
 #define DSA_ERR_CUDA 5         /* a CUDA launch failed (cudaGetLastError after the launch)       */
 
