@@ -312,8 +312,10 @@ size_t dsa_select_workspace_size(int Q, int P_ld, int select_k);
  * GPU loading the library keeps until the process exits.
  *   Q must be <= 64 (else DSA_ERR_UNSUPPORTED).  All calls on a device share the
  *   array: each call clears the part it uses first, and calls that overlap on
- *   the GPU race on it.  The first call on a device looks up the array's device
- *   address; make it before any stream capture.  It allocates nothing.
+ *   the GPU race on it.  The first call on a device (with Q > 0) looks up the
+ *   array's device address; make it before any stream capture.  The address
+ *   is kept for the life of the process: the device's primary context must not
+ *   be reset in between (cudaDeviceReset).  It allocates nothing.
  */
 int dsa_select_noalloc(const void* q, const float* weights, float scale, const void* pool_keys,
                        int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
@@ -388,6 +390,27 @@ int dsa_decode_layer(const dsa_decode_layer_args* args, void* stream);
 /* Workspace sizes for the geometry in *args; returns their sum. */
 size_t dsa_decode_layer_workspace_size(const dsa_decode_layer_args* args, size_t* ws_select,
                                        size_t* ws_mla);
+
+/*
+ * dsa_set_failure_drill - arm (DSA_DRILL_SKIP_ARM) or disarm (0) a drill of
+ * the kernels' give-up path, for tests of failure detection.
+ *
+ * The pages have no counterpart: the library's waits on its own asynchronous
+ * copies and tensor-core MMAs are bounded (1 s of the GPU's global timer), and
+ * a wait that runs out sets DSA_DEV_TIMEOUT in *status_dev, issues nothing
+ * more, waits (bounded) for what it already issued, frees its tensor memory
+ * and returns, so the CUDA context stays usable.  Nothing in a correct run
+ * makes such a wait run out.  While the drill is armed, every launch of the
+ * tensor-core kernels (index scoring, attention) skips arming the barrier its
+ * first wait needs: that wait runs out after 1 ms with no copy or MMA in
+ * flight, the kernel takes the give-up path, and the call's outputs are
+ * unspecified (status_dev carries DSA_DEV_TIMEOUT).  The setting is process
+ * wide and read when a call launches its kernels (a graph captured meanwhile
+ * keeps it).  Never arm it in production.  Returns DSA_OK, or
+ * DSA_ERR_INVALID_ARG for an unknown drill.
+ */
+#define DSA_DRILL_SKIP_ARM 1
+int dsa_set_failure_drill(int drill);
 
 /* Human-readable name of a DSA_* return code (static string). */
 const char* dsa_status_string(int status);

@@ -33,8 +33,7 @@ Sources, by page and section (the pages print no code and no worked values):
 * module glm5next_dsa, Constants, MASKED_ATTN_MAX_KEYS: dense masked attention
   is the attention oracle (here: dense softmax over exactly the selected rows).
 
-Readings where the pages are silent (each is listed in the design notes):
-LayerNorm uses the population variance and an explicit epsilon; ``ape`` is a
+Readings where the pages are silent: LayerNorm uses the population variance and an explicit epsilon; ``ape`` is a
 [kpool, D] fp32 bias added to the gate logits per slot and channel; the causal
 rule counts a pool when its last token is at or before the query position; the
 attention output stays in latent space with an explicit softmax scale; an empty

@@ -67,6 +67,7 @@ SIGNATURES = {
     "dsa_status_string": (ctypes.c_char_p, [c_int]),
     "dsa_version": (c_int, []),
     "dsa_kernel_launches": (ctypes.c_uint64, []),
+    "dsa_set_failure_drill": (c_int, [c_int]),
 }
 
 

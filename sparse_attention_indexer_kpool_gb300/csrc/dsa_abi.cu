@@ -146,6 +146,30 @@ std::atomic<unsigned long long>& launch_counter() {
   static std::atomic<unsigned long long> n{0};
   return n;
 }
+
+namespace {
+std::atomic<int> g_drill{0};
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];
+}  // namespace
+
+int failure_drill() { return g_drill.load(std::memory_order_relaxed); }
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return 152;
+  }
+  int n = g_sms[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    return 152;
+  }
+  g_sms[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
 }  // namespace dsa
 
 extern "C" {
@@ -153,6 +177,12 @@ extern "C" {
 int dsa_version(void) { return 10000; }
 
 uint64_t dsa_kernel_launches(void) { return dsa::launch_counter().load(); }
+
+int dsa_set_failure_drill(int drill) {
+  if (drill != 0 && drill != DSA_DRILL_SKIP_ARM) return DSA_ERR_INVALID_ARG;
+  dsa::g_drill.store(drill, std::memory_order_relaxed);
+  return DSA_OK;
+}
 
 const char* dsa_status_string(int status) {
   switch (status) {

@@ -16,8 +16,22 @@
 
 namespace dsa {
 
-constexpr int kNumSMs = 152;         // GB300: 2 dies x 76 SMs (launch-shape heuristics only)
 constexpr int kKpoolMax = DSA_KPOOL_MAX;
+
+// SMs of the current device (cudaDevAttrMultiProcessorCount, read once per
+// device), for launch shapes; 152, the GB300's count, when no device answers.
+int num_sms();
+
+// Bounded waits.  A wait on an mbarrier gives up after kWaitNs of the GPU's
+// global timer; the kernel then flags DSA_DEV_TIMEOUT, issues nothing more,
+// waits (bounded again) for the copies and MMAs it already issued and frees
+// its tensor memory before it returns.  Under a failure drill (tests only:
+// dsa_set_failure_drill) the tensor-core kernels skip arming the barrier of
+// their first wait, and every wait of those launches gives up after
+// kDrillWaitNs.
+constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s
+constexpr unsigned long long kDrillWaitNs = 1000000ull;  // 1 ms
+int failure_drill();  // the drill armed for the launches that follow (0: none)
 
 // ---------------------------------------------------------------- launches
 // Every kernel of the library is launched through launch_kernel, which counts
@@ -154,12 +168,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: gives up after `limit` polls and reports false.
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: gives up after about `limit_ns` nanoseconds and reports false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  uint32_t limit = (1u << 22)) {
-  for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
+                                                  unsigned long long limit_ns = kWaitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
 }
 // 1-D bulk copy global -> shared (TMA engine), completion counted on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes,

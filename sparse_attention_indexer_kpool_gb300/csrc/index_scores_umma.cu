@@ -169,9 +169,9 @@ __device__ __forceinline__ void epi_bar() {
 }
 // Bounded wait that also gives up at once after another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                              int32_t* status) {
+                                              int32_t* status, unsigned long long limit_ns) {
   if (*abort) return false;
-  if (mbar_wait_bounded(bar, parity)) return true;
+  if (mbar_wait_bounded(bar, parity, limit_ns)) return true;
   flag(status, DSA_DEV_TIMEOUT);
   *abort = 1;
   return false;
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                              const int32_t* __restrict__ cu_pool_cap,
                              const int32_t* __restrict__ q_seq, const int32_t* __restrict__ q_pos,
                              int Q, int B, int kpool, int P_ld, float* __restrict__ scores,
-                             uint32_t* __restrict__ hist, const EarlyStart es,
+                             uint32_t* __restrict__ hist, const EarlyStart es, int drill,
                              int32_t* status) {
   using C = Cfg<G>;
   using LY = Layout<G>;
@@ -211,6 +211,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   int* s_prefix = reinterpret_cast<int*>(sbase + LY::prefix(n_groups, early));
   volatile int* abort = &ctl.abort;
   const bool use_hist = G == 1 && hist != nullptr;
+  // a failure drill loads nothing and arms no barrier: the first waits run out
+  const unsigned long long wait_ns = drill ? kDrillWaitNs : kWaitNs;
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    return wait_or_abort(bar, parity, abort, status, wait_ns);
+  };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -310,7 +315,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
 
   if (warp == 0) {
     // ================= TMA producer =================
-    if (lane == 0) {
+    if (lane == 0 && drill == 0) {
       // decode reads every key once: keep the call's other data in L2 instead; in a
       // chunk every query group rereads every key tile, so there the keys stay
       const uint64_t keys_policy = G == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
@@ -323,7 +328,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         const long long seg_hi = min(t_hi, (long long)s_prefix[gi + 1]);
         const int slot = seg % C::kBSlots;
         if (((b_used >> slot) & 1) &&
-            !wait_or_abort(&ctl.bempty[slot], ((b_par >> slot) & 1) ^ 1, abort, status))
+            !wait(&ctl.bempty[slot], ((b_par >> slot) & 1) ^ 1))
           break;
         const long long base0 =
             gi < kBaseCache ? (long long)s_base[gi]
@@ -340,7 +345,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         b_used |= 1u << slot;
         for (; t < seg_hi; ++t) {
           if (((a_used >> stage) & 1) &&
-              !wait_or_abort(&ctl.empty[stage], ((a_par >> stage) & 1) ^ 1, abort, status))
+              !wait(&ctl.empty[stage], ((a_par >> stage) & 1) ^ 1))
             break;
           if (!waited && t - s_prefix[gi] >= s_safe[gi]) {
             pdl_wait();  // this tile may hold a pool the compress rewrites
@@ -374,15 +379,15 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         while (s_prefix[gi + 1] <= t) ++gi;
         const long long seg_hi = min(t_hi, (long long)s_prefix[gi + 1]);
         const int slot = seg % C::kBSlots;
-        if (!wait_or_abort(&ctl.bfull[slot], (seg / C::kBSlots) & 1, abort, status)) break;
+        if (!wait(&ctl.bfull[slot], (seg / C::kBSlots) & 1)) break;
         const uint32_t b_lo = smem_u32(sbase + LY::b + (size_t)slot * C::kBBytes);
         const uint32_t b_hi = b_lo + N * 128;
         for (; t < seg_hi; ++t, ++tc) {
           const int acc = (int)(tc & 1);
-          if (!wait_or_abort(&ctl.full[stage], (a_par >> stage) & 1, abort, status)) break;
+          if (!wait(&ctl.full[stage], (a_par >> stage) & 1)) break;
           a_par ^= 1u << stage;
           if (tc >= 2 &&  // the epilogue has drained this accumulator's previous tile
-              !wait_or_abort(&ctl.tempty[acc], (uint32_t)((tc >> 1) - 1) & 1, abort, status))
+              !wait(&ctl.tempty[acc], (uint32_t)((tc >> 1) - 1) & 1))
             break;
           tc_fence_after();
           const uint32_t a_lo = smem_u32(sbase + LY::a + (size_t)stage * kABytes);
@@ -459,7 +464,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         ncmax = max(ncmax, mq[u].n_cand);
       }
       const long long base = mq[0].base;  // every query of a group reads one sequence
-      const bool b_ok = wait_or_abort(&ctl.bfull[slot], (seg / C::kBSlots) & 1, abort, status);
+      const bool b_ok = wait(&ctl.bfull[slot], (seg / C::kBSlots) & 1);
       float* wq = s_w + slot * G * kH;
       // fold scale into the weights once per group: w * max(0, scale * dot) equals
       // (w * scale) * max(0, dot) for scale > 0 (up to rounding)
@@ -480,7 +485,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           pv = pool_valid[base + p];
           if (q_pos != nullptr) ps = pool_start[base + p];
         }
-        if (!b_ok || !wait_or_abort(&ctl.tfull[acc], (uint32_t)(tc >> 1) & 1, abort, status))
+        if (!b_ok || !wait(&ctl.tfull[acc], (uint32_t)(tc >> 1) & 1))
           continue;  // keep walking so that every warp meets the same barriers
         tc_fence_after();
         const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N);
@@ -620,7 +625,8 @@ int launch_g(const void* q, const float* weights, float scale, const void* pool_
   // A scoring CTA cannot share an SM with a CTA of the compress kernel still
   // running beside an early start (measured: those CTAs begin ~2 us late and
   // finish last), so a few busy SMs are left out of the grid.
-  const int grid = (busy_ctas > 0 && busy_ctas <= kNumSMs / 8) ? kNumSMs - busy_ctas : kNumSMs;
+  const int sms = num_sms();
+  const int grid = (busy_ctas > 0 && busy_ctas <= sms / 8) ? sms - busy_ctas : sms;
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kThreadsU, 1, 1);
   cfg.dynamicSmemBytes = smem;
@@ -630,7 +636,7 @@ int launch_g(const void* q, const float* weights, float scale, const void* pool_
   const cudaError_t e = launch_kernel(&cfg, index_scores_umma_kernel<G>, mk, mq, weights,
                                            scale, pool_start, pool_valid, n_pools, cu_pool_cap,
                                            q_seq, q_pos, Q, B, kpool, P_ld, scores, hist,
-                                           es, status);
+                                           es, failure_drill(), status);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

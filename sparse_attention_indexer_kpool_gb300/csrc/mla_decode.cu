@@ -537,7 +537,7 @@ bool fast_path(int Hm, int L, int dtype) { return dtype == DSA_BF16 && L == kL &
 // at most 64 splits (the merge keeps one weight per split on chip).
 void split_plan(int Q, int Hm, int W, int* n_split, int* rows_per_split) {
   const int n_hg = Hm / kHG;
-  int s = kNumSMs / (Q * n_hg);
+  int s = num_sms() / (Q * n_hg);
   const int max_s = (W + kNT - 1) / kNT;
   if (s > max_s) s = max_s;
   if (s > 64) s = 64;

@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                     const int32_t* __restrict__ token_ids, int B, int W, float sm_scale,
                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                     float* __restrict__ part_o, float* __restrict__ part_ml, int early,
-                    PagedKv pk, int32_t* status) {
+                    PagedKv pk, int drill, int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char* sb = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   MCtl& c = *reinterpret_cast<MCtl*>(sb + kOffCtl);
@@ -194,6 +194,9 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   const uint32_t kvb = smem_u32(sb + kOffKv), qb = smem_u32(sb + kOffQ);
   const uint32_t ptb = smem_u32(sb + kOffPt);
   constexpr uint32_t idesc_s = umma_idesc_bf16(kRows, kHh, false);
+  // a failure drill issues no MMA and arms no barrier: the first wait runs out
+  const bool issue = drill == 0;
+  const unsigned long long wait_ns = drill ? kDrillWaitNs : kWaitNs;
 
   // ---- 2. S^T = C q^T  (M = 128 rows, N = 32 heads, K = 512)
   if (kKv != kKvPagedE4M3) {
@@ -221,7 +224,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncthreads();
-      if (threadIdx.x == 0) {
+      if (threadIdx.x == 0 && issue) {
         tc_fence_after();
         const uint32_t tm = c.tmem_base;
 #pragma unroll
@@ -268,7 +271,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && issue) {
       tc_fence_after();
       const uint32_t tm = c.tmem_base;
 #pragma unroll
@@ -279,18 +282,17 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       }
     }
   }
-  if (threadIdx.x == 0) umma_commit(&c.s_ready);
+  if (threadIdx.x == 0 && issue) umma_commit(&c.s_ready);
   tc_fence_after();
   const uint32_t tmem = c.tmem_base;
-  bool ok = mbar_wait_bounded(&c.s_ready, 0);
-  if (!ok && lane == 0) flag(status, DSA_DEV_TIMEOUT);
+  const bool s_done = mbar_wait_bounded(&c.s_ready, 0, wait_ns);
   tc_fence_after();
 
   // ---- 3. softmax over the rows, per head (thread = row r, heads 16 hq .. 16 hq + 15)
   const int r = qw * 32 + lane;
   float z[16];
   tmem_ld16(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(hq * 16), z);
-  const bool row_ok = c.tok[r] >= 0 && ok;
+  const bool row_ok = c.tok[r] >= 0;
   const float rs = kKv == kKvPagedE4M3 ? c.rs[r] : 1.f;  // the row's E4M3 scale
   const float zs = kKv == kKvPagedE4M3 ? sm_scale * kLog2e * rs : sm_scale * kLog2e;
 #pragma unroll
@@ -302,107 +304,129 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     const float m = transpose_reduce16<true>(t, lane);
     if (lane < 16) c.red[hq][qw][lane] = m;
   }
-  __syncthreads();
-  if (threadIdx.x < kHh) {
-    const int h2 = threadIdx.x >> 4, l2 = threadIdx.x & 15;
-    c.m_fin[threadIdx.x] =
-        fmaxf(fmaxf(c.red[h2][0][l2], c.red[h2][1][l2]), fmaxf(c.red[h2][2][l2], c.red[h2][3][l2]));
-  }
-  __syncthreads();
-  float p[16];
+  // Every thread takes the same branch from here: the scores exist only if
+  // every thread saw them complete.  After a timeout nothing more is issued.
+  bool ok = __syncthreads_and(s_done) != 0;
+  uint64_t* pending = (!ok && issue) ? &c.s_ready : nullptr;  // issued, completion unseen
+  if (ok) {
+    if (threadIdx.x < kHh) {
+      const int h2 = threadIdx.x >> 4, l2 = threadIdx.x & 15;
+      c.m_fin[threadIdx.x] = fmaxf(fmaxf(c.red[h2][0][l2], c.red[h2][1][l2]),
+                                   fmaxf(c.red[h2][2][l2], c.red[h2][3][l2]));
+    }
+    __syncthreads();
+    float p[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int h = hq * 16 + i;
-    const float m = c.m_fin[h];
-    p[i] = (m == -INFINITY || z[i] == -INFINITY) ? 0.f : exp2f(z[i] - m);
-    *reinterpret_cast<__nv_bfloat16*>(sb + kOffPt + (r >> 6) * kPtBlock + h * 128 +
-                                      ((((r & 63) >> 3) ^ (h & 7)) << 4) + (r & 7) * 2) =
-        __float2bfloat16_rn(kKv == kKvPagedE4M3 ? p[i] * rs : p[i]);
-  }
-  {
-    const float l = transpose_reduce16<false>(p, lane);
-    if (lane < 16) c.red[hq][qw][lane] = l;
-  }
-  fence_proxy_async_smem();  // P^T is read by the tensor cores next
-  tc_fence_before();
-  __syncthreads();
-  if (threadIdx.x < kHh) {
-    const int h2 = threadIdx.x >> 4, l2 = threadIdx.x & 15;
-    c.l_fin[threadIdx.x] =
-        (c.red[h2][0][l2] + c.red[h2][1][l2]) + (c.red[h2][2][l2] + c.red[h2][3][l2]);
+    for (int i = 0; i < 16; ++i) {
+      const int h = hq * 16 + i;
+      const float m = c.m_fin[h];
+      p[i] = (m == -INFINITY || z[i] == -INFINITY) ? 0.f : exp2f(z[i] - m);
+      *reinterpret_cast<__nv_bfloat16*>(sb + kOffPt + (r >> 6) * kPtBlock + h * 128 +
+                                        ((((r & 63) >> 3) ^ (h & 7)) << 4) + (r & 7) * 2) =
+          __float2bfloat16_rn(kKv == kKvPagedE4M3 ? p[i] * rs : p[i]);
+    }
+    {
+      const float l = transpose_reduce16<false>(p, lane);
+      if (lane < 16) c.red[hq][qw][lane] = l;
+    }
+    fence_proxy_async_smem();  // P^T is read by the tensor cores next
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < kHh) {
+      const int h2 = threadIdx.x >> 4, l2 = threadIdx.x & 15;
+      c.l_fin[threadIdx.x] =
+          (c.red[h2][0][l2] + c.red[h2][1][l2]) + (c.red[h2][2][l2] + c.red[h2][3][l2]);
+    }
+
+    // ---- 4. O^T = C^T P^T  (M = 128 latent columns x 4 chunks, N = 32 heads, K = 128 rows)
+    if (threadIdx.x == 0) {
+      tc_fence_after();
+      constexpr uint32_t idesc = umma_idesc_bf16(128, kHh, true);
+#pragma unroll
+      for (int mc = 0; mc < 4; ++mc) {
+#pragma unroll
+        for (int kr = 0; kr < 8; ++kr) {
+          const uint64_t a = umma_desc_sw128(kvb + 2 * mc * kKvBlock + kr * 2048, kKvBlock, 1024);
+          const uint64_t bd = sw128_desc(ptb + (kr >> 2) * kPtBlock + (kr & 3) * 32);
+          umma_bf16(tmem + kHh + mc * kHh, a, bd, idesc, kr > 0 ? 1u : 0u);
+        }
+      }
+      umma_commit(&c.o_ready);
+    }
+    const bool o_done = mbar_wait_bounded(&c.o_ready, 0, wait_ns);
+    ok = __syncthreads_and(o_done) != 0;  // (this barrier also publishes l_fin)
+    if (!ok) pending = &c.o_ready;
+    tc_fence_after();
   }
 
-  // ---- 4. O^T = C^T P^T  (M = 128 latent columns x 4 chunks, N = 32 heads, K = 128 rows)
-  if (threadIdx.x == 0) {
-    tc_fence_after();
-    constexpr uint32_t idesc = umma_idesc_bf16(128, kHh, true);
+  if (ok) {
+    // ---- 5. epilogue.  Split partials: straight from TMEM (a warp's 32 lanes are
+    // 32 consecutive latent columns of one head, so each store is a 128-byte row
+    // piece).  A single split: staged through shared memory [head][latent] (the
+    // row tile is free now) and normalised into bf16 with 8-byte stores.
+    if (n_split > 1) {
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        const int mc = hq + 2 * cc;
+        const int col = mc * 128 + qw * 32 + lane;
+        float o[32];
+        tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHh + mc * kHh), o);
+        float* dst = part_o + (qh0 * n_split + split) * kL + col;
 #pragma unroll
-    for (int mc = 0; mc < 4; ++mc) {
+        for (int i = 0; i < 32; ++i) dst[(long long)i * n_split * kL] = o[i];
+      }
+      tc_fence_before();
+    }
+    float* stage = reinterpret_cast<float*>(sb + kOffKv);
+    if (n_split == 1) {
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        const int mc = hq + 2 * cc;
+        const int col = mc * 128 + qw * 32 + lane;
+        float o[32];
+        tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHh + mc * kHh), o);
 #pragma unroll
-      for (int kr = 0; kr < 8; ++kr) {
-        const uint64_t a = umma_desc_sw128(kvb + 2 * mc * kKvBlock + kr * 2048, kKvBlock, 1024);
-        const uint64_t bd = sw128_desc(ptb + (kr >> 2) * kPtBlock + (kr & 3) * 32);
-        umma_bf16(tmem + kHh + mc * kHh, a, bd, idesc, kr > 0 ? 1u : 0u);
+        for (int i = 0; i < 32; ++i) stage[i * kL + col] = o[i];
+      }
+      tc_fence_before();
+    }
+    __syncthreads();
+    for (int f = threadIdx.x; n_split == 1 && f < kHh * kL / 4; f += kThreadsM) {
+      const int h = f / (kL / 4), c4 = f % (kL / 4);
+      const float4 v = *reinterpret_cast<const float4*>(stage + h * kL + c4 * 4);
+      const float l = c.l_fin[h];
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      *reinterpret_cast<uint2*>(out + (qh0 + h) * kL + c4 * 4) =
+          make_uint2(pack_bf16(v.x * inv, v.y * inv), pack_bf16(v.z * inv, v.w * inv));
+    }
+    if (threadIdx.x < kHh) {
+      const int h = threadIdx.x;
+      const float m = c.m_fin[h], l = c.l_fin[h];
+      if (n_split == 1) {
+        if (lse) lse[qh0 + h] = l > 0.f ? (m + log2f(l)) / kLog2e : -INFINITY;
+      } else {
+        part_ml[((qh0 + h) * n_split + split) * 2] = m;
+        part_ml[((qh0 + h) * n_split + split) * 2 + 1] = l;
       }
     }
-    umma_commit(&c.o_ready);
-  }
-  __syncthreads();  // l_fin is complete
-  ok = mbar_wait_bounded(&c.o_ready, 0) && ok;
-  if (!ok && lane == 0) flag(status, DSA_DEV_TIMEOUT);
-  tc_fence_after();
-
-  // ---- 5. epilogue.  Split partials: straight from TMEM (a warp's 32 lanes are
-  // 32 consecutive latent columns of one head, so each store is a 128-byte row
-  // piece).  A single split: staged through shared memory [head][latent] (the
-  // row tile is free now) and normalised into bf16 with 8-byte stores.
-  if (n_split > 1) {
-#pragma unroll 1
-    for (int cc = 0; cc < 2; ++cc) {
-      const int mc = hq + 2 * cc;
-      const int col = mc * 128 + qw * 32 + lane;
-      float o[32];
-      tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHh + mc * kHh), o);
-      float* dst = part_o + (qh0 * n_split + split) * kL + col;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) dst[(long long)i * n_split * kL] = ok ? o[i] : 0.f;
-    }
-    tc_fence_before();
-  }
-  float* stage = reinterpret_cast<float*>(sb + kOffKv);
-  if (n_split == 1) {
-#pragma unroll 1
-    for (int cc = 0; cc < 2; ++cc) {
-      const int mc = hq + 2 * cc;
-      const int col = mc * 128 + qw * 32 + lane;
-      float o[32];
-      tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHh + mc * kHh), o);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) stage[i * kL + col] = ok ? o[i] : 0.f;
-    }
-    tc_fence_before();
-  }
-  __syncthreads();
-  for (int f = threadIdx.x; n_split == 1 && f < kHh * kL / 4; f += kThreadsM) {
-    const int h = f / (kL / 4), c4 = f % (kL / 4);
-    const float4 v = *reinterpret_cast<const float4*>(stage + h * kL + c4 * 4);
-    const float l = c.l_fin[h];
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    *reinterpret_cast<uint2*>(out + (qh0 + h) * kL + c4 * 4) =
-        make_uint2(pack_bf16(v.x * inv, v.y * inv), pack_bf16(v.z * inv, v.w * inv));
-  }
-  if (threadIdx.x < kHh) {
-    const int h = threadIdx.x;
-    const float m = c.m_fin[h], l = ok ? c.l_fin[h] : 0.f;
+  } else {
+    // Gave up: this CTA's share reads as "nothing selected" (a split with a
+    // zero sum is skipped by the merge).
+    if (threadIdx.x == 0) flag(status, DSA_DEV_TIMEOUT);
     if (n_split == 1) {
-      if (lse) lse[qh0 + h] = l > 0.f ? (m + log2f(l)) / kLog2e : -INFINITY;
-    } else {
-      part_ml[((qh0 + h) * n_split + split) * 2] = m;
-      part_ml[((qh0 + h) * n_split + split) * 2 + 1] = l;
+      for (int f = threadIdx.x; f < kHh * kL / 4; f += kThreadsM)
+        *reinterpret_cast<uint2*>(out + qh0 * kL + (long long)f * 4) = make_uint2(0u, 0u);
+      if (lse && threadIdx.x < kHh) lse[qh0 + threadIdx.x] = -INFINITY;
+    } else if (threadIdx.x < kHh) {
+      part_ml[((qh0 + threadIdx.x) * n_split + split) * 2] = -INFINITY;
+      part_ml[((qh0 + threadIdx.x) * n_split + split) * 2 + 1] = 0.f;
     }
   }
+  // TMEM is freed only after every MMA this CTA issued has retired (bounded).
+  if (threadIdx.x == 0 && pending != nullptr) mbar_wait_bounded(pending, 0);
+  tc_fence_before();
+  __syncthreads();
   if (warp == 1) {
-    __syncwarp();
     tc_fence_after();
     tmem_dealloc<kTmemCols>(tmem);
   }
@@ -468,7 +492,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                       int B, int W, int tiles_per_split, float sm_scale,
                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                       float* __restrict__ part_o, float* __restrict__ part_ml, PagedKv pk,
-                      int32_t* status) {
+                      int drill, int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char* sb = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   SCtl& c = *reinterpret_cast<SCtl*>(sb + kOffCtlS);
@@ -528,6 +552,11 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       kKv == kKvContig ? static_cast<const void*>(kv) : pk.pages);
   bool ok = true;
   int r = qw * 32 + lane;  // this thread's row of the tile in the softmax
+  // a failure drill issues no MMA and arms no barrier: the first wait runs out
+  const bool issue = drill == 0;
+  const unsigned long long wait_ns = drill ? kDrillWaitNs : kWaitNs;
+  uint64_t* pending = nullptr;  // MMAs issued whose completion was not seen
+  uint32_t pend_ph = 0;
 
   // the cache row of tile row `rr` (-1: none); flags bad ids and pages
   auto row_of = [&](int t, int rr, int* tok_out) -> int {
@@ -554,7 +583,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     return (int)prow;
   };
 
-  for (int t = t_lo; t < t_hi && ok; ++t) {
+  for (int t = t_lo; t < t_hi; ++t) {
     const uint32_t ph = (uint32_t)((t - t_lo) & 1);
     // ---- 1. this tile's rows; the next tile's rows go to L2 meanwhile
     if (threadIdx.x < kRows) {
@@ -634,7 +663,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     tc_fence_after();
 
     // ---- 2. S^T = C q^T  (M = 128 rows, N = 64 heads, K = 512)
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && issue) {
       constexpr uint32_t idesc = umma_idesc_bf16(kRows, kHs, false);
 #pragma unroll
       for (int kk = 0; kk < 32; ++kk) {
@@ -644,14 +673,13 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       }
       umma_commit(&c.s_ready);
     }
-    ok = mbar_wait_bounded(&c.s_ready, ph);
-    if (!ok && lane == 0) flag(status, DSA_DEV_TIMEOUT);
+    const bool s_done = mbar_wait_bounded(&c.s_ready, ph, wait_ns);
     tc_fence_after();
 
     // ---- 3. softmax against the running max (thread = row r, heads 32 hg ..)
     float z[32];
     tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(hg * 32), z);
-    const bool row_ok = c.tok[r] >= 0 && ok;
+    const bool row_ok = c.tok[r] >= 0;
     const float rsr = kKv == kKvPagedE4M3 ? c.rs[r] : 1.f;
     const float zs = kKv == kKvPagedE4M3 ? sm_scale * kLog2e * rsr : sm_scale * kLog2e;
 #pragma unroll
@@ -663,7 +691,16 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       c.red[qw][hg * 32 + lane] = transpose_reduce32<true>(tt, lane);
     }
     if (threadIdx.x == 0) c.rescale = 0;
-    __syncthreads();
+    // Every thread takes the same branch: the scores exist only if every thread
+    // saw them complete.  After a timeout nothing more is issued.
+    ok = __syncthreads_and(s_done) != 0;
+    if (!ok) {
+      if (issue) {
+        pending = &c.s_ready;
+        pend_ph = ph;
+      }
+      break;
+    }
     if (threadIdx.x < kHs) {
       const int h = threadIdx.x;
       const float tmax = fmaxf(fmaxf(c.red[0][h], c.red[1][h]), fmaxf(c.red[2][h], c.red[3][h]));
@@ -727,49 +764,70 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       }
       umma_commit(&c.o_ready);
     }
-    ok = mbar_wait_bounded(&c.o_ready, ph) && ok;  // the tiles are free again after this
-    if (!ok && lane == 0) flag(status, DSA_DEV_TIMEOUT);
+    const bool o_done = mbar_wait_bounded(&c.o_ready, ph, wait_ns);
     tc_fence_after();
-    __syncthreads();
+    ok = __syncthreads_and(o_done) != 0;  // the tiles are free again after this
+    if (!ok) {
+      pending = &c.o_ready;
+      pend_ph = ph;
+      break;
+    }
   }
 
   // ---- 5. epilogue: O^T -> shared [head][latent] fp32, then whole rows out
-  float* stage = reinterpret_cast<float*>(sb + kOffKvS);
-  const bool any = t_hi > t_lo;
+  if (ok) {
+    float* stage = reinterpret_cast<float*>(sb + kOffKvS);
+    const bool any = t_hi > t_lo;
 #pragma unroll 1
-  for (int mc = 0; mc < 4; ++mc) {
-    float o[32];
-    tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHs + mc * kHs + hg * 32), o);
-    const int col = mc * 128 + qw * 32 + lane;
+    for (int mc = 0; mc < 4; ++mc) {
+      float o[32];
+      tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHs + mc * kHs + hg * 32), o);
+      const int col = mc * 128 + qw * 32 + lane;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) stage[(hg * 32 + i) * kL + col] = (ok && any) ? o[i] : 0.f;
+      for (int i = 0; i < 32; ++i) stage[(hg * 32 + i) * kL + col] = any ? o[i] : 0.f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    for (int f = threadIdx.x; f < kHs * kL / 4; f += kThreadsM) {
+      const int h = f / (kL / 4), c4 = f % (kL / 4);
+      const float4 v = *reinterpret_cast<const float4*>(stage + h * kL + c4 * 4);
+      if (n_split == 1) {
+        const float l = c.l_run[h];
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        *reinterpret_cast<uint2*>(out + (qh0 + h) * kL + c4 * 4) =
+            make_uint2(pack_bf16(v.x * inv, v.y * inv), pack_bf16(v.z * inv, v.w * inv));
+      } else {
+        *reinterpret_cast<float4*>(part_o + ((qh0 + h) * n_split + split) * kL + c4 * 4) = v;
+      }
+    }
+    if (threadIdx.x < kHs) {
+      const int h = threadIdx.x;
+      const float m = c.m_run[h], l = any ? c.l_run[h] : 0.f;
+      if (n_split == 1) {
+        if (lse) lse[qh0 + h] = l > 0.f ? (m + log2f(l)) / kLog2e : -INFINITY;
+      } else {
+        part_ml[((qh0 + h) * n_split + split) * 2] = m;
+        part_ml[((qh0 + h) * n_split + split) * 2 + 1] = l;
+      }
+    }
+  } else {
+    // Gave up: this CTA's share reads as "nothing selected" (a split with a
+    // zero sum is skipped by the merge).
+    if (threadIdx.x == 0) flag(status, DSA_DEV_TIMEOUT);
+    if (n_split == 1) {
+      for (int f = threadIdx.x; f < kHs * kL / 4; f += kThreadsM)
+        *reinterpret_cast<uint2*>(out + qh0 * kL + (long long)f * 4) = make_uint2(0u, 0u);
+      if (lse && threadIdx.x < kHs) lse[qh0 + threadIdx.x] = -INFINITY;
+    } else if (threadIdx.x < kHs) {
+      part_ml[((qh0 + threadIdx.x) * n_split + split) * 2] = -INFINITY;
+      part_ml[((qh0 + threadIdx.x) * n_split + split) * 2 + 1] = 0.f;
+    }
   }
+  // TMEM is freed only after every MMA this CTA issued has retired (bounded).
+  if (threadIdx.x == 0 && pending != nullptr) mbar_wait_bounded(pending, pend_ph);
   tc_fence_before();
   __syncthreads();
-  for (int f = threadIdx.x; f < kHs * kL / 4; f += kThreadsM) {
-    const int h = f / (kL / 4), c4 = f % (kL / 4);
-    const float4 v = *reinterpret_cast<const float4*>(stage + h * kL + c4 * 4);
-    if (n_split == 1) {
-      const float l = c.l_run[h];
-      const float inv = (ok && l > 0.f) ? 1.f / l : 0.f;
-      *reinterpret_cast<uint2*>(out + (qh0 + h) * kL + c4 * 4) =
-          make_uint2(pack_bf16(v.x * inv, v.y * inv), pack_bf16(v.z * inv, v.w * inv));
-    } else {
-      *reinterpret_cast<float4*>(part_o + ((qh0 + h) * n_split + split) * kL + c4 * 4) = v;
-    }
-  }
-  if (threadIdx.x < kHs) {
-    const int h = threadIdx.x;
-    const float m = c.m_run[h], l = (ok && any) ? c.l_run[h] : 0.f;
-    if (n_split == 1) {
-      if (lse) lse[qh0 + h] = l > 0.f ? (m + log2f(l)) / kLog2e : -INFINITY;
-    } else {
-      part_ml[((qh0 + h) * n_split + split) * 2] = m;
-      part_ml[((qh0 + h) * n_split + split) * 2 + 1] = l;
-    }
-  }
   if (warp == 1) {
-    __syncwarp();
     tc_fence_after();
     tmem_dealloc<kTmemColsS>(tmem);
   }
@@ -783,7 +841,7 @@ int mla_umma_splits(int out_width) { return (out_width + kRows - 1) / kRows; }
 // adapt to Q.
 bool mla_umma_ok(int Q, int Hm, int L, int out_width, int dtype) {
   return mla_umma_shape_ok(Hm, L, dtype) &&
-         (long long)Q * mla_umma_splits(out_width) * (kHm / kHh) <= 4LL * kNumSMs;
+         (long long)Q * mla_umma_splits(out_width) * (kHm / kHh) <= 4LL * num_sms();
 }
 bool mla_umma_shape_ok(int Hm, int L, int dtype) {
   return dtype == DSA_BF16 && Hm == kHm && L == kL;
@@ -813,7 +871,7 @@ int launch_kind(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
   return launch_kernel(&cfg, mla_umma_kernel<kKv>, (const __nv_bfloat16*)q_lat,
                        (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, out_width,
                        sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml, early ? 1 : 0,
-                       pk, status_dev) == cudaSuccess
+                       pk, failure_drill(), status_dev) == cudaSuccess
              ? DSA_OK
              : DSA_ERR_CUDA;
 }
@@ -821,7 +879,8 @@ int launch_kind(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
 
 int mla_stream_splits(int Q, int out_width) {
   const int n_tiles = (out_width + kRows - 1) / kRows;
-  int s = Q >= kNumSMs ? 1 : kNumSMs / Q;  // CTAs within one wave
+  const int sms = num_sms();
+  int s = Q >= sms ? 1 : sms / Q;  // CTAs within one wave
   s = s < 1 ? 1 : (s > n_tiles ? n_tiles : s);
   const int per = (n_tiles + s - 1) / s;
   return (n_tiles + per - 1) / per;
@@ -855,7 +914,7 @@ int launch_stream_kind(const void* q_lat, const void* kv, const int32_t* cu_seql
   return launch_kernel(&cfg, mla_stream_kernel<kKv>, (const __nv_bfloat16*)q_lat,
                        (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, out_width,
                        per, sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml, pk,
-                       status_dev) == cudaSuccess
+                       failure_drill(), status_dev) == cudaSuccess
              ? DSA_OK
              : DSA_ERR_CUDA;
 }

@@ -17,9 +17,11 @@
 //    left in it: each call clears the part it uses before the scoring kernel
 //    runs, and calls that overlap on the GPU (different streams, no ordering
 //    between them) race on it and must not be issued;
-//  * the first call on each device looks up the array's device address
-//    (cudaGetSymbolAddress, with that device current); make that first call
-//    before any stream capture.
+//  * the first call on each device with at least one query looks up the
+//    array's device address (cudaGetSymbolAddress, with that device current),
+//    whatever its geometry; make that first call before any stream capture.
+//    The address is kept for the life of the process, which assumes the
+//    device's primary context lives as long (no cudaDeviceReset in between).
 #include <cmath>
 #include <mutex>
 
@@ -87,11 +89,14 @@ extern "C" int dsa_select_noalloc(const void* q, const float* weights, float sca
       (q_pos && !aligned(q_pos, 4)) || (status_dev && !aligned(status_dev, 4)))
     return DSA_ERR_MISALIGNED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the address is looked up on every device's first call, whatever the
+  // geometry, so that no later call does it inside a stream capture
+  uint32_t* scratch = nullptr;
+  int r = scratch_for_current_device(&scratch);
+  if (r != DSA_OK) return r;
   uint32_t* hist = nullptr;
-  int r;
   if (dsa::index_fills_histogram(Q, q_seq, H, D, dtype)) {
-    r = scratch_for_current_device(&hist);
-    if (r != DSA_OK) return r;
+    hist = scratch;
     // the histogram must start at zero: clear this call's share of the array
     if (cudaMemsetAsync(hist, 0, (size_t)Q * kHistBins * sizeof(uint32_t), st) != cudaSuccess)
       return DSA_ERR_CUDA;

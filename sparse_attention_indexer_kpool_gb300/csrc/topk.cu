@@ -601,7 +601,7 @@ int launch_select(const float* scores, int Q, int P_ld, int select_k, int32_t* p
   const size_t smem = SelLayout(select_k).total;
   if (smem > 227 * 1024) return DSA_ERR_UNSUPPORTED;
   int C = 1;
-  while (C < 16 && Q * C * 2 <= kNumSMs && (long long)P_ld >= (long long)C * 2 * 4096) C *= 2;
+  while (C < 16 && Q * C * 2 <= num_sms() && (long long)P_ld >= (long long)C * 2 * 4096) C *= 2;
   if (C == 16 && clusters16_resident(smem) < Q) C = 8;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -269,3 +269,12 @@ def dsa_decode_layer(k, gate, valid, ape, ln_gamma, ln_beta, ln_eps, cu_seqlens,
 def dsa_kernel_launches() -> int:
     """Kernels the library has launched (or recorded into a stream capture) so far."""
     return int(_lib.load().dsa_kernel_launches())
+
+
+DSA_DRILL_SKIP_ARM = 1
+
+
+def dsa_set_failure_drill(drill: int) -> None:
+    """Arm (DSA_DRILL_SKIP_ARM) or disarm (0) the give-up drill of the tensor-core
+    kernels, process wide (tests of failure detection only)."""
+    _check("dsa_set_failure_drill", _lib.load().dsa_set_failure_drill(int(drill)))

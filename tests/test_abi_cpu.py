@@ -115,6 +115,15 @@ def test_rejected_and_empty_calls_launch_nothing(lib):
     assert lib.dsa_kernel_launches() == n
 
 
+def test_failure_drill_setting(lib):
+    """The drill switch takes 0 and the one defined drill, and refuses others."""
+    drill = header_define("DSA_DRILL_SKIP_ARM")
+    assert lib.dsa_set_failure_drill(drill) == ERR["DSA_OK"]
+    assert lib.dsa_set_failure_drill(0) == ERR["DSA_OK"]
+    assert lib.dsa_set_failure_drill(7) == ERR["DSA_ERR_INVALID_ARG"]
+    assert lib.dsa_set_failure_drill(-1) == ERR["DSA_ERR_INVALID_ARG"]
+
+
 def test_expand_validation(lib):
     f = lib.dsa_expand_selection
     assert f(A, A, A, A, 2, 2, 8, 4, 31, A, None, None) == ERR["DSA_ERR_INVALID_ARG"]  # W < K*kp

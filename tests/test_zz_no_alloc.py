@@ -48,6 +48,22 @@ def test_noalloc_matches_select_on_two_calls_in_a_row():
         assert int(st.item()) == int(buf.status.item()) == 0, call
 
 
+def test_noalloc_matches_select_where_no_scratch_is_used():
+    """fp32 at a small geometry: the scoring kernel keeps no histogram, the
+    selection builds its own on chip, and the static array is not touched."""
+    for call, seed in enumerate((7, 8)):
+        bt = synth.tiny(device="cuda", seed=seed)
+        buf = pipeline.LayerBuffers.alloc(bt)
+        pipeline.compress(bt, buf)
+        pipeline.select(bt, buf)
+        scores, ids, tok, st = _noalloc(bt, buf)
+        torch.cuda.synchronize()
+        assert torch.equal(scores, buf.scores), call
+        assert torch.equal(ids, buf.pool_ids), call
+        assert torch.equal(tok, buf.token_ids), call
+        assert int(st.item()) == int(buf.status.item()) == 0, call
+
+
 def test_noalloc_refuses_more_queries_than_its_scratch():
     geo = Geometry(D=128, H=32, kpool=4, select_k=8, out_width=32, Hm=64, L=512, dtype="bf16")
     bt = synth.make_batch(geo, [64] * 65, [0] * 65, device="cuda", seed=3)
