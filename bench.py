@@ -304,7 +304,7 @@ def paged_attention(reps=20, page_size=64):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     pcs = {"paged_bf16": synth.paged_cache(bt.kv, bt.cu_seqlens, page_size, seed=5),
            "paged_e4m3": synth.paged_cache(bt.kv, bt.cu_seqlens, page_size, e4m3=True, seed=6)}
-    ws = torch.zeros(max(ops.mla_paged_workspace_bytes(bt.q_lat, bt.kv, W), 16),
+    ws = torch.empty(max(ops.mla_paged_workspace_bytes(bt.q_lat, bt.kv, W), 16),
                      dtype=torch.uint8, device="cuda")
     calls = {"contiguous_bf16": lambda: ops.dsa_mla_selected_decode(
         bt.q_lat, bt.kv, bt.cu_seqlens, bt.q_seq, buf.token_ids, bt.sm_scale, out, lse,

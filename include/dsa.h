@@ -224,11 +224,7 @@ int dsa_expand_selection(const int32_t* pool_ids, const int32_t* pool_start,
  *   q_lat [Q, Hm, L] activation dtype; kv_latent [sum T_b, L] activation dtype
  *   token_ids [Q, out_width] int32 (from dsa_expand_selection)
  *   out [Q, Hm, L] activation dtype; lse [Q, Hm] fp32 (may be NULL)
- *   workspace: dsa_mla_selected_decode_workspace_size(...) bytes, 16-byte
- *   aligned, ZERO-FILLED BEFORE ITS FIRST USE (it holds counters through which
- *   the CTAs of one call meet; every call leaves them re-armed, so a workspace
- *   is zeroed once at allocation and then reused).  Two calls in flight at the
- *   same time must not share a workspace.
+ *   workspace: dsa_mla_selected_decode_workspace_size(...) bytes, 16-byte aligned
  * Supported: L multiple of 8 up to 1024 and Hm up to 128 in both dtypes; bf16
  * with L = 512 and Hm a multiple of 16 runs on the tensor cores.
  * Device faults: DSA_DEV_BAD_TOKEN (token id >= T_b: row skipped), DSA_DEV_BAD_QSEQ.
@@ -257,8 +253,7 @@ size_t dsa_mla_selected_decode_workspace_size(int Q, int Hm, int L, int out_widt
  *   block_table [B, max_pages] int32: token t of sequence b is row
  *     t % page_size of page block_table[b * max_pages + t / page_size];
  *   seq_lens [B] int32: token ids at or past seq_lens[b] are flagged.
- * Every other argument, output and fault is that of dsa_mla_selected_decode,
- * the workspace rules included (zero-filled before its first use).
+ * Every other argument, output and fault is that of dsa_mla_selected_decode.
  * A token whose block is past the table or whose page is outside [0, n_pages)
  * is skipped and flagged DSA_DEV_BAD_PAGE.  The library reads the cache and
  * the table; it owns none of them.
@@ -346,8 +341,7 @@ int dsa_select_noalloc(const void* q, const float* weights, float scale, const v
  * enqueued before the call has finished writing them when it starts.
  *   ws_select: dsa_select_workspace_size(Q, P_ld, select_k) bytes, zero-filled
  *              before first use, left zeroed (as for dsa_select).
- *   ws_mla:    dsa_mla_selected_decode_workspace_size(Q, Hm, L, out_width, dtype)
- *              bytes, zero-filled before first use (as for dsa_mla_selected_decode).
+ *   ws_mla:    dsa_mla_selected_decode_workspace_size(Q, Hm, L, out_width, dtype).
  *   pool_begin may be NULL (every pool from 0; no early streaming).
  */
 typedef struct dsa_decode_layer_args {

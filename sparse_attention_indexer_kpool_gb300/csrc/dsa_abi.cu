@@ -74,23 +74,20 @@ int run_select(const void* q, const float* weights, float scale, const void* poo
                const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
                int select_k, int out_width, int dtype, float* scores, int32_t* pool_ids,
                int32_t* token_ids, void* workspace, int32_t* status_dev, cudaStream_t st,
-               dsa::EarlyStart early = {}, int busy_ctas = 0, bool ids_meet = false) {
+               dsa::EarlyStart early = {}, int busy_ctas = 0) {
   // Decode geometry: the scoring kernel also counts each query's score
-  // histogram into the workspace and the selection starts from it, as soon as
-  // the query's own scores are out (meeting counters in the workspace).
-  // Otherwise the selection kernel builds the histogram itself.
+  // histogram into the workspace and the selection starts from it.  Otherwise
+  // the selection kernel builds the histogram itself.
   const bool hist = dsa::index_fills_histogram(Q, q_seq, H, D, dtype);
-  unsigned long long* meets = hist ? dsa::select_workspace_meets(workspace, Q) : nullptr;
   int r = dsa::launch_index_scores(q, weights, scale, pool_keys, pool_rows, pool_start,
                                    pool_valid, n_pools, cu_pool_cap, q_seq, q_pos, Q, B, H, D,
                                    kpool, P_ld, dtype, scores,
-                                   hist ? dsa::topk_workspace_hist(workspace) : nullptr, meets,
+                                   hist ? dsa::topk_workspace_hist(workspace) : nullptr,
                                    status_dev, st, early, busy_ctas);
   if (r != DSA_OK) return r;
-  return dsa::launch_select_after_index(
-      scores, Q, P_ld, select_k, pool_ids, hist ? dsa::topk_workspace_hist(workspace) : nullptr,
-      meets, ids_meet && meets != nullptr, pool_start, cu_pool_cap, q_seq, B, kpool, out_width,
-      token_ids, status_dev, st);
+  return dsa::launch_select_after_index(scores, Q, P_ld, select_k, pool_ids,
+                                        hist ? workspace : nullptr, pool_start, cu_pool_cap,
+                                        q_seq, B, kpool, out_width, token_ids, status_dev, st);
 }
 
 int check_mla(const void* q_lat, const void* kv_latent, const int32_t* cu_seqlens,
@@ -237,7 +234,7 @@ int dsa_index_scores(const void* q, const float* weights, float scale, const voi
   if (Q > 65535) return DSA_ERR_UNSUPPORTED;
   return dsa::launch_index_scores(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid,
                                   n_pools, cu_pool_cap, q_seq, q_pos, Q, B, H, D, kpool, P_ld,
-                                  dtype, scores, nullptr, nullptr, status_dev, as_stream(stream));
+                                  dtype, scores, nullptr, status_dev, as_stream(stream));
 }
 
 size_t dsa_topk_pools_workspace_size(int Q, int P_ld, int select_k) {
@@ -382,26 +379,20 @@ int dsa_decode_layer(const dsa_decode_layer_args* a, void* stream) {
   if (rs == kNoWork) return DSA_OK;  // no queries: nothing to select or attend
   // Inside this call the scoring kernel may stream the key tiles below
   // pool_begin[b] before the compress ends (it does not write them); with no
-  // pool_begin the compress rewrites every pool.  With the decode geometry the
-  // top-k publishes each query's ids on the select workspace's counters and the
-  // one-tile attention of that query starts on them.
-  const bool ids_meet =
-      dsa::index_fills_histogram(a->Q, a->q_seq, a->H, a->D, a->dtype) &&
-      dsa::mla_umma_ok(a->Q, a->Hm, a->L, a->out_width, a->dtype);
+  // pool_begin the compress rewrites every pool.
   r = run_select(a->q, a->weights, a->scale, a->pool_keys, a->pool_rows, a->pool_start,
                  a->pool_valid, a->n_pools, a->cu_pool_cap, a->q_seq, a->q_pos, a->Q, a->B, a->H,
                  a->D, a->kpool, a->P_ld, a->select_k, a->out_width, a->dtype, a->scores,
                  a->pool_ids, a->token_ids, a->ws_select, a->status_dev, st,
                  rc == DSA_OK ? dsa::EarlyStart{a->pool_begin, a->valid, a->cu_seqlens}
                               : dsa::EarlyStart{},
-                 rc == DSA_OK ? dsa::kpool_compress_ctas(a->B, a->max_pools) : 0, ids_meet);
+                 rc == DSA_OK ? dsa::kpool_compress_ctas(a->B, a->max_pools) : 0);
   if (r != DSA_OK) return r;
   // the attention's inputs other than the token ids predate this call
-  return dsa::launch_mla_selected_decode(
-      a->q_lat, a->kv_latent, a->cu_seqlens, a->q_seq, a->token_ids, a->Q, a->B, a->Hm, a->L,
-      a->out_width, a->sm_scale, a->dtype, a->out, a->lse, a->ws_mla, a->ws_mla_bytes,
-      a->status_dev, st, true,
-      ids_meet ? dsa::select_workspace_meets(a->ws_select, a->Q) : nullptr);
+  return dsa::launch_mla_selected_decode(a->q_lat, a->kv_latent, a->cu_seqlens, a->q_seq,
+                                         a->token_ids, a->Q, a->B, a->Hm, a->L, a->out_width,
+                                         a->sm_scale, a->dtype, a->out, a->lse, a->ws_mla,
+                                         a->ws_mla_bytes, a->status_dev, st, true);
 }
 
 }  // extern "C"

@@ -185,82 +185,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     if (global_ns() - t0 > limit_ns) return false;
   }
 }
-// ---------------------------------------------------------------- meetings in global memory
-// Kernels and CTAs that hand work to each other inside one call meet through
-// 64-bit counters in a workspace that only grow.  A meeting is worth 2^20:
-// party s of n adds its share w_s = floor((s+1) 2^20 / n) - floor(s 2^20 / n),
-// so a complete meeting adds exactly 2^20 whatever n is, and counters that
-// start at zero (a zero-filled workspace) stay multiples of 2^20 between
-// calls.  Nothing is ever reset.
-//  * A group of CTAs of one grid (all resident at once) meets on one counter:
-//    each adds its share and waits for the next multiple of 2^20 above the
-//    value it found (group_meet).
-//  * A producer kernel hands to a consumer kernel of the same call through a
-//    pair: the producers add their shares to `done` once their outputs are
-//    stored; a consumer takes base = `used` rounded down to a multiple of 2^20
-//    (the consumers of this call add to `used` only when they have finished,
-//    and together add less than 2^20 until the last one has), waits for
-//    `done` >= base + 2^20, and adds its own share to `used` when it no longer
-//    reads the producers' outputs.  A consumer that is one thread-block
-//    cluster instead checks that the pair rests equal on a multiple of 2^20
-//    before it waits (else the workspace was not zero-filled: it waits for the
-//    whole producer kernel) and, once every CTA of the cluster has read the
-//    pair, sets both to `done` rounded up to a multiple of 2^20.
-constexpr int kMeetShift = 20;
-constexpr unsigned long long kMeetUnit = 1ull << kMeetShift;
-
-__device__ __forceinline__ unsigned long long meet_share(int s, int n) {
-  return ((unsigned long long)(s + 1) << kMeetShift) / (unsigned long long)n -
-         ((unsigned long long)s << kMeetShift) / (unsigned long long)n;
-}
-// parts [a, b) of n equal parts of 2^shift (0 <= a <= b <= n); the parts of
-// any cover of [0, n) sum to exactly 2^shift
-__device__ __forceinline__ unsigned long long meet_part(long long a, long long b, long long n,
-                                                        int shift) {
-  return ((unsigned long long)b << shift) / (unsigned long long)n -
-         ((unsigned long long)a << shift) / (unsigned long long)n;
-}
-// add w with release semantics: every store of this thread, and of its CTA
-// before a barrier it took after fencing them, is visible to whoever sees it
-__device__ __forceinline__ void meet_add(unsigned long long* c, unsigned long long w) {
-  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(c), "l"(w) : "memory");
-}
-__device__ __forceinline__ unsigned long long meet_load(const unsigned long long* c) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(c) : "memory");
-  return v;
-}
-__device__ __forceinline__ unsigned long long meet_base(const unsigned long long* used) {
-  return (meet_load(used) >> kMeetShift) << kMeetShift;
-}
-// Bounded wait until *c >= target (acquire); false when the limit ran out.
-__device__ __forceinline__ bool meet_wait(const unsigned long long* c, unsigned long long target,
-                                          unsigned long long limit_ns) {
-  if ((long long)(meet_load(c) - target) >= 0) return true;
-  const unsigned long long t0 = global_ns();
-  for (;;) {
-#pragma unroll 1
-    for (int i = 0; i < 16; ++i)
-      if ((long long)(meet_load(c) - target) >= 0) return true;
-    if (global_ns() - t0 > limit_ns) return false;
-  }
-}
-// Party s of a group of n CTAs meeting on *cnt: called by one thread after a
-// barrier of its CTA (every thread fenced its stores before that barrier).
-// Returns false when the bounded wait ran out.
-__device__ __forceinline__ bool group_meet(unsigned long long* cnt, int s, int n,
-                                           unsigned long long limit_ns) {
-  const unsigned long long w = meet_share(s, n);
-  unsigned long long old;
-  asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], %2;"
-               : "=l"(old)
-               : "l"(cnt), "l"(w)
-               : "memory");
-  const unsigned long long target = ((old >> kMeetShift) + 1) << kMeetShift;
-  if ((long long)(old + w - target) >= 0) return true;  // the last share
-  return meet_wait(cnt, target, limit_ns);
-}
-
 // 1-D bulk copy global -> shared (TMA engine), completion counted on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes,
                                          uint64_t* bar) {
@@ -314,9 +238,8 @@ int launch_index_scores(const void* q, const float* weights, float scale, const 
                         int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
                         const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
                         const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
-                        int dtype, float* scores, uint32_t* score_hist,
-                        unsigned long long* meets, int32_t* status_dev, cudaStream_t stream,
-                        EarlyStart early = {}, int busy_ctas = 0);
+                        int dtype, float* scores, uint32_t* score_hist, int32_t* status_dev,
+                        cudaStream_t stream, EarlyStart early = {}, int busy_ctas = 0);
 // tcgen05 index kernel: queries per key tile (1 or 8), 0 when Q does not fit it
 int umma_index_group(int Q, const int32_t* q_seq);
 int launch_index_scores_umma(const void* q, const float* weights, float scale,
@@ -324,9 +247,8 @@ int launch_index_scores_umma(const void* q, const float* weights, float scale,
                              const uint8_t* pool_valid, const int32_t* n_pools,
                              const int32_t* cu_pool_cap, const int32_t* q_seq,
                              const int32_t* q_pos, int Q, int B, int kpool, int P_ld,
-                             float* scores, uint32_t* hist, unsigned long long* meets,
-                             EarlyStart early, int32_t* status_dev, cudaStream_t stream,
-                             int busy_ctas = 0);
+                             float* scores, uint32_t* hist, EarlyStart early,
+                             int32_t* status_dev, cudaStream_t stream, int busy_ctas = 0);
 // whether the decode kernel can start streaming before the compress of its call ends
 bool umma_index_early_ok(int Q, const int32_t* q_seq, const int32_t* q_pos);
 // true when launch_index_scores also counts the per-query score histogram
@@ -334,14 +256,8 @@ bool index_fills_histogram(int Q, const int32_t* q_seq, int H, int D, int dtype)
 size_t topk_workspace_size(int Q, int P_ld, int select_k);
 size_t select_workspace_size(int Q, int P_ld, int select_k);
 uint32_t* topk_workspace_hist(void* workspace);
-// the fused select workspace's meeting counters: four per query (topk.cu)
-unsigned long long* select_workspace_meets(void* workspace, int Q);
-// hist: the scoring kernel's histograms (NULL: the top-k builds its own);
-// meets: the per-query meeting counters (NULL: wait for the whole previous
-// kernel); ids_meet: publish each query's ids on its counters for the attention
 int launch_select_after_index(const float* scores, int Q, int P_ld, int select_k,
-                              int32_t* pool_ids, uint32_t* hist, unsigned long long* meets,
-                              bool ids_meet, const int32_t* pool_start,
+                              int32_t* pool_ids, void* workspace, const int32_t* pool_start,
                               const int32_t* cu_pool_cap, const int32_t* q_seq, int B, int kpool,
                               int out_width, int32_t* token_ids, int32_t* status_dev,
                               cudaStream_t stream);
@@ -365,16 +281,12 @@ struct PagedKv {
 bool mla_umma_ok(int Q, int Hm, int L, int out_width, int dtype);
 bool mla_umma_shape_ok(int Hm, int L, int dtype);  // the geometry alone, any number of queries
 int mla_umma_splits(int out_width);
-// paged: NULL for the contiguous cache (kv + cu_seqlens).  sync: NULL, or the
-// workspace's group counters when the splits are merged inside the kernel
+// paged: NULL for the contiguous cache (kv + cu_seqlens)
 int launch_mla_umma(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
                     const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int out_width,
                     float sm_scale, void* out, float* lse, float* part_o, float* part_ml,
-                    uint32_t* sync, unsigned long long* ids_meets, bool early,
-                    int32_t* status_dev, cudaStream_t stream, const PagedKv* paged = nullptr);
-// whether the one-tile kernel merges its splits itself (every CTA resident at
-// once) instead of leaving them to the merge kernel
-bool mla_umma_merges_in_kernel(int Q, int out_width);
+                    bool early, int32_t* status_dev, cudaStream_t stream,
+                    const PagedKv* paged = nullptr);
 // streaming tcgen05 attention (same geometry, many queries): one CTA per query
 // and range of 128-row tiles, all 64 heads, online softmax; splits of the tiles
 int mla_stream_splits(int Q, int out_width);
@@ -390,16 +302,12 @@ int launch_mla_paged_decode(const void* q_lat, const PagedKv& kv, const int32_t*
                             float sm_scale, int dtype, void* out, float* lse, void* workspace,
                             size_t ws_bytes, int32_t* status_dev, cudaStream_t stream);
 // early: the caller guarantees that only the token ids come from kernels still in
-// flight (the attention of a fused decode call), so the rest is read before the
-// wait.  ids_meets (early only): the fused select workspace's meeting counters,
-// on which the top-k publishes each query's ids (then the attention of a query
-// starts as soon as its own ids are out)
+// flight (the attention of a fused decode call), so the rest is read before the wait
 int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
                                const int32_t* q_seq, const int32_t* token_ids, int Q, int B,
                                int Hm, int L, int out_width, float sm_scale, int dtype, void* out,
                                float* lse, void* workspace, size_t ws_bytes, int32_t* status_dev,
-                               cudaStream_t stream, bool early = false,
-                               unsigned long long* ids_meets = nullptr);
+                               cudaStream_t stream, bool early = false);
 }  // namespace dsa
 
 #define DSA_LAUNCH_CHECK()                          \

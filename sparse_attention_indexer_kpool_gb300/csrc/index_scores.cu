@@ -108,13 +108,12 @@ int launch_index_scores(const void* q, const float* weights, float scale, const 
                         int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
                         const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
                         const int32_t* q_pos, int Q, int B, int H, int D, int kpool, int P_ld,
-                        int dtype, float* scores, uint32_t* score_hist,
-                        unsigned long long* meets, int32_t* status_dev, cudaStream_t stream,
-                        EarlyStart early, int busy_ctas) {
+                        int dtype, float* scores, uint32_t* score_hist, int32_t* status_dev,
+                        cudaStream_t stream, EarlyStart early, int busy_ctas) {
   if (index_uses_tensor_cores(H, D, dtype) && umma_index_group(Q, q_seq) != 0)
     return launch_index_scores_umma(q, weights, scale, pool_keys, pool_rows, pool_start,
                                     pool_valid, n_pools, cu_pool_cap, q_seq, q_pos, Q, B, kpool,
-                                    P_ld, scores, score_hist, meets, early, status_dev, stream,
+                                    P_ld, scores, score_hist, early, status_dev, stream,
                                     busy_ctas);
   // the SIMT kernel fills no histogram; callers ask index_fills_histogram first
   cudaLaunchAttribute attr = pdl_attr();

@@ -188,9 +188,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                              const int32_t* __restrict__ cu_pool_cap,
                              const int32_t* __restrict__ q_seq, const int32_t* __restrict__ q_pos,
                              int Q, int B, int kpool, int P_ld, float* __restrict__ scores,
-                             uint32_t* __restrict__ hist,
-                             unsigned long long* __restrict__ meets, const EarlyStart es,
-                             int drill, int32_t* status) {
+                             uint32_t* __restrict__ hist, const EarlyStart es, int drill,
+                             int32_t* status) {
   using C = Cfg<G>;
   using LY = Layout<G>;
   constexpr int N = C::N;
@@ -446,7 +445,6 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     long long tc = 0;
     for (long long t = t_lo; t < t_hi; ++seg) {
       while (s_prefix[gi + 1] <= t) ++gi;
-      const long long seg_lo = t;
       const long long seg_hi = min(t_hi, (long long)s_prefix[gi + 1]);
       const int slot = seg % C::kBSlots;
       int np_known = -1;
@@ -530,14 +528,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             s_hist[i] = 0;
           }
         }
-        if (meets) __threadfence();  // this thread's scores and counts, before the share
         epi_bar();
-        if (meets && ew == 0 && lane == 0) {
-          // the tiles of this segment: their part of the half of the query's
-          // meeting that its tiles carry (the row's tail fill carries the other)
-          const long long q0 = s_prefix[gi], nq = s_prefix[gi + 1] - q0;
-          meet_add(meets + 4 * gi, meet_part(seg_lo - q0, seg_hi - q0, nq, kMeetShift - 1));
-        }
       }
     }
     if (early) {
@@ -571,22 +562,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       }
     }
   }
-  if (meets) __threadfence();  // the fill's stores, before the shares below
   tc_fence_before();
   __syncthreads();
-  if (meets) {
-    // The tail fill carries the other half of each query's meeting (all of it
-    // for a query with no tiles): the CTA that filled the whole row adds it, or
-    // with every CTA filling a part of every row, each adds its part.
-    for (int qi = threadIdx.x; qi < Q; qi += kThreadsU) {
-      const int shift = s_prefix[qi + 1] > s_prefix[qi] ? kMeetShift - 1 : kMeetShift;
-      if (n_groups >= (int)gridDim.x) {
-        if (qi % (int)gridDim.x == (int)blockIdx.x) meet_add(meets + 4 * qi, 1ull << shift);
-      } else {
-        meet_add(meets + 4 * qi, meet_part(blockIdx.x, blockIdx.x + 1, gridDim.x, shift));
-      }
-    }
-  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -629,8 +606,8 @@ int launch_g(const void* q, const float* weights, float scale, const void* pool_
              int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
              const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,
              const int32_t* q_pos, int Q, int B, int kpool, int P_ld, float* scores,
-             uint32_t* hist, unsigned long long* meets, const EarlyStart& es, int32_t* status,
-             cudaStream_t stream, int busy_ctas) {
+             uint32_t* hist, const EarlyStart& es, int32_t* status, cudaStream_t stream,
+             int busy_ctas) {
   const size_t smem = Layout<G>::bytes((Q + G - 1) / G, es.pool_begin != nullptr);
   if (smem > (size_t)kSmemMax) return DSA_ERR_UNSUPPORTED;
   CUtensorMap mk, mq;
@@ -659,7 +636,7 @@ int launch_g(const void* q, const float* weights, float scale, const void* pool_
   const cudaError_t e = launch_kernel(&cfg, index_scores_umma_kernel<G>, mk, mq, weights,
                                            scale, pool_start, pool_valid, n_pools, cu_pool_cap,
                                            q_seq, q_pos, Q, B, kpool, P_ld, scores, hist,
-                                           meets, es, failure_drill(), status);
+                                           es, failure_drill(), status);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -682,21 +659,19 @@ int launch_index_scores_umma(const void* q, const float* weights, float scale,
                              const uint8_t* pool_valid, const int32_t* n_pools,
                              const int32_t* cu_pool_cap, const int32_t* q_seq,
                              const int32_t* q_pos, int Q, int B, int kpool, int P_ld,
-                             float* scores, uint32_t* hist, unsigned long long* meets,
-                             EarlyStart es, int32_t* status_dev, cudaStream_t stream,
-                             int busy_ctas) {
+                             float* scores, uint32_t* hist, EarlyStart es,
+                             int32_t* status_dev, cudaStream_t stream, int busy_ctas) {
   const int G = umma_index_group(Q, q_seq);
   if (G == 8)
     return launch_g<8>(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid, n_pools,
-                       cu_pool_cap, q_seq, q_pos, Q, B, kpool, P_ld, scores, nullptr, nullptr,
+                       cu_pool_cap, q_seq, q_pos, Q, B, kpool, P_ld, scores, nullptr,
                        EarlyStart{}, status_dev, stream, 0);
   if (G == 1) {
     const bool early = es.pool_begin != nullptr && es.valid != nullptr &&
                        es.cu_seqlens != nullptr && umma_index_early_ok(Q, q_seq, q_pos);
     return launch_g<1>(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid, n_pools,
                        cu_pool_cap, q_seq, q_pos, Q, B, kpool, P_ld, scores, hist,
-                       hist ? meets : nullptr, early ? es : EarlyStart{}, status_dev, stream,
-                       early ? busy_ctas : 0);
+                       early ? es : EarlyStart{}, status_dev, stream, early ? busy_ctas : 0);
   }
   return DSA_ERR_UNSUPPORTED;
 }

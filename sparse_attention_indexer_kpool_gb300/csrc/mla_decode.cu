@@ -23,7 +23,6 @@
 #include <math.h>
 
 #include "dsa_internal.cuh"
-#include "mla_merge.cuh"
 
 namespace dsa {
 namespace {
@@ -301,12 +300,55 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merge split partials: one CTA per (query, head); 128 threads x 4 latent columns.
+// Every split's partial row and (max, sum) pair of a batch is requested before
+// any of them is used, and the batch maximum rescales the running sums, so up to
+// kMergeMax splits cost a single round trip to memory.
+constexpr int kMergeMax = 16;   // splits held in registers per batch
 __global__ void __launch_bounds__(128)
     mla_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int Hm,
                      int n_split, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
   pdl_wait();
   const long long qh = (long long)blockIdx.y * Hm + blockIdx.x;
-  merge_partials<kL>(part_o, part_ml, qh, n_split, threadIdx.x * 4, out, lse, threadIdx.x == 0);
+  const float* ml = part_ml + qh * n_split * 2;
+  const int d = threadIdx.x * 4;
+  float mx = -INFINITY, den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < n_split; s0 += kMergeMax) {
+    float4 v[kMergeMax];
+    float mm[kMergeMax], ll[kMergeMax];
+#pragma unroll
+    for (int u = 0; u < kMergeMax; ++u) {
+      const int sp = s0 + u;
+      ll[u] = 0.f;
+      mm[u] = -INFINITY;
+      if (sp < n_split) {
+        v[u] = __ldg(reinterpret_cast<const float4*>(part_o + (qh * n_split + sp) * kL + d));
+        mm[u] = __ldg(ml + 2 * sp);
+        ll[u] = __ldg(ml + 2 * sp + 1);
+      }
+    }
+    float bm = mx;
+#pragma unroll
+    for (int u = 0; u < kMergeMax; ++u)
+      if (ll[u] > 0.f) bm = fmaxf(bm, mm[u]);
+    if (bm == -INFINITY) continue;  // nothing selected so far
+    const float r = mx == -INFINITY ? 0.f : exp2f(mx - bm);
+    den *= r;
+    acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
+    mx = bm;
+#pragma unroll
+    for (int u = 0; u < kMergeMax; ++u) {
+      if (ll[u] > 0.f) {
+        const float w = exp2f(mm[u] - mx);
+        den += ll[u] * w;
+        acc.x += w * v[u].x; acc.y += w * v[u].y; acc.z += w * v[u].z; acc.w += w * v[u].w;
+      }
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  *reinterpret_cast<uint2*>(out + qh * kL + d) =
+      make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+  if (lse && threadIdx.x == 0) lse[qh] = den > 0.f ? (mx + log2f(den)) / kLog2e : -INFINITY;
 }
 
 // Generic SIMT kernel: one CTA per (head, query); two passes over the rows.
@@ -507,44 +549,26 @@ void split_plan(int Q, int Hm, int W, int* n_split, int* rows_per_split) {
 
 }  // namespace
 
-namespace {
-// Split workspace: fp32 partial outputs [Q, Hm, S, L], then their (max, sum)
-// pairs [Q, Hm, S, 2]; for the one-tile kernel, 256-byte aligned after them, a
-// 64-bit meeting counter per (query, head half) group (sync_bytes).
-size_t partial_bytes(int Q, int Hm, int L, int n_split) {
-  const size_t slots = (size_t)Q * Hm * n_split;
-  return slots * L * 4 + slots * 2 * 4;
-}
-size_t sync_offset(int Q, int Hm, int L, int n_split) {
-  return (partial_bytes(Q, Hm, L, n_split) + 255) & ~size_t(255);
-}
-size_t sync_bytes(int Q) { return (size_t)Q * 2 * 2 * sizeof(uint32_t); }
-uint32_t* sync_words(void* ws, int Q, int Hm, int L, int n_split) {
-  return reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(ws) +
-                                     sync_offset(Q, Hm, L, n_split));
-}
-}  // namespace
-
 size_t mla_workspace_size(int Q, int Hm, int L, int out_width, int dtype) {
-  if (mla_umma_ok(Q, Hm, L, out_width, dtype)) {
-    const int n_split = mla_umma_splits(out_width);
-    return n_split == 1 ? 0 : sync_offset(Q, Hm, L, n_split) + sync_bytes(Q);
-  }
   int n_split = 1;
-  if (mla_umma_shape_ok(Hm, L, dtype)) {
+  if (mla_umma_ok(Q, Hm, L, out_width, dtype)) {
+    n_split = mla_umma_splits(out_width);
+  } else if (mla_umma_shape_ok(Hm, L, dtype)) {
     n_split = mla_stream_splits(Q, out_width);
   } else if (fast_path(Hm, L, dtype)) {
     int rows;
     split_plan(Q, Hm, out_width, &n_split, &rows);
   }
-  return n_split == 1 ? 0 : partial_bytes(Q, Hm, L, n_split);
+  if (n_split == 1) return 0;
+  const size_t slots = (size_t)Q * Hm * n_split;
+  return slots * L * 4 + slots * 2 * 4;
 }
 
 int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
                                const int32_t* q_seq, const int32_t* token_ids, int Q, int B,
                                int Hm, int L, int out_width, float sm_scale, int dtype, void* out,
                                float* lse, void* workspace, size_t ws_bytes, int32_t* status_dev,
-                               cudaStream_t stream, bool early, unsigned long long* ids_meets) {
+                               cudaStream_t stream, bool early) {
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr.val.programmaticStreamSerializationAllowed = 1;
@@ -558,13 +582,10 @@ int launch_mla_selected_decode(const void* q_lat, const void* kv, const int32_t*
       return DSA_ERR_WORKSPACE;
     float* part_o = n_split > 1 ? static_cast<float*>(workspace) : nullptr;
     float* part_ml = part_o ? part_o + (size_t)Q * Hm * n_split * L : nullptr;
-    uint32_t* sync = mla_umma_merges_in_kernel(Q, out_width)
-                         ? sync_words(workspace, Q, Hm, L, n_split)
-                         : nullptr;
     const int r = launch_mla_umma(q_lat, kv, cu_seqlens, q_seq, token_ids, Q, B, out_width,
-                                  sm_scale, out, lse, part_o, part_ml, sync, ids_meets, early,
-                                  status_dev, stream);
-    if (r != DSA_OK || n_split == 1 || sync) return r;
+                                  sm_scale, out, lse, part_o, part_ml, early, status_dev,
+                                  stream);
+    if (r != DSA_OK || n_split == 1) return r;
     cfg.gridDim = dim3(Hm, Q, 1);
     cfg.blockDim = dim3(128, 1, 1);
     cfg.dynamicSmemBytes = 0;
@@ -651,12 +672,11 @@ bool paged_umma(int Q, int Hm, int L, int out_width, int dtype, int kv_dtype) {
 
 size_t mla_paged_workspace_size(int Q, int Hm, int L, int out_width, int dtype, int kv_dtype) {
   if (!paged_umma(Q, Hm, L, out_width, dtype, kv_dtype)) return 0;
-  if (mla_umma_ok(Q, Hm, L, out_width, dtype)) {
-    const int n_split = mla_umma_splits(out_width);
-    return n_split == 1 ? 0 : sync_offset(Q, Hm, L, n_split) + sync_bytes(Q);
-  }
-  const int n_split = mla_stream_splits(Q, out_width);
-  return n_split == 1 ? 0 : partial_bytes(Q, Hm, L, n_split);
+  const int n_split = mla_umma_ok(Q, Hm, L, out_width, dtype) ? mla_umma_splits(out_width)
+                                                              : mla_stream_splits(Q, out_width);
+  if (n_split == 1) return 0;
+  const size_t slots = (size_t)Q * Hm * n_split;
+  return slots * L * 4 + slots * 2 * 4;
 }
 
 int launch_mla_paged_decode(const void* q_lat, const PagedKv& kv, const int32_t* q_seq,
@@ -678,16 +698,13 @@ int launch_mla_paged_decode(const void* q_lat, const PagedKv& kv, const int32_t*
       return DSA_ERR_WORKSPACE;
     float* part_o = n_split > 1 ? static_cast<float*>(workspace) : nullptr;
     float* part_ml = part_o ? part_o + (size_t)Q * Hm * n_split * L : nullptr;
-    uint32_t* sync = few && mla_umma_merges_in_kernel(Q, out_width)
-                         ? sync_words(workspace, Q, Hm, L, n_split)
-                         : nullptr;
     const int r = few ? launch_mla_umma(q_lat, nullptr, nullptr, q_seq, token_ids, Q, B,
-                                        out_width, sm_scale, out, lse, part_o, part_ml, sync,
-                                        nullptr, false, status_dev, stream, &kv)
+                                        out_width, sm_scale, out, lse, part_o, part_ml, false,
+                                        status_dev, stream, &kv)
                       : launch_mla_stream(q_lat, nullptr, nullptr, q_seq, token_ids, Q, B,
                                           out_width, sm_scale, out, lse, part_o, part_ml,
                                           status_dev, stream, &kv);
-    if (r != DSA_OK || n_split == 1 || sync) return r;
+    if (r != DSA_OK || n_split == 1) return r;
     cfg.gridDim = dim3(Hm, Q, 1);
     cfg.blockDim = dim3(128, 1, 1);
     cfg.dynamicSmemBytes = 0;

@@ -40,7 +40,6 @@
 #include <mutex>
 
 #include "dsa_internal.cuh"
-#include "mla_merge.cuh"
 #include "umma.cuh"
 
 namespace dsa {
@@ -117,9 +116,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                     const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ q_seq,
                     const int32_t* __restrict__ token_ids, int B, int W, float sm_scale,
                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
-                    float* __restrict__ part_o, float* __restrict__ part_ml,
-                    uint32_t* __restrict__ sync, unsigned long long* __restrict__ ids_meets,
-                    int early, PagedKv pk, int drill, int32_t* status) {
+                    float* __restrict__ part_o, float* __restrict__ part_ml, int early,
+                    PagedKv pk, int drill, int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char* sb = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   MCtl& c = *reinterpret_cast<MCtl*>(sb + kOffCtl);
@@ -128,10 +126,6 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   const int qw = warp & 3;   // TMEM lanes 32 qw .. 32 qw + 31
   const int hq = warp >> 2;  // softmax: heads 16 hq .. 16 hq + 15; epilogue: chunk pair
 
-  // sync (splits merged in this kernel): the meeting counter of this (query,
-  // head half) group
-  unsigned long long* g_cnt =
-      sync ? reinterpret_cast<unsigned long long*>(sync) + (qi * 2 + hf) : nullptr;
   if (threadIdx.x == 0) {
     mbar_init(&c.s_ready, 1);
     mbar_init(&c.o_ready, 1);
@@ -169,21 +163,13 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   } else {
     Tb = seq_ok ? pk.seq_lens[b] : 0;
   }
-  // the meeting on which the top-k of this call publishes this query's ids
-  unsigned long long* idm = ids_meets ? ids_meets + 4 * qi + 2 : nullptr;
   if (early) {
-    if (idm) {
-      if (threadIdx.x == 0 && !meet_wait(idm, meet_base(idm + 1) + kMeetUnit, kWaitNs))
-        flag(status, DSA_DEV_TIMEOUT);
-      __syncthreads();
-    } else {
-      pdl_wait();  // the token ids of this call
-    }
+    pdl_wait();  // the token ids of this call
     pdl_launch_dependents();
   }
   if (threadIdx.x < kRows) {
     const int j = split * kRows + threadIdx.x;
-    int tok = (j < W && seq_ok) ? __ldcg(token_ids + (long long)qi * W + j) : -1;
+    int tok = (j < W && seq_ok) ? token_ids[(long long)qi * W + j] : -1;
     if (tok >= Tb) {
       if (hf == 0) flag(status, DSA_DEV_BAD_TOKEN);
       tok = -1;
@@ -438,31 +424,11 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   }
   // TMEM is freed only after every MMA this CTA issued has retired (bounded).
   if (threadIdx.x == 0 && pending != nullptr) mbar_wait_bounded(pending, 0);
-  if (g_cnt != nullptr) __threadfence();  // this thread's partials, before the meeting
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<kTmemCols>(tmem);
-  }
-  if (g_cnt != nullptr) {
-    // The n_split CTAs of this (query, head half) are all resident (the grid
-    // fits the SMs); once every partial is out, each merges a 1/n_split share
-    // of the group's 32 x 512 outputs.
-    if (threadIdx.x == 0 && !group_meet(g_cnt, split, n_split, wait_ns))
-      flag(status, DSA_DEV_TIMEOUT);
-    __syncthreads();
-    constexpr int kUnits = kHh * (kL / 4);  // (head, 4 latent columns) outputs of the group
-    const int u_lo = split * kUnits / n_split, u_hi = (split + 1) * kUnits / n_split;
-    for (int u = u_lo + threadIdx.x; u < u_hi; u += kThreadsM) {
-      const int h = u / (kL / 4), d = (u % (kL / 4)) * 4;
-      merge_partials<kL>(part_o, part_ml, qh0 + h, n_split, d, out, lse, d == 0);
-    }
-  }
-  if (idm != nullptr) {
-    // this CTA reads no more ids; it ends only after the kernel before it
-    if (threadIdx.x == 0) meet_add(idm + 1, meet_share(split * 2 + hf, n_split * 2));
-    pdl_wait();
   }
 }
 
@@ -885,9 +851,8 @@ namespace {
 template <int kKv>
 int launch_kind(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
                 const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int out_width,
-                float sm_scale, void* out, float* lse, float* part_o, float* part_ml,
-                uint32_t* sync, unsigned long long* ids_meets, bool early, const PagedKv& pk,
-                int32_t* status_dev, cudaStream_t stream) {
+                float sm_scale, void* out, float* lse, float* part_o, float* part_ml, bool early,
+                const PagedKv& pk, int32_t* status_dev, cudaStream_t stream) {
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(mla_umma_kernel<kKv>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -905,8 +870,8 @@ int launch_kind(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
   cfg.numAttrs = 1;
   return launch_kernel(&cfg, mla_umma_kernel<kKv>, (const __nv_bfloat16*)q_lat,
                        (const __nv_bfloat16*)kv, cu_seqlens, q_seq, token_ids, B, out_width,
-                       sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml, sync, ids_meets,
-                       early ? 1 : 0, pk, failure_drill(), status_dev) == cudaSuccess
+                       sm_scale, (__nv_bfloat16*)out, lse, part_o, part_ml, early ? 1 : 0,
+                       pk, failure_drill(), status_dev) == cudaSuccess
              ? DSA_OK
              : DSA_ERR_CUDA;
 }
@@ -975,25 +940,18 @@ int launch_mla_stream(const void* q_lat, const void* kv, const int32_t* cu_seqle
 int launch_mla_umma(const void* q_lat, const void* kv, const int32_t* cu_seqlens,
                     const int32_t* q_seq, const int32_t* token_ids, int Q, int B, int out_width,
                     float sm_scale, void* out, float* lse, float* part_o, float* part_ml,
-                    uint32_t* sync, unsigned long long* ids_meets, bool early,
-                    int32_t* status_dev, cudaStream_t stream, const PagedKv* paged) {
+                    bool early, int32_t* status_dev, cudaStream_t stream, const PagedKv* paged) {
   if (!paged)
     return launch_kind<kKvContig>(q_lat, kv, cu_seqlens, q_seq, token_ids, Q, B, out_width,
-                                  sm_scale, out, lse, part_o, part_ml, sync,
-                                  early ? ids_meets : nullptr, early, PagedKv{}, status_dev,
-                                  stream);
+                                  sm_scale, out, lse, part_o, part_ml, early, PagedKv{},
+                                  status_dev, stream);
   if (paged->kv_dtype == DSA_FP8_E4M3)
     return launch_kind<kKvPagedE4M3>(q_lat, nullptr, nullptr, q_seq, token_ids, Q, B, out_width,
-                                     sm_scale, out, lse, part_o, part_ml, sync, nullptr, early,
-                                     *paged, status_dev, stream);
+                                     sm_scale, out, lse, part_o, part_ml, early, *paged,
+                                     status_dev, stream);
   return launch_kind<kKvPaged>(q_lat, nullptr, nullptr, q_seq, token_ids, Q, B, out_width,
-                               sm_scale, out, lse, part_o, part_ml, sync, nullptr, early, *paged,
-                               status_dev, stream);
-}
-
-bool mla_umma_merges_in_kernel(int Q, int out_width) {
-  const int n_split = mla_umma_splits(out_width);
-  return n_split > 1 && (long long)Q * n_split * (kHm / kHh) <= num_sms();
+                               sm_scale, out, lse, part_o, part_ml, early, *paged, status_dev,
+                               stream);
 }
 
 }  // namespace dsa

@@ -105,9 +105,9 @@ extern "C" int dsa_select_noalloc(const void* q, const float* weights, float sca
   // own on chip: no scratch is touched
   r = dsa::launch_index_scores(q, weights, scale, pool_keys, pool_rows, pool_start, pool_valid,
                                n_pools, cu_pool_cap, q_seq, q_pos, Q, B, H, D, kpool, P_ld, dtype,
-                               scores, hist, nullptr, status_dev, st);
+                               scores, hist, status_dev, st);
   if (r != DSA_OK) return r;
-  return dsa::launch_select_after_index(scores, Q, P_ld, select_k, pool_ids, hist, nullptr, false,
-                                        pool_start, cu_pool_cap, q_seq, B, kpool, out_width,
-                                        token_ids, status_dev, st);
+  return dsa::launch_select_after_index(scores, Q, P_ld, select_k, pool_ids, hist, pool_start,
+                                        cu_pool_cap, q_seq, B, kpool, out_width, token_ids,
+                                        status_dev, st);
 }

@@ -49,11 +49,6 @@ struct ExpandArgs {   // optional fused expand_selection (token_ids == nullptr: 
   int B, kpool, W;
   int32_t* token_ids;
   int32_t* status;
-  // the fused select path: four meeting counters per query (see
-  // select_workspace_meets); nullptr: the kernel waits for the whole previous
-  // kernel instead.  ids_meet: publish the query's ids for the attention.
-  unsigned long long* meets;
-  int ids_meet;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -263,7 +258,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t s_wtot[64];
   __shared__ uint32_t s_cnt[2][17];  // per-rank sure / tie counts, exclusive prefix in [.][r]
   __shared__ uint64_t s_res;
-  __shared__ int s_meet;  // the scores' meeting counters were at rest: wait on them
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int C = (int)cluster.num_blocks();
@@ -271,37 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float* row = scores + (long long)q * P_ld;
   const int lo = (int)((long long)P_ld * rank / C);
   const int hi = (int)((long long)P_ld * (rank + 1) / C);
-  unsigned long long* mq = ex.meets ? ex.meets + 4 * q : nullptr;
   if (threadIdx.x == 0) { s_nsure = 0; s_ntie = 0; }
-  if (mq) {
-    // The scoring kernel publishes each query's scores and histogram as soon
-    // as they are out: this row starts without waiting for the other rows.
-    // Between calls the counters rest equal, on a multiple of the meeting unit
-    // (this cluster re-arms them below); any other state is a workspace that
-    // was not zero-filled: then the whole scoring kernel is waited for.
-    if (threadIdx.x == 0) {
-      const unsigned long long used = meet_load(mq + 1), done = meet_load(mq);
-      s_meet = (used & (kMeetUnit - 1)) == 0 && done - used <= kMeetUnit;
-      if (!s_meet) flag(ex.status, DSA_DEV_HIST_MISMATCH);
-      else if (!meet_wait(mq, used + kMeetUnit, kWaitNs)) flag(ex.status, DSA_DEV_TIMEOUT);
-      if (ex.ids_meet && rank == 0) {
-        // the ids counters, for the attention that starts on them, rest equal
-        // too (the attention of the previous call has ended); re-arm them if not
-        const unsigned long long iu = meet_load(mq + 3), id = meet_load(mq + 2);
-        if (iu != id || (iu & (kMeetUnit - 1)) != 0) {
-          const unsigned long long v = ((iu > id ? iu : id) + kMeetUnit - 1) & ~(kMeetUnit - 1);
-          mq[2] = v;
-          mq[3] = v;
-          __threadfence();
-          flag(ex.status, DSA_DEV_HIST_MISMATCH);
-        }
-      }
-    }
-    __syncthreads();
-    if (!s_meet) pdl_wait();
-  } else {
-    pdl_wait();
-  }
+  pdl_wait();
   pdl_launch_dependents();  // the next kernel may start its own prologue
 
   // The histogram (when the scoring kernel counted it), the first batch of this
@@ -319,14 +284,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
   for (int u = 0; u < kBatch; ++u) {
     const int i = lo + u * kThreads + threadIdx.x;
-    v_first[u] = i < hi ? __ldcg(row + i) : -INFINITY;
+    v_first[u] = i < hi ? row[i] : -INFINITY;
   }
   const int b = ex.token_ids ? (ex.q_seq ? ex.q_seq[q] : 0) : 0;
   const bool seq_ok = !ex.token_ids || (b >= 0 && b < ex.B);
   // slice element i of the pass starting at `base` (the first batch is in registers)
   auto slice = [&](int base, int u) -> float {
     const int i = base + u * kThreads + threadIdx.x;
-    return base == lo ? v_first[u] : (i < hi ? __ldcg(row + i) : -INFINITY);
+    return base == lo ? v_first[u] : (i < hi ? row[i] : -INFINITY);
   };
 
   // ---- 1. histogram of the top 12 key bits
@@ -415,14 +380,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long cap_base = (ex.token_ids && seq_ok) ? ex.cu_pool_cap[b] : 0;
   const int cap = (ex.token_ids && seq_ok) ? ex.cu_pool_cap[b + 1] - ex.cu_pool_cap[b] : 0;
   cluster.sync();  // every slice's lists and counts are final
-  if (mq && rank == 0 && threadIdx.x == 0) {
-    // Every CTA of the cluster has read the counters and every share of the
-    // scoring kernel is in: re-arm them for the next call (equal, on a
-    // multiple of the unit).
-    const unsigned long long v = (meet_load(mq) + kMeetUnit - 1) & ~(kMeetUnit - 1);
-    mq[0] = v;
-    mq[1] = v;
-  }
   // ---- 4. all-gather the cluster's lists
   if (threadIdx.x < 2 * C) {
     const int r = threadIdx.x % C, which = threadIdx.x / C;
@@ -476,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // start of a selected pool's tokens (-1 when it cannot be expanded)
   auto pool_first_token = [&](uint64_t key) -> int {
     const int p = key_pool(key);
-    return (tok && seq_ok && p < cap) ? __ldcg(pstart + cap_base + p) : -1;
+    return (tok && seq_ok && p < cap) ? pstart[cap_base + p] : -1;
   };
   // writes one selected key's pool id and token ids at output slot `pos`
   auto emit_with = [&](uint32_t pos, uint64_t key, int st) {
@@ -540,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) s_nsel = 0;
     __syncthreads();
     uint32_t cnt = 0;
-    for (int i = threadIdx.x; i < P_ld; i += kThreads) cnt += is_candidate(__ldcg(row + i));
+    for (int i = threadIdx.x; i < P_ld; i += kThreads) cnt += is_candidate(row[i]);
     atomicAdd(&s_nsel, cnt);
     __syncthreads();
     const uint32_t n_cand = s_nsel;
@@ -550,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (n_sel > 0) {
       auto get = [&](int i, uint64_t& k) {
-        const float sc = __ldcg(row + i);
+        const float sc = row[i];
         if (!is_candidate(sc)) return false;
         k = full_key(sc, i);
         return true;
@@ -573,14 +530,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (gh && rank == 0)  // leave the histogram the scoring kernel filled zeroed for the next call
     for (int i = threadIdx.x; i < kBins; i += kThreads) gh[i] = 0;
-  if (mq) {
-    // this CTA's ids are out: publish them for the attention of a fused decode
-    // call
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0 && ex.ids_meet) meet_add(mq + 2, meet_share(rank, C));
-    pdl_wait();  // the kernel ends only after the one before it
-  }
 }
 
 __global__ void expand_kernel(const int32_t* __restrict__ pool_ids,
@@ -677,28 +626,22 @@ int launch_select(const float* scores, int Q, int P_ld, int select_k, int32_t* p
 }  // namespace
 
 // Standalone top-k needs no workspace: the histogram lives on chip.  The fused
-// select path keeps in its workspace a [Q][4096] histogram and, 256-byte
-// aligned after it, four meeting counters per query:
-//   [0] scores done: added to by the scoring kernel once a query's scores and
-//       histogram are stored; [1] scores used: set equal to [0] by the top-k
-//       once its cluster has passed the meeting; [2] ids done: added to by the
-//       top-k once the query's ids are stored (fused decode call); [3] ids used:
-//       added to by the attention once it no longer reads them.
+// select path keeps a [Q][4096] histogram in its workspace.
 size_t topk_workspace_size(int Q, int P_ld, int select_k) {
   (void)Q; (void)P_ld; (void)select_k;
   return 0;
 }
 size_t select_workspace_size(int Q, int P_ld, int select_k) {
   (void)P_ld; (void)select_k;
-  return align256((size_t)Q * kBins * 4) + align256((size_t)Q * 4 * 8);
+  return align256((size_t)Q * kBins * 4) + 256;  // histograms, then the tile counter
+}
+
+int* select_workspace_counter(void* workspace, int Q) {
+  return reinterpret_cast<int*>(static_cast<unsigned char*>(workspace) +
+                                align256((size_t)Q * kBins * 4));
 }
 
 uint32_t* topk_workspace_hist(void* workspace) { return static_cast<uint32_t*>(workspace); }
-
-unsigned long long* select_workspace_meets(void* workspace, int Q) {
-  return reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(workspace) +
-                                               align256((size_t)Q * kBins * 4));
-}
 
 int launch_topk_pools(const float* scores, int Q, int P_ld, int select_k, int32_t* pool_ids,
                       void* workspace, size_t ws_bytes, cudaStream_t stream) {
@@ -708,14 +651,13 @@ int launch_topk_pools(const float* scores, int Q, int P_ld, int select_k, int32_
 }
 
 int launch_select_after_index(const float* scores, int Q, int P_ld, int select_k,
-                              int32_t* pool_ids, uint32_t* hist, unsigned long long* meets,
-                              bool ids_meet, const int32_t* pool_start,
+                              int32_t* pool_ids, void* workspace, const int32_t* pool_start,
                               const int32_t* cu_pool_cap, const int32_t* q_seq, int B, int kpool,
                               int out_width, int32_t* token_ids, int32_t* status_dev,
                               cudaStream_t stream) {
-  ExpandArgs ex = {pool_start, cu_pool_cap, q_seq, B,     kpool,
-                   out_width,  token_ids,   status_dev, meets, ids_meet ? 1 : 0};
-  return launch_select(scores, Q, P_ld, select_k, pool_ids, hist, ex, stream);
+  ExpandArgs ex = {pool_start, cu_pool_cap, q_seq, B, kpool, out_width, token_ids, status_dev};
+  return launch_select(scores, Q, P_ld, select_k, pool_ids,
+                       static_cast<uint32_t*>(workspace), ex, stream);
 }
 
 int launch_expand_selection(const int32_t* pool_ids, const int32_t* pool_start,

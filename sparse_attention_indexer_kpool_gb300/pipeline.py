@@ -53,7 +53,7 @@ class LayerBuffers:
             lse=torch.empty(Q, g.Hm, dtype=torch.float32, device=dev),
             ws_topk=torch.empty(max(ws_t, 16), dtype=torch.uint8, device=dev),
             ws_select=torch.zeros(max(ws_s, 16), dtype=torch.uint8, device=dev),
-            ws_mla=torch.zeros(ws_m, dtype=torch.uint8, device=dev) if ws_m else None,
+            ws_mla=torch.empty(ws_m, dtype=torch.uint8, device=dev) if ws_m else None,
             status=torch.zeros(1, dtype=torch.int32, device=dev))
 
 

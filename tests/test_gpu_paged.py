@@ -29,7 +29,7 @@ def run_paged(bt, token_ids, pc):
     lse = torch.full((Q, Hm), 7.0, dtype=torch.float32, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     n = ops.mla_paged_workspace_bytes(bt.q_lat, pc.pages, token_ids.shape[1])
-    ws = torch.zeros(max(n, 16), dtype=torch.uint8, device=DEV)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=DEV)
     ops.dsa_mla_paged_decode(bt.q_lat, pc.pages, pc.row_scale, pc.block_table, pc.seq_lens,
                              pc.page_size, bt.q_seq, token_ids, bt.sm_scale, out, lse, ws, st)
     torch.cuda.synchronize()

@@ -183,7 +183,7 @@ def test_mla_bad_tokens_and_empty_rows():
     out = torch.empty(Q, 64, 512, dtype=torch.bfloat16, device=DEV)
     lse = torch.empty(Q, 64, dtype=torch.float32, device=DEV)
     nb = ops.mla_workspace_bytes(Q, 64, 512, W, ops.DSA_BF16)
-    ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device=DEV)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     ops.dsa_mla_selected_decode(bt.q_lat, bt.kv, bt.cu_seqlens, bt.q_seq, tok, bt.sm_scale, out,
                                 lse, ws, st)
