@@ -35,6 +35,7 @@ for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
 METRIC = "DSA decode queries/sec at 262k ctx; index+attend HBM GB/s vs peak (1 GB300)"
 UNIT = "queries/s"
 N_LAYERS = 11
+N_QUERY_SETS = 4      # seeded query sets per layer that consecutive steps rotate over
 
 
 def parse():
@@ -49,6 +50,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fixed-queries", action="store_true",
+                    help="every step reuses one query set (default: steps rotate over "
+                         "N_QUERY_SETS seeded sets, so consecutive steps select different rows)")
     ap.add_argument("--breakdown", action="store_true",
                     help="diagnostic: per-stage in-graph times (extra events between stages)")
     ap.add_argument("--leg", choices=["prefill_index", "prefill_attention", "paged_attention"],
@@ -363,27 +367,39 @@ def run_ours(args, dist):
     B = 4
     Q = B
 
-    # ---- per-step host I/O lives in two contiguous staging buffers
+    # ---- per-step host I/O lives in contiguous staging buffers: one step's
+    # queries of every layer (a query set) per N_QUERY_SETS, and the outputs
     q_bytes = Q * geo.H * geo.D * 2
     w_bytes = Q * geo.H * 4
     ql_bytes = Q * geo.Hm * geo.L * 2
     in_per_layer = q_bytes + w_bytes + ql_bytes
+    set_bytes = n_layers * in_per_layer
     out_per_layer = Q * geo.Hm * geo.L * 2 + Q * geo.Hm * 4
-    stage_in = torch.empty(n_layers * in_per_layer, dtype=torch.uint8, device=dev)
+    n_sets = 1 if args.fixed_queries else N_QUERY_SETS
+    stage_in = torch.empty(n_sets * set_bytes, dtype=torch.uint8, device=dev)
     stage_out = torch.empty(n_layers * out_per_layer, dtype=torch.uint8, device=dev)
 
     layers = []
+    qsets = []   # qsets[l][k]: (q, weights, q_lat) of layer l in query set k
     for l in range(n_layers):
         bt = synth.make_batch(geo, [T] * B, [0] * B, device=dev, seed=3000 + 100 * l)
         bt.q_pos = None                      # decode query at T-1: every complete pool is visible
-        o = l * in_per_layer
-        for name, nb, dt, shape in (("q", q_bytes, torch.bfloat16, (Q, geo.H, geo.D)),
-                                    ("weights", w_bytes, torch.float32, (Q, geo.H)),
-                                    ("q_lat", ql_bytes, torch.bfloat16, (Q, geo.Hm, geo.L))):
-            view = stage_in[o:o + nb].view(dt).view(shape)
-            view.copy_(getattr(bt, name))
-            setattr(bt, name, view)
-            o += nb
+        sets = []
+        for k in range(n_sets):
+            src = (bt.q, bt.weights, bt.q_lat) if k == 0 else synth.query_set(
+                geo, Q, device=dev, seed=900000 + 100 * l + k)
+            o = k * set_bytes + l * in_per_layer
+            views = []
+            for t, nb, dt, shape in ((src[0], q_bytes, torch.bfloat16, (Q, geo.H, geo.D)),
+                                     (src[1], w_bytes, torch.float32, (Q, geo.H)),
+                                     (src[2], ql_bytes, torch.bfloat16, (Q, geo.Hm, geo.L))):
+                view = stage_in[o:o + nb].view(dt).view(shape)
+                view.copy_(t)
+                views.append(view)
+                o += nb
+            sets.append(tuple(views))
+        bt.q, bt.weights, bt.q_lat = sets[0]
+        qsets.append(sets)
         buf = pipeline.LayerBuffers.alloc(bt)
         buf.scores_idx = torch.empty_like(buf.scores)
         o = l * out_per_layer
@@ -406,12 +422,14 @@ def run_ours(args, dist):
         assert int(buf.status.item()) == 0
         buf.pool_begin = (buf.n_pools - 1).clamp(min=0).to(torch.int32)
 
-    def step(events=None):
+    def step(events=None, qset=0):
         """One decode step over every layer: one dsa_decode_layer call per layer
-        (compress of the just-completed pool -> select -> attend).  With events,
-        the three stage calls run separately and events[layer] = (before, after)
-        the select call (index_scores + top-k + expand)."""
+        (compress of the just-completed pool -> select -> attend), on query set
+        ``qset``.  With events, the three stage calls run separately and
+        events[layer] = (before, after) the select call (index_scores + top-k +
+        expand)."""
         for li, (bt, buf) in enumerate(layers):
+            bt.q, bt.weights, bt.q_lat = qsets[li][qset % n_sets]
             if events is None:
                 pipeline.decode_layer(bt, buf, pool_begin=buf.pool_begin, max_pools=1)
                 continue
@@ -422,8 +440,8 @@ def run_ours(args, dist):
             pipeline.attend(bt, buf)
 
     # ---- warm-up (eager), then capture
-    for _ in range(max(3, args.warmup)):
-        step()
+    for w in range(max(3, args.warmup)):
+        step(qset=w)
     torch.cuda.synchronize()
 
     K = args.steps
@@ -437,7 +455,7 @@ def run_ours(args, dist):
     with torch.cuda.stream(side):
         with torch.cuda.graph(g_plain, stream=side):
             for s in range(S):
-                step()
+                step(qset=s)
     # the library's own count of the kernels recorded for S steps
     launches_per_step = (ops.dsa_kernel_launches() - n0) // S
     # g_ev: the same steps with timing events around every select call (the
@@ -453,11 +471,11 @@ def run_ours(args, dist):
         with torch.cuda.stream(side):
             with torch.cuda.graph(g_ev, stream=side):
                 for s in range(S):
-                    step(ev[s])
-    g1 = torch.cuda.CUDAGraph()
+                    step(ev[s], qset=s)
+    g1 = torch.cuda.CUDAGraph()   # one step on query set 0 (the end-to-end leg's staging area)
     with torch.cuda.stream(side):
         with torch.cuda.graph(g1, stream=side):
-            step()
+            step(qset=0)
     # g_idx: the dominant kernel alone (the scoring kernel of every layer, back to
     # back), for its roofline; dsa_index_scores runs the same tcgen05 kernel as
     # the select call, without counting the top-k histogram
@@ -465,7 +483,8 @@ def run_ours(args, dist):
     with torch.cuda.stream(side):
         with torch.cuda.graph(g_idx, stream=side):
             for s in range(S):
-                for bt, buf in layers:
+                for li, (bt, buf) in enumerate(layers):
+                    bt.q, bt.weights, bt.q_lat = qsets[li][s % n_sets]
                     ops.dsa_index_scores(bt.q, bt.weights, bt.scale, buf.pool_keys,
                                          buf.pool_start, buf.pool_valid, buf.n_pools,
                                          bt.cu_pool_cap, bt.q_seq, bt.q_pos, geo.kpool,
@@ -512,15 +531,19 @@ def run_ours(args, dist):
     clocks = sampler.stop()
     ms = dist.max(t0.elapsed_time(t1))
 
-    # ---- end to end: pinned host inputs -> device, the step, results -> host
+    # ---- end to end: pinned host inputs -> device, the step, results -> host.
+    # Every step copies the next query set from the host into the staging area
+    # the one-step graph reads, so consecutive steps select different rows.
     e2e = None
     if not args.no_e2e:
         h_in = torch.empty(stage_in.numel(), dtype=torch.uint8, pin_memory=True)
         h_in.copy_(stage_in)
+        h_sets = [h_in[k * set_bytes:(k + 1) * set_bytes] for k in range(n_sets)]
+        d_set0 = stage_in[:set_bytes]
         h_out = torch.empty(stage_out.numel(), dtype=torch.uint8, pin_memory=True)
         stream = torch.cuda.current_stream()
-        for _ in range(3):
-            stage_in.copy_(h_in, non_blocking=True)
+        for i in range(3):
+            d_set0.copy_(h_sets[i % n_sets], non_blocking=True)
             g1.replay()
             h_out.copy_(stage_out, non_blocking=True)
         torch.cuda.synchronize()
@@ -528,8 +551,8 @@ def run_ours(args, dist):
         a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         wall0 = time.perf_counter()
         a.record()
-        for _ in range(K):
-            stage_in.copy_(h_in, non_blocking=True)
+        for i in range(K):
+            d_set0.copy_(h_sets[(i + 1) % n_sets], non_blocking=True)
             g1.replay()
             h_out.copy_(stage_out, non_blocking=True)
         b_.record()
@@ -537,7 +560,7 @@ def run_ours(args, dist):
         wall = time.perf_counter() - wall0
         e_ms = dist.max(max(a.elapsed_time(b_), wall * 1e3))
         e2e = {"value": dist.world * Q * K / (e_ms / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": int(stage_in.numel()),
+               "h2d_bytes_per_step": int(set_bytes),
                "d2h_bytes_per_step": int(stage_out.numel())}
 
     breakdown = None
@@ -607,7 +630,10 @@ def run_ours(args, dist):
                    "mla_heads": geo.Hm, "latent": geo.L,
                    "l2": "inputs larger than L2: %d layers x %d MiB pool keys cycle through "
                          "the 129 MB L2" % (n_layers, B * (T // geo.kpool) * geo.D * 2 >> 20),
-                   "graph": "CUDA graph of %d steps replayed %d times" % (S, R)},
+                   "graph": "CUDA graph of %d steps replayed %d times" % (S, R),
+                   "queries": ("one seeded query set reused by every step" if n_sets == 1 else
+                               "consecutive steps rotate over %d seeded query sets per layer "
+                               "(q, weights, q_lat), so they select different rows" % n_sets)},
         "gpu_launches": launches_per_step * K,
         "roofline": roofline, "select_call_in_step": select_call,
         "step_hbm_gbs": round(step_gbs, 1), "step_frac_of_peak": round(step_gbs / hbm_peak, 4),
@@ -697,22 +723,127 @@ def host_layer(layer):
     }
 
 
-def cpu_baseline(layer, seconds):
-    host = host_layer(layer)
+def _oracle_loop(host, first, seconds):
+    """Decode query-layers through the oracle for about ``seconds`` (sequences
+    round-robin from ``first``); returns (query-layers done, seconds taken)."""
     B = len(host["k"])
     n, t0 = 0, time.perf_counter()
     while True:
-        oracle_query_layer(host, n % B)
+        oracle_query_layer(host, (first + n) % B)
         n += 1
         if time.perf_counter() - t0 >= seconds:
             break
-    dt = time.perf_counter() - t0
-    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", "1"))
-    return {"value": round(n / dt / N_LAYERS, 4), "unit": UNIT, "cores": threads,
-            "kind": "oracle",
-            "sample": f"{n} decode query-layers of the 262k workload (layer 0, sequences "
-                      f"round-robin) through the numpy float64 oracle in {dt:.1f} s; "
+    return n, time.perf_counter() - t0
+
+
+def _cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=20).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return "unknown"
+
+
+def _share(host):
+    """The host arrays as shared-memory tensors, so that worker processes receive
+    them by handle instead of by copy."""
+    import numpy as np
+    import torch
+
+    def conv(v):
+        if isinstance(v, np.ndarray):
+            return _Shared(torch.from_numpy(v).share_memory_())
+        if isinstance(v, _Rows):
+            return _Rows(v.t.share_memory_())
+        if isinstance(v, list):
+            return [conv(x) for x in v]
+        return v
+    return {k: conv(v) for k, v in host.items()}
+
+
+class _Shared:
+    """A shared-memory tensor that the oracle reads as a numpy array."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __reduce__(self):
+        return (_Shared, (self.t,))
+
+
+def _unshare(host):
+    def conv(v):
+        if isinstance(v, _Shared):
+            return v.t.numpy()
+        if isinstance(v, list):
+            return [conv(x) for x in v]
+        return v
+    return {k: conv(v) for k, v in host.items()}
+
+
+def _oracle_worker_shared(job):
+    host, first, seconds = job
+    return _oracle_loop(_unshare(host), first, seconds)
+
+
+def cpu_baseline(layer, seconds, cores=None):
+    """The oracle on this host's cores: one core, then every core (one process
+    per core, each running whole query-layers of the same workload)."""
+    host = host_layer(layer)
+    n1, dt1 = _oracle_loop(host, 0, seconds)
+    v1 = n1 / dt1 / N_LAYERS
+    if cores is None:
+        cores = (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+                 else os.cpu_count())
+    v_all, n_all, dt_all = v1, n1, dt1
+    if cores > 1:
+        import torch.multiprocessing as tmp
+        shared = _share(host)
+        ctx = tmp.get_context("spawn")     # workers never touch the GPU
+        with ctx.Pool(cores) as pool:
+            pool.map(_oracle_worker_shared, [(shared, i, 0.5) for i in range(cores)])  # start-up
+            res = pool.map(_oracle_worker_shared, [(shared, i, seconds) for i in range(cores)])
+        n_all = sum(r[0] for r in res)
+        dt_all = max(r[1] for r in res)
+        v_all = n_all / dt_all / N_LAYERS
+    return {"value": round(v_all, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "value_all": round(v_all, 4), "cores_all": cores,
+            "value_1core": round(v1, 4), "cpu_model": _cpu_model(),
+            "sample": f"decode query-layers of the 262k workload (layer 0, sequences "
+                      f"round-robin) through the numpy float64 oracle, one query-layer at a "
+                      f"time per process (BLAS on one thread): {n_all} query-layers on "
+                      f"{cores} cores in {dt_all:.1f} s and {n1} on one core in {dt1:.1f} s; "
                       f"queries/s = query-layers/s / {N_LAYERS} layers"}
+
+
+def oracle_layer_cache(bt):
+    """The pool cache of an equal-length batch, built by the oracle (for the CPU
+    legs when no GPU built it)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    T, geo = bt.lengths[0], bt.geo
+    cap = T // geo.kpool
+
+    class _Buf:
+        pass
+    buf = _Buf()
+    f = lambda t: t.detach().to("cpu", torch.float64).numpy()
+    pk, ps, pv = [], [], []
+    for b in range(bt.B):
+        o = oracle.kpool_compress(f(bt.k[b * T:(b + 1) * T]), f(bt.gate[b * T:(b + 1) * T]),
+                                  bt.valid[b * T:(b + 1) * T].cpu().numpy(), f(bt.ape),
+                                  f(bt.ln_gamma), f(bt.ln_beta), geo.ln_eps, [0, T], [0, cap],
+                                  geo.kpool, "bf16")
+        pk.append(o[0]); ps.append(o[1]); pv.append(o[2])
+    buf.pool_keys = torch.tensor(np.concatenate(pk), dtype=torch.float64)
+    buf.pool_start = torch.tensor(np.concatenate(ps), dtype=torch.int32)
+    buf.pool_valid = torch.tensor(np.concatenate(pv), dtype=torch.uint8)
+    return buf
 
 
 def run_reference(args, dist):
@@ -732,22 +863,7 @@ def run_reference(args, dist):
     # the oracle builds its own pool cache for the sample (setup, not timed)
     T = args.seqlen
     cap = T // geo.kpool
-
-    class _Buf:
-        pass
-    buf = _Buf()
-    f = lambda t: t.detach().to("cpu", torch.float64).numpy()
-    pk, ps, pv = [], [], []
-    for b in range(4):
-        o = oracle.kpool_compress(f(bt.k[b * T:(b + 1) * T]), f(bt.gate[b * T:(b + 1) * T]),
-                                  bt.valid[b * T:(b + 1) * T].cpu().numpy(), f(bt.ape),
-                                  f(bt.ln_gamma), f(bt.ln_beta), geo.ln_eps, [0, T], [0, cap],
-                                  geo.kpool, "bf16")
-        pk.append(o[0]); ps.append(o[1]); pv.append(o[2])
-    buf.pool_keys = torch.tensor(np.concatenate(pk), dtype=torch.float64)
-    buf.pool_start = torch.tensor(np.concatenate(ps), dtype=torch.int32)
-    buf.pool_valid = torch.tensor(np.concatenate(pv), dtype=torch.uint8)
-    host = host_layer((bt, buf))
+    host = host_layer((bt, oracle_layer_cache(bt)))
     # Size each step so that the whole run stays within a few minutes: one
     # query-layer per step, restricted to the first P_s pools of its sequence
     # (the oracle's time is dominated by the scoring pass, linear in the pools).

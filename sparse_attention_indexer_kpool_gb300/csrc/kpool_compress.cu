@@ -257,6 +257,173 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   }
 }
 
+// Bulk builds (a cache build, a prefill chunk's pools) in bf16 with D = 128: a
+// half-warp per pool, lane j owning channels [8j, 8j + 8) with 16-byte loads;
+// each CTA takes kWidePools consecutive pools of one sequence, so its metadata
+// loads and its first-valid-token scan serve all of them, and many pools'
+// rows are in flight per SM.  The LayerNorm statistics are reduced in the
+// order of the warp-per-pool kernel above (lane j holds that kernel's lanes 2j
+// and 2j + 1), so the two kernels write bit-identical keys.
+constexpr int kWidePools = 128;   // pools per CTA
+constexpr int kWideMin = 32;      // launches covering at least this many pools per sequence
+
+__device__ __forceinline__ float half_sum(float v, unsigned mask) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(mask, v, o, 16);
+  return v;
+}
+
+template <int KP>  // slots held per pool (>= kpool)
+__global__ void __launch_bounds__(256, KP <= 4 ? 2 : 1)
+    kpool_compress_wide_kernel(const __nv_bfloat16* __restrict__ k,
+                               const __nv_bfloat16* __restrict__ gate,
+                               const uint8_t* __restrict__ valid, const float* __restrict__ ape,
+                               const __nv_bfloat16* __restrict__ ln_gamma,
+                               const __nv_bfloat16* __restrict__ ln_beta, float ln_eps,
+                               const int32_t* __restrict__ cu_seqlens,
+                               const int32_t* __restrict__ cu_pool_cap,
+                               const int32_t* __restrict__ pool_begin, int kpool, int max_pools,
+                               __nv_bfloat16* __restrict__ pool_keys,
+                               int32_t* __restrict__ pool_start,
+                               uint8_t* __restrict__ pool_valid, int32_t* __restrict__ n_pools,
+                               int32_t* status) {
+  constexpr int D = 128;
+  using T = __nv_bfloat16;
+  __shared__ int s_min;
+  __shared__ float s_ape[KP * D];
+  pdl_wait();
+  pdl_launch_dependents();  // the next kernel may start its prologue
+  const int b = blockIdx.y;
+  const long long lo = cu_seqlens[b];
+  const int Tb = cu_seqlens[b + 1] - cu_seqlens[b];
+  const long long cap_lo = cu_pool_cap[b];
+  const int cap = cu_pool_cap[b + 1] - cu_pool_cap[b];
+  const int begin = pool_begin ? pool_begin[b] : 0;
+  const int end = (int)min((long long)begin + max_pools, (long long)cap);
+  const int p_first = begin + blockIdx.x * kWidePools;
+  if (!(p_first < end || blockIdx.x == 0)) return;  // nothing of this sequence here
+  for (int i = threadIdx.x; i < kpool * D; i += blockDim.x) s_ape[i] = ape[i];
+  const int t0 = first_valid_token(valid + 0, lo, Tb, &s_min);  // (its barriers publish s_ape)
+  const int P = (Tb - t0) / kpool;
+  const int P_eff = min(P, cap);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    n_pools[b] = P_eff;
+    if (P > cap) flag(status, DSA_DEV_POOL_OVERFLOW);
+    if (P_eff > end) flag(status, DSA_DEV_POOL_UNCOVERED);
+  }
+  const int half = threadIdx.x >> 4, j = threadIdx.x & 15;
+  const unsigned hmask = 0xffffu << (threadIdx.x & 16);
+  float g[8], be[8];
+  Vec<T, 8>::load(ln_gamma + j * 8, g);
+  Vec<T, 8>::load(ln_beta + j * 8, be);
+  const int p_end = min(p_first + kWidePools, end);
+  for (int p = p_first + half; p < p_end; p += blockDim.x / 16) {
+    if (p < 0) continue;
+    T* out = pool_keys + (cap_lo + p) * D + j * 8;
+    if (p >= P_eff) {  // sentinel entry
+      *reinterpret_cast<uint4*>(out) = make_uint4(0u, 0u, 0u, 0u);
+      if (j == 0) {
+        pool_start[cap_lo + p] = -1;
+        pool_valid[cap_lo + p] = 0;
+      }
+      continue;
+    }
+    const long long s0 = lo + t0 + (long long)p * kpool;
+    float kn[KP][8], lg[KP][8];
+    bool all_valid = true;
+#pragma unroll
+    for (int s = 0; s < KP; ++s) {
+      if (s < kpool) {
+        Vec<T, 8>::load(k + (s0 + s) * D + j * 8, kn[s]);
+        Vec<T, 8>::load(gate + (s0 + s) * D + j * 8, lg[s]);
+        all_valid &= valid[s0 + s] != 0;
+      }
+    }
+#pragma unroll
+    for (int s = 0; s < KP; ++s) {
+      if (s < kpool) {
+        // the warp-per-pool kernel's lane partials (4 channels each), its tree
+        float sa = 0.f, sb = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sa += kn[s][i];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sb += kn[s][4 + i];
+        sa = half_sum(sa, hmask);
+        sb = half_sum(sb, hmask);
+        const float mean = (sa + sb) * (1.0f / D);
+        float qa = 0.f, qb = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float dx = kn[s][i] - mean;
+          qa += dx * dx;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float dx = kn[s][4 + i] - mean;
+          qb += dx * dx;
+        }
+        qa = half_sum(qa, hmask);
+        qb = half_sum(qb, hmask);
+        const float var = (qa + qb) * (1.0f / D);
+        const float rstd = 1.0f / sqrtf(var + ln_eps);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          kn[s][i] = Act<T>::round((kn[s][i] - mean) * rstd * g[i] + be[i]);
+          lg[s][i] = lg[s][i] + s_ape[s * D + j * 8 + i];
+        }
+      }
+    }
+    float res[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float m = lg[0][i];
+#pragma unroll
+      for (int s = 1; s < KP; ++s)
+        if (s < kpool) m = fmaxf(m, lg[s][i]);
+      float den = 0.f, acc = 0.f;
+#pragma unroll
+      for (int s = 0; s < KP; ++s) {
+        if (s < kpool) {
+          const float e = expf(lg[s][i] - m);
+          den += e;
+          acc += e * kn[s][i];
+        }
+      }
+      res[i] = acc / den;
+    }
+    Vec<T, 8>::store(out, res);
+    if (j == 0) {
+      pool_start[cap_lo + p] = t0 + p * kpool;
+      pool_valid[cap_lo + p] = all_valid ? 1 : 0;
+    }
+  }
+}
+
+template <int KP>
+int launch_wide(const void* k, const void* gate, const uint8_t* valid, const float* ape,
+                const void* g, const void* be, float eps, const int32_t* cu, const int32_t* cap,
+                const int32_t* begin, int B, int kpool, int max_pools, void* pk, int32_t* ps,
+                uint8_t* pv, int32_t* np, int32_t* st, cudaStream_t stream) {
+  using T = __nv_bfloat16;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((max_pools + kWidePools - 1) / kWidePools, B, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = launch_kernel(
+      &cfg, kpool_compress_wide_kernel<KP>, (const T*)k, (const T*)gate, valid, ape, (const T*)g,
+      (const T*)be, eps, cu, cap, begin, kpool, max_pools, (T*)pk, ps, pv, np, st);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+bool uses_wide(int D, int max_pools, int dtype) {
+  return dtype == DSA_BF16 && D == 128 && max_pools >= kWideMin;
+}
+
 template <typename T, int V>
 int launch_t(const void* k, const void* gate, const uint8_t* valid, const float* ape,
              const void* g, const void* be, float eps, const int32_t* cu, const int32_t* cap,
@@ -281,6 +448,7 @@ int launch_t(const void* k, const void* gate, const uint8_t* valid, const float*
 }  // namespace
 
 int kpool_compress_ctas(int B, int max_pools) {
+  if (max_pools >= kWideMin) return (max_pools + kWidePools - 1) / kWidePools * B;
   return max(1, (max_pools + kWarpsPerCta - 1) / kWarpsPerCta) * B;
 }
 
@@ -290,6 +458,15 @@ int launch_kpool_compress(const void* k, const void* gate, const uint8_t* valid,
                           const int32_t* pool_begin, int B, int D, int kpool, int max_pools,
                           int dtype, void* pool_keys, int32_t* pool_start, uint8_t* pool_valid,
                           int32_t* n_pools, int32_t* status_dev, cudaStream_t stream) {
+  if (uses_wide(D, max_pools, dtype)) {
+    if (kpool <= 4)
+      return launch_wide<4>(k, gate, valid, ape, ln_gamma, ln_beta, ln_eps, cu_seqlens,
+                            cu_pool_cap, pool_begin, B, kpool, max_pools, pool_keys, pool_start,
+                            pool_valid, n_pools, status_dev, stream);
+    return launch_wide<8>(k, gate, valid, ape, ln_gamma, ln_beta, ln_eps, cu_seqlens, cu_pool_cap,
+                          pool_begin, B, kpool, max_pools, pool_keys, pool_start, pool_valid,
+                          n_pools, status_dev, stream);
+  }
 #define DSA_COMPRESS_CASE(TT, VV)                                                            \
   return launch_t<TT, VV>(k, gate, valid, ape, ln_gamma, ln_beta, ln_eps, cu_seqlens,        \
                           cu_pool_cap, pool_begin, B, kpool, max_pools, pool_keys, pool_start, \

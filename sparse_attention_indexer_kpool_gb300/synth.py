@@ -168,6 +168,20 @@ def make_batch(geo: Geometry, lengths, pads, *, device="cpu", seed=0, queries="d
                  q_lat=q_lat, kv=kv, scale=1.0 / math.sqrt(D), sm_scale=1.0 / math.sqrt(L))
 
 
+def query_set(geo: Geometry, Q: int, *, device="cpu", seed=0, weights_std=None):
+    """Another draw of a batch's per-step query inputs (q, weights, q_lat) with
+    make_batch's normal distributions: a decode step's queries change from step
+    to step while the caches stay."""
+    dev = torch.device(device)
+    g = _gen(dev, seed)
+    act = torch_dtype(geo.dtype)
+    wstd = weights_std if weights_std is not None else math.sqrt(1.0 / 32.0)
+    q = _normal((Q, geo.H, geo.D), 1.0, g, dev, act)
+    weights = _normal((Q, geo.H), wstd, g, dev, torch.float32)
+    q_lat = _normal((Q, geo.Hm, geo.L), 1.0, g, dev, act)
+    return q, weights, q_lat
+
+
 # --------------------------------------------------------------------------
 # the five named workloads
 # --------------------------------------------------------------------------

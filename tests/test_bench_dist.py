@@ -78,3 +78,17 @@ def test_reference_arm_prints_one_contract_line():
     assert cb["unit"] == d["unit"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_cpu_baseline_on_one_and_on_several_cores():
+    """The bench's CPU baseline: the oracle on one core and in one process per
+    core (two here), with the cores, their model and both rates reported."""
+    import bench
+    from sparse_attention_indexer_kpool_gb300 import synth
+    bt = synth.make_batch(synth.GEO_MAIN, [2048] * 4, [0] * 4, device="cpu", seed=5)
+    bt.q_pos = None
+    cb = bench.cpu_baseline((bt, bench.oracle_layer_cache(bt)), 0.3, cores=2)
+    assert cb["kind"] == "oracle" and cb["unit"] == bench.UNIT
+    assert cb["cores"] == cb["cores_all"] == 2
+    assert cb["value"] == cb["value_all"] > 0 and cb["value_1core"] > 0
+    assert isinstance(cb["cpu_model"], str) and cb["sample"]

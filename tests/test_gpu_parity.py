@@ -119,6 +119,27 @@ def test_incremental_compress_matches_full_build():
     assert torch.equal(full.pool_start, buf.pool_start)
 
 
+@pytest.mark.parametrize("kpool", [1, 3, 4, 8])
+def test_bulk_compress_equals_pool_by_pool(kpool):
+    """A bulk build (bf16, D = 128: the wide kernel, a half-warp per pool) writes
+    the keys that sixteen-pool incremental calls (the warp-per-pool kernel)
+    write, bit for bit, on ragged sequences with padding; and both match the
+    oracle."""
+    geo = Geometry(D=128, H=32, kpool=kpool, select_k=16, out_width=16 * kpool, Hm=64, L=512,
+                   dtype="bf16")
+    bt = synth.make_batch(geo, [1203, 40, 2500, 7], [5, 0, 1, 2], device=DEV, seed=90 + kpool)
+    bulk = pipeline.LayerBuffers.alloc(bt)
+    pipeline.compress(bt, bulk)                     # max_pools = P_ld: the wide kernel
+    inc = pipeline.LayerBuffers.alloc(bt)
+    for p0 in range(0, bt.P_ld, 16):                # sixteen pools per call: the warp kernel
+        begin = torch.full((bt.B,), p0, dtype=torch.int32, device=DEV)
+        pipeline.compress(bt, inc, pool_begin=begin, max_pools=16)
+    torch.cuda.synchronize()
+    for name in ("pool_keys", "pool_start", "pool_valid", "n_pools"):
+        assert torch.equal(getattr(bulk, name), getattr(inc, name)), name
+    par.check_compress(oracle_inputs(bt), bulk)
+
+
 def _topk_gpu(scores, k):
     Q, P = scores.shape
     ws = torch.empty(ops.topk_workspace_bytes(Q, P, k), dtype=torch.uint8, device=DEV)
@@ -329,11 +350,16 @@ def _assert_same_outputs(a, b):
         assert torch.equal(getattr(a, name), getattr(b, name)), name
 
 
-def test_decode_layer_matches_the_three_calls():
+@pytest.mark.parametrize("decode_form", [False, True])
+def test_decode_layer_matches_the_three_calls(decode_form):
     """The fused call writes what compress -> select -> attend write, for a full
-    build and for an incremental step (the scoring kernel then starts streaming
-    the key tiles below pool_begin before the compress has finished)."""
+    build and for an incremental step.  In the decode form (no query positions:
+    every complete pool is visible, as at the last token) the incremental step's
+    scoring kernel streams the key tiles below pool_begin before the compress
+    kernel has ended."""
     for bt in (ragged_small(seed=51), synth.single32k(device=DEV, seed=52), synth.tiny(device=DEV)):
+        if decode_form:
+            bt.q_pos = None
         a = pipeline.LayerBuffers.alloc(bt)
         b = pipeline.LayerBuffers.alloc(bt)
         pipeline.decode_layer(bt, a)
@@ -355,19 +381,22 @@ def test_decode_layer_matches_the_three_calls():
         assert int(a.status.item()) == 0
 
 
+@pytest.mark.parametrize("decode_form", [False, True])
 @pytest.mark.parametrize("step", ["last_pool", "past_last_pool", "half"])
-def test_decode_layer_incremental_pool_count_from_the_valid_mask(step):
+def test_decode_layer_incremental_pool_count_from_the_valid_mask(step, decode_form):
     """Incremental steps on sequences that start with 0, 37, 255, 256 or 1000
-    padding tokens, a short fully valid one and an all-padding one.  Inside the
-    fused call the scoring kernel scores the key tiles below pool_begin before
-    the compress has ended, with each pool count found from the valid mask when
-    the first valid token is among the sequence's first 256 tokens (else it
-    reads the count the compress wrote); the fused call must write exactly what
-    the three separate calls write."""
+    padding tokens, a short fully valid one and an all-padding one.  In the
+    decode form (no query positions) the fused call scores the key tiles below
+    pool_begin before its compress kernel has ended, with each pool count found
+    from the valid mask when the first valid token is among the sequence's
+    first 256 tokens (else it reads the count the compress wrote); it must write
+    exactly what the three separate calls write."""
     big = Geometry(D=128, H=32, kpool=4, select_k=512, out_width=2048, Hm=64, L=512, dtype="bf16")
     lengths = [3000, 3000, 2900, 3100, 4000, 250, 200]
     pads = [0, 37, 255, 256, 1000, 0, 200]
     bt = synth.make_batch(big, lengths, pads, device=DEV, seed=71)
+    if decode_form:
+        bt.q_pos = None
     a = pipeline.LayerBuffers.alloc(bt)
     b = pipeline.LayerBuffers.alloc(bt)
     pipeline.decode_layer(bt, a)
@@ -394,8 +423,10 @@ def test_decode_layer_incremental_pool_count_from_the_valid_mask(step):
 
 def test_decode_layer_launches_what_the_three_calls_launch():
     """The library's launch count: the fused call launches as many kernels as
-    compress -> select -> attend, and an incremental step launches them again."""
+    compress -> select -> attend, for a full build and for a decode step (no
+    query positions, one new pool per sequence)."""
     bt = ragged_small(seed=54)
+    bt.q_pos = None
     a = pipeline.LayerBuffers.alloc(bt)
     b = pipeline.LayerBuffers.alloc(bt)
     n0 = ops.dsa_kernel_launches()
@@ -407,7 +438,47 @@ def test_decode_layer_launches_what_the_three_calls_launch():
     assert n1 - n0 == n2 - n1 >= 4
     begin = (a.n_pools - 1).clamp(min=0).to(torch.int32)
     pipeline.decode_layer(bt, a, pool_begin=begin, max_pools=1)
-    assert ops.dsa_kernel_launches() - n2 == n1 - n0
+    n3 = ops.dsa_kernel_launches()
+    pipeline.run_layer(bt, b, pool_begin=begin, max_pools=1)
+    torch.cuda.synchronize()
+    assert n3 - n2 == n1 - n0
+    assert ops.dsa_kernel_launches() - n3 == n2 - n1
+    _assert_same_outputs(a, b)
+
+
+def test_decode_step_shared_sequence_and_straddling_pools():
+    """A decode-form incremental step (the scoring kernel starts before the
+    compress ends) with two queries on one sequence, a sequence with no query,
+    and recompressed pools that straddle a 128-pool key tile (three pools from
+    pool 127): the same outputs as compress -> select -> attend, and the
+    oracle's pool keys."""
+    geo = Geometry(D=128, H=32, kpool=4, select_k=64, out_width=256, Hm=64, L=512, dtype="bf16")
+    bt = synth.make_batch(geo, [3000, 1500, 600, 800], [2, 0, 5, 0], device=DEV, seed=81)
+    bt.q_pos = None
+    bt.q_seq = torch.tensor([0, 0, 1, 2], dtype=torch.int32, device=DEV)  # sequence 3: no query
+    a = pipeline.LayerBuffers.alloc(bt)
+    b = pipeline.LayerBuffers.alloc(bt)
+    pipeline.decode_layer(bt, a)
+    pipeline.run_layer(bt, b)
+    torch.cuda.synchronize()
+    _assert_same_outputs(a, b)
+    begin = torch.tensor([127, 300, 126, 10], dtype=torch.int32, device=DEV)
+    for s, p0 in enumerate(begin.tolist()):       # new content for the recompressed pools
+        lo = int(bt.cu_seqlens[s]) + bt.pads[s] + p0 * geo.kpool
+        bt.k[lo:lo + 3 * geo.kpool] *= -1
+        bt.gate[lo:lo + 3 * geo.kpool] += 1
+    for buf in (a, b):
+        buf.scores.fill_(7.0)
+    pipeline.decode_layer(bt, a, pool_begin=begin, max_pools=3)
+    pipeline.run_layer(bt, b, pool_begin=begin, max_pools=3)
+    torch.cuda.synchronize()
+    _assert_same_outputs(a, b)
+    # complete pools follow the recompressed ones: flagged by both forms alike
+    assert int(a.status.item()) == ops.DEV_POOL_UNCOVERED
+    o = oracle_inputs(bt)
+    par.check_compress(o, a)
+    par.check_scores(o, a)
+    par.check_topk(a, geo.select_k)
 
 
 def test_decode_layer_parity_against_the_oracle():
