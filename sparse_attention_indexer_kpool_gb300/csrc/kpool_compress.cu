@@ -14,12 +14,17 @@
 // the pooled key is written with one vector store per lane.  HBM-bound: a full
 // build streams 2 * D * sizeof(act) bytes per token and writes D * sizeof(act)
 // / kpool bytes per token.
+#include <mutex>
+
 #include "dsa_internal.cuh"
 
 namespace dsa {
 namespace {
 
 constexpr int kWarpsPerCta = 8;
+// softmax weights as 2^((l - max) log2 e): e^x in the form the special-function
+// unit evaluates (the same expression in every compress kernel, so they agree)
+constexpr float kLog2e = 1.4426950408889634f;
 
 template <typename T, int V>
 struct Vec;  // V consecutive activation values
@@ -243,7 +248,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
 #pragma unroll
     for (int s = 0; s < kKpoolMax; ++s) {
       if (s < kpool) {
-        const float e = expf(lg[s][i] - m);
+        const float e = exp2f((lg[s][i] - m) * kLog2e);
         den += e;
         acc += e * kn[s][i];
       }
@@ -257,15 +262,30 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   }
 }
 
-// Bulk builds (a cache build, a prefill chunk's pools) in bf16 with D = 128: a
-// half-warp per pool, lane j owning channels [8j, 8j + 8) with 16-byte loads;
-// each CTA takes kWidePools consecutive pools of one sequence, so its metadata
-// loads and its first-valid-token scan serve all of them, and many pools'
-// rows are in flight per SM.  The LayerNorm statistics are reduced in the
-// order of the warp-per-pool kernel above (lane j holds that kernel's lanes 2j
-// and 2j + 1), so the two kernels write bit-identical keys.
-constexpr int kWidePools = 128;   // pools per CTA
+// Bulk builds (a cache build, a prefill chunk's pools) in bf16 with D = 128.
+// Each CTA takes kWidePools consecutive pools of one sequence, whose token rows
+// are one contiguous stretch of k and one of gate: a producer warp streams them
+// with 1-D bulk copies (TMA) into a ring of shared-memory stages of 16 pools,
+// while the 16 half-warps of the other eight warps compute one pool each per
+// stage (lane j owning channels
+// [8j, 8j + 8)) and write 16-byte key pieces.  The metadata loads and the
+// first-valid-token scan are shared by the CTA's pools.  The LayerNorm
+// statistics are reduced in the order of the warp-per-pool kernel above (lane
+// j holds that kernel's lanes 2j and 2j + 1), so the two kernels write
+// bit-identical keys.  Waits on the ring are bounded (DSA_DEV_TIMEOUT).
+constexpr int kWidePools = 256;   // pools per CTA
+constexpr int kStagePools = 16;   // pools per ring stage (one per half-warp)
 constexpr int kWideMin = 32;      // launches covering at least this many pools per sequence
+constexpr int kWideConsumers = 256;             // 8 warps, 16 half-warps
+constexpr int kWideThreads = kWideConsumers + 32;  // + the producer warp
+
+template <int KP>
+struct WideCfg {
+  static constexpr int kStageBytes = kStagePools * KP * 128 * 2;  // one array (k or gate)
+  static constexpr int kStages = 2;
+  static constexpr int kCtasPerSm = KP <= 4 ? 3 : 1;  // 64 KB of ring each at kpool <= 4
+  static constexpr size_t kSmem = 128 + (size_t)kStages * 2 * kStageBytes;
+};
 
 __device__ __forceinline__ float half_sum(float v, unsigned mask) {
 #pragma unroll
@@ -274,7 +294,7 @@ __device__ __forceinline__ float half_sum(float v, unsigned mask) {
 }
 
 template <int KP>  // slots held per pool (>= kpool)
-__global__ void __launch_bounds__(256, KP <= 4 ? 2 : 1)
+__global__ void __launch_bounds__(kWideThreads, WideCfg<KP>::kCtasPerSm)
     kpool_compress_wide_kernel(const __nv_bfloat16* __restrict__ k,
                                const __nv_bfloat16* __restrict__ gate,
                                const uint8_t* __restrict__ valid, const float* __restrict__ ape,
@@ -289,8 +309,14 @@ __global__ void __launch_bounds__(256, KP <= 4 ? 2 : 1)
                                int32_t* status) {
   constexpr int D = 128;
   using T = __nv_bfloat16;
+  using WC = WideCfg<KP>;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char* ring = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+  static_assert(kWidePools * KP <= 2048, "valid bytes on chip");
   __shared__ int s_min;
-  __shared__ float s_ape[KP * D];
+  __shared__ __align__(16) float s_ape[KP * D];
+  __shared__ uint8_t s_valid[kWidePools * KP];
+  __shared__ uint64_t full[4], empty[4];
   pdl_wait();
   pdl_launch_dependents();  // the next kernel may start its prologue
   const int b = blockIdx.y;
@@ -303,7 +329,14 @@ __global__ void __launch_bounds__(256, KP <= 4 ? 2 : 1)
   const int p_first = begin + blockIdx.x * kWidePools;
   if (!(p_first < end || blockIdx.x == 0)) return;  // nothing of this sequence here
   for (int i = threadIdx.x; i < kpool * D; i += blockDim.x) s_ape[i] = ape[i];
-  const int t0 = first_valid_token(valid + 0, lo, Tb, &s_min);  // (its barriers publish s_ape)
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < WC::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWideConsumers / 32);
+    }
+    fence_mbar_init();
+  }
+  const int t0 = first_valid_token(valid + 0, lo, Tb, &s_min);  // (its barriers publish the above)
   const int P = (Tb - t0) / kpool;
   const int P_eff = min(P, cap);
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -311,90 +344,162 @@ __global__ void __launch_bounds__(256, KP <= 4 ? 2 : 1)
     if (P > cap) flag(status, DSA_DEV_POOL_OVERFLOW);
     if (P_eff > end) flag(status, DSA_DEV_POOL_UNCOVERED);
   }
+  // this CTA's pools [pa, pb); the computed ones [pa, pc), sentinels after
+  const int pa = max(p_first, 0), pb = min(p_first + kWidePools, end);
+  const int pc = max(pa, min(pb, P_eff));
+  const int n_stages_work = (pc - pa + kStagePools - 1) / kStagePools;
   const int half = threadIdx.x >> 4, j = threadIdx.x & 15;
   const unsigned hmask = 0xffffu << (threadIdx.x & 16);
+  const size_t row_bytes = (size_t)D * 2;
+
+  if (threadIdx.x >= kWideConsumers) {
+    // ---- producer warp (lane 0): the rows of 16 pools per stage, k then gate
+    if (threadIdx.x != kWideConsumers) return;
+    int i = 0;
+    for (; i < n_stages_work; ++i) {
+      const int st = i % WC::kStages;
+      if (i >= WC::kStages &&
+          !mbar_wait_bounded(&empty[st], (uint32_t)((i / WC::kStages) - 1) & 1)) {
+        flag(status, DSA_DEV_TIMEOUT);
+        break;
+      }
+      const int p0 = pa + i * kStagePools, np = min(kStagePools, pc - p0);
+      const uint32_t bytes = (uint32_t)((size_t)np * kpool * row_bytes);
+      const long long row0 = lo + t0 + (long long)p0 * kpool;
+      unsigned char* sk = ring + (size_t)st * 2 * WC::kStageBytes;
+      mbar_arrive_expect_tx(&full[st], 2 * bytes);
+      bulk_g2s(sk, k + row0 * D, bytes, &full[st]);
+      bulk_g2s(sk + WC::kStageBytes, gate + row0 * D, bytes, &full[st]);
+    }
+    // never leave a copy in flight: wait for the last fills issued
+    for (int f = max(0, i - WC::kStages); f < i; ++f)
+      mbar_wait_bounded(&full[f % WC::kStages], (uint32_t)(f / WC::kStages) & 1);
+    return;
+  }
+  // the valid bytes of every slot of the computed pools, once per CTA
+  const long long tok0 = lo + t0 + (long long)pa * kpool;
+  for (int i = threadIdx.x; i < (pc - pa) * kpool; i += kWideConsumers) s_valid[i] = valid[tok0 + i];
+  asm volatile("bar.sync 1, %0;" ::"n"(kWideConsumers) : "memory");  // the consumer warps
   float g[8], be[8];
   Vec<T, 8>::load(ln_gamma + j * 8, g);
   Vec<T, 8>::load(ln_beta + j * 8, be);
-  const int p_end = min(p_first + kWidePools, end);
-  for (int p = p_first + half; p < p_end; p += blockDim.x / 16) {
-    if (p < 0) continue;
-    T* out = pool_keys + (cap_lo + p) * D + j * 8;
-    if (p >= P_eff) {  // sentinel entry
-      *reinterpret_cast<uint4*>(out) = make_uint4(0u, 0u, 0u, 0u);
-      if (j == 0) {
-        pool_start[cap_lo + p] = -1;
-        pool_valid[cap_lo + p] = 0;
-      }
-      continue;
-    }
-    const long long s0 = lo + t0 + (long long)p * kpool;
-    float kn[KP][8], lg[KP][8];
-    bool all_valid = true;
-#pragma unroll
-    for (int s = 0; s < KP; ++s) {
-      if (s < kpool) {
-        Vec<T, 8>::load(k + (s0 + s) * D + j * 8, kn[s]);
-        Vec<T, 8>::load(gate + (s0 + s) * D + j * 8, lg[s]);
-        all_valid &= valid[s0 + s] != 0;
-      }
-    }
-#pragma unroll
-    for (int s = 0; s < KP; ++s) {
-      if (s < kpool) {
-        // the warp-per-pool kernel's lane partials (4 channels each), its tree
-        float sa = 0.f, sb = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) sa += kn[s][i];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) sb += kn[s][4 + i];
-        sa = half_sum(sa, hmask);
-        sb = half_sum(sb, hmask);
-        const float mean = (sa + sb) * (1.0f / D);
-        float qa = 0.f, qb = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float dx = kn[s][i] - mean;
-          qa += dx * dx;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float dx = kn[s][4 + i] - mean;
-          qb += dx * dx;
-        }
-        qa = half_sum(qa, hmask);
-        qb = half_sum(qb, hmask);
-        const float var = (qa + qb) * (1.0f / D);
-        const float rstd = 1.0f / sqrtf(var + ln_eps);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          kn[s][i] = Act<T>::round((kn[s][i] - mean) * rstd * g[i] + be[i]);
-          lg[s][i] = lg[s][i] + s_ape[s * D + j * 8 + i];
-        }
-      }
-    }
-    float res[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float m = lg[0][i];
-#pragma unroll
-      for (int s = 1; s < KP; ++s)
-        if (s < kpool) m = fmaxf(m, lg[s][i]);
-      float den = 0.f, acc = 0.f;
+  bool ok = true;
+  for (int i = 0; i < n_stages_work; ++i) {
+    const int st = i % WC::kStages;
+    ok = ok && mbar_wait_bounded(&full[st], (uint32_t)(i / WC::kStages) & 1);
+    const int p = pa + i * kStagePools + half;
+    if (ok && p < pc) {
+      // this pool's slot rows in the stage: k at sk, gate at sk + kStageBytes
+      unsigned char* sk = ring + (size_t)st * 2 * WC::kStageBytes +
+                          (size_t)half * kpool * row_bytes + j * 16;
+      // 1. LayerNorm of each slot, in the warp-per-pool kernel's order (its
+      // lanes 2j and 2j + 1); the bf16-rounded result replaces the row in place
 #pragma unroll
       for (int s = 0; s < KP; ++s) {
         if (s < kpool) {
-          const float e = expf(lg[s][i] - m);
-          den += e;
-          acc += e * kn[s][i];
+          float kn[8];
+          const uint4 a = *reinterpret_cast<const uint4*>(sk + s * row_bytes);
+          const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            kn[2 * u] = bf16lo(av[u]);
+            kn[2 * u + 1] = bf16hi(av[u]);
+          }
+          float sa = 0.f, sb = 0.f;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) sa += kn[c];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) sb += kn[4 + c];
+          sa = half_sum(sa, hmask);
+          sb = half_sum(sb, hmask);
+          const float mean = (sa + sb) * (1.0f / D);
+          float qa = 0.f, qb = 0.f;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float dx = kn[c] - mean;
+            qa += dx * dx;
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float dx = kn[4 + c] - mean;
+            qb += dx * dx;
+          }
+          qa = half_sum(qa, hmask);
+          qb = half_sum(qb, hmask);
+          const float var = (qa + qb) * (1.0f / D);
+          const float rstd = 1.0f / sqrtf(var + ln_eps);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) kn[c] = Act<T>::round((kn[c] - mean) * rstd * g[c] + be[c]);
+          *reinterpret_cast<uint4*>(sk + s * row_bytes) =
+              make_uint4(pack_bf16(kn[0], kn[1]), pack_bf16(kn[2], kn[3]),
+                         pack_bf16(kn[4], kn[5]), pack_bf16(kn[6], kn[7]));
         }
       }
-      res[i] = acc / den;
+      // 2. per channel, the softmax over the slots of gate + ape weighs the
+      // normalised rows (the logits are formed again in the second pass)
+      auto logits = [&](int s, float (&l)[8]) {
+        const uint4 c4 = *reinterpret_cast<const uint4*>(sk + WC::kStageBytes + s * row_bytes);
+        const float4 a0 = *reinterpret_cast<const float4*>(s_ape + s * D + j * 8);
+        const float4 a1 = *reinterpret_cast<const float4*>(s_ape + s * D + j * 8 + 4);
+        l[0] = bf16lo(c4.x) + a0.x;
+        l[1] = bf16hi(c4.x) + a0.y;
+        l[2] = bf16lo(c4.y) + a0.z;
+        l[3] = bf16hi(c4.y) + a0.w;
+        l[4] = bf16lo(c4.z) + a1.x;
+        l[5] = bf16hi(c4.z) + a1.y;
+        l[6] = bf16lo(c4.w) + a1.z;
+        l[7] = bf16hi(c4.w) + a1.w;
+      };
+      float m[8], den[8], acc[8];
+      logits(0, m);
+#pragma unroll
+      for (int s = 1; s < KP; ++s) {
+        if (s < kpool) {
+          float l[8];
+          logits(s, l);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) m[c] = fmaxf(m[c], l[c]);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) den[c] = acc[c] = 0.f;
+#pragma unroll
+      for (int s = 0; s < KP; ++s) {
+        if (s < kpool) {
+          float l[8];
+          logits(s, l);
+          const uint4 a = *reinterpret_cast<const uint4*>(sk + s * row_bytes);
+          const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float kv = (c & 1) ? bf16hi(av[c >> 1]) : bf16lo(av[c >> 1]);
+            const float e = exp2f((l[c] - m[c]) * kLog2e);
+            den[c] += e;
+            acc[c] += e * kv;
+          }
+        }
+      }
+      float res[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) res[c] = acc[c] / den[c];
+      Vec<T, 8>::store(pool_keys + (cap_lo + p) * D + j * 8, res);
+      if (j == 0) {
+        bool all_valid = true;
+        for (int s = 0; s < kpool; ++s) all_valid &= s_valid[(p - pa) * kpool + s] != 0;
+        pool_start[cap_lo + p] = t0 + p * kpool;
+        pool_valid[cap_lo + p] = all_valid ? 1 : 0;
+      }
     }
-    Vec<T, 8>::store(out, res);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive1(&empty[st]);  // this warp is done with the stage
+  }
+  if (!ok && (threadIdx.x & 31) == 0) flag(status, DSA_DEV_TIMEOUT);
+  // sentinels: pools of the range past the complete ones
+  for (int p = pc + half; p < pb; p += kWideConsumers / 16) {
+    *reinterpret_cast<uint4*>(pool_keys + (cap_lo + p) * D + j * 8) = make_uint4(0u, 0u, 0u, 0u);
     if (j == 0) {
-      pool_start[cap_lo + p] = t0 + p * kpool;
-      pool_valid[cap_lo + p] = all_valid ? 1 : 0;
+      pool_start[cap_lo + p] = -1;
+      pool_valid[cap_lo + p] = 0;
     }
   }
 }
@@ -405,9 +510,15 @@ int launch_wide(const void* k, const void* gate, const uint8_t* valid, const flo
                 const int32_t* begin, int B, int kpool, int max_pools, void* pk, int32_t* ps,
                 uint8_t* pv, int32_t* np, int32_t* st, cudaStream_t stream) {
   using T = __nv_bfloat16;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(kpool_compress_wide_kernel<KP>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)WideCfg<KP>::kSmem);
+  });
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((max_pools + kWidePools - 1) / kWidePools, B, 1);
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.blockDim = dim3(kWideThreads, 1, 1);
+  cfg.dynamicSmemBytes = WideCfg<KP>::kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
