@@ -26,6 +26,38 @@ constexpr int kWarpsPerCta = 8;
 // unit evaluates (the same expression in every compress kernel, so they agree)
 constexpr float kLog2e = 1.4426950408889634f;
 
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32, a few ulp); the
+// arguments here are <= 0, and a result below 2^-126 flushes to zero: a slot
+// weight that small is lost against the largest slot's weight of 1
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// sum of N channel values, left to right
+template <int N>
+__device__ __forceinline__ float lane_sum(const float* x) {
+  float v = x[0];
+#pragma unroll
+  for (int i = 1; i < N; ++i) v = v + x[i];
+  return v;
+}
+// sum of squares of N channel values, left to right
+template <int N>
+__device__ __forceinline__ float lane_sq(const float* x) {
+  float v = x[0] * x[0];
+#pragma unroll
+  for (int i = 1; i < N; ++i) v = fmaf(x[i], x[i], v);
+  return v;
+}
+// warp sum: lanes 2j and 2j + 1 first, then across the pairs
+__device__ __forceinline__ float pair_first_warp_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+#pragma unroll
+  for (int o = 16; o > 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 template <typename T, int V>
 struct Vec;  // V consecutive activation values
 template <>
@@ -215,46 +247,45 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
       all_valid &= valid[s0 + s] != 0;
     }
   }
+  // logits, their per-channel maximum over the slots
+#pragma unroll
+  for (int s = 0; s < kKpoolMax; ++s)
+    if (s < kpool)
+#pragma unroll
+      for (int i = 0; i < V; ++i) lg[s][i] = lg[s][i] + ap[s][i];
+  float m[V], den[V], acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    m[i] = lg[0][i];
+#pragma unroll
+    for (int s = 1; s < kKpoolMax; ++s)
+      if (s < kpool) m[i] = fmaxf(m[i], lg[s][i]);
+    den[i] = acc[i] = 0.f;
+  }
+  // per slot: LayerNorm (statistics summed over the lane's channels, then the
+  // lane pair, then the warp: the order of the bulk kernel below), the
+  // normalised row rounded to the activation dtype, and its softmax weight
 #pragma unroll
   for (int s = 0; s < kKpoolMax; ++s) {
     if (s < kpool) {
-      float sum = 0.f;
+      const float mean = pair_first_warp_sum(lane_sum<V>(kn[s])) * (1.0f / D);
+      float dx[V];
 #pragma unroll
-      for (int i = 0; i < V; ++i) sum += kn[s][i];
-      const float mean = warp_sum(sum) * (1.0f / D);
-      float sq = 0.f;
-#pragma unroll
-      for (int i = 0; i < V; ++i) {
-        const float dx = kn[s][i] - mean;
-        sq += dx * dx;
-      }
-      const float var = warp_sum(sq) * (1.0f / D);
-      const float rstd = 1.0f / sqrtf(var + ln_eps);
+      for (int i = 0; i < V; ++i) dx[i] = kn[s][i] - mean;
+      const float var = pair_first_warp_sum(lane_sq<V>(dx)) * (1.0f / D);
+      const float rstd = rsqrtf(var + ln_eps);
 #pragma unroll
       for (int i = 0; i < V; ++i) {
-        kn[s][i] = Act<T>::round((kn[s][i] - mean) * rstd * g[i] + be[i]);
-        lg[s][i] = lg[s][i] + ap[s][i];
+        const float y = Act<T>::round(fmaf(dx[i] * rstd, g[i], be[i]));
+        const float e = exp2_approx((lg[s][i] - m[i]) * kLog2e);
+        den[i] += e;
+        acc[i] = fmaf(e, y, acc[i]);
       }
     }
   }
   float res[V];
 #pragma unroll
-  for (int i = 0; i < V; ++i) {
-    float m = lg[0][i];
-#pragma unroll
-    for (int s = 1; s < kKpoolMax; ++s)
-      if (s < kpool) m = fmaxf(m, lg[s][i]);
-    float den = 0.f, acc = 0.f;
-#pragma unroll
-    for (int s = 0; s < kKpoolMax; ++s) {
-      if (s < kpool) {
-        const float e = exp2f((lg[s][i] - m) * kLog2e);
-        den += e;
-        acc += e * kn[s][i];
-      }
-    }
-    res[i] = acc / den;
-  }
+  for (int i = 0; i < V; ++i) res[i] = __fdividef(acc[i], den[i]);  // den in [1, kpool]
   Vec<T, V>::store(out, res);
   if (lane == 0) {
     pool_start[cap_lo + p] = t0 + p * kpool;
@@ -392,51 +423,7 @@ __global__ void __launch_bounds__(kWideThreads, WideCfg<KP>::kCtasPerSm)
       // this pool's slot rows in the stage: k at sk, gate at sk + kStageBytes
       unsigned char* sk = ring + (size_t)st * 2 * WC::kStageBytes +
                           (size_t)half * kpool * row_bytes + j * 16;
-      // 1. LayerNorm of each slot, in the warp-per-pool kernel's order (its
-      // lanes 2j and 2j + 1); the bf16-rounded result replaces the row in place
-#pragma unroll
-      for (int s = 0; s < KP; ++s) {
-        if (s < kpool) {
-          float kn[8];
-          const uint4 a = *reinterpret_cast<const uint4*>(sk + s * row_bytes);
-          const uint32_t av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            kn[2 * u] = bf16lo(av[u]);
-            kn[2 * u + 1] = bf16hi(av[u]);
-          }
-          float sa = 0.f, sb = 0.f;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) sa += kn[c];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) sb += kn[4 + c];
-          sa = half_sum(sa, hmask);
-          sb = half_sum(sb, hmask);
-          const float mean = (sa + sb) * (1.0f / D);
-          float qa = 0.f, qb = 0.f;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float dx = kn[c] - mean;
-            qa += dx * dx;
-          }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float dx = kn[4 + c] - mean;
-            qb += dx * dx;
-          }
-          qa = half_sum(qa, hmask);
-          qb = half_sum(qb, hmask);
-          const float var = (qa + qb) * (1.0f / D);
-          const float rstd = 1.0f / sqrtf(var + ln_eps);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) kn[c] = Act<T>::round((kn[c] - mean) * rstd * g[c] + be[c]);
-          *reinterpret_cast<uint4*>(sk + s * row_bytes) =
-              make_uint4(pack_bf16(kn[0], kn[1]), pack_bf16(kn[2], kn[3]),
-                         pack_bf16(kn[4], kn[5]), pack_bf16(kn[6], kn[7]));
-        }
-      }
-      // 2. per channel, the softmax over the slots of gate + ape weighs the
-      // normalised rows (the logits are formed again in the second pass)
+      // the slot logits gate + ape of the pool's 8 channels of this lane
       auto logits = [&](int s, float (&l)[8]) {
         const uint4 c4 = *reinterpret_cast<const uint4*>(sk + WC::kStageBytes + s * row_bytes);
         const float4 a0 = *reinterpret_cast<const float4*>(s_ape + s * D + j * 8);
@@ -450,6 +437,7 @@ __global__ void __launch_bounds__(kWideThreads, WideCfg<KP>::kCtasPerSm)
         l[6] = bf16lo(c4.w) + a1.z;
         l[7] = bf16hi(c4.w) + a1.w;
       };
+      // 1. the per-channel maximum of the logits over the slots
       float m[8], den[8], acc[8];
       logits(0, m);
 #pragma unroll
@@ -463,25 +451,46 @@ __global__ void __launch_bounds__(kWideThreads, WideCfg<KP>::kCtasPerSm)
       }
 #pragma unroll
       for (int c = 0; c < 8; ++c) den[c] = acc[c] = 0.f;
+      // 2. per slot: the LayerNorm of the k row (statistics in the warp-per-pool
+      // kernel's order: lane j holds its lanes 2j and 2j + 1), rounded to bf16,
+      // weighed by the softmax weight (the logits are formed again)
 #pragma unroll
       for (int s = 0; s < KP; ++s) {
         if (s < kpool) {
-          float l[8];
-          logits(s, l);
+          float x[8], dx[8], l[8];
           const uint4 a = *reinterpret_cast<const uint4*>(sk + s * row_bytes);
           const uint32_t av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const float kv = (c & 1) ? bf16hi(av[c >> 1]) : bf16lo(av[c >> 1]);
-            const float e = exp2f((l[c] - m[c]) * kLog2e);
-            den[c] += e;
-            acc[c] += e * kv;
+          for (int u = 0; u < 4; ++u) {
+            x[2 * u] = bf16lo(av[u]);
+            x[2 * u + 1] = bf16hi(av[u]);
+          }
+          const float mean =
+              half_sum(lane_sum<4>(x) + lane_sum<4>(x + 4), hmask) * (1.0f / D);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) dx[c] = x[c] - mean;
+          const float var = half_sum(lane_sq<4>(dx) + lane_sq<4>(dx + 4), hmask) * (1.0f / D);
+          const float rstd = rsqrtf(var + ln_eps);
+          logits(s, l);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            // the normalised pair rounded to bf16 (round to nearest even)
+            const uint32_t yy = pack_bf16(fmaf(dx[2 * u] * rstd, g[2 * u], be[2 * u]),
+                                          fmaf(dx[2 * u + 1] * rstd, g[2 * u + 1], be[2 * u + 1]));
+            const float y[2] = {bf16lo(yy), bf16hi(yy)};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int c = 2 * u + h;
+              const float e = exp2_approx((l[c] - m[c]) * kLog2e);
+              den[c] += e;
+              acc[c] = fmaf(e, y[h], acc[c]);
+            }
           }
         }
       }
       float res[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) res[c] = acc[c] / den[c];
+      for (int c = 0; c < 8; ++c) res[c] = __fdividef(acc[c], den[c]);  // den in [1, kpool]
       Vec<T, 8>::store(pool_keys + (cap_lo + p) * D + j * 8, res);
       if (j == 0) {
         bool all_valid = true;
