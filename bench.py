@@ -55,13 +55,16 @@ def parse():
                          "N_QUERY_SETS seeded sets, so consecutive steps select different rows)")
     ap.add_argument("--breakdown", action="store_true",
                     help="diagnostic: per-stage in-graph times (extra events between stages)")
-    ap.add_argument("--leg", choices=["prefill_index", "prefill_attention", "paged_attention"],
+    ap.add_argument("--leg", choices=["prefill_index", "prefill_attention", "paged_attention",
+                                      "projections"],
                     help="run only this side measurement and print its JSON object (for "
                          "profiling one kernel without the decode step)")
     ap.add_argument("--no-paged", action="store_true",
                     help="skip the paged / E4M3 attention leg")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the prefill-chunk scoring measurement")
+    ap.add_argument("--no-projections", action="store_true",
+                    help="skip the projection leg (hidden state -> the path's inputs)")
     return ap.parse_args()
 
 
@@ -282,6 +285,91 @@ def prefill_attention(peaks_path, reps=5):
             "us": round(us, 1), "flops": flops, "tflops": round(tf, 1), "bound": "tensor",
             "peak_tflops": peak, "frac": round(tf / peak, 4),
             "timing": "median of %d calls, L2 flushed before each" % reps}
+
+
+def projections(peaks_path, reps=20):
+    """The projections before the selection (dsa_indexer_project: hidden state
+    and query latent to k, gate, weights, q, q_nope and the latent-space
+    query) at the full-size shapes (hidden 6144, query latent 2048, 32 index
+    heads of 128, 64 MLA heads with a 192-wide no-rope part, latent 512;
+    random-init weights):
+    * decode: 4 tokens per layer, 11 layers of distinct weights (915 MB, past
+      the L2) called back to back from a CUDA graph: a weight stream, against
+      HBM;
+    * prefill: one 4096-token chunk, L2 flushed before every call: against the
+      bf16 tensor peak."""
+    import torch
+
+    from sparse_attention_indexer_kpool_gb300 import pipeline, synth
+    g = synth.PROJ_MAIN
+    scale = g["H"] ** -0.5
+    hbm = json.load(open(peaks_path))["hbm_gbs"] if os.path.exists(peaks_path) else 6800.0
+    peak = json.load(open(peaks_path))["bf16_tflops"] if os.path.exists(peaks_path) else 1900.0
+    M1, M2 = 2 * g["D"] + g["H"], g["H"] * g["D"] + g["Hm"] * g["nope"]
+
+    def act_bytes(T):  # activations in, outputs out, q_nope written and read back
+        return 2 * T * (g["hidden"] + g["q_rank"] + 2 * g["D"] + g["H"] * g["D"]
+                        + 2 * g["Hm"] * g["nope"] + g["Hm"] * g["L"]) + 4 * T * g["H"]
+
+    w_bytes = 2 * (M1 * g["hidden"] + M2 * g["q_rank"] + g["Hm"] * g["L"] * g["nope"])
+    pis = [synth.projection_inputs(4, **g, device="cuda", seed=5000 + 100 * l)
+           for l in range(N_LAYERS)]
+    bufs = [pipeline.ProjectionBuffers.alloc(pi) for pi in pis]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):          # warm-up off the default stream, as for capture
+        for _ in range(3):
+            for pi, b in zip(pis, bufs):
+                pipeline.project(pi, b, scale)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()         # one decode step's projections, 11 layers
+    with torch.cuda.graph(graph):
+        for pi, b in zip(pis, bufs):
+            pipeline.project(pi, b, scale)
+    graph.replay()
+    torch.cuda.synchronize()
+    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        graph.replay()
+    b_.record()
+    torch.cuda.synchronize()
+    assert all(int(b.status.item()) == 0 for b in bufs)
+    dec_us = a.elapsed_time(b_) * 1e3 / (reps * N_LAYERS)
+    dec_bytes = w_bytes + act_bytes(4)
+    dec_gbs = dec_bytes / (dec_us * 1e-6) / 1e9
+    del pis, bufs
+    T = 4096
+    pi = synth.projection_inputs(T, **g, device="cuda", seed=6000)
+    buf = pipeline.ProjectionBuffers.alloc(pi)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        pipeline.project(pi, buf, scale)
+    times = []
+    for _ in range(max(3, reps // 4)):
+        flush.fill_(1)
+        a.record()
+        pipeline.project(pi, buf, scale)
+        b_.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b_))
+    assert int(buf.status.item()) == 0
+    pre_us = statistics.median(times) * 1e3
+    flops = 2.0 * T * (M1 * g["hidden"] + M2 * g["q_rank"] + g["Hm"] * g["L"] * g["nope"])
+    tf = flops / (pre_us * 1e-6) / 1e12
+    return {"kernel": "proj_gemm_kernel (tcgen05, 128 output features x 16/64/128/256 tokens "
+                      "per tile, split contraction below two CTAs per SM)",
+            "shapes": dict(g),
+            "decode": {"tokens": 4, "layers": N_LAYERS, "us_per_layer": round(dec_us, 2),
+                       "bytes_per_layer": dec_bytes, "gbs": round(dec_gbs, 1), "bound": "hbm",
+                       "peak_gbs": hbm, "frac": round(dec_gbs / hbm, 4),
+                       "timing": "%d replays of a CUDA graph of %d calls, one per layer"
+                                 % (reps, N_LAYERS)},
+            "prefill": {"tokens": T, "us": round(pre_us, 1), "flops": flops,
+                        "tflops": round(tf, 1), "bound": "tensor", "peak_tflops": peak,
+                        "frac": round(tf / peak, 4),
+                        "timing": "median of %d calls, L2 flushed before each" % len(times)}}
 
 
 def paged_attention(reps=20, page_size=64):
@@ -650,6 +738,8 @@ def run_ours(args, dist):
         out["prefill_attention"] = prefill_attention(peaks_path)
     if not args.no_paged:
         out["paged_attention"] = paged_attention()
+    if not args.no_projections:
+        out["projections"] = projections(peaks_path)
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(layers[0], args.cpu_seconds)
     if dist.rank == 0:
@@ -908,7 +998,8 @@ def main():
             peaks = os.path.join(ROOT, "MEASURED_PEAKS.json")
             legs = {"prefill_index": lambda: prefill_index(peaks),
                     "prefill_attention": lambda: prefill_attention(peaks),
-                    "paged_attention": paged_attention}
+                    "paged_attention": paged_attention,
+                    "projections": lambda: projections(peaks)}
             print(json.dumps({args.leg: legs[args.leg]()}), flush=True)
         elif args.impl == "reference":
             run_reference(args, dist)

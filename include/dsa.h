@@ -392,6 +392,58 @@ size_t dsa_decode_layer_workspace_size(const dsa_decode_layer_args* args, size_t
                                        size_t* ws_mla);
 
 /*
+ * dsa_indexer_project - the per-token projections that feed the path: the
+ * indexer key, its slot logits and head weights from the hidden state, the
+ * indexer query and the MLA no-rope query from the query latent, and the
+ * latent-space MLA query (module glm5next_dsa, Modules: build and layer, the
+ * DSA block's tensors; Traps carried from Slice 8: NoPE, no rotary part).
+ * The pages name these tensors but print no formula; the library takes them
+ * as plain bias-free linear maps, every output feature f of token t being
+ *   out[t, f] = alpha * sum_k W[f, k] * in[t, k]     (fp32 accumulation)
+ *
+ *   x      [T, hidden]  bf16   hidden states of the T tokens
+ *   w_kgw  [2D + H, hidden] bf16  rows 0..D-1 -> k, D..2D-1 -> gate,
+ *                              2D..2D+H-1 -> weights (alpha = weights_scale)
+ *   cq     [T, q_rank]  bf16   query latent of the T tokens
+ *   w_q    [H*D + Hm*nope, q_rank] bf16  rows 0..H*D-1 -> q (head h owns
+ *                              rows h*D..h*D+D-1), the rest -> q_nope
+ *   w_uk_t [Hm, L, nope] bf16  per MLA head, the key up-projection W_uk_h
+ *                              ([nope, L]) stored transposed (a load-time
+ *                              re-layout): q_lat[t, h, l] =
+ *                              sum_n q_nope[t, h, n] * W_uk_h[n, l], so that
+ *                              <q_lat_h, c> = <q_nope_h, W_uk_h c> for a latent
+ *                              cache row c.
+ * Outputs (bf16 unless stated; every element of every token is written):
+ *   k_out, gate_out [rows, D]: token t to row kv_rows[t] (kv_rows NULL: row t;
+ *                   a negative entry drops the token), e.g. straight into the
+ *                   key and gate caches that dsa_kpool_compress reads
+ *   weights_out     [T, H] fp32
+ *   q_out           [T, H, D]
+ *   q_nope_out      [T, Hm, nope] (also the input of the latent projection)
+ *   q_lat_out       [T, Hm, L]
+ * Sizes: hidden and q_rank multiples of 8, nope a multiple of 64.
+ * Alignment: x, w_kgw, cq, w_q, w_uk_t, q_nope_out and the workspace on 16
+ * bytes; bf16 outputs on 2, weights_out, kv_rows and status_dev on 4.
+ * Workspace: dsa_indexer_project_workspace_size bytes (0: none needed).  Its
+ * first bytes are counters that must be ZERO before the first call that uses
+ * the workspace; every call leaves them zero.  Calls that share a workspace
+ * must not overlap on the GPU.
+ * Outputs are deterministic: a contraction split across CTAs is added in split
+ * order whatever order the CTAs finish in.
+ * Device faults: DSA_DEV_TIMEOUT (outputs unspecified).
+ * Returns DSA_ERR_UNSUPPORTED for sizes outside the above, DSA_ERR_WORKSPACE
+ * for a missing or short workspace; T == 0 is a no-op.
+ */
+int dsa_indexer_project(const void* x, const void* w_kgw, const void* cq, const void* w_q,
+                        const void* w_uk_t, int T, int hidden, int q_rank, int H, int D, int Hm,
+                        int nope, int L, float weights_scale, const int32_t* kv_rows,
+                        void* k_out, void* gate_out, float* weights_out, void* q_out,
+                        void* q_nope_out, void* q_lat_out, void* workspace, size_t ws_bytes,
+                        int32_t* status_dev, void* stream);
+size_t dsa_indexer_project_workspace_size(int T, int hidden, int q_rank, int H, int D, int Hm,
+                                          int nope, int L);
+
+/*
  * dsa_set_failure_drill - arm (DSA_DRILL_SKIP_ARM) or disarm (0) a drill of
  * the kernels' give-up path, for tests of failure detection.
  *

@@ -37,7 +37,9 @@ Readings where the pages are silent: LayerNorm uses the population variance and 
 [kpool, D] fp32 bias added to the gate logits per slot and channel; the causal
 rule counts a pool when its last token is at or before the query position; the
 attention output stays in latent space with an explicit softmax scale; an empty
-selection gives out = 0, lse = -inf.
+selection gives out = 0, lse = -inf.  The projections before a1 (hidden state
+and query latent to k, gate, weights, q and the latent-space query) are
+bias-free linear maps: the pages name the tensors but give no formula.
 
 The paged-cache attention (the pages' paged decode and its fp8 variant) reads
 its rows through a block table and decodes E4M3 codes with one fp32 scale per
@@ -439,6 +441,69 @@ def mla_paged_decode(q_lat, pages, row_scale, kv_dtype: str, block_table, seq_le
             raise ValueError(f"unknown kv dtype {kv_dtype!r}")
         out[i], lse[i] = attend_rows(q_lat[i], C, sm_scale)
     return round_store(out, dtype), lse, status
+
+
+# --------------------------------------------------------------------------
+# the projections before a1: hidden state / query latent -> the path's inputs
+# --------------------------------------------------------------------------
+def linear(inp, w, alpha: float = 1.0) -> np.ndarray:
+    """out[t, f] = alpha * sum_k w[f, k] * inp[t, k], exactly (float64, no bias).
+
+    Module glm5next_dsa, Modules: build and layer name the block's projection
+    tensors but print no formula; a bias-free linear map is the plain reading.
+    """
+    inp = np.asarray(inp, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    return alpha * (inp @ w.T)
+
+
+def absorb_query(q_nope, w_uk_t) -> np.ndarray:
+    """Latent-space MLA query: q_lat[t, h, l] = sum_n q_nope[t, h, n] * W_uk_h[n, l].
+
+    ``w_uk_t[h]`` is W_uk_h transposed ([L, nope]).  With the key up-projection
+    k_h = W_uk_h c of a latent row c, <q_nope_h, k_h> = <q_lat_h, c>: the
+    attention scores the latent cache directly (module glm5next_dsa, the NoPE MLA
+    over the selected tokens, whose output stays in latent space).
+    """
+    q_nope = np.asarray(q_nope, dtype=np.float64)
+    w_uk_t = np.asarray(w_uk_t, dtype=np.float64)
+    T, Hm, nope = q_nope.shape
+    out = np.zeros((T, Hm, w_uk_t.shape[1]))
+    for h in range(Hm):
+        out[:, h, :] = q_nope[:, h, :] @ w_uk_t[h].T
+    return out
+
+
+def indexer_project(x, w_kgw, cq, w_q, w_uk_t, H: int, D: int, Hm: int, nope: int,
+                    weights_scale: float, rounded: bool = True) -> dict:
+    """The per-token inputs of the path from a layer's activations.
+
+    * x [T, hidden] through w_kgw [2D + H, hidden]: rows 0..D-1 give the indexer
+      key k (LayerNorm'ed later by kpool_compress), rows D..2D-1 its slot-logit
+      gate, rows 2D.. the per-head weights, times ``weights_scale``;
+    * the query latent cq [T, q_rank] through w_q [H*D + Hm*nope, q_rank]: the
+      indexer query (head h from rows h*D..h*D+D-1), then the MLA no-rope query;
+    * the no-rope query through the transposed key up-projection (absorb_query).
+
+    With ``rounded`` the stored outputs are rounded as the library stores them:
+    bf16 for k, gate, q, q_nope and q_lat, fp32 for the weights; q_lat is then
+    computed from the stored (bf16) q_nope, the tensor the latent projection reads.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    T = x.shape[0]
+    hid = linear(x, w_kgw)
+    k, gate = hid[:, :D], hid[:, D:2 * D]
+    weights = weights_scale * hid[:, 2 * D:2 * D + H]
+    qq = linear(cq, w_q)
+    q = qq[:, :H * D].reshape(T, H, D)
+    q_nope = qq[:, H * D:H * D + Hm * nope].reshape(T, Hm, nope)
+    if rounded:
+        k, gate, q, q_nope = (round_bf16(a) for a in (k, gate, q, q_nope))
+        weights = round_f32(weights)
+    q_lat = absorb_query(q_nope, w_uk_t)
+    if rounded:
+        q_lat = round_bf16(q_lat)
+    return dict(k=k, gate=gate, weights=weights, q=q, q_nope=q_nope, q_lat=q_lat)
 
 
 # --------------------------------------------------------------------------

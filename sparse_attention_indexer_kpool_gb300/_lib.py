@@ -68,6 +68,9 @@ SIGNATURES = {
     "dsa_version": (c_int, []),
     "dsa_kernel_launches": (ctypes.c_uint64, []),
     "dsa_set_failure_drill": (c_int, [c_int]),
+    "dsa_indexer_project": (c_int, [c_void_p] * 5 + [c_int] * 8 + [c_float] + [c_void_p] * 8
+                            + [c_size_t] + [c_void_p] * 2),
+    "dsa_indexer_project_workspace_size": (c_size_t, [c_int] * 8),
 }
 
 

@@ -26,7 +26,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                      "--expt-relaxed-constexpr", "-Xptxas", "-v", "-I", INCLUDE]
 SOURCES = ["dsa_abi.cu", "kpool_compress.cu", "index_scores.cu", "index_scores_umma.cu",
-           "topk.cu", "mla_decode.cu", "mla_umma.cu", "select_noalloc.cu"]
+           "topk.cu", "mla_decode.cu", "mla_umma.cu", "select_noalloc.cu",
+           "indexer_proj.cu"]
 
 
 def _nvcc() -> str:

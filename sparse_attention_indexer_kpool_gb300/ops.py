@@ -266,6 +266,34 @@ def dsa_decode_layer(k, gate, valid, ape, ln_gamma, ln_beta, ln_eps, cu_seqlens,
     _check("dsa_decode_layer", _lib.load().dsa_decode_layer(ctypes.byref(a), _stream(stream)))
 
 
+def indexer_project_workspace_bytes(T, hidden, q_rank, H, D, Hm, nope, L) -> int:
+    return int(_lib.load().dsa_indexer_project_workspace_size(T, hidden, q_rank, H, D, Hm, nope,
+                                                              L))
+
+
+def dsa_indexer_project(x, w_kgw, cq, w_q, w_uk_t, weights_scale, k_out, gate_out, weights_out,
+                        q_out, q_nope_out, q_lat_out, workspace=None, kv_rows=None, status=None,
+                        stream=None):
+    """x [T, hidden], w_kgw [2D+H, hidden], cq [T, q_rank], w_q [H*D+Hm*nope, q_rank],
+    w_uk_t [Hm, L, nope] (bf16); outputs k_out/gate_out [rows, D], weights_out [T, H] fp32,
+    q_out [T, H, D], q_nope_out [T, Hm, nope], q_lat_out [T, Hm, L]."""
+    bf = torch.bfloat16
+    T, hidden = x.shape
+    q_rank = cq.shape[1]
+    Hm, L, nope = w_uk_t.shape
+    H, D = q_out.shape[1], q_out.shape[2]
+    code = _lib.load().dsa_indexer_project(
+        _ptr(x, bf, "x"), _ptr(w_kgw, bf, "w_kgw"), _ptr(cq, bf, "cq"), _ptr(w_q, bf, "w_q"),
+        _ptr(w_uk_t, bf, "w_uk_t"), T, hidden, q_rank, H, D, Hm, nope, L, float(weights_scale),
+        _ptr(kv_rows, torch.int32, "kv_rows"), _ptr(k_out, bf, "k_out"),
+        _ptr(gate_out, bf, "gate_out"), _ptr(weights_out, torch.float32, "weights_out"),
+        _ptr(q_out, bf, "q_out"), _ptr(q_nope_out, bf, "q_nope_out"),
+        _ptr(q_lat_out, bf, "q_lat_out"), _ptr(workspace, torch.uint8, "workspace"),
+        0 if workspace is None else workspace.numel(), _ptr(status, torch.int32, "status"),
+        _stream(stream))
+    _check("dsa_indexer_project", code)
+
+
 def dsa_kernel_launches() -> int:
     """Kernels the library has launched (or recorded into a stream capture) so far."""
     return int(_lib.load().dsa_kernel_launches())

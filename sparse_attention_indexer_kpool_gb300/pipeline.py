@@ -107,3 +107,41 @@ def run_layer(bt: Batch, buf: LayerBuffers, pool_begin=None, max_pools=None, str
     compress(bt, buf, pool_begin, max_pools, stream)
     (select if fused else select_stages)(bt, buf, stream)
     attend(bt, buf, stream)
+
+
+@dataclass
+class ProjectionBuffers:
+    """Outputs and workspace of dsa_indexer_project for one layer."""
+    k: torch.Tensor          # [rows, D] bf16 (rows = T, or the cache rows kv_rows points into)
+    gate: torch.Tensor       # [rows, D] bf16
+    weights: torch.Tensor    # [T, H] fp32
+    q: torch.Tensor          # [T, H, D] bf16
+    q_nope: torch.Tensor     # [T, Hm, nope] bf16
+    q_lat: torch.Tensor      # [T, Hm, L] bf16
+    ws: torch.Tensor | None  # counters zeroed here, left zero by every call
+    status: torch.Tensor
+
+    @staticmethod
+    def alloc(pi, rows=None, device=None) -> "ProjectionBuffers":
+        dev = device or pi.x.device
+        T, hidden = pi.x.shape
+        bf = torch.bfloat16
+        rows = T if rows is None else rows
+        ws = ops.indexer_project_workspace_bytes(T, hidden, pi.cq.shape[1], pi.H, pi.D, pi.Hm,
+                                                 pi.nope, pi.L)
+        return ProjectionBuffers(
+            k=torch.zeros(rows, pi.D, dtype=bf, device=dev),
+            gate=torch.zeros(rows, pi.D, dtype=bf, device=dev),
+            weights=torch.empty(T, pi.H, dtype=torch.float32, device=dev),
+            q=torch.empty(T, pi.H, pi.D, dtype=bf, device=dev),
+            q_nope=torch.empty(T, pi.Hm, pi.nope, dtype=bf, device=dev),
+            q_lat=torch.empty(T, pi.Hm, pi.L, dtype=bf, device=dev),
+            ws=torch.zeros(ws, dtype=torch.uint8, device=dev) if ws else None,
+            status=torch.zeros(1, dtype=torch.int32, device=dev))
+
+
+def project(pi, buf: ProjectionBuffers, weights_scale: float, kv_rows=None, stream=None):
+    """The indexer projections of one layer: k, gate, weights, q, q_nope, q_lat."""
+    ops.dsa_indexer_project(pi.x, pi.w_kgw, pi.cq, pi.w_q, pi.w_uk_t, weights_scale, buf.k,
+                            buf.gate, buf.weights, buf.q, buf.q_nope, buf.q_lat, buf.ws,
+                            kv_rows, buf.status, stream)

@@ -304,3 +304,39 @@ def paged_cache(kv, cu_seqlens, page_size: int, *, e4m3=False, seed=0, n_spare=3
         codes[dst[c0:c0 + (1 << 20)]] = (rows / s[:, None]).to(torch.float8_e4m3fn)
         scale[dst[c0:c0 + (1 << 20)]] = s
     return PagedCache(codes, scale.float(), table, seq_lens, page_size)
+
+
+@dataclass
+class ProjectionInputs:
+    """One layer's projection inputs (bf16): activations and random-init weights."""
+    x: torch.Tensor        # [T, hidden] hidden states
+    cq: torch.Tensor       # [T, q_rank] query latent
+    w_kgw: torch.Tensor    # [2D + H, hidden] rows of k, gate, weights
+    w_q: torch.Tensor      # [H*D + Hm*nope, q_rank] rows of q, then q_nope
+    w_uk_t: torch.Tensor   # [Hm, L, nope] key up-projection, transposed per head
+    H: int
+    D: int
+    Hm: int
+    nope: int
+    L: int
+
+
+# Shape assumptions for the projections at full size (the pages give the
+# indexer's 32 heads of 128 and the latent width 512, but no hidden size,
+# query-latent rank or no-rope head size)
+PROJ_MAIN = dict(hidden=6144, q_rank=2048, H=32, D=128, Hm=64, nope=192, L=512)
+
+
+def projection_inputs(T: int, hidden: int, q_rank: int, H: int, D: int, Hm: int, nope: int,
+                      L: int, *, device="cpu", seed=0) -> ProjectionInputs:
+    """Activations ~ N(0, 1); weights ~ N(0, 1/fan_in), so every output has
+    about unit scale."""
+    g = _gen(device, seed)
+    bf = torch.bfloat16
+    return ProjectionInputs(
+        x=_normal((T, hidden), 1.0, g, device, bf),
+        cq=_normal((T, q_rank), 1.0, g, device, bf),
+        w_kgw=_normal((2 * D + H, hidden), hidden ** -0.5, g, device, bf),
+        w_q=_normal((H * D + Hm * nope, q_rank), q_rank ** -0.5, g, device, bf),
+        w_uk_t=_normal((Hm, L, nope), nope ** -0.5, g, device, bf),
+        H=H, D=D, Hm=Hm, nope=nope, L=L)

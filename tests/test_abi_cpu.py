@@ -247,3 +247,31 @@ def test_decode_layer_validation(lib):
     assert s_sel.value == lib.dsa_select_workspace_size(4, 1000, 512)
     assert s_mla.value == lib.dsa_mla_selected_decode_workspace_size(4, 64, 512, 2048, 0)
     assert tot == s_sel.value + s_mla.value
+
+
+def test_indexer_project_validation(lib):
+    f = lib.dsa_indexer_project
+    def call(**kw):
+        a = dict(x=A, w=A, cq=A, wq=A, wuk=A, T=4, hidden=6144, q_rank=2048, H=32, D=128, Hm=64,
+                 nope=192, L=512, ws_scale=0.17, rows=None, k=A, g=A, w_out=A, q=A, qn=A, ql=A,
+                 ws=A, ws_bytes=1 << 30, st=None)
+        a.update(kw)
+        return f(a["x"], a["w"], a["cq"], a["wq"], a["wuk"], a["T"], a["hidden"], a["q_rank"],
+                 a["H"], a["D"], a["Hm"], a["nope"], a["L"], a["ws_scale"], a["rows"], a["k"],
+                 a["g"], a["w_out"], a["q"], a["qn"], a["ql"], a["ws"], a["ws_bytes"], a["st"],
+                 None)
+    size = lib.dsa_indexer_project_workspace_size
+    assert size(4, 6144, 2048, 32, 128, 64, 192, 512) > 0        # 4 tokens: split contractions
+    assert size(0, 6144, 2048, 32, 128, 64, 192, 512) == 0
+    assert call(nope=100) == ERR["DSA_ERR_UNSUPPORTED"]           # not whole 64-wide stages
+    assert call(hidden=6148) == ERR["DSA_ERR_UNSUPPORTED"]        # row stride not 16 bytes
+    assert call(H=0) == ERR["DSA_ERR_INVALID_ARG"]
+    assert call(ws_scale=float("nan")) == ERR["DSA_ERR_INVALID_ARG"]
+    assert call(x=None) == ERR["DSA_ERR_INVALID_ARG"]
+    assert call(x=A + 8) == ERR["DSA_ERR_MISALIGNED"]
+    assert call(w_out=A + 2) == ERR["DSA_ERR_MISALIGNED"]
+    assert call(ws=None, ws_bytes=0) == ERR["DSA_ERR_WORKSPACE"]
+    assert call(ws_bytes=16) == ERR["DSA_ERR_WORKSPACE"]
+    n = lib.dsa_kernel_launches()
+    assert call(T=0) == ERR["DSA_OK"]                             # no tokens: no-op
+    assert lib.dsa_kernel_launches() == n

@@ -48,6 +48,15 @@ MUTATIONS = {
     "fp8_subnormals_as_normals": ("np.where(e == 0, (m / 8.0) * 2.0 ** -6,",
                                   "np.where(e == 0, (1.0 + m / 8.0) * 2.0 ** -7,"),
     "fp8_row_scale_dropped": ("* np.asarray(row_scale, np.float64)[rows][:, None]", "* 1.0"),
+    "projection_transposed_weight": ("return alpha * (inp @ w.T)", "return alpha * (inp @ w)"),
+    "absorb_untransposed": ("out[:, h, :] = q_nope[:, h, :] @ w_uk_t[h].T",
+                            "out[:, h, :] = q_nope[:, h, :] @ w_uk_t[h]"),
+    "gate_rows_swapped_with_k": ("k, gate = hid[:, :D], hid[:, D:2 * D]",
+                                 "gate, k = hid[:, :D], hid[:, D:2 * D]"),
+    "weights_scale_dropped": ("weights = weights_scale * hid[:, 2 * D:2 * D + H]",
+                              "weights = hid[:, 2 * D:2 * D + H]"),
+    "q_lat_from_unrounded_query": ("k, gate, q, q_nope = (round_bf16(a) for a in (k, gate, q, q_nope))",
+                                   "k, gate, q = (round_bf16(a) for a in (k, gate, q))"),
 }
 
 

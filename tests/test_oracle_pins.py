@@ -558,3 +558,99 @@ def test_mla_paged_bad_page_and_bad_token_skip_the_row():
     got = oracle.mla_paged_decode(q, pages, None, "bf16", table, lengths, page_size, [0],
                                   np.array([[0, 5, 10, -1]]), 1.0, "f32")   # 10 >= seq_lens[0]
     assert got[2] == oracle.ST_BAD_TOKEN and np.array_equal(got[0], want[0])
+
+
+# ---------------------------------------------------------------- projections
+def _proj_case(rng, T=3, hidden=12, q_rank=10, H=2, D=4, Hm=3, nope=5, L=5):
+    g = lambda *s: oracle.round_bf16(rng.standard_normal(s))  # bf16-exact values
+    return dict(x=g(T, hidden), w_kgw=g(2 * D + H, hidden), cq=g(T, q_rank),
+                w_q=g(H * D + Hm * nope, q_rank), w_uk_t=g(Hm, L, nope), H=H, D=D, Hm=Hm,
+                nope=nope)
+
+
+def test_projection_of_unit_vectors_reads_weight_columns():
+    """A one-hot token selects one input column: the outputs are that column of
+    each weight block, exactly (bf16 values store unchanged), and the row blocks
+    land in k, gate, weights, q (head by head) and q_nope in that order."""
+    rng = np.random.default_rng(11)
+    c = _proj_case(rng)
+    T, hidden = c["x"].shape
+    cols = [0, 7, hidden - 1]
+    x = np.zeros((T, hidden))
+    x[np.arange(T), cols] = 1.0
+    qcols = [4, 0, 9]
+    cq = np.zeros_like(c["cq"])
+    cq[np.arange(T), qcols] = 1.0
+    H, D, Hm, nope = c["H"], c["D"], c["Hm"], c["nope"]
+    o = oracle.indexer_project(x, c["w_kgw"], cq, c["w_q"], c["w_uk_t"], H, D, Hm, nope, 0.25)
+    for t in range(T):
+        col = c["w_kgw"][:, cols[t]]
+        assert np.array_equal(o["k"][t], col[:D])
+        assert np.array_equal(o["gate"][t], col[D:2 * D])
+        assert np.array_equal(o["weights"][t], 0.25 * col[2 * D:])   # a power of two: exact
+        qc = c["w_q"][:, qcols[t]]
+        for h in range(H):
+            assert np.array_equal(o["q"][t, h], qc[h * D:(h + 1) * D])
+        assert np.array_equal(o["q_nope"][t].ravel(), qc[H * D:])
+
+
+def test_projection_against_brute_force_sums():
+    """Every output element as an explicit sum of products (math.fsum, exact
+    rounding of the float64 sum), before the storage rounding."""
+    rng = np.random.default_rng(12)
+    c = _proj_case(rng)
+    H, D, Hm, nope = c["H"], c["D"], c["Hm"], c["nope"]
+    o = oracle.indexer_project(c["x"], c["w_kgw"], c["cq"], c["w_q"], c["w_uk_t"], H, D, Hm,
+                               nope, 0.5, rounded=False)
+    T = c["x"].shape[0]
+    for t in range(T):
+        for f in range(2 * D + H):
+            v = math.fsum(float(c["w_kgw"][f, k]) * float(c["x"][t, k])
+                          for k in range(c["x"].shape[1]))
+            got = o["k"][t, f] if f < D else o["gate"][t, f - D] if f < 2 * D else \
+                o["weights"][t, f - 2 * D] / 0.5
+            assert got == pytest.approx(v, rel=1e-12, abs=1e-12)
+        for f in range(H * D + Hm * nope):
+            v = math.fsum(float(c["w_q"][f, k]) * float(c["cq"][t, k])
+                          for k in range(c["cq"].shape[1]))
+            got = o["q"][t].ravel()[f] if f < H * D else o["q_nope"][t].ravel()[f - H * D]
+            assert got == pytest.approx(v, rel=1e-12, abs=1e-12)
+        for h in range(Hm):
+            for l in range(c["w_uk_t"].shape[1]):
+                v = math.fsum(float(o["q_nope"][t, h, n]) * float(c["w_uk_t"][h, l, n])
+                              for n in range(nope))
+                assert o["q_lat"][t, h, l] == pytest.approx(v, rel=1e-12, abs=1e-12)
+
+
+def test_absorbed_query_scores_a_latent_row_like_its_up_projected_key():
+    """The reason for the latent-space query: for any latent cache row c,
+    <q_lat_h, c> = <q_nope_h, W_uk_h c> with W_uk_h = w_uk_t[h]^T.  L == nope
+    here, so reading w_uk_t[h] untransposed has the right shape and must fail."""
+    rng = np.random.default_rng(13)
+    c = _proj_case(rng, nope=5, L=5)
+    Hm = c["Hm"]
+    q_nope = rng.standard_normal((2, Hm, 5))
+    q_lat = oracle.absorb_query(q_nope, c["w_uk_t"])
+    cvec = rng.standard_normal(5)
+    for h in range(Hm):
+        key = c["w_uk_t"][h].T @ cvec                  # W_uk_h c
+        for t in range(2):
+            assert q_lat[t, h] @ cvec == pytest.approx(q_nope[t, h] @ key, rel=1e-12)
+            wrong = q_nope[t, h] @ (c["w_uk_t"][h] @ cvec)
+            assert abs(q_lat[t, h] @ cvec - wrong) > 1e-6
+
+
+def test_projection_storage_roundings():
+    """k, gate, q, q_nope, q_lat are stored in bf16 (to nearest even), the
+    weights in fp32, and q_lat is formed from the stored q_nope."""
+    rng = np.random.default_rng(14)
+    c = _proj_case(rng)
+    args = (c["x"], c["w_kgw"], c["cq"], c["w_q"], c["w_uk_t"], c["H"], c["D"], c["Hm"],
+            c["nope"], 0.3)
+    ex = oracle.indexer_project(*args, rounded=False)
+    st = oracle.indexer_project(*args)
+    for n in ("k", "gate", "q", "q_nope"):
+        assert np.array_equal(st[n], oracle.round_bf16(ex[n]))
+    assert np.array_equal(st["weights"], ex["weights"].astype(np.float32).astype(np.float64))
+    assert np.array_equal(st["q_lat"],
+                          oracle.round_bf16(oracle.absorb_query(st["q_nope"], c["w_uk_t"])))
