@@ -37,7 +37,6 @@ namespace {
 
 constexpr int kPM = 128;            // output features per tile (MMA M = TMEM lanes)
 constexpr int kPK = 64;             // contraction elements per stage (one 128-byte row)
-constexpr int kPThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kPSegs = 3;           // output tensors per launch
 
 // Features [f0, f1) of every batch go to one output tensor:
@@ -73,17 +72,31 @@ struct PCfg {
   static constexpr int kABytes = kPM * 128;
   static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = BN <= 16 ? 4 : BN <= 128 ? 3 : 4;
-  static constexpr int kCtasPerSm = BN <= 16 ? 3 : BN <= 128 ? 2 : 1;
-  static constexpr int kTmemCols = BN < 32 ? 32 : BN;
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes;
+  static constexpr int kStages = BN <= 16 ? 4 : BN <= 64 ? 6 : BN <= 128 ? 5 : 4;
+  // a handful of tokens: up to three CTAs per SM, each streaming its own
+  // weight rows; otherwise one persistent CTA per SM
+  static constexpr int kCtasPerSm = BN <= 16 ? 3 : 1;
+  // warp 0 TMA, warp 1 MMA, then the epilogue: four warps (one per TMEM lane
+  // quarter) for a handful of tokens, eight (two per quarter, each taking half
+  // of the tile's tokens) otherwise
+  static constexpr int kEpiWarps = BN <= 16 ? 4 : 8;
+  static constexpr int kThreads = (2 + kEpiWarps) * 32;
+  static constexpr int kAccCols = BN;                    // one accumulator
+  static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // two, double-buffered
+  // per epilogue warp, 16 tokens x 32 features of fp32 on their way to
+  // 16-byte stores (rows padded to 36 floats: 16-byte aligned, and the
+  // 128-bit reads of eight lanes fall on distinct banks)
+  static constexpr int kOutPitch = 36;
+  static constexpr int kOutBytes = BN <= 16 ? 0 : kEpiWarps * 16 * kOutPitch * 4;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kOutBytes;
 };
 
+template <int kWarps>
 __device__ __forceinline__ void proj_epi_bar() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
 }
 
-// One thread's output feature: where its values go, fixed for the whole tile.
+// One output feature: where its values go, fixed for the whole tile.
 struct ProjOut {
   unsigned char* base;  // the feature's element of token row 0 (batch offset included)
   long long ld_bytes;   // bytes between token rows
@@ -94,6 +107,7 @@ struct ProjOut {
 __device__ __forceinline__ ProjOut proj_out(const ProjArgs& pa, int b, int f) {
   ProjOut o{};
   o.on = false;
+  if (f >= pa.M) return o;
   for (int s = 0; s < pa.n_segs; ++s) {
     const ProjSeg& g = pa.seg[s];
     if (f >= g.f0 && f < g.f1) {
@@ -108,47 +122,73 @@ __device__ __forceinline__ ProjOut proj_out(const ProjArgs& pa, int b, int f) {
   }
   return o;
 }
+__device__ __forceinline__ long long proj_row(const int32_t* map, int t) {
+  return map ? (long long)map[t] : (long long)t;  // negative: a dropped token
+}
 __device__ __forceinline__ void proj_put(const ProjOut& o, int t, float v) {
-  long long row = t;
-  if (o.map) {
-    row = o.map[t];
-    if (row < 0) return;  // a dropped token
-  }
+  const long long row = proj_row(o.map, t);
+  if (row < 0) return;
   unsigned char* p = o.base + row * o.ld_bytes;
   if (o.f32)
     *reinterpret_cast<float*>(p) = o.alpha * v;
   else
     *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(o.alpha * v);
 }
+// Eight consecutive features [f, f + 8) of one segment, 16-byte aligned in
+// every token row: stored with one (bf16) or two (fp32) 16-byte stores.
+__device__ __forceinline__ bool proj_vec_ok(const ProjArgs& pa, int b, int f, ProjOut* o) {
+  *o = proj_out(pa, b, f);
+  if (!o->on || f + 8 > pa.M) return false;
+  const ProjOut e = proj_out(pa, b, f + 7);
+  if (!e.on || e.base != o->base + 7 * (o->f32 ? 4 : 2)) return false;  // one segment
+  return ((reinterpret_cast<uintptr_t>(o->base) | (uintptr_t)o->ld_bytes) & 15) == 0;
+}
+
+// Work item w (persistent CTAs take w = blockIdx.x, + gridDim.x, ...): the
+// output tile (token tiles fastest, then feature tiles, then batches) and the
+// split of its contraction.
+struct ProjItem {
+  int nt, mt, b, split, ks_lo, n_k, tile;
+};
+__device__ __forceinline__ ProjItem proj_item(const ProjArgs& pa, int w, int S, int n_tiles,
+                                              int m_tiles) {
+  ProjItem it;
+  it.tile = w / S;
+  it.split = w % S;
+  it.nt = it.tile % n_tiles;
+  it.mt = (it.tile / n_tiles) % m_tiles;
+  it.b = it.tile / (n_tiles * m_tiles);
+  it.ks_lo = (int)((long long)pa.k_steps * it.split / S);
+  it.n_k = (int)((long long)pa.k_steps * (it.split + 1) / S) - it.ks_lo;  // >= 1
+  return it;
+}
 
 template <int BN>
-__global__ void __launch_bounds__(kPThreads, PCfg<BN>::kCtasPerSm)
+__global__ void __launch_bounds__(PCfg<BN>::kThreads, PCfg<BN>::kCtasPerSm)
     proj_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                     const __grid_constant__ CUtensorMap tmap_x, const ProjArgs pa,
-                     int32_t* status) {
+                     const __grid_constant__ CUtensorMap tmap_x, const ProjArgs pa, int n_items,
+                     int S, int32_t* status) {
   using C = PCfg<BN>;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char* sbase = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ uint64_t full[C::kStages], empty[C::kStages], acc_full;
+  float* s_out = reinterpret_cast<float*>(sbase + (size_t)C::kStages * C::kStageBytes);
+  __shared__ uint64_t full[C::kStages], empty[C::kStages], tfull[2], tempty[2], done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort, s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = (pa.T + BN - 1) / BN, m_tiles = (pa.M + kPM - 1) / kPM;
-  const int nt = blockIdx.x % n_tiles;
-  const int mt = (blockIdx.x / n_tiles) % m_tiles;
-  const int b = blockIdx.x / (n_tiles * m_tiles);
-  const int split = blockIdx.y, S = gridDim.y;
-  const int ks_lo = (int)((long long)pa.k_steps * split / S);
-  const int ks_hi = (int)((long long)pa.k_steps * (split + 1) / S);
-  const int n_k = ks_hi - ks_lo;  // >= 1: the host never splits finer than the stages
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(&acc_full, 1);
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&tfull[j], 1);
+      mbar_init(&tempty[j], C::kEpiWarps);  // every epilogue warp
+    }
+    mbar_init(&done, 1);
     fence_mbar_init();
     s_abort = 0;
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w))
@@ -162,16 +202,17 @@ __global__ void __launch_bounds__(kPThreads, PCfg<BN>::kCtasPerSm)
   }
   // wait_start 1: every input may come from the kernel just before; 2: only
   // x may - the weights are model parameters, so the producer streams the
-  // first stages of weight rows before it waits
-  const int pre = pa.wait_start == 2 ? min(n_k, C::kStages) : 0;
+  // first stages of weight rows of its first tile before it waits
+  const ProjItem first = proj_item(pa, blockIdx.x, S, n_tiles, m_tiles);
+  const int pre = pa.wait_start == 2 ? min(first.n_k, C::kStages) : 0;
   if (pa.wait_start == 1) pdl_wait();
   __syncthreads();  // the barriers are initialised
   if (pre > 0) {
     if (threadIdx.x == 0) {
-      const int a_row = b * pa.M + mt * kPM;
+      const int a_row = first.b * pa.M + first.mt * kPM;
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&full[i], C::kStageBytes);
-        tma_load_2d(sbase + (size_t)i * C::kStageBytes, &tmap_w, (ks_lo + i) * kPK, a_row,
+        tma_load_2d(sbase + (size_t)i * C::kStageBytes, &tmap_w, (first.ks_lo + i) * kPK, a_row,
                     &full[i]);
       }
     }
@@ -182,124 +223,204 @@ __global__ void __launch_bounds__(kPThreads, PCfg<BN>::kCtasPerSm)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   volatile int* abort = &s_abort;
+  auto give_up = [&]() {
+    flag(status, DSA_DEV_TIMEOUT);
+    *abort = 1;
+  };
 
   if (warp == 0) {
-    // ================= TMA producer =================
+    // ================= TMA producer: one ring across all of this CTA's tiles
     if (lane == 0) {
-      const int a_row = b * pa.M + mt * kPM;
-      const int x_row = nt * BN;
-      int i = 0;
-      for (; i < n_k; ++i) {
-        const int st = i % C::kStages;
-        if (i >= C::kStages &&
-            !mbar_wait_bounded(&empty[st], (uint32_t)((i / C::kStages) - 1) & 1)) {
-          flag(status, DSA_DEV_TIMEOUT);
-          *abort = 1;
-          break;
+      int it = 0;  // k-steps issued
+      bool stop = false;
+      for (int w = blockIdx.x; w < n_items && !stop; w += gridDim.x) {
+        const ProjItem pi = proj_item(pa, w, S, n_tiles, m_tiles);
+        const int a_row = pi.b * pa.M + pi.mt * kPM;
+        for (int i = 0; i < pi.n_k; ++i, ++it) {
+          const int st = it % C::kStages;
+          if (it >= pre) {  // (the first `pre` weight tiles are already on their way)
+            if (*abort) { stop = true; break; }
+            if (it >= C::kStages &&
+                !mbar_wait_bounded(&empty[st], (uint32_t)((it / C::kStages) - 1) & 1)) {
+              give_up();
+              stop = true;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+            tma_load_2d(sbase + (size_t)st * C::kStageBytes, &tmap_w, (pi.ks_lo + i) * kPK,
+                        a_row, &full[st]);
+          }
+          tma_load_2d(sbase + (size_t)st * C::kStageBytes + C::kABytes, &tmap_x,
+                      pi.b * pa.x_col_batch + (pi.ks_lo + i) * kPK, pi.nt * BN, &full[st]);
         }
-        if (*abort && i >= pre) break;  // (a stage whose weights are in flight gets its x too)
-        unsigned char* sa = sbase + (size_t)st * C::kStageBytes;
-        const int kx = (ks_lo + i) * kPK;
-        if (i >= pre) {  // (the first `pre` weight tiles are already on their way)
-          mbar_arrive_expect_tx(&full[st], C::kStageBytes);
-          tma_load_2d(sa, &tmap_w, kx, a_row, &full[st]);
-        }
-        tma_load_2d(sa + C::kABytes, &tmap_x, b * pa.x_col_batch + kx, x_row, &full[st]);
       }
       // never leave a copy in flight: wait for the last fill of every stage used
-      for (int f = max(0, i - C::kStages); f < i; ++f)
+      for (int f = max(0, it - C::kStages); f < it; ++f)
         mbar_wait_bounded(&full[f % C::kStages], (uint32_t)(f / C::kStages) & 1);
     }
   } else if (warp == 1) {
-    // ================= MMA issuer =================
+    // ================= MMA issuer: accumulators alternate between two TMEM buffers
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_bf16(kPM, BN, false);
-      for (int i = 0; i < n_k; ++i) {
-        const int st = i % C::kStages;
+      int it = 0, j = 0;
+      bool stop = false;
+      for (int w = blockIdx.x; w < n_items && !stop; w += gridDim.x, ++j) {
+        const ProjItem pi = proj_item(pa, w, S, n_tiles, m_tiles);
+        const int acc = j & 1;
         if (*abort) break;
-        if (!mbar_wait_bounded(&full[st], (uint32_t)(i / C::kStages) & 1)) {
-          flag(status, DSA_DEV_TIMEOUT);
-          *abort = 1;
+        if (j >= 2 && !mbar_wait_bounded(&tempty[acc], (uint32_t)((j >> 1) - 1) & 1)) {
+          give_up();
           break;
         }
         tc_fence_after();
-        const uint32_t a = smem_u32(sbase + (size_t)st * C::kStageBytes);
-        const uint32_t bb = a + C::kABytes;
+        const uint32_t d = tmem + (uint32_t)(acc * C::kAccCols);
+        for (int i = 0; i < pi.n_k; ++i, ++it) {
+          const int st = it % C::kStages;
+          if (*abort || !mbar_wait_bounded(&full[st], (uint32_t)(it / C::kStages) & 1)) {
+            give_up();
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = smem_u32(sbase + (size_t)st * C::kStageBytes);
+          const uint32_t bb = a + C::kABytes;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // 16 elements = 32 bytes per MMA
-          umma_bf16(tmem, sw128_desc(a + kk * 32), sw128_desc(bb + kk * 32), idesc,
-                    (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&empty[st]);  // the stage may be refilled once these MMAs are done
+          for (int kk = 0; kk < 4; ++kk)  // 16 elements = 32 bytes per MMA
+            umma_bf16(d, sw128_desc(a + kk * 32), sw128_desc(bb + kk * 32), idesc,
+                      (i > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&empty[st]);  // the stage may be refilled once these MMAs are done
+        }
+        if (!stop) umma_commit(&tfull[acc]);  // the tile's accumulator is complete
       }
-      umma_commit(&acc_full);           // every MMA issued above has completed
-      mbar_wait_bounded(&acc_full, 0);  // retire them before TMEM is freed
+      umma_commit(&done);               // every MMA issued above has completed
+      mbar_wait_bounded(&done, 0);      // retire them before TMEM is freed
     }
   } else {
-    // ================= epilogue =================
+    // ================= epilogue (warps 2..)
     const int quarter = warp & 3;  // the TMEM lanes this warp may read
+    const int half = (warp - 2) >> 2;  // which half of the tile's tokens (8 warps)
     const int r = quarter * 32 + lane;
-    const int f = mt * kPM + r;    // output feature within the batch
-    const ProjOut out = f < pa.M ? proj_out(pa, b, f) : ProjOut{};
-    const bool ok = mbar_wait_bounded(&acc_full, 0);
-    tc_fence_after();
-    if (!ok) {
-      flag(status, DSA_DEV_TIMEOUT);
-      *abort = 1;
-    }
-    proj_epi_bar();
-    const bool good = !*abort;
-    const int t0 = nt * BN;
-    const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16);
-    float* part = S > 1 ? pa.part + ((size_t)blockIdx.x * S + split) * BN * kPM : nullptr;
+    float* so = s_out + (size_t)(warp - 2) * 16 * C::kOutPitch;
+    int j = 0;
+    for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++j) {
+      const ProjItem pi = proj_item(pa, w, S, n_tiles, m_tiles);
+      const int acc = j & 1;
+      // after a failed wait the loop still runs to the end with nothing read
+      // or stored, so that the four warps pass the same named barriers
+      const bool ok = !*abort && mbar_wait_bounded(&tfull[acc], (uint32_t)(j >> 1) & 1);
+      if (!ok) give_up();
+      tc_fence_after();
+      const int t0 = pi.nt * BN;
+      const int fw = pi.mt * kPM + quarter * 32;  // this warp's first feature
+      const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::kAccCols);
+      if (S > 1) {
+        // split contraction: fp32 partial to the workspace; the split of this
+        // tile that arrives last adds the partials in split order
+        float* part = pa.part + ((size_t)pi.tile * S + pi.split) * BN * kPM;
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 16) {
-      float v[16];
-      tmem_ld16(tb + c0, v);
+        for (int c0 = 0; ok && half == 0 && c0 < BN; c0 += 16) {
+          float v[16];
+          tmem_ld16(tb + c0, v);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float x = good ? v[c] : 0.f;
-        if (S > 1)
-          part[(c0 + c) * kPM + r] = x;
-        else if (out.on && t0 + c0 + c < pa.T)
-          proj_put(out, t0 + c0 + c, x);
-      }
-    }
-    if (S > 1) {
-      // the last split of this tile to arrive adds the partials in split order
-      __threadfence();
-      proj_epi_bar();
-      if (r == 0) s_last = atomicAdd(&pa.counter[blockIdx.x], 1u) == (uint32_t)(S - 1);
-      proj_epi_bar();
-      if (s_last) {
-        __threadfence();
-        const float* p0 = pa.part + (size_t)blockIdx.x * S * BN * kPM;
-        // 4 token columns x 8 splits of loads in flight per round; each column
-        // is still summed in split order
-        for (int c0 = 0; c0 < BN && t0 + c0 < pa.T; c0 += 4) {
-          float acc[4];
-          for (int s0 = 0; s0 < S; s0 += 8) {
-            float v[8][4];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-#pragma unroll
-              for (int c = 0; c < 4; ++c)
-                v[u][c] = s0 + u < S ? __ldcg(p0 + ((size_t)(s0 + u) * BN + c0 + c) * kPM + r)
-                                     : 0.f;
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-#pragma unroll
-              for (int c = 0; c < 4; ++c)
-                if (s0 + u == 0)
-                  acc[c] = v[u][c];
-                else if (s0 + u < S)
-                  acc[c] += v[u][c];
-          }
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            if (out.on && t0 + c0 + c < pa.T) proj_put(out, t0 + c0 + c, acc[c]);
+          for (int c = 0; c < 16; ++c) part[(c0 + c) * kPM + r] = v[c];
         }
-        if (r == 0) pa.counter[blockIdx.x] = 0u;  // re-armed for the next call
+        __threadfence();
+        proj_epi_bar<C::kEpiWarps>();
+        if (warp == 2 && lane == 0)
+          s_last = atomicAdd(&pa.counter[pi.tile], 1u) == (uint32_t)(S - 1);
+        proj_epi_bar<C::kEpiWarps>();
+        if (s_last && ok && half == 0) {
+          __threadfence();
+          const ProjOut out = proj_out(pa, pi.b, fw + lane);
+          const float* p0 = pa.part + (size_t)pi.tile * S * BN * kPM;
+          // 4 token columns x 8 splits of loads in flight per round; each
+          // column is still summed in split order
+          for (int c0 = 0; c0 < BN && t0 + c0 < pa.T; c0 += 4) {
+            float sum[4];
+            for (int s0 = 0; s0 < S; s0 += 8) {
+              float v[8][4];
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                  v[u][c] = s0 + u < S ? __ldcg(p0 + ((size_t)(s0 + u) * BN + c0 + c) * kPM + r)
+                                       : 0.f;
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                  if (s0 + u == 0)
+                    sum[c] = v[u][c];
+                  else if (s0 + u < S)
+                    sum[c] += v[u][c];
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              if (out.on && t0 + c0 + c < pa.T) proj_put(out, t0 + c0 + c, sum[c]);
+          }
+        }
+        if (s_last && warp == 2 && lane == 0) pa.counter[pi.tile] = 0u;  // re-armed
+      } else if (!ok) {
+        // nothing to read
+      } else if (BN <= 16) {  // (four epilogue warps: half is 0)
+        const ProjOut out = proj_out(pa, pi.b, fw + lane);
+        float v[16];
+        tmem_ld16(tb, v);
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          if (out.on && t0 + c < pa.T) proj_put(out, t0 + c, v[c]);
+      } else {
+        // this warp's half of the tokens, 16 at a time through shared memory:
+        // lane l then writes the 8 features [8 (l % 4), +8) of tokens l / 4
+        // and l / 4 + 8 of the 16, as 16 bytes each
+        const int chunk = lane & 3;
+        ProjOut vo;
+        const bool vec = proj_vec_ok(pa, pi.b, fw + 8 * chunk, &vo);
+        const int c_lo = half * (BN / 2), c_hi = c_lo + BN / 2;
+#pragma unroll 1
+        for (int c0 = c_lo; c0 < c_hi && t0 + c0 < pa.T; c0 += 16) {
+          float v[16];
+          tmem_ld16(tb + c0, v);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) so[c * C::kOutPitch + lane] = v[c];
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int c = (lane >> 2) + 8 * i, t = t0 + c0 + c;
+            if (t >= pa.T) continue;
+            const float4 lo = *reinterpret_cast<const float4*>(so + c * C::kOutPitch + 8 * chunk);
+            const float4 hi =
+                *reinterpret_cast<const float4*>(so + c * C::kOutPitch + 8 * chunk + 4);
+            const float src[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+            if (vec) {
+              const long long row = proj_row(vo.map, t);
+              if (row < 0) continue;
+              unsigned char* p = vo.base + row * vo.ld_bytes;
+              float y[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) y[e] = vo.alpha * src[e];
+              if (vo.f32) {
+                reinterpret_cast<float4*>(p)[0] = make_float4(y[0], y[1], y[2], y[3]);
+                reinterpret_cast<float4*>(p)[1] = make_float4(y[4], y[5], y[6], y[7]);
+              } else {
+                *reinterpret_cast<uint4*>(p) =
+                    make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
+                               pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const ProjOut o = proj_out(pa, pi.b, fw + 8 * chunk + e);
+                if (o.on) proj_put(o, t, src[e]);
+              }
+            }
+          }
+          __syncwarp();
+        }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(&tempty[acc]);  // the accumulator may be reused
     }
   }
   if (pa.wait_end) pdl_wait();  // finish after the kernel before this one
@@ -343,12 +464,7 @@ bool proj_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
 }
 
 int proj_bn(int T) { return T <= 16 ? 16 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
-int proj_ctas_per_sm(int bn) {
-  return bn == 16    ? PCfg<16>::kCtasPerSm
-         : bn == 64  ? PCfg<64>::kCtasPerSm
-         : bn == 128 ? PCfg<128>::kCtasPerSm
-                     : PCfg<256>::kCtasPerSm;
-}
+int proj_ctas_per_sm(int bn) { return bn <= 16 ? PCfg<16>::kCtasPerSm : PCfg<256>::kCtasPerSm; }
 
 // One projection GEMM: out features [0, M) per batch, nb batches, T tokens,
 // contraction K.  Returns the split count and the workspace bytes it needs
@@ -389,8 +505,9 @@ int launch_proj_bn(const CUtensorMap& mw, const CUtensorMap& mx, const ProjArgs&
                          (int)C::kSmem);
   });
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(plan.tiles, plan.splits, 1);
-  cfg.blockDim = dim3(kPThreads, 1, 1);
+  const int n_items = plan.tiles * plan.splits;
+  cfg.gridDim = dim3(min(n_items, C::kCtasPerSm * num_sms()), 1, 1);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -398,7 +515,8 @@ int launch_proj_bn(const CUtensorMap& mw, const CUtensorMap& mx, const ProjArgs&
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return launch_kernel(&cfg, proj_gemm_kernel<BN>, mw, mx, pa, status) == cudaSuccess
+  return launch_kernel(&cfg, proj_gemm_kernel<BN>, mw, mx, pa, n_items, plan.splits, status) ==
+                 cudaSuccess
              ? DSA_OK
              : DSA_ERR_CUDA;
 }
