@@ -233,10 +233,32 @@ def prefill_index(peaks_path, reps=10):
         times.append(a.elapsed_time(b))
     assert int(buf.status.item()) == 0
     us = statistics.median(times) * 1e3
+    # the chunk's own pools: compress of the 4096 new tokens (512 pools of 8)
+    # into the cache after the context's 16 384, L2 flushed before each call
+    n_ctx = int(bt.q_pos[0].item())
+    begin = torch.tensor([n_ctx // g.kpool], dtype=torch.int32, device="cuda")
+    n_new = bt.Q // g.kpool
+    ctimes = []
+    for i in range(reps + 3):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        pipeline.compress(bt, buf, pool_begin=begin, max_pools=n_new)
+        b.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            ctimes.append(a.elapsed_time(b))
+    assert int(buf.status.item()) == 0
+    c_us = statistics.median(ctimes) * 1e3
+    c_bytes = bt.Q * (2 * g.D * 2 + 1) + n_new * (g.D * 2 + 5)
     peak = json.load(open(peaks_path))["bf16_tflops"] if os.path.exists(peaks_path) else 1900.0
     tf = flops / (us * 1e-6) / 1e12
     return {"workload": "prefill: 4096 chunk queries after 131072 ctx, kpool 8, %d pools, "
                         "causal" % P,
+            "chunk_compress": {"pools": n_new, "us": round(c_us, 2), "bytes": c_bytes,
+                               "gbs": round(c_bytes / (c_us * 1e-6) / 1e9, 1),
+                               "kernel": "kpool_compress_wide_kernel<8>",
+                               "timing": "median of %d calls, L2 flushed before each" % reps},
             "kernel": "index_scores_umma_kernel (8 queries per key tile)",
             "us": round(us, 2), "flops": flops, "tflops": round(tf, 1), "bound": "tensor",
             "peak_tflops": peak, "peak_source": "measured bf16 burst" if

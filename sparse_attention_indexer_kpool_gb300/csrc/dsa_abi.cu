@@ -386,7 +386,7 @@ int dsa_decode_layer(const dsa_decode_layer_args* a, void* stream) {
                  a->pool_ids, a->token_ids, a->ws_select, a->status_dev, st,
                  rc == DSA_OK ? dsa::EarlyStart{a->pool_begin, a->valid, a->cu_seqlens}
                               : dsa::EarlyStart{},
-                 rc == DSA_OK ? dsa::kpool_compress_ctas(a->B, a->max_pools) : 0);
+                 rc == DSA_OK ? dsa::kpool_compress_ctas(a->B, a->kpool, a->max_pools) : 0);
   if (r != DSA_OK) return r;
   // the attention's inputs other than the token ids predate this call
   return dsa::launch_mla_selected_decode(a->q_lat, a->kv_latent, a->cu_seqlens, a->q_seq,

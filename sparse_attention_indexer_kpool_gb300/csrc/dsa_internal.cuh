@@ -222,7 +222,7 @@ __device__ __forceinline__ bool is_candidate(float s) { return s > -INFINITY; }
 namespace dsa {
 // CTAs of one launch of the compress kernel (they stay resident while a
 // scoring kernel of the same call starts early)
-int kpool_compress_ctas(int B, int max_pools);
+int kpool_compress_ctas(int B, int kpool, int max_pools);
 // The compress of the same call, for a scoring kernel that starts before that
 // compress has ended: it rewrites pools [pool_begin[b], ...) of sequence b, and
 // the pool count it writes follows from the first valid token of the sequence.

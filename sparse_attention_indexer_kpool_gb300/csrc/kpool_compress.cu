@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
 }
 
 // Bulk builds (a cache build, a prefill chunk's pools) in bf16 with D = 128.
-// Each CTA takes kWidePools consecutive pools of one sequence, whose token rows
+// Each CTA takes up to kWidePools consecutive pools of one sequence, whose token rows
 // are one contiguous stretch of k and one of gate: a producer warp streams them
 // with 1-D bulk copies (TMA) into a ring of shared-memory stages of 16 pools,
 // while the 16 half-warps of the other eight warps compute one pool each per
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
 // statistics are reduced in the order of the warp-per-pool kernel above (lane
 // j holds that kernel's lanes 2j and 2j + 1), so the two kernels write
 // bit-identical keys.  Waits on the ring are bounded (DSA_DEV_TIMEOUT).
-constexpr int kWidePools = 256;   // pools per CTA
+constexpr int kWidePools = 256;   // most pools per CTA (fewer when that leaves SMs idle)
 constexpr int kStagePools = 16;   // pools per ring stage (one per half-warp)
 constexpr int kWideMin = 32;      // launches covering at least this many pools per sequence
 constexpr int kWideConsumers = 256;             // 8 warps, 16 half-warps
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kWideThreads, WideCfg<KP>::kCtasPerSm)
                                const int32_t* __restrict__ cu_seqlens,
                                const int32_t* __restrict__ cu_pool_cap,
                                const int32_t* __restrict__ pool_begin, int kpool, int max_pools,
-                               __nv_bfloat16* __restrict__ pool_keys,
+                               int ppc, __nv_bfloat16* __restrict__ pool_keys,
                                int32_t* __restrict__ pool_start,
                                uint8_t* __restrict__ pool_valid, int32_t* __restrict__ n_pools,
                                int32_t* status) {
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(kWideThreads, WideCfg<KP>::kCtasPerSm)
   const int cap = cu_pool_cap[b + 1] - cu_pool_cap[b];
   const int begin = pool_begin ? pool_begin[b] : 0;
   const int end = (int)min((long long)begin + max_pools, (long long)cap);
-  const int p_first = begin + blockIdx.x * kWidePools;
+  const int p_first = begin + blockIdx.x * ppc;
   if (!(p_first < end || blockIdx.x == 0)) return;  // nothing of this sequence here
   for (int i = threadIdx.x; i < kpool * D; i += blockDim.x) s_ape[i] = ape[i];
   if (threadIdx.x == 0) {
@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(kWideThreads, WideCfg<KP>::kCtasPerSm)
     if (P_eff > end) flag(status, DSA_DEV_POOL_UNCOVERED);
   }
   // this CTA's pools [pa, pb); the computed ones [pa, pc), sentinels after
-  const int pa = max(p_first, 0), pb = min(p_first + kWidePools, end);
+  const int pa = max(p_first, 0), pb = min(p_first + ppc, end);
   const int pc = max(pa, min(pb, P_eff));
   const int n_stages_work = (pc - pa + kStagePools - 1) / kStagePools;
   const int half = threadIdx.x >> 4, j = threadIdx.x & 15;
@@ -513,6 +513,15 @@ __global__ void __launch_bounds__(kWideThreads, WideCfg<KP>::kCtasPerSm)
   }
 }
 
+// Pools per CTA of the bulk kernel: kWidePools, or fewer (a multiple of the
+// 16-pool stage) when that many would leave SMs without a CTA.
+int wide_pools_per_cta(int B, int max_pools, int ctas_per_sm) {
+  const long long slots = (long long)num_sms() * ctas_per_sm;
+  const long long want = ((long long)B * max_pools + slots - 1) / slots;
+  const int ppc = (int)((want + kStagePools - 1) / kStagePools * kStagePools);
+  return max(kStagePools, min(kWidePools, ppc));
+}
+
 template <int KP>
 int launch_wide(const void* k, const void* gate, const uint8_t* valid, const float* ape,
                 const void* g, const void* be, float eps, const int32_t* cu, const int32_t* cap,
@@ -525,7 +534,8 @@ int launch_wide(const void* k, const void* gate, const uint8_t* valid, const flo
                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)WideCfg<KP>::kSmem);
   });
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((max_pools + kWidePools - 1) / kWidePools, B, 1);
+  const int ppc = wide_pools_per_cta(B, max_pools, WideCfg<KP>::kCtasPerSm);
+  cfg.gridDim = dim3((max_pools + ppc - 1) / ppc, B, 1);
   cfg.blockDim = dim3(kWideThreads, 1, 1);
   cfg.dynamicSmemBytes = WideCfg<KP>::kSmem;
   cfg.stream = stream;
@@ -536,7 +546,7 @@ int launch_wide(const void* k, const void* gate, const uint8_t* valid, const flo
   cfg.numAttrs = 1;
   cudaError_t e = launch_kernel(
       &cfg, kpool_compress_wide_kernel<KP>, (const T*)k, (const T*)gate, valid, ape, (const T*)g,
-      (const T*)be, eps, cu, cap, begin, kpool, max_pools, (T*)pk, ps, pv, np, st);
+      (const T*)be, eps, cu, cap, begin, kpool, max_pools, ppc, (T*)pk, ps, pv, np, st);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -567,8 +577,12 @@ int launch_t(const void* k, const void* gate, const uint8_t* valid, const float*
 
 }  // namespace
 
-int kpool_compress_ctas(int B, int max_pools) {
-  if (max_pools >= kWideMin) return (max_pools + kWidePools - 1) / kWidePools * B;
+int kpool_compress_ctas(int B, int kpool, int max_pools) {
+  if (max_pools >= kWideMin) {
+    const int ppc = wide_pools_per_cta(B, max_pools, kpool <= 4 ? WideCfg<4>::kCtasPerSm
+                                                                : WideCfg<8>::kCtasPerSm);
+    return (max_pools + ppc - 1) / ppc * B;
+  }
   return max(1, (max_pools + kWarpsPerCta - 1) / kWarpsPerCta) * B;
 }
 
