@@ -63,6 +63,10 @@ def parse():
                     help="skip the paged / E4M3 attention leg")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the prefill-chunk scoring measurement")
+    ap.add_argument("--per-layer-metadata", action="store_true",
+                    help="give every layer its own copy of the batch layout (cu_seqlens, "
+                         "cu_pool_cap, q_seq, pool_begin) and padding mask instead of one "
+                         "set shared by the layers")
     ap.add_argument("--no-projections", action="store_true",
                     help="skip the projection leg (hidden state -> the path's inputs)")
     return ap.parse_args()
@@ -494,6 +498,13 @@ def run_ours(args, dist):
     for l in range(n_layers):
         bt = synth.make_batch(geo, [T] * B, [0] * B, device=dev, seed=3000 + 100 * l)
         bt.q_pos = None                      # decode query at T-1: every complete pool is visible
+        if l > 0 and not args.per_layer_metadata:
+            # one batch of sequences: its layout (cu_seqlens, cu_pool_cap,
+            # q_seq) and padding mask are the same tensors in every layer;
+            # caches and queries stay per layer
+            b0 = layers[0][0]
+            bt.cu_seqlens, bt.cu_pool_cap, bt.q_seq, bt.valid = (
+                b0.cu_seqlens, b0.cu_pool_cap, b0.q_seq, b0.valid)
         sets = []
         for k in range(n_sets):
             src = (bt.q, bt.weights, bt.q_lat) if k == 0 else synth.query_set(
@@ -531,6 +542,10 @@ def run_ours(args, dist):
     for bt, buf in layers:
         assert int(buf.status.item()) == 0
         buf.pool_begin = (buf.n_pools - 1).clamp(min=0).to(torch.int32)
+    if not args.per_layer_metadata:
+        for bt, buf in layers[1:]:
+            assert torch.equal(buf.pool_begin, layers[0][1].pool_begin)
+            buf.pool_begin = layers[0][1].pool_begin
 
     def step(events=None, qset=0):
         """One decode step over every layer: one dsa_decode_layer call per layer
@@ -743,7 +758,12 @@ def run_ours(args, dist):
                    "graph": "CUDA graph of %d steps replayed %d times" % (S, R),
                    "queries": ("one seeded query set reused by every step" if n_sets == 1 else
                                "consecutive steps rotate over %d seeded query sets per layer "
-                               "(q, weights, q_lat), so they select different rows" % n_sets)},
+                               "(q, weights, q_lat), so they select different rows" % n_sets),
+                   "batch_metadata": ("per layer: every layer has its own copy of the batch "
+                                      "layout and padding mask" if args.per_layer_metadata else
+                                      "shared: the layers read one batch layout (cu_seqlens, "
+                                      "cu_pool_cap, q_seq, pool_begin) and padding mask; "
+                                      "caches and queries are per layer")},
         "gpu_launches": launches_per_step * K,
         "roofline": roofline, "select_call_in_step": select_call,
         "step_hbm_gbs": round(step_gbs, 1), "step_frac_of_peak": round(step_gbs / hbm_peak, 4),
