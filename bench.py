@@ -530,14 +530,21 @@ def run_ours(args, dist):
         layers.append((bt, buf))
     torch.cuda.synchronize()
 
-    # ---- full cache build (kpool_compress over every token), timed for information
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
+    # ---- full cache build (kpool_compress over every token): built once, then
+    # rebuilt three times (the same result) and timed; the median is reported
     for bt, buf in layers:
         pipeline.compress(bt, buf)
-    e1.record()
-    torch.cuda.synchronize()
-    build_ms = e0.elapsed_time(e1)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    build_times = []
+    for _ in range(3):
+        torch.cuda.synchronize()
+        e0.record()
+        for bt, buf in layers:
+            pipeline.compress(bt, buf)
+        e1.record()
+        torch.cuda.synchronize()
+        build_times.append(e0.elapsed_time(e1))
+    build_ms = statistics.median(build_times)
     build_bytes = n_layers * (B * T * (2 * geo.D * 2 + 1) + B * (T // geo.kpool) * (geo.D * 2 + 5))
     for bt, buf in layers:
         assert int(buf.status.item()) == 0
@@ -770,7 +777,11 @@ def run_ours(args, dist):
         "ms_per_step_with_event_nodes": None if ev_step_ms is None else round(ev_step_ms, 5),
         "algorithmic_bytes_per_query_layer": ab,
         "compress_build": {"ms": round(build_ms, 3),
-                           "gbs": round(build_bytes / (build_ms * 1e-3) / 1e9, 1)},
+                           "gbs": round(build_bytes / (build_ms * 1e-3) / 1e9, 1),
+                           "frac": round(build_bytes / (build_ms * 1e-3) / 1e9 / hbm_peak, 4),
+                           "timing": "median of 3 warm rebuilds of the 11 layers' caches "
+                                     "(11 launches each; %d MiB moved "
+                                     "per rebuild, past the L2)" % (build_bytes >> 20)},
         "clocks": clocks, "e2e": e2e,
     }
     if breakdown:
