@@ -308,6 +308,9 @@ __global__ void __launch_bounds__(128)
     mla_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int Hm,
                      int n_split, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
   pdl_wait();
+  // the kernel after this one (the first of the next call) may start its
+  // prologue: it waits for this one before it reads anything
+  pdl_launch_dependents();
   const long long qh = (long long)blockIdx.y * Hm + blockIdx.x;
   const float* ml = part_ml + qh * n_split * 2;
   const int d = threadIdx.x * 4;
