@@ -337,8 +337,11 @@ int dsa_select_noalloc(const void* q, const float* weights, float scale, const v
  * that its earlier kernels do not write: the scoring kernel streams the key
  * tiles below pool_begin[b] while the compress still runs (decode geometry,
  * q_pos == NULL), and the attention kernel loads its query block before the
- * token ids exist.  As with every call, inputs are ordered by the stream: work
- * enqueued before the call has finished writing them when it starts.
+ * token ids exist.  With max_pools == 1 in that geometry (a decode step: one
+ * new pool per sequence, bf16, D = 128) the compress runs inside the scoring
+ * kernel and the call launches one kernel fewer.  As with every call, inputs
+ * are ordered by the stream: work enqueued before the call has finished
+ * writing them when it starts.
  *   ws_select: dsa_select_workspace_size(Q, P_ld, select_k) bytes, zero-filled
  *              before first use, left zeroed (as for dsa_select).
  *   ws_mla:    dsa_mla_selected_decode_workspace_size(Q, Hm, L, out_width, dtype).

@@ -230,7 +230,23 @@ struct EarlyStart {
   const int32_t* pool_begin = nullptr;  // nullptr: no early start
   const uint8_t* valid = nullptr;
   const int32_t* cu_seqlens = nullptr;
+  // Set (k != nullptr) when the scoring kernel does the compress of its call
+  // itself (bf16, D = 128, one pool per sequence from pool_begin[b]): it is
+  // then the first kernel of the call, and no compress kernel is launched.
+  const __nv_bfloat16* k = nullptr;
+  const __nv_bfloat16* gate = nullptr;
+  const float* ape = nullptr;
+  const __nv_bfloat16* ln_gamma = nullptr;
+  const __nv_bfloat16* ln_beta = nullptr;
+  float ln_eps = 0.f;
+  __nv_bfloat16* pool_keys_out = nullptr;
+  int32_t* pool_start_out = nullptr;
+  uint8_t* pool_valid_out = nullptr;
+  int32_t* n_pools_out = nullptr;
 };
+// whether launch_index_scores starts the scoring kernel early with es
+bool index_early_start(const EarlyStart& es, int Q, const int32_t* q_seq, const int32_t* q_pos,
+                       int H, int D, int dtype);
 int launch_kpool_compress(const void* k, const void* gate, const uint8_t* valid, const float* ape,
                           const void* ln_gamma, const void* ln_beta, float ln_eps,
                           const int32_t* cu_seqlens, const int32_t* cu_pool_cap,

@@ -104,6 +104,13 @@ bool index_fills_histogram(int Q, const int32_t* q_seq, int H, int D, int dtype)
   return index_uses_tensor_cores(H, D, dtype) && umma_index_group(Q, q_seq) == 1;
 }
 
+bool index_early_start(const EarlyStart& es, int Q, const int32_t* q_seq, const int32_t* q_pos,
+                       int H, int D, int dtype) {
+  return es.pool_begin != nullptr && es.valid != nullptr && es.cu_seqlens != nullptr &&
+         index_uses_tensor_cores(H, D, dtype) && umma_index_group(Q, q_seq) == 1 &&
+         umma_index_early_ok(Q, q_seq, q_pos);
+}
+
 int launch_index_scores(const void* q, const float* weights, float scale, const void* pool_keys,
                         int pool_rows, const int32_t* pool_start, const uint8_t* pool_valid,
                         const int32_t* n_pools, const int32_t* cu_pool_cap, const int32_t* q_seq,

@@ -36,6 +36,7 @@
 
 #include <mutex>
 
+#include "compress_pool.cuh"
 #include "dsa_internal.cuh"
 #include "umma.cuh"
 
@@ -47,7 +48,8 @@ constexpr int kBM = 128;                       // pools per tile (MMA M)
 constexpr int kABytes = kBM * kD * 2;          // 32 KB key tile
 constexpr int kHalfA = kBM * 64 * 2;           // one 64-channel box of it
 constexpr int kEpiWarps = 8;
-constexpr int kThreadsU = (2 + kEpiWarps) * 32;
+constexpr int kCompressWarp = 2 + kEpiWarps;  // the decode compress, when the call fuses it
+constexpr int kThreadsU = (3 + kEpiWarps) * 32;
 constexpr int kHistBins = 4096;
 constexpr int kSmemMax = 227 * 1024;
 constexpr int kBaseCache = 4096;               // groups whose cache base is kept on chip
@@ -70,6 +72,7 @@ struct Ctl {
   uint64_t bfull[2], bempty[2];    // query block slots
   uint64_t tfull[2], tempty[2];    // TMEM accumulators
   uint64_t done;                   // all MMAs of the CTA retired
+  uint64_t cdone;                  // the compress warp's pools are written
   uint32_t tmem_base;
   int abort;
   int scan_warp[kThreadsU / 32];   // tile prefix scan: per-warp totals and carry
@@ -147,6 +150,8 @@ __device__ __forceinline__ int early_pool_count(const EarlyStart& es, int b, int
                                                 int lane) {
   const long long lo = es.cu_seqlens[b];
   const int T = es.cu_seqlens[b + 1] - es.cu_seqlens[b];
+  if (es.k != nullptr)  // the call's compress is in this kernel: scan the whole sequence
+    return min((T - first_valid_warp(es.valid, lo, T, lane)) / kpool, cap);
   const int lim = min(T, kScanTokens);
   uint32_t nz[kScanTokens / 32];
 #pragma unroll
@@ -205,6 +210,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   // streamed and scored before the compress has finished, with the pool count
   // found from the compress's own inputs.
   const bool early = G == 1 && es.pool_begin != nullptr;
+  // the compress of the call runs in this kernel (see EarlyStart)
+  const bool fused = early && es.k != nullptr;
   int* s_base = reinterpret_cast<int*>(sbase + LY::base);  // first cache row of group gi
   int* s_safe = s_base + LY::cached(n_groups);             // early: tiles readable at once
   int* s_np = s_safe + LY::cached(n_groups);               // early: pool count, or -1
@@ -231,6 +238,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       mbar_init(&ctl.tempty[j], C::kTileWarps);
     }
     mbar_init(&ctl.done, 1);
+    mbar_init(&ctl.cdone, 1);
     fence_mbar_init();
     ctl.abort = 0;
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_keys))
@@ -248,7 +256,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   }
   if (use_hist)
     for (int i = threadIdx.x; i < kHistBins; i += kThreadsU) s_hist[i] = 0;
-  if (!early) {
+  if (!early || fused) {
     pdl_wait();  // the pool cache may come from the kernel just before
     pdl_launch_dependents();
   }
@@ -348,7 +356,12 @@ __global__ void __launch_bounds__(kThreadsU, 1)
               !wait(&ctl.empty[stage], ((a_par >> stage) & 1) ^ 1))
             break;
           if (!waited && t - s_prefix[gi] >= s_safe[gi]) {
-            pdl_wait();  // this tile may hold a pool the compress rewrites
+            // this tile may hold a pool the compress rewrites
+            if (fused) {
+              if (!wait(&ctl.cdone, 0)) break;
+            } else {
+              pdl_wait();
+            }
             waited = true;
           }
           const int row = (int)(base0 + (t - s_prefix[gi]) * kBM);
@@ -409,7 +422,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       umma_commit(&ctl.done);  // retire every MMA before TMEM is freed
       mbar_wait_bounded(&ctl.done, 0);
     }
-  } else {
+  } else if (warp < kCompressWarp) {
     // ================= epilogue =================
     constexpr int GH = G == 1 ? 1 : G / 2;  // queries per warp of each tile
     const int ew = warp - 2;                // 0..7
@@ -474,7 +487,10 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         const int acc = (int)(tc & 1);
         if (G == 1 && acc != half) continue;  // the other half's tile
         if (!waited && t - s_prefix[gi] >= s_safe[gi]) {  // a tile the compress may rewrite
-          pdl_wait();
+          if (fused)
+            (void)wait(&ctl.cdone, 0);
+          else
+            pdl_wait();
           waited = true;
         }
         const int p = (int)(t - s_prefix[gi]) * kBM + r;
@@ -533,13 +549,75 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     }
     if (early) {
       // every CTA ends after the compress, so that the end of this kernel
-      // implies the end of the compress for whatever waits on it
-      if (!waited) pdl_wait();
-      if (blockIdx.x == 0)  // the range checks the tile plan skipped
+      // implies the end of the compress for whatever waits on it (a fused
+      // compress is part of this CTA)
+      if (!waited && !fused) pdl_wait();
+      if (blockIdx.x == 0 && !fused)  // the range checks the tile plan skipped
         for (int qi = ew * 32 + lane; qi < Q; qi += kEpiWarps * 32)
           qmeta(qi, Q, q_seq, q_pos, n_pools, cu_pool_cap, pool_start, B, kpool, P_ld, status,
                 true);
+      if (blockIdx.x == 0 && fused)  // the same, with the pool counts found from the inputs
+        for (int qi = ew; qi < Q; qi += kEpiWarps) {
+          const int b = q_seq ? q_seq[qi] : 0;
+          const int np = (b >= 0 && b < B)
+                             ? early_pool_count(es, b, cu_pool_cap[b + 1] - cu_pool_cap[b],
+                                                kpool, lane)
+                             : 0;
+          if (lane == 0)
+            qmeta(qi, Q, q_seq, q_pos, n_pools, cu_pool_cap, pool_start, B, kpool, P_ld, status,
+                  true, np);
+        }
     }
+  } else if (fused) {
+    // ================= compress warp (the call's one new pool per sequence) =================
+    // Sequences of the tiles in this CTA's range that may hold a rewritten
+    // pool, and every gridDim.x-th sequence that no query's tiles cover (its
+    // cache is updated all the same).  Two CTAs that share a sequence write
+    // the same bytes.
+    auto compress_seq = [&](int b) {
+      const long long lo = es.cu_seqlens[b];
+      const int Tb = es.cu_seqlens[b + 1] - es.cu_seqlens[b];
+      const long long cap_lo = cu_pool_cap[b];
+      const int cap = cu_pool_cap[b + 1] - cu_pool_cap[b];
+      const int begin = es.pool_begin[b];
+      const int end = (int)min((long long)begin + 1, (long long)cap);
+      const int t0 = first_valid_warp(es.valid, lo, Tb, lane);
+      const int P = (Tb - t0) / kpool;
+      const int P_eff = min(P, cap);
+      if (lane == 0) {
+        es.n_pools_out[b] = P_eff;
+        if (P > cap) flag(status, DSA_DEV_POOL_OVERFLOW);
+        if (P_eff > end) flag(status, DSA_DEV_POOL_UNCOVERED);
+      }
+      const int p = begin;
+      if (p < 0 || p >= end) return;
+      __nv_bfloat16* out = es.pool_keys_out + (cap_lo + p) * kD + lane * 4;
+      if (p >= P_eff)
+        compress_sentinel_warp<__nv_bfloat16, 4>(lane, out, es.pool_start_out + cap_lo + p,
+                                                 es.pool_valid_out + cap_lo + p);
+      else
+        compress_pool_warp<__nv_bfloat16, 4>(es.k, es.gate, es.valid, es.ape, es.ln_gamma,
+                                             es.ln_beta, es.ln_eps,
+                                             lo + t0 + (long long)p * kpool, kpool, lane, out,
+                                             t0 + p * kpool, es.pool_start_out + cap_lo + p,
+                                             es.pool_valid_out + cap_lo + p);
+    };
+    for (int gi = 0; gi < n_groups; ++gi) {
+      const long long u0 = (long long)s_prefix[gi] + s_safe[gi], u1 = s_prefix[gi + 1];
+      const int b = q_seq ? q_seq[gi] : 0;
+      if (u0 < u1 && max(u0, t_lo) < min(u1, t_hi) && b >= 0 && b < B) compress_seq(b);
+    }
+    for (int b = blockIdx.x; b < B; b += gridDim.x) {
+      bool covered = false;
+      for (int gi = 0; gi < n_groups && !covered; ++gi)
+        covered = (q_seq ? q_seq[gi] : 0) == b && s_safe[gi] < s_prefix[gi + 1] - s_prefix[gi];
+      if (!covered) compress_seq(b);
+    }
+    // the writes above are read by this CTA's TMA loads and by its epilogue
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __threadfence_block();
+    __syncwarp();
+    if (lane == 0) mbar_arrive1(&ctl.cdone);
   }
 
   // Fill the rest of each row (pools past every tile of its group) with -inf.

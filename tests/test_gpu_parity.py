@@ -423,8 +423,9 @@ def test_decode_layer_incremental_pool_count_from_the_valid_mask(step, decode_fo
 
 def test_decode_layer_launches_what_the_three_calls_launch():
     """The library's launch count: the fused call launches as many kernels as
-    compress -> select -> attend, for a full build and for a decode step (no
-    query positions, one new pool per sequence)."""
+    compress -> select -> attend for a full build, and one fewer for a decode
+    step (no query positions, one new pool per sequence), whose compress runs
+    inside the scoring kernel; the outputs are the same."""
     bt = ragged_small(seed=54)
     bt.q_pos = None
     a = pipeline.LayerBuffers.alloc(bt)
@@ -441,7 +442,7 @@ def test_decode_layer_launches_what_the_three_calls_launch():
     n3 = ops.dsa_kernel_launches()
     pipeline.run_layer(bt, b, pool_begin=begin, max_pools=1)
     torch.cuda.synchronize()
-    assert n3 - n2 == n1 - n0
+    assert n3 - n2 == n1 - n0 - 1
     assert ops.dsa_kernel_launches() - n3 == n2 - n1
     _assert_same_outputs(a, b)
 
@@ -572,3 +573,42 @@ def test_streaming_attention_large_logit_in_a_late_or_first_tile(tile):
     st = par.check_mla(o, buf)
     assert st == 0 and int(buf.status.item()) == 0
     assert float(buf.lse[0, 0]) > float(buf.lse[0, 1]) + 8.0
+
+
+@pytest.mark.parametrize("seed", [91, 92])
+def test_decode_step_fused_compress_shared_and_uncovered_sequences(seed):
+    """The decode form whose compress runs inside the scoring kernel (one new
+    pool per sequence): two queries on one sequence (both CTAs holding its new
+    pool write it), a sequence no query reads (its pool is still written), a
+    new pool that is not complete (a sentinel), one at a tile's first pool and
+    one mid-tile; the same outputs as compress -> select -> attend, and the
+    oracle's pool keys and counts."""
+    geo = Geometry(D=128, H=32, kpool=4, select_k=64, out_width=256, Hm=64, L=512, dtype="bf16")
+    bt = synth.make_batch(geo, [3000, 1501, 600, 800, 2052], [2, 0, 5, 0, 3], device=DEV,
+                          seed=seed)
+    bt.q_pos = None
+    bt.q_seq = torch.tensor([0, 0, 1, 2, 4], dtype=torch.int32, device=DEV)  # 3: no query
+    a = pipeline.LayerBuffers.alloc(bt)
+    b = pipeline.LayerBuffers.alloc(bt)
+    pipeline.run_layer(bt, a)
+    pipeline.run_layer(bt, b)
+    torch.cuda.synchronize()
+    # pool 128 opens a tile; sequence 1's pool 375 is incomplete (1501 tokens)
+    begin = torch.tensor([128, 375, 140, 150, 300], dtype=torch.int32, device=DEV)
+    for s_, p0 in enumerate(begin.tolist()):      # new content for the recompressed pool
+        lo = int(bt.cu_seqlens[s_]) + bt.pads[s_] + p0 * geo.kpool
+        hi = min(lo + geo.kpool, int(bt.cu_seqlens[s_ + 1]))
+        bt.k[lo:hi] *= -1
+        bt.gate[lo:hi] += 1
+    n0 = ops.dsa_kernel_launches()
+    pipeline.decode_layer(bt, a, pool_begin=begin, max_pools=1)
+    n1 = ops.dsa_kernel_launches()
+    pipeline.run_layer(bt, b, pool_begin=begin, max_pools=1)
+    n2 = ops.dsa_kernel_launches()
+    torch.cuda.synchronize()
+    assert n1 - n0 == n2 - n1 - 1                       # the compress ran inside the scoring
+    _assert_same_outputs(a, b)
+    assert torch.equal(a.pool_keys, b.pool_keys) and torch.equal(a.n_pools, b.n_pools)
+    assert torch.equal(a.pool_start, b.pool_start) and torch.equal(a.pool_valid, b.pool_valid)
+    o = oracle_inputs(bt)
+    par.check_compress(o, a)
