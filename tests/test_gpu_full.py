@@ -154,3 +154,29 @@ def test_prefill_chunk_sampled():
              out_width=bt.geo.out_width)
     par.check_expand(o, buf, rows=rows)
     _mla_rows(bt, buf, rows)
+
+
+@pytest.mark.slow
+def test_long262k_decode_steps_repeated():
+    """The bench's decode step, called again and again on one 262k layer (top-k
+    clusters of 16, the compress inside the scoring kernel): no status bit is
+    ever set, and every call gives what compress -> select -> attend gives."""
+    bt = synth.long262k(device=DEV, layer=1)
+    bt.q_pos = None
+    a = pipeline.LayerBuffers.alloc(bt)
+    b = pipeline.LayerBuffers.alloc(bt)
+    pipeline.compress(bt, a)
+    pipeline.compress(bt, b)
+    torch.cuda.synchronize()
+    begin = (a.n_pools - 1).clamp(min=0).to(torch.int32)
+    for step in range(24):
+        bt.q, bt.weights, bt.q_lat = synth.query_set(bt.geo, bt.Q, device=DEV, seed=700 + step)
+        pipeline.decode_layer(bt, a, pool_begin=begin, max_pools=1)
+        torch.cuda.synchronize()
+        assert int(a.status.item()) == 0, step
+        if step % 8 == 0:
+            pipeline.run_layer(bt, b, pool_begin=begin, max_pools=1)
+            torch.cuda.synchronize()
+            assert int(b.status.item()) == 0, step
+            for n in ("scores", "pool_ids", "token_ids", "out", "lse"):
+                assert torch.equal(getattr(a, n), getattr(b, n)), (step, n)
