@@ -27,7 +27,11 @@
 //              4096-bin histogram of the score keys' top 12 bits for the top-k
 //              that follows.  For G = 1 the two halves of the epilogue take
 //              alternate tiles (one accumulator each); for G = 8 each half takes
-//              four of the eight queries of every tile.
+//              four of the eight queries of every tile;
+//   warp 10    (fused decode call only) the call's compress of one new pool per
+//              sequence, with the compress kernels' own per-pool code; the
+//              producer and the epilogue wait for it, on an in-CTA barrier,
+//              only at the tile that holds the new pool.
 // Every mbarrier wait is bounded.  On a timeout the kernel flags DSA_DEV_TIMEOUT,
 // stops issuing work, waits (bounded) for its own copies and MMAs in flight and
 // frees its TMEM before it returns.
@@ -208,7 +212,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   // [es.pool_begin[b], ...)): the tile plan comes from the call's inputs only;
   // the key tiles below pool_begin[b], which that compress does not write, are
   // streamed and scored before the compress has finished, with the pool count
-  // found from the compress's own inputs.
+  // found from the compress's own inputs.  Fused (es.k set), that compress is
+  // warp 10 of this kernel, which is then the call's first kernel.
   const bool early = G == 1 && es.pool_begin != nullptr;
   // the compress of the call runs in this kernel (see EarlyStart)
   const bool fused = early && es.k != nullptr;
@@ -702,7 +707,8 @@ int launch_g(const void* q, const float* weights, float scale, const void* pool_
   cudaLaunchConfig_t cfg = {};
   // A scoring CTA cannot share an SM with a CTA of the compress kernel still
   // running beside an early start (measured: those CTAs begin ~2 us late and
-  // finish last), so a few busy SMs are left out of the grid.
+  // finish last), so a few busy SMs are left out of the grid; the fused form
+  // (the compress in this kernel) keeps that grid, which measured faster.
   const int sms = num_sms();
   const int grid = (busy_ctas > 0 && busy_ctas <= sms / 8) ? sms - busy_ctas : sms;
   cfg.gridDim = dim3(grid, 1, 1);
