@@ -442,29 +442,39 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 // raised only when a tile's max exceeds it by more than 8 (base 2): then O^T
 // and the sum are rescaled first; otherwise probabilities up to 2^8 are kept,
 // which is exact up to rounding since O and the sum share the reference.
+//
+// The row tile is loaded two column blocks (128 latent columns) at a time, one
+// cp.async group each.  O^T += C^T P^T reads exactly those two blocks per latent
+// chunk, so each chunk's MMAs commit on their own barrier and, once they have
+// completed, the chunk's blocks take the next tile's rows; the next tile's
+// S^T MMAs then start on each block pair as it lands.  P is stored row-major
+// (64 heads of a row in one 128-byte swizzled line) and read MN-major by the
+// tensor cores, so each thread writes its 32 probabilities as four 16-byte
+// pieces.
 constexpr int kHs = 64;                  // heads per CTA
 constexpr int kQBlockS = kHs * 128;      // 64 heads x 64 latent columns, 8 KB
-constexpr int kPtBlockS = kHs * 128;     // 64 heads x 64 rows, 8 KB
+constexpr int kPBytesS = kRows * 128;    // P: 128 rows x 64 heads, bf16, 16 KB
 constexpr int kTmemColsS = 512;          // S^T (64) + O^T (4 x 64)
 constexpr float kRescaleAt = 8.f;        // base-2 growth of the max that forces a rescale
 
 struct SCtl {
-  uint64_t s_ready, o_ready;
+  float m_run[kHs], l_run[kHs], alpha[kHs];  // first: 16-byte aligned
+  float red[4][kHs];  // [row quarter][head]: per-warp partials
+  float rs[2][kRows];  // row scales (E4M3) of the current and the next tile
+  int tok[2][kRows];
+  int prow[2][kRows];
+  uint64_t s_ready, o_ready[4];
   uint32_t tmem_base;
   int rescale;
-  int tok[kRows];
-  int prow[kRows];
-  float rs[kRows];
-  float red[4][kHs];  // [row quarter][head]: per-warp partials
-  float m_run[kHs], l_run[kHs], alpha[kHs], tsum[kHs];
 };
 constexpr size_t kOffKvS = 0;
 constexpr size_t kOffQS = kOffKvS + 8 * (size_t)kKvBlock;
 constexpr size_t kOffPtS = kOffQS + 8 * (size_t)kQBlockS;
-constexpr size_t kOffCtlS = kOffPtS + 2 * (size_t)kPtBlockS;
+constexpr size_t kOffCtlS = kOffPtS + (size_t)kPBytesS;
 constexpr size_t kSmemBytesS = 1024 + kOffCtlS + sizeof(SCtl);
 static_assert(kSmemBytesS <= 227 * 1024, "shared memory budget");
 static_assert((size_t)kHs * kL * 4 <= 8 * (size_t)kKvBlock, "O staging fits the row tile");
+static_assert(kOffCtlS % 16 == 0, "the control block's float arrays are read as float4");
 
 // 32 values per lane (one row, 32 heads) reduced over the warp's 32 rows; lane l
 // ends with the reduction of head l (31 shuffles).
@@ -482,6 +492,14 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
     }
   }
   return v[0];
+}
+
+// 2^x on the special-function unit (ex2.approx, relative error below 2^-22;
+// 2^-inf = +0).
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 template <int kKv>
@@ -506,7 +524,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&c.s_ready, 1);
-    mbar_init(&c.o_ready, 1);
+#pragma unroll
+    for (int mc = 0; mc < 4; ++mc) mbar_init(&c.o_ready[mc], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -582,18 +601,17 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     *tok_out = tok;
     return (int)prow;
   };
-
-  for (int t = t_lo; t < t_hi; ++t) {
-    const uint32_t ph = (uint32_t)((t - t_lo) & 1);
-    // ---- 1. this tile's rows; the next tile's rows go to L2 meanwhile
+  // tile t's token ids and cache rows into slot `buf` (threads 0..127), and its
+  // rows into L2 (threads 128..255)
+  auto tile_ids = [&](int t, int buf) {
     if (threadIdx.x < kRows) {
       int tok;
       const int prow = row_of(t, threadIdx.x, &tok);
-      c.tok[threadIdx.x] = tok;
-      c.prow[threadIdx.x] = prow;
-    } else if (t + 1 < t_hi) {
+      c.tok[buf][threadIdx.x] = tok;
+      c.prow[buf][threadIdx.x] = prow;
+    } else {
       const int rr = threadIdx.x - kRows;
-      const int j = (t + 1) * kRows + rr;
+      const int j = t * kRows + rr;
       const int tok = (j < W && seq_ok) ? toks[j] : -1;
       if (tok >= 0 && tok < Tb) {
         long long prow = row_base + tok;
@@ -612,12 +630,15 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         }
       }
     }
-    __syncthreads();
+  };
+  // column blocks 2j and 2j + 1 (latent 128 j .. 128 j + 127) of the tile whose
+  // cache rows are in slot `buf`, as one cp.async group
+  auto gather_pair = [&](int buf, int j) {
     if (kKv != kKvPagedE4M3) {
       const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(rows_base);
-      for (int i = threadIdx.x; i < kRows * 64; i += kThreadsM) {
-        const int rr = i >> 6, ch = i & 63;
-        const int prow = c.prow[rr];
+      for (int i = threadIdx.x; i < kRows * 16; i += kThreadsM) {
+        const int rr = i >> 4, ch = 16 * j + (i & 15);
+        const int prow = c.prow[buf][rr];
         const bool okr = prow >= 0;
         cp_async16(smem_u32(sb + kOffKvS + (ch >> 3) * kKvBlock + rr * 128 +
                             (((ch & 7) ^ (rr & 7)) << 4)),
@@ -625,23 +646,23 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       }
     } else {
       const uint4* src = reinterpret_cast<const uint4*>(rows_base);
-      constexpr int kPer = kRows * (kL / 16) / kThreadsM;
+      constexpr int kPer = kRows * 8 / kThreadsM;  // sixteen-byte loads of 16 codes
       uint4 raw[kPer];
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
         const int i = u * kThreadsM + threadIdx.x;
-        const int prow = c.prow[i >> 5];
-        raw[u] = prow >= 0 ? __ldg(src + (long long)prow * (kL / 16) + (i & 31))
+        const int prow = c.prow[buf][i >> 3];
+        raw[u] = prow >= 0 ? __ldg(src + (long long)prow * (kL / 16) + 8 * j + (i & 7))
                            : make_uint4(0u, 0u, 0u, 0u);
       }
-      if (threadIdx.x < kRows) {
-        const int prow = c.prow[threadIdx.x];
-        c.rs[threadIdx.x] = prow >= 0 ? pk.row_scale[prow] : 0.f;
+      if (j == 0 && threadIdx.x < kRows) {
+        const int prow = c.prow[buf][threadIdx.x];
+        c.rs[buf][threadIdx.x] = prow >= 0 ? pk.row_scale[prow] : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
         const int i = u * kThreadsM + threadIdx.x;
-        const int rr = i >> 5, c16 = i & 31;
+        const int rr = i >> 3, c16 = 8 * j + (i & 7);
         const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
 #pragma unroll
         for (int hf2 = 0; hf2 < 2; ++hf2) {
@@ -656,31 +677,47 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       }
     }
     cp_async_commit();
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+  };
 
-    // ---- 2. S^T = C q^T  (M = 128 rows, N = 64 heads, K = 512)
-    if (threadIdx.x == 0 && issue) {
-      constexpr uint32_t idesc = umma_idesc_bf16(kRows, kHs, false);
+  if (t_lo < t_hi) {
+    tile_ids(t_lo, 0);
+    __syncthreads();
+#pragma unroll 1
+    for (int j = 0; j < 4; ++j) gather_pair(0, j);
+  }
+  for (int t = t_lo; t < t_hi; ++t) {
+    const int cur = (t - t_lo) & 1;
+    const uint32_t ph = (uint32_t)cur;
+    // ---- 1. S^T = C q^T  (M = 128 rows, N = 64 heads, K = 512), two column
+    // blocks at a time as their rows land
 #pragma unroll
-      for (int kk = 0; kk < 32; ++kk) {
-        const uint32_t blk = kk >> 2, off = (kk & 3) * 32;
-        umma_bf16(tmem, sw128_desc(kvb + blk * kKvBlock + off),
-                  sw128_desc(qb + blk * kQBlockS + off), idesc, kk > 0 ? 1u : 0u);
+    for (int j = 0; j < 4; ++j) {
+      cp_async_wait_pending(3 - j);  // the query's group is older than every row group
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (threadIdx.x == 0 && issue) {
+        constexpr uint32_t idesc = umma_idesc_bf16(kRows, kHs, false);
+#pragma unroll
+        for (int kk = 8 * j; kk < 8 * j + 8; ++kk) {
+          const uint32_t blk = kk >> 2, off = (kk & 3) * 32;
+          umma_bf16(tmem, sw128_desc(kvb + blk * kKvBlock + off),
+                    sw128_desc(qb + blk * kQBlockS + off), idesc, kk > 0 ? 1u : 0u);
+        }
+        if (j == 3) umma_commit(&c.s_ready);
       }
-      umma_commit(&c.s_ready);
     }
+    // the next tile's ids meanwhile (slot cur ^ 1 is free: its tile is done)
+    if (t + 1 < t_hi) tile_ids(t + 1, cur ^ 1);
     const bool s_done = mbar_wait_bounded(&c.s_ready, ph, wait_ns);
     tc_fence_after();
 
-    // ---- 3. softmax against the running max (thread = row r, heads 32 hg ..)
+    // ---- 2. softmax against the running max (thread = row r, heads 32 hg ..)
     float z[32];
     tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(hg * 32), z);
-    const bool row_ok = c.tok[r] >= 0;
-    const float rsr = kKv == kKvPagedE4M3 ? c.rs[r] : 1.f;
+    const bool row_ok = c.tok[cur][r] >= 0;
+    const float rsr = kKv == kKvPagedE4M3 ? c.rs[cur][r] : 1.f;
     const float zs = kKv == kKvPagedE4M3 ? sm_scale * kLog2e * rsr : sm_scale * kLog2e;
 #pragma unroll
     for (int i = 0; i < 32; ++i) z[i] = row_ok ? z[i] * zs : -INFINITY;
@@ -717,15 +754,29 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       c.alpha[h] = alpha;
     }
     __syncthreads();
+    // p = 2^(z - m); a head with no row so far (m = -inf) has only z = -inf
+    // here, and 2^-inf = 0
     float p[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int h = hg * 32 + i;
-      const float m = c.m_run[h];
-      p[i] = (m == -INFINITY || z[i] == -INFINITY) ? 0.f : exp2f(z[i] - m);
-      *reinterpret_cast<__nv_bfloat16*>(sb + kOffPtS + (r >> 6) * kPtBlockS + h * 128 +
-                                        ((((r & 63) >> 3) ^ (h & 7)) << 4) + (r & 7) * 2) =
-          __float2bfloat16_rn(kKv == kKvPagedE4M3 ? p[i] * rsr : p[i]);
+    for (int q4 = 0; q4 < 8; ++q4) {
+      const float4 m4 = reinterpret_cast<const float4*>(c.m_run + hg * 32)[q4];
+      const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float m = mv[e] == -INFINITY ? 0.f : mv[e];
+        p[4 * q4 + e] = ex2_fast(z[4 * q4 + e] - m);
+      }
+    }
+    // row r of P: heads 32 hg .. 32 hg + 31 are the 16-byte chunks 4 hg .. 4 hg + 3
+    // of its 128-byte line, at the swizzled position chunk ^ (r & 7)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float sc = kKv == kKvPagedE4M3 ? rsr : 1.f;
+      const uint4 w = make_uint4(pack_bf16(p[8 * q] * sc, p[8 * q + 1] * sc),
+                                 pack_bf16(p[8 * q + 2] * sc, p[8 * q + 3] * sc),
+                                 pack_bf16(p[8 * q + 4] * sc, p[8 * q + 5] * sc),
+                                 pack_bf16(p[8 * q + 6] * sc, p[8 * q + 7] * sc));
+      *reinterpret_cast<uint4*>(sb + kOffPtS + r * 128 + (((hg * 4 + q) ^ (r & 7)) << 4)) = w;
     }
     c.red[qw][hg * 32 + lane] = transpose_reduce32<false>(p, lane);
     // a raised reference: rescale what O^T holds so far (never on the first tile)
@@ -740,7 +791,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         tmem_st32(ta, o);
       }
     }
-    fence_proxy_async_smem();  // P^T is read by the tensor cores next
+    fence_proxy_async_smem();  // P is read by the tensor cores next
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x < kHs) {
@@ -749,30 +800,38 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       c.l_run[h] = c.l_run[h] * c.alpha[h] + s;
     }
 
-    // ---- 4. O^T += C^T P^T  (M = 128 latent x 4 chunks, N = 64 heads, K = 128 rows)
+    // ---- 3. O^T += C^T P^T  (M = 128 latent x 4 chunks, N = 64 heads, K = 128
+    // rows); chunk mc reads column blocks 2 mc and 2 mc + 1 and commits alone
     if (threadIdx.x == 0) {
       tc_fence_after();
-      constexpr uint32_t idesc = umma_idesc_bf16(128, kHs, true);
+      constexpr uint32_t idesc = umma_idesc_bf16(128, kHs, true, true);
 #pragma unroll
       for (int mc = 0; mc < 4; ++mc) {
 #pragma unroll
         for (int kr = 0; kr < 8; ++kr) {
           const uint64_t a = umma_desc_sw128(kvb + 2 * mc * kKvBlock + kr * 2048, kKvBlock, 1024);
-          const uint64_t bd = sw128_desc(ptb + (kr >> 2) * kPtBlockS + (kr & 3) * 32);
+          const uint64_t bd = umma_desc_sw128(ptb + kr * 2048, kPBytesS, 1024);
           umma_bf16(tmem + kHs + mc * kHs, a, bd, idesc, (t > t_lo || kr > 0) ? 1u : 0u);
         }
+        umma_commit(&c.o_ready[mc]);
       }
-      umma_commit(&c.o_ready);
     }
-    const bool o_done = mbar_wait_bounded(&c.o_ready, ph, wait_ns);
-    tc_fence_after();
-    ok = __syncthreads_and(o_done) != 0;  // the tiles are free again after this
-    if (!ok) {
-      pending = &c.o_ready;
-      pend_ph = ph;
-      break;
+    // as each chunk completes, its two column blocks take the next tile's rows
+#pragma unroll 1
+    for (int mc = 0; mc < 4; ++mc) {
+      const bool o_done = mbar_wait_bounded(&c.o_ready[mc], ph, wait_ns);
+      tc_fence_after();
+      ok = __syncthreads_and(o_done) != 0;
+      if (!ok) {
+        pending = &c.o_ready[3];  // commits complete in order: the last covers all
+        pend_ph = ph;
+        break;
+      }
+      if (t + 1 < t_hi) gather_pair(cur ^ 1, mc);
     }
+    if (!ok) break;
   }
+  cp_async_wait<0>();  // no copy into shared memory is left in flight
 
   // ---- 5. epilogue: O^T -> shared [head][latent] fp32, then whole rows out
   if (ok) {

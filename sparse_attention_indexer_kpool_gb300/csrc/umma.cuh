@@ -62,11 +62,12 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return umma_desc_sw128(saddr, 16, 1024);
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, B K-major,
-// A K-major or (a_mn) MN-major, shape M x N.
-__host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n, bool a_mn) {
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, each
+// K-major or (a_mn, b_mn) MN-major, shape M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n, bool a_mn,
+                                                       bool b_mn = false) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
-         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
