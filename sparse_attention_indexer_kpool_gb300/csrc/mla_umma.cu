@@ -577,10 +577,13 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   uint64_t* pending = nullptr;  // MMAs issued whose completion was not seen
   uint32_t pend_ph = 0;
 
-  // the cache row of tile row `rr` (-1: none); flags bad ids and pages
-  auto row_of = [&](int t, int rr, int* tok_out) -> int {
-    const int j = t * kRows + rr;
-    int tok = (j < W && seq_ok) ? toks[j] : -1;
+  // token id of row (threadIdx.x mod 128) of tile t, as stored (-1: none)
+  auto load_tok = [&](int t) -> int {
+    const int j = t * kRows + (threadIdx.x & (kRows - 1));
+    return (j < W && seq_ok) ? toks[j] : -1;
+  };
+  // the cache row of a stored token id (-1: none); flags bad ids and pages
+  auto row_of = [&](int tok, int* tok_out) -> int {
     if (tok >= Tb) {
       flag(status, DSA_DEV_BAD_TOKEN);
       tok = -1;
@@ -601,33 +604,28 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     *tok_out = tok;
     return (int)prow;
   };
-  // tile t's token ids and cache rows into slot `buf` (threads 0..127), and its
-  // rows into L2 (threads 128..255)
-  auto tile_ids = [&](int t, int buf) {
+  // a tile's token ids (from load_tok) -> its cache rows in slot `buf` (threads
+  // 0..127); threads 128..255 bring the same rows into L2
+  auto tile_ids = [&](int tok_raw, int buf) {
     if (threadIdx.x < kRows) {
       int tok;
-      const int prow = row_of(t, threadIdx.x, &tok);
+      const int prow = row_of(tok_raw, &tok);
       c.tok[buf][threadIdx.x] = tok;
       c.prow[buf][threadIdx.x] = prow;
-    } else {
-      const int rr = threadIdx.x - kRows;
-      const int j = t * kRows + rr;
-      const int tok = (j < W && seq_ok) ? toks[j] : -1;
-      if (tok >= 0 && tok < Tb) {
-        long long prow = row_base + tok;
-        if (kKv != kKvContig) {
-          const int blk = tok / pk.page_size;
-          const int page =
-              blk < pk.max_pages ? pk.block_table[(long long)b * pk.max_pages + blk] : -1;
-          prow = (page >= 0 && page < pk.n_pages) ? (long long)page * pk.page_size +
-                                                        tok % pk.page_size
-                                                  : -1;
-        }
-        if (prow >= 0) {
-          const unsigned char* p = rows_base + (size_t)prow * row_bytes;
-          for (size_t o = 0; o < row_bytes; o += 128)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(p + o));
-        }
+    } else if (tok_raw >= 0 && tok_raw < Tb) {
+      long long prow = row_base + tok_raw;
+      if (kKv != kKvContig) {
+        const int blk = tok_raw / pk.page_size;
+        const int page =
+            blk < pk.max_pages ? pk.block_table[(long long)b * pk.max_pages + blk] : -1;
+        prow = (page >= 0 && page < pk.n_pages)
+                   ? (long long)page * pk.page_size + tok_raw % pk.page_size
+                   : -1;
+      }
+      if (prow >= 0) {
+        const unsigned char* p = rows_base + (size_t)prow * row_bytes;
+        for (size_t o = 0; o < row_bytes; o += 128)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(p + o));
       }
     }
   };
@@ -680,7 +678,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   };
 
   if (t_lo < t_hi) {
-    tile_ids(t_lo, 0);
+    tile_ids(load_tok(t_lo), 0);
     __syncthreads();
 #pragma unroll 1
     for (int j = 0; j < 4; ++j) gather_pair(0, j);
@@ -688,6 +686,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   for (int t = t_lo; t < t_hi; ++t) {
     const int cur = (t - t_lo) & 1;
     const uint32_t ph = (uint32_t)cur;
+    const int tok_next = t + 1 < t_hi ? load_tok(t + 1) : -1;  // in flight during step 1
     // ---- 1. S^T = C q^T  (M = 128 rows, N = 64 heads, K = 512), two column
     // blocks at a time as their rows land
 #pragma unroll
@@ -709,7 +708,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       }
     }
     // the next tile's ids meanwhile (slot cur ^ 1 is free: its tile is done)
-    if (t + 1 < t_hi) tile_ids(t + 1, cur ^ 1);
+    if (t + 1 < t_hi) tile_ids(tok_next, cur ^ 1);
     const bool s_done = mbar_wait_bounded(&c.s_ready, ph, wait_ns);
     tc_fence_after();
 
@@ -801,12 +800,12 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     }
 
     // ---- 3. O^T += C^T P^T  (M = 128 latent x 4 chunks, N = 64 heads, K = 128
-    // rows); chunk mc reads column blocks 2 mc and 2 mc + 1 and commits alone
-    if (threadIdx.x == 0) {
-      tc_fence_after();
-      constexpr uint32_t idesc = umma_idesc_bf16(128, kHs, true, true);
-#pragma unroll
-      for (int mc = 0; mc < 4; ++mc) {
+    // rows); chunk mc reads column blocks 2 mc and 2 mc + 1 and commits alone.
+    // The issuing thread stays one chunk ahead: it would otherwise wait for
+    // room in the tensor pipe's queue while every thread waits for it.
+    auto issue_pv = [&](int mc) {
+      if (threadIdx.x == 0) {
+        constexpr uint32_t idesc = umma_idesc_bf16(128, kHs, true, true);
 #pragma unroll
         for (int kr = 0; kr < 8; ++kr) {
           const uint64_t a = umma_desc_sw128(kvb + 2 * mc * kKvBlock + kr * 2048, kKvBlock, 1024);
@@ -815,15 +814,19 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         }
         umma_commit(&c.o_ready[mc]);
       }
-    }
+    };
+    if (threadIdx.x == 0) tc_fence_after();
+    issue_pv(0);
     // as each chunk completes, its two column blocks take the next tile's rows
 #pragma unroll 1
     for (int mc = 0; mc < 4; ++mc) {
+      if (mc + 1 < 4) issue_pv(mc + 1);
       const bool o_done = mbar_wait_bounded(&c.o_ready[mc], ph, wait_ns);
       tc_fence_after();
       ok = __syncthreads_and(o_done) != 0;
       if (!ok) {
-        pending = &c.o_ready[3];  // commits complete in order: the last covers all
+        // commits complete in order: the last one issued (chunk mc + 1) covers all
+        pending = &c.o_ready[mc + 1 < 4 ? mc + 1 : 3];
         pend_ph = ph;
         break;
       }
