@@ -629,14 +629,23 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       }
     }
   };
+  // bf16 rows: this thread copies sixteen bytes of rows (tid / 16) + 16 k,
+  // k = 0..7, in every block pair; their cache rows are read once per tile
+  int my_rows[8];
+  auto load_my_rows = [&](int buf) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) my_rows[k] = c.prow[buf][(threadIdx.x >> 4) + 16 * k];
+  };
   // column blocks 2j and 2j + 1 (latent 128 j .. 128 j + 127) of the tile whose
-  // cache rows are in slot `buf`, as one cp.async group
+  // cache rows are in slot `buf` (bf16: in my_rows), as one cp.async group
   auto gather_pair = [&](int buf, int j) {
     if (kKv != kKvPagedE4M3) {
       const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(rows_base);
-      for (int i = threadIdx.x; i < kRows * 16; i += kThreadsM) {
-        const int rr = i >> 4, ch = 16 * j + (i & 15);
-        const int prow = c.prow[buf][rr];
+      const int ch = 16 * j + (threadIdx.x & 15);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int rr = (threadIdx.x >> 4) + 16 * k;
+        const int prow = my_rows[k];
         const bool okr = prow >= 0;
         cp_async16(smem_u32(sb + kOffKvS + (ch >> 3) * kKvBlock + rr * 128 +
                             (((ch & 7) ^ (rr & 7)) << 4)),
@@ -680,6 +689,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   if (t_lo < t_hi) {
     tile_ids(load_tok(t_lo), 0);
     __syncthreads();
+    if (kKv != kKvPagedE4M3) load_my_rows(0);
 #pragma unroll 1
     for (int j = 0; j < 4; ++j) gather_pair(0, j);
   }
@@ -817,6 +827,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     };
     if (threadIdx.x == 0) tc_fence_after();
     issue_pv(0);
+    if (kKv != kKvPagedE4M3 && t + 1 < t_hi) load_my_rows(cur ^ 1);
     // as each chunk completes, its two column blocks take the next tile's rows
 #pragma unroll 1
     for (int mc = 0; mc < 4; ++mc) {
