@@ -466,6 +466,7 @@ struct SCtl {
   uint64_t s_ready, o_ready[4];
   uint32_t tmem_base;
   int rescale;
+  int fail;  // a thread saw an MMA chunk not complete in time
 };
 constexpr size_t kOffKvS = 0;
 constexpr size_t kOffQS = kOffKvS + 8 * (size_t)kKvBlock;
@@ -527,6 +528,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 #pragma unroll
     for (int mc = 0; mc < 4; ++mc) mbar_init(&c.o_ready[mc], 1);
     fence_mbar_init();
+    c.fail = 0;
   }
   if (warp == 1) {
     tmem_alloc<kTmemColsS>(&c.tmem_base);
@@ -739,7 +741,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     if (threadIdx.x == 0) c.rescale = 0;
     // Every thread takes the same branch: the scores exist only if every thread
     // saw them complete.  After a timeout nothing more is issued.
-    ok = __syncthreads_and(s_done) != 0;
+    ok = __syncthreads_and(s_done) != 0 && c.fail == 0;
     if (!ok) {
       if (issue) {
         pending = &c.s_ready;
@@ -828,23 +830,25 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     if (threadIdx.x == 0) tc_fence_after();
     issue_pv(0);
     if (kKv != kKvPagedE4M3 && t + 1 < t_hi) load_my_rows(cur ^ 1);
-    // as each chunk completes, its two column blocks take the next tile's rows
+    // As each chunk completes, its two column blocks take the next tile's rows.
+    // Every thread waits for the chunk itself (no block barrier: the issuing
+    // thread may still be queueing the next chunk).  A thread that gives up
+    // skips its copies and raises c.fail, which every thread reads after the
+    // next block barrier (the next tile's softmax, or the end of the loop).
 #pragma unroll 1
     for (int mc = 0; mc < 4; ++mc) {
       if (mc + 1 < 4) issue_pv(mc + 1);
       const bool o_done = mbar_wait_bounded(&c.o_ready[mc], ph, wait_ns);
       tc_fence_after();
-      ok = __syncthreads_and(o_done) != 0;
-      if (!ok) {
-        // commits complete in order: the last one issued (chunk mc + 1) covers all
-        pending = &c.o_ready[mc + 1 < 4 ? mc + 1 : 3];
-        pend_ph = ph;
-        break;
-      }
-      if (t + 1 < t_hi) gather_pair(cur ^ 1, mc);
+      if (!o_done) c.fail = 1;
+      if (o_done && t + 1 < t_hi) gather_pair(cur ^ 1, mc);
     }
-    if (!ok) break;
+    pending = &c.o_ready[3];  // the last chunk's commit covers every MMA so far
+    pend_ph = ph;
   }
+  // the last tile's chunks: each thread waited for them; all must have landed
+  ok = __syncthreads_and(ok) != 0 && c.fail == 0;
+  if (ok) pending = nullptr;
   cp_async_wait<0>();  // no copy into shared memory is left in flight
 
   // ---- 5. epilogue: O^T -> shared [head][latent] fp32, then whole rows out
