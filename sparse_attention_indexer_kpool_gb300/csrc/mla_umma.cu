@@ -466,7 +466,8 @@ struct SCtl {
   uint64_t s_ready, o_ready[4];
   uint32_t tmem_base;
   int rescale;
-  int fail;  // a thread saw an MMA chunk not complete in time
+  int fail;       // a thread saw an MMA chunk not complete in time
+  int exceed[2];  // [tile parity]: a score passed its head's reference by the margin
 };
 constexpr size_t kOffKvS = 0;
 constexpr size_t kOffQS = kOffKvS + 8 * (size_t)kKvBlock;
@@ -529,6 +530,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     for (int mc = 0; mc < 4; ++mc) mbar_init(&c.o_ready[mc], 1);
     fence_mbar_init();
     c.fail = 0;
+    c.exceed[0] = c.exceed[1] = 0;
   }
   if (warp == 1) {
     tmem_alloc<kTmemColsS>(&c.tmem_base);
@@ -578,6 +580,9 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   const unsigned long long wait_ns = drill ? kDrillWaitNs : kWaitNs;
   uint64_t* pending = nullptr;  // MMAs issued whose completion was not seen
   uint32_t pend_ph = 0;
+  float l_part[32];  // row r's softmax sums of heads 32 hg .. (same reference as O^T)
+#pragma unroll
+  for (int i = 0; i < 32; ++i) l_part[i] = 0.f;
 
   // token id of row (threadIdx.x mod 128) of tile t, as stored (-1: none)
   auto load_tok = [&](int t) -> int {
@@ -724,7 +729,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     const bool s_done = mbar_wait_bounded(&c.s_ready, ph, wait_ns);
     tc_fence_after();
 
-    // ---- 2. softmax against the running max (thread = row r, heads 32 hg ..)
+    // ---- 2. softmax against the running reference (thread = row r, heads 32 hg ..)
     float z[32];
     tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(hg * 32), z);
     const bool row_ok = c.tok[cur][r] >= 0;
@@ -732,13 +737,23 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     const float zs = kKv == kKvPagedE4M3 ? sm_scale * kLog2e * rsr : sm_scale * kLog2e;
 #pragma unroll
     for (int i = 0; i < 32; ++i) z[i] = row_ok ? z[i] * zs : -INFINITY;
-    {
-      float tt[32];
+    // The tile's max per head is needed only where a score passes the head's
+    // reference by more than the margin (always on a head's first valid row:
+    // the reference starts at -inf); a flag per tile says whether any did.
+    float mv[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) tt[i] = z[i];
-      c.red[qw][hg * 32 + lane] = transpose_reduce32<true>(tt, lane);
+    for (int q4 = 0; q4 < 8; ++q4) {
+      const float4 m4 = reinterpret_cast<const float4*>(c.m_run + hg * 32)[q4];
+      mv[4 * q4] = m4.x;
+      mv[4 * q4 + 1] = m4.y;
+      mv[4 * q4 + 2] = m4.z;
+      mv[4 * q4 + 3] = m4.w;
     }
-    if (threadIdx.x == 0) c.rescale = 0;
+    bool exceed = false;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) exceed |= z[i] > mv[i] + kRescaleAt;
+    if (exceed) c.exceed[cur] = 1;
+    if (threadIdx.x == 0) c.exceed[cur ^ 1] = 0;  // read last in the previous tile
     // Every thread takes the same branch: the scores exist only if every thread
     // saw them complete.  After a timeout nothing more is issued.
     ok = __syncthreads_and(s_done) != 0 && c.fail == 0;
@@ -749,35 +764,49 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       }
       break;
     }
-    if (threadIdx.x < kHs) {
-      const int h = threadIdx.x;
-      const float tmax = fmaxf(fmaxf(c.red[0][h], c.red[1][h]), fmaxf(c.red[2][h], c.red[3][h]));
-      const float m_old = c.m_run[h];
-      float m_new = m_old, alpha = 1.f;
-      if (m_old == -INFINITY) {
-        m_new = tmax;  // first rows of this head: nothing accumulated yet
-      } else if (tmax > m_old + kRescaleAt) {
-        m_new = tmax;
-        alpha = exp2f(m_old - m_new);
-        c.rescale = 1;
+    const bool full = c.exceed[cur] != 0;
+    bool rescale = false;
+    if (full) {
+      {
+        float tt[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) tt[i] = z[i];
+        c.red[qw][hg * 32 + lane] = transpose_reduce32<true>(tt, lane);
       }
-      c.m_run[h] = m_new;
-      c.alpha[h] = alpha;
+      if (threadIdx.x == 0) c.rescale = 0;
+      __syncthreads();
+      if (threadIdx.x < kHs) {
+        const int h = threadIdx.x;
+        const float tmax =
+            fmaxf(fmaxf(c.red[0][h], c.red[1][h]), fmaxf(c.red[2][h], c.red[3][h]));
+        const float m_old = c.m_run[h];
+        float m_new = m_old, alpha = 1.f;
+        if (m_old == -INFINITY) {
+          m_new = tmax;  // first rows of this head: nothing accumulated yet
+        } else if (tmax > m_old + kRescaleAt) {
+          m_new = tmax;
+          alpha = exp2f(m_old - m_new);
+          c.rescale = 1;
+        }
+        c.m_run[h] = m_new;
+        c.alpha[h] = alpha;
+      }
+      __syncthreads();
+      rescale = c.rescale != 0;
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        const float4 m4 = reinterpret_cast<const float4*>(c.m_run + hg * 32)[q4];
+        mv[4 * q4] = m4.x;
+        mv[4 * q4 + 1] = m4.y;
+        mv[4 * q4 + 2] = m4.z;
+        mv[4 * q4 + 3] = m4.w;
+      }
     }
-    __syncthreads();
     // p = 2^(z - m); a head with no row so far (m = -inf) has only z = -inf
     // here, and 2^-inf = 0
     float p[32];
 #pragma unroll
-    for (int q4 = 0; q4 < 8; ++q4) {
-      const float4 m4 = reinterpret_cast<const float4*>(c.m_run + hg * 32)[q4];
-      const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float m = mv[e] == -INFINITY ? 0.f : mv[e];
-        p[4 * q4 + e] = ex2_fast(z[4 * q4 + e] - m);
-      }
-    }
+    for (int i = 0; i < 32; ++i) p[i] = ex2_fast(z[i] - (mv[i] == -INFINITY ? 0.f : mv[i]));
     // row r of P: heads 32 hg .. 32 hg + 31 are the 16-byte chunks 4 hg .. 4 hg + 3
     // of its 128-byte line, at the swizzled position chunk ^ (r & 7)
 #pragma unroll
@@ -789,27 +818,30 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                                  pack_bf16(p[8 * q + 6] * sc, p[8 * q + 7] * sc));
       *reinterpret_cast<uint4*>(sb + kOffPtS + r * 128 + (((hg * 4 + q) ^ (r & 7)) << 4)) = w;
     }
-    c.red[qw][hg * 32 + lane] = transpose_reduce32<false>(p, lane);
-    // a raised reference: rescale what O^T holds so far (never on the first tile)
-    if (c.rescale && t > t_lo) {
-#pragma unroll 1
-      for (int mc = 0; mc < 4; ++mc) {
-        float o[32];
-        const uint32_t ta = tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHs + mc * kHs + hg * 32);
-        tmem_ld32(ta, o);
+    // this row's running sums per head (reduced over the rows at the end), and
+    // on a raised reference what O^T holds so far, rescaled first
+    if (rescale) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] *= c.alpha[hg * 32 + i];
-        tmem_st32(ta, o);
+      for (int i = 0; i < 32; ++i) l_part[i] = l_part[i] * c.alpha[hg * 32 + i] + p[i];
+      if (t > t_lo) {
+#pragma unroll 1
+        for (int mc = 0; mc < 4; ++mc) {
+          float o[32];
+          const uint32_t ta =
+              tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(kHs + mc * kHs + hg * 32);
+          tmem_ld32(ta, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= c.alpha[hg * 32 + i];
+          tmem_st32(ta, o);
+        }
       }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) l_part[i] += p[i];
     }
     fence_proxy_async_smem();  // P is read by the tensor cores next
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x < kHs) {
-      const int h = threadIdx.x;
-      const float s = (c.red[0][h] + c.red[1][h]) + (c.red[2][h] + c.red[3][h]);
-      c.l_run[h] = c.l_run[h] * c.alpha[h] + s;
-    }
 
     // ---- 3. O^T += C^T P^T  (M = 128 latent x 4 chunks, N = 64 heads, K = 128
     // rows); chunk mc reads column blocks 2 mc and 2 mc + 1 and commits alone.
@@ -851,8 +883,15 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   if (ok) pending = nullptr;
   cp_async_wait<0>();  // no copy into shared memory is left in flight
 
-  // ---- 5. epilogue: O^T -> shared [head][latent] fp32, then whole rows out
+  // ---- 5. epilogue: the sums over the rows, O^T -> shared [head][latent] fp32,
+  // then whole rows out
   if (ok) {
+    c.red[qw][hg * 32 + lane] = transpose_reduce32<false>(l_part, lane);
+    __syncthreads();
+    if (threadIdx.x < kHs) {
+      const int h = threadIdx.x;
+      c.l_run[h] = (c.red[0][h] + c.red[1][h]) + (c.red[2][h] + c.red[3][h]);
+    }
     float* stage = reinterpret_cast<float*>(sb + kOffKvS);
     const bool any = t_hi > t_lo;
 #pragma unroll 1
