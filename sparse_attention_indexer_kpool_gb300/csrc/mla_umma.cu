@@ -643,8 +643,33 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 #pragma unroll
     for (int k = 0; k < 8; ++k) my_rows[k] = c.prow[buf][(threadIdx.x >> 4) + 16 * k];
   };
+  // E4M3 rows: a tile's codes, all sixteen 16-byte loads per thread, go to
+  // registers ahead of the blocks being free (rows (i / 8), i = u * 256 + tid,
+  // codes 16 (8 j + i mod 8) .. of block pair j), with the rows' scales
+  constexpr int kE4Per = kRows * 8 / kThreadsM;
+  uint4 e_raw[kKv == kKvPagedE4M3 ? 4 : 1][kE4Per];
+  auto e4m3_load = [&](int buf) {
+    if (kKv == kKvPagedE4M3) {
+      const uint4* src = reinterpret_cast<const uint4*>(rows_base);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int u = 0; u < kE4Per; ++u) {
+          const int i = u * kThreadsM + threadIdx.x;
+          const int prow = c.prow[buf][i >> 3];
+          e_raw[j][u] = prow >= 0 ? __ldg(src + (long long)prow * (kL / 16) + 8 * j + (i & 7))
+                                  : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      if (threadIdx.x < kRows) {
+        const int prow = c.prow[buf][threadIdx.x];
+        c.rs[buf][threadIdx.x] = prow >= 0 ? pk.row_scale[prow] : 0.f;
+      }
+    }
+  };
   // column blocks 2j and 2j + 1 (latent 128 j .. 128 j + 127) of the tile whose
-  // cache rows are in slot `buf` (bf16: in my_rows), as one cp.async group
+  // cache rows are in slot `buf` (bf16: in my_rows; E4M3: codes in e_raw), as
+  // one cp.async group
   auto gather_pair = [&](int buf, int j) {
     if (kKv != kKvPagedE4M3) {
       const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(rows_base);
@@ -659,25 +684,12 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                    okr ? src + (long long)prow * kL + ch * 8 : src, okr);
       }
     } else {
-      const uint4* src = reinterpret_cast<const uint4*>(rows_base);
-      constexpr int kPer = kRows * 8 / kThreadsM;  // sixteen-byte loads of 16 codes
-      uint4 raw[kPer];
+      // the codes were loaded into e_raw by e4m3_load; convert and store
 #pragma unroll
-      for (int u = 0; u < kPer; ++u) {
-        const int i = u * kThreadsM + threadIdx.x;
-        const int prow = c.prow[buf][i >> 3];
-        raw[u] = prow >= 0 ? __ldg(src + (long long)prow * (kL / 16) + 8 * j + (i & 7))
-                           : make_uint4(0u, 0u, 0u, 0u);
-      }
-      if (j == 0 && threadIdx.x < kRows) {
-        const int prow = c.prow[buf][threadIdx.x];
-        c.rs[buf][threadIdx.x] = prow >= 0 ? pk.row_scale[prow] : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < kPer; ++u) {
+      for (int u = 0; u < kE4Per; ++u) {
         const int i = u * kThreadsM + threadIdx.x;
         const int rr = i >> 3, c16 = 8 * j + (i & 7);
-        const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+        const uint32_t w[4] = {e_raw[j][u].x, e_raw[j][u].y, e_raw[j][u].z, e_raw[j][u].w};
 #pragma unroll
         for (int hf2 = 0; hf2 < 2; ++hf2) {
           const int ch = 2 * c16 + hf2;
@@ -697,7 +709,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     tile_ids(load_tok(t_lo), 0);
     __syncthreads();
     if (kKv != kKvPagedE4M3) load_my_rows(0);
-#pragma unroll 1
+    e4m3_load(0);
+#pragma unroll
     for (int j = 0; j < 4; ++j) gather_pair(0, j);
   }
   for (int t = t_lo; t < t_hi; ++t) {
@@ -861,13 +874,18 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     };
     if (threadIdx.x == 0) tc_fence_after();
     issue_pv(0);
-    if (kKv != kKvPagedE4M3 && t + 1 < t_hi) load_my_rows(cur ^ 1);
+    if (t + 1 < t_hi) {
+      if (kKv != kKvPagedE4M3)
+        load_my_rows(cur ^ 1);
+      else
+        e4m3_load(cur ^ 1);  // the loads fly while the PV chunks run
+    }
     // As each chunk completes, its two column blocks take the next tile's rows.
     // Every thread waits for the chunk itself (no block barrier: the issuing
     // thread may still be queueing the next chunk).  A thread that gives up
     // skips its copies and raises c.fail, which every thread reads after the
     // next block barrier (the next tile's softmax, or the end of the loop).
-#pragma unroll 1
+#pragma unroll
     for (int mc = 0; mc < 4; ++mc) {
       if (mc + 1 < 4) issue_pv(mc + 1);
       const bool o_done = mbar_wait_bounded(&c.o_ready[mc], ph, wait_ns);
