@@ -664,9 +664,12 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                                   : make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      if (threadIdx.x < kRows) {
-        const int prow = c.prow[buf][threadIdx.x];
-        c.rs[buf][threadIdx.x] = prow >= 0 ? pk.row_scale[prow] : 0.f;
+      // the scales by threads 128..255: thread 0 issues the MMAs and must not
+      // wait for a load here
+      if (threadIdx.x >= kRows) {
+        const int rr = threadIdx.x - kRows;
+        const int prow = c.prow[buf][rr];
+        c.rs[buf][rr] = prow >= 0 ? pk.row_scale[prow] : 0.f;
       }
     }
   };
