@@ -633,12 +633,7 @@ size_t topk_workspace_size(int Q, int P_ld, int select_k) {
 }
 size_t select_workspace_size(int Q, int P_ld, int select_k) {
   (void)P_ld; (void)select_k;
-  return align256((size_t)Q * kBins * 4) + 256;  // histograms, then the tile counter
-}
-
-int* select_workspace_counter(void* workspace, int Q) {
-  return reinterpret_cast<int*>(static_cast<unsigned char*>(workspace) +
-                                align256((size_t)Q * kBins * 4));
+  return align256((size_t)Q * kBins * 4);  // the per-query histograms
 }
 
 uint32_t* topk_workspace_hist(void* workspace) { return static_cast<uint32_t*>(workspace); }
