@@ -465,6 +465,12 @@ size_t dsa_indexer_project_workspace_size(int T, int hidden, int q_rank, int H, 
  * DSA_ERR_INVALID_ARG for an unknown drill.
  */
 #define DSA_DRILL_SKIP_ARM 1
+/* The streaming attention kernel (many queries, or any paged call) issues its
+ * MMAs but arms none of the barriers of its PV chunks: those waits run out with
+ * MMAs in flight; the kernel issues nothing more, drains them through one more
+ * commit, frees its tensor memory and returns (DSA_DEV_TIMEOUT).  The other
+ * tensor-core kernels take it as DSA_DRILL_SKIP_ARM. */
+#define DSA_DRILL_SKIP_PV_COMMIT 2
 int dsa_set_failure_drill(int drill);
 
 /* Human-readable name of a DSA_* return code (static string). */

@@ -179,7 +179,8 @@ int dsa_version(void) { return 10000; }
 uint64_t dsa_kernel_launches(void) { return dsa::launch_counter().load(); }
 
 int dsa_set_failure_drill(int drill) {
-  if (drill != 0 && drill != DSA_DRILL_SKIP_ARM) return DSA_ERR_INVALID_ARG;
+  if (drill != 0 && drill != DSA_DRILL_SKIP_ARM && drill != DSA_DRILL_SKIP_PV_COMMIT)
+    return DSA_ERR_INVALID_ARG;
   dsa::g_drill.store(drill, std::memory_order_relaxed);
   return DSA_OK;
 }

@@ -464,6 +464,7 @@ struct SCtl {
   int tok[2][kRows];
   int prow[2][kRows];
   uint64_t s_ready, o_ready[4];
+  uint64_t drain;  // give-up path: one commit that tracks every MMA issued
   uint32_t tmem_base;
   int rescale;
   int fail;       // a thread saw an MMA chunk not complete in time
@@ -528,6 +529,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     mbar_init(&c.s_ready, 1);
 #pragma unroll
     for (int mc = 0; mc < 4; ++mc) mbar_init(&c.o_ready[mc], 1);
+    mbar_init(&c.drain, 1);
     fence_mbar_init();
     c.fail = 0;
     c.exceed[0] = c.exceed[1] = 0;
@@ -575,11 +577,12 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       kKv == kKvContig ? static_cast<const void*>(kv) : pk.pages);
   bool ok = true;
   int r = qw * 32 + lane;  // this thread's row of the tile in the softmax
-  // a failure drill issues no MMA and arms no barrier: the first wait runs out
-  const bool issue = drill == 0;
+  // Failure drills: DSA_DRILL_SKIP_ARM issues no MMA and arms no barrier (the
+  // first wait runs out); DSA_DRILL_SKIP_PV_COMMIT issues every MMA but arms
+  // no PV chunk barrier (those waits run out with MMAs in flight).
+  const bool issue = drill != DSA_DRILL_SKIP_ARM;
+  const bool arm_pv = drill != DSA_DRILL_SKIP_PV_COMMIT;
   const unsigned long long wait_ns = drill ? kDrillWaitNs : kWaitNs;
-  uint64_t* pending = nullptr;  // MMAs issued whose completion was not seen
-  uint32_t pend_ph = 0;
   float l_part[32];  // row r's softmax sums of heads 32 hg .. (same reference as O^T)
 #pragma unroll
   for (int i = 0; i < 32; ++i) l_part[i] = 0.f;
@@ -733,12 +736,17 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       __syncthreads();
       tc_fence_after();
       if (threadIdx.x == 0 && issue) {
-        constexpr uint32_t idesc = umma_idesc_bf16(kRows, kHs, false);
+        // after a thread gave up on a PV chunk (c.fail, written before this
+        // barrier) no MMA is issued; the commit still comes, and completes once
+        // the MMAs already issued have drained
+        if (c.fail == 0) {
+          constexpr uint32_t idesc = umma_idesc_bf16(kRows, kHs, false);
 #pragma unroll
-        for (int kk = 8 * j; kk < 8 * j + 8; ++kk) {
-          const uint32_t blk = kk >> 2, off = (kk & 3) * 32;
-          umma_bf16(tmem, sw128_desc(kvb + blk * kKvBlock + off),
-                    sw128_desc(qb + blk * kQBlockS + off), idesc, kk > 0 ? 1u : 0u);
+          for (int kk = 8 * j; kk < 8 * j + 8; ++kk) {
+            const uint32_t blk = kk >> 2, off = (kk & 3) * 32;
+            umma_bf16(tmem, sw128_desc(kvb + blk * kKvBlock + off),
+                      sw128_desc(qb + blk * kQBlockS + off), idesc, kk > 0 ? 1u : 0u);
+          }
         }
         if (j == 3) umma_commit(&c.s_ready);
       }
@@ -776,13 +784,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     // Every thread takes the same branch: the scores exist only if every thread
     // saw them complete.  After a timeout nothing more is issued.
     ok = __syncthreads_and(s_done) != 0 && c.fail == 0;
-    if (!ok) {
-      if (issue) {
-        pending = &c.s_ready;
-        pend_ph = ph;
-      }
-      break;
-    }
+    if (!ok) break;
     const bool full = c.exceed[cur] != 0;
     bool rescale = false;
     if (full) {
@@ -875,7 +877,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
           const uint64_t bd = umma_desc_sw128(ptb + kr * 2048, kPBytesS, 1024);
           umma_bf16(tmem + kHs + mc * kHs, a, bd, idesc, (t > t_lo || kr > 0) ? 1u : 0u);
         }
-        umma_commit(&c.o_ready[mc]);
+        if (arm_pv) umma_commit(&c.o_ready[mc]);
       }
     };
     if (threadIdx.x == 0) tc_fence_after();
@@ -899,12 +901,9 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       if (!o_done) c.fail = 1;
       if (o_done && t + 1 < t_hi) gather_pair(cur ^ 1, mc);
     }
-    pending = &c.o_ready[3];  // the last chunk's commit covers every MMA so far
-    pend_ph = ph;
   }
   // the last tile's chunks: each thread waited for them; all must have landed
   ok = __syncthreads_and(ok) != 0 && c.fail == 0;
-  if (ok) pending = nullptr;
   cp_async_wait<0>();  // no copy into shared memory is left in flight
 
   // ---- 5. epilogue: the sums over the rows, O^T -> shared [head][latent] fp32,
@@ -963,8 +962,12 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       part_ml[((qh0 + threadIdx.x) * n_split + split) * 2 + 1] = 0.f;
     }
   }
-  // TMEM is freed only after every MMA this CTA issued has retired (bounded).
-  if (threadIdx.x == 0 && pending != nullptr) mbar_wait_bounded(pending, pend_ph);
+  // TMEM is freed only after every MMA this CTA issued has retired: after a
+  // give-up, one more commit tracks all of them (bounded wait).
+  if (!ok && issue && threadIdx.x == 0) {
+    umma_commit(&c.drain);
+    mbar_wait_bounded(&c.drain, 0);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -300,9 +300,11 @@ def dsa_kernel_launches() -> int:
 
 
 DSA_DRILL_SKIP_ARM = 1
+DSA_DRILL_SKIP_PV_COMMIT = 2
 
 
 def dsa_set_failure_drill(drill: int) -> None:
-    """Arm (DSA_DRILL_SKIP_ARM) or disarm (0) the give-up drill of the tensor-core
-    kernels, process wide (tests of failure detection only)."""
+    """Arm (DSA_DRILL_SKIP_ARM, DSA_DRILL_SKIP_PV_COMMIT) or disarm (0) a give-up
+    drill of the tensor-core kernels, process wide (tests of failure detection
+    only)."""
     _check("dsa_set_failure_drill", _lib.load().dsa_set_failure_drill(int(drill)))

@@ -116,9 +116,9 @@ def test_rejected_and_empty_calls_launch_nothing(lib):
 
 
 def test_failure_drill_setting(lib):
-    """The drill switch takes 0 and the one defined drill, and refuses others."""
-    drill = header_define("DSA_DRILL_SKIP_ARM")
-    assert lib.dsa_set_failure_drill(drill) == ERR["DSA_OK"]
+    """The drill switch takes 0 and the defined drills, and refuses others."""
+    for name in ("DSA_DRILL_SKIP_ARM", "DSA_DRILL_SKIP_PV_COMMIT"):
+        assert lib.dsa_set_failure_drill(header_define(name)) == ERR["DSA_OK"]
     assert lib.dsa_set_failure_drill(0) == ERR["DSA_OK"]
     assert lib.dsa_set_failure_drill(7) == ERR["DSA_ERR_INVALID_ARG"]
     assert lib.dsa_set_failure_drill(-1) == ERR["DSA_ERR_INVALID_ARG"]

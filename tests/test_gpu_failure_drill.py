@@ -27,8 +27,11 @@ def decode_batch(n_seq=4, seed=21, select_k=64):
 
 
 class drill:
+    def __init__(self, mode=ops.DSA_DRILL_SKIP_ARM):
+        self.mode = mode
+
     def __enter__(self):
-        ops.dsa_set_failure_drill(ops.DSA_DRILL_SKIP_ARM)
+        ops.dsa_set_failure_drill(self.mode)
 
     def __exit__(self, *exc):
         ops.dsa_set_failure_drill(0)
@@ -79,6 +82,39 @@ def test_attention_kernels_give_up_and_recover(n_seq, select_k):
         torch.cuda.synchronize()
     assert int(buf.status.item()) & TIMEOUT
     # the give-up path reports "nothing selected" for the CTAs that gave up
+    assert torch.isinf(buf.lse).all() and (buf.out == 0).all()
+    buf.status.zero_()
+    pipeline.attend(bt, buf)
+    torch.cuda.synchronize()
+    assert int(buf.status.item()) == 0
+    assert_same(buf, ref, ("out", "lse"))
+
+
+@pytest.mark.parametrize("case", ["eight_tiles_per_cta", "one_tile_per_cta"])
+def test_streaming_attention_gives_up_with_mmas_in_flight(case):
+    """The drill that lets the streaming attention kernel issue its MMAs but arm
+    none of its PV chunk barriers: those waits run out with MMAs in flight (64
+    queries x 2048 rows: eight 128-row tiles per CTA, two splits; 320 queries
+    x 128 rows: one tile per CTA).  The kernel issues nothing more, drains
+    through one more commit, frees its tensor memory and returns: the call is
+    flagged, its outputs read "nothing selected", and the same call afterwards
+    gives the outputs it gave before."""
+    if case == "eight_tiles_per_cta":
+        bt = decode_batch(n_seq=64, seed=24, select_k=512)
+    else:
+        geo = Geometry(D=128, H=32, kpool=4, select_k=32, out_width=128, Hm=64, L=512,
+                       dtype="bf16")
+        bt = synth.make_batch(geo, [600 + 3 * i for i in range(320)], [0] * 320, device=DEV,
+                              seed=25)
+    buf = pipeline.LayerBuffers.alloc(bt)
+    pipeline.run_layer(bt, buf)
+    torch.cuda.synchronize()
+    assert int(buf.status.item()) == 0
+    ref = snapshot(buf)
+    with drill(ops.DSA_DRILL_SKIP_PV_COMMIT):
+        pipeline.attend(bt, buf)
+        torch.cuda.synchronize()
+    assert int(buf.status.item()) & TIMEOUT
     assert torch.isinf(buf.lse).all() and (buf.out == 0).all()
     buf.status.zero_()
     pipeline.attend(bt, buf)
