@@ -467,7 +467,6 @@ struct SCtl {
   uint64_t drain;  // give-up path: one commit that tracks every MMA issued
   uint32_t tmem_base;
   int rescale;
-  int fail;       // a thread saw an MMA chunk not complete in time
   int exceed[2];  // [tile parity]: a score passed its head's reference by the margin
 };
 constexpr size_t kOffKvS = 0;
@@ -531,7 +530,6 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     for (int mc = 0; mc < 4; ++mc) mbar_init(&c.o_ready[mc], 1);
     mbar_init(&c.drain, 1);
     fence_mbar_init();
-    c.fail = 0;
     c.exceed[0] = c.exceed[1] = 0;
   }
   if (warp == 1) {
@@ -583,6 +581,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   const bool issue = drill != DSA_DRILL_SKIP_ARM;
   const bool arm_pv = drill != DSA_DRILL_SKIP_PV_COMMIT;
   const unsigned long long wait_ns = drill ? kDrillWaitNs : kWaitNs;
+  bool pv_failed = false;  // this thread's wait on a PV chunk ran out
   float l_part[32];  // row r's softmax sums of heads 32 hg .. (same reference as O^T)
 #pragma unroll
   for (int i = 0; i < 32; ++i) l_part[i] = 0.f;
@@ -728,18 +727,21 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     const int tok_next = t + 1 < t_hi ? load_tok(t + 1) : -1;  // in flight during step 1
     // ---- 1. S^T = C q^T  (M = 128 rows, N = 64 heads, K = 512), two column
     // blocks at a time as their rows land
+    bool go = true;  // no thread gave up on a PV chunk (the tile's first barrier says)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       cp_async_wait_pending(3 - j);  // the query's group is older than every row group
       fence_proxy_async_smem();
       tc_fence_before();
-      __syncthreads();
+      if (j == 0)
+        go = __syncthreads_or(pv_failed) == 0;
+      else
+        __syncthreads();
       tc_fence_after();
       if (threadIdx.x == 0 && issue) {
-        // after a thread gave up on a PV chunk (c.fail, written before this
-        // barrier) no MMA is issued; the commit still comes, and completes once
-        // the MMAs already issued have drained
-        if (c.fail == 0) {
+        // after a thread gave up on a PV chunk no MMA is issued; the commit
+        // still comes, and completes once the MMAs already issued have drained
+        if (go) {
           constexpr uint32_t idesc = umma_idesc_bf16(kRows, kHs, false);
 #pragma unroll
           for (int kk = 8 * j; kk < 8 * j + 8; ++kk) {
@@ -783,7 +785,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     if (threadIdx.x == 0) c.exceed[cur ^ 1] = 0;  // read last in the previous tile
     // Every thread takes the same branch: the scores exist only if every thread
     // saw them complete.  After a timeout nothing more is issued.
-    ok = __syncthreads_and(s_done) != 0 && c.fail == 0;
+    ok = __syncthreads_and(s_done) != 0 && go;
     if (!ok) break;
     const bool full = c.exceed[cur] != 0;
     bool rescale = false;
@@ -891,19 +893,19 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     // As each chunk completes, its two column blocks take the next tile's rows.
     // Every thread waits for the chunk itself (no block barrier: the issuing
     // thread may still be queueing the next chunk).  A thread that gives up
-    // skips its copies and raises c.fail, which every thread reads after the
-    // next block barrier (the next tile's softmax, or the end of the loop).
+    // skips its copies and says so at the next block barrier (the next tile's
+    // first one, or the end of the loop).
 #pragma unroll
     for (int mc = 0; mc < 4; ++mc) {
       if (mc + 1 < 4) issue_pv(mc + 1);
       const bool o_done = mbar_wait_bounded(&c.o_ready[mc], ph, wait_ns);
       tc_fence_after();
-      if (!o_done) c.fail = 1;
+      if (!o_done) pv_failed = true;
       if (o_done && t + 1 < t_hi) gather_pair(cur ^ 1, mc);
     }
   }
   // the last tile's chunks: each thread waited for them; all must have landed
-  ok = __syncthreads_and(ok) != 0 && c.fail == 0;
+  ok = __syncthreads_and(ok && !pv_failed) != 0;
   cp_async_wait<0>();  // no copy into shared memory is left in flight
 
   // ---- 5. epilogue: the sums over the rows, O^T -> shared [head][latent] fp32,
