@@ -510,20 +510,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           continue;  // keep walking so that every warp meets the same barriers
         tc_fence_after();
         const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N);
-#pragma unroll
-        for (int u = 0; u < GH; ++u) {
-          float v[32];
-          tmem_ld32(tb + (uint32_t)((qw0 + u) * kH), v);
-          const float4* w4 = reinterpret_cast<const float4*>(wq + (qw0 + u) * kH);
-          float sc = 0.f;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 w = w4[i];
-            sc = fmaf(w.x, fmaxf(v[4 * i + 0], 0.f), sc);
-            sc = fmaf(w.y, fmaxf(v[4 * i + 1], 0.f), sc);
-            sc = fmaf(w.z, fmaxf(v[4 * i + 2], 0.f), sc);
-            sc = fmaf(w.w, fmaxf(v[4 * i + 3], 0.f), sc);
-          }
+        // the score of query u at this row: sum over the heads in order
+        auto put = [&](int u, float sc) {
           if (sc == 0.f) sc = 0.f;  // -0 -> +0
           const QMeta& m = mq[u];
           if (m.valid && p < P_ld) {
@@ -531,6 +519,50 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             if (cand && q_pos != nullptr) cand = ps + kpool - 1 <= m.pos;
             scores[(long long)(gi * G + qw0 + u) * P_ld + p] = cand ? sc : -INFINITY;
             if (use_hist && cand) atomicAdd(&s_hist[score_key(sc) >> 20], 1u);
+          }
+        };
+        if constexpr (GH % 2 == 0) {
+          // two queries at a time: both loads before one wait, two independent
+          // sums (each in head order, as below)
+#pragma unroll
+          for (int u = 0; u < GH; u += 2) {
+            float va[32], vb[32];
+            tmem_ld32x2(tb + (uint32_t)((qw0 + u) * kH), tb + (uint32_t)((qw0 + u + 1) * kH), va,
+                        vb);
+            const float4* wa4 = reinterpret_cast<const float4*>(wq + (qw0 + u) * kH);
+            const float4* wb4 = reinterpret_cast<const float4*>(wq + (qw0 + u + 1) * kH);
+            float sa = 0.f, sb = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 wa = wa4[i], wb = wb4[i];
+              sa = fmaf(wa.x, fmaxf(va[4 * i + 0], 0.f), sa);
+              sb = fmaf(wb.x, fmaxf(vb[4 * i + 0], 0.f), sb);
+              sa = fmaf(wa.y, fmaxf(va[4 * i + 1], 0.f), sa);
+              sb = fmaf(wb.y, fmaxf(vb[4 * i + 1], 0.f), sb);
+              sa = fmaf(wa.z, fmaxf(va[4 * i + 2], 0.f), sa);
+              sb = fmaf(wb.z, fmaxf(vb[4 * i + 2], 0.f), sb);
+              sa = fmaf(wa.w, fmaxf(va[4 * i + 3], 0.f), sa);
+              sb = fmaf(wb.w, fmaxf(vb[4 * i + 3], 0.f), sb);
+            }
+            put(u, sa);
+            put(u + 1, sb);
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < GH; ++u) {
+            float v[32];
+            tmem_ld32(tb + (uint32_t)((qw0 + u) * kH), v);
+            const float4* w4 = reinterpret_cast<const float4*>(wq + (qw0 + u) * kH);
+            float sc = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 w = w4[i];
+              sc = fmaf(w.x, fmaxf(v[4 * i + 0], 0.f), sc);
+              sc = fmaf(w.y, fmaxf(v[4 * i + 1], 0.f), sc);
+              sc = fmaf(w.z, fmaxf(v[4 * i + 2], 0.f), sc);
+              sc = fmaf(w.w, fmaxf(v[4 * i + 3], 0.f), sc);
+            }
+            put(u, sc);
           }
         }
         tc_fence_before();
