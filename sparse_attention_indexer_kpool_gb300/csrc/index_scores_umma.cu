@@ -531,21 +531,28 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                         vb);
             const float4* wa4 = reinterpret_cast<const float4*>(wq + (qw0 + u) * kH);
             const float4* wb4 = reinterpret_cast<const float4*>(wq + (qw0 + u + 1) * kH);
-            float sa = 0.f, sb = 0.f;
+            // packed fp32 FMA: even and odd heads in the two halves, added last
+            unsigned long long sa2 = 0ull, sb2 = 0ull;
+            auto ffma2 = [](unsigned long long acc, float w0, float w1, float x0, float x1) {
+              unsigned long long w, x, d;
+              asm("mov.b64 %0, {%1, %2};" : "=l"(w) : "f"(w0), "f"(w1));
+              asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+              asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(w), "l"(x), "l"(acc));
+              return d;
+            };
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float4 wa = wa4[i], wb = wb4[i];
-              sa = fmaf(wa.x, fmaxf(va[4 * i + 0], 0.f), sa);
-              sb = fmaf(wb.x, fmaxf(vb[4 * i + 0], 0.f), sb);
-              sa = fmaf(wa.y, fmaxf(va[4 * i + 1], 0.f), sa);
-              sb = fmaf(wb.y, fmaxf(vb[4 * i + 1], 0.f), sb);
-              sa = fmaf(wa.z, fmaxf(va[4 * i + 2], 0.f), sa);
-              sb = fmaf(wb.z, fmaxf(vb[4 * i + 2], 0.f), sb);
-              sa = fmaf(wa.w, fmaxf(va[4 * i + 3], 0.f), sa);
-              sb = fmaf(wb.w, fmaxf(vb[4 * i + 3], 0.f), sb);
+              sa2 = ffma2(sa2, wa.x, wa.y, fmaxf(va[4 * i + 0], 0.f), fmaxf(va[4 * i + 1], 0.f));
+              sb2 = ffma2(sb2, wb.x, wb.y, fmaxf(vb[4 * i + 0], 0.f), fmaxf(vb[4 * i + 1], 0.f));
+              sa2 = ffma2(sa2, wa.z, wa.w, fmaxf(va[4 * i + 2], 0.f), fmaxf(va[4 * i + 3], 0.f));
+              sb2 = ffma2(sb2, wb.z, wb.w, fmaxf(vb[4 * i + 2], 0.f), fmaxf(vb[4 * i + 3], 0.f));
             }
-            put(u, sa);
-            put(u + 1, sb);
+            float a0, a1, b0, b1;
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(sa2));
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(b0), "=f"(b1) : "l"(sb2));
+            put(u, a0 + a1);
+            put(u + 1, b0 + b1);
           }
         } else {
 #pragma unroll
