@@ -496,6 +496,23 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
   return v[0];
 }
 
+// Two fp32 multiplies / adds in one packed instruction (each element rounded as
+// the scalar instruction rounds it).
+__device__ __forceinline__ void mul2(float& a0, float& a1, float b0, float b1) {
+  unsigned long long a, b;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(b0), "f"(b1));
+  asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(a) : "l"(b));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a));
+}
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  unsigned long long a, b;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(b0), "f"(b1));
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(a) : "l"(b));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a));
+}
+
 // 2^x on the special-function unit (ex2.approx, relative error below 2^-22;
 // 2^-inf = +0).
 __device__ __forceinline__ float ex2_fast(float x) {
@@ -765,7 +782,9 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     const float rsr = kKv == kKvPagedE4M3 ? c.rs[cur][r] : 1.f;
     const float zs = kKv == kKvPagedE4M3 ? sm_scale * kLog2e * rsr : sm_scale * kLog2e;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) z[i] = row_ok ? z[i] * zs : -INFINITY;
+    for (int i = 0; i < 32; i += 2) mul2(z[i], z[i + 1], zs, zs);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = row_ok ? z[i] : -INFINITY;
     // The tile's max per head is needed only where a score passes the head's
     // reference by more than the margin (always on a head's first valid row:
     // the reference starts at -inf); a flag per tile says whether any did.
@@ -860,7 +879,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) l_part[i] += p[i];
+      for (int i = 0; i < 32; i += 2) add2(l_part[i], l_part[i + 1], p[i], p[i + 1]);
     }
     fence_proxy_async_smem();  // P is read by the tensor cores next
     tc_fence_before();
