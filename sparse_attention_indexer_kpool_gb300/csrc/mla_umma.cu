@@ -15,8 +15,10 @@
 //   3. softmax per head over the 128 rows: each thread reads its row's scores
 //      of 16 heads, a butterfly over the warp reduces the 16 columns across the
 //      warp's 32 rows, four warps combine through shared memory; the
-//      probabilities are written to shared memory as P^T (32 heads x 128 rows,
-//      bf16, swizzled) and the per-head max (base 2) and sum are kept;
+//      probabilities are written to shared memory row-major (P: 128 rows x 32
+//      heads, bf16, one 64-byte swizzled line per row, two 16-byte stores per
+//      thread, read MN-major by the tensor cores) and the per-head max (base
+//      2) and sum are kept;
 //   4. O^T = C^T P^T: M = 128 latent columns (four chunks), N = 32 heads, K = 128
 //      rows.  A is the same gathered tile read MN-major, so the rows are never
 //      transposed;
@@ -49,7 +51,7 @@ constexpr int kL = 512, kHm = 64, kHh = 32, kRows = 128;
 constexpr int kThreadsM = 256;
 constexpr int kKvBlock = kRows * 128;   // 128 rows x 64 latent columns, 16 KB
 constexpr int kQBlock = kHh * 128;      // 32 heads x 64 latent columns, 4 KB
-constexpr int kPtBlock = kHh * 128;     // 32 heads x 64 rows, 4 KB
+constexpr int kPBytes = kRows * kHh * 2;  // P: 128 rows x 32 heads, bf16, 8 KB
 constexpr int kTmemCols = 256;          // S^T (32 columns) + O^T (4 x 32 columns)
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -71,7 +73,7 @@ struct MCtl {
 constexpr size_t kOffKv = 0;
 constexpr size_t kOffQ = kOffKv + 8 * (size_t)kKvBlock;
 constexpr size_t kOffPt = kOffQ + 8 * (size_t)kQBlock;
-constexpr size_t kOffCtl = kOffPt + 2 * (size_t)kPtBlock;
+constexpr size_t kOffCtl = kOffPt + (size_t)kPBytes;
 constexpr size_t kSmemBytes = 1024 + kOffCtl + sizeof(MCtl);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert((size_t)kHh * kL * 4 <= 8 * (size_t)kKvBlock, "O staging fits the row tile");
@@ -321,9 +323,18 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       const int h = hq * 16 + i;
       const float m = c.m_fin[h];
       p[i] = (m == -INFINITY || z[i] == -INFINITY) ? 0.f : exp2f(z[i] - m);
-      *reinterpret_cast<__nv_bfloat16*>(sb + kOffPt + (r >> 6) * kPtBlock + h * 128 +
-                                        ((((r & 63) >> 3) ^ (h & 7)) << 4) + (r & 7) * 2) =
-          __float2bfloat16_rn(kKv == kKvPagedE4M3 ? p[i] * rs : p[i]);
+    }
+    // P row-major: row r's 32 heads in one 64-byte line (64-byte swizzle), read
+    // MN-major by the tensor cores; this thread's 16 heads are the 16-byte
+    // chunks 2 hq and 2 hq + 1
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float sc = kKv == kKvPagedE4M3 ? rs : 1.f;
+      const uint4 w = make_uint4(pack_bf16(p[8 * q] * sc, p[8 * q + 1] * sc),
+                                 pack_bf16(p[8 * q + 2] * sc, p[8 * q + 3] * sc),
+                                 pack_bf16(p[8 * q + 4] * sc, p[8 * q + 5] * sc),
+                                 pack_bf16(p[8 * q + 6] * sc, p[8 * q + 7] * sc));
+      *reinterpret_cast<uint4*>(sb + kOffPt + r * 64 + (((2 * hq + q) ^ ((r >> 1) & 3)) << 4)) = w;
     }
     {
       const float l = transpose_reduce16<false>(p, lane);
@@ -341,13 +352,14 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     // ---- 4. O^T = C^T P^T  (M = 128 latent columns x 4 chunks, N = 32 heads, K = 128 rows)
     if (threadIdx.x == 0) {
       tc_fence_after();
-      constexpr uint32_t idesc = umma_idesc_bf16(128, kHh, true);
+      constexpr uint32_t idesc = umma_idesc_bf16(128, kHh, true, true);
 #pragma unroll
       for (int mc = 0; mc < 4; ++mc) {
 #pragma unroll
         for (int kr = 0; kr < 8; ++kr) {
           const uint64_t a = umma_desc_sw128(kvb + 2 * mc * kKvBlock + kr * 2048, kKvBlock, 1024);
-          const uint64_t bd = sw128_desc(ptb + (kr >> 2) * kPtBlock + (kr & 3) * 32);
+          // 16 rows of P per step; 8-row groups 512 bytes apart; N = 32 is one atom
+          const uint64_t bd = umma_desc_sw64(ptb + kr * 1024, kPBytes, 512);
           umma_bf16(tmem + kHh + mc * kHh, a, bd, idesc, kr > 0 ? 1u : 0u);
         }
       }

@@ -61,6 +61,15 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return umma_desc_sw128(saddr, 16, 1024);
 }
+// The same descriptor with the 64-byte swizzle: an atom is 8 rows of 64 bytes
+// (512 bytes, 512-byte aligned); the 16-byte chunk c of row r is stored at chunk
+// position c ^ ((r >> 1) & 3).
+__device__ __forceinline__ uint64_t umma_desc_sw64(uint32_t saddr, uint32_t lbo_bytes,
+                                                   uint32_t sbo_bytes) {
+  return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo_bytes >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) |
+         ((uint64_t)4 << 61);
+}
 
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, each
 // K-major or (a_mn, b_mn) MN-major, shape M x N.
