@@ -55,12 +55,21 @@ constexpr int kPBytes = kRows * kHh * 2;  // P: 128 rows x 32 heads, bf16, 8 KB
 constexpr int kTmemCols = 256;          // S^T (32 columns) + O^T (4 x 32 columns)
 constexpr float kLog2e = 1.4426950408889634f;
 
+// 2^x on the special-function unit (ex2.approx, relative error below 2^-22;
+// 2^-inf = +0).
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Row sources of the kernel.
 constexpr int kKvContig = 0;   // bf16 rows at cu_seqlens[b] + tok
 constexpr int kKvPaged = 1;    // bf16 rows through the block table
 constexpr int kKvPagedE4M3 = 2;  // E4M3 rows through the block table, one fp32 scale per row
 
 struct MCtl {
+  float m_fin[kHh], l_fin[kHh];  // first: 16-byte aligned
   uint64_t s_ready, o_ready;
   uint32_t tmem_base;
   int pad;
@@ -68,7 +77,6 @@ struct MCtl {
   int prow[kRows];   // the row of the cache (-1: none)
   float rs[kRows];   // E4M3: the row's scale
   float red[2][4][16];  // [head quarter pair][row quarter][head]: per-warp partials
-  float m_fin[kHh], l_fin[kHh];
 };
 constexpr size_t kOffKv = 0;
 constexpr size_t kOffQ = kOffKv + 8 * (size_t)kKvBlock;
@@ -77,6 +85,7 @@ constexpr size_t kOffCtl = kOffPt + (size_t)kPBytes;
 constexpr size_t kSmemBytes = 1024 + kOffCtl + sizeof(MCtl);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert((size_t)kHh * kL * 4 <= 8 * (size_t)kKvBlock, "O staging fits the row tile");
+static_assert(kOffCtl % 16 == 0, "m_fin is read as float4");
 
 // Two E4M3 codes (low byte first) -> two bf16 (low half first), exactly: every
 // E4M3 value is a half and a bfloat16 value.
@@ -317,12 +326,15 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                                    fmaxf(c.red[h2][2][l2], c.red[h2][3][l2]));
     }
     __syncthreads();
+    // p = 2^(z - m); a head with no row (m = -inf) has only z = -inf, 2^-inf = 0
     float p[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int h = hq * 16 + i;
-      const float m = c.m_fin[h];
-      p[i] = (m == -INFINITY || z[i] == -INFINITY) ? 0.f : exp2f(z[i] - m);
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const float4 m4 = reinterpret_cast<const float4*>(c.m_fin + hq * 16)[q4];
+      const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        p[4 * q4 + e] = ex2_fast(z[4 * q4 + e] - (mv[e] == -INFINITY ? 0.f : mv[e]));
     }
     // P row-major: row r's 32 heads in one 64-byte line (64-byte swizzle), read
     // MN-major by the tensor cores; this thread's 16 heads are the 16-byte
@@ -525,13 +537,6 @@ __device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a));
 }
 
-// 2^x on the special-function unit (ex2.approx, relative error below 2^-22;
-// 2^-inf = +0).
-__device__ __forceinline__ float ex2_fast(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 template <int kKv>
 __global__ void __launch_bounds__(kThreadsM, 1)
