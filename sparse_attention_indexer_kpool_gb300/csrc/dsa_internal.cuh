@@ -147,6 +147,14 @@ __device__ __forceinline__ void cp_async_wait_pending(int n) {
 }
 
 // ---------------------------------------------------------------- mbarrier + bulk copy
+// 2^x on the special-function unit (ex2.approx, relative error below 2^-22;
+// 2^-inf = +0).
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
 }

@@ -335,14 +335,14 @@ __global__ void __launch_bounds__(128)
     for (int u = 0; u < kMergeMax; ++u)
       if (ll[u] > 0.f) bm = fmaxf(bm, mm[u]);
     if (bm == -INFINITY) continue;  // nothing selected so far
-    const float r = mx == -INFINITY ? 0.f : exp2f(mx - bm);
+    const float r = mx == -INFINITY ? 0.f : ex2_fast(mx - bm);
     den *= r;
     acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
     mx = bm;
 #pragma unroll
     for (int u = 0; u < kMergeMax; ++u) {
       if (ll[u] > 0.f) {
-        const float w = exp2f(mm[u] - mx);
+        const float w = ex2_fast(mm[u] - mx);
         den += ll[u] * w;
         acc.x += w * v[u].x; acc.y += w * v[u].y; acc.z += w * v[u].z; acc.w += w * v[u].w;
       }

@@ -55,13 +55,6 @@ constexpr int kPBytes = kRows * kHh * 2;  // P: 128 rows x 32 heads, bf16, 8 KB
 constexpr int kTmemCols = 256;          // S^T (32 columns) + O^T (4 x 32 columns)
 constexpr float kLog2e = 1.4426950408889634f;
 
-// 2^x on the special-function unit (ex2.approx, relative error below 2^-22;
-// 2^-inf = +0).
-__device__ __forceinline__ float ex2_fast(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // Row sources of the kernel.
 constexpr int kKvContig = 0;   // bf16 rows at cu_seqlens[b] + tok
