@@ -581,12 +581,22 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       if (use_hist) {  // flush this query's histogram
         epi_bar();
         uint32_t* gh = hist + (size_t)gi * kHistBins;
-        for (int i = ew * 32 + lane; i < kHistBins; i += kEpiWarps * 32) {
-          const uint32_t v = s_hist[i];
-          if (v) {
-            atomicAdd(&gh[i], v);
-            s_hist[i] = 0;
-          }
+        // 16 bins per thread as four 16-byte reads, all issued before any add
+        static_assert(kHistBins == 16 * kEpiWarps * 32, "four 16-byte groups of bins per thread");
+        const int et = ew * 32 + lane;
+        uint4 hv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          hv[k] = reinterpret_cast<const uint4*>(s_hist)[k * kEpiWarps * 32 + et];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i0 = 4 * (k * kEpiWarps * 32 + et);
+          if (hv[k].x) atomicAdd(&gh[i0], hv[k].x);
+          if (hv[k].y) atomicAdd(&gh[i0 + 1], hv[k].y);
+          if (hv[k].z) atomicAdd(&gh[i0 + 2], hv[k].z);
+          if (hv[k].w) atomicAdd(&gh[i0 + 3], hv[k].w);
+          if (hv[k].x | hv[k].y | hv[k].z | hv[k].w)
+            reinterpret_cast<uint4*>(s_hist)[k * kEpiWarps * 32 + et] = make_uint4(0, 0, 0, 0);
         }
         epi_bar();
       }
