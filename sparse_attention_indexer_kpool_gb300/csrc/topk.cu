@@ -39,7 +39,6 @@ constexpr int kBins = 4096;           // top 12 bits of the 32-bit score key
 constexpr int kBinShift = 20;
 constexpr int kTieCap = 4096;         // on-chip tie-list capacity (overflow: exact slow path)
 constexpr int kThreads = 1024;
-constexpr int kFast = 512;            // register bitonic width (keys per half block)
 constexpr int kSmallSort = 1024;      // general path: rank sort up to this many keys
 
 struct ExpandArgs {   // optional fused expand_selection (token_ids == nullptr: off)
@@ -170,35 +169,6 @@ __device__ void sort_desc(uint64_t* keys, int n, uint64_t* tmp) {
       __syncthreads();
     }
   }
-}
-
-// Two independent 512-key descending bitonic sorts, one per half of the block,
-// one key per thread: xor-shuffles for partner distances < 32, shared memory
-// (xch, 1024 keys) above.
-__device__ uint64_t bitonic512_desc(uint64_t key, uint64_t* xch) {
-  const int pos = threadIdx.x & (kFast - 1);
-#pragma unroll 1
-  for (int k = 2; k <= kFast; k <<= 1) {
-#pragma unroll 1
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      uint64_t other;
-      if (j >= 32) {
-        xch[threadIdx.x] = key;
-        __syncthreads();
-        other = xch[threadIdx.x ^ j];
-        __syncthreads();
-      } else {
-        const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)key, j);
-        const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(key >> 32), j);
-        other = ((uint64_t)hi << 32) | lo;
-      }
-      const bool lower = (pos & j) == 0;
-      const bool desc_block = (pos & k) == 0;
-      const bool keep_max = lower == desc_block;
-      key = keep_max ? (key > other ? key : other) : (key < other ? key : other);
-    }
-  }
-  return key;
 }
 
 // Shared-memory layout of the select kernel (dynamic).  Region A holds the
