@@ -152,3 +152,48 @@ def test_paged_e4m3_long262k_layer():
     assert st == 0
     ref = oracle_paged(bt, buf.token_ids, pc)
     assert_close(out, lse, ref, bt.geo.dtype)
+
+
+@pytest.mark.parametrize("Q", [4, 320])  # the one-tile kernel; the streaming kernel
+def test_paged_e4m3_every_code_decodes_exactly(Q):
+    """Every E4M3 code but the two NaNs (both zeros, the subnormals, the largest
+    normals, both signs) through a one-row selection: the softmax weight of the
+    one row is exactly 1, so each output is the code's value times the row's
+    scale.  With a power-of-two scale bf16 holds that product exactly (an E4M3
+    value has at most four significant bits), so the kernels' outputs must equal
+    the oracle's decode bit for bit."""
+    L, Hm, page_size, W = 512, 64, 16, 128
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)  # 254 codes
+    n_blocks = -(-Q // page_size)
+    n_rows = (n_blocks + 1) * page_size
+    pages = np.zeros((n_rows, L), np.uint8)
+    for r in range(n_rows):  # row r: every code, rotated by r
+        pages[r] = np.resize(np.roll(codes, r), L)
+    scale = 0.125
+    g = torch.Generator(device="cpu").manual_seed(95)
+    q_lat = torch.randn((Q, Hm, L), generator=g).to(torch.bfloat16).to(DEV)
+    perm = torch.randperm(n_blocks + 1, generator=g)[:n_blocks].to(torch.int32)
+    block_table = torch.full((1, n_blocks + 1), -1, dtype=torch.int32)
+    block_table[0, :n_blocks] = perm
+    token_ids = torch.full((Q, W), -1, dtype=torch.int32)
+    token_ids[:, 0] = torch.arange(Q, dtype=torch.int32)   # query q selects token q only
+    pc = synth.PagedCache(torch.from_numpy(pages).to(DEV).view(torch.float8_e4m3fn),
+                          torch.full((n_rows,), scale, dtype=torch.float32, device=DEV),
+                          block_table.to(DEV), torch.tensor([Q], dtype=torch.int32, device=DEV),
+                          page_size)
+    out = torch.full((Q, Hm, L), 7.0, dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((Q, Hm), 7.0, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    n = ops.mla_paged_workspace_bytes(q_lat, pc.pages, W)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=DEV)
+    ops.dsa_mla_paged_decode(q_lat, pc.pages, pc.row_scale, pc.block_table, pc.seq_lens, page_size,
+                             torch.zeros(Q, dtype=torch.int32, device=DEV), token_ids.to(DEV),
+                             0.05, out, lse, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    # the cache row of token q: page block_table[q // page_size], slot q % page_size
+    rows = perm.numpy()[np.arange(Q) // page_size].astype(np.int64) * page_size + np.arange(Q) % page_size
+    want = oracle.fp8_e4m3_decode(pages[rows]) * scale               # [Q, L], exact
+    got = out.float().cpu().double().numpy()
+    assert np.array_equal(got, np.broadcast_to(want[:, None, :], got.shape))
+    assert torch.isfinite(lse).all()
